@@ -1,0 +1,118 @@
+"""Seeded synthetic inputs for the attention backward-over-backward workloads.
+
+This module only draws random numbers and holds the named workload shapes.  It
+contains none of the method's arithmetic, so both the CUDA path and the fp64
+CPU oracle take their inputs from here without sharing any computation.
+
+Recipe (the pages benchmark an isolated attention layer on synthetic tensors):
+
+* one CPU ``torch.Generator`` seeded with ``seed``;
+* draws in the fixed order Q, K, V, dO, U_Q, U_K, U_V, each of shape
+  ``[B, H, N, d]`` (contiguous, row-major);
+* ``dist="unit"``: all seven tensors ~ N(0, 1) (the tiny fp32 workload);
+* ``dist="scaled"``: Q, K, V ~ N(0, 1) / d**0.25 so that Q K^T has unit
+  variance; dO, U_Q, U_K, U_V ~ N(0, 1);
+* ``peaked_k_rows``: for every (b, h) pick floor(0.05 N) distinct key rows
+  with the same generator (after the seven draws) and multiply them by 4,
+  which makes some softmax rows peaked;
+* ``stress``: Q, K ~ N(0, 1) (unscaled), so the scaled scores tau Q K^T have
+  unit variance and the x4 key rows are truly peaked;
+* bf16 workloads round the fp32 draws to bf16 (round to nearest even) as the
+  last step; the oracle then reads the bf16 values exactly, as fp64.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+NAMES = ("Q", "K", "V", "dO", "UQ", "UK", "UV")
+
+
+@dataclass(frozen=True)
+class Workload:
+    """A named problem shape: batch B, heads H, sequence N, head dim d."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str  # "f32" or "bf16"
+    dist: str = "scaled"  # "unit" or "scaled"
+    peaked_k_rows: bool = False
+    stress: bool = False
+    seed: int = 0
+
+    @property
+    def tau(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Fixed GEMM list of both passes: 19 GEMMs of 2 N^2 d each."""
+        return 38.0 * self.N * self.N * self.d * self.B * self.H
+
+
+# The five workloads of the isolated-layer benchmark (non-causal).
+TINY_F32 = Workload("tiny_f32_B1_H1_N128_d64", 1, 1, 128, 64, "f32", dist="unit")
+GPT2_LAYER = Workload("gpt2_layer_B4_H12_N1024_d64", 4, 12, 1024, 64, "bf16")
+MID_LENGTH = Workload("mid_B1_H12_N8192_d64", 1, 12, 8192, 64, "bf16")
+MID_LENGTH_PEAKED = Workload("mid_peaked_B1_H12_N8192_d64", 1, 12, 8192, 64, "bf16",
+                             peaked_k_rows=True)
+MID_LENGTH_STRESS = Workload("mid_stress_B1_H12_N8192_d64", 1, 12, 8192, 64, "bf16",
+                             peaked_k_rows=True, stress=True)
+LONG_CONTEXT = Workload("long_B1_H4_N65536_d64", 1, 4, 65536, 64, "bf16")
+EXTREME_D64 = Workload("extreme_B1_H1_N262144_d64", 1, 1, 262144, 64, "bf16")
+EXTREME_D128 = Workload("extreme_B1_H1_N131072_d128", 1, 1, 131072, 128, "bf16")
+
+WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PEAKED,
+                                 MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128)}
+
+
+def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
+    """Draw the seven input tensors of ``w`` on the CPU.
+
+    Returns fp32 tensors for ``dtype="f32"`` and bf16 tensors for
+    ``dtype="bf16"``, all contiguous ``[B, H, N, d]``.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    out = {}
+    for name in NAMES:
+        out[name] = torch.randn(shape, generator=g, dtype=torch.float32)
+    if w.dist == "scaled":
+        s = w.d ** -0.25
+        for name in ("Q", "K", "V"):
+            if w.stress and name in ("Q", "K"):
+                continue
+            out[name].mul_(s)
+    elif w.dist != "unit":
+        raise ValueError(f"unknown dist {w.dist!r}")
+    if w.peaked_k_rows:
+        n_peak = int(math.floor(0.05 * w.N))
+        for b in range(w.B):
+            for h in range(w.H):
+                idx = torch.randperm(w.N, generator=g)[:n_peak]
+                out["K"][b, h, idx, :] *= 4.0
+    if w.dtype == "bf16":
+        out = {k: v.to(torch.bfloat16) for k, v in out.items()}
+    elif w.dtype != "f32":
+        raise ValueError(f"unknown dtype {w.dtype!r}")
+    return out
+
+
+def small_workload(B: int, H: int, N: int, d: int, dtype: str, seed: int = 0,
+                   dist: str | None = None, **kw) -> Workload:
+    """An ad-hoc shape for parity and edge-case tests."""
+    if dist is None:
+        dist = "unit" if dtype == "f32" else "scaled"
+    return Workload(f"adhoc_B{B}_H{H}_N{N}_d{d}_{dtype}", B, H, N, d, dtype, dist=dist,
+                    seed=seed, **kw)
+
+
+def as_float64_numpy(t: torch.Tensor):
+    """Exact fp64 copy (bf16 and fp32 values are representable in fp64)."""
+    return t.detach().to("cpu").to(torch.float64).numpy()

@@ -1,0 +1,290 @@
+"""Plain fp64 oracle for exact backward-over-backward of softmax attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``.  The CUDA library never imports,
+links or calls it, and it shares no code with the CUDA path.
+
+Every function works on ONE (batch, head) slice: 2-D numpy arrays of shape
+``[N, d]`` (rows are sequence positions) in float64, plus the scale ``tau``.
+The batched helpers at the end loop over ``[B, H]``.
+
+Sources (web pages on the method; sections named as on the pages):
+
+* [FBN] "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+  Attention", paper notes (papernotes.org): section 方法详解/整体框架 (the
+  objective Phi and the four outputs) and 关键设计 1 (the row scalars D, alpha,
+  E, the matrix F, the affine rule for d~P and the three affine corrections).
+* [FAB] "FlashAttention 的反向传播设计：在 SRAM 内部重计算 Softmax 的显存收益"
+  (bjdmk.com.cn): section 一 (forward S, P, O and the first backward dV, dP,
+  dS, D, dQ, dK) and section 二 (recomputing P from saved row statistics).
+
+Readings where the pages are silent (each is listed in the design notes):
+
+* L is the natural-log logsumexp of the scaled scores, P = exp(S - L).
+* D_i = dO_i . O_i, which equals sum_j P_ij dP_ij ([FAB] section 一).
+* The pages print F, alpha, E, the d~P rule and the corrections, but not
+  d~K, d~V, nor what B, R and Omega contain.  ``bob`` differentiates Phi by
+  hand (chain rule through F, G, dP, D and the softmax); ``bob_affine`` then
+  names B = P K, R = (P o dP) K, Omega = (P o d~P0) K + dS U_K, the only
+  assignment that makes the printed corrections alpha-free and exact.
+
+Parity pins (tests/test_oracle.py): central finite differences of Phi, exact
+symbolic differentiation (sympy) on tiny inputs, a loop-only brute force,
+the printed affine identities, sum_j P_ij = 1, shift invariances, Hessian
+symmetry, the N = 1 closed form, the U_Q = U_K = 0 reduction to a first
+backward, and JVP identities of the forward.  No function here is unpinned.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# Forward, row state and first backward  ([FAB] sections 一 and 二)
+# --------------------------------------------------------------------------
+
+def forward(Q, K, V, tau):
+    """S = tau Q K^T, L = logsumexp_j S_ij, P = exp(S - L), O = P V.
+
+    [FAB] section 一 (S, P = softmax(S), O = P V) with the softmax written
+    through the saved row statistic L as in [FAB] section 二.
+    """
+    S = tau * (Q @ K.T)
+    m = S.max(axis=1, keepdims=True)
+    L = m[:, 0] + np.log(np.exp(S - m).sum(axis=1))
+    P = np.exp(S - L[:, None])
+    O = P @ V
+    return S, P, O, L
+
+
+def prep(Q, K, V, dO, tau):
+    """Row state the BoB consumes: O, L and D_i = dO_i . O_i.
+
+    [FBN] 关键设计 1 defines D_i = dO_i^T O_i; [FAB] section 一 gives the same
+    scalar as sum_j dP_ij P_ij.
+    """
+    _, _, O, L = forward(Q, K, V, tau)
+    D = (dO * O).sum(axis=1)
+    return O, L, D
+
+
+def first_backward(Q, K, V, dO, tau):
+    """dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = tau dS K, dK = tau dS^T Q.
+
+    [FAB] section 一.  The 1/sqrt(d) of the page is the general scale tau.
+    """
+    _, P, O, _ = forward(Q, K, V, tau)
+    dV = P.T @ dO
+    dP = dO @ V.T
+    D = (P * dP).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    dQ = tau * (dS @ K)
+    dK = tau * (dS.T @ Q)
+    return dQ, dK, dV
+
+
+def phi(Q, K, V, dO, UQ, UK, UV, tau):
+    """Phi = <dQ, U_Q> + <dK, U_K> + <dV, U_V>  ([FBN] 方法详解/整体框架)."""
+    dQ, dK, dV = first_backward(Q, K, V, dO, tau)
+    return float((dQ * UQ).sum() + (dK * UK).sum() + (dV * UV).sum())
+
+
+# --------------------------------------------------------------------------
+# Backward-over-backward, plain matrix form
+# --------------------------------------------------------------------------
+
+def bob(Q, K, V, dO, UQ, UK, UV, tau):
+    """Total derivatives of Phi w.r.t. Q, K, V and dO, with O, L, D functions
+    of the inputs ([FBN] 方法详解/整体框架).
+
+    Phi rewritten with the first backward: Phi = sum_ij dS_ij F_ij +
+    sum_ij P_ij G_ij, where F = tau (U_Q K^T + Q U_K^T) ([FBN] 关键设计 1)
+    and G = dO U_V^T.  Chain rule, one node at a time:
+
+    * through D:   dPhi/dP_ij holds  d~P = d~P0 - alpha dP  with
+      d~P0 = F o (dP - D) + G and alpha_i = sum_j P_ij F_ij  ([FBN] 关键设计 1);
+    * through the softmax: d~S = P o (d~P - E), E_i = sum_j P_ij d~P_ij;
+    * through dP = dO V^T: the gradient w.r.t. dP is P o (F - alpha);
+    * through F and G: gradients dS and P.
+
+    Returns d~Q = tau (d~S K + dS U_K), d~K = tau (d~S^T Q + dS^T U_Q),
+    d~V = (P o (F - alpha))^T dO, d~dO = P U_V + (P o (F - alpha)) V,
+    and the row scalars alpha and E.
+    """
+    S, P, O, L = forward(Q, K, V, tau)
+    dP = dO @ V.T
+    D = (dO * O).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    F = tau * (UQ @ K.T + Q @ UK.T)
+    G = dO @ UV.T
+    alpha = (P * F).sum(axis=1)
+    dPt0 = F * (dP - D[:, None]) + G
+    dPt = dPt0 - alpha[:, None] * dP
+    E = (P * dPt).sum(axis=1)
+    dSt = P * (dPt - E[:, None])
+    dPdP = P * (F - alpha[:, None])  # gradient of Phi w.r.t. dP
+    return {
+        "dQt": tau * (dSt @ K + dS @ UK),
+        "dKt": tau * (dSt.T @ Q + dS.T @ UQ),
+        "dVt": dPdP.T @ dO,
+        "ddOt": P @ UV + dPdP @ V,
+        "alpha": alpha,
+        "E": E,
+        "L": L,
+        "D": D,
+    }
+
+
+def bob_affine(Q, K, V, dO, UQ, UK, UV, tau):
+    """Row outputs through the alpha-free accumulators and the affine
+    correction of [FBN] 关键设计 1:
+
+        E = E0 - alpha D,  d~dO = d~dO0 - alpha O,  d~Q = tau (Omega - alpha R - E B)
+
+    with E0_i = sum_j P_ij d~P0_ij, B = P K, R = (P o dP) K,
+    Omega = (P o d~P0) K + dS U_K and d~dO0 = P U_V + (P o F) V.
+    """
+    S, P, O, L = forward(Q, K, V, tau)
+    dP = dO @ V.T
+    D = (dO * O).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    F = tau * (UQ @ K.T + Q @ UK.T)
+    G = dO @ UV.T
+    dPt0 = F * (dP - D[:, None]) + G
+    alpha = (P * F).sum(axis=1)
+    E0 = (P * dPt0).sum(axis=1)
+    B = P @ K
+    R = (P * dP) @ K
+    Omega = (P * dPt0) @ K + dS @ UK
+    ddOt0 = P @ UV + (P * F) @ V
+    E = E0 - alpha * D
+    return {
+        "dQt": tau * (Omega - alpha[:, None] * R - E[:, None] * B),
+        "ddOt": ddOt0 - alpha[:, None] * O,
+        "alpha": alpha,
+        "E": E,
+        "E0": E0,
+    }
+
+
+# --------------------------------------------------------------------------
+# One row at a time: O(N d) per row, for long sequences
+# --------------------------------------------------------------------------
+
+def bob_rows(Q, K, V, dO, UQ, UK, UV, tau, rows):
+    """Row-side outputs (L, D, alpha, E, d~Q, d~dO) for the listed rows only.
+
+    The same definitions as ``bob`` restricted to row i: every quantity of
+    row i needs only row i of Q, dO, U_Q and all of K, V, U_K, U_V.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    out = {k: [] for k in ("L", "D", "alpha", "E", "dQt", "ddOt")}
+    for i in rows:
+        s = tau * (K @ Q[i])
+        m = s.max()
+        Li = m + np.log(np.exp(s - m).sum())
+        p = np.exp(s - Li)
+        o = p @ V
+        Di = dO[i] @ o
+        dp = V @ dO[i]
+        ds = p * (dp - Di)
+        f = tau * (K @ UQ[i] + UK @ Q[i])
+        g = UV @ dO[i]
+        a = p @ f
+        dpt = f * (dp - Di) + g - a * dp
+        Ei = p @ dpt
+        dst = p * (dpt - Ei)
+        out["L"].append(Li)
+        out["D"].append(Di)
+        out["alpha"].append(a)
+        out["E"].append(Ei)
+        out["dQt"].append(tau * (dst @ K + ds @ UK))
+        out["ddOt"].append(p @ UV + (p * (f - a)) @ V)
+    return {k: np.array(v) for k, v in out.items()}
+
+
+# --------------------------------------------------------------------------
+# Brute force: scalar loops only (tiny N, d), an independent restatement
+# --------------------------------------------------------------------------
+
+def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau):
+    """The same derivatives as ``bob`` written as explicit element sums.
+
+    No matrix products, no vectorised reductions: every entry is a nested
+    loop over (i, j, k), so a transposed operand or a dropped term in the
+    matrix form shows up as a mismatch.
+    """
+    N, d = Q.shape
+
+    def dot(a, b):
+        s = 0.0
+        for k in range(d):
+            s += a[k] * b[k]
+        return s
+
+    S = [[tau * dot(Q[i], K[j]) for j in range(N)] for i in range(N)]
+    P = [[0.0] * N for _ in range(N)]
+    L = [0.0] * N
+    for i in range(N):
+        m = max(S[i])
+        z = 0.0
+        for j in range(N):
+            z += np.exp(S[i][j] - m)
+        L[i] = m + np.log(z)
+        for j in range(N):
+            P[i][j] = np.exp(S[i][j] - L[i])
+    O = [[sum(P[i][j] * V[j][k] for j in range(N)) for k in range(d)] for i in range(N)]
+    D = [dot(dO[i], O[i]) for i in range(N)]
+    dP = [[dot(dO[i], V[j]) for j in range(N)] for i in range(N)]
+    F = [[tau * (dot(UQ[i], K[j]) + dot(Q[i], UK[j])) for j in range(N)] for i in range(N)]
+    G = [[dot(dO[i], UV[j]) for j in range(N)] for i in range(N)]
+    alpha = [sum(P[i][j] * F[i][j] for j in range(N)) for i in range(N)]
+    dPt = [[F[i][j] * (dP[i][j] - D[i]) + G[i][j] - alpha[i] * dP[i][j] for j in range(N)]
+           for i in range(N)]
+    E = [sum(P[i][j] * dPt[i][j] for j in range(N)) for i in range(N)]
+    dS = [[P[i][j] * (dP[i][j] - D[i]) for j in range(N)] for i in range(N)]
+    dSt = [[P[i][j] * (dPt[i][j] - E[i]) for j in range(N)] for i in range(N)]
+    dQt = np.zeros((N, d))
+    dKt = np.zeros((N, d))
+    dVt = np.zeros((N, d))
+    ddOt = np.zeros((N, d))
+    for i in range(N):
+        for j in range(N):
+            w = P[i][j] * (F[i][j] - alpha[i])
+            for k in range(d):
+                dQt[i, k] += tau * (dSt[i][j] * K[j][k] + dS[i][j] * UK[j][k])
+                dKt[j, k] += tau * (dSt[i][j] * Q[i][k] + dS[i][j] * UQ[i][k])
+                dVt[j, k] += w * dO[i][k]
+                ddOt[i, k] += P[i][j] * UV[j][k] + w * V[j][k]
+    return {"dQt": dQt, "dKt": dKt, "dVt": dVt, "ddOt": ddOt,
+            "alpha": np.array(alpha), "E": np.array(E)}
+
+
+# --------------------------------------------------------------------------
+# Batched helpers over [B, H, N, d]
+# --------------------------------------------------------------------------
+
+def prep_batched(Q, K, V, dO, tau):
+    """``prep`` for every (b, h) of [B, H, N, d] arrays."""
+    B, H, N, d = Q.shape
+    O = np.empty((B, H, N, d))
+    L = np.empty((B, H, N))
+    D = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            O[b, h], L[b, h], D[b, h] = prep(Q[b, h], K[b, h], V[b, h], dO[b, h], tau)
+    return O, L, D
+
+
+def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None):
+    """``bob`` for every (b, h) (or the listed (b, h) pairs)."""
+    B, H, N, d = Q.shape
+    keys = ("dQt", "dKt", "dVt", "ddOt", "alpha", "E", "L", "D")
+    out = {k: np.full((B, H, N, d) if k in ("dQt", "dKt", "dVt", "ddOt") else (B, H, N),
+                      np.nan) for k in keys}
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        r = bob(Q[b, h], K[b, h], V[b, h], dO[b, h], UQ[b, h], UK[b, h], UV[b, h], tau)
+        for k in keys:
+            out[k][b, h] = r[k]
+    return out

@@ -1,0 +1,317 @@
+"""Pins for the fp64 oracle: each check fixes the oracle to something other
+than itself (finite differences, exact symbolic differentiation, a library
+routine, a closed form, an exact invariant or a loop-only brute force)."""
+import numpy as np
+import pytest
+
+from oracle import bob as orc
+
+RTOL_FD = 2e-7
+
+
+def rand_inputs(N, d, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return [scale * rng.standard_normal((N, d)) for _ in range(7)]
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# --------------------------------------------------------------------------
+# forward / prep / first backward
+# --------------------------------------------------------------------------
+
+def test_forward_matches_scipy_softmax():
+    from scipy.special import logsumexp, softmax
+    Q, K, V, *_ = rand_inputs(9, 4, 1)
+    tau = 0.37
+    S, P, O, L = orc.forward(Q, K, V, tau)
+    assert np.allclose(S, tau * np.einsum("ik,jk->ij", Q, K), rtol=1e-14, atol=1e-14)
+    assert np.allclose(L, logsumexp(S, axis=1), rtol=1e-14)
+    assert np.allclose(P, softmax(S, axis=1), rtol=1e-13)
+    assert np.allclose(P.sum(axis=1), 1.0, atol=1e-14)
+    assert np.allclose(O, np.einsum("ij,jk->ik", softmax(S, axis=1), V), rtol=1e-13)
+
+
+def test_prep_D_is_rowsum_P_dP():
+    Q, K, V, dO, *_ = rand_inputs(11, 5, 2)
+    tau = 0.5
+    O, L, D = orc.prep(Q, K, V, dO, tau)
+    _, P, _, _ = orc.forward(Q, K, V, tau)
+    dP = dO @ V.T
+    assert np.allclose(D, (P * dP).sum(axis=1), rtol=1e-12, atol=1e-13)
+
+
+def _fd_grad(fun, X, h=1e-5):
+    g = np.zeros_like(X)
+    for idx in np.ndindex(*X.shape):
+        Xp = X.copy()
+        Xm = X.copy()
+        Xp[idx] += h
+        Xm[idx] -= h
+        g[idx] = (fun(Xp) - fun(Xm)) / (2 * h)
+    return g
+
+
+def test_first_backward_matches_fd_of_output_inner_product():
+    Q, K, V, dO, *_ = rand_inputs(6, 3, 3)
+    tau = 0.6
+    dQ, dK, dV = orc.first_backward(Q, K, V, dO, tau)
+
+    def psi(Q_, K_, V_):
+        return float((orc.forward(Q_, K_, V_, tau)[2] * dO).sum())
+
+    assert rel(dQ, _fd_grad(lambda X: psi(X, K, V), Q)) < RTOL_FD
+    assert rel(dK, _fd_grad(lambda X: psi(Q, X, V), K)) < RTOL_FD
+    assert rel(dV, _fd_grad(lambda X: psi(Q, K, X), V)) < RTOL_FD
+
+
+def test_first_backward_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    Q, K, V, dO, *_ = rand_inputs(13, 6, 4)
+    tau = 1 / np.sqrt(6)
+    dQ, dK, dV = orc.first_backward(Q, K, V, dO, tau)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (Q, K, V))
+    out = torch.softmax(tau * tq @ tk.T, dim=-1) @ tv
+    gq, gk, gv = torch.autograd.grad(out, (tq, tk, tv), torch.tensor(dO))
+    assert rel(dQ, gq.numpy()) < 1e-13
+    assert rel(dK, gk.numpy()) < 1e-13
+    assert rel(dV, gv.numpy()) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# BoB against finite differences of Phi
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,d,seed,tau", [(7, 5, 0, 1 / np.sqrt(5)), (16, 8, 1, 0.35),
+                                          (3, 2, 2, 1.3), (12, 4, 3, 0.5)])
+def test_bob_matches_fd_of_phi(N, d, seed, tau):
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(N, d, seed)
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    args = [Q, K, V, dO]
+    for pos, key in enumerate(("dQt", "dKt", "dVt", "ddOt")):
+        def f(X, pos=pos):
+            a = list(args)
+            a[pos] = X
+            return orc.phi(*a, UQ, UK, UV, tau)
+        assert rel(r[key], _fd_grad(f, args[pos])) < RTOL_FD, key
+
+
+def test_bob_matches_fd_with_peaked_rows():
+    # large scores: nearly one-hot softmax rows
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(8, 3, 5)
+    Q = 3.0 * Q
+    K[2] *= 4.0
+    tau = 1.0
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    for pos, key in ((0, "dQt"), (1, "dKt")):
+        args = [Q, K, V, dO]
+
+        def f(X, pos=pos):
+            a = list(args)
+            a[pos] = X
+            return orc.phi(*a, UQ, UK, UV, tau)
+        assert rel(r[key], _fd_grad(f, args[pos], h=1e-6)) < 1e-6, key
+
+
+# --------------------------------------------------------------------------
+# Exact symbolic differentiation (sympy) on a tiny case
+# --------------------------------------------------------------------------
+
+def test_bob_matches_sympy_exact_derivative():
+    sp = pytest.importorskip("sympy")
+    N, d = 3, 2
+    rng = np.random.default_rng(7)
+    vals = [np.round(rng.standard_normal((N, d)), 3) for _ in range(7)]
+    tau = sp.Rational(7, 10)
+
+    def mat(name):
+        return sp.Matrix(N, d, lambda i, k: sp.Symbol(f"{name}_{i}_{k}"))
+
+    Qs, Ks, Vs, dOs = mat("Q"), mat("K"), mat("V"), mat("dO")
+    UQ, UK, UV = (sp.Matrix(v.tolist()).applyfunc(sp.nsimplify) for v in vals[4:])
+    S = tau * Qs * Ks.T
+    Pm = sp.Matrix(N, N, lambda i, j: sp.exp(S[i, j]) / sum(sp.exp(S[i, c]) for c in range(N)))
+    Om = Pm * Vs
+    dV = Pm.T * dOs
+    dP = dOs * Vs.T
+    Dv = [sum(Pm[i, j] * dP[i, j] for j in range(N)) for i in range(N)]
+    dS = sp.Matrix(N, N, lambda i, j: Pm[i, j] * (dP[i, j] - Dv[i]))
+    dQ = tau * dS * Ks
+    dK = tau * dS.T * Qs
+    Phi = sum(dQ[i, k] * UQ[i, k] + dK[i, k] * UK[i, k] + dV[i, k] * UV[i, k]
+              for i in range(N) for k in range(d))
+    subs = {}
+    for M, v in zip((Qs, Ks, Vs, dOs), vals[:4]):
+        for i in range(N):
+            for k in range(d):
+                subs[M[i, k]] = sp.nsimplify(v[i, k])
+    r = orc.bob(*vals, float(tau))
+    for M, key in ((Qs, "dQt"), (Ks, "dKt"), (Vs, "dVt"), (dOs, "ddOt")):
+        exact = np.array([[float(sp.diff(Phi, M[i, k]).evalf(30, subs=subs))
+                           for k in range(d)] for i in range(N)])
+        assert rel(r[key], exact) < 1e-12, key
+    del Om
+
+
+# --------------------------------------------------------------------------
+# Brute force, affine form, per-row form
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,d,seed", [(1, 3, 0), (5, 3, 1), (12, 6, 2)])
+def test_bob_matches_bruteforce(N, d, seed):
+    args = rand_inputs(N, d, seed)
+    tau = 0.41
+    r = orc.bob(*args, tau)
+    b = orc.bob_bruteforce(*args, tau)
+    for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+        assert rel(r[key], b[key]) < 1e-12, key
+
+
+def test_affine_identities_of_the_row_outputs():
+    # E = E0 - alpha D, d~dO = d~dO0 - alpha O, d~Q = tau (Omega - alpha R - E B)
+    args = rand_inputs(40, 8, 11)
+    tau = 1 / np.sqrt(8)
+    r = orc.bob(*args, tau)
+    a = orc.bob_affine(*args, tau)
+    for key in ("dQt", "ddOt", "alpha", "E"):
+        assert rel(a[key], r[key]) < 1e-12, key
+
+
+def test_rows_form_matches_matrix_form():
+    args = rand_inputs(37, 6, 12)
+    tau = 0.4
+    r = orc.bob(*args, tau)
+    rows = [0, 5, 17, 36]
+    s = orc.bob_rows(*args, tau, rows)
+    for key in ("dQt", "ddOt", "alpha", "E", "L", "D"):
+        assert rel(s[key], r[key][rows]) < 1e-12, key
+
+
+# --------------------------------------------------------------------------
+# Exact invariants and closed forms
+# --------------------------------------------------------------------------
+
+def test_invariants():
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(33, 7, 13)
+    tau = 0.45
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    dQ, dK, dV = orc.first_backward(Q, K, V, dO, tau)
+    ph = orc.phi(Q, K, V, dO, UQ, UK, UV, tau)
+    scale = np.abs(ph) + 1.0
+    # Phi is invariant under K -> K + 1 c^T and V -> V + 1 c^T
+    assert np.abs(r["dKt"].sum(axis=0)).max() < 1e-12 * np.abs(r["dKt"]).max() * 33
+    assert np.abs(r["dVt"].sum(axis=0)).max() < 1e-12 * np.abs(r["dVt"]).max() * 33
+    # Phi is linear in dO
+    assert abs((r["ddOt"] * dO).sum() - ph) < 1e-12 * scale
+    # dQ and dK are linear in V and dV does not depend on V
+    assert abs((r["dVt"] * V).sum() - ((dQ * UQ).sum() + (dK * UK).sum())) < 1e-12 * scale
+    # Q -> sQ, K -> K/s leaves S unchanged
+    lhs = (r["dQt"] * Q).sum() - (r["dKt"] * K).sum()
+    rhs = (dK * UK).sum() - (dQ * UQ).sum()
+    assert abs(lhs - rhs) < 1e-12 * scale
+
+
+def test_linear_in_perturbations_and_zero_at_zero():
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(10, 4, 14)
+    tau = 0.7
+    W = rand_inputs(10, 4, 15)
+    r1 = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    r2 = orc.bob(Q, K, V, dO, W[0], W[1], W[2], tau)
+    r12 = orc.bob(Q, K, V, dO, UQ + 2 * W[0], UK + 2 * W[1], UV + 2 * W[2], tau)
+    for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+        assert rel(r12[key], r1[key] + 2 * r2[key]) < 1e-12, key
+    z = np.zeros_like(Q)
+    r0 = orc.bob(Q, K, V, dO, z, z, z, tau)
+    for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+        assert np.abs(r0[key]).max() == 0.0, key
+
+
+def test_hessian_symmetry():
+    # (d~Q, d~K, d~V) = Hessian of psi = <Attn(Q,K,V), dO> applied to U
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(9, 3, 16)
+    W = rand_inputs(9, 3, 17)[:3]
+    tau = 0.8
+    ru = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    rw = orc.bob(Q, K, V, dO, *W, tau)
+    a = sum((ru[k] * w).sum() for k, w in zip(("dQt", "dKt", "dVt"), W))
+    b = sum((rw[k] * u).sum() for k, u in zip(("dQt", "dKt", "dVt"), (UQ, UK, UV)))
+    assert abs(a - b) < 1e-12 * (abs(a) + 1)
+
+
+def test_n_equals_one_closed_form():
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(1, 5, 18)
+    tau = 0.3
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    alpha = tau * (UQ[0] @ K[0] + Q[0] @ UK[0])
+    Dv = dO[0] @ V[0]
+    # dS = 0 up to the rounding of dP - D (D is dO . O with O = V exactly)
+    assert np.abs(r["dQt"]).max() < 1e-15 and np.abs(r["dKt"]).max() < 1e-15
+    assert np.abs(r["dVt"]).max() < 1e-15
+    assert np.allclose(r["ddOt"], UV, rtol=1e-14, atol=1e-15)
+    assert np.isclose(r["alpha"][0], alpha, rtol=1e-14)
+    assert np.isclose(r["E"][0], dO[0] @ UV[0] - alpha * Dv, rtol=1e-13, atol=1e-14)
+
+
+def test_uq_uk_zero_reduces_to_first_backward_with_v_replaced():
+    torch = pytest.importorskip("torch")
+    Q, K, V, dO, _, _, UV = rand_inputs(14, 5, 19)
+    tau = 1 / np.sqrt(5)
+    z = np.zeros_like(Q)
+    r = orc.bob(Q, K, V, dO, z, z, UV, tau)
+    tq, tk, tu = (torch.tensor(x, requires_grad=True) for x in (Q, K, UV))
+    att = torch.softmax(tau * tq @ tk.T, dim=-1) @ tu
+    gq, gk = torch.autograd.grad(att, (tq, tk), torch.tensor(dO))
+    assert rel(r["ddOt"], att.detach().numpy()) < 1e-13
+    assert np.abs(r["dVt"]).max() == 0
+    assert rel(r["dQt"], gq.numpy()) < 1e-12
+    assert rel(r["dKt"], gk.numpy()) < 1e-12
+
+
+def test_jvp_identities_of_the_forward():
+    # d~dO is the JVP of O along (U_Q, U_K, U_V); alpha is the JVP of L
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(10, 4, 20)
+    tau = 0.55
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau)
+    h = 1e-5
+    _, _, Op, Lp = orc.forward(Q + h * UQ, K + h * UK, V + h * UV, tau)
+    _, _, Om, Lm = orc.forward(Q - h * UQ, K - h * UK, V - h * UV, tau)
+    assert rel(r["ddOt"], (Op - Om) / (2 * h)) < 1e-8
+    assert rel(r["alpha"], (Lp - Lm) / (2 * h)) < 1e-8
+
+
+def test_matches_torch_double_backward():
+    torch = pytest.importorskip("torch")
+    N, d = 24, 8
+    args = rand_inputs(N, d, 21)
+    tau = 1 / np.sqrt(d)
+    r = orc.bob(*args, tau)
+    tq, tk, tv, tdo = (torch.tensor(x, requires_grad=True) for x in args[:4])
+    uq, uk, uv = (torch.tensor(x) for x in args[4:])
+    out = torch.softmax(tau * tq @ tk.T, dim=-1) @ tv
+    dq, dk, dv = torch.autograd.grad(out, (tq, tk, tv), tdo, create_graph=True)
+    ph = (dq * uq).sum() + (dk * uk).sum() + (dv * uv).sum()
+    g = torch.autograd.grad(ph, (tq, tk, tv, tdo))
+    for key, t in zip(("dQt", "dKt", "dVt", "ddOt"), g):
+        assert rel(r[key], t.numpy()) < 1e-12, key
+
+
+def test_golden_fixture():
+    """Stored oracle outputs (written by tests/golden/make_golden.py) guard
+    against an unintended change of the oracle's arithmetic."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "bob_N6_d3_seed5.txt")
+    data = {}
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *vals = line.split()
+            data[key] = np.array([float(v) for v in vals])
+    args = rand_inputs(6, 3, 5)
+    r = orc.bob(*args, 0.5)
+    for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+        assert rel(r[key].ravel(), data[key]) < 1e-14, key
