@@ -1,0 +1,239 @@
+// C ABI of libflashbob: argument checks, dispatch and the device error word.
+// The declarations and their contracts are in include/flashbob.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/flashbob.h"
+#include "internal.h"
+
+namespace flashbob {
+namespace {
+
+// One error word per device that loads the library; kernels receive its
+// device address (taken with cudaGetSymbolAddress while that device is
+// current) and write a nonzero code when a bounded wait gives up.
+__device__ unsigned int g_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_error_ptr[kMaxDevices];
+std::mutex g_error_mu;
+
+struct Range {
+  uintptr_t lo, hi;
+};
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+flashbob_status check_sizes(int B, int H, int N, int d, float tau) {
+  if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return FLASHBOB_ERR_INVALID_ARG;
+  if (!(isfinite(tau) && tau > 0.f)) return FLASHBOB_ERR_INVALID_ARG;
+  if (d > 128 || B > 65535 || H > 65535) return FLASHBOB_ERR_UNSUPPORTED;
+  return FLASHBOB_OK;
+}
+
+flashbob_status check_dtype(flashbob_dtype t) {
+  return (t == FLASHBOB_F32 || t == FLASHBOB_BF16) ? FLASHBOB_OK : FLASHBOB_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+cudaError_t error_word_ptr(unsigned int** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_error_mu);
+  if (g_error_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) return e;
+    g_error_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *ptr = g_error_ptr[dev];
+  return cudaSuccess;
+}
+
+namespace {
+
+// Checks shared by flashbob_bob and its two passes: which buffers a pass
+// reads and writes follows from a.passes.
+flashbob_status run_bob(BobArgs& a, flashbob_dtype in_dtype) {
+  flashbob_status st = check_dtype(in_dtype);
+  if (st != FLASHBOB_OK) return st;
+  a.bf16 = in_dtype == FLASHBOB_BF16;
+  const bool p1 = a.passes & kPass1, p2 = a.passes & kPass2;
+  const size_t rows = (size_t)(a.B > 0 ? a.B : 0) * (a.H > 0 ? a.H : 0) * (a.N > 0 ? a.N : 0);
+  const size_t dd = a.d > 0 ? (size_t)a.d : 0;
+  const size_t inb = rows * dd * (a.bf16 ? 2 : 4), mat = rows * dd * 4, vec = rows * 4;
+  struct Buf {
+    const void* p;
+    size_t bytes;
+    bool out;
+  };
+  Buf bufs[16];
+  int n = 0;
+  auto add = [&](const void* p, size_t bytes, bool out) { bufs[n++] = Buf{p, bytes, out}; };
+  add(a.Q, inb, false);
+  add(a.K, inb, false);
+  add(a.V, inb, false);
+  add(a.dO, inb, false);
+  add(a.L, vec, false);
+  add(a.D, vec, false);
+  add(a.UQ, inb, false);
+  add(a.UK, inb, false);
+  add(a.UV, inb, false);
+  if (p1) {
+    add(a.O, mat, false);
+    add(a.dQt, mat, true);
+    add(a.ddOt, mat, true);
+  }
+  if (p2) {
+    add(a.dKt, mat, true);
+    add(a.dVt, mat, true);
+  }
+  add(a.alpha, vec, p1);  // written by pass 1, read by pass 2
+  add(a.E, vec, p1);
+  for (int i = 0; i < n; ++i)
+    if (!bufs[i].p) return FLASHBOB_ERR_INVALID_ARG;
+  st = check_sizes(a.B, a.H, a.N, a.d, a.tau);
+  if (st != FLASHBOB_OK) return st;
+  for (int i = 0; i < n; ++i)
+    if (!aligned16(bufs[i].p)) return FLASHBOB_ERR_MISALIGNED;
+  for (int i = 0; i < n; ++i) {
+    if (!bufs[i].out) continue;
+    const Range o{(uintptr_t)bufs[i].p, (uintptr_t)bufs[i].p + bufs[i].bytes};
+    for (int j = 0; j < n; ++j) {
+      if (j == i) continue;
+      const Range r{(uintptr_t)bufs[j].p, (uintptr_t)bufs[j].p + bufs[j].bytes};
+      if (overlaps(o, r)) return FLASHBOB_ERR_INVALID_ARG;
+    }
+  }
+  if (error_word_ptr(&a.err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  const cudaError_t e = tc_supported(a) ? tc_bob(a) : simt_bob(a);
+  return e == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
+}
+}  // namespace
+
+}  // namespace flashbob
+
+using namespace flashbob;
+
+extern "C" {
+
+const char* flashbob_status_string(flashbob_status s) {
+  switch (s) {
+    case FLASHBOB_OK: return "FLASHBOB_OK";
+    case FLASHBOB_ERR_INVALID_ARG: return "FLASHBOB_ERR_INVALID_ARG";
+    case FLASHBOB_ERR_UNSUPPORTED: return "FLASHBOB_ERR_UNSUPPORTED";
+    case FLASHBOB_ERR_MISALIGNED: return "FLASHBOB_ERR_MISALIGNED";
+    case FLASHBOB_ERR_CUDA: return "FLASHBOB_ERR_CUDA";
+    case FLASHBOB_ERR_TIMEOUT: return "FLASHBOB_ERR_TIMEOUT";
+  }
+  return "FLASHBOB_UNKNOWN_STATUS";
+}
+
+flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
+                              float* O, float* L, float* D, int B, int H, int N, int d,
+                              float tau, flashbob_dtype in_dtype, void* stream) {
+  flashbob_status st = check_dtype(in_dtype);
+  if (st != FLASHBOB_OK) return st;
+  if (!Q || !K || !V || !dO || !O || !L || !D) return FLASHBOB_ERR_INVALID_ARG;
+  st = check_sizes(B, H, N, d, tau);
+  if (st != FLASHBOB_OK) return st;
+  const void* ptrs[] = {Q, K, V, dO, O, L, D};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FLASHBOB_ERR_MISALIGNED;
+  const size_t rows = (size_t)B * H * N;
+  const size_t in_bytes = rows * d * (in_dtype == FLASHBOB_BF16 ? 2 : 4);
+  const Range ins[] = {{(uintptr_t)Q, (uintptr_t)Q + in_bytes},
+                       {(uintptr_t)K, (uintptr_t)K + in_bytes},
+                       {(uintptr_t)V, (uintptr_t)V + in_bytes},
+                       {(uintptr_t)dO, (uintptr_t)dO + in_bytes}};
+  const Range outs[] = {{(uintptr_t)O, (uintptr_t)O + rows * d * 4},
+                        {(uintptr_t)L, (uintptr_t)L + rows * 4},
+                        {(uintptr_t)D, (uintptr_t)D + rows * 4}};
+  for (const Range& o : outs) {
+    for (const Range& i : ins)
+      if (overlaps(o, i)) return FLASHBOB_ERR_INVALID_ARG;
+    for (const Range& o2 : outs)
+      if (&o != &o2 && overlaps(o, o2)) return FLASHBOB_ERR_INVALID_ARG;
+  }
+  PrepArgs a{Q, K, V, dO, O, L, D, B, H, N, d, tau, in_dtype == FLASHBOB_BF16,
+             (cudaStream_t)stream};
+  return simt_prep(a) == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
+}
+
+flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const float* O,
+                             const void* dO, const float* L, const float* D, const void* UQ,
+                             const void* UK, const void* UV, float tau, float* dQt, float* dKt,
+                             float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
+                             int N, int d, flashbob_dtype in_dtype, void* stream) {
+  BobArgs a{Q,     K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, dKt, dVt, ddOt, alpha, E, B, H, N, d,
+            false, (cudaStream_t)stream, nullptr, kPass1 | kPass2};
+  return run_bob(a, in_dtype);
+}
+
+flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, const float* O,
+                                   const void* dO, const float* L, const float* D,
+                                   const void* UQ, const void* UK, const void* UV, float tau,
+                                   float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
+                                   int N, int d, flashbob_dtype in_dtype, void* stream) {
+  BobArgs a{Q,     K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, nullptr, nullptr, ddOt, alpha, E, B,
+            H,     N, d, false, (cudaStream_t)stream, nullptr, kPass1};
+  return run_bob(a, in_dtype);
+}
+
+flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, const void* dO,
+                                   const float* L, const float* D, const float* alpha,
+                                   const float* E, const void* UQ, const void* UK,
+                                   const void* UV, float tau, float* dKt, float* dVt, int B,
+                                   int H, int N, int d, flashbob_dtype in_dtype, void* stream) {
+  // alpha and E are inputs of pass 2; the BobArgs fields keep their names.
+  BobArgs a{Q,       K,       V,     nullptr, dO, L, D, UQ, UK, UV, tau, nullptr, dKt, dVt,
+            nullptr, (float*)alpha, (float*)E, B, H, N, d, false, (cudaStream_t)stream, nullptr,
+            kPass2};
+  return run_bob(a, in_dtype);
+}
+
+flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1, int* Bc1,
+                                        int* Br2, int* Bc2, size_t* smem_bytes_pass1,
+                                        size_t* smem_bytes_pass2) {
+  if (check_dtype(in_dtype) != FLASHBOB_OK) return FLASHBOB_ERR_INVALID_ARG;
+  if (d <= 0 || d > 128) return FLASHBOB_ERR_UNSUPPORTED;
+  BobArgs probe{};
+  probe.d = d;
+  probe.N = 1;
+  probe.bf16 = in_dtype == FLASHBOB_BF16;
+  const bool tc = tc_supported(probe);
+  const int br1 = tc ? kTcRows : kSimtTile, bc1 = tc ? kTcStream : kSimtTile;
+  const int bc2 = tc ? kTcRows : kSimtTile, br2 = tc ? kTcStream : kSimtTile;
+  if (Br1) *Br1 = br1;
+  if (Bc1) *Bc1 = bc1;
+  if (Br2) *Br2 = br2;
+  if (Bc2) *Bc2 = bc2;
+  if (smem_bytes_pass1) *smem_bytes_pass1 = tc ? tc_pass1_smem() : simt_pass1_smem(d);
+  if (smem_bytes_pass2) *smem_bytes_pass2 = tc ? tc_pass2_smem() : simt_pass2_smem(d);
+  return FLASHBOB_OK;
+}
+
+flashbob_status flashbob_last_device_error(void) {
+  unsigned int* p = nullptr;
+  if (error_word_ptr(&p) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return FLASHBOB_ERR_CUDA;
+    return FLASHBOB_ERR_TIMEOUT;
+  }
+  return FLASHBOB_OK;
+}
+
+}  // extern "C"

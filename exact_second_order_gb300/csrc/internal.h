@@ -1,0 +1,55 @@
+// Internal interface between the C ABI (flashbob_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace flashbob {
+
+struct PrepArgs {
+  const void *Q, *K, *V, *dO;
+  float *O, *L, *D;
+  int B, H, N, d;
+  float tau;
+  bool bf16;
+  cudaStream_t stream;
+};
+
+struct BobArgs {
+  const void *Q, *K, *V;
+  const float* O;
+  const void* dO;
+  const float *L, *D;
+  const void *UQ, *UK, *UV;
+  float tau;
+  float *dQt, *dKt, *dVt, *ddOt, *alpha, *E;
+  int B, H, N, d;
+  bool bf16;
+  cudaStream_t stream;
+  unsigned int* err;  // device error word of the current device
+  int passes;         // bit 0: pass 1, bit 1: pass 2
+};
+
+constexpr int kPass1 = 1;
+constexpr int kPass2 = 2;
+
+// fp32 CUDA-core kernels (any 1 <= d <= 128; fp32 or bf16 inputs).
+constexpr int kSimtTile = 32;
+cudaError_t simt_prep(const PrepArgs& a);
+cudaError_t simt_bob(const BobArgs& a);
+size_t simt_pass1_smem(int d);
+size_t simt_pass2_smem(int d);
+
+// tcgen05 tensor-core kernels (bf16 inputs, d = 64).
+constexpr int kTcRows = 128;    // rows of the resident block (MMA M) in both passes
+constexpr int kTcStream = 32;   // rows of a streamed tile (MMA N of the score GEMMs)
+bool tc_supported(const BobArgs& a);
+cudaError_t tc_bob(const BobArgs& a);
+size_t tc_pass1_smem();
+size_t tc_pass2_smem();
+
+// Device error word (one per device): a kernel writes a nonzero code when a
+// bounded wait gives up.  Codes: 1 = mbarrier wait timed out.
+cudaError_t error_word_ptr(unsigned int** ptr);
+
+}  // namespace flashbob

@@ -1,0 +1,187 @@
+"""Python binding of libflashbob (argument marshalling only).
+
+The functions carry the C names of ``include/flashbob.h``.  Tensors are
+PyTorch CUDA tensors used only as device memory; every step of the
+computation runs in the library's kernels.  Loading fails loudly when the
+library has not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libflashbob.so")
+
+FLASHBOB_OK = 0
+FLASHBOB_ERR_INVALID_ARG = 1
+FLASHBOB_ERR_UNSUPPORTED = 2
+FLASHBOB_ERR_MISALIGNED = 3
+FLASHBOB_ERR_CUDA = 4
+FLASHBOB_ERR_TIMEOUT = 5
+FLASHBOB_F32 = 0
+FLASHBOB_BF16 = 1
+
+# Every entry point the header declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SIGNATURES = {
+    "flashbob_prep": ([_P] * 7 + [_I] * 4 + [_F, _I, _P], _I),
+    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 5 + [_P], _I),
+    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 5 + [_P], _I),
+    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 5 + [_P], _I),
+    "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
+                                + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
+    "flashbob_last_device_error": ([], _I),
+    "flashbob_status_string": ([_I], ctypes.c_char_p),
+}
+
+_lib = None
+
+
+class FlashbobError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {flashbob_status_string(status)}")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libflashbob.so (once) and declare the signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with exact_second_order_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return FLASHBOB_F32
+    if t.dtype == torch.bfloat16:
+        return FLASHBOB_BF16
+    raise TypeError(f"unsupported input dtype {t.dtype}")
+
+
+def _stream_handle(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return t.data_ptr()
+
+
+def flashbob_status_string(status: int) -> str:
+    return load_library().flashbob_status_string(status).decode()
+
+
+def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, stream=None) -> None:
+    """O, L, D of [B, H, N, d] inputs (see flashbob_prep in the header)."""
+    B, H, N, d = Q.shape
+    st = load_library().flashbob_prep(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, N, d,
+        float(tau), _dtype_code(Q), _stream_handle(stream))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_prep")
+
+
+def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, ddOt, alpha, E,
+                 stream=None) -> None:
+    """d~Q, d~K, d~V, d~dO, alpha, E (see flashbob_bob in the header)."""
+    B, H, N, d = Q.shape
+    st = load_library().flashbob_bob(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
+        _ptr(UV), float(tau), _ptr(dQt), _ptr(dKt), _ptr(dVt), _ptr(ddOt), _ptr(alpha), _ptr(E),
+        B, H, N, d, _dtype_code(Q), _stream_handle(stream))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_bob")
+
+
+def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, alpha, E,
+                       stream=None) -> None:
+    """Pass 1 only: d~Q, d~dO, alpha, E (see flashbob_bob_pass1 in the header)."""
+    B, H, N, d = Q.shape
+    st = load_library().flashbob_bob_pass1(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
+        _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, N, d,
+        _dtype_code(Q), _stream_handle(stream))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_bob_pass1")
+
+
+def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt, dVt,
+                       stream=None) -> None:
+    """Pass 2 only: d~K, d~V from pass 1's alpha, E (see flashbob_bob_pass2)."""
+    B, H, N, d = Q.shape
+    st = load_library().flashbob_bob_pass2(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(D), _ptr(alpha), _ptr(E), _ptr(UQ),
+        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, N, d, _dtype_code(Q),
+        _stream_handle(stream))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_bob_pass2")
+
+
+def flashbob_bob_tile_sizes(d: int, in_dtype: int) -> dict:
+    """Tiles and dynamic shared memory of flashbob_bob for (d, in_dtype)."""
+    v = [ctypes.c_int() for _ in range(4)]
+    s = [ctypes.c_size_t() for _ in range(2)]
+    st = load_library().flashbob_bob_tile_sizes(d, in_dtype, *(ctypes.byref(x) for x in v),
+                                                *(ctypes.byref(x) for x in s))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_bob_tile_sizes")
+    return {"Br1": v[0].value, "Bc1": v[1].value, "Br2": v[2].value, "Bc2": v[3].value,
+            "smem_bytes_pass1": s[0].value, "smem_bytes_pass2": s[1].value}
+
+
+def flashbob_last_device_error() -> int:
+    """Status of the device error word (synchronises the device, then clears)."""
+    return load_library().flashbob_last_device_error()
+
+
+# ---------------------------------------------------------------------------
+# Convenience wrappers: allocate the outputs with torch, then call the ABI.
+# ---------------------------------------------------------------------------
+
+def prep(Q, K, V, dO, tau: float, stream=None):
+    """Allocate O, L, D on Q's device and run flashbob_prep."""
+    import torch
+    B, H, N, d = Q.shape
+    O = torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device)
+    L = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    D = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    flashbob_prep(Q, K, V, dO, O, L, D, tau, stream)
+    return O, L, D
+
+
+def alloc_bob_outputs(Q, fill: float | None = None) -> dict:
+    """fp32 output buffers of flashbob_bob (optionally filled, e.g. with NaN)."""
+    import torch
+    B, H, N, d = Q.shape
+    out = {k: torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device)
+           for k in ("dQt", "dKt", "dVt", "ddOt")}
+    out.update({k: torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+                for k in ("alpha", "E")})
+    if fill is not None:
+        for t in out.values():
+            t.fill_(fill)
+    return out
+
+
+def bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, out: dict | None = None, stream=None):
+    """Run flashbob_bob into ``out`` (allocated when None); returns the dict."""
+    if out is None:
+        out = alloc_bob_outputs(Q)
+    flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, out["dQt"], out["dKt"], out["dVt"],
+                 out["ddOt"], out["alpha"], out["E"], stream)
+    return out

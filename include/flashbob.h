@@ -1,0 +1,142 @@
+/*
+ * flashbob.h -- C ABI of libflashbob: exact backward-over-backward (BoB) of
+ * softmax attention on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages on the method; sections named as on the pages):
+ *   [FBN] "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+ *         Attention" (paper notes): 方法详解/整体框架 (the objective Phi and the
+ *         four outputs), 关键设计 1 (row scalars alpha, E and the affine
+ *         correction), 关键设计 2 (two-pass row/column schedule, no atomics).
+ *   [FAB] "FlashAttention 的反向传播设计：在 SRAM 内部重计算 Softmax 的显存收益":
+ *         section 一 (forward and first-backward formulas), section 二 (P is
+ *         recomputed from saved row statistics).
+ *
+ * Notation, per (batch b, head h): Q, K, V, dO, U_Q, U_K, U_V are N x d;
+ * S = tau Q K^T, L_i = log sum_j exp(S_ij), P = exp(S - L), O = P V,
+ * D_i = dO_i . O_i, dP = dO V^T, dS = P o (dP - D), dQ = tau dS K,
+ * dK = tau dS^T Q, dV = P^T dO, and
+ *     Phi = <dQ, U_Q> + <dK, U_K> + <dV, U_V>.
+ * flashbob_bob returns the total derivatives d~Q, d~K, d~V, d~dO of Phi with
+ * respect to Q, K, V and dO, plus the row scalars alpha_i = sum_j P_ij F_ij
+ * (F = tau (U_Q K^T + Q U_K^T)) and E_i = sum_j P_ij d~P_ij.
+ *
+ * Layout: every N x d tensor is a contiguous row-major [B, H, N, d] array;
+ * every length-N row vector is a contiguous [B, H, N] array.  Inputs are
+ * either all fp32 or all bf16 (Q, K, V, dO, U_Q, U_K, U_V; selected by
+ * in_dtype); O, L, D and every output are fp32.
+ *
+ * Ownership: the caller allocates and owns every buffer; all data pointers
+ * are DEVICE pointers on the current CUDA device.  The library allocates no
+ * device memory.  Its only device state is one error word per device,
+ * written when a kernel's bounded wait gives up (see
+ * flashbob_last_device_error).
+ *
+ * Calling convention: argument checks run on the host and return before any
+ * launch; work is enqueued on `stream` (a cudaStream_t; NULL means the
+ * legacy default stream) and the call returns without synchronising.  Two
+ * calls on different streams must not share output buffers.
+ *
+ * Errors: a call that returns anything but FLASHBOB_OK has launched nothing
+ * (FLASHBOB_ERR_CUDA: a launch failed; earlier launches of the same call may
+ * have run).  Outputs may not overlap inputs or each other.
+ */
+#ifndef FLASHBOB_H
+#define FLASHBOB_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLASHBOB_OK = 0,
+  FLASHBOB_ERR_INVALID_ARG = 1, /* null pointer, size <= 0, bad tau, overlap  */
+  FLASHBOB_ERR_UNSUPPORTED = 2, /* d > 128, or sizes beyond the grid limits   */
+  FLASHBOB_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned              */
+  FLASHBOB_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed       */
+  FLASHBOB_ERR_TIMEOUT = 5      /* a kernel's bounded wait gave up            */
+} flashbob_status;
+
+typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
+
+/*
+ * flashbob_prep: forward row state for the BoB ([FAB] sections 一/二,
+ * [FBN] 关键设计 1 for D).
+ *   in : Q, K, V, dO  [B,H,N,d] of in_dtype
+ *   out: O [B,H,N,d] fp32 (O = P V), L [B,H,N] fp32 (natural-log logsumexp of
+ *        tau Q K^T per row), D [B,H,N] fp32 (D_i = dO_i . O_i)
+ *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
+ *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535.  One launch.
+ */
+flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
+                              float* O, float* L, float* D, int B, int H, int N, int d,
+                              float tau, flashbob_dtype in_dtype, void* stream);
+
+/*
+ * flashbob_bob: exact BoB of softmax attention with the two-pass schedule of
+ * [FBN] 关键设计 2; the closed form and affine correction of [FBN] 关键设计 1.
+ *   in : Q, K, V, dO, U_Q, U_K, U_V [B,H,N,d] of in_dtype; O [B,H,N,d] fp32;
+ *        L, D [B,H,N] fp32 (as written by flashbob_prep); tau as in prep.
+ *   out: dQt, dKt, dVt, ddOt [B,H,N,d] fp32 (d~Q, d~K, d~V, d~dO);
+ *        alpha, E [B,H,N] fp32.  Every element is written exactly once.
+ *   Pass 1 (row-resident) writes d~Q, d~dO, alpha, E; pass 2 (column-
+ *   resident) reads alpha, E and writes d~K, d~V.  No N x N tensor is ever
+ *   written to device memory and no atomics are used.
+ *   Limits: as flashbob_prep.  bf16 inputs with d = 64 run the tcgen05
+ *   tensor-core kernels; every other case runs the fp32 CUDA-core kernels.
+ */
+flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const float* O,
+                             const void* dO, const float* L, const float* D, const void* UQ,
+                             const void* UK, const void* UV, float tau, float* dQt, float* dKt,
+                             float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
+                             int N, int d, flashbob_dtype in_dtype, void* stream);
+
+/*
+ * flashbob_bob_pass1 / flashbob_bob_pass2: the two launches of flashbob_bob,
+ * callable one at a time ([FBN] 关键设计 2).  Same arguments, layouts and
+ * limits as flashbob_bob.
+ *   pass 1 (row-resident): reads Q, K, V, O, dO, L, D, U_Q, U_K, U_V and
+ *     writes dQt, ddOt, alpha, E.
+ *   pass 2 (column-resident): reads Q, K, V, dO, L, D, U_Q, U_K, U_V and the
+ *     alpha, E written by pass 1, and writes dKt, dVt.
+ * flashbob_bob(...) is exactly pass 1 followed by pass 2 on the same stream.
+ */
+flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, const float* O,
+                                   const void* dO, const float* L, const float* D,
+                                   const void* UQ, const void* UK, const void* UV, float tau,
+                                   float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
+                                   int N, int d, flashbob_dtype in_dtype, void* stream);
+
+flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, const void* dO,
+                                   const float* L, const float* D, const float* alpha,
+                                   const float* E, const void* UQ, const void* UK,
+                                   const void* UV, float tau, float* dKt, float* dVt, int B,
+                                   int H, int N, int d, flashbob_dtype in_dtype, void* stream);
+
+/*
+ * flashbob_bob_tile_sizes: the tiles flashbob_bob uses for (d, in_dtype):
+ * pass-1 row block Br1 and column tile Bc1, pass-2 column block Bc2 and row
+ * tile Br2, and each pass's dynamic shared memory per CTA in bytes.  Any
+ * output pointer may be NULL.  FLASHBOB_ERR_UNSUPPORTED for d outside 1..128.
+ */
+flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1, int* Bc1,
+                                        int* Br2, int* Bc2, size_t* smem_bytes_pass1,
+                                        size_t* smem_bytes_pass2);
+
+/*
+ * flashbob_last_device_error: FLASHBOB_ERR_TIMEOUT if a kernel of this
+ * library on the current device gave up a bounded wait since the previous
+ * call of this function, else FLASHBOB_OK (FLASHBOB_ERR_CUDA if the word
+ * cannot be read).  Synchronises the current device, then clears the word.
+ */
+flashbob_status flashbob_last_device_error(void);
+
+/* flashbob_status_string: a static, human-readable name of `s`. */
+const char* flashbob_status_string(flashbob_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHBOB_H */

@@ -1,0 +1,95 @@
+"""Shared helpers of the parity tests: run the CUDA path through the C ABI on
+seeded inputs and compare with the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from exact_second_order_gb300 import flashbob as fb
+from exact_second_order_gb300.inputs import NAMES, as_float64_numpy, make_inputs
+from oracle import bob as orc
+
+# Gates: relative Frobenius error on every output.
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+MAT_KEYS = ("dQt", "dKt", "dVt", "ddOt")
+ROW_KEYS = ("alpha", "E")
+
+
+def rel_fro(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    num = np.linalg.norm(got - ref)
+    if den == 0.0:
+        return num  # absolute check for a zero reference
+    return num / den
+
+
+def run_cuda(w, stream=None, fill_nan=True):
+    """Inputs of workload ``w`` (CPU tensors) and the device results of
+    flashbob_prep + flashbob_bob."""
+    x = make_inputs(w)
+    dev = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, stream)
+    out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan") if fill_nan else None)
+    fb.bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"], dev["UK"], dev["UV"],
+           w.tau, out=out, stream=stream)
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    return x, dev, {"O": O, "L": L, "D": D}, out
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def oracle_inputs(x):
+    return [as_float64_numpy(x[k]) for k in NAMES]
+
+
+def full_oracle_errors(w, x, state, out, heads=None):
+    """Relative Frobenius errors of every output against the full oracle."""
+    args = oracle_inputs(x)
+    Q, K, V, dO = args[:4]
+    ref = orc.bob_batched(*args, w.tau, heads=heads)
+    O, L, D = orc.prep_batched(Q, K, V, dO, w.tau) if heads is None else (None, None, None)
+    errs = {}
+    sel = (lambda a: a) if heads is None else (lambda a: np.stack([a[b, h] for b, h in heads]))
+    for k in MAT_KEYS + ROW_KEYS:
+        errs[k] = rel_fro(sel(to_np(out[k])), sel(ref[k]))
+    errs["L"] = rel_fro(sel(to_np(state["L"])), sel(ref["L"]))
+    errs["D"] = rel_fro(sel(to_np(state["D"])), sel(ref["D"]))
+    if O is not None:
+        errs["O"] = rel_fro(to_np(state["O"]), O)
+    return errs
+
+
+def sampled_row_errors(w, x, out, state, n_rows=256, seed=1234, heads=None):
+    """Row outputs of ``n_rows`` seeded rows per listed head against
+    ``oracle.bob_rows`` (O(N d) per row)."""
+    rng = np.random.default_rng(seed)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    got = {k: [] for k in ("dQt", "ddOt", "alpha", "E", "L", "D")}
+    ref = {k: [] for k in got}
+    for b, h in heads:
+        rows = np.sort(rng.choice(N, size=min(n_rows, N), replace=False))
+        args = [as_float64_numpy(x[k][b, h]) for k in NAMES]
+        r = orc.bob_rows(*args, w.tau, rows)
+        for k in got:
+            src = out[k] if k in out else state[k]
+            got[k].append(to_np(src[b, h][rows]))
+            ref[k].append(r[k])
+    return {k: rel_fro(np.concatenate(got[k]), np.concatenate(ref[k])) for k in got}
+
+
+def column_sum_residuals(out):
+    """|sum_j d~K_j| and |sum_j d~V_j| relative to the column norms: both sums
+    vanish exactly (Phi is invariant under K -> K + 1 c^T, V -> V + 1 c^T)."""
+    res = {}
+    for k in ("dKt", "dVt"):
+        a = out[k].double()
+        s = a.sum(dim=2)  # [B, H, d]
+        scale = a.pow(2).sum(dim=2).sqrt()
+        res[k] = float((s.norm() / scale.norm()).item())
+    return res

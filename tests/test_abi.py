@@ -1,0 +1,156 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point the header declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_second_order_gb300 import flashbob as fb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def lib():
+    if not os.path.exists(fb.LIB_PATH):
+        from exact_second_order_gb300.build import build
+        build()
+    return fb.load_library()
+
+
+def declared_entry_points():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(flashbob_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for n in ("flashbob_prep", "flashbob_bob", "flashbob_bob_pass1", "flashbob_bob_pass2",
+              "flashbob_bob_tile_sizes",
+              "flashbob_last_device_error", "flashbob_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+        assert name in fb._SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert fb.flashbob_status_string(0) == "FLASHBOB_OK"
+    assert fb.flashbob_status_string(5) == "FLASHBOB_ERR_TIMEOUT"
+    assert fb.flashbob_status_string(99) == "FLASHBOB_UNKNOWN_STATUS"
+
+
+def test_tile_sizes(lib):
+    t = fb.flashbob_bob_tile_sizes(64, fb.FLASHBOB_F32)
+    assert t["Br1"] > 0 and t["Bc2"] > 0 and t["smem_bytes_pass1"] > 0
+    t = fb.flashbob_bob_tile_sizes(64, fb.FLASHBOB_BF16)
+    assert t["smem_bytes_pass1"] <= 232448 and t["smem_bytes_pass2"] <= 232448
+    t = fb.flashbob_bob_tile_sizes(128, fb.FLASHBOB_BF16)
+    assert t["smem_bytes_pass1"] <= 232448
+    for bad in (0, -1, 129):
+        assert lib.flashbob_bob_tile_sizes(bad, 0, None, None, None, None, None, None) == \
+            fb.FLASHBOB_ERR_UNSUPPORTED
+    assert lib.flashbob_bob_tile_sizes(64, 7, None, None, None, None, None, None) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+
+
+def _bob_raw(lib, ptrs, tau=0.125, B=1, H=1, N=8, d=64, dtype=0):
+    return lib.flashbob_bob(*ptrs[:10], tau, *ptrs[10:], B, H, N, d, dtype, None)
+
+
+def _fake_ptrs(n=16, stride=1 << 20, base=1 << 32):
+    # distinct, 16-byte aligned, non-overlapping addresses; never dereferenced
+    return [base + i * stride for i in range(n)]
+
+
+def test_bob_rejects_bad_arguments_on_the_host(lib):
+    ok = _fake_ptrs()
+    E = fb
+    # null pointer
+    for i in range(16):
+        p = list(ok)
+        p[i] = None
+        assert _bob_raw(lib, p) == E.FLASHBOB_ERR_INVALID_ARG
+    # sizes and tau
+    for kw in ({"B": 0}, {"H": -1}, {"N": 0}, {"d": 0}, {"tau": 0.0}, {"tau": -1.0},
+               {"tau": float("nan")}, {"tau": float("inf")}, {"dtype": 3}):
+        assert _bob_raw(lib, ok, **kw) == E.FLASHBOB_ERR_INVALID_ARG, kw
+    assert _bob_raw(lib, ok, d=129) == E.FLASHBOB_ERR_UNSUPPORTED
+    assert _bob_raw(lib, ok, H=70000) == E.FLASHBOB_ERR_UNSUPPORTED
+    # misaligned pointer
+    for i in range(16):
+        p = list(ok)
+        p[i] += 8
+        assert _bob_raw(lib, p) == E.FLASHBOB_ERR_MISALIGNED
+    # an output overlapping an input, and two overlapping outputs
+    p = list(ok)
+    p[10] = p[0] + 16
+    assert _bob_raw(lib, p) == E.FLASHBOB_ERR_INVALID_ARG
+    p = list(ok)
+    p[11] = p[10]
+    assert _bob_raw(lib, p) == E.FLASHBOB_ERR_INVALID_ARG
+
+
+def test_prep_rejects_bad_arguments_on_the_host(lib):
+    ok = _fake_ptrs(7)
+
+    def call(p=ok, B=1, H=1, N=8, d=64, tau=0.125, dtype=0):
+        return lib.flashbob_prep(*p, B, H, N, d, tau, dtype, None)
+    for i in range(7):
+        p = list(ok)
+        p[i] = None
+        assert call(p) == fb.FLASHBOB_ERR_INVALID_ARG
+        p = list(ok)
+        p[i] += 4
+        assert call(p) == fb.FLASHBOB_ERR_MISALIGNED
+    assert call(N=0) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert call(tau=float("nan")) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert call(d=200) == fb.FLASHBOB_ERR_UNSUPPORTED
+    p = list(ok)
+    p[4] = p[3]
+    assert call(p) == fb.FLASHBOB_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    saved = fb._lib
+    fb._lib = None
+    try:
+        with pytest.raises(ImportError):
+            fb.load_library(str(tmp_path / "missing.so"))
+    finally:
+        fb._lib = saved
+
+
+def test_pass_entry_points_reject_bad_arguments_on_the_host(lib):
+    ok = _fake_ptrs()
+    p1 = ok[:15]
+    bad = list(p1)
+    bad[3] = None  # O
+    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 8, 64, 0, None) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+    bad = list(p1)
+    bad[10] = bad[4]  # d~Q over dO
+    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 8, 64, 0, None) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+    p2 = ok[:13]
+    bad = list(p2)
+    bad[6] = None  # alpha
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 8, 64, 0, None) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+    bad = list(p2)
+    bad[11] = bad[6]  # d~K over alpha
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 8, 64, 0, None) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+    bad = list(p2)
+    bad[12] += 4
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 8, 64, 0, None) == \
+        fb.FLASHBOB_ERR_MISALIGNED

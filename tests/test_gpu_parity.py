@@ -1,0 +1,143 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small shapes: every output against the full oracle, element by element
+(relative Frobenius error).  Full workload sizes: 256 seeded rows per head
+against the per-row oracle, plus the exact column-sum invariants of d~K
+and d~V, NaN-poisoned outputs (every element written) and the memory check.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_second_order_gb300 import flashbob as fb
+from exact_second_order_gb300 import inputs as wl
+from tests.helpers import (MAT_KEYS, ROW_KEYS, TOL, column_sum_residuals, full_oracle_errors,
+                           run_cuda, sampled_row_errors)
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert_all_written(out):
+    for k, t in out.items():
+        assert not torch.isnan(t).any().item(), f"{k} has unwritten (NaN) elements"
+
+
+def _check_full(w, heads=None):
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    errs = full_oracle_errors(w, x, state, out, heads=heads)
+    tol = TOL[w.dtype]
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{w.name}: {bad} (all: {errs})"
+    return errs
+
+
+def test_tiny_f32_workload_full_oracle():
+    errs = _check_full(wl.TINY_F32)
+    assert max(errs.values()) < 1e-4
+
+
+@pytest.mark.parametrize("N", [1, 2, 7, 31, 33, 65, 129, 300])
+@pytest.mark.parametrize("d", [64, 128, 5, 100])
+def test_f32_ragged_shapes(N, d):
+    _check_full(wl.small_workload(1, 2, N, d, "f32", seed=N + d))
+
+
+def test_f32_batch_heads():
+    _check_full(wl.small_workload(2, 3, 97, 64, "f32", seed=3))
+
+
+@pytest.mark.parametrize("N", [1, 7, 32, 127, 128, 129, 300, 1000])
+@pytest.mark.parametrize("d", [64, 128, 96])
+def test_bf16_ragged_shapes(N, d):
+    _check_full(wl.small_workload(1, 2, N, d, "bf16", seed=N + d))
+
+
+def test_bf16_peaked_and_stress_small():
+    _check_full(wl.small_workload(1, 2, 700, 64, "bf16", seed=9, peaked_k_rows=True))
+    _check_full(wl.small_workload(1, 2, 700, 64, "bf16", seed=9, peaked_k_rows=True,
+                                  stress=True))
+
+
+def test_gpt2_layer_workload_full_oracle():
+    _check_full(wl.GPT2_LAYER)
+
+
+@pytest.mark.parametrize("w", [wl.MID_LENGTH, wl.MID_LENGTH_PEAKED, wl.MID_LENGTH_STRESS],
+                         ids=lambda w: w.name)
+def test_mid_length_workloads(w):
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    errs = sampled_row_errors(w, x, out, state)
+    assert max(errs.values()) <= TOL["bf16"], errs
+    res = column_sum_residuals(out)
+    assert max(res.values()) <= TOL["bf16"], res
+    # full oracle on one head covers d~K and d~V element by element
+    full = full_oracle_errors(w, x, state, out, heads=[(0, 0)])
+    assert max(full.values()) <= TOL["bf16"], full
+
+
+def _memory_checked_run(w):
+    torch.cuda.synchronize()
+    x = wl.make_inputs(w)
+    dev = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau)
+    out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan"))
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    before_alloc = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    fb.bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"], dev["UK"], dev["UV"],
+           w.tau, out=out)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.max_memory_allocated() - before_alloc <= 64 << 20
+    assert free_before - free_after <= 64 << 20
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    return x, dev, {"O": O, "L": L, "D": D}, out
+
+
+@pytest.mark.parametrize("w", [wl.LONG_CONTEXT, wl.EXTREME_D64, wl.EXTREME_D128],
+                         ids=lambda w: w.name)
+def test_long_workloads_sampled_rows_and_memory(w):
+    x, dev, state, out = _memory_checked_run(w)
+    _assert_all_written(out)
+    heads = [(0, h) for h in range(w.H)]
+    errs = sampled_row_errors(w, x, out, state, n_rows=256 if w.H == 1 else 64, heads=heads)
+    assert max(errs.values()) <= TOL["bf16"], errs
+    res = column_sum_residuals(out)
+    assert max(res.values()) <= TOL["bf16"], res
+
+
+def test_stream_argument_is_honoured():
+    w = wl.small_workload(1, 2, 200, 64, "bf16", seed=5)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        x, dev, state, out = run_cuda(w, stream=s)
+    errs = full_oracle_errors(w, x, state, out)
+    assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_repeated_calls_are_deterministic():
+    w = wl.small_workload(1, 3, 333, 64, "bf16", seed=6)
+    _, dev, state, out1 = run_cuda(w)
+    out2 = fb.bob(dev["Q"], dev["K"], dev["V"], state["O"], dev["dO"], state["L"], state["D"],
+                  dev["UQ"], dev["UK"], dev["UV"], w.tau)
+    torch.cuda.synchronize()
+    for k in MAT_KEYS + ROW_KEYS:
+        assert torch.equal(out1[k], out2[k]), k
+
+
+def test_bad_arguments_return_codes_and_launch_nothing():
+    w = wl.small_workload(1, 1, 64, 64, "bf16")
+    x, dev, state, out = run_cuda(w)
+    before = {k: v.clone() for k, v in out.items()}
+    with pytest.raises(fb.FlashbobError) as e:
+        fb.bob(dev["Q"], dev["K"], dev["V"], state["O"], dev["dO"], state["L"], state["D"],
+               dev["UQ"], dev["UK"], dev["UV"], float("nan"), out=out)
+    assert e.value.status == fb.FLASHBOB_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    for k in out:
+        assert torch.equal(out[k], before[k]) or torch.isnan(before[k]).all()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    np.testing.assert_equal(fb.flashbob_status_string(0), "FLASHBOB_OK")
