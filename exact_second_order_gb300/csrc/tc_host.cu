@@ -1,0 +1,44 @@
+// Host side of the tensor-core path: which calls it serves, the TMA tensor
+// maps of the seven bf16 inputs, and the two launches on the caller's stream.
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace flashbob {
+
+cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
+                            const CUtensorMap* maps32);
+cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
+                            const CUtensorMap* maps32);
+
+bool tc_supported(const BobArgs& a) { return a.bf16 && a.d == 64; }
+
+cudaError_t tc_bob(const BobArgs& a) {
+  const int BH = a.B * a.H;
+  cudaError_t e = cudaSuccess;
+  if (a.passes & kPass1) {
+    CUtensorMap m128[3], m32[4];
+    const void* rows[3] = {a.Q, a.dO, a.UQ};
+    const void* cols[4] = {a.K, a.V, a.UK, a.UV};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16_d64(&m128[i], rows[i], BH, a.N, kTcRows);
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16_d64(&m32[i], cols[i], BH, a.N, kTcStream);
+    if (e != cudaSuccess) return e;
+    e = tc_launch_pass1(a, m128, m32);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.passes & kPass2) {
+    CUtensorMap m128[4], m32[3];
+    const void* res[4] = {a.K, a.V, a.UK, a.UV};
+    const void* str[3] = {a.Q, a.dO, a.UQ};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16_d64(&m128[i], res[i], BH, a.N, kTcRows);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16_d64(&m32[i], str[i], BH, a.N, kTcStream);
+    if (e != cudaSuccess) return e;
+    e = tc_launch_pass2(a, m128, m32);
+  }
+  return e;
+}
+
+}  // namespace flashbob

@@ -1,0 +1,360 @@
+// Pass 1 of the exact attention backward-over-backward on sm_103a tensor
+// cores: bf16 inputs, head dim 64, fp32 accumulation in tensor memory.
+//
+// "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+// Attention" (paper notes), 关键设计 2: a block of query rows stays on chip
+// while key/value column tiles stream past; P is recomputed from the saved
+// logsumexp L; the six row accumulators (alpha, E0, B, R, Omega, d~dO0) are
+// alpha-free, and 关键设计 1's affine correction
+//     E = E0 - alpha D,  d~dO = d~dO0 - alpha O,  d~Q = tau (Omega - alpha R - E B)
+// runs once in the epilogue, so every output row is written exactly once.
+//
+// CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
+//   warp 0      TMA producer: Q, dO, U_Q blocks once, then K, V, U_K, U_V
+//               tiles of 32 key rows through a 6-stage mbarrier ring;
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
+//   warps 2-5   elementwise warpgroup 0 (tiles 0, 2, 4, ...),
+//   warps 6-9   elementwise warpgroup 1 (tiles 1, 3, 5, ...).
+// TMEM (512 columns x 128 lanes, fp32):
+//   [0,64) B = P K   [64,128) R = (P o dP) K   [128,192) Omega   [192,256) d~dO0
+//   [256,384) score buffer 0, [384,512) score buffer 1, each holding
+//   S = Q K^T | dP = dO V^T | F' = U_Q K^T + Q U_K^T | G = dO U_V^T (32 columns each).
+// Once a warpgroup has read a score buffer it overwrites consumed columns
+// with the bf16 A operands (P, P o dP, P o d~P0, dS, P o F) of the output
+// GEMMs, which read A straight from TMEM.
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace flashbob {
+namespace {
+using namespace tc;
+
+constexpr int BM = kTcRows;      // 128 query rows per CTA
+constexpr int BN = kTcStream;    // 32 key rows per streamed tile
+constexpr int DH = 64;           // head dim
+constexpr int NST = 6;           // stages of the K/V/U_K/U_V ring
+constexpr int NTHREADS = 320;
+constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
+constexpr uint32_t TILE_BYTES = BN * DH * 2;   // 4 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Smem1 {
+  alignas(1024) uint8_t q[BLOCK_BYTES];
+  alignas(1024) uint8_t dO[BLOCK_BYTES];
+  alignas(1024) uint8_t uq[BLOCK_BYTES];
+  alignas(1024) uint8_t kv[NST][4][TILE_BYTES];  // K, V, U_K, U_V
+  float part_a[2][BM];
+  float part_e[2][BM];
+  uint64_t bar_q;
+  uint64_t kv_full[NST];
+  uint64_t kv_empty[NST];
+  uint64_t sc_full[2];
+  uint64_t op_ready[2];
+  uint64_t out_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// TMEM columns of the bf16 operand slots inside a score buffer, for the two
+// K = 16 steps of the output GEMMs.  Chunk 0 (score columns 0..15) writes
+// only columns it has consumed (the first 16 of each 32-column score);
+// chunk 1 may also use columns 16..23 of S and dP, which it loaded itself.
+__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return c ? 72 : 0; }
+__device__ __forceinline__ constexpr uint32_t slot_PdP(int c) { return c ? 96 : 8; }
+__device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return c ? 104 : 32; }
+__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 16 : 40; }
+__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return c ? 48 : 64; }
+
+// Bounded wait on a barrier whose copies must land before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_pass1_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+                    const __grid_constant__ CUtensorMap mUQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mUK,
+                    const __grid_constant__ CUtensorMap mUV, const float* __restrict__ O,
+                    const float* __restrict__ L, const float* __restrict__ D,
+                    float* __restrict__ dQt, float* __restrict__ ddOt,
+                    float* __restrict__ alpha, float* __restrict__ E, int H, int N, float tau,
+                    unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem1& sm = *reinterpret_cast<Smem1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                        ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * H + blockIdx.y;
+  const int row0 = blockIdx.x * BM;
+  const int T = (N + BN - 1) / BN;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.bar_q, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.sc_full[b], 1);
+      mbar_init(&sm.op_ready[b], 128);
+    }
+    mbar_init(&sm.out_full, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      tma_prefetch_desc(&mUK);
+      tma_prefetch_desc(&mUV);
+      mbar_expect_tx(&sm.bar_q, 3 * BLOCK_BYTES);
+      tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
+      tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
+      tma_load_3d(sm.uq, &mUQ, &sm.bar_q, 0, row0, bh);
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NST;
+        if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+        mbar_expect_tx(&sm.kv_full[s], 4 * TILE_BYTES);
+        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.kv[s][1], &mV, &sm.kv_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.kv[s][2], &mUK, &sm.kv_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.kv[s][3], &mUV, &sm.kv_full[s], 0, t * BN, bh);
+        issued = t + 1;
+      }
+      // No copy may still be in flight when the CTA exits.
+      drain_wait(&sm.bar_q, 0);
+      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
+        drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(BM, BN, false);  // scores: N = 32, B K-major
+      constexpr uint32_t idO = idesc_bf16(BM, DH, true);   // outputs: N = 64, B MN-major
+      const uint32_t aq = smem_u32(sm.q), ado = smem_u32(sm.dO), auq = smem_u32(sm.uq);
+      auto issue_scores = [&](int t) {
+        const int s = t % NST;
+        const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        const uint32_t bk = smem_u32(sm.kv[s][0]), bv = smem_u32(sm.kv[s][1]);
+        const uint32_t buk = smem_u32(sm.kv[s][2]), buv = smem_u32(sm.kv[s][3]);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t o = 32 * kk;  // 16 bf16 along K inside the 128-byte swizzled row
+          const uint64_t dq = smem_desc_sw128(aq + o, 16, 1024);
+          const uint64_t ddo = smem_desc_sw128(ado + o, 16, 1024);
+          const uint64_t duq = smem_desc_sw128(auq + o, 16, 1024);
+          const uint64_t dk = smem_desc_sw128(bk + o, 16, 1024);
+          const uint64_t dv = smem_desc_sw128(bv + o, 16, 1024);
+          const uint64_t duk = smem_desc_sw128(buk + o, 16, 1024);
+          const uint64_t duv = smem_desc_sw128(buv + o, 16, 1024);
+          const uint32_t acc = kk > 0;
+          mma_ss(sc + 0, dq, dk, idS, acc);     // S  = Q K^T
+          mma_ss(sc + 32, ddo, dv, idS, acc);   // dP = dO V^T
+          mma_ss(sc + 64, duq, dk, idS, acc);   // F' = U_Q K^T
+          mma_ss(sc + 64, dq, duk, idS, 1);     //    + Q U_K^T
+          mma_ss(sc + 96, ddo, duv, idS, acc);  // G  = dO U_V^T
+        }
+        mma_commit(&sm.sc_full[t & 1]);
+      };
+      auto issue_outputs = [&](int t) {
+        const int s = t % NST;
+        const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        const uint32_t bk = smem_u32(sm.kv[s][0]), bv = smem_u32(sm.kv[s][1]);
+        const uint32_t buk = smem_u32(sm.kv[s][2]), buv = smem_u32(sm.kv[s][3]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t o = 16 * 128 * c;  // 16 key rows further down the tile
+          const uint64_t dk = smem_desc_sw128(bk + o, 16, 1024);
+          const uint64_t dv = smem_desc_sw128(bv + o, 16, 1024);
+          const uint64_t duk = smem_desc_sw128(buk + o, 16, 1024);
+          const uint64_t duv = smem_desc_sw128(buv + o, 16, 1024);
+          const uint32_t acc = (t > 0 || c > 0);
+          mma_ts(tbase + 0, sc + slot_P(c), dk, idO, acc);      // B     += P K
+          mma_ts(tbase + 64, sc + slot_PdP(c), dk, idO, acc);   // R     += (P o dP) K
+          mma_ts(tbase + 128, sc + slot_PdPt(c), dk, idO, acc); // Omega += (P o d~P0) K
+          mma_ts(tbase + 128, sc + slot_dS(c), duk, idO, 1);    //       +  dS U_K
+          mma_ts(tbase + 192, sc + slot_P(c), duv, idO, acc);   // d~dO0 += P U_V
+          mma_ts(tbase + 192, sc + slot_PF(c), dv, idO, 1);     //       +  (P o F) V
+        }
+        mma_commit(&sm.kv_empty[s]);
+      };
+      bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
+      tc_fence_after();
+      for (int t = 0; ok && t < 2 && t < T; ++t) {
+        ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+        tc_fence_after();
+        if (ok) issue_scores(t);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t);
+        if (t + 2 < T) {
+          ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + 2);
+        }
+      }
+      mma_commit(&sm.out_full);  // every MMA issued above has finished
+    }
+  } else {
+    // ---------------- elementwise warpgroups + epilogue ----------------
+    const int wg = (warp - 2) >> 2;      // 0 or 1
+    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane;      // row inside the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int gr = row0 + r;
+    const size_t rowvec = static_cast<size_t>(bh) * N + gr;
+    const float c1 = tau * kLog2e;
+    const float Lr2 = gr < N ? L[rowvec] * kLog2e : 0.f;
+    const float Dr = gr < N ? D[rowvec] : 0.f;
+    float a_acc = 0.f, e_acc = 0.f;
+    bool ok = true;
+    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
+
+    for (int u = 0;; ++u) {
+      const int t = 2 * u + wg;
+      if (t >= T) break;
+      // tcgen05.ld/st are warp-collective: take the decision warp-uniformly.
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+      const int col0 = t * BN;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t s[16], dp[16], f[16], g[16];
+        tmem_ld16(sc + 0 + 16 * c, s);
+        tmem_ld16(sc + 32 + 16 * c, dp);
+        tmem_ld16(sc + 64 + 16 * c, f);
+        tmem_ld16(sc + 96 + 16 * c, g);
+        tmem_wait_ld();
+        uint32_t oP[8], oPdP[8], oPdPt[8], odS[8], oPF[8];
+        const int jbase = col0 + 16 * c;
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float pv[2], pdp[2], pdpt[2], ds[2], pf[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = e + h;
+            float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
+            if (jbase + j >= N) p = 0.f;
+            const float dpv = u2f(dp[j]);
+            const float x = dpv - Dr;
+            const float ft = u2f(f[j]) * tau;
+            const float dpt0 = fmaf(ft, x, u2f(g[j]));
+            pv[h] = p;
+            pdp[h] = p * dpv;
+            pdpt[h] = p * dpt0;
+            ds[h] = p * x;
+            pf[h] = p * ft;
+            a_acc += pf[h];
+            e_acc += pdpt[h];
+          }
+          oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+          oPdP[e >> 1] = pack_bf16x2(pdp[0], pdp[1]);
+          oPdPt[e >> 1] = pack_bf16x2(pdpt[0], pdpt[1]);
+          odS[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+          oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
+        }
+        tmem_st8(sc + slot_P(c), oP);
+        tmem_st8(sc + slot_PdP(c), oPdP);
+        tmem_st8(sc + slot_PdPt(c), oPdPt);
+        tmem_st8(sc + slot_dS(c), odS);
+        tmem_st8(sc + slot_PF(c), oPF);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sm.op_ready[wg]);
+    }
+
+    // Epilogue: combine the two warpgroups' row sums, then the affine
+    // correction; warpgroup wg writes output columns [32 wg, 32 wg + 32).
+    sm.part_a[wg][r] = a_acc;
+    sm.part_e[wg][r] = e_acc;
+    named_bar_sync(1, 256);
+    const float al = sm.part_a[0][r] + sm.part_a[1][r];
+    const float Ei = (sm.part_e[0][r] + sm.part_e[1][r]) - al * Dr;
+    ok = __all_sync(0xffffffffu, mbar_wait(&sm.out_full, 0, abort_flag, err) && ok &&
+                                     !*abort_flag);
+    tc_fence_after();
+    const uint32_t acc_base = tbase + lane_off;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = 32 * wg + 16 * h;
+      uint32_t vb[16], vr[16], vw[16], vo[16];
+      tmem_ld16(acc_base + 0 + col, vb);
+      tmem_ld16(acc_base + 64 + col, vr);
+      tmem_ld16(acc_base + 128 + col, vw);
+      tmem_ld16(acc_base + 192 + col, vo);
+      tmem_wait_ld();
+      if (ok && gr < N) {
+        const size_t off = rowvec * DH + col;
+        const float4* o4 = reinterpret_cast<const float4*>(O + off);
+        float4* q4 = reinterpret_cast<float4*>(dQt + off);
+        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 ov = o4[k];
+          float4 qv, dv;
+          qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - Ei * u2f(vb[4 * k + 0]));
+          qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - Ei * u2f(vb[4 * k + 1]));
+          qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - Ei * u2f(vb[4 * k + 2]));
+          qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - Ei * u2f(vb[4 * k + 3]));
+          dv.x = u2f(vo[4 * k + 0]) - al * ov.x;
+          dv.y = u2f(vo[4 * k + 1]) - al * ov.y;
+          dv.z = u2f(vo[4 * k + 2]) - al * ov.z;
+          dv.w = u2f(vo[4 * k + 3]) - al * ov.w;
+          q4[k] = qv;
+          d4[k] = dv;
+        }
+      }
+    }
+    if (ok && wg == 0 && gr < N) {
+      alpha[rowvec] = al;
+      E[rowvec] = Ei;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+size_t tc_pass1_smem() { return sizeof(Smem1) + 1024; }
+
+cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
+                            const CUtensorMap* maps32) {
+  // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
+  const size_t smem = tc_pass1_smem();
+  cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
+  tc_pass1_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
+      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.N, a.tau, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace flashbob

@@ -1,0 +1,321 @@
+// Pass 2 of the exact attention backward-over-backward on sm_103a tensor
+// cores: bf16 inputs, head dim 64, fp32 accumulation in tensor memory.
+//
+// "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+// Attention" (paper notes), 关键设计 2: a block of key rows stays on chip
+// while query row tiles stream past together with the row scalars (alpha, E)
+// of pass 1; the column outputs are summed on chip and written once, with no
+// atomics.  With the transposed scores of the resident key rows j against a
+// streamed query row i:
+//     dS   = P o (dP - D)
+//     d~S  = P o (F o (dP - D) + G - alpha dP - E)       (d~P - E, times P)
+//     W    = P o (F - alpha)                              (gradient w.r.t. dP)
+//     d~K_j = tau sum_i (d~S_ij Q_i + dS_ij U_Q,i),   d~V_j = sum_i W_ij dO_i
+// (F = tau (U_Q K^T + Q U_K^T), G = dO U_V^T; the same chain rule as pass 1).
+//
+// CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
+//   warp 0      TMA producer: K, V, U_K, U_V blocks once, then Q, dO, U_Q
+//               tiles of 32 query rows through a 6-stage mbarrier ring;
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
+//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1 (even / odd tiles).
+// TMEM: [0,64) d~K accumulator, [64,128) d~V accumulator, [128,256) and
+// [256,384) score buffers S^T | dP^T | F'^T | G^T (32 columns each).
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace flashbob {
+namespace {
+using namespace tc;
+
+constexpr int BM = kTcRows;    // 128 key rows per CTA
+constexpr int BN = kTcStream;  // 32 query rows per streamed tile
+constexpr int DH = 64;
+constexpr int NST = 6;
+constexpr int NTHREADS = 320;
+constexpr uint32_t BLOCK_BYTES = BM * DH * 2;
+constexpr uint32_t TILE_BYTES = BN * DH * 2;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Smem2 {
+  alignas(1024) uint8_t k[BLOCK_BYTES];
+  alignas(1024) uint8_t v[BLOCK_BYTES];
+  alignas(1024) uint8_t uk[BLOCK_BYTES];
+  alignas(1024) uint8_t uv[BLOCK_BYTES];
+  alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, dO, U_Q
+  float4 scal[2][2][BN];  // per warpgroup, double-buffered: (L log2 e, D, alpha, E)
+  uint64_t bar_kv;
+  uint64_t st_full[NST];
+  uint64_t st_empty[NST];
+  uint64_t sc_full[2];
+  uint64_t op_ready[2];
+  uint64_t out_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// bf16 operand slots inside a score buffer (see pass 1 for the rule).
+__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 40 : 0; }
+__device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return c ? 64 : 8; }
+__device__ __forceinline__ constexpr uint32_t slot_W(int c) { return c ? 72 : 32; }
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                    const __grid_constant__ CUtensorMap mUK, const __grid_constant__ CUtensorMap mUV,
+                    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+                    const __grid_constant__ CUtensorMap mUQ, const float* __restrict__ L,
+                    const float* __restrict__ D, const float* __restrict__ alpha,
+                    const float* __restrict__ E, float* __restrict__ dKt,
+                    float* __restrict__ dVt, int H, int N, float tau, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem2& sm = *reinterpret_cast<Smem2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                        ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * H + blockIdx.y;
+  const int j0 = blockIdx.x * BM;
+  const int T = (N + BN - 1) / BN;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.bar_kv, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.st_full[s], 1);
+      mbar_init(&sm.st_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.sc_full[b], 1);
+      mbar_init(&sm.op_ready[b], 128);
+    }
+    mbar_init(&sm.out_full, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mdO);
+      tma_prefetch_desc(&mUQ);
+      mbar_expect_tx(&sm.bar_kv, 4 * BLOCK_BYTES);
+      tma_load_3d(sm.k, &mK, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.v, &mV, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.uk, &mUK, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.uv, &mUV, &sm.bar_kv, 0, j0, bh);
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NST;
+        if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+        mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
+        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.st[s][1], &mdO, &sm.st_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.st[s][2], &mUQ, &sm.st_full[s], 0, t * BN, bh);
+        issued = t + 1;
+      }
+      drain_wait(&sm.bar_kv, 0);
+      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
+        drain_wait(&sm.st_full[t % NST], (t / NST) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(BM, BN, false);
+      constexpr uint32_t idO = idesc_bf16(BM, DH, true);
+      const uint32_t ak = smem_u32(sm.k), av = smem_u32(sm.v);
+      const uint32_t auk = smem_u32(sm.uk), auv = smem_u32(sm.uv);
+      auto issue_scores = [&](int t) {
+        const int s = t % NST;
+        const uint32_t sc = tbase + 128 + 128 * (t & 1);
+        const uint32_t bq = smem_u32(sm.st[s][0]), bdo = smem_u32(sm.st[s][1]);
+        const uint32_t buq = smem_u32(sm.st[s][2]);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t o = 32 * kk;
+          const uint64_t dk = smem_desc_sw128(ak + o, 16, 1024);
+          const uint64_t dv = smem_desc_sw128(av + o, 16, 1024);
+          const uint64_t duk = smem_desc_sw128(auk + o, 16, 1024);
+          const uint64_t duv = smem_desc_sw128(auv + o, 16, 1024);
+          const uint64_t dq = smem_desc_sw128(bq + o, 16, 1024);
+          const uint64_t ddo = smem_desc_sw128(bdo + o, 16, 1024);
+          const uint64_t duq = smem_desc_sw128(buq + o, 16, 1024);
+          const uint32_t acc = kk > 0;
+          mma_ss(sc + 0, dk, dq, idS, acc);     // S^T  = K Q^T
+          mma_ss(sc + 32, dv, ddo, idS, acc);   // dP^T = V dO^T
+          mma_ss(sc + 64, dk, duq, idS, acc);   // F'^T = K U_Q^T
+          mma_ss(sc + 64, duk, dq, idS, 1);     //      + U_K Q^T
+          mma_ss(sc + 96, duv, ddo, idS, acc);  // G^T  = U_V dO^T
+        }
+        mma_commit(&sm.sc_full[t & 1]);
+      };
+      auto issue_outputs = [&](int t) {
+        const int s = t % NST;
+        const uint32_t sc = tbase + 128 + 128 * (t & 1);
+        const uint32_t bq = smem_u32(sm.st[s][0]), bdo = smem_u32(sm.st[s][1]);
+        const uint32_t buq = smem_u32(sm.st[s][2]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t o = 16 * 128 * c;
+          const uint64_t dq = smem_desc_sw128(bq + o, 16, 1024);
+          const uint64_t ddo = smem_desc_sw128(bdo + o, 16, 1024);
+          const uint64_t duq = smem_desc_sw128(buq + o, 16, 1024);
+          const uint32_t acc = (t > 0 || c > 0);
+          mma_ts(tbase + 0, sc + slot_dSt(c), dq, idO, acc);  // d~K += d~S^T Q
+          mma_ts(tbase + 0, sc + slot_dS(c), duq, idO, 1);    //     +  dS^T U_Q
+          mma_ts(tbase + 64, sc + slot_W(c), ddo, idO, acc);  // d~V += W^T dO
+        }
+        mma_commit(&sm.st_empty[s]);
+      };
+      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err);
+      tc_fence_after();
+      for (int t = 0; ok && t < 2 && t < T; ++t) {
+        ok = mbar_wait(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+        tc_fence_after();
+        if (ok) issue_scores(t);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t);
+        if (t + 2 < T) {
+          ok = mbar_wait(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + 2);
+        }
+      }
+      mma_commit(&sm.out_full);
+    }
+  } else {
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // key row inside the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int gj = j0 + r;
+    const size_t head = static_cast<size_t>(bh) * N;
+    const float c1 = tau * kLog2e;
+    const uint32_t sc = tbase + lane_off + 128 + 128 * wg;
+    const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
+    bool ok = true;
+
+    for (int u = 0;; ++u) {
+      const int t = 2 * u + wg;
+      if (t >= T) break;
+      float4* scal = sm.scal[wg][u & 1];
+      if (loader) {
+        const int i = t * BN + lane;
+        float4 v;
+        if (i < N) {
+          v = make_float4(L[head + i] * kLog2e, D[head + i], alpha[head + i], E[head + i]);
+        } else {
+          v = make_float4(INFINITY, 0.f, 0.f, 0.f);  // P = exp2(-inf) = 0 for rows past N
+        }
+        scal[lane] = v;
+      }
+      named_bar_sync(2 + wg, 128);
+      // Warp-uniform decision (tcgen05.ld/st are warp-collective); after a
+      // failed wait keep looping so every thread passes the same named
+      // barriers, but skip the work.
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
+      if (!ok) continue;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t s[16], dp[16], f[16], g[16];
+        tmem_ld16(sc + 0 + 16 * c, s);
+        tmem_ld16(sc + 32 + 16 * c, dp);
+        tmem_ld16(sc + 64 + 16 * c, f);
+        tmem_ld16(sc + 96 + 16 * c, g);
+        tmem_wait_ld();
+        uint32_t odS[8], odSt[8], oW[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float vds[2], vdst[2], vw[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = 16 * c + e + h;
+            const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row i
+            const float p = ex2_approx(fmaf(u2f(s[e + h]), c1, -rs.x));
+            const float dpv = u2f(dp[e + h]);
+            const float x = dpv - rs.y;
+            const float ft = u2f(f[e + h]) * tau;
+            vds[h] = p * x;
+            vdst[h] = p * (fmaf(ft, x, u2f(g[e + h])) - fmaf(rs.z, dpv, rs.w));
+            vw[h] = p * (ft - rs.z);
+          }
+          odS[e >> 1] = pack_bf16x2(vds[0], vds[1]);
+          odSt[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
+          oW[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+        }
+        tmem_st8(sc + slot_dS(c), odS);
+        tmem_st8(sc + slot_dSt(c), odSt);
+        tmem_st8(sc + slot_W(c), oW);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sm.op_ready[wg]);
+    }
+
+    ok = __all_sync(0xffffffffu, mbar_wait(&sm.out_full, 0, abort_flag, err) && ok &&
+                                     !*abort_flag);
+    tc_fence_after();
+    const uint32_t acc_base = tbase + lane_off;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = 32 * wg + 16 * h;
+      uint32_t vk[16], vv[16];
+      tmem_ld16(acc_base + 0 + col, vk);
+      tmem_ld16(acc_base + 64 + col, vv);
+      tmem_wait_ld();
+      if (ok && gj < N) {
+        const size_t off = (head + gj) * DH + col;
+        float4* k4 = reinterpret_cast<float4*>(dKt + off);
+        float4* v4 = reinterpret_cast<float4*>(dVt + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          k4[k] = make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]),
+                              tau * u2f(vk[4 * k + 2]), tau * u2f(vk[4 * k + 3]));
+          v4[k] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
+                              u2f(vv[4 * k + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+size_t tc_pass2_smem() { return sizeof(Smem2) + 1024; }
+
+cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
+                            const CUtensorMap* maps32) {
+  // maps128: K, V, U_K, U_V with 128-row boxes; maps32: Q, dO, U_Q with 32-row boxes.
+  const size_t smem = tc_pass2_smem();
+  cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
+  tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D,
+      a.alpha, a.E, a.dKt, a.dVt, a.H, a.N, a.tau, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace flashbob
