@@ -164,8 +164,10 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
       if (&o != &o2 && overlaps(o, o2)) return FLASHBOB_ERR_INVALID_ARG;
   }
   PrepArgs a{Q, K, V, dO, O, L, D, B, H, N, d, tau, in_dtype == FLASHBOB_BF16,
-             (cudaStream_t)stream};
-  return simt_prep(a) == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
+             (cudaStream_t)stream, nullptr};
+  if (error_word_ptr(&a.err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  const cudaError_t e = tc_prep_supported(a) ? tc_prep(a) : simt_prep(a);
+  return e == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
 }
 
 flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const float* O,

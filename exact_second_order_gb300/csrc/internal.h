@@ -13,6 +13,7 @@ struct PrepArgs {
   float tau;
   bool bf16;
   cudaStream_t stream;
+  unsigned int* err;  // device error word of the current device
 };
 
 struct BobArgs {
@@ -44,6 +45,8 @@ size_t simt_pass2_smem(int d);
 constexpr int kTcRows = 128;    // rows of the resident block (MMA M) in both passes
 constexpr int kTcStream = 32;   // rows of a streamed tile (MMA N of the score GEMMs)
 bool tc_supported(const BobArgs& a);
+bool tc_prep_supported(const PrepArgs& a);
+cudaError_t tc_prep(const PrepArgs& a);
 cudaError_t tc_bob(const BobArgs& a);
 size_t tc_pass1_smem();
 size_t tc_pass2_smem();

@@ -79,6 +79,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait on a barrier whose copies must land before the CTA exits
+// (used on the way out, also after an abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
 // --------------------------------------------------------------------------
 // TMA
 // --------------------------------------------------------------------------

@@ -65,14 +65,6 @@ __device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return c ? 104 
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 16 : 40; }
 __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return c ? 48 : 64; }
 
-// Bounded wait on a barrier whose copies must land before the CTA exits.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                     const __grid_constant__ CUtensorMap mUQ, const __grid_constant__ CUtensorMap mK,

@@ -58,13 +58,6 @@ __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 40 : 0
 __device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return c ? 64 : 8; }
 __device__ __forceinline__ constexpr uint32_t slot_W(int c) { return c ? 72 : 32; }
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                     const __grid_constant__ CUtensorMap mUK, const __grid_constant__ CUtensorMap mUV,

@@ -1,0 +1,298 @@
+// Row state of the attention backward-over-backward on sm_103a tensor cores:
+// O = P V, L = logsumexp(tau Q K^T) and D_i = dO_i . O_i for bf16 inputs,
+// head dim 64 ("FlashAttention 的反向传播设计" blog, sections 一 and 二; D as
+// in "FlashBoB" paper notes, 关键设计 1).
+//
+// Two phases inside one CTA of 128 query rows, both streaming the same key
+// tiles of 32 rows:
+//   phase A: S = Q K^T on the tensor cores; the elementwise warpgroups keep
+//            a running row max m and sum l of exp2(S tau log2 e - m), which
+//            gives L at the end of the phase;
+//   phase B: S = Q K^T again, P = exp(S - L) (already normalised, so the
+//            accumulator never needs rescaling) goes to TMEM as bf16 and
+//            O += P V runs with A read from TMEM.
+// The epilogue writes O and the row scalars; D comes from dO (bf16, read
+// from global memory) dotted with the fp32 O.
+//
+// 320 threads: warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps 2-5
+// and 6-9 elementwise warpgroups on alternate tiles.  TMEM: [0,64) O,
+// [64,96) and [96,128) score buffers.
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace flashbob {
+namespace {
+using namespace tc;
+
+constexpr int BM = kTcRows;
+constexpr int BN = kTcStream;
+constexpr int DH = 64;
+constexpr int NST = 6;
+constexpr int NTHREADS = 320;
+constexpr uint32_t BLOCK_BYTES = BM * DH * 2;
+constexpr uint32_t TILE_BYTES = BN * DH * 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Smem0 {
+  alignas(1024) uint8_t q[BLOCK_BYTES];
+  alignas(1024) uint8_t kv[NST][2][TILE_BYTES];  // K, V
+  float part_m[2][BM];
+  float part_l[2][BM];
+  float part_d[2][BM];
+  uint64_t bar_q;
+  uint64_t kv_full[NST];
+  uint64_t kv_empty[NST];
+  uint64_t sc_full[2];
+  uint64_t op_ready[2];
+  uint64_t out_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                   const __grid_constant__ CUtensorMap mV, const __nv_bfloat16* __restrict__ dO,
+                   float* __restrict__ O, float* __restrict__ L, float* __restrict__ D, int H,
+                   int N, float tau, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem0& sm = *reinterpret_cast<Smem0*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                        ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * H + blockIdx.y;
+  const int row0 = blockIdx.x * BM;
+  const int T = (N + BN - 1) / BN;
+  const int T2 = 2 * T;  // phase A tiles 0..T-1, phase B tiles T..2T-1
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.bar_q, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.sc_full[b], 1);
+      mbar_init(&sm.op_ready[b], 128);
+    }
+    mbar_init(&sm.out_full, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      mbar_expect_tx(&sm.bar_q, BLOCK_BYTES);
+      tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
+      int issued = 0;
+      for (int t = 0; t < T2; ++t) {
+        const int s = t % NST;
+        const bool phase_b = t >= T;
+        const int kt = phase_b ? t - T : t;
+        if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+        mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * TILE_BYTES);
+        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, kt * BN, bh);
+        if (phase_b) tma_load_3d(sm.kv[s][1], &mV, &sm.kv_full[s], 0, kt * BN, bh);
+        issued = t + 1;
+      }
+      drain_wait(&sm.bar_q, 0);
+      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
+        drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(BM, BN, false);
+      constexpr uint32_t idO = idesc_bf16(BM, DH, true);
+      const uint32_t aq = smem_u32(sm.q);
+      auto issue_scores = [&](int t) {
+        const int s = t % NST;
+        const uint32_t sc = tbase + 64 + 32 * (t & 1);
+        const uint32_t bk = smem_u32(sm.kv[s][0]);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t o = 32 * kk;
+          mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
+                 kk > 0);
+        }
+        mma_commit(&sm.sc_full[t & 1]);
+        if (t < T) mma_commit(&sm.kv_empty[s]);  // phase A reads the stage only here
+      };
+      auto issue_pv = [&](int t) {
+        const int s = t % NST;
+        const uint32_t sc = tbase + 64 + 32 * (t & 1);
+        const uint32_t bv = smem_u32(sm.kv[s][1]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, 16, 1024), idO,
+                 (t > T || c > 0));
+        }
+        mma_commit(&sm.kv_empty[s]);
+      };
+      bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
+      tc_fence_after();
+      for (int t = 0; ok && t < 2 && t < T2; ++t) {
+        ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+        tc_fence_after();
+        if (ok) issue_scores(t);
+      }
+      for (int t = 0; ok && t < T2; ++t) {
+        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        if (t >= T) issue_pv(t);
+        if (t + 2 < T2) {
+          ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + 2);
+        }
+      }
+      mma_commit(&sm.out_full);
+    }
+  } else {
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int gr = row0 + r;
+    const size_t rowvec = static_cast<size_t>(bh) * N + gr;
+    const float c1 = tau * kLog2e;
+    const uint32_t sc = tbase + lane_off + 64 + 32 * wg;
+    float m = -INFINITY, l = 0.f, L2 = 0.f;
+    bool ok = true, have_L = false;
+    // Both warpgroups have finished phase A: combine their (m, l) into L.
+    // Each warpgroup passes here exactly once (named barrier 1).
+    auto combine = [&]() {
+      sm.part_m[wg][r] = m;
+      sm.part_l[wg][r] = l;
+      named_bar_sync(1, 256);
+      const float m0 = sm.part_m[0][r], m1 = sm.part_m[1][r];
+      const float mm = fmaxf(m0, m1);  // finite: tile 0 always has a valid column
+      const float ll =
+          sm.part_l[0][r] * ex2_approx(m0 - mm) + sm.part_l[1][r] * ex2_approx(m1 - mm);
+      L2 = mm + __log2f(ll);
+      have_L = true;
+    };
+
+    for (int u = 0;; ++u) {
+      const int t = 2 * u + wg;
+      if (t >= T2) break;
+      const bool phase_b = t >= T;
+      if (phase_b && !have_L) combine();
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
+      if (ok) {
+        tc_fence_after();
+        const int col0 = (phase_b ? t - T : t) * BN;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t s[16];
+          tmem_ld16(sc + 16 * c, s);
+          tmem_wait_ld();
+          if (!phase_b) {
+            float mx = m;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (col0 + 16 * c + j < N) mx = fmaxf(mx, u2f(s[j]) * c1);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (col0 + 16 * c + j < N) acc += ex2_approx(u2f(s[j]) * c1 - mx);
+            l = (m == -INFINITY) ? acc : l * ex2_approx(m - mx) + acc;
+            m = mx;
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              float p0 = ex2_approx(fmaf(u2f(s[e]), c1, -L2));
+              float p1 = ex2_approx(fmaf(u2f(s[e + 1]), c1, -L2));
+              if (col0 + 16 * c + e >= N) p0 = 0.f;
+              if (col0 + 16 * c + e + 1 >= N) p1 = 0.f;
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st8(sc + 8 * c, pk);  // P chunk c over consumed score columns
+          }
+        }
+        if (phase_b) tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm.op_ready[wg]);
+      }
+    }
+    if (!have_L) combine();  // a warpgroup with no phase-B tile (T = 1)
+
+    ok = __all_sync(0xffffffffu, mbar_wait(&sm.out_full, 0, abort_flag, err) && ok &&
+                                     !*abort_flag);
+    tc_fence_after();
+    float dpart = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = 32 * wg + 16 * h;
+      uint32_t vo[16];
+      tmem_ld16(tbase + lane_off + col, vo);
+      tmem_wait_ld();
+      if (ok && gr < N) {
+        const size_t off = rowvec * DH + col;
+        float4* o4 = reinterpret_cast<float4*>(O + off);
+        const uint4* g4 = reinterpret_cast<const uint4*>(dO + off);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint4 raw = g4[k];  // 8 bf16 of dO
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w[q] << 16);
+            const float hi = __uint_as_float(w[q] & 0xFFFF0000u);
+            dpart = fmaf(lo, u2f(vo[8 * k + 2 * q]), dpart);
+            dpart = fmaf(hi, u2f(vo[8 * k + 2 * q + 1]), dpart);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          o4[k] = make_float4(u2f(vo[4 * k]), u2f(vo[4 * k + 1]), u2f(vo[4 * k + 2]),
+                              u2f(vo[4 * k + 3]));
+      }
+    }
+    sm.part_d[wg][r] = dpart;
+    named_bar_sync(1, 256);
+    if (ok && wg == 0 && gr < N) {
+      L[rowvec] = L2 * kLn2;
+      D[rowvec] = sm.part_d[0][r] + sm.part_d[1][r];
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
+  }
+}
+
+}  // namespace
+
+bool tc_prep_supported(const PrepArgs& a) { return a.bf16 && a.d == 64; }
+
+cudaError_t tc_prep(const PrepArgs& a) {
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv;
+  cudaError_t e = tc::make_map_bf16_d64(&mq, a.Q, BH, a.N, kTcRows);
+  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mk, a.K, BH, a.N, kTcStream);
+  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mv, a.V, BH, a.N, kTcStream);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(Smem0) + 1024;
+  e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
+  tc_prep_kernel<<<grid, NTHREADS, smem, a.stream>>>(mq, mk, mv, (const __nv_bfloat16*)a.dO, a.O,
+                                                     a.L, a.D, a.H, a.N, a.tau, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace flashbob

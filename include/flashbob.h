@@ -67,7 +67,8 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
  *   out: O [B,H,N,d] fp32 (O = P V), L [B,H,N] fp32 (natural-log logsumexp of
  *        tau Q K^T per row), D [B,H,N] fp32 (D_i = dO_i . O_i)
  *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
- *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535.  One launch.
+ *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535.  One launch: bf16 inputs
+ *   with d = 64 run a tcgen05 kernel, every other case fp32 CUDA cores.
  */
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
                               float* O, float* L, float* D, int B, int H, int N, int d,

@@ -43,13 +43,22 @@ import numpy as np
 # Forward, row state and first backward  ([FAB] sections 一 and 二)
 # --------------------------------------------------------------------------
 
-def forward(Q, K, V, tau):
+def causal_mask(N):
+    """True where key j is visible from query i (j <= i): the causal mask of
+    the pages' benchmarks ([FBN] 实验关键数据)."""
+    return np.tril(np.ones((N, N), dtype=bool))
+
+
+def forward(Q, K, V, tau, causal=False):
     """S = tau Q K^T, L = logsumexp_j S_ij, P = exp(S - L), O = P V.
 
     [FAB] section 一 (S, P = softmax(S), O = P V) with the softmax written
-    through the saved row statistic L as in [FAB] section 二.
+    through the saved row statistic L as in [FAB] section 二.  With
+    ``causal`` the scores of keys j > i are -inf, so P_ij = 0 there.
     """
     S = tau * (Q @ K.T)
+    if causal:
+        S = np.where(causal_mask(Q.shape[0]), S, -np.inf)
     m = S.max(axis=1, keepdims=True)
     L = m[:, 0] + np.log(np.exp(S - m).sum(axis=1))
     P = np.exp(S - L[:, None])
@@ -57,23 +66,23 @@ def forward(Q, K, V, tau):
     return S, P, O, L
 
 
-def prep(Q, K, V, dO, tau):
+def prep(Q, K, V, dO, tau, causal=False):
     """Row state the BoB consumes: O, L and D_i = dO_i . O_i.
 
     [FBN] 关键设计 1 defines D_i = dO_i^T O_i; [FAB] section 一 gives the same
     scalar as sum_j dP_ij P_ij.
     """
-    _, _, O, L = forward(Q, K, V, tau)
+    _, _, O, L = forward(Q, K, V, tau, causal)
     D = (dO * O).sum(axis=1)
     return O, L, D
 
 
-def first_backward(Q, K, V, dO, tau):
+def first_backward(Q, K, V, dO, tau, causal=False):
     """dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = tau dS K, dK = tau dS^T Q.
 
     [FAB] section 一.  The 1/sqrt(d) of the page is the general scale tau.
     """
-    _, P, O, _ = forward(Q, K, V, tau)
+    _, P, O, _ = forward(Q, K, V, tau, causal)
     dV = P.T @ dO
     dP = dO @ V.T
     D = (P * dP).sum(axis=1)
@@ -83,9 +92,9 @@ def first_backward(Q, K, V, dO, tau):
     return dQ, dK, dV
 
 
-def phi(Q, K, V, dO, UQ, UK, UV, tau):
+def phi(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     """Phi = <dQ, U_Q> + <dK, U_K> + <dV, U_V>  ([FBN] 方法详解/整体框架)."""
-    dQ, dK, dV = first_backward(Q, K, V, dO, tau)
+    dQ, dK, dV = first_backward(Q, K, V, dO, tau, causal)
     return float((dQ * UQ).sum() + (dK * UK).sum() + (dV * UV).sum())
 
 
@@ -93,7 +102,7 @@ def phi(Q, K, V, dO, UQ, UK, UV, tau):
 # Backward-over-backward, plain matrix form
 # --------------------------------------------------------------------------
 
-def bob(Q, K, V, dO, UQ, UK, UV, tau):
+def bob(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     """Total derivatives of Phi w.r.t. Q, K, V and dO, with O, L, D functions
     of the inputs ([FBN] 方法详解/整体框架).
 
@@ -109,9 +118,10 @@ def bob(Q, K, V, dO, UQ, UK, UV, tau):
 
     Returns d~Q = tau (d~S K + dS U_K), d~K = tau (d~S^T Q + dS^T U_Q),
     d~V = (P o (F - alpha))^T dO, d~dO = P U_V + (P o (F - alpha)) V,
-    and the row scalars alpha and E.
+    and the row scalars alpha and E.  With ``causal`` P vanishes above the
+    diagonal, and every term above carries a factor P.
     """
-    S, P, O, L = forward(Q, K, V, tau)
+    S, P, O, L = forward(Q, K, V, tau, causal)
     dP = dO @ V.T
     D = (dO * O).sum(axis=1)
     dS = P * (dP - D[:, None])
@@ -135,7 +145,7 @@ def bob(Q, K, V, dO, UQ, UK, UV, tau):
     }
 
 
-def bob_affine(Q, K, V, dO, UQ, UK, UV, tau):
+def bob_affine(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     """Row outputs through the alpha-free accumulators and the affine
     correction of [FBN] 关键设计 1:
 
@@ -144,7 +154,7 @@ def bob_affine(Q, K, V, dO, UQ, UK, UV, tau):
     with E0_i = sum_j P_ij d~P0_ij, B = P K, R = (P o dP) K,
     Omega = (P o d~P0) K + dS U_K and d~dO0 = P U_V + (P o F) V.
     """
-    S, P, O, L = forward(Q, K, V, tau)
+    S, P, O, L = forward(Q, K, V, tau, causal)
     dP = dO @ V.T
     D = (dO * O).sum(axis=1)
     dS = P * (dP - D[:, None])
@@ -171,16 +181,19 @@ def bob_affine(Q, K, V, dO, UQ, UK, UV, tau):
 # One row at a time: O(N d) per row, for long sequences
 # --------------------------------------------------------------------------
 
-def bob_rows(Q, K, V, dO, UQ, UK, UV, tau, rows):
+def bob_rows(Q, K, V, dO, UQ, UK, UV, tau, rows, causal=False):
     """Row-side outputs (L, D, alpha, E, d~Q, d~dO) for the listed rows only.
 
     The same definitions as ``bob`` restricted to row i: every quantity of
-    row i needs only row i of Q, dO, U_Q and all of K, V, U_K, U_V.
+    row i needs only row i of Q, dO, U_Q and all of K, V, U_K, U_V (only the
+    keys j <= i with ``causal``).
     """
     rows = np.asarray(rows, dtype=np.int64)
     out = {k: [] for k in ("L", "D", "alpha", "E", "dQt", "ddOt")}
     for i in rows:
         s = tau * (K @ Q[i])
+        if causal:
+            s = np.where(np.arange(K.shape[0]) <= i, s, -np.inf)
         m = s.max()
         Li = m + np.log(np.exp(s - m).sum())
         p = np.exp(s - Li)
@@ -207,7 +220,7 @@ def bob_rows(Q, K, V, dO, UQ, UK, UV, tau, rows):
 # Brute force: scalar loops only (tiny N, d), an independent restatement
 # --------------------------------------------------------------------------
 
-def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau):
+def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     """The same derivatives as ``bob`` written as explicit element sums.
 
     No matrix products, no vectorised reductions: every entry is a nested
@@ -222,17 +235,21 @@ def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau):
             s += a[k] * b[k]
         return s
 
+    def visible(i, j):
+        return j <= i or not causal
+
     S = [[tau * dot(Q[i], K[j]) for j in range(N)] for i in range(N)]
     P = [[0.0] * N for _ in range(N)]
     L = [0.0] * N
     for i in range(N):
-        m = max(S[i])
+        m = max(S[i][j] for j in range(N) if visible(i, j))
         z = 0.0
         for j in range(N):
-            z += np.exp(S[i][j] - m)
+            if visible(i, j):
+                z += np.exp(S[i][j] - m)
         L[i] = m + np.log(z)
         for j in range(N):
-            P[i][j] = np.exp(S[i][j] - L[i])
+            P[i][j] = np.exp(S[i][j] - L[i]) if visible(i, j) else 0.0
     O = [[sum(P[i][j] * V[j][k] for j in range(N)) for k in range(d)] for i in range(N)]
     D = [dot(dO[i], O[i]) for i in range(N)]
     dP = [[dot(dO[i], V[j]) for j in range(N)] for i in range(N)]
@@ -264,7 +281,7 @@ def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau):
 # Batched helpers over [B, H, N, d]
 # --------------------------------------------------------------------------
 
-def prep_batched(Q, K, V, dO, tau):
+def prep_batched(Q, K, V, dO, tau, causal=False):
     """``prep`` for every (b, h) of [B, H, N, d] arrays."""
     B, H, N, d = Q.shape
     O = np.empty((B, H, N, d))
@@ -272,11 +289,11 @@ def prep_batched(Q, K, V, dO, tau):
     D = np.empty((B, H, N))
     for b in range(B):
         for h in range(H):
-            O[b, h], L[b, h], D[b, h] = prep(Q[b, h], K[b, h], V[b, h], dO[b, h], tau)
+            O[b, h], L[b, h], D[b, h] = prep(Q[b, h], K[b, h], V[b, h], dO[b, h], tau, causal)
     return O, L, D
 
 
-def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None):
+def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None, causal=False):
     """``bob`` for every (b, h) (or the listed (b, h) pairs)."""
     B, H, N, d = Q.shape
     keys = ("dQt", "dKt", "dVt", "ddOt", "alpha", "E", "L", "D")
@@ -284,7 +301,7 @@ def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None):
                       np.nan) for k in keys}
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in pairs:
-        r = bob(Q[b, h], K[b, h], V[b, h], dO[b, h], UQ[b, h], UK[b, h], UV[b, h], tau)
+        r = bob(Q[b, h], K[b, h], V[b, h], dO[b, h], UQ[b, h], UK[b, h], UV[b, h], tau, causal)
         for k in keys:
             out[k][b, h] = r[k]
     return out

@@ -315,3 +315,65 @@ def test_golden_fixture():
     r = orc.bob(*args, 0.5)
     for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
         assert rel(r[key].ravel(), data[key]) < 1e-14, key
+
+
+# --------------------------------------------------------------------------
+# Causal mask (the setting of the pages' timing tables)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,d,seed", [(6, 3, 30), (11, 4, 31)])
+def test_causal_bob_matches_fd_of_phi(N, d, seed):
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(N, d, seed)
+    tau = 0.6
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau, causal=True)
+    args = [Q, K, V, dO]
+    for pos, key in enumerate(("dQt", "dKt", "dVt", "ddOt")):
+        def f(X, pos=pos):
+            a = list(args)
+            a[pos] = X
+            return orc.phi(*a, UQ, UK, UV, tau, causal=True)
+        assert rel(r[key], _fd_grad(f, args[pos])) < RTOL_FD, key
+
+
+def test_causal_matches_bruteforce_rows_affine_and_torch():
+    torch = pytest.importorskip("torch")
+    N, d = 13, 5
+    args = rand_inputs(N, d, 32)
+    tau = 0.45
+    r = orc.bob(*args, tau, causal=True)
+    b = orc.bob_bruteforce(*args, tau, causal=True)
+    a = orc.bob_affine(*args, tau, causal=True)
+    rows = [0, 1, 6, 12]
+    s = orc.bob_rows(*args, tau, rows, causal=True)
+    for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+        assert rel(r[key], b[key]) < 1e-12, key
+    for key in ("dQt", "ddOt", "alpha", "E"):
+        assert rel(a[key], r[key]) < 1e-12, key
+        assert rel(s[key], r[key][rows]) < 1e-12, key
+    tq, tk, tv, tdo = (torch.tensor(x, requires_grad=True) for x in args[:4])
+    uq, uk, uv = (torch.tensor(x) for x in args[4:])
+    mask = torch.ones(N, N, dtype=torch.bool).tril()
+    sc = (tau * tq @ tk.T).masked_fill(~mask, float("-inf"))
+    out = torch.softmax(sc, dim=-1) @ tv
+    dq, dk, dv = torch.autograd.grad(out, (tq, tk, tv), tdo, create_graph=True)
+    ph = (dq * uq).sum() + (dk * uk).sum() + (dv * uv).sum()
+    g = torch.autograd.grad(ph, (tq, tk, tv, tdo))
+    for key, t in zip(("dQt", "dKt", "dVt", "ddOt"), g):
+        assert rel(r[key], t.numpy()) < 1e-12, key
+
+
+def test_causal_first_row_and_invariants():
+    Q, K, V, dO, UQ, UK, UV = rand_inputs(9, 4, 33)
+    tau = 0.5
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau, causal=True)
+    # query 0 sees only key 0: the N = 1 closed form for its row
+    alpha0 = tau * (UQ[0] @ K[0] + Q[0] @ UK[0])
+    assert np.isclose(r["alpha"][0], alpha0, rtol=1e-13)
+    assert np.allclose(r["ddOt"][0], UV[0], rtol=1e-13, atol=1e-14)
+    assert np.abs(r["dQt"][0]).max() < 1e-14
+    # the last key is seen only by the last query: its softmax weight sits in
+    # one row, and the shift invariances still hold
+    ph = orc.phi(Q, K, V, dO, UQ, UK, UV, tau, causal=True)
+    assert abs((r["ddOt"] * dO).sum() - ph) < 1e-12 * (abs(ph) + 1)
+    assert np.abs(r["dKt"].sum(axis=0)).max() < 1e-12 * np.abs(r["dKt"]).max() * 9
+    assert np.abs(r["dVt"].sum(axis=0)).max() < 1e-12 * np.abs(r["dVt"]).max() * 9
