@@ -136,7 +136,7 @@ def oracle_rows_sample(w, x, seconds: float, rows_per_chunk: int = 16, seed: int
     done, t0 = 0, time.perf_counter()
     while True:
         rows = rng.choice(w.N, size=rows_per_chunk, replace=False)
-        orc.bob_rows(*args, w.tau, rows)
+        orc.bob_rows(*args, w.tau, rows, causal=w.causal)
         done += rows_per_chunk
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -144,8 +144,9 @@ def oracle_rows_sample(w, x, seconds: float, rows_per_chunk: int = 16, seed: int
 
 
 def row_flops(w) -> float:
-    """FLOPs credited per oracle row: the row-side GEMMs (pass 1 list)."""
-    return 2.0 * PASS1_GEMMS * w.N * w.d
+    """FLOPs credited per oracle row: the row-side GEMMs (pass 1 list); a
+    causal row sees half the keys on average."""
+    return (0.5 if w.causal else 1.0) * 2.0 * PASS1_GEMMS * w.N * w.d
 
 
 def run_reference(args, w, rank, world):
@@ -168,7 +169,7 @@ def run_reference(args, w, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
-                                        "d": w.d, "causal": False},
+                                        "d": w.d, "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{t_rows} seeded rows of head (0,0) through oracle.bob_rows "
                                    f"(fp64 numpy), {row_flops(w):.3e} flops credited per row"},
@@ -201,7 +202,7 @@ def main():
 
     x = make_inputs(w)
     dev = {k: v.cuda() for k, v in x.items()}
-    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau)
+    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
     out = fb.alloc_bob_outputs(dev["Q"])
     stream = torch.cuda.current_stream()
 
@@ -210,12 +211,12 @@ def main():
             ev[0].record(stream)
         fb.flashbob_bob_pass1(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"],
                               dev["UK"], dev["UV"], w.tau, out["dQt"], out["ddOt"],
-                              out["alpha"], out["E"], stream)
+                              out["alpha"], out["E"], causal=w.causal, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         fb.flashbob_bob_pass2(dev["Q"], dev["K"], dev["V"], dev["dO"], L, D, out["alpha"],
                               out["E"], dev["UQ"], dev["UK"], dev["UV"], w.tau, out["dKt"],
-                              out["dVt"], stream)
+                              out["dVt"], causal=w.causal, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -248,7 +249,8 @@ def main():
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     heads = w.B * w.H
-    unit_flops = 2.0 * w.N * w.N * w.d * heads
+    # one N x N x d GEMM per (batch, head); half of it under the causal mask
+    unit_flops = (0.5 if w.causal else 1.0) * 2.0 * w.N * w.N * w.d * heads
     flops = (PASS1_GEMMS + PASS2_GEMMS) * unit_flops
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
@@ -272,7 +274,8 @@ def main():
                 dev_state[k].copy_(host_state[k], non_blocking=True)
             fb.flashbob_bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"],
                             dev["UK"], dev["UV"], w.tau, out["dQt"], out["dKt"], out["dVt"],
-                            out["ddOt"], out["alpha"], out["E"], stream)
+                            out["ddOt"], out["alpha"], out["E"], causal=w.causal,
+                            stream=stream)
             for k in host_out:
                 host_out[k].copy_(out[k], non_blocking=True)
 
@@ -308,7 +311,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": False,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "tau": w.tau, "flops_per_step_per_gpu": flops,
                    "flop_convention": "38*N^2*d*B*H (19 GEMMs of 2*N^2*d)",
                    "l2": f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "

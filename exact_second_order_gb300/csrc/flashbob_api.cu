@@ -62,9 +62,11 @@ namespace {
 
 // Checks shared by flashbob_bob and its two passes: which buffers a pass
 // reads and writes follows from a.passes.
-flashbob_status run_bob(BobArgs& a, flashbob_dtype in_dtype) {
+flashbob_status run_bob(BobArgs& a, int causal, flashbob_dtype in_dtype) {
   flashbob_status st = check_dtype(in_dtype);
   if (st != FLASHBOB_OK) return st;
+  if (causal != 0 && causal != 1) return FLASHBOB_ERR_INVALID_ARG;
+  a.causal = causal == 1;
   a.bf16 = in_dtype == FLASHBOB_BF16;
   const bool p1 = a.passes & kPass1, p2 = a.passes & kPass2;
   const size_t rows = (size_t)(a.B > 0 ? a.B : 0) * (a.H > 0 ? a.H : 0) * (a.N > 0 ? a.N : 0);
@@ -139,9 +141,10 @@ const char* flashbob_status_string(flashbob_status s) {
 
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
                               float* O, float* L, float* D, int B, int H, int N, int d,
-                              float tau, flashbob_dtype in_dtype, void* stream) {
+                              float tau, int causal, flashbob_dtype in_dtype, void* stream) {
   flashbob_status st = check_dtype(in_dtype);
   if (st != FLASHBOB_OK) return st;
+  if (causal != 0 && causal != 1) return FLASHBOB_ERR_INVALID_ARG;
   if (!Q || !K || !V || !dO || !O || !L || !D) return FLASHBOB_ERR_INVALID_ARG;
   st = check_sizes(B, H, N, d, tau);
   if (st != FLASHBOB_OK) return st;
@@ -163,8 +166,8 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
     for (const Range& o2 : outs)
       if (&o != &o2 && overlaps(o, o2)) return FLASHBOB_ERR_INVALID_ARG;
   }
-  PrepArgs a{Q, K, V, dO, O, L, D, B, H, N, d, tau, in_dtype == FLASHBOB_BF16,
-             (cudaStream_t)stream, nullptr};
+  PrepArgs a{Q,         K,    V,  dO, O, L, D, B, H, N, d, tau, causal == 1,
+             in_dtype == FLASHBOB_BF16, (cudaStream_t)stream, nullptr};
   if (error_word_ptr(&a.err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
   const cudaError_t e = tc_prep_supported(a) ? tc_prep(a) : simt_prep(a);
   return e == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
@@ -174,32 +177,34 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
                              const void* dO, const float* L, const float* D, const void* UQ,
                              const void* UK, const void* UV, float tau, float* dQt, float* dKt,
                              float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
-                             int N, int d, flashbob_dtype in_dtype, void* stream) {
-  BobArgs a{Q,     K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, dKt, dVt, ddOt, alpha, E, B, H, N, d,
-            false, (cudaStream_t)stream, nullptr, kPass1 | kPass2};
-  return run_bob(a, in_dtype);
+                             int N, int d, int causal, flashbob_dtype in_dtype, void* stream) {
+  BobArgs a{Q, K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, dKt, dVt, ddOt, alpha, E, B, H, N, d,
+            false, false, (cudaStream_t)stream, nullptr, kPass1 | kPass2};
+  return run_bob(a, causal, in_dtype);
 }
 
 flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, const float* O,
                                    const void* dO, const float* L, const float* D,
                                    const void* UQ, const void* UK, const void* UV, float tau,
                                    float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
-                                   int N, int d, flashbob_dtype in_dtype, void* stream) {
-  BobArgs a{Q,     K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, nullptr, nullptr, ddOt, alpha, E, B,
-            H,     N, d, false, (cudaStream_t)stream, nullptr, kPass1};
-  return run_bob(a, in_dtype);
+                                   int N, int d, int causal, flashbob_dtype in_dtype,
+                                   void* stream) {
+  BobArgs a{Q, K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, nullptr, nullptr, ddOt, alpha, E, B, H,
+            N, d, false, false, (cudaStream_t)stream, nullptr, kPass1};
+  return run_bob(a, causal, in_dtype);
 }
 
 flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, const void* dO,
                                    const float* L, const float* D, const float* alpha,
                                    const float* E, const void* UQ, const void* UK,
                                    const void* UV, float tau, float* dKt, float* dVt, int B,
-                                   int H, int N, int d, flashbob_dtype in_dtype, void* stream) {
+                                   int H, int N, int d, int causal, flashbob_dtype in_dtype,
+                                   void* stream) {
   // alpha and E are inputs of pass 2; the BobArgs fields keep their names.
-  BobArgs a{Q,       K,       V,     nullptr, dO, L, D, UQ, UK, UV, tau, nullptr, dKt, dVt,
-            nullptr, (float*)alpha, (float*)E, B, H, N, d, false, (cudaStream_t)stream, nullptr,
+  BobArgs a{Q,     K,     V, nullptr, dO, L, D, UQ, UK, UV, tau, nullptr, dKt, dVt, nullptr,
+            (float*)alpha, (float*)E, B, H, N, d, false, false, (cudaStream_t)stream, nullptr,
             kPass2};
-  return run_bob(a, in_dtype);
+  return run_bob(a, causal, in_dtype);
 }
 
 flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1, int* Bc1,

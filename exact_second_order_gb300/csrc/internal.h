@@ -11,6 +11,7 @@ struct PrepArgs {
   float *O, *L, *D;
   int B, H, N, d;
   float tau;
+  bool causal;
   bool bf16;
   cudaStream_t stream;
   unsigned int* err;  // device error word of the current device
@@ -25,6 +26,7 @@ struct BobArgs {
   float tau;
   float *dQt, *dKt, *dVt, *ddOt, *alpha, *E;
   int B, H, N, d;
+  bool causal;
   bool bf16;
   cudaStream_t stream;
   unsigned int* err;  // device error word of the current device

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
                                                   const T* __restrict__ V, const T* __restrict__ dO,
                                                   float* __restrict__ O, float* __restrict__ L,
                                                   float* __restrict__ D, int H, int N, int d,
-                                                  float tau) {
+                                                  float tau, int causal) {
   extern __shared__ float sm[];
   float* Qs = sm;
   float* Ks = Qs + SB * (DP + 1);
@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
 #pragma unroll
   for (int j = 0; j < DP / 8; ++j) acc[j] = 0.f;
 
-  for (int col0 = 0; col0 < N; col0 += SB) {
+  const int gr = row0 + r;
+  const int col_end = causal ? min(N, row0 + SB) : N;  // keys j <= i under the causal mask
+  for (int col0 = 0; col0 < col_end; col0 += SB) {
     __syncthreads();
     load_tile<T, DP>(Ks, K + base, col0, N, d);
     load_tile<T, DP>(Vs, V + base, col0, N, d);
@@ -98,11 +100,12 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
     float mx = -INFINITY;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      s[u] = (col0 + q + 8 * u < N) ? s[u] * c : -INFINITY;
+      const int j = col0 + q + 8 * u;
+      s[u] = (j < N && !(causal && j > gr)) ? s[u] * c : -INFINITY;
       mx = fmaxf(mx, s[u]);
     }
     mx = row8_max(mx);
-    const float m_new = fmaxf(m, mx);  // finite: column col0 is always valid
+    const float m_new = fmaxf(m, mx);  // finite: column col0 <= row0 is always visible
     const float scale = exp2f(m - m_new);
     float ps = 0.f;
 #pragma unroll
@@ -125,7 +128,6 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
     __syncwarp();
   }
 
-  const int gr = row0 + r;
   const float inv_l = 1.f / l;
   float dsum = 0.f;
 #pragma unroll
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
     const float* __restrict__ O, const T* __restrict__ dO, const float* __restrict__ L,
     const float* __restrict__ D, const T* __restrict__ UQ, const T* __restrict__ UK,
     const T* __restrict__ UV, float tau, float* __restrict__ dQt, float* __restrict__ ddOt,
-    float* __restrict__ alpha, float* __restrict__ E, int H, int N, int d) {
+    float* __restrict__ alpha, float* __restrict__ E, int H, int N, int d, int causal) {
   extern __shared__ float sm[];
   constexpr int TP = SB * (DP + 1);
   constexpr int OP = SB * (SB + 1);
@@ -192,8 +194,9 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
 #pragma unroll
   for (int j = 0; j < DP / 8; ++j) accB[j] = accR[j] = accW[j] = accO[j] = 0.f;
   float a_part = 0.f, e_part = 0.f;
+  const int col_end = causal ? min(N, row0 + SB) : N;
 
-  for (int col0 = 0; col0 < N; col0 += SB) {
+  for (int col0 = 0; col0 < col_end; col0 += SB) {
     __syncthreads();
     load_tile<T, DP>(Ks, K + base, col0, N, d);
     load_tile<T, DP>(Vs, V + base, col0, N, d);
@@ -219,7 +222,8 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int cc = q + 8 * u;
-      const float p = (col0 + cc < N) ? exp2f(s[u] * c - Lr2) : 0.f;
+      const int j = col0 + cc;
+      const float p = (j < N && !(causal && j > gr)) ? exp2f(s[u] * c - Lr2) : 0.f;
       const float x = dp[u] - Dr;
       const float ft = f[u] * tau;
       const float dpt0 = fmaf(ft, x, g[u]);
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
     const T* __restrict__ dO, const float* __restrict__ L, const float* __restrict__ D,
     const float* __restrict__ alpha, const float* __restrict__ E, const T* __restrict__ UQ,
     const T* __restrict__ UK, const T* __restrict__ UV, float tau, float* __restrict__ dKt,
-    float* __restrict__ dVt, int H, int N, int d) {
+    float* __restrict__ dVt, int H, int N, int d, int causal) {
   extern __shared__ float sm[];
   constexpr int TP = SB * (DP + 1);
   constexpr int OP = SB * (SB + 1);
@@ -319,7 +323,9 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
 #pragma unroll
   for (int j = 0; j < DP / 8; ++j) accK[j] = accV[j] = 0.f;
 
-  for (int row0 = 0; row0 < N; row0 += SB) {
+  const int gj = j0 + jr;
+  // Under the causal mask key j is seen by queries i >= j only.
+  for (int row0 = causal ? j0 : 0; row0 < N; row0 += SB) {
     __syncthreads();
     load_tile<T, DP>(Qs, Q + base, row0, N, d);
     load_tile<T, DP>(dOs, dO + base, row0, N, d);
@@ -352,7 +358,8 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int ii = q + 8 * u;
-      const float p = (row0 + ii < N) ? exp2f(s[u] * c - Ls2[ii]) : 0.f;
+      const int i = row0 + ii;
+      const float p = (i < N && !(causal && i < gj)) ? exp2f(s[u] * c - Ls2[ii]) : 0.f;
       const float x = dp[u] - Ds[ii];
       const float ft = f[u] * tau;
       const float a = As[ii];
@@ -374,7 +381,6 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
     }
   }
 
-  const int gj = j0 + jr;
   if (gj < N) {
 #pragma unroll
     for (int j = 0; j < DP / 8; ++j) {
@@ -403,7 +409,7 @@ cudaError_t run_prep(const PrepArgs& a) {
   dim3 grid((a.N + SB - 1) / SB, a.H, a.B);
   prep_kernel<T, DP><<<grid, NT, smem, a.stream>>>(
       (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.O, a.L, a.D, a.H, a.N, a.d,
-      a.tau);
+      a.tau, a.causal ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -421,14 +427,15 @@ cudaError_t run_bob(const BobArgs& a) {
     pass1_kernel<T, DP><<<grid, NT, s1, a.stream>>>(
         (const T*)a.Q, (const T*)a.K, (const T*)a.V, a.O, (const T*)a.dO, a.L, a.D,
         (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dQt, a.ddOt, a.alpha, a.E, a.H,
-        a.N, a.d);
+        a.N, a.d, a.causal ? 1 : 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (a.passes & kPass2) {
     pass2_kernel<T, DP><<<grid, NT, s2, a.stream>>>(
         (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.L, a.D, a.alpha, a.E,
-        (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dKt, a.dVt, a.H, a.N, a.d);
+        (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dKt, a.dVt, a.H, a.N, a.d,
+        a.causal ? 1 : 0);
     e = cudaGetLastError();
   }
   return e;

@@ -65,6 +65,54 @@ __device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return c ? 104 
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 16 : 40; }
 __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return c ? 48 : 64; }
 
+// One 16-column chunk of a score buffer, one row per thread: read S, dP, F',
+// G from TMEM, form P = exp(S - L) and the five bf16 A operands of the
+// output GEMMs, add to the row sums alpha and E0, and write the operands back
+// over consumed columns.
+template <bool MASKED, int C>
+__device__ __forceinline__ void p1_chunk(uint32_t sc, int col0, int jmax, float c1, float Lr2,
+                                         float Dr, float tau, float& a_acc, float& e_acc) {
+  uint32_t s[16], dp[16], f[16], g[16];
+  tmem_ld16(sc + 0 + 16 * C, s);
+  tmem_ld16(sc + 32 + 16 * C, dp);
+  tmem_ld16(sc + 64 + 16 * C, f);
+  tmem_ld16(sc + 96 + 16 * C, g);
+  tmem_wait_ld();
+  uint32_t oP[8], oPdP[8], oPdPt[8], odS[8], oPF[8];
+  const int jbase = col0 + 16 * C;
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float pv[2], pdp[2], pdpt[2], ds[2], pf[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = e + h;
+      float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
+      if (MASKED && jbase + j > jmax) p = 0.f;
+      const float dpv = u2f(dp[j]);
+      const float x = dpv - Dr;
+      const float ft = u2f(f[j]) * tau;
+      const float dpt0 = fmaf(ft, x, u2f(g[j]));
+      pv[h] = p;
+      pdp[h] = p * dpv;
+      pdpt[h] = p * dpt0;
+      ds[h] = p * x;
+      pf[h] = p * ft;
+      a_acc += pf[h];
+      e_acc += pdpt[h];
+    }
+    oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+    oPdP[e >> 1] = pack_bf16x2(pdp[0], pdp[1]);
+    oPdPt[e >> 1] = pack_bf16x2(pdpt[0], pdpt[1]);
+    odS[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+    oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
+  }
+  tmem_st8(sc + slot_P(C), oP);
+  tmem_st8(sc + slot_PdP(C), oPdP);
+  tmem_st8(sc + slot_PdPt(C), oPdPt);
+  tmem_st8(sc + slot_dS(C), odS);
+  tmem_st8(sc + slot_PF(C), oPF);
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                     const __grid_constant__ CUtensorMap mUQ, const __grid_constant__ CUtensorMap mK,
@@ -73,14 +121,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float* __restrict__ L, const float* __restrict__ D,
                     float* __restrict__ dQt, float* __restrict__ ddOt,
                     float* __restrict__ alpha, float* __restrict__ E, int H, int N, float tau,
-                    unsigned int* err) {
+                    int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem1& sm = *reinterpret_cast<Smem1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
-  const int row0 = blockIdx.x * BM;
-  const int T = (N + BN - 1) / BN;
+  // Causal: the last row blocks see the most keys, so they start first.
+  const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
+  const int col_end = causal ? min(N, row0 + BM) : N;  // keys j <= i under the causal mask
+  const int T = (col_end + BN - 1) / BN;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -227,47 +277,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const int col0 = t * BN;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t s[16], dp[16], f[16], g[16];
-        tmem_ld16(sc + 0 + 16 * c, s);
-        tmem_ld16(sc + 32 + 16 * c, dp);
-        tmem_ld16(sc + 64 + 16 * c, f);
-        tmem_ld16(sc + 96 + 16 * c, g);
-        tmem_wait_ld();
-        uint32_t oP[8], oPdP[8], oPdPt[8], odS[8], oPF[8];
-        const int jbase = col0 + 16 * c;
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float pv[2], pdp[2], pdpt[2], ds[2], pf[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = e + h;
-            float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
-            if (jbase + j >= N) p = 0.f;
-            const float dpv = u2f(dp[j]);
-            const float x = dpv - Dr;
-            const float ft = u2f(f[j]) * tau;
-            const float dpt0 = fmaf(ft, x, u2f(g[j]));
-            pv[h] = p;
-            pdp[h] = p * dpv;
-            pdpt[h] = p * dpt0;
-            ds[h] = p * x;
-            pf[h] = p * ft;
-            a_acc += pf[h];
-            e_acc += pdpt[h];
-          }
-          oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          oPdP[e >> 1] = pack_bf16x2(pdp[0], pdp[1]);
-          oPdPt[e >> 1] = pack_bf16x2(pdpt[0], pdpt[1]);
-          odS[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-          oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
-        }
-        tmem_st8(sc + slot_P(c), oP);
-        tmem_st8(sc + slot_PdP(c), oPdP);
-        tmem_st8(sc + slot_PdPt(c), oPdPt);
-        tmem_st8(sc + slot_dS(c), odS);
-        tmem_st8(sc + slot_PF(c), oPF);
+      // Columns past N, or (causal) past this row, get P = 0.  Only tiles
+      // that reach past N or past the block's first row take the masked path.
+      const bool masked = (col0 + BN > N) || (causal && col0 + BN - 1 > row0);
+      const int jmax = causal ? min(N - 1, gr) : N - 1;
+      if (masked) {
+        p1_chunk<true, 0>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_chunk<true, 1>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+      } else {
+        p1_chunk<false, 0>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_chunk<false, 1>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -345,7 +364,7 @@ cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_pass1_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.N, a.tau, a.err);
+      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,44 @@ __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 40 : 0
 __device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return c ? 64 : 8; }
 __device__ __forceinline__ constexpr uint32_t slot_W(int c) { return c ? 72 : 32; }
 
+// One 16-column chunk of a transposed score buffer, one key row per thread:
+// with the row scalars of the streamed query rows form dS, d~S and W and
+// write them as bf16 A operands over consumed columns.
+template <bool MASKED, int C>
+__device__ __forceinline__ void p2_chunk(uint32_t sc, const float4* scal, int ibase, int gj,
+                                         float c1, float tau) {
+  uint32_t s[16], dp[16], f[16], g[16];
+  tmem_ld16(sc + 0 + 16 * C, s);
+  tmem_ld16(sc + 32 + 16 * C, dp);
+  tmem_ld16(sc + 64 + 16 * C, f);
+  tmem_ld16(sc + 96 + 16 * C, g);
+  tmem_wait_ld();
+  uint32_t odS[8], odSt[8], oW[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float vds[2], vdst[2], vw[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 16 * C + e + h;
+      const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row i
+      float p = ex2_approx(fmaf(u2f(s[e + h]), c1, -rs.x));
+      if (MASKED && ibase + i < gj) p = 0.f;
+      const float dpv = u2f(dp[e + h]);
+      const float x = dpv - rs.y;
+      const float ft = u2f(f[e + h]) * tau;
+      vds[h] = p * x;
+      vdst[h] = p * (fmaf(ft, x, u2f(g[e + h])) - fmaf(rs.z, dpv, rs.w));
+      vw[h] = p * (ft - rs.z);
+    }
+    odS[e >> 1] = pack_bf16x2(vds[0], vds[1]);
+    odSt[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
+    oW[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+  }
+  tmem_st8(sc + slot_dS(C), odS);
+  tmem_st8(sc + slot_dSt(C), odSt);
+  tmem_st8(sc + slot_W(C), oW);
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                     const __grid_constant__ CUtensorMap mUK, const __grid_constant__ CUtensorMap mUV,
@@ -65,14 +103,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap mUQ, const float* __restrict__ L,
                     const float* __restrict__ D, const float* __restrict__ alpha,
                     const float* __restrict__ E, float* __restrict__ dKt,
-                    float* __restrict__ dVt, int H, int N, float tau, unsigned int* err) {
+                    float* __restrict__ dVt, int H, int N, float tau, int causal,
+                    unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem2& sm = *reinterpret_cast<Smem2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
   const int j0 = blockIdx.x * BM;
-  const int T = (N + BN - 1) / BN;
+  // Query tiles t0 .. T-1 stream past; under the causal mask key j is seen
+  // only by queries i >= j, so the tiles before the block are skipped.
+  // Ring slots and barrier phases count tiles from t0.
+  const int t0 = causal ? j0 / BN : 0;
+  const int T = (N + BN - 1) / BN - t0;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -110,9 +153,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int s = t % NST;
         if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
-        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.st[s][1], &mdO, &sm.st_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.st[s][2], &mUQ, &sm.st_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
+        tma_load_3d(sm.st[s][1], &mdO, &sm.st_full[s], 0, (t + t0) * BN, bh);
+        tma_load_3d(sm.st[s][2], &mUQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
         issued = t + 1;
       }
       drain_wait(&sm.bar_kv, 0);
@@ -205,7 +248,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (t >= T) break;
       float4* scal = sm.scal[wg][u & 1];
       if (loader) {
-        const int i = t * BN + lane;
+        const int i = (t + t0) * BN + lane;
         float4 v;
         if (i < N) {
           v = make_float4(L[head + i] * kLog2e, D[head + i], alpha[head + i], E[head + i]);
@@ -221,37 +264,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
       if (!ok) continue;
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t s[16], dp[16], f[16], g[16];
-        tmem_ld16(sc + 0 + 16 * c, s);
-        tmem_ld16(sc + 32 + 16 * c, dp);
-        tmem_ld16(sc + 64 + 16 * c, f);
-        tmem_ld16(sc + 96 + 16 * c, g);
-        tmem_wait_ld();
-        uint32_t odS[8], odSt[8], oW[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float vds[2], vdst[2], vw[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int i = 16 * c + e + h;
-            const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row i
-            const float p = ex2_approx(fmaf(u2f(s[e + h]), c1, -rs.x));
-            const float dpv = u2f(dp[e + h]);
-            const float x = dpv - rs.y;
-            const float ft = u2f(f[e + h]) * tau;
-            vds[h] = p * x;
-            vdst[h] = p * (fmaf(ft, x, u2f(g[e + h])) - fmaf(rs.z, dpv, rs.w));
-            vw[h] = p * (ft - rs.z);
-          }
-          odS[e >> 1] = pack_bf16x2(vds[0], vds[1]);
-          odSt[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
-          oW[e >> 1] = pack_bf16x2(vw[0], vw[1]);
-        }
-        tmem_st8(sc + slot_dS(c), odS);
-        tmem_st8(sc + slot_dSt(c), odSt);
-        tmem_st8(sc + slot_W(c), oW);
+      // Causal: queries i < j (this thread's key row) get P = 0; only the
+      // tiles that overlap the key block take the masked path.  Rows past N
+      // carry L = +inf, so their P is 0 on both paths.
+      const int ibase = (t + t0) * BN;
+      if (causal && ibase < j0 + BM) {
+        p2_chunk<true, 0>(sc, scal, ibase, gj, c1, tau);
+        p2_chunk<true, 1>(sc, scal, ibase, gj, c1, tau);
+      } else {
+        p2_chunk<false, 0>(sc, scal, ibase, gj, c1, tau);
+        p2_chunk<false, 1>(sc, scal, ibase, gj, c1, tau);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -307,7 +329,7 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D,
-      a.alpha, a.E, a.dKt, a.dVt, a.H, a.N, a.tau, a.err);
+      a.alpha, a.E, a.dKt, a.dVt, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

@@ -54,14 +54,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __nv_bfloat16* __restrict__ dO,
                    float* __restrict__ O, float* __restrict__ L, float* __restrict__ D, int H,
-                   int N, float tau, unsigned int* err) {
+                   int N, float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem0& sm = *reinterpret_cast<Smem0*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
-  const int row0 = blockIdx.x * BM;
-  const int T = (N + BN - 1) / BN;
+  const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
+  const int col_end = causal ? min(N, row0 + BM) : N;  // keys j <= i under the causal mask
+  const int T = (col_end + BN - 1) / BN;
   const int T2 = 2 * T;  // phase A tiles 0..T-1, phase B tiles T..2T-1
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok) {
         tc_fence_after();
         const int col0 = (phase_b ? t - T : t) * BN;
+        const int jmax = causal ? min(N - 1, gr) : N - 1;  // visible keys j <= jmax
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t s[16];
@@ -199,12 +201,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float mx = m;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (col0 + 16 * c + j < N) mx = fmaxf(mx, u2f(s[j]) * c1);
+              if (col0 + 16 * c + j <= jmax) mx = fmaxf(mx, u2f(s[j]) * c1);
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (col0 + 16 * c + j < N) acc += ex2_approx(u2f(s[j]) * c1 - mx);
-            l = (m == -INFINITY) ? acc : l * ex2_approx(m - mx) + acc;
+              if (col0 + 16 * c + j <= jmax) acc += ex2_approx(u2f(s[j]) * c1 - mx);
+            // A chunk may hold no visible column (mx stays m, acc = 0).
+            l = (mx == -INFINITY) ? l : (m == -INFINITY ? acc : l * ex2_approx(m - mx) + acc);
             m = mx;
           } else {
             uint32_t pk[8];
@@ -212,8 +215,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int e = 0; e < 16; e += 2) {
               float p0 = ex2_approx(fmaf(u2f(s[e]), c1, -L2));
               float p1 = ex2_approx(fmaf(u2f(s[e + 1]), c1, -L2));
-              if (col0 + 16 * c + e >= N) p0 = 0.f;
-              if (col0 + 16 * c + e + 1 >= N) p1 = 0.f;
+              if (col0 + 16 * c + e > jmax) p0 = 0.f;
+              if (col0 + 16 * c + e + 1 > jmax) p1 = 0.f;
               pk[e >> 1] = pack_bf16x2(p0, p1);
             }
             tmem_st8(sc + 8 * c, pk);  // P chunk c over consumed score columns
@@ -291,7 +294,8 @@ cudaError_t tc_prep(const PrepArgs& a) {
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_prep_kernel<<<grid, NTHREADS, smem, a.stream>>>(mq, mk, mv, (const __nv_bfloat16*)a.dO, a.O,
-                                                     a.L, a.D, a.H, a.N, a.tau, a.err);
+                                                     a.L, a.D, a.H, a.N, a.tau,
+                                                     a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

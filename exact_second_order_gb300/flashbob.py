@@ -27,10 +27,10 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _SIGNATURES = {
-    "flashbob_prep": ([_P] * 7 + [_I] * 4 + [_F, _I, _P], _I),
-    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 5 + [_P], _I),
-    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 5 + [_P], _I),
-    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 5 + [_P], _I),
+    "flashbob_prep": ([_P] * 7 + [_I] * 4 + [_F, _I, _I, _P], _I),
+    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 6 + [_P], _I),
+    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 6 + [_P], _I),
+    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 6 + [_P], _I),
     "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
@@ -86,48 +86,48 @@ def flashbob_status_string(status: int) -> str:
     return load_library().flashbob_status_string(status).decode()
 
 
-def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, stream=None) -> None:
+def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream=None) -> None:
     """O, L, D of [B, H, N, d] inputs (see flashbob_prep in the header)."""
     B, H, N, d = Q.shape
     st = load_library().flashbob_prep(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, N, d,
-        float(tau), _dtype_code(Q), _stream_handle(stream))
+        float(tau), int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_prep")
 
 
 def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, ddOt, alpha, E,
-                 stream=None) -> None:
+                 causal: bool = False, stream=None) -> None:
     """d~Q, d~K, d~V, d~dO, alpha, E (see flashbob_bob in the header)."""
     B, H, N, d = Q.shape
     st = load_library().flashbob_bob(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
         _ptr(UV), float(tau), _ptr(dQt), _ptr(dKt), _ptr(dVt), _ptr(ddOt), _ptr(alpha), _ptr(E),
-        B, H, N, d, _dtype_code(Q), _stream_handle(stream))
+        B, H, N, d, int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob")
 
 
 def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, alpha, E,
-                       stream=None) -> None:
+                       causal: bool = False, stream=None) -> None:
     """Pass 1 only: d~Q, d~dO, alpha, E (see flashbob_bob_pass1 in the header)."""
     B, H, N, d = Q.shape
     st = load_library().flashbob_bob_pass1(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
         _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, N, d,
-        _dtype_code(Q), _stream_handle(stream))
+        int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass1")
 
 
 def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt, dVt,
-                       stream=None) -> None:
+                       causal: bool = False, stream=None) -> None:
     """Pass 2 only: d~K, d~V from pass 1's alpha, E (see flashbob_bob_pass2)."""
     B, H, N, d = Q.shape
     st = load_library().flashbob_bob_pass2(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(D), _ptr(alpha), _ptr(E), _ptr(UQ),
-        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, N, d, _dtype_code(Q),
-        _stream_handle(stream))
+        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, N, d, int(causal),
+        _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass2")
 
@@ -153,14 +153,14 @@ def flashbob_last_device_error() -> int:
 # Convenience wrappers: allocate the outputs with torch, then call the ABI.
 # ---------------------------------------------------------------------------
 
-def prep(Q, K, V, dO, tau: float, stream=None):
+def prep(Q, K, V, dO, tau: float, causal: bool = False, stream=None):
     """Allocate O, L, D on Q's device and run flashbob_prep."""
     import torch
     B, H, N, d = Q.shape
     O = torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device)
     L = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
     D = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
-    flashbob_prep(Q, K, V, dO, O, L, D, tau, stream)
+    flashbob_prep(Q, K, V, dO, O, L, D, tau, causal, stream)
     return O, L, D
 
 
@@ -178,10 +178,11 @@ def alloc_bob_outputs(Q, fill: float | None = None) -> dict:
     return out
 
 
-def bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, out: dict | None = None, stream=None):
+def bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, out: dict | None = None,
+        causal: bool = False, stream=None):
     """Run flashbob_bob into ``out`` (allocated when None); returns the dict."""
     if out is None:
         out = alloc_bob_outputs(Q)
     flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, out["dQt"], out["dKt"], out["dVt"],
-                 out["ddOt"], out["alpha"], out["E"], stream)
+                 out["ddOt"], out["alpha"], out["E"], causal, stream)
     return out

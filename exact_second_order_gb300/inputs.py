@@ -44,6 +44,7 @@ class Workload:
     peaked_k_rows: bool = False
     stress: bool = False
     seed: int = 0
+    causal: bool = False
 
     @property
     def tau(self) -> float:
@@ -51,8 +52,9 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Fixed GEMM list of both passes: 19 GEMMs of 2 N^2 d each."""
-        return 38.0 * self.N * self.N * self.d * self.B * self.H
+        """Fixed GEMM list of both passes: 19 GEMMs of 2 N^2 d each (half of
+        that under the causal mask)."""
+        return (0.5 if self.causal else 1.0) * 38.0 * self.N * self.N * self.d * self.B * self.H
 
 
 # The five workloads of the isolated-layer benchmark (non-causal).
@@ -67,8 +69,15 @@ LONG_CONTEXT = Workload("long_B1_H4_N65536_d64", 1, 4, 65536, 64, "bf16")
 EXTREME_D64 = Workload("extreme_B1_H1_N262144_d64", 1, 1, 262144, 64, "bf16")
 EXTREME_D128 = Workload("extreme_B1_H1_N131072_d128", 1, 1, 131072, 128, "bf16")
 
+# Causal shapes of the pages' isolated-layer timing table (B=4, H=12, bf16).
+CAUSAL_N4096 = Workload("causal_B4_H12_N4096_d64", 4, 12, 4096, 64, "bf16", causal=True)
+CAUSAL_N16384 = Workload("causal_B4_H12_N16384_d64", 4, 12, 16384, 64, "bf16", causal=True)
+# A mid-size case for detailed profiles: inputs (~0.3 GB) larger than L2.
+PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
+
 WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PEAKED,
-                                 MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128)}
+                                 MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128,
+                                 CAUSAL_N4096, CAUSAL_N16384, PROFILE)}
 
 
 def make_inputs(w: Workload) -> dict[str, torch.Tensor]:

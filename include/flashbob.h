@@ -67,18 +67,21 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
  *   out: O [B,H,N,d] fp32 (O = P V), L [B,H,N] fp32 (natural-log logsumexp of
  *        tau Q K^T per row), D [B,H,N] fp32 (D_i = dO_i . O_i)
  *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
+ *   causal: 0 = full attention; 1 = query i sees keys j <= i only (the
+ *        setting of [FBN] 实验关键数据); other values are rejected.
  *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535.  One launch: bf16 inputs
  *   with d = 64 run a tcgen05 kernel, every other case fp32 CUDA cores.
  */
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
                               float* O, float* L, float* D, int B, int H, int N, int d,
-                              float tau, flashbob_dtype in_dtype, void* stream);
+                              float tau, int causal, flashbob_dtype in_dtype, void* stream);
 
 /*
  * flashbob_bob: exact BoB of softmax attention with the two-pass schedule of
  * [FBN] 关键设计 2; the closed form and affine correction of [FBN] 关键设计 1.
  *   in : Q, K, V, dO, U_Q, U_K, U_V [B,H,N,d] of in_dtype; O [B,H,N,d] fp32;
- *        L, D [B,H,N] fp32 (as written by flashbob_prep); tau as in prep.
+ *        L, D [B,H,N] fp32 (as written by flashbob_prep with the same
+ *        causal flag); tau and causal as in prep.
  *   out: dQt, dKt, dVt, ddOt [B,H,N,d] fp32 (d~Q, d~K, d~V, d~dO);
  *        alpha, E [B,H,N] fp32.  Every element is written exactly once.
  *   Pass 1 (row-resident) writes d~Q, d~dO, alpha, E; pass 2 (column-
@@ -91,7 +94,7 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
                              const void* dO, const float* L, const float* D, const void* UQ,
                              const void* UK, const void* UV, float tau, float* dQt, float* dKt,
                              float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
-                             int N, int d, flashbob_dtype in_dtype, void* stream);
+                             int N, int d, int causal, flashbob_dtype in_dtype, void* stream);
 
 /*
  * flashbob_bob_pass1 / flashbob_bob_pass2: the two launches of flashbob_bob,
@@ -107,13 +110,15 @@ flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, 
                                    const void* dO, const float* L, const float* D,
                                    const void* UQ, const void* UK, const void* UV, float tau,
                                    float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
-                                   int N, int d, flashbob_dtype in_dtype, void* stream);
+                                   int N, int d, int causal, flashbob_dtype in_dtype,
+                                   void* stream);
 
 flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, const void* dO,
                                    const float* L, const float* D, const float* alpha,
                                    const float* E, const void* UQ, const void* UK,
                                    const void* UV, float tau, float* dKt, float* dVt, int B,
-                                   int H, int N, int d, flashbob_dtype in_dtype, void* stream);
+                                   int H, int N, int d, int causal, flashbob_dtype in_dtype,
+                                   void* stream);
 
 /*
  * flashbob_bob_tile_sizes: the tiles flashbob_bob uses for (d, in_dtype):

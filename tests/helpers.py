@@ -30,10 +30,11 @@ def run_cuda(w, stream=None, fill_nan=True):
     flashbob_prep + flashbob_bob."""
     x = make_inputs(w)
     dev = {k: v.cuda() for k, v in x.items()}
-    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, stream)
+    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal,
+                      stream=stream)
     out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan") if fill_nan else None)
     fb.bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"], dev["UK"], dev["UV"],
-           w.tau, out=out, stream=stream)
+           w.tau, out=out, causal=w.causal, stream=stream)
     torch.cuda.synchronize()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
     return x, dev, {"O": O, "L": L, "D": D}, out
@@ -51,8 +52,9 @@ def full_oracle_errors(w, x, state, out, heads=None):
     """Relative Frobenius errors of every output against the full oracle."""
     args = oracle_inputs(x)
     Q, K, V, dO = args[:4]
-    ref = orc.bob_batched(*args, w.tau, heads=heads)
-    O, L, D = orc.prep_batched(Q, K, V, dO, w.tau) if heads is None else (None, None, None)
+    ref = orc.bob_batched(*args, w.tau, heads=heads, causal=w.causal)
+    O, L, D = (orc.prep_batched(Q, K, V, dO, w.tau, causal=w.causal) if heads is None
+               else (None, None, None))
     errs = {}
     sel = (lambda a: a) if heads is None else (lambda a: np.stack([a[b, h] for b, h in heads]))
     for k in MAT_KEYS + ROW_KEYS:
@@ -75,7 +77,7 @@ def sampled_row_errors(w, x, out, state, n_rows=256, seed=1234, heads=None):
     for b, h in heads:
         rows = np.sort(rng.choice(N, size=min(n_rows, N), replace=False))
         args = [as_float64_numpy(x[k][b, h]) for k in NAMES]
-        r = orc.bob_rows(*args, w.tau, rows)
+        r = orc.bob_rows(*args, w.tau, rows, causal=w.causal)
         for k in got:
             src = out[k] if k in out else state[k]
             got[k].append(to_np(src[b, h][rows]))

@@ -81,14 +81,14 @@ def _memory_checked_run(w):
     torch.cuda.synchronize()
     x = wl.make_inputs(w)
     dev = {k: v.cuda() for k, v in x.items()}
-    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau)
+    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
     out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan"))
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats()
     before_alloc = torch.cuda.memory_allocated()
     free_before, _ = torch.cuda.mem_get_info()
     fb.bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"], dev["UK"], dev["UV"],
-           w.tau, out=out)
+           w.tau, out=out, causal=w.causal)
     torch.cuda.synchronize()
     free_after, _ = torch.cuda.mem_get_info()
     assert torch.cuda.max_memory_allocated() - before_alloc <= 64 << 20
@@ -141,3 +141,26 @@ def test_bad_arguments_return_codes_and_launch_nothing():
         assert torch.equal(out[k], before[k]) or torch.isnan(before[k]).all()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
     np.testing.assert_equal(fb.flashbob_status_string(0), "FLASHBOB_OK")
+
+
+# --------------------------------------------------------------------------
+# Causal mask (the setting of the pages' timing tables)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N", [1, 5, 32, 127, 128, 129, 300, 700])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (64, "f32"), (96, "bf16")])
+def test_causal_small_shapes(N, d, dtype):
+    _check_full(wl.small_workload(1, 2, N, d, dtype, seed=N + d, causal=True))
+
+
+def test_causal_pages_shape_sampled_rows():
+    w = wl.CAUSAL_N4096
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    heads = [(0, 0), (1, 5), (3, 11)]
+    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=heads)
+    assert max(errs.values()) <= TOL["bf16"], errs
+    res = column_sum_residuals(out)
+    assert max(res.values()) <= TOL["bf16"], res
+    full = full_oracle_errors(w, x, state, out, heads=[(2, 7)])
+    assert max(full.values()) <= TOL["bf16"], full
