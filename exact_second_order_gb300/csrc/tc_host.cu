@@ -7,8 +7,7 @@ namespace flashbob {
 
 cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps32);
-cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
-                            const CUtensorMap* maps32);
+cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps32);
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && a.d == 64; }
 
@@ -28,15 +27,12 @@ cudaError_t tc_bob(const BobArgs& a) {
     if (e != cudaSuccess) return e;
   }
   if (a.passes & kPass2) {
-    CUtensorMap m128[4], m32[3];
-    const void* res[4] = {a.K, a.V, a.UK, a.UV};
+    CUtensorMap m32[3];
     const void* str[3] = {a.Q, a.dO, a.UQ};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m128[i], res[i], BH, a.N, kTcRows);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
       e = tc::make_map_bf16_d64(&m32[i], str[i], BH, a.N, kTcStream);
     if (e != cudaSuccess) return e;
-    e = tc_launch_pass2(a, m128, m32);
+    e = tc_launch_pass2(a, m32);
   }
   return e;
 }

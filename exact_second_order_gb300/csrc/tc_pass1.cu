@@ -10,18 +10,21 @@
 // runs once in the epilogue, so every output row is written exactly once.
 //
 // CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
-//   warp 0      TMA producer: Q, dO, U_Q blocks once, then K, V, U_K, U_V
+//   warp 0      TMA producer: Q, dO, U_Q blocks once, then K, U_K, V, U_V
 //               tiles of 32 key rows through a 6-stage mbarrier ring;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
 //   warps 2-5   elementwise warpgroup 0 (tiles 0, 2, 4, ...),
 //   warps 6-9   elementwise warpgroup 1 (tiles 1, 3, 5, ...).
 // TMEM (512 columns x 128 lanes, fp32):
-//   [0,64) B = P K   [64,128) R = (P o dP) K   [128,192) Omega   [192,256) d~dO0
+//   [0,64) B = P K   [64,128) d~dO0   [128,192) R = (P o dP) K   [192,256) Omega
 //   [256,384) score buffer 0, [384,512) score buffer 1, each holding
-//   S = Q K^T | dP = dO V^T | F' = U_Q K^T + Q U_K^T | G = dO U_V^T (32 columns each).
-// Once a warpgroup has read a score buffer it overwrites consumed columns
-// with the bf16 A operands (P, P o dP, P o d~P0, dS, P o F) of the output
-// GEMMs, which read A straight from TMEM.
+//   S = Q K^T | F' = Q U_K^T + U_Q K^T | dP = dO V^T | G = dO U_V^T (32 columns each).
+// GEMMs that share an operand run as one wider MMA: Q [K; U_K]^T gives S and
+// half of F' (N = 64), dO [V; U_V]^T gives dP and G (N = 64), and
+// P [K | U_V] gives both B and the P U_V part of d~dO0 (N = 128).  Once a
+// warpgroup has read a score buffer it overwrites consumed columns with the
+// bf16 A operands (P, P o dP, P o d~P0, dS, P o F) of the output GEMMs,
+// which read A straight from TMEM.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -42,7 +45,7 @@ struct Smem1 {
   alignas(1024) uint8_t q[BLOCK_BYTES];
   alignas(1024) uint8_t dO[BLOCK_BYTES];
   alignas(1024) uint8_t uq[BLOCK_BYTES];
-  alignas(1024) uint8_t kv[NST][4][TILE_BYTES];  // K, V, U_K, U_V
+  alignas(1024) uint8_t kv[NST][4][TILE_BYTES];  // K, U_K, V, U_V (K|U_K and V|U_V adjacent)
   float part_a[2][BM];
   float part_e[2][BM];
   uint64_t bar_q;
@@ -55,15 +58,19 @@ struct Smem1 {
   int abort_flag;
 };
 
+// Score buffer layout (columns): S at 0, F' at 32, dP at 64, G at 96.
+constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;
 // TMEM columns of the bf16 operand slots inside a score buffer, for the two
 // K = 16 steps of the output GEMMs.  Chunk 0 (score columns 0..15) writes
 // only columns it has consumed (the first 16 of each 32-column score);
-// chunk 1 may also use columns 16..23 of S and dP, which it loaded itself.
+// chunk 1 may also use columns 16..31 of S and F', which it loaded itself.
 __device__ __forceinline__ constexpr uint32_t slot_P(int c) { return c ? 72 : 0; }
 __device__ __forceinline__ constexpr uint32_t slot_PdP(int c) { return c ? 96 : 8; }
 __device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return c ? 104 : 32; }
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 16 : 40; }
 __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return c ? 48 : 64; }
+// Output accumulators.
+constexpr uint32_t kAccB = 0, kAccdO = 64, kAccR = 128, kAccW = 192;
 
 // One 16-column chunk of a score buffer, one row per thread: read S, dP, F',
 // G from TMEM, form P = exp(S - L) and the five bf16 A operands of the
@@ -73,10 +80,10 @@ template <bool MASKED, int C>
 __device__ __forceinline__ void p1_chunk(uint32_t sc, int col0, int jmax, float c1, float Lr2,
                                          float Dr, float tau, float& a_acc, float& e_acc) {
   uint32_t s[16], dp[16], f[16], g[16];
-  tmem_ld16(sc + 0 + 16 * C, s);
-  tmem_ld16(sc + 32 + 16 * C, dp);
-  tmem_ld16(sc + 64 + 16 * C, f);
-  tmem_ld16(sc + 96 + 16 * C, g);
+  tmem_ld16(sc + kColS + 16 * C, s);
+  tmem_ld16(sc + kColdP + 16 * C, dp);
+  tmem_ld16(sc + kColF + 16 * C, f);
+  tmem_ld16(sc + kColG + 16 * C, g);
   tmem_wait_ld();
   uint32_t oP[8], oPdP[8], oPdPt[8], odS[8], oPF[8];
   const int jbase = col0 + 16 * C;
@@ -171,8 +178,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.kv_full[s], 4 * TILE_BYTES);
         tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.kv[s][1], &mV, &sm.kv_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.kv[s][2], &mUK, &sm.kv_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.kv[s][1], &mUK, &sm.kv_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.kv[s][2], &mV, &sm.kv_full[s], 0, t * BN, bh);
         tma_load_3d(sm.kv[s][3], &mUV, &sm.kv_full[s], 0, t * BN, bh);
         issued = t + 1;
       }
@@ -184,52 +191,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(BM, BN, false);  // scores: N = 32, B K-major
-      constexpr uint32_t idO = idesc_bf16(BM, DH, true);   // outputs: N = 64, B MN-major
-      const uint32_t aq = smem_u32(sm.q), ado = smem_u32(sm.dO), auq = smem_u32(sm.uq);
+      constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);       // N = 32, B K-major
+      constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);   // N = 64, B K-major
+      constexpr uint32_t idO64 = idesc_bf16(BM, DH, true);        // N = 64, B MN-major
+      constexpr uint32_t idO128 = idesc_bf16(BM, 2 * DH, true);   // N = 128, B MN-major
+      // Descriptors of the resident blocks and of stage 0; a k-step adds
+      // 32 bytes (16 bf16 inside the swizzled row) and a stage adds
+      // 4 * TILE_BYTES to the start-address field (address >> 4).
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
+      const uint64_t ddo0 = smem_desc_sw128(smem_u32(sm.dO), 16, 1024);
+      const uint64_t duq0 = smem_desc_sw128(smem_u32(sm.uq), 16, 1024);
+      const uint32_t kv0 = smem_u32(sm.kv[0][0]);
+      const uint64_t dK0 = smem_desc_sw128(kv0, 16, 1024);                   // K (and K;U_K)
+      const uint64_t dV0 = smem_desc_sw128(kv0 + 2 * TILE_BYTES, 16, 1024);  // V (and V;U_V)
+      const uint64_t dUK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);
+      // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
+      const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
       auto issue_scores = [&](int t) {
-        const int s = t % NST;
+        const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        const uint32_t bk = smem_u32(sm.kv[s][0]), bv = smem_u32(sm.kv[s][1]);
-        const uint32_t buk = smem_u32(sm.kv[s][2]), buv = smem_u32(sm.kv[s][3]);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t o = 32 * kk;  // 16 bf16 along K inside the 128-byte swizzled row
-          const uint64_t dq = smem_desc_sw128(aq + o, 16, 1024);
-          const uint64_t ddo = smem_desc_sw128(ado + o, 16, 1024);
-          const uint64_t duq = smem_desc_sw128(auq + o, 16, 1024);
-          const uint64_t dk = smem_desc_sw128(bk + o, 16, 1024);
-          const uint64_t dv = smem_desc_sw128(bv + o, 16, 1024);
-          const uint64_t duk = smem_desc_sw128(buk + o, 16, 1024);
-          const uint64_t duv = smem_desc_sw128(buv + o, 16, 1024);
+          const uint64_t o = 2 * kk;  // 32 bytes >> 4
           const uint32_t acc = kk > 0;
-          mma_ss(sc + 0, dq, dk, idS, acc);     // S  = Q K^T
-          mma_ss(sc + 32, ddo, dv, idS, acc);   // dP = dO V^T
-          mma_ss(sc + 64, duq, dk, idS, acc);   // F' = U_Q K^T
-          mma_ss(sc + 64, dq, duk, idS, 1);     //    + Q U_K^T
-          mma_ss(sc + 96, ddo, duv, idS, acc);  // G  = dO U_V^T
+          mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);  // [S | F'] = Q [K; U_K]^T
+          mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);   // F' += U_Q K^T
+          mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
         }
         mma_commit(&sm.sc_full[t & 1]);
       };
       auto issue_outputs = [&](int t) {
         const int s = t % NST;
+        const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        const uint32_t bk = smem_u32(sm.kv[s][0]), bv = smem_u32(sm.kv[s][1]);
-        const uint32_t buk = smem_u32(sm.kv[s][2]), buv = smem_u32(sm.kv[s][3]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t o = 16 * 128 * c;  // 16 key rows further down the tile
-          const uint64_t dk = smem_desc_sw128(bk + o, 16, 1024);
-          const uint64_t dv = smem_desc_sw128(bv + o, 16, 1024);
-          const uint64_t duk = smem_desc_sw128(buk + o, 16, 1024);
-          const uint64_t duv = smem_desc_sw128(buv + o, 16, 1024);
+          const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
           const uint32_t acc = (t > 0 || c > 0);
-          mma_ts(tbase + 0, sc + slot_P(c), dk, idO, acc);      // B     += P K
-          mma_ts(tbase + 64, sc + slot_PdP(c), dk, idO, acc);   // R     += (P o dP) K
-          mma_ts(tbase + 128, sc + slot_PdPt(c), dk, idO, acc); // Omega += (P o d~P0) K
-          mma_ts(tbase + 128, sc + slot_dS(c), duk, idO, 1);    //       +  dS U_K
-          mma_ts(tbase + 192, sc + slot_P(c), duv, idO, acc);   // d~dO0 += P U_V
-          mma_ts(tbase + 192, sc + slot_PF(c), dv, idO, 1);     //       +  (P o F) V
+          mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
+          mma_ts(tbase + kAccR, sc + slot_PdP(c), dK0 + so + o, idO64, acc);   // R += (P o dP) K
+          mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
+          mma_ts(tbase + kAccW, sc + slot_dS(c), dUK0 + so + o, idO64, 1);     //       +  dS U_K
+          mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
         }
         mma_commit(&sm.kv_empty[s]);
       };
@@ -308,10 +311,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int h = 0; h < 2; ++h) {
       const int col = 32 * wg + 16 * h;
       uint32_t vb[16], vr[16], vw[16], vo[16];
-      tmem_ld16(acc_base + 0 + col, vb);
-      tmem_ld16(acc_base + 64 + col, vr);
-      tmem_ld16(acc_base + 128 + col, vw);
-      tmem_ld16(acc_base + 192 + col, vo);
+      tmem_ld16(acc_base + kAccB + col, vb);
+      tmem_ld16(acc_base + kAccR + col, vr);
+      tmem_ld16(acc_base + kAccW + col, vw);
+      tmem_ld16(acc_base + kAccdO + col, vo);
       tmem_wait_ld();
       if (ok && gr < N) {
         const size_t off = rowvec * DH + col;

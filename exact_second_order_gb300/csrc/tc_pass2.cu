@@ -14,12 +14,16 @@
 // (F = tau (U_Q K^T + Q U_K^T), G = dO U_V^T; the same chain rule as pass 1).
 //
 // CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
-//   warp 0      TMA producer: K, V, U_K, U_V blocks once, then Q, dO, U_Q
-//               tiles of 32 query rows through a 6-stage mbarrier ring;
+//   warp 0      TMA producer: Q, U_Q, dO tiles of 32 query rows through a
+//               10-stage mbarrier ring;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
-//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1 (even / odd tiles).
-// TMEM: [0,64) d~K accumulator, [64,128) d~V accumulator, [128,256) and
-// [256,384) score buffers S^T | dP^T | F'^T | G^T (32 columns each).
+//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1 (even / odd tiles); at the
+//               start they also copy their key row of K, U_K / V, U_V into TMEM.
+// TMEM: [0,64) d~K accumulator, [64,128) d~V accumulator, [128,256) the
+// resident K | V | U_K | U_V block as bf16 (the A operands of every score
+// GEMM, so shared memory only feeds the 32-row B tiles), [256,384) and
+// [384,512) score buffers S^T | F'^T | dP^T | G^T (32 columns each).
+// K [Q; U_Q]^T gives S^T and half of F'^T in one N = 64 MMA.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -30,22 +34,17 @@ using namespace tc;
 constexpr int BM = kTcRows;    // 128 key rows per CTA
 constexpr int BN = kTcStream;  // 32 query rows per streamed tile
 constexpr int DH = 64;
-constexpr int NST = 6;
+constexpr int NST = 10;
 constexpr int NTHREADS = 320;
-constexpr uint32_t BLOCK_BYTES = BM * DH * 2;
 constexpr uint32_t TILE_BYTES = BN * DH * 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Smem2 {
-  alignas(1024) uint8_t k[BLOCK_BYTES];
-  alignas(1024) uint8_t v[BLOCK_BYTES];
-  alignas(1024) uint8_t uk[BLOCK_BYTES];
-  alignas(1024) uint8_t uv[BLOCK_BYTES];
-  alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, dO, U_Q
+  alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, U_Q, dO (Q|U_Q adjacent)
   float4 scal[2][2][BN];  // per warpgroup, double-buffered: (L log2 e, D, alpha, E)
-  uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
+  uint64_t a_ready;
   uint64_t sc_full[2];
   uint64_t op_ready[2];
   uint64_t out_full;
@@ -53,10 +52,50 @@ struct Smem2 {
   int abort_flag;
 };
 
-// bf16 operand slots inside a score buffer (see pass 1 for the rule).
+// TMEM columns.
+constexpr uint32_t kAccK = 0, kAccV = 64;
+constexpr uint32_t kAK = 128, kAV = 160, kAUK = 192, kAUV = 224;  // 64 bf16 = 32 columns each
+constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;  // inside a score buffer
+
+// bf16 operand slots inside a score buffer: chunk 0 writes only columns it
+// has read (the first 16 of S^T and F'^T), chunk 1 only columns chunk 0 read.
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 40 : 0; }
 __device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return c ? 64 : 8; }
 __device__ __forceinline__ constexpr uint32_t slot_W(int c) { return c ? 72 : 32; }
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Copy one 64-element bf16 row (zeros past N) into 32 TMEM columns.
+// `row` is null for rows past N.
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16* row) {
+  uint32_t r[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) r[k] = 0u;
+  if (row != nullptr) {
+    const uint4* src = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 v = src[k];
+      r[4 * k] = v.x;
+      r[4 * k + 1] = v.y;
+      r[4 * k + 2] = v.z;
+      r[4 * k + 3] = v.w;
+    }
+  }
+  tmem_st32(taddr, r);
+}
 
 // One 16-column chunk of a transposed score buffer, one key row per thread:
 // with the row scalars of the streamed query rows form dS, d~S and W and
@@ -65,10 +104,10 @@ template <bool MASKED, int C>
 __device__ __forceinline__ void p2_chunk(uint32_t sc, const float4* scal, int ibase, int gj,
                                          float c1, float tau) {
   uint32_t s[16], dp[16], f[16], g[16];
-  tmem_ld16(sc + 0 + 16 * C, s);
-  tmem_ld16(sc + 32 + 16 * C, dp);
-  tmem_ld16(sc + 64 + 16 * C, f);
-  tmem_ld16(sc + 96 + 16 * C, g);
+  tmem_ld16(sc + kColS + 16 * C, s);
+  tmem_ld16(sc + kColdP + 16 * C, dp);
+  tmem_ld16(sc + kColF + 16 * C, f);
+  tmem_ld16(sc + kColG + 16 * C, g);
   tmem_wait_ld();
   uint32_t odS[8], odSt[8], oW[8];
 #pragma unroll
@@ -97,8 +136,8 @@ __device__ __forceinline__ void p2_chunk(uint32_t sc, const float4* scal, int ib
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
-                    const __grid_constant__ CUtensorMap mUK, const __grid_constant__ CUtensorMap mUV,
+    tc_pass2_kernel(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
+                    const __nv_bfloat16* __restrict__ UK, const __nv_bfloat16* __restrict__ UV,
                     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                     const __grid_constant__ CUtensorMap mUQ, const float* __restrict__ L,
                     const float* __restrict__ D, const float* __restrict__ alpha,
@@ -119,7 +158,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.bar_kv, 1);
+    mbar_init(&sm.a_ready, 256);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.st_full[s], 1);
       mbar_init(&sm.st_empty[s], 1);
@@ -143,74 +182,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
       tma_prefetch_desc(&mUQ);
-      mbar_expect_tx(&sm.bar_kv, 4 * BLOCK_BYTES);
-      tma_load_3d(sm.k, &mK, &sm.bar_kv, 0, j0, bh);
-      tma_load_3d(sm.v, &mV, &sm.bar_kv, 0, j0, bh);
-      tma_load_3d(sm.uk, &mUK, &sm.bar_kv, 0, j0, bh);
-      tma_load_3d(sm.uv, &mUV, &sm.bar_kv, 0, j0, bh);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % NST;
         if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
         tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
-        tma_load_3d(sm.st[s][1], &mdO, &sm.st_full[s], 0, (t + t0) * BN, bh);
-        tma_load_3d(sm.st[s][2], &mUQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
+        tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
+        tma_load_3d(sm.st[s][2], &mdO, &sm.st_full[s], 0, (t + t0) * BN, bh);
         issued = t + 1;
       }
-      drain_wait(&sm.bar_kv, 0);
       for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
         drain_wait(&sm.st_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(BM, BN, false);
-      constexpr uint32_t idO = idesc_bf16(BM, DH, true);
-      const uint32_t ak = smem_u32(sm.k), av = smem_u32(sm.v);
-      const uint32_t auk = smem_u32(sm.uk), auv = smem_u32(sm.uv);
+      constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
+      constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
+      constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 64, B MN-major
+      const uint32_t st0 = smem_u32(sm.st[0][0]);
+      const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
+      const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
+      const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
       auto issue_scores = [&](int t) {
-        const int s = t % NST;
-        const uint32_t sc = tbase + 128 + 128 * (t & 1);
-        const uint32_t bq = smem_u32(sm.st[s][0]), bdo = smem_u32(sm.st[s][1]);
-        const uint32_t buq = smem_u32(sm.st[s][2]);
+        const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
+        const uint32_t sc = tbase + 256 + 128 * (t & 1);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t o = 32 * kk;
-          const uint64_t dk = smem_desc_sw128(ak + o, 16, 1024);
-          const uint64_t dv = smem_desc_sw128(av + o, 16, 1024);
-          const uint64_t duk = smem_desc_sw128(auk + o, 16, 1024);
-          const uint64_t duv = smem_desc_sw128(auv + o, 16, 1024);
-          const uint64_t dq = smem_desc_sw128(bq + o, 16, 1024);
-          const uint64_t ddo = smem_desc_sw128(bdo + o, 16, 1024);
-          const uint64_t duq = smem_desc_sw128(buq + o, 16, 1024);
+          const uint64_t o = 2 * kk;       // 32 bytes >> 4 along K in the B tiles
+          const uint32_t ao = 8 * kk;      // 16 bf16 = 8 TMEM columns along K in A
           const uint32_t acc = kk > 0;
-          mma_ss(sc + 0, dk, dq, idS, acc);     // S^T  = K Q^T
-          mma_ss(sc + 32, dv, ddo, idS, acc);   // dP^T = V dO^T
-          mma_ss(sc + 64, dk, duq, idS, acc);   // F'^T = K U_Q^T
-          mma_ss(sc + 64, duk, dq, idS, 1);     //      + U_K Q^T
-          mma_ss(sc + 96, duv, ddo, idS, acc);  // G^T  = U_V dO^T
+          mma_ts(sc + kColS, tbase + kAK + ao, dQ0 + so + o, idS64, acc);   // [S^T | F'^T] = K [Q; U_Q]^T
+          mma_ts(sc + kColF, tbase + kAUK + ao, dQ0 + so + o, idS32, 1);    // F'^T += U_K Q^T
+          mma_ts(sc + kColdP, tbase + kAV + ao, ddO0 + so + o, idS32, acc); // dP^T = V dO^T
+          mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
         }
         mma_commit(&sm.sc_full[t & 1]);
       };
       auto issue_outputs = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + 128 + 128 * (t & 1);
-        const uint32_t bq = smem_u32(sm.st[s][0]), bdo = smem_u32(sm.st[s][1]);
-        const uint32_t buq = smem_u32(sm.st[s][2]);
+        const uint64_t so = (uint64_t)(s * 3 * TILE_BYTES) >> 4;
+        const uint32_t sc = tbase + 256 + 128 * (t & 1);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t o = 16 * 128 * c;
-          const uint64_t dq = smem_desc_sw128(bq + o, 16, 1024);
-          const uint64_t ddo = smem_desc_sw128(bdo + o, 16, 1024);
-          const uint64_t duq = smem_desc_sw128(buq + o, 16, 1024);
+          const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
           const uint32_t acc = (t > 0 || c > 0);
-          mma_ts(tbase + 0, sc + slot_dSt(c), dq, idO, acc);  // d~K += d~S^T Q
-          mma_ts(tbase + 0, sc + slot_dS(c), duq, idO, 1);    //     +  dS^T U_Q
-          mma_ts(tbase + 64, sc + slot_W(c), ddo, idO, acc);  // d~V += W^T dO
+          mma_ts(tbase + kAccK, sc + slot_dSt(c), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
+          mma_ts(tbase + kAccK, sc + slot_dS(c), dUQ0 + so + o, idO, 1);    //     +  dS^T U_Q
+          mma_ts(tbase + kAccV, sc + slot_W(c), ddO0 + so + o, idO, acc);   // d~V += W^T dO
         }
         mma_commit(&sm.st_empty[s]);
       };
-      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err);
+      bool ok = mbar_wait(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
       tc_fence_after();
       for (int t = 0; ok && t < 2 && t < T; ++t) {
         ok = mbar_wait(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
@@ -239,9 +262,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int gj = j0 + r;
     const size_t head = static_cast<size_t>(bh) * N;
     const float c1 = tau * kLog2e;
-    const uint32_t sc = tbase + lane_off + 128 + 128 * wg;
+    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
     const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
     bool ok = true;
+
+    // Resident key block into TMEM: warpgroup 0 copies K and U_K, warpgroup
+    // 1 copies V and U_V, one key row per thread.
+    {
+      const bool valid = gj < N;
+      const size_t roff = valid ? (head + gj) * DH : 0;
+      if (wg == 0) {
+        row_to_tmem(tbase + lane_off + kAK, valid ? K + roff : nullptr);
+        row_to_tmem(tbase + lane_off + kAUK, valid ? UK + roff : nullptr);
+      } else {
+        row_to_tmem(tbase + lane_off + kAV, valid ? V + roff : nullptr);
+        row_to_tmem(tbase + lane_off + kAUV, valid ? UV + roff : nullptr);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sm.a_ready);
+    }
 
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
@@ -288,8 +328,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int h = 0; h < 2; ++h) {
       const int col = 32 * wg + 16 * h;
       uint32_t vk[16], vv[16];
-      tmem_ld16(acc_base + 0 + col, vk);
-      tmem_ld16(acc_base + 64 + col, vv);
+      tmem_ld16(acc_base + kAccK + col, vk);
+      tmem_ld16(acc_base + kAccV + col, vv);
       tmem_wait_ld();
       if (ok && gj < N) {
         const size_t off = (head + gj) * DH + col;
@@ -319,17 +359,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 size_t tc_pass2_smem() { return sizeof(Smem2) + 1024; }
 
-cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
-                            const CUtensorMap* maps32) {
-  // maps128: K, V, U_K, U_V with 128-row boxes; maps32: Q, dO, U_Q with 32-row boxes.
+cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps32) {
+  // maps32: Q, dO, U_Q with 32-row boxes; K, V, U_K, U_V are read directly.
   const size_t smem = tc_pass2_smem();
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D,
-      a.alpha, a.E, a.dKt, a.dVt, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
+      (const __nv_bfloat16*)a.K, (const __nv_bfloat16*)a.V, (const __nv_bfloat16*)a.UK,
+      (const __nv_bfloat16*)a.UV, maps32[0], maps32[1], maps32[2], a.L, a.D, a.alpha, a.E,
+      a.dKt, a.dVt, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 
