@@ -52,7 +52,7 @@ struct Smem1 {
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
   uint64_t sc_full[2];
-  uint64_t op_ready[2];
+  uint64_t op_ready[2][2];  // [buffer][chunk]: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -77,14 +77,11 @@ constexpr uint32_t kAccB = 0, kAccdO = 64, kAccR = 128, kAccW = 192;
 // output GEMMs, add to the row sums alpha and E0, and write the operands back
 // over consumed columns.
 template <bool MASKED, int C>
-__device__ __forceinline__ void p1_chunk(uint32_t sc, int col0, int jmax, float c1, float Lr2,
-                                         float Dr, float tau, float& a_acc, float& e_acc) {
-  uint32_t s[16], dp[16], f[16], g[16];
-  tmem_ld16(sc + kColS + 16 * C, s);
-  tmem_ld16(sc + kColdP + 16 * C, dp);
-  tmem_ld16(sc + kColF + 16 * C, f);
-  tmem_ld16(sc + kColG + 16 * C, g);
-  tmem_wait_ld();
+__device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
+                                         const uint32_t (&dp)[16], const uint32_t (&f)[16],
+                                         const uint32_t (&g)[16], int col0, int jmax, float c1,
+                                         float Lr2, float Dr, float tau, float& a_acc,
+                                         float& e_acc) {
   uint32_t oP[8], oPdP[8], oPdPt[8], odS[8], oPF[8];
   const int jbase = col0 + 16 * C;
 #pragma unroll
@@ -120,6 +117,35 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, int col0, int jmax, float 
   tmem_st8(sc + slot_PF(C), oPF);
 }
 
+// One 32-column tile, one row per thread: read all of S, F', dP, G (both
+// 16-column chunks) with a single wait, then form the bf16 A operands of
+// the output GEMMs chunk by chunk.  Each chunk is handed to the MMA issuer
+// as soon as it is in TMEM, so the output MMAs of chunk 0 overlap the
+// arithmetic of chunk 1.
+template <bool MASKED>
+__device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready0, uint64_t* ready1, int col0,
+                                        int jmax, float c1, float Lr2, float Dr, float tau,
+                                        float& a_acc, float& e_acc) {
+  uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
+  tmem_ld16(sc + kColS, s0);
+  tmem_ld16(sc + kColdP, dp0);
+  tmem_ld16(sc + kColF, f0);
+  tmem_ld16(sc + kColG, g0);
+  tmem_ld16(sc + kColS + 16, s1);
+  tmem_ld16(sc + kColdP + 16, dp1);
+  tmem_ld16(sc + kColF + 16, f1);
+  tmem_ld16(sc + kColG + 16, g1);
+  tmem_wait_ld();
+  p1_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+  tmem_wait_st();
+  tc_fence_before();
+  warp_arrive(ready0);
+  p1_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+  tmem_wait_st();
+  tc_fence_before();
+  warp_arrive(ready1);
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                     const __grid_constant__ CUtensorMap mUQ, const __grid_constant__ CUtensorMap mK,
@@ -148,7 +174,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.op_ready[b], 128);
+      mbar_init(&sm.op_ready[b][0], 4);
+      mbar_init(&sm.op_ready[b][1], 4);
     }
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
@@ -220,21 +247,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit(&sm.sc_full[t & 1]);
       };
-      auto issue_outputs = [&](int t) {
+      auto issue_outputs = [&](int t, int c) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
-          const uint32_t acc = (t > 0 || c > 0);
-          mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
-          mma_ts(tbase + kAccR, sc + slot_PdP(c), dK0 + so + o, idO64, acc);   // R += (P o dP) K
-          mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
-          mma_ts(tbase + kAccW, sc + slot_dS(c), dUK0 + so + o, idO64, 1);     //       +  dS U_K
-          mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
-        }
-        mma_commit(&sm.kv_empty[s]);
+        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
+        const uint32_t acc = (t > 0 || c > 0);
+        const uint32_t aP = sc + (c ? slot_P(1) : slot_P(0));
+        const uint32_t aPdP = sc + (c ? slot_PdP(1) : slot_PdP(0));
+        const uint32_t aPdPt = sc + (c ? slot_PdPt(1) : slot_PdPt(0));
+        const uint32_t adS = sc + (c ? slot_dS(1) : slot_dS(0));
+        const uint32_t aPF = sc + (c ? slot_PF(1) : slot_PF(0));
+        mma_ts(tbase + kAccB, aP, dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
+        mma_ts(tbase + kAccR, aPdP, dK0 + so + o, idO64, acc);   // R += (P o dP) K
+        mma_ts(tbase + kAccW, aPdPt, dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
+        mma_ts(tbase + kAccW, adS, dUK0 + so + o, idO64, 1);     //       +  dS U_K
+        mma_ts(tbase + kAccdO, aPF, dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
+        if (c == 1) mma_commit(&sm.kv_empty[s]);
       };
       bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
       tc_fence_after();
@@ -244,10 +273,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (ok) issue_scores(t);
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_outputs(t);
+        issue_outputs(t, 0);
+        ok = mbar_wait(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t, 1);
         if (t + 2 < T) {
           ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
@@ -276,7 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int t = 2 * u + wg;
       if (t >= T) break;
       // tcgen05.ld/st are warp-collective: take the decision warp-uniformly.
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
+      ok = mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
       if (!ok) break;
       tc_fence_after();
       const int col0 = t * BN;
@@ -285,15 +318,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > N) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(N - 1, gr) : N - 1;
       if (masked) {
-        p1_chunk<true, 0>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
-        p1_chunk<true, 1>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_tile<true>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], col0, jmax, c1, Lr2, Dr, tau,
+                      a_acc, e_acc);
       } else {
-        p1_chunk<false, 0>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
-        p1_chunk<false, 1>(sc, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_tile<false>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], col0, jmax, c1, Lr2, Dr,
+                       tau, a_acc, e_acc);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&sm.op_ready[wg]);
     }
 
     // Epilogue: combine the two warpgroups' row sums, then the affine
@@ -303,8 +333,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     named_bar_sync(1, 256);
     const float al = sm.part_a[0][r] + sm.part_a[1][r];
     const float Ei = (sm.part_e[0][r] + sm.part_e[1][r]) - al * Dr;
-    ok = __all_sync(0xffffffffu, mbar_wait(&sm.out_full, 0, abort_flag, err) && ok &&
-                                     !*abort_flag);
+    ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
 #pragma unroll

@@ -46,7 +46,7 @@ struct Smem2 {
   uint64_t st_empty[NST];
   uint64_t a_ready;
   uint64_t sc_full[2];
-  uint64_t op_ready[2];
+  uint64_t op_ready[2][2];  // [buffer][chunk]: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -101,14 +101,10 @@ __device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16*
 // with the row scalars of the streamed query rows form dS, d~S and W and
 // write them as bf16 A operands over consumed columns.
 template <bool MASKED, int C>
-__device__ __forceinline__ void p2_chunk(uint32_t sc, const float4* scal, int ibase, int gj,
-                                         float c1, float tau) {
-  uint32_t s[16], dp[16], f[16], g[16];
-  tmem_ld16(sc + kColS + 16 * C, s);
-  tmem_ld16(sc + kColdP + 16 * C, dp);
-  tmem_ld16(sc + kColF + 16 * C, f);
-  tmem_ld16(sc + kColG + 16 * C, g);
-  tmem_wait_ld();
+__device__ __forceinline__ void p2_chunk(uint32_t sc, const uint32_t (&s)[16],
+                                         const uint32_t (&dp)[16], const uint32_t (&f)[16],
+                                         const uint32_t (&g)[16], const float4* scal, int ibase,
+                                         int gj, float c1, float tau) {
   uint32_t odS[8], odSt[8], oW[8];
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
@@ -135,6 +131,32 @@ __device__ __forceinline__ void p2_chunk(uint32_t sc, const float4* scal, int ib
   tmem_st8(sc + slot_W(C), oW);
 }
 
+// One 32-column tile, one key row per thread; the same chunked hand-off to
+// the MMA issuer as in pass 1.
+template <bool MASKED>
+__device__ __forceinline__ void p2_tile(uint32_t sc, uint64_t* ready0, uint64_t* ready1,
+                                        const float4* scal, int ibase, int gj, float c1,
+                                        float tau) {
+  uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
+  tmem_ld16(sc + kColS, s0);
+  tmem_ld16(sc + kColdP, dp0);
+  tmem_ld16(sc + kColF, f0);
+  tmem_ld16(sc + kColG, g0);
+  tmem_ld16(sc + kColS + 16, s1);
+  tmem_ld16(sc + kColdP + 16, dp1);
+  tmem_ld16(sc + kColF + 16, f1);
+  tmem_ld16(sc + kColG + 16, g1);
+  tmem_wait_ld();
+  p2_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, scal, ibase, gj, c1, tau);
+  tmem_wait_st();
+  tc_fence_before();
+  warp_arrive(ready0);
+  p2_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, scal, ibase, gj, c1, tau);
+  tmem_wait_st();
+  tc_fence_before();
+  warp_arrive(ready1);
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_kernel(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
                     const __nv_bfloat16* __restrict__ UK, const __nv_bfloat16* __restrict__ UV,
@@ -158,14 +180,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.a_ready, 256);
+    mbar_init(&sm.a_ready, 8);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.st_full[s], 1);
       mbar_init(&sm.st_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.op_ready[b], 128);
+      mbar_init(&sm.op_ready[b][0], 4);
+      mbar_init(&sm.op_ready[b][1], 4);
     }
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
@@ -219,19 +242,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit(&sm.sc_full[t & 1]);
       };
-      auto issue_outputs = [&](int t) {
+      auto issue_outputs = [&](int t, int c) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 3 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
-          const uint32_t acc = (t > 0 || c > 0);
-          mma_ts(tbase + kAccK, sc + slot_dSt(c), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
-          mma_ts(tbase + kAccK, sc + slot_dS(c), dUQ0 + so + o, idO, 1);    //     +  dS^T U_Q
-          mma_ts(tbase + kAccV, sc + slot_W(c), ddO0 + so + o, idO, acc);   // d~V += W^T dO
-        }
-        mma_commit(&sm.st_empty[s]);
+        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
+        const uint32_t acc = (t > 0 || c > 0);
+        mma_ts(tbase + kAccK, sc + (c ? slot_dSt(1) : slot_dSt(0)), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
+        mma_ts(tbase + kAccK, sc + (c ? slot_dS(1) : slot_dS(0)), dUQ0 + so + o, idO, 1);     //     +  dS^T U_Q
+        mma_ts(tbase + kAccV, sc + (c ? slot_W(1) : slot_W(0)), ddO0 + so + o, idO, acc);     // d~V += W^T dO
+        if (c == 1) mma_commit(&sm.st_empty[s]);
       };
       bool ok = mbar_wait(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
       tc_fence_after();
@@ -241,10 +261,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (ok) issue_scores(t);
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_outputs(t);
+        issue_outputs(t, 0);
+        ok = mbar_wait(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t, 1);
         if (t + 2 < T) {
           ok = mbar_wait(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
@@ -280,7 +304,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sm.a_ready);
+      warp_arrive(&sm.a_ready);
     }
 
     for (int u = 0;; ++u) {
@@ -301,7 +325,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Warp-uniform decision (tcgen05.ld/st are warp-collective); after a
       // failed wait keep looping so every thread passes the same named
       // barriers, but skip the work.
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
+      ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
       if (!ok) continue;
       tc_fence_after();
       // Causal: queries i < j (this thread's key row) get P = 0; only the
@@ -309,19 +333,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // carry L = +inf, so their P is 0 on both paths.
       const int ibase = (t + t0) * BN;
       if (causal && ibase < j0 + BM) {
-        p2_chunk<true, 0>(sc, scal, ibase, gj, c1, tau);
-        p2_chunk<true, 1>(sc, scal, ibase, gj, c1, tau);
+        p2_tile<true>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], scal, ibase, gj, c1, tau);
       } else {
-        p2_chunk<false, 0>(sc, scal, ibase, gj, c1, tau);
-        p2_chunk<false, 1>(sc, scal, ibase, gj, c1, tau);
+        p2_tile<false>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], scal, ibase, gj, c1, tau);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&sm.op_ready[wg]);
     }
 
-    ok = __all_sync(0xffffffffu, mbar_wait(&sm.out_full, 0, abort_flag, err) && ok &&
-                                     !*abort_flag);
+    ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
 #pragma unroll

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.op_ready[b], 128);
+      mbar_init(&sm.op_ready[b], 4);  // one arrive per elementwise warp
     }
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (t >= T2) break;
       const bool phase_b = t >= T;
       if (phase_b && !have_L) combine();
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&sm.sc_full[wg], u & 1, abort_flag, err));
+      ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
       if (ok) {
         tc_fence_after();
         const int col0 = (phase_b ? t - T : t) * BN;
@@ -224,13 +224,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (phase_b) tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&sm.op_ready[wg]);
+        warp_arrive(&sm.op_ready[wg]);
       }
     }
     if (!have_L) combine();  // a warpgroup with no phase-B tile (T = 1)
 
-    ok = __all_sync(0xffffffffu, mbar_wait(&sm.out_full, 0, abort_flag, err) && ok &&
-                                     !*abort_flag);
+    ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     float dpart = 0.f;
 #pragma unroll
