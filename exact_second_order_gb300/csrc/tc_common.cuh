@@ -169,6 +169,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// One lane of a fully active warp (the lowest, so always the same lane):
+// the MMA warp runs its issue loop on all 32 lanes, which keeps addresses and
+// descriptors warp-uniform, and lets this lane issue each tcgen05 op.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n.reg .b32 rx;\n.reg .pred px;\nelect.sync rx|px, %1;\n@px mov.s32 %0, 1;\n}\n"
+      : "+r"(pred)
+      : "r"(0xffffffffu));
+  return pred != 0;
+}
+
 // Arrive once on `bar` when every MMA this thread issued so far has finished.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
