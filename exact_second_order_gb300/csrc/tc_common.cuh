@@ -64,25 +64,29 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // up at once, so every thread still reaches the teardown (TMEM release).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err) {
-  // The clock and the abort flag are read once per 256 polls, so a phase
-  // that completes is seen at the next poll.
-  uint64_t t0 = 0;
+// Slow path of mbar_wait, kept out of line so that the common case (the
+// phase has already completed) is a single try_wait.  The clock and the
+// abort flag are read once per 64 polls.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag, unsigned int* err) {
+  const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    const uint64_t now = global_timer_ns();
-    if (t0 == 0) {
-      t0 = now;
-    } else if (now - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
       atomicExch(err, 1u);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
 // One lane of the warp waits; the result is shared with the whole warp so
