@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (one thread) ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    {
       constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);       // N = 32, B K-major
       constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);   // N = 64, B K-major
       constexpr uint32_t idO64 = idesc_bf16(BM, DH, true);        // N = 64, B MN-major
@@ -241,11 +241,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t o = 2 * kk;  // 32 bytes >> 4
           const uint32_t acc = kk > 0;
-          mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);  // [S | F'] = Q [K; U_K]^T
-          mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);   // F' += U_Q K^T
-          mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
+          if (elect_one()) mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);  // [S | F'] = Q [K; U_K]^T
+          if (elect_one()) mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);   // F' += U_Q K^T
+          if (elect_one()) mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
         }
-        mma_commit(&sm.sc_full[t & 1]);
+        if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
       };
       auto issue_outputs = [&](int t, int c) {
         const int s = t % NST;
@@ -258,37 +258,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t aPdPt = sc + (c ? slot_PdPt(1) : slot_PdPt(0));
         const uint32_t adS = sc + (c ? slot_dS(1) : slot_dS(0));
         const uint32_t aPF = sc + (c ? slot_PF(1) : slot_PF(0));
-        mma_ts(tbase + kAccB, aP, dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
-        mma_ts(tbase + kAccR, aPdP, dK0 + so + o, idO64, acc);   // R += (P o dP) K
-        mma_ts(tbase + kAccW, aPdPt, dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
-        mma_ts(tbase + kAccW, adS, dUK0 + so + o, idO64, 1);     //       +  dS U_K
-        mma_ts(tbase + kAccdO, aPF, dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
-        if (c == 1) mma_commit(&sm.kv_empty[s]);
+        if (elect_one()) mma_ts(tbase + kAccB, aP, dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
+        if (elect_one()) mma_ts(tbase + kAccR, aPdP, dK0 + so + o, idO64, acc);   // R += (P o dP) K
+        if (elect_one()) mma_ts(tbase + kAccW, aPdPt, dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
+        if (elect_one()) mma_ts(tbase + kAccW, adS, dUK0 + so + o, idO64, 1);     //       +  dS U_K
+        if (elect_one()) mma_ts(tbase + kAccdO, aPF, dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
+        if (c == 1 && elect_one()) mma_commit(&sm.kv_empty[s]);
       };
-      bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
+      bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
       tc_fence_after();
       for (int t = 0; ok && t < 2 && t < T; ++t) {
-        ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
         tc_fence_after();
         if (ok) issue_scores(t);
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t, 0);
-        ok = mbar_wait(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t, 1);
         if (t + 2 < T) {
-          ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           issue_scores(t + 2);
         }
       }
-      mma_commit(&sm.out_full);  // every MMA issued above has finished
+      if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
     }
   } else {
     // ---------------- elementwise warpgroups + epilogue ----------------

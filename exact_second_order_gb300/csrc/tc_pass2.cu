@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         drain_wait(&sm.st_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer: one thread
+    {  // MMA issuer: whole warp, one elected lane issues
       constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
       constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
       constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 64, B MN-major
@@ -235,12 +235,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint64_t o = 2 * kk;       // 32 bytes >> 4 along K in the B tiles
           const uint32_t ao = 8 * kk;      // 16 bf16 = 8 TMEM columns along K in A
           const uint32_t acc = kk > 0;
-          mma_ts(sc + kColS, tbase + kAK + ao, dQ0 + so + o, idS64, acc);   // [S^T | F'^T] = K [Q; U_Q]^T
-          mma_ts(sc + kColF, tbase + kAUK + ao, dQ0 + so + o, idS32, 1);    // F'^T += U_K Q^T
-          mma_ts(sc + kColdP, tbase + kAV + ao, ddO0 + so + o, idS32, acc); // dP^T = V dO^T
-          mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
+          if (elect_one()) mma_ts(sc + kColS, tbase + kAK + ao, dQ0 + so + o, idS64, acc);   // [S^T | F'^T] = K [Q; U_Q]^T
+          if (elect_one()) mma_ts(sc + kColF, tbase + kAUK + ao, dQ0 + so + o, idS32, 1);    // F'^T += U_K Q^T
+          if (elect_one()) mma_ts(sc + kColdP, tbase + kAV + ao, ddO0 + so + o, idS32, acc); // dP^T = V dO^T
+          if (elect_one()) mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
         }
-        mma_commit(&sm.sc_full[t & 1]);
+        if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
       };
       auto issue_outputs = [&](int t, int c) {
         const int s = t % NST;
@@ -248,35 +248,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
         const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
         const uint32_t acc = (t > 0 || c > 0);
-        mma_ts(tbase + kAccK, sc + (c ? slot_dSt(1) : slot_dSt(0)), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
-        mma_ts(tbase + kAccK, sc + (c ? slot_dS(1) : slot_dS(0)), dUQ0 + so + o, idO, 1);     //     +  dS^T U_Q
-        mma_ts(tbase + kAccV, sc + (c ? slot_W(1) : slot_W(0)), ddO0 + so + o, idO, acc);     // d~V += W^T dO
-        if (c == 1) mma_commit(&sm.st_empty[s]);
+        if (elect_one()) mma_ts(tbase + kAccK, sc + (c ? slot_dSt(1) : slot_dSt(0)), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
+        if (elect_one()) mma_ts(tbase + kAccK, sc + (c ? slot_dS(1) : slot_dS(0)), dUQ0 + so + o, idO, 1);     //     +  dS^T U_Q
+        if (elect_one()) mma_ts(tbase + kAccV, sc + (c ? slot_W(1) : slot_W(0)), ddO0 + so + o, idO, acc);     // d~V += W^T dO
+        if (c == 1 && elect_one()) mma_commit(&sm.st_empty[s]);
       };
-      bool ok = mbar_wait(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
+      bool ok = mbar_wait_warp(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
       tc_fence_after();
       for (int t = 0; ok && t < 2 && t < T; ++t) {
-        ok = mbar_wait(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
         tc_fence_after();
         if (ok) issue_scores(t);
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t, 0);
-        ok = mbar_wait(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t, 1);
         if (t + 2 < T) {
-          ok = mbar_wait(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          ok = mbar_wait_warp(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           issue_scores(t + 2);
         }
       }
-      mma_commit(&sm.out_full);
+      if (elect_one()) mma_commit(&sm.out_full);
     }
   } else {
     const int wg = (warp - 2) >> 2;
