@@ -9,13 +9,12 @@
 //     E = E0 - alpha D,  d~dO = d~dO0 - alpha O,  d~Q = tau (Omega - alpha R - E B)
 // runs once in the epilogue, so every output row is written exactly once.
 //
-// CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 352 threads:
+// CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
 //   warp 0      TMA producer: Q, dO, U_Q blocks once, then K, U_K, V, U_V
 //               tiles of 32 key rows through a 6-stage mbarrier ring;
-//   warp 1      TMEM allocator and issuer of the score GEMMs;
-//   warp 2      issuer of the output GEMMs;
-//   warps 3-6   elementwise warpgroup 0 (tiles 0, 2, 4, ...),
-//   warps 7-10  elementwise warpgroup 1 (tiles 1, 3, 5, ...).
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
+//   warps 2-5   elementwise warpgroup 0 (tiles 0, 2, 4, ...),
+//   warps 6-9   elementwise warpgroup 1 (tiles 1, 3, 5, ...).
 // TMEM (512 columns x 128 lanes, fp32):
 //   [0,64) B = P K   [64,128) d~dO0   [128,192) R = (P o dP) K   [192,256) Omega
 //   [256,384) score buffer 0, [384,512) score buffer 1, each holding
@@ -37,7 +36,7 @@ constexpr int BM = kTcRows;      // 128 query rows per CTA
 constexpr int BN = kTcStream;    // 32 key rows per streamed tile
 constexpr int DH = 64;           // head dim
 constexpr int NST = 6;           // stages of the K/V/U_K/U_V ring
-constexpr int NTHREADS = 352;
+constexpr int NTHREADS = 320;
 constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
 constexpr uint32_t TILE_BYTES = BN * DH * 2;   // 4 KiB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -54,9 +53,7 @@ struct Smem1 {
   uint64_t kv_empty[NST];
   uint64_t sc_full[2];
   uint64_t op_ready[2][2];  // [buffer][chunk]: one arrive per elementwise warp
-  uint64_t buf_free[2];     // output GEMMs of a buffer's tile have completed
   uint64_t out_full;
-  uint64_t sc_done;  // every score GEMM has completed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -179,10 +176,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b][0], 4);
       mbar_init(&sm.op_ready[b][1], 4);
-      mbar_init(&sm.buf_free[b], 1);
     }
     mbar_init(&sm.out_full, 1);
-    mbar_init(&sm.sc_done, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -220,37 +215,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
         drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
     }
-  } else if (warp == 1 || warp == 2) {
-    // ---------------- MMA issuers: warp 1 scores, warp 2 outputs ----------------
-    // Every tcgen05.mma costs the issuing warp tens of cycles whatever its N,
-    // so the two GEMM groups are issued by two warps (each on all 32 lanes,
-    // one elected lane issuing) and their waits overlap the other's issue.
-    // Order between them comes from barriers: a score buffer is refilled only
-    // after the output GEMMs that read its operands have completed (buf_free).
-    constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);       // N = 32, B K-major
-    constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);   // N = 64, B K-major
-    constexpr uint32_t idO64 = idesc_bf16(BM, DH, true);        // N = 64, B MN-major
-    constexpr uint32_t idO128 = idesc_bf16(BM, 2 * DH, true);   // N = 128, B MN-major
-    // Descriptors of the resident blocks and of stage 0; a k-step adds
-    // 32 bytes (16 bf16 inside the swizzled row) and a stage adds
-    // 4 * TILE_BYTES to the start-address field (address >> 4).
-    const uint32_t kv0 = smem_u32(sm.kv[0][0]);
-    const uint64_t dK0 = smem_desc_sw128(kv0, 16, 1024);                   // K (and K;U_K)
-    const uint64_t dV0 = smem_desc_sw128(kv0 + 2 * TILE_BYTES, 16, 1024);  // V (and V;U_V)
-    bool ok = true;
-    if (warp == 1) {
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    {
+      constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);       // N = 32, B K-major
+      constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);   // N = 64, B K-major
+      constexpr uint32_t idO64 = idesc_bf16(BM, DH, true);        // N = 64, B MN-major
+      constexpr uint32_t idO128 = idesc_bf16(BM, 2 * DH, true);   // N = 128, B MN-major
+      // Descriptors of the resident blocks and of stage 0; a k-step adds
+      // 32 bytes (16 bf16 inside the swizzled row) and a stage adds
+      // 4 * TILE_BYTES to the start-address field (address >> 4).
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
       const uint64_t ddo0 = smem_desc_sw128(smem_u32(sm.dO), 16, 1024);
       const uint64_t duq0 = smem_desc_sw128(smem_u32(sm.uq), 16, 1024);
-      ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
-      for (int t = 0; ok && t < T; ++t) {
-        if (t >= 2) {  // the output GEMMs of tile t - 2 have read this buffer
-          ok = mbar_wait_warp(&sm.buf_free[t & 1], ((t >> 1) - 1) & 1, abort_flag, err);
-          if (!ok) break;
-        }
-        ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
+      const uint32_t kv0 = smem_u32(sm.kv[0][0]);
+      const uint64_t dK0 = smem_desc_sw128(kv0, 16, 1024);                   // K (and K;U_K)
+      const uint64_t dV0 = smem_desc_sw128(kv0 + 2 * TILE_BYTES, 16, 1024);  // V (and V;U_V)
+      const uint64_t dUK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);
+      // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
+      const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
+      auto issue_scores = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
 #pragma unroll
@@ -262,40 +246,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (elect_one()) mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
         }
         if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
-      }
-      if (elect_one()) mma_commit(&sm.sc_done);  // no score MMA in flight at teardown
-    } else {
-      const uint64_t dUK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);
-      // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
-      const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
-      for (int t = 0; ok && t < T; ++t) {
+      };
+      auto issue_outputs = [&](int t, int c) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          ok = mbar_wait_warp(&sm.op_ready[t & 1][c], (t >> 1) & 1, abort_flag, err);
+        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
+        const uint32_t acc = (t > 0 || c > 0);
+        const uint32_t aP = sc + (c ? slot_P(1) : slot_P(0));
+        const uint32_t aPdP = sc + (c ? slot_PdP(1) : slot_PdP(0));
+        const uint32_t aPdPt = sc + (c ? slot_PdPt(1) : slot_PdPt(0));
+        const uint32_t adS = sc + (c ? slot_dS(1) : slot_dS(0));
+        const uint32_t aPF = sc + (c ? slot_PF(1) : slot_PF(0));
+        if (elect_one()) mma_ts(tbase + kAccB, aP, dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
+        if (elect_one()) mma_ts(tbase + kAccR, aPdP, dK0 + so + o, idO64, acc);   // R += (P o dP) K
+        if (elect_one()) mma_ts(tbase + kAccW, aPdPt, dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
+        if (elect_one()) mma_ts(tbase + kAccW, adS, dUK0 + so + o, idO64, 1);     //       +  dS U_K
+        if (elect_one()) mma_ts(tbase + kAccdO, aPF, dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
+        if (c == 1 && elect_one()) mma_commit(&sm.kv_empty[s]);
+      };
+      bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
+      tc_fence_after();
+      for (int t = 0; ok && t < 2 && t < T; ++t) {
+        ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+        tc_fence_after();
+        if (ok) issue_scores(t);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t, 0);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t, 1);
+        if (t + 2 < T) {
+          ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
-          const uint32_t acc = (t > 0 || c > 0);
-          if (elect_one()) mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
-          if (elect_one()) mma_ts(tbase + kAccR, sc + slot_PdP(c), dK0 + so + o, idO64, acc);   // R += (P o dP) K
-          if (elect_one()) mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
-          if (elect_one()) mma_ts(tbase + kAccW, sc + slot_dS(c), dUK0 + so + o, idO64, 1);     //       +  dS U_K
-          if (elect_one()) mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
+          issue_scores(t + 2);
         }
-        if (!ok) break;
-        // Score GEMMs of tile t finished before its operands existed, so
-        // these commits cover every reader of the stage and of the buffer.
-        if (elect_one()) mma_commit(&sm.kv_empty[s]);
-        if (elect_one()) mma_commit(&sm.buf_free[t & 1]);
       }
-      if (elect_one()) mma_commit(&sm.out_full);  // every output MMA has finished
+      if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
     }
   } else {
     // ---------------- elementwise warpgroups + epilogue ----------------
-    const int wg = (warp - 3) >> 2;      // 0 or 1
+    const int wg = (warp - 2) >> 2;      // 0 or 1
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;      // row inside the block = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -337,7 +334,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float al = sm.part_a[0][r] + sm.part_a[1][r];
     const float Ei = (sm.part_e[0][r] + sm.part_e[1][r]) - al * Dr;
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
-    ok = mbar_wait_warp(&sm.sc_done, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;

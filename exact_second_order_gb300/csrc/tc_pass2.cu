@@ -13,12 +13,11 @@
 //     d~K_j = tau sum_i (d~S_ij Q_i + dS_ij U_Q,i),   d~V_j = sum_i W_ij dO_i
 // (F = tau (U_Q K^T + Q U_K^T), G = dO U_V^T; the same chain rule as pass 1).
 //
-// CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 352 threads:
+// CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
 //   warp 0      TMA producer: Q, U_Q, dO tiles of 32 query rows through a
 //               10-stage mbarrier ring;
-//   warp 1      TMEM allocator and issuer of the score GEMMs;
-//   warp 2      issuer of the output GEMMs;
-//   warps 3-6 / 7-10  elementwise warpgroups 0 / 1 (even / odd tiles); at the
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
+//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1 (even / odd tiles); at the
 //               start they also copy their key row of K, U_K / V, U_V into TMEM.
 // TMEM: [0,64) d~K accumulator, [64,128) d~V accumulator, [128,256) the
 // resident K | V | U_K | U_V block as bf16 (the A operands of every score
@@ -36,7 +35,7 @@ constexpr int BM = kTcRows;    // 128 key rows per CTA
 constexpr int BN = kTcStream;  // 32 query rows per streamed tile
 constexpr int DH = 64;
 constexpr int NST = 10;
-constexpr int NTHREADS = 352;
+constexpr int NTHREADS = 320;
 constexpr uint32_t TILE_BYTES = BN * DH * 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -48,8 +47,6 @@ struct Smem2 {
   uint64_t a_ready;
   uint64_t sc_full[2];
   uint64_t op_ready[2][2];  // [buffer][chunk]: one arrive per elementwise warp
-  uint64_t buf_free[2];     // output GEMMs of a buffer's tile have completed
-  uint64_t sc_done;         // every score GEMM has completed
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -192,10 +189,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b][0], 4);
       mbar_init(&sm.op_ready[b][1], 4);
-      mbar_init(&sm.buf_free[b], 1);
     }
     mbar_init(&sm.out_full, 1);
-    mbar_init(&sm.sc_done, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -223,26 +218,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
         drain_wait(&sm.st_full[t % NST], (t / NST) & 1);
     }
-  } else if (warp == 1 || warp == 2) {
-    // MMA issuers (all 32 lanes, one elected lane issues): warp 1 the score
-    // GEMMs, warp 2 the output GEMMs; ordered through barriers (see pass 1).
-    constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
-    constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
-    constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 64, B MN-major
-    const uint32_t st0 = smem_u32(sm.st[0][0]);
-    const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
-    const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
-    bool ok = true;
-    if (warp == 1) {
-      ok = mbar_wait_warp(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
-      for (int t = 0; ok && t < T; ++t) {
-        if (t >= 2) {  // the output GEMMs of tile t - 2 have read this buffer
-          ok = mbar_wait_warp(&sm.buf_free[t & 1], ((t >> 1) - 1) & 1, abort_flag, err);
-          if (!ok) break;
-        }
-        ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
+  } else if (warp == 1) {
+    {  // MMA issuer: whole warp, one elected lane issues
+      constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
+      constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
+      constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 64, B MN-major
+      const uint32_t st0 = smem_u32(sm.st[0][0]);
+      const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
+      const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
+      const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
+      auto issue_scores = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
 #pragma unroll
@@ -256,33 +241,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (elect_one()) mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
         }
         if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
-      }
-      if (elect_one()) mma_commit(&sm.sc_done);  // no score MMA in flight at teardown
-    } else {
-      const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
-      for (int t = 0; ok && t < T; ++t) {
+      };
+      auto issue_outputs = [&](int t, int c) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 3 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          ok = mbar_wait_warp(&sm.op_ready[t & 1][c], (t >> 1) & 1, abort_flag, err);
+        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
+        const uint32_t acc = (t > 0 || c > 0);
+        if (elect_one()) mma_ts(tbase + kAccK, sc + (c ? slot_dSt(1) : slot_dSt(0)), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
+        if (elect_one()) mma_ts(tbase + kAccK, sc + (c ? slot_dS(1) : slot_dS(0)), dUQ0 + so + o, idO, 1);     //     +  dS^T U_Q
+        if (elect_one()) mma_ts(tbase + kAccV, sc + (c ? slot_W(1) : slot_W(0)), ddO0 + so + o, idO, acc);     // d~V += W^T dO
+        if (c == 1 && elect_one()) mma_commit(&sm.st_empty[s]);
+      };
+      bool ok = mbar_wait_warp(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
+      tc_fence_after();
+      for (int t = 0; ok && t < 2 && t < T; ++t) {
+        ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+        tc_fence_after();
+        if (ok) issue_scores(t);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t, 0);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t, 1);
+        if (t + 2 < T) {
+          ok = mbar_wait_warp(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
-          const uint32_t acc = (t > 0 || c > 0);
-          if (elect_one()) mma_ts(tbase + kAccK, sc + slot_dSt(c), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
-          if (elect_one()) mma_ts(tbase + kAccK, sc + slot_dS(c), dUQ0 + so + o, idO, 1);    //     +  dS^T U_Q
-          if (elect_one()) mma_ts(tbase + kAccV, sc + slot_W(c), ddO0 + so + o, idO, acc);   // d~V += W^T dO
+          issue_scores(t + 2);
         }
-        if (!ok) break;
-        if (elect_one()) mma_commit(&sm.st_empty[s]);
-        if (elect_one()) mma_commit(&sm.buf_free[t & 1]);
       }
       if (elect_one()) mma_commit(&sm.out_full);
     }
   } else {
-    const int wg = (warp - 3) >> 2;
+    const int wg = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // key row inside the block = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -343,7 +340,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
-    ok = mbar_wait_warp(&sm.sc_done, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
