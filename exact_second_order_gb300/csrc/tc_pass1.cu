@@ -52,7 +52,7 @@ struct Smem1 {
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
   uint64_t sc_full[2];
-  uint64_t op_ready[2][2];  // [buffer][chunk]: one arrive per elementwise warp
+  uint64_t op_ready[2];  // per buffer: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -118,14 +118,12 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
 }
 
 // One 32-column tile, one row per thread: read all of S, F', dP, G (both
-// 16-column chunks) with a single wait, then form the bf16 A operands of
-// the output GEMMs chunk by chunk.  Each chunk is handed to the MMA issuer
-// as soon as it is in TMEM, so the output MMAs of chunk 0 overlap the
-// arithmetic of chunk 1.
+// 16-column chunks) with a single wait, form the bf16 A operands of the
+// output GEMMs, and hand the tile to the MMA issuer once they are in TMEM.
 template <bool MASKED>
-__device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready0, uint64_t* ready1, int col0,
-                                        int jmax, float c1, float Lr2, float Dr, float tau,
-                                        float& a_acc, float& e_acc) {
+__device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready, int col0, int jmax,
+                                        float c1, float Lr2, float Dr, float tau, float& a_acc,
+                                        float& e_acc) {
   uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
   tmem_ld16(sc + kColS, s0);
   tmem_ld16(sc + kColdP, dp0);
@@ -137,13 +135,10 @@ __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready0, uint64_t*
   tmem_ld16(sc + kColG + 16, g1);
   tmem_wait_ld();
   p1_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
-  tmem_wait_st();
-  tc_fence_before();
-  warp_arrive(ready0);
   p1_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
   tmem_wait_st();
   tc_fence_before();
-  warp_arrive(ready1);
+  warp_arrive(ready);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -174,8 +169,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.op_ready[b][0], 4);
-      mbar_init(&sm.op_ready[b][1], 4);
+      mbar_init(&sm.op_ready[b], 4);
     }
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
@@ -234,36 +228,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t dUK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);
       // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
       const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
+      // One elected lane issues each group of MMAs as one straight block.
       auto issue_scores = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint64_t o = 2 * kk;  // 32 bytes >> 4
-          const uint32_t acc = kk > 0;
-          if (elect_one()) mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);  // [S | F'] = Q [K; U_K]^T
-          if (elect_one()) mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);   // F' += U_Q K^T
-          if (elect_one()) mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint64_t o = 2 * kk;  // 32 bytes >> 4
+            const uint32_t acc = kk > 0;
+            mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);   // [S | F'] = Q [K; U_K]^T
+            mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);    // F' += U_Q K^T
+            mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc); // [dP | G] = dO [V; U_V]^T
+          }
+          mma_commit(&sm.sc_full[t & 1]);
         }
-        if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
+        __syncwarp();
       };
-      auto issue_outputs = [&](int t, int c) {
+      auto issue_outputs = [&](int t) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
-        const uint32_t acc = (t > 0 || c > 0);
-        const uint32_t aP = sc + (c ? slot_P(1) : slot_P(0));
-        const uint32_t aPdP = sc + (c ? slot_PdP(1) : slot_PdP(0));
-        const uint32_t aPdPt = sc + (c ? slot_PdPt(1) : slot_PdPt(0));
-        const uint32_t adS = sc + (c ? slot_dS(1) : slot_dS(0));
-        const uint32_t aPF = sc + (c ? slot_PF(1) : slot_PF(0));
-        if (elect_one()) mma_ts(tbase + kAccB, aP, dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
-        if (elect_one()) mma_ts(tbase + kAccR, aPdP, dK0 + so + o, idO64, acc);   // R += (P o dP) K
-        if (elect_one()) mma_ts(tbase + kAccW, aPdPt, dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
-        if (elect_one()) mma_ts(tbase + kAccW, adS, dUK0 + so + o, idO64, 1);     //       +  dS U_K
-        if (elect_one()) mma_ts(tbase + kAccdO, aPF, dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
-        if (c == 1 && elect_one()) mma_commit(&sm.kv_empty[s]);
+        if (elect_one()) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
+            const uint32_t acc = (t > 0 || c > 0);
+            mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
+            mma_ts(tbase + kAccR, sc + slot_PdP(c), dK0 + so + o, idO64, acc);   // R += (P o dP) K
+            mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
+            mma_ts(tbase + kAccW, sc + slot_dS(c), dUK0 + so + o, idO64, 1);     //       +  dS U_K
+            mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
+          }
+          mma_commit(&sm.kv_empty[s]);
+        }
+        __syncwarp();
       };
       bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
       tc_fence_after();
@@ -273,14 +272,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (ok) issue_scores(t);
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait_warp(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_outputs(t, 0);
-        ok = mbar_wait_warp(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
-        issue_outputs(t, 1);
+        issue_outputs(t);
         if (t + 2 < T) {
           ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
@@ -318,11 +313,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > N) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(N - 1, gr) : N - 1;
       if (masked) {
-        p1_tile<true>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], col0, jmax, c1, Lr2, Dr, tau,
-                      a_acc, e_acc);
+        p1_tile<true>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
       } else {
-        p1_tile<false>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], col0, jmax, c1, Lr2, Dr,
-                       tau, a_acc, e_acc);
+        p1_tile<false>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
       }
     }
 

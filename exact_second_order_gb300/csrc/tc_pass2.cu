@@ -46,7 +46,7 @@ struct Smem2 {
   uint64_t st_empty[NST];
   uint64_t a_ready;
   uint64_t sc_full[2];
-  uint64_t op_ready[2][2];  // [buffer][chunk]: one arrive per elementwise warp
+  uint64_t op_ready[2];  // per buffer: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -131,12 +131,10 @@ __device__ __forceinline__ void p2_chunk(uint32_t sc, const uint32_t (&s)[16],
   tmem_st8(sc + slot_W(C), oW);
 }
 
-// One 32-column tile, one key row per thread; the same chunked hand-off to
-// the MMA issuer as in pass 1.
+// One 32-column tile, one key row per thread (the same hand-off as pass 1).
 template <bool MASKED>
-__device__ __forceinline__ void p2_tile(uint32_t sc, uint64_t* ready0, uint64_t* ready1,
-                                        const float4* scal, int ibase, int gj, float c1,
-                                        float tau) {
+__device__ __forceinline__ void p2_tile(uint32_t sc, uint64_t* ready, const float4* scal,
+                                        int ibase, int gj, float c1, float tau) {
   uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
   tmem_ld16(sc + kColS, s0);
   tmem_ld16(sc + kColdP, dp0);
@@ -148,16 +146,13 @@ __device__ __forceinline__ void p2_tile(uint32_t sc, uint64_t* ready0, uint64_t*
   tmem_ld16(sc + kColG + 16, g1);
   tmem_wait_ld();
   p2_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, scal, ibase, gj, c1, tau);
-  tmem_wait_st();
-  tc_fence_before();
-  warp_arrive(ready0);
   p2_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, scal, ibase, gj, c1, tau);
   tmem_wait_st();
   tc_fence_before();
-  warp_arrive(ready1);
+  warp_arrive(ready);
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __maxnreg__(200)
     tc_pass2_kernel(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
                     const __nv_bfloat16* __restrict__ UK, const __nv_bfloat16* __restrict__ UV,
                     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
@@ -187,8 +182,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.op_ready[b][0], 4);
-      mbar_init(&sm.op_ready[b][1], 4);
+      mbar_init(&sm.op_ready[b], 4);
     }
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
@@ -227,31 +221,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
       const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
       const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
+      // One elected lane issues each group of MMAs as one straight block.
       auto issue_scores = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint64_t o = 2 * kk;       // 32 bytes >> 4 along K in the B tiles
-          const uint32_t ao = 8 * kk;      // 16 bf16 = 8 TMEM columns along K in A
-          const uint32_t acc = kk > 0;
-          if (elect_one()) mma_ts(sc + kColS, tbase + kAK + ao, dQ0 + so + o, idS64, acc);   // [S^T | F'^T] = K [Q; U_Q]^T
-          if (elect_one()) mma_ts(sc + kColF, tbase + kAUK + ao, dQ0 + so + o, idS32, 1);    // F'^T += U_K Q^T
-          if (elect_one()) mma_ts(sc + kColdP, tbase + kAV + ao, ddO0 + so + o, idS32, acc); // dP^T = V dO^T
-          if (elect_one()) mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint64_t o = 2 * kk;       // 32 bytes >> 4 along K in the B tiles
+            const uint32_t ao = 8 * kk;      // 16 bf16 = 8 TMEM columns along K in A
+            const uint32_t acc = kk > 0;
+            mma_ts(sc + kColS, tbase + kAK + ao, dQ0 + so + o, idS64, acc);   // [S^T | F'^T] = K [Q; U_Q]^T
+            mma_ts(sc + kColF, tbase + kAUK + ao, dQ0 + so + o, idS32, 1);    // F'^T += U_K Q^T
+            mma_ts(sc + kColdP, tbase + kAV + ao, ddO0 + so + o, idS32, acc); // dP^T = V dO^T
+            mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
+          }
+          mma_commit(&sm.sc_full[t & 1]);
         }
-        if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
+        __syncwarp();
       };
-      auto issue_outputs = [&](int t, int c) {
+      auto issue_outputs = [&](int t) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 3 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
-        const uint32_t acc = (t > 0 || c > 0);
-        if (elect_one()) mma_ts(tbase + kAccK, sc + (c ? slot_dSt(1) : slot_dSt(0)), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
-        if (elect_one()) mma_ts(tbase + kAccK, sc + (c ? slot_dS(1) : slot_dS(0)), dUQ0 + so + o, idO, 1);     //     +  dS^T U_Q
-        if (elect_one()) mma_ts(tbase + kAccV, sc + (c ? slot_W(1) : slot_W(0)), ddO0 + so + o, idO, acc);     // d~V += W^T dO
-        if (c == 1 && elect_one()) mma_commit(&sm.st_empty[s]);
+        if (elect_one()) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
+            const uint32_t acc = (t > 0 || c > 0);
+            mma_ts(tbase + kAccK, sc + slot_dSt(c), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
+            mma_ts(tbase + kAccK, sc + slot_dS(c), dUQ0 + so + o, idO, 1);    //     +  dS^T U_Q
+            mma_ts(tbase + kAccV, sc + slot_W(c), ddO0 + so + o, idO, acc);   // d~V += W^T dO
+          }
+          mma_commit(&sm.st_empty[s]);
+        }
+        __syncwarp();
       };
       bool ok = mbar_wait_warp(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
       tc_fence_after();
@@ -261,14 +265,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (ok) issue_scores(t);
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait_warp(&sm.op_ready[t & 1][0], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_outputs(t, 0);
-        ok = mbar_wait_warp(&sm.op_ready[t & 1][1], (t >> 1) & 1, abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
-        issue_outputs(t, 1);
+        issue_outputs(t);
         if (t + 2 < T) {
           ok = mbar_wait_warp(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
           if (!ok) break;
@@ -333,9 +333,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // carry L = +inf, so their P is 0 on both paths.
       const int ibase = (t + t0) * BN;
       if (causal && ibase < j0 + BM) {
-        p2_tile<true>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], scal, ibase, gj, c1, tau);
+        p2_tile<true>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
       } else {
-        p2_tile<false>(sc, &sm.op_ready[wg][0], &sm.op_ready[wg][1], scal, ibase, gj, c1, tau);
+        p2_tile<false>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
       }
     }
 
