@@ -54,6 +54,30 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def reduce_max(x: float, world: int, device="cpu") -> float:
+    """Largest value over the ranks (the job is as slow as its slowest rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processes its own units (weak
+    scaling, no data exchange), divided by the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
+
+
+def rank_workload(w, rank: int):
+    """Rank r processes its own seeded copy of the workload (independent
+    (batch, head) units, the same shape on every rank)."""
+    from dataclasses import replace
+    return replace(w, seed=w.seed + rank)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -200,7 +224,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    x = make_inputs(w)
+    x = make_inputs(rank_workload(w, rank))
     dev = {k: v.cuda() for k, v in x.items()}
     O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
     out = fb.alloc_bob_outputs(dev["Q"])
@@ -243,16 +267,13 @@ def main():
     total_ms = evs[0][0].elapsed_time(evs[-1][2])
     p1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     p2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
     heads = w.B * w.H
     # one N x N x d GEMM per (batch, head); half of it under the causal mask
     unit_flops = (0.5 if w.causal else 1.0) * 2.0 * w.N * w.N * w.d * heads
     flops = (PASS1_GEMMS + PASS2_GEMMS) * unit_flops
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops, args.steps, world, total_ms)
 
     # end to end: pinned host inputs -> device, the C-ABI call, outputs -> host
     e2e = None
@@ -288,12 +309,8 @@ def main():
             e2e_step()
         t1.record(stream)
         barrier()
-        e_ms = t0.elapsed_time(t1)
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * flops * n_e2e / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
+        e2e = {"value": job_tflops(flops, n_e2e, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / n_e2e, "steps": n_e2e}
 
