@@ -131,28 +131,36 @@ __device__ __forceinline__ void p2_chunk(uint32_t sc, const uint32_t (&s)[16],
   tmem_st8(sc + slot_W(C), oW);
 }
 
-// One 32-column tile, one key row per thread (the same hand-off as pass 1).
+// One 32-column tile, one key row per thread (the same hand-off as pass 1);
+// the two 16-column chunks are read one after the other, which keeps the
+// register count within what 10 warps per SM allow.
 template <bool MASKED>
 __device__ __forceinline__ void p2_tile(uint32_t sc, uint64_t* ready, const float4* scal,
                                         int ibase, int gj, float c1, float tau) {
-  uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
-  tmem_ld16(sc + kColS, s0);
-  tmem_ld16(sc + kColdP, dp0);
-  tmem_ld16(sc + kColF, f0);
-  tmem_ld16(sc + kColG, g0);
-  tmem_ld16(sc + kColS + 16, s1);
-  tmem_ld16(sc + kColdP + 16, dp1);
-  tmem_ld16(sc + kColF + 16, f1);
-  tmem_ld16(sc + kColG + 16, g1);
-  tmem_wait_ld();
-  p2_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, scal, ibase, gj, c1, tau);
-  p2_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, scal, ibase, gj, c1, tau);
+  {
+    uint32_t s0[16], dp0[16], f0[16], g0[16];
+    tmem_ld16(sc + kColS, s0);
+    tmem_ld16(sc + kColdP, dp0);
+    tmem_ld16(sc + kColF, f0);
+    tmem_ld16(sc + kColG, g0);
+    tmem_wait_ld();
+    p2_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, scal, ibase, gj, c1, tau);
+  }
+  {
+    uint32_t s1[16], dp1[16], f1[16], g1[16];
+    tmem_ld16(sc + kColS + 16, s1);
+    tmem_ld16(sc + kColdP + 16, dp1);
+    tmem_ld16(sc + kColF + 16, f1);
+    tmem_ld16(sc + kColG + 16, g1);
+    tmem_wait_ld();
+    p2_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, scal, ibase, gj, c1, tau);
+  }
   tmem_wait_st();
   tc_fence_before();
   warp_arrive(ready);
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_kernel(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
                     const __nv_bfloat16* __restrict__ UK, const __nv_bfloat16* __restrict__ UV,
                     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
