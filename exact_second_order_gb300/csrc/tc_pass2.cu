@@ -315,36 +315,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       warp_arrive(&sm.a_ready);
     }
 
+    // Row scalars of a streamed tile, (L log2 e, D, alpha, E) per query row;
+    // rows past N get L = +inf so that P = exp2(-inf) = 0.
+    auto load_scalars = [&](int t) {
+      const int i = (t + t0) * BN + lane;
+      if (t < T && i < N)
+        return make_float4(L[head + i] * kLog2e, D[head + i], alpha[head + i], E[head + i]);
+      return make_float4(INFINITY, 0.f, 0.f, 0.f);
+    };
+    // The loader warp fetches the scalars one tile ahead into registers, so
+    // their global-memory latency hides behind the current tile.
+    if (loader) sm.scal[wg][0][lane] = load_scalars(wg);
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
       if (t >= T) break;
       float4* scal = sm.scal[wg][u & 1];
-      if (loader) {
-        const int i = (t + t0) * BN + lane;
-        float4 v;
-        if (i < N) {
-          v = make_float4(L[head + i] * kLog2e, D[head + i], alpha[head + i], E[head + i]);
-        } else {
-          v = make_float4(INFINITY, 0.f, 0.f, 0.f);  // P = exp2(-inf) = 0 for rows past N
-        }
-        scal[lane] = v;
-      }
-      named_bar_sync(2 + wg, 128);
+      named_bar_sync(2 + wg, 128);  // scal is written; last tile's readers are done
+      float4 next = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (loader) next = load_scalars(t + 2);
       // Warp-uniform decision (tcgen05.ld/st are warp-collective); after a
       // failed wait keep looping so every thread passes the same named
       // barriers, but skip the work.
       ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
-      if (!ok) continue;
-      tc_fence_after();
-      // Causal: queries i < j (this thread's key row) get P = 0; only the
-      // tiles that overlap the key block take the masked path.  Rows past N
-      // carry L = +inf, so their P is 0 on both paths.
-      const int ibase = (t + t0) * BN;
-      if (causal && ibase < j0 + BM) {
-        p2_tile<true>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
-      } else {
-        p2_tile<false>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
+      if (ok) {
+        tc_fence_after();
+        // Causal: queries i < j (this thread's key row) get P = 0; only the
+        // tiles that overlap the key block take the masked path.  Rows past N
+        // carry L = +inf, so their P is 0 on both paths.
+        const int ibase = (t + t0) * BN;
+        if (causal && ibase < j0 + BM) {
+          p2_tile<true>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
+        } else {
+          p2_tile<false>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
+        }
       }
+      // Every thread passed this iteration's barrier, so nobody still reads
+      // the other buffer.
+      if (loader) sm.scal[wg][(u + 1) & 1][lane] = next;
     }
 
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
