@@ -218,7 +218,7 @@ flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1
   probe.bf16 = in_dtype == FLASHBOB_BF16;
   const bool tc = tc_supported(probe);
   const int br1 = tc ? kTcRows : kSimtTile, bc1 = tc ? kTcStream : kSimtTile;
-  const int bc2 = tc ? kTcRows : kSimtTile, br2 = tc ? kTcStream : kSimtTile;
+  const int bc2 = tc ? kTcRows : kSimtTile, br2 = tc ? kTcStream2 : kSimtTile;
   if (Br1) *Br1 = br1;
   if (Bc1) *Bc1 = bc1;
   if (Br2) *Br2 = br2;

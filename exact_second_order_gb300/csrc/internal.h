@@ -45,7 +45,8 @@ size_t simt_pass2_smem(int d);
 
 // tcgen05 tensor-core kernels (bf16 inputs, d = 64).
 constexpr int kTcRows = 128;    // rows of the resident block (MMA M) in both passes
-constexpr int kTcStream = 32;   // rows of a streamed tile (MMA N of the score GEMMs)
+constexpr int kTcStream = 32;   // rows of a streamed key tile in pass 1 and prep
+constexpr int kTcStream2 = 64;  // rows of a streamed query tile in pass 2
 bool tc_supported(const BobArgs& a);
 bool tc_prep_supported(const PrepArgs& a);
 cudaError_t tc_prep(const PrepArgs& a);

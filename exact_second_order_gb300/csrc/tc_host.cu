@@ -7,7 +7,8 @@ namespace flashbob {
 
 cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps32);
-cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps32);
+cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
+                            const CUtensorMap* maps64);
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && a.d == 64; }
 
@@ -27,12 +28,15 @@ cudaError_t tc_bob(const BobArgs& a) {
     if (e != cudaSuccess) return e;
   }
   if (a.passes & kPass2) {
-    CUtensorMap m32[3];
-    const void* str[3] = {a.Q, a.dO, a.UQ};
+    CUtensorMap m128[4], m64[3];
+    const void* res[4] = {a.K, a.UK, a.V, a.UV};
+    const void* str[3] = {a.Q, a.UQ, a.dO};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16_d64(&m128[i], res[i], BH, a.N, kTcRows);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m32[i], str[i], BH, a.N, kTcStream);
+      e = tc::make_map_bf16_d64(&m64[i], str[i], BH, a.N, kTcStream2);
     if (e != cudaSuccess) return e;
-    e = tc_launch_pass2(a, m32);
+    e = tc_launch_pass2(a, m128, m64);
   }
   return e;
 }

@@ -14,16 +14,22 @@
 // (F = tau (U_Q K^T + Q U_K^T), G = dO U_V^T; the same chain rule as pass 1).
 //
 // CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
-//   warp 0      TMA producer: Q, U_Q, dO tiles of 32 query rows through a
-//               10-stage mbarrier ring;
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
-//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1 (even / odd tiles); at the
-//               start they also copy their key row of K, U_K / V, U_V into TMEM.
-// TMEM: [0,64) d~K accumulator, [64,128) d~V accumulator, [128,256) the
-// resident K | V | U_K | U_V block as bf16 (the A operands of every score
-// GEMM, so shared memory only feeds the 32-row B tiles), [256,384) and
-// [384,512) score buffers S^T | F'^T | dP^T | G^T (32 columns each).
-// K [Q; U_Q]^T gives S^T and half of F'^T in one N = 64 MMA.
+//   warp 0      TMA producer: the resident K, U_K, V, U_V block, then Q, U_Q,
+//               dO tiles of 64 query rows through a 4-stage mbarrier ring;
+//   warp 1      TMEM allocator and MMA issuer (all lanes, one elected lane
+//               issues each group of MMAs);
+//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: query rows 0-31 / 32-63
+//               of every tile (the 16-row K steps 0-1 / 2-3 of its output
+//               GEMMs).
+// Every tcgen05.mma costs the pipe tens of cycles whatever its width, so
+// the tile is 64 query rows wide: the score GEMMs are K [Q; U_Q]^T (N = 128,
+// S^T and half of F'^T), U_K Q^T, V dO^T and U_V dO^T (N = 64 each).
+// TMEM: [0,64) d~K, [64,128) d~V accumulators; [128,384) one score buffer
+// S^T | F'^T | dP^T | G^T (64 columns each); [384,480) the bf16 A operands
+// dS^T, d~S^T, W^T of the output GEMMs.  Because the operands have their own
+// columns, the score buffer is free as soon as both warpgroups have read it
+// into registers, and the score GEMMs of the next tile run while the
+// warpgroups do the arithmetic of this one.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -31,22 +37,26 @@ namespace flashbob {
 namespace {
 using namespace tc;
 
-constexpr int BM = kTcRows;    // 128 key rows per CTA
-constexpr int BN = kTcStream;  // 32 query rows per streamed tile
+constexpr int BM = kTcRows;  // 128 key rows per CTA
+constexpr int BQ = kTcStream2;  // 64 query rows per streamed tile
 constexpr int DH = 64;
-constexpr int NST = 10;
+constexpr int NST = 4;
 constexpr int NTHREADS = 320;
-constexpr uint32_t TILE_BYTES = BN * DH * 2;
+constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
+constexpr uint32_t TILE_BYTES = BQ * DH * 2;   // 8 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Smem2 {
+  alignas(1024) uint8_t kb[4][BLOCK_BYTES];      // K, U_K, V, U_V (resident)
   alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, U_Q, dO (Q|U_Q adjacent)
-  float4 scal[2][2][BN];  // per warpgroup, double-buffered: (L log2 e, D, alpha, E)
+  float4 scal[2][2][32];  // per warpgroup, double-buffered: (L log2 e, D, alpha, E)
+  uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
-  uint64_t a_ready;
-  uint64_t sc_full[2];
-  uint64_t op_ready[2];  // per buffer: one arrive per elementwise warp
+  uint64_t sc_full;   // score GEMMs of a tile have completed
+  uint64_t sc_free;   // both warpgroups have read the score buffer (8 warps)
+  uint64_t op_ready;  // the operands of a tile are in TMEM (8 warps)
+  uint64_t op_free;   // the output GEMMs of a tile have completed
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -54,117 +64,96 @@ struct Smem2 {
 
 // TMEM columns.
 constexpr uint32_t kAccK = 0, kAccV = 64;
-constexpr uint32_t kAK = 128, kAV = 160, kAUK = 192, kAUV = 224;  // 64 bf16 = 32 columns each
-constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;  // inside a score buffer
+constexpr uint32_t kSc = 128;  // score buffer
+constexpr uint32_t kColS = 0, kColF = 64, kColdP = 128, kColG = 192;  // inside the score buffer
+constexpr uint32_t kOp = 384;  // operand area: operand x, K step kk at kOp + 32 x + 8 kk
+constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
 
-// bf16 operand slots inside a score buffer: chunk 0 writes only columns it
-// has read (the first 16 of S^T and F'^T), chunk 1 only columns chunk 0 read.
-__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 40 : 0; }
-__device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return c ? 64 : 8; }
-__device__ __forceinline__ constexpr uint32_t slot_W(int c) { return c ? 72 : 32; }
-
-// 32 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
+__device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
+  return kOp + 32 * x + 8 * kk;
 }
 
-// Copy one 64-element bf16 row (zeros past N) into 32 TMEM columns.
-// `row` is null for rows past N.
-__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16* row) {
-  uint32_t r[32];
-#pragma unroll
-  for (int k = 0; k < 32; ++k) r[k] = 0u;
-  if (row != nullptr) {
-    const uint4* src = reinterpret_cast<const uint4*>(row);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint4 v = src[k];
-      r[4 * k] = v.x;
-      r[4 * k + 1] = v.y;
-      r[4 * k + 2] = v.z;
-      r[4 * k + 3] = v.w;
-    }
-  }
-  tmem_st32(taddr, r);
-}
-
-// One 16-column chunk of a transposed score buffer, one key row per thread:
-// with the row scalars of the streamed query rows form dS, d~S and W and
-// write them as bf16 A operands over consumed columns.
-template <bool MASKED, int C>
-__device__ __forceinline__ void p2_chunk(uint32_t sc, const uint32_t (&s)[16],
-                                         const uint32_t (&dp)[16], const uint32_t (&f)[16],
-                                         const uint32_t (&g)[16], const float4* scal, int ibase,
-                                         int gj, float c1, float tau) {
-  uint32_t odS[8], odSt[8], oW[8];
+// 16 query rows (one K step of the output GEMMs) of the score buffer, one
+// key row per thread: dS, d~S and W packed as bf16 pairs (8 registers each).
+template <bool MASKED>
+__device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t (&dp)[16],
+                                         const uint32_t (&f)[16], const uint32_t (&g)[16],
+                                         const float4* scal, int ibase, int gj, float c1,
+                                         float tau, uint32_t (&ods)[8], uint32_t (&odst)[8],
+                                         uint32_t (&ow)[8]) {
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
     float vds[2], vdst[2], vw[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int i = 16 * C + e + h;
-      const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row i
-      float p = ex2_approx(fmaf(u2f(s[e + h]), c1, -rs.x));
+      const int i = e + h;
+      const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row ibase + i
+      float p = ex2_approx(fmaf(u2f(s[i]), c1, -rs.x));
       if (MASKED && ibase + i < gj) p = 0.f;
-      const float dpv = u2f(dp[e + h]);
+      const float dpv = u2f(dp[i]);
       const float x = dpv - rs.y;
-      const float ft = u2f(f[e + h]) * tau;
+      const float ft = u2f(f[i]) * tau;
       vds[h] = p * x;
-      vdst[h] = p * (fmaf(ft, x, u2f(g[e + h])) - fmaf(rs.z, dpv, rs.w));
+      vdst[h] = p * (fmaf(ft, x, u2f(g[i])) - fmaf(rs.z, dpv, rs.w));
       vw[h] = p * (ft - rs.z);
     }
-    odS[e >> 1] = pack_bf16x2(vds[0], vds[1]);
-    odSt[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
-    oW[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+    ods[e >> 1] = pack_bf16x2(vds[0], vds[1]);
+    odst[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
+    ow[e >> 1] = pack_bf16x2(vw[0], vw[1]);
   }
-  tmem_st8(sc + slot_dS(C), odS);
-  tmem_st8(sc + slot_dSt(C), odSt);
-  tmem_st8(sc + slot_W(C), oW);
 }
 
-// One 32-column tile, one key row per thread (the same hand-off as pass 1);
-// the two 16-column chunks are read one after the other, which keeps the
-// register count within what 10 warps per SM allow.
+__device__ __forceinline__ void load_scores(uint32_t sc, int col, uint32_t (&s)[16],
+                                            uint32_t (&dp)[16], uint32_t (&f)[16],
+                                            uint32_t (&g)[16]) {
+  tmem_ld16(sc + kColS + col, s);
+  tmem_ld16(sc + kColdP + col, dp);
+  tmem_ld16(sc + kColF + col, f);
+  tmem_ld16(sc + kColG + col, g);
+}
+
+// The 32 query rows of one warpgroup: read both 16-row chunks of the scores
+// (then release the buffer), form the operands, and write them to the
+// operand area once the previous tile's output GEMMs are done with it.
 template <bool MASKED>
-__device__ __forceinline__ void p2_tile(uint32_t sc, uint64_t* ready, const float4* scal,
-                                        int ibase, int gj, float c1, float tau) {
+__device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const float4* scal,
+                                        int ibase, int gj, float c1, float tau, Smem2& sm,
+                                        int t, volatile int* abort_flag, unsigned int* err) {
+  uint32_t a_ds[8], a_dst[8], a_w[8], b_ds[8], b_dst[8], b_w[8];
   {
-    uint32_t s0[16], dp0[16], f0[16], g0[16];
-    tmem_ld16(sc + kColS, s0);
-    tmem_ld16(sc + kColdP, dp0);
-    tmem_ld16(sc + kColF, f0);
-    tmem_ld16(sc + kColG, g0);
+    uint32_t s[16], dp[16], f[16], g[16];
+    load_scores(sc, 32 * wg, s, dp, f, g);
     tmem_wait_ld();
-    p2_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, scal, ibase, gj, c1, tau);
+    p2_chunk<MASKED>(s, dp, f, g, scal, ibase, gj, c1, tau, a_ds, a_dst, a_w);
   }
   {
-    uint32_t s1[16], dp1[16], f1[16], g1[16];
-    tmem_ld16(sc + kColS + 16, s1);
-    tmem_ld16(sc + kColdP + 16, dp1);
-    tmem_ld16(sc + kColF + 16, f1);
-    tmem_ld16(sc + kColG + 16, g1);
+    uint32_t s[16], dp[16], f[16], g[16];
+    load_scores(sc, 32 * wg + 16, s, dp, f, g);
     tmem_wait_ld();
-    p2_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, scal, ibase, gj, c1, tau);
+    tc_fence_before();
+    warp_arrive(&sm.sc_free);  // this warp is done with the score buffer
+    p2_chunk<MASKED>(s, dp, f, g, scal + 16, ibase + 16, gj, c1, tau, b_ds, b_dst, b_w);
   }
+  if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
+  tc_fence_after();
+  const int kk = 2 * wg;
+  tmem_st8(opb + op_col(kOpdS, kk), a_ds);
+  tmem_st8(opb + op_col(kOpdSt, kk), a_dst);
+  tmem_st8(opb + op_col(kOpW, kk), a_w);
+  tmem_st8(opb + op_col(kOpdS, kk + 1), b_ds);
+  tmem_st8(opb + op_col(kOpdSt, kk + 1), b_dst);
+  tmem_st8(opb + op_col(kOpW, kk + 1), b_w);
   tmem_wait_st();
   tc_fence_before();
-  warp_arrive(ready);
+  warp_arrive(&sm.op_ready);
+  return true;
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    tc_pass2_kernel(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-                    const __nv_bfloat16* __restrict__ UK, const __nv_bfloat16* __restrict__ UV,
-                    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
-                    const __grid_constant__ CUtensorMap mUQ, const float* __restrict__ L,
+    tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mUK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mUV,
+                    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mUQ,
+                    const __grid_constant__ CUtensorMap mdO, const float* __restrict__ L,
                     const float* __restrict__ D, const float* __restrict__ alpha,
                     const float* __restrict__ E, float* __restrict__ dKt,
                     float* __restrict__ dVt, int H, int N, float tau, int causal,
@@ -175,23 +164,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
   const int j0 = blockIdx.x * BM;
-  // Query tiles t0 .. T-1 stream past; under the causal mask key j is seen
-  // only by queries i >= j, so the tiles before the block are skipped.
+  // Query tiles t0 .. of 64 rows stream past; under the causal mask key j is
+  // seen only by queries i >= j, so the tiles before the block are skipped.
   // Ring slots and barrier phases count tiles from t0.
-  const int t0 = causal ? j0 / BN : 0;
-  const int T = (N + BN - 1) / BN - t0;
+  const int t0 = causal ? j0 / BQ : 0;
+  const int T = (N + BQ - 1) / BQ - t0;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.a_ready, 8);
+    mbar_init(&sm.bar_kv, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.st_full[s], 1);
       mbar_init(&sm.st_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.op_ready[b], 4);
-    }
+    mbar_init(&sm.sc_full, 1);
+    mbar_init(&sm.sc_free, 8);
+    mbar_init(&sm.op_ready, 8);
+    mbar_init(&sm.op_free, 1);
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
@@ -205,87 +194,99 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&mQ);
-      tma_prefetch_desc(&mdO);
       tma_prefetch_desc(&mUQ);
+      tma_prefetch_desc(&mdO);
+      mbar_expect_tx(&sm.bar_kv, 4 * BLOCK_BYTES);
+      tma_load_3d(sm.kb[0], &mK, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.kb[1], &mUK, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.kb[2], &mV, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.kb[3], &mUV, &sm.bar_kv, 0, j0, bh);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % NST;
         if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
-        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
-        tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, (t + t0) * BN, bh);
-        tma_load_3d(sm.st[s][2], &mdO, &sm.st_full[s], 0, (t + t0) * BN, bh);
+        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, (t + t0) * BQ, bh);
+        tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, (t + t0) * BQ, bh);
+        tma_load_3d(sm.st[s][2], &mdO, &sm.st_full[s], 0, (t + t0) * BQ, bh);
         issued = t + 1;
       }
+      // No copy may still be in flight when the CTA exits.
+      drain_wait(&sm.bar_kv, 0);
       for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
         drain_wait(&sm.st_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
-    {  // MMA issuer: whole warp, one elected lane issues
-      constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
-      constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
-      constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 64, B MN-major
-      const uint32_t st0 = smem_u32(sm.st[0][0]);
-      const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
-      const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
-      const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
-      // One elected lane issues each group of MMAs as one straight block.
-      auto issue_scores = [&](int t) {
-        const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        if (elect_one()) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t idS64 = idesc_bf16(BM, BQ, false);       // N = 64, B K-major
+    constexpr uint32_t idS128 = idesc_bf16(BM, 2 * BQ, false);  // N = 128, B K-major
+    constexpr uint32_t idO = idesc_bf16(BM, DH, true);          // N = 64, B MN-major
+    const uint64_t dK = smem_desc_sw128(smem_u32(sm.kb[0]), 16, 1024);
+    const uint64_t dUK = smem_desc_sw128(smem_u32(sm.kb[1]), 16, 1024);
+    const uint64_t dV = smem_desc_sw128(smem_u32(sm.kb[2]), 16, 1024);
+    const uint64_t dUV = smem_desc_sw128(smem_u32(sm.kb[3]), 16, 1024);
+    const uint32_t st0 = smem_u32(sm.st[0][0]);
+    const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
+    const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
+    const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
+    const uint32_t sc = tbase + kSc;
+    auto issue_scores = [&](int t) {
+      const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
+      if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint64_t o = 2 * kk;       // 32 bytes >> 4 along K in the B tiles
-            const uint32_t ao = 8 * kk;      // 16 bf16 = 8 TMEM columns along K in A
-            const uint32_t acc = kk > 0;
-            mma_ts(sc + kColS, tbase + kAK + ao, dQ0 + so + o, idS64, acc);   // [S^T | F'^T] = K [Q; U_Q]^T
-            mma_ts(sc + kColF, tbase + kAUK + ao, dQ0 + so + o, idS32, 1);    // F'^T += U_K Q^T
-            mma_ts(sc + kColdP, tbase + kAV + ao, ddO0 + so + o, idS32, acc); // dP^T = V dO^T
-            mma_ts(sc + kColG, tbase + kAUV + ao, ddO0 + so + o, idS32, acc); // G^T  = U_V dO^T
-          }
-          mma_commit(&sm.sc_full[t & 1]);
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t o = 2 * kk;  // 16 bf16 along d = 32 bytes >> 4
+          const uint32_t acc = kk > 0;
+          mma_ss(sc + kColS, dK + o, dQ0 + so + o, idS128, acc);    // [S^T | F'^T] = K [Q; U_Q]^T
+          mma_ss(sc + kColF, dUK + o, dQ0 + so + o, idS64, 1);      // F'^T += U_K Q^T
+          mma_ss(sc + kColdP, dV + o, ddO0 + so + o, idS64, acc);   // dP^T = V dO^T
+          mma_ss(sc + kColG, dUV + o, ddO0 + so + o, idS64, acc);   // G^T  = U_V dO^T
         }
-        __syncwarp();
-      };
-      auto issue_outputs = [&](int t) {
-        const int s = t % NST;
-        const uint64_t so = (uint64_t)(s * 3 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        if (elect_one()) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 query rows further down
-            const uint32_t acc = (t > 0 || c > 0);
-            mma_ts(tbase + kAccK, sc + slot_dSt(c), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
-            mma_ts(tbase + kAccK, sc + slot_dS(c), dUQ0 + so + o, idO, 1);    //     +  dS^T U_Q
-            mma_ts(tbase + kAccV, sc + slot_W(c), ddO0 + so + o, idO, acc);   // d~V += W^T dO
-          }
-          mma_commit(&sm.st_empty[s]);
-        }
-        __syncwarp();
-      };
-      bool ok = mbar_wait_warp(&sm.a_ready, 0, abort_flag, err);  // K, V, U_K, U_V are in TMEM
-      tc_fence_after();
-      for (int t = 0; ok && t < 2 && t < T; ++t) {
-        ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
-        tc_fence_after();
-        if (ok) issue_scores(t);
+        mma_commit(&sm.sc_full);
       }
-      for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+      __syncwarp();
+    };
+    auto issue_outputs = [&](int t) {
+      const int s = t % NST;
+      const uint64_t so = (uint64_t)(s * 3 * TILE_BYTES) >> 4;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint64_t o = (uint64_t)(16 * 128 * kk) >> 4;  // 16 query rows further down
+          const uint32_t acc = (t > 0 || kk > 0);
+          mma_ts(tbase + kAccK, tbase + op_col(kOpdSt, kk), dQ0 + so + o, idO, acc);  // d~K += d~S^T Q
+          mma_ts(tbase + kAccK, tbase + op_col(kOpdS, kk), dUQ0 + so + o, idO, 1);    //     +  dS^T U_Q
+          mma_ts(tbase + kAccV, tbase + op_col(kOpW, kk), ddO0 + so + o, idO, acc);   // d~V += W^T dO
+        }
+        mma_commit(&sm.op_free);
+        mma_commit(&sm.st_empty[s]);
+      }
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
+    for (int t = 0; ok && t < T; ++t) {
+      if (t > 0) {  // both warpgroups hold the scores of tile t - 1 in registers
+        ok = mbar_wait_warp(&sm.sc_free, (t - 1) & 1, abort_flag, err);
+        if (!ok) break;
+      }
+      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+      if (!ok) break;
+      tc_fence_after();
+      issue_scores(t);
+      if (t > 0) {
+        ok = mbar_wait_warp(&sm.op_ready, (t - 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_outputs(t);
-        if (t + 2 < T) {
-          ok = mbar_wait_warp(&sm.st_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_scores(t + 2);
-        }
+        issue_outputs(t - 1);
       }
-      if (elect_one()) mma_commit(&sm.out_full);
     }
+    if (ok && T > 0) {
+      ok = mbar_wait_warp(&sm.op_ready, (T - 1) & 1, abort_flag, err);
+      tc_fence_after();
+      if (ok) issue_outputs(T - 1);
+    }
+    if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
+    __syncwarp();
   } else {
     const int wg = (warp - 2) >> 2;
     const int quad = warp & 3;
@@ -294,64 +295,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int gj = j0 + r;
     const size_t head = static_cast<size_t>(bh) * N;
     const float c1 = tau * kLog2e;
-    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
+    const uint32_t sc = tbase + lane_off + kSc;
+    const uint32_t opb = tbase + lane_off;
     const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
     bool ok = true;
 
-    // Resident key block into TMEM: warpgroup 0 copies K and U_K, warpgroup
-    // 1 copies V and U_V, one key row per thread.
-    {
-      const bool valid = gj < N;
-      const size_t roff = valid ? (head + gj) * DH : 0;
-      if (wg == 0) {
-        row_to_tmem(tbase + lane_off + kAK, valid ? K + roff : nullptr);
-        row_to_tmem(tbase + lane_off + kAUK, valid ? UK + roff : nullptr);
-      } else {
-        row_to_tmem(tbase + lane_off + kAV, valid ? V + roff : nullptr);
-        row_to_tmem(tbase + lane_off + kAUV, valid ? UV + roff : nullptr);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      warp_arrive(&sm.a_ready);
-    }
-
-    // Row scalars of a streamed tile, (L log2 e, D, alpha, E) per query row;
-    // rows past N get L = +inf so that P = exp2(-inf) = 0.
+    // Row scalars (L log2 e, D, alpha, E) of this warpgroup's 32 query rows
+    // of tile t; rows past N get L = +inf so that P = exp2(-inf) = 0.
     auto load_scalars = [&](int t) {
-      const int i = (t + t0) * BN + lane;
+      const int i = (t + t0) * BQ + 32 * wg + lane;
       if (t < T && i < N)
         return make_float4(L[head + i] * kLog2e, D[head + i], alpha[head + i], E[head + i]);
       return make_float4(INFINITY, 0.f, 0.f, 0.f);
     };
     // The loader warp fetches the scalars one tile ahead into registers, so
     // their global-memory latency hides behind the current tile.
-    if (loader) sm.scal[wg][0][lane] = load_scalars(wg);
-    for (int u = 0;; ++u) {
-      const int t = 2 * u + wg;
-      if (t >= T) break;
-      float4* scal = sm.scal[wg][u & 1];
+    if (loader) sm.scal[wg][0][lane] = load_scalars(0);
+    for (int t = 0; t < T; ++t) {
+      const float4* scal = sm.scal[wg][t & 1];
       named_bar_sync(2 + wg, 128);  // scal is written; last tile's readers are done
       float4 next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (loader) next = load_scalars(t + 2);
-      // Warp-uniform decision (tcgen05.ld/st are warp-collective); after a
+      if (loader) next = load_scalars(t + 1);
+      // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
       // failed wait keep looping so every thread passes the same named
       // barriers, but skip the work.
-      ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
+      ok = ok && mbar_wait_warp(&sm.sc_full, t & 1, abort_flag, err);
       if (ok) {
         tc_fence_after();
         // Causal: queries i < j (this thread's key row) get P = 0; only the
-        // tiles that overlap the key block take the masked path.  Rows past N
-        // carry L = +inf, so their P is 0 on both paths.
-        const int ibase = (t + t0) * BN;
-        if (causal && ibase < j0 + BM) {
-          p2_tile<true>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
-        } else {
-          p2_tile<false>(sc, &sm.op_ready[wg], scal, ibase, gj, c1, tau);
-        }
+        // tiles that overlap the key block take the masked path.
+        const int ibase = (t + t0) * BQ + 32 * wg;
+        if (causal && ibase < j0 + BM)
+          ok = p2_half<true>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+        else
+          ok = p2_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
       }
       // Every thread passed this iteration's barrier, so nobody still reads
       // the other buffer.
-      if (loader) sm.scal[wg][(u + 1) & 1][lane] = next;
+      if (loader) sm.scal[wg][(t + 1) & 1][lane] = next;
     }
 
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
@@ -393,17 +374,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 size_t tc_pass2_smem() { return sizeof(Smem2) + 1024; }
 
-cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps32) {
-  // maps32: Q, dO, U_Q with 32-row boxes; K, V, U_K, U_V are read directly.
+cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
+                            const CUtensorMap* maps64) {
+  // maps128: K, U_K, V, U_V with 128-row boxes; maps64: Q, U_Q, dO with 64-row boxes.
   const size_t smem = tc_pass2_smem();
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
-      (const __nv_bfloat16*)a.K, (const __nv_bfloat16*)a.V, (const __nv_bfloat16*)a.UK,
-      (const __nv_bfloat16*)a.UV, maps32[0], maps32[1], maps32[2], a.L, a.D, a.alpha, a.E,
-      a.dKt, a.dVt, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
+      maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L, a.D,
+      a.alpha, a.E, a.dKt, a.dVt, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 
