@@ -305,3 +305,51 @@ def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None, causal=False):
         for k in keys:
             out[k][b, h] = r[k]
     return out
+
+
+# --------------------------------------------------------------------------
+# Grouped-query attention: H query heads share H_kv key/value heads
+# --------------------------------------------------------------------------
+
+def phi_gqa(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
+    """Phi for [H, N, d] query-side arrays and [H_kv, N, d] key-side arrays:
+    query head h attends to key/value head h // (H / H_kv), and the first
+    backward's dK, dV of a shared head sum the contributions of its query
+    heads ([FBN] 关键设计 3), so Phi is the sum of the per-head objectives."""
+    H, Hkv = Q.shape[0], K.shape[0]
+    G = H // Hkv
+    total = 0.0
+    for h in range(H):
+        g = h // G
+        total += phi(Q[h], K[g], V[g], dO[h], UQ[h], UK[g], UV[g], tau, causal)
+    return total
+
+
+def bob_gqa(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
+    """BoB of ``phi_gqa``: d~Q, d~dO, alpha, E per query head; d~K, d~V of a
+    shared head are the sums over its query heads of the per-head results."""
+    H, Hkv = Q.shape[0], K.shape[0]
+    G = H // Hkv
+    out = {"dQt": np.zeros(Q.shape), "ddOt": np.zeros(Q.shape), "dKt": np.zeros(K.shape),
+           "dVt": np.zeros(K.shape), "alpha": np.zeros(Q.shape[:2]), "E": np.zeros(Q.shape[:2]),
+           "L": np.zeros(Q.shape[:2]), "D": np.zeros(Q.shape[:2])}
+    for h in range(H):
+        g = h // G
+        r = bob(Q[h], K[g], V[g], dO[h], UQ[h], UK[g], UV[g], tau, causal)
+        for k in ("dQt", "ddOt", "alpha", "E", "L", "D"):
+            out[k][h] = r[k]
+        out["dKt"][g] += r["dKt"]
+        out["dVt"][g] += r["dVt"]
+    return out
+
+
+def prep_gqa(Q, K, V, dO, tau, causal=False):
+    """O, L, D per query head with the shared key/value heads."""
+    H, Hkv = Q.shape[0], K.shape[0]
+    G = H // Hkv
+    O = np.empty(Q.shape)
+    L = np.empty(Q.shape[:2])
+    D = np.empty(Q.shape[:2])
+    for h in range(H):
+        O[h], L[h], D[h] = prep(Q[h], K[h // G], V[h // G], dO[h], tau, causal)
+    return O, L, D

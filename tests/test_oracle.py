@@ -377,3 +377,57 @@ def test_causal_first_row_and_invariants():
     assert abs((r["ddOt"] * dO).sum() - ph) < 1e-12 * (abs(ph) + 1)
     assert np.abs(r["dKt"].sum(axis=0)).max() < 1e-12 * np.abs(r["dKt"]).max() * 9
     assert np.abs(r["dVt"].sum(axis=0)).max() < 1e-12 * np.abs(r["dVt"]).max() * 9
+
+
+# --------------------------------------------------------------------------
+# Grouped-query attention
+# --------------------------------------------------------------------------
+
+def _rand_gqa(H, Hkv, N, d, seed):
+    rng = np.random.default_rng(seed)
+    q = [rng.standard_normal((H, N, d)) for _ in range(2)]
+    k = [rng.standard_normal((Hkv, N, d)) for _ in range(2)]
+    dO, UQ = rng.standard_normal((H, N, d)), rng.standard_normal((H, N, d))
+    UK, UV = rng.standard_normal((Hkv, N, d)), rng.standard_normal((Hkv, N, d))
+    return q[0], k[0], k[1], dO, UQ, UK, UV
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_matches_fd_of_phi(causal):
+    Q, K, V, dO, UQ, UK, UV = _rand_gqa(4, 2, 5, 3, 40)
+    tau = 0.55
+    r = orc.bob_gqa(Q, K, V, dO, UQ, UK, UV, tau, causal)
+    args = [Q, K, V, dO]
+    for pos, key in enumerate(("dQt", "dKt", "dVt", "ddOt")):
+        def f(X, pos=pos):
+            a = list(args)
+            a[pos] = X
+            return orc.phi_gqa(*a, UQ, UK, UV, tau, causal)
+        assert rel(r[key], _fd_grad(f, args[pos])) < RTOL_FD, key
+
+
+def test_gqa_matches_torch_double_backward_with_shared_heads():
+    torch = pytest.importorskip("torch")
+    H, Hkv, N, d = 6, 2, 9, 4
+    Q, K, V, dO, UQ, UK, UV = _rand_gqa(H, Hkv, N, d, 41)
+    tau = 0.5
+    r = orc.bob_gqa(Q, K, V, dO, UQ, UK, UV, tau)
+    tq, tk, tv, tdo = (torch.tensor(x, requires_grad=True) for x in (Q, K, V, dO))
+    uq, uk, uv = (torch.tensor(x) for x in (UQ, UK, UV))
+    kr = tk.repeat_interleave(H // Hkv, dim=0)  # autograd sums the group's gradients
+    vr = tv.repeat_interleave(H // Hkv, dim=0)
+    out = torch.softmax(tau * tq @ kr.transpose(1, 2), dim=-1) @ vr
+    dq, dk, dv = torch.autograd.grad(out, (tq, tk, tv), tdo, create_graph=True)
+    ph = (dq * uq).sum() + (dk * uk).sum() + (dv * uv).sum()
+    g = torch.autograd.grad(ph, (tq, tk, tv, tdo))
+    for key, t in zip(("dQt", "dKt", "dVt", "ddOt"), g):
+        assert rel(r[key], t.numpy()) < 1e-12, key
+
+
+def test_gqa_with_one_group_is_mha():
+    Q, K, V, dO, UQ, UK, UV = _rand_gqa(3, 3, 7, 4, 42)
+    r = orc.bob_gqa(Q, K, V, dO, UQ, UK, UV, 0.4)
+    for h in range(3):
+        m = orc.bob(Q[h], K[h], V[h], dO[h], UQ[h], UK[h], UV[h], 0.4)
+        for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+            assert rel(r[key][h], m[key]) < 1e-14, key
