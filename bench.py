@@ -155,7 +155,7 @@ def oracle_rows_sample(w, x, seconds: float, rows_per_chunk: int = 16, seed: int
 
     from exact_second_order_gb300.inputs import NAMES, as_float64_numpy
     from oracle import bob as orc
-    args = [as_float64_numpy(x[k][0, 0]) for k in NAMES]
+    args = [as_float64_numpy(x[k][0, 0]) for k in NAMES]  # query head 0 uses key head 0
     rng = np.random.default_rng(seed)
     done, t0 = 0, time.perf_counter()
     while True:
@@ -193,7 +193,7 @@ def run_reference(args, w, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
-                                        "d": w.d, "causal": w.causal},
+                                        "d": w.d, "Hkv": w.kv_heads, "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{t_rows} seeded rows of head (0,0) through oracle.bob_rows "
                                    f"(fp64 numpy), {row_flops(w):.3e} flops credited per row"},
@@ -227,7 +227,7 @@ def main():
     x = make_inputs(rank_workload(w, rank))
     dev = {k: v.cuda() for k, v in x.items()}
     O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
-    out = fb.alloc_bob_outputs(dev["Q"])
+    out = fb.alloc_bob_outputs(dev["Q"], K=dev["K"])
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
@@ -328,7 +328,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "N": w.N, "d": w.d,
+                   "causal": w.causal,
                    "tau": w.tau, "flops_per_step_per_gpu": flops,
                    "flop_convention": "38*N^2*d*B*H (19 GEMMs of 2*N^2*d)",
                    "l2": f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "

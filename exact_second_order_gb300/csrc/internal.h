@@ -9,7 +9,7 @@ namespace flashbob {
 struct PrepArgs {
   const void *Q, *K, *V, *dO;
   float *O, *L, *D;
-  int B, H, N, d;
+  int B, H, Hkv, N, d;  // Hkv key/value heads, shared by H / Hkv query heads each
   float tau;
   bool causal;
   bool bf16;
@@ -25,7 +25,7 @@ struct BobArgs {
   const void *UQ, *UK, *UV;
   float tau;
   float *dQt, *dKt, *dVt, *ddOt, *alpha, *E;
-  int B, H, N, d;
+  int B, H, Hkv, N, d;  // Hkv key/value heads, shared by H / Hkv query heads each
   bool causal;
   bool bf16;
   cudaStream_t stream;

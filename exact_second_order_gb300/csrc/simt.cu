@@ -63,8 +63,8 @@ template <typename T, int DP>
 __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                   const T* __restrict__ V, const T* __restrict__ dO,
                                                   float* __restrict__ O, float* __restrict__ L,
-                                                  float* __restrict__ D, int H, int N, int d,
-                                                  float tau, int causal) {
+                                                  float* __restrict__ D, int H, int Hkv, int N,
+                                                  int d, float tau, int causal) {
   extern __shared__ float sm[];
   float* Qs = sm;
   float* Ks = Qs + SB * (DP + 1);
@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
   float* Ps = Vs + SB * (DP + 1);  // [SB][SB + 1]
   const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
   const size_t base = bh * N * d;
+  // key/value head shared by this query head (grouped-query attention)
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * N * d;
   const int row0 = blockIdx.x * SB;
   const int t = threadIdx.x, r = t >> 3, q = t & 7;
   const float c = tau * kLog2e;  // scores in log2 units
@@ -86,8 +88,8 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
   const int col_end = causal ? min(N, row0 + SB) : N;  // keys j <= i under the causal mask
   for (int col0 = 0; col0 < col_end; col0 += SB) {
     __syncthreads();
-    load_tile<T, DP>(Ks, K + base, col0, N, d);
-    load_tile<T, DP>(Vs, V + base, col0, N, d);
+    load_tile<T, DP>(Ks, K + kbase, col0, N, d);
+    load_tile<T, DP>(Vs, V + kbase, col0, N, d);
     __syncthreads();
     float s[4];
 #pragma unroll
@@ -160,7 +162,8 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
     const float* __restrict__ O, const T* __restrict__ dO, const float* __restrict__ L,
     const float* __restrict__ D, const T* __restrict__ UQ, const T* __restrict__ UK,
     const T* __restrict__ UV, float tau, float* __restrict__ dQt, float* __restrict__ ddOt,
-    float* __restrict__ alpha, float* __restrict__ E, int H, int N, int d, int causal) {
+    float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv, int N, int d,
+    int causal) {
   extern __shared__ float sm[];
   constexpr int TP = SB * (DP + 1);
   constexpr int OP = SB * (SB + 1);
@@ -179,6 +182,8 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
 
   const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
   const size_t base = bh * N * d;
+  // key/value head shared by this query head (grouped-query attention)
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * N * d;
   const int row0 = blockIdx.x * SB;
   const int t = threadIdx.x, r = t >> 3, q = t & 7;
   const int gr = row0 + r;
@@ -198,10 +203,10 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
 
   for (int col0 = 0; col0 < col_end; col0 += SB) {
     __syncthreads();
-    load_tile<T, DP>(Ks, K + base, col0, N, d);
-    load_tile<T, DP>(Vs, V + base, col0, N, d);
-    load_tile<T, DP>(UKs, UK + base, col0, N, d);
-    load_tile<T, DP>(UVs, UV + base, col0, N, d);
+    load_tile<T, DP>(Ks, K + kbase, col0, N, d);
+    load_tile<T, DP>(Vs, V + kbase, col0, N, d);
+    load_tile<T, DP>(UKs, UK + kbase, col0, N, d);
+    load_tile<T, DP>(UVs, UV + kbase, col0, N, d);
     __syncthreads();
     float s[4], dp[4], f[4], g[4];
 #pragma unroll
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
     const T* __restrict__ dO, const float* __restrict__ L, const float* __restrict__ D,
     const float* __restrict__ alpha, const float* __restrict__ E, const T* __restrict__ UQ,
     const T* __restrict__ UK, const T* __restrict__ UV, float tau, float* __restrict__ dKt,
-    float* __restrict__ dVt, int H, int N, int d, int causal) {
+    float* __restrict__ dVt, int H, int Hkv, int N, int d, int causal) {
   extern __shared__ float sm[];
   constexpr int TP = SB * (DP + 1);
   constexpr int OP = SB * (SB + 1);
@@ -308,85 +313,92 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
   float* As = Ds + SB;
   float* Es = As + SB;
 
-  const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
-  const size_t base = bh * N * d;
+  // One CTA per key block of a key/value head; the H / Hkv query heads that
+  // share the head are summed on chip (grouped-query attention).
+  const int G = H / Hkv;
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y) * N * d;
   const int j0 = blockIdx.x * SB;
   const int t = threadIdx.x, jr = t >> 3, q = t & 7;
   const float c = tau * kLog2e;
 
-  load_tile<T, DP>(Ks, K + base, j0, N, d);
-  load_tile<T, DP>(Vs, V + base, j0, N, d);
-  load_tile<T, DP>(UKs, UK + base, j0, N, d);
-  load_tile<T, DP>(UVs, UV + base, j0, N, d);
+  load_tile<T, DP>(Ks, K + kbase, j0, N, d);
+  load_tile<T, DP>(Vs, V + kbase, j0, N, d);
+  load_tile<T, DP>(UKs, UK + kbase, j0, N, d);
+  load_tile<T, DP>(UVs, UV + kbase, j0, N, d);
 
   float accK[DP / 8], accV[DP / 8];
 #pragma unroll
   for (int j = 0; j < DP / 8; ++j) accK[j] = accV[j] = 0.f;
 
   const int gj = j0 + jr;
-  // Under the causal mask key j is seen by queries i >= j only.
-  for (int row0 = causal ? j0 : 0; row0 < N; row0 += SB) {
-    __syncthreads();
-    load_tile<T, DP>(Qs, Q + base, row0, N, d);
-    load_tile<T, DP>(dOs, dO + base, row0, N, d);
-    load_tile<T, DP>(UQs, UQ + base, row0, N, d);
-    if (t < SB) {
-      const int gi = row0 + t;
-      const bool ok = gi < N;
-      Ls2[t] = ok ? L[bh * N + gi] * kLog2e : 0.f;
-      Ds[t] = ok ? D[bh * N + gi] : 0.f;
-      As[t] = ok ? alpha[bh * N + gi] : 0.f;
-      Es[t] = ok ? E[bh * N + gi] : 0.f;
-    }
-    __syncthreads();
-    float s[4], dp[4], f[4], g[4];
+  for (int hh = 0; hh < G; ++hh) {
+    const size_t bh = (size_t)blockIdx.z * H + (size_t)blockIdx.y * G + hh;
+    const size_t base = bh * N * d;
+    // Under the causal mask key j is seen by queries i >= j only.
+    for (int row0 = causal ? j0 : 0; row0 < N; row0 += SB) {
+      __syncthreads();
+      load_tile<T, DP>(Qs, Q + base, row0, N, d);
+      load_tile<T, DP>(dOs, dO + base, row0, N, d);
+      load_tile<T, DP>(UQs, UQ + base, row0, N, d);
+      if (t < SB) {
+        const int gi = row0 + t;
+        const bool ok = gi < N;
+        Ls2[t] = ok ? L[bh * N + gi] * kLog2e : 0.f;
+        Ds[t] = ok ? D[bh * N + gi] : 0.f;
+        As[t] = ok ? alpha[bh * N + gi] : 0.f;
+        Es[t] = ok ? E[bh * N + gi] : 0.f;
+      }
+      __syncthreads();
+      float s[4], dp[4], f[4], g[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) s[u] = dp[u] = f[u] = g[u] = 0.f;
-    for (int k = 0; k < d; ++k) {
-      const int jk = jr * (DP + 1) + k;
-      const float kv = Ks[jk], vv = Vs[jk], ukv = UKs[jk], uvv = UVs[jk];
+      for (int u = 0; u < 4; ++u) s[u] = dp[u] = f[u] = g[u] = 0.f;
+      for (int k = 0; k < d; ++k) {
+        const int jk = jr * (DP + 1) + k;
+        const float kv = Ks[jk], vv = Vs[jk], ukv = UKs[jk], uvv = UVs[jk];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ik = (q + 8 * u) * (DP + 1) + k;
+          const float qv = Qs[ik];
+          s[u] = fmaf(kv, qv, s[u]);
+          dp[u] = fmaf(vv, dOs[ik], dp[u]);
+          f[u] = fmaf(kv, UQs[ik], fmaf(ukv, qv, f[u]));
+          g[u] = fmaf(uvv, dOs[ik], g[u]);
+        }
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int ik = (q + 8 * u) * (DP + 1) + k;
-        const float qv = Qs[ik];
-        s[u] = fmaf(kv, qv, s[u]);
-        dp[u] = fmaf(vv, dOs[ik], dp[u]);
-        f[u] = fmaf(kv, UQs[ik], fmaf(ukv, qv, f[u]));
-        g[u] = fmaf(uvv, dOs[ik], g[u]);
+        const int ii = q + 8 * u;
+        const int i = row0 + ii;
+        const float p = (i < N && !(causal && i < gj)) ? exp2f(s[u] * c - Ls2[ii]) : 0.f;
+        const float x = dp[u] - Ds[ii];
+        const float ft = f[u] * tau;
+        const float a = As[ii];
+        dSTs[jr * (SB + 1) + ii] = p * x;
+        dStTs[jr * (SB + 1) + ii] = p * (fmaf(ft, x, g[u]) - a * dp[u] - Es[ii]);
+        WTs[jr * (SB + 1) + ii] = p * (ft - a);
+      }
+      __syncwarp();
+      for (int ii = 0; ii < SB; ++ii) {
+        const float ds = dSTs[jr * (SB + 1) + ii];
+        const float dst = dStTs[jr * (SB + 1) + ii];
+        const float w = WTs[jr * (SB + 1) + ii];
+#pragma unroll
+        for (int j = 0; j < DP / 8; ++j) {
+          const int ik = ii * (DP + 1) + q + 8 * j;
+          accK[j] = fmaf(dst, Qs[ik], fmaf(ds, UQs[ik], accK[j]));
+          accV[j] = fmaf(w, dOs[ik], accV[j]);
+        }
       }
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int ii = q + 8 * u;
-      const int i = row0 + ii;
-      const float p = (i < N && !(causal && i < gj)) ? exp2f(s[u] * c - Ls2[ii]) : 0.f;
-      const float x = dp[u] - Ds[ii];
-      const float ft = f[u] * tau;
-      const float a = As[ii];
-      dSTs[jr * (SB + 1) + ii] = p * x;
-      dStTs[jr * (SB + 1) + ii] = p * (fmaf(ft, x, g[u]) - a * dp[u] - Es[ii]);
-      WTs[jr * (SB + 1) + ii] = p * (ft - a);
-    }
-    __syncwarp();
-    for (int ii = 0; ii < SB; ++ii) {
-      const float ds = dSTs[jr * (SB + 1) + ii];
-      const float dst = dStTs[jr * (SB + 1) + ii];
-      const float w = WTs[jr * (SB + 1) + ii];
-#pragma unroll
-      for (int j = 0; j < DP / 8; ++j) {
-        const int ik = ii * (DP + 1) + q + 8 * j;
-        accK[j] = fmaf(dst, Qs[ik], fmaf(ds, UQs[ik], accK[j]));
-        accV[j] = fmaf(w, dOs[ik], accV[j]);
-      }
-    }
-  }
+
+  }  // query heads of the group
 
   if (gj < N) {
 #pragma unroll
     for (int j = 0; j < DP / 8; ++j) {
       const int k = q + 8 * j;
       if (k < d) {
-        const size_t o = base + (size_t)gj * d + k;
+        const size_t o = kbase + (size_t)gj * d + k;
         dKt[o] = tau * accK[j];
         dVt[o] = accV[j];
       }
@@ -408,8 +420,8 @@ cudaError_t run_prep(const PrepArgs& a) {
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + SB - 1) / SB, a.H, a.B);
   prep_kernel<T, DP><<<grid, NT, smem, a.stream>>>(
-      (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.O, a.L, a.D, a.H, a.N, a.d,
-      a.tau, a.causal ? 1 : 0);
+      (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.O, a.L, a.D, a.H, a.Hkv,
+      a.N, a.d, a.tau, a.causal ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -427,15 +439,16 @@ cudaError_t run_bob(const BobArgs& a) {
     pass1_kernel<T, DP><<<grid, NT, s1, a.stream>>>(
         (const T*)a.Q, (const T*)a.K, (const T*)a.V, a.O, (const T*)a.dO, a.L, a.D,
         (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dQt, a.ddOt, a.alpha, a.E, a.H,
-        a.N, a.d, a.causal ? 1 : 0);
+        a.Hkv, a.N, a.d, a.causal ? 1 : 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (a.passes & kPass2) {
-    pass2_kernel<T, DP><<<grid, NT, s2, a.stream>>>(
+    const dim3 grid2((a.N + SB - 1) / SB, a.Hkv, a.B);  // one CTA per key block of a shared head
+    pass2_kernel<T, DP><<<grid2, NT, s2, a.stream>>>(
         (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.L, a.D, a.alpha, a.E,
-        (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dKt, a.dVt, a.H, a.N, a.d,
-        a.causal ? 1 : 0);
+        (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dKt, a.dVt, a.H, a.Hkv, a.N,
+        a.d, a.causal ? 1 : 0);
     e = cudaGetLastError();
   }
   return e;

@@ -13,7 +13,7 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
 bool tc_supported(const BobArgs& a) { return a.bf16 && a.d == 64; }
 
 cudaError_t tc_bob(const BobArgs& a) {
-  const int BH = a.B * a.H;
+  const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
   cudaError_t e = cudaSuccess;
   if (a.passes & kPass1) {
     CUtensorMap m128[3], m32[4];
@@ -22,7 +22,7 @@ cudaError_t tc_bob(const BobArgs& a) {
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
       e = tc::make_map_bf16_d64(&m128[i], rows[i], BH, a.N, kTcRows);
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m32[i], cols[i], BH, a.N, kTcStream);
+      e = tc::make_map_bf16_d64(&m32[i], cols[i], BHkv, a.N, kTcStream);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass1(a, m128, m32);
     if (e != cudaSuccess) return e;
@@ -32,7 +32,7 @@ cudaError_t tc_bob(const BobArgs& a) {
     const void* res[4] = {a.K, a.UK, a.V, a.UV};
     const void* str[3] = {a.Q, a.UQ, a.dO};
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m128[i], res[i], BH, a.N, kTcRows);
+      e = tc::make_map_bf16_d64(&m128[i], res[i], BHkv, a.N, kTcRows);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
       e = tc::make_map_bf16_d64(&m64[i], str[i], BH, a.N, kTcStream2);
     if (e != cudaSuccess) return e;

@@ -148,13 +148,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap mUV, const float* __restrict__ O,
                     const float* __restrict__ L, const float* __restrict__ D,
                     float* __restrict__ dQt, float* __restrict__ ddOt,
-                    float* __restrict__ alpha, float* __restrict__ E, int H, int N, float tau,
-                    int causal, unsigned int* err) {
+                    float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv, int N,
+                    float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem1& sm = *reinterpret_cast<Smem1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
+  // key/value head shared by this query head (grouped-query attention)
+  const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);
   // Causal: the last row blocks see the most keys, so they start first.
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
   const int col_end = causal ? min(N, row0 + BM) : N;  // keys j <= i under the causal mask
@@ -198,10 +200,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int s = t % NST;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.kv_full[s], 4 * TILE_BYTES);
-        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.kv[s][1], &mUK, &sm.kv_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.kv[s][2], &mV, &sm.kv_full[s], 0, t * BN, bh);
-        tma_load_3d(sm.kv[s][3], &mUV, &sm.kv_full[s], 0, t * BN, bh);
+        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, t * BN, bkv);
+        tma_load_3d(sm.kv[s][1], &mUK, &sm.kv_full[s], 0, t * BN, bkv);
+        tma_load_3d(sm.kv[s][2], &mV, &sm.kv_full[s], 0, t * BN, bkv);
+        tma_load_3d(sm.kv[s][3], &mUV, &sm.kv_full[s], 0, t * BN, bkv);
         issued = t + 1;
       }
       // No copy may still be in flight when the CTA exits.
@@ -390,7 +392,7 @@ cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_pass1_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
+      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.N, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

@@ -156,19 +156,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap mdO, const float* __restrict__ L,
                     const float* __restrict__ D, const float* __restrict__ alpha,
                     const float* __restrict__ E, float* __restrict__ dKt,
-                    float* __restrict__ dVt, int H, int N, float tau, int causal,
+                    float* __restrict__ dVt, int H, int Hkv, int N, float tau, int causal,
                     unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem2& sm = *reinterpret_cast<Smem2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.z * H + blockIdx.y;
+  // One CTA per key block of a key/value head.  Grouped-query attention: the
+  // G = H / Hkv query heads sharing the head stream past one after the other
+  // and their contributions are summed on chip ([FBN] 关键设计 3).
+  const int G = H / Hkv;
+  const int bkv = blockIdx.z * Hkv + blockIdx.y;
+  const int hq0 = blockIdx.z * H + blockIdx.y * G;  // first query head of the group
   const int j0 = blockIdx.x * BM;
   // Query tiles t0 .. of 64 rows stream past; under the causal mask key j is
   // seen only by queries i >= j, so the tiles before the block are skipped.
-  // Ring slots and barrier phases count tiles from t0.
+  // f = (query head in group) * Tq + (tile - t0) numbers the streamed tiles;
+  // ring slots and barrier phases count f.
   const int t0 = causal ? j0 / BQ : 0;
-  const int T = (N + BQ - 1) / BQ - t0;
+  const int Tq = (N + BQ - 1) / BQ - t0;
+  const int T = G * Tq;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -197,18 +204,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mUQ);
       tma_prefetch_desc(&mdO);
       mbar_expect_tx(&sm.bar_kv, 4 * BLOCK_BYTES);
-      tma_load_3d(sm.kb[0], &mK, &sm.bar_kv, 0, j0, bh);
-      tma_load_3d(sm.kb[1], &mUK, &sm.bar_kv, 0, j0, bh);
-      tma_load_3d(sm.kb[2], &mV, &sm.bar_kv, 0, j0, bh);
-      tma_load_3d(sm.kb[3], &mUV, &sm.bar_kv, 0, j0, bh);
+      tma_load_3d(sm.kb[0], &mK, &sm.bar_kv, 0, j0, bkv);
+      tma_load_3d(sm.kb[1], &mUK, &sm.bar_kv, 0, j0, bkv);
+      tma_load_3d(sm.kb[2], &mV, &sm.bar_kv, 0, j0, bkv);
+      tma_load_3d(sm.kb[3], &mUV, &sm.bar_kv, 0, j0, bkv);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % NST;
         if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+        const int row = (t % Tq + t0) * BQ, zq = hq0 + t / Tq;
         mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
-        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, (t + t0) * BQ, bh);
-        tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, (t + t0) * BQ, bh);
-        tma_load_3d(sm.st[s][2], &mdO, &sm.st_full[s], 0, (t + t0) * BQ, bh);
+        tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, row, zq);
+        tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, row, zq);
+        tma_load_3d(sm.st[s][2], &mdO, &sm.st_full[s], 0, row, zq);
         issued = t + 1;
       }
       // No copy may still be in flight when the CTA exits.
@@ -293,7 +301,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quad * 32 + lane;  // key row inside the block = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int gj = j0 + r;
-    const size_t head = static_cast<size_t>(bh) * N;
     const float c1 = tau * kLog2e;
     const uint32_t sc = tbase + lane_off + kSc;
     const uint32_t opb = tbase + lane_off;
@@ -301,16 +308,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool ok = true;
 
     // Row scalars (L log2 e, D, alpha, E) of this warpgroup's 32 query rows
-    // of tile t; rows past N get L = +inf so that P = exp2(-inf) = 0.
-    auto load_scalars = [&](int t) {
-      const int i = (t + t0) * BQ + 32 * wg + lane;
-      if (t < T && i < N)
-        return make_float4(L[head + i] * kLog2e, D[head + i], alpha[head + i], E[head + i]);
-      return make_float4(INFINITY, 0.f, 0.f, 0.f);
+    // of streamed tile f, which is tile ft of the head whose rows start at
+    // fh; rows past N get L = +inf so that P = exp2(-inf) = 0.  (ft, fh)
+    // step along with f instead of dividing f by Tq.
+    int ft = 0;
+    const float* fL = L + static_cast<size_t>(hq0) * N;
+    auto load_scalars = [&](int f) {
+      const int i = (ft + t0) * BQ + 32 * wg + lane;
+      float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
+      if (f < T && i < N) {
+        const size_t o = static_cast<size_t>(fL - L) + i;
+        v = make_float4(fL[i] * kLog2e, D[o], alpha[o], E[o]);
+      }
+      if (++ft == Tq) { ft = 0; fL += N; }
+      return v;
     };
     // The loader warp fetches the scalars one tile ahead into registers, so
     // their global-memory latency hides behind the current tile.
     if (loader) sm.scal[wg][0][lane] = load_scalars(0);
+    int tq = 0;  // tile of the current query head, (t mod Tq)
     for (int t = 0; t < T; ++t) {
       const float4* scal = sm.scal[wg][t & 1];
       named_bar_sync(2 + wg, 128);  // scal is written; last tile's readers are done
@@ -324,7 +340,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         // Causal: queries i < j (this thread's key row) get P = 0; only the
         // tiles that overlap the key block take the masked path.
-        const int ibase = (t + t0) * BQ + 32 * wg;
+        const int ibase = (tq + t0) * BQ + 32 * wg;
         if (causal && ibase < j0 + BM)
           ok = p2_half<true>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
         else
@@ -333,6 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Every thread passed this iteration's barrier, so nobody still reads
       // the other buffer.
       if (loader) sm.scal[wg][(t + 1) & 1][lane] = next;
+      if (++tq == Tq) tq = 0;
     }
 
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
@@ -347,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld16(acc_base + kAccV + col, vv);
       tmem_wait_ld();
       if (ok && gj < N) {
-        const size_t off = (head + gj) * DH + col;
+        const size_t off = (static_cast<size_t>(bkv) * N + gj) * DH + col;
         float4* k4 = reinterpret_cast<float4*>(dKt + off);
         float4* v4 = reinterpret_cast<float4*>(dVt + off);
 #pragma unroll
@@ -381,10 +398,10 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
+  dim3 grid((a.N + BM - 1) / BM, a.Hkv, a.B);  // one CTA per key block of a shared head
   tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L, a.D,
-      a.alpha, a.E, a.dKt, a.dVt, a.H, a.N, a.tau, a.causal ? 1 : 0, a.err);
+      a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.N, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

@@ -54,12 +54,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __nv_bfloat16* __restrict__ dO,
                    float* __restrict__ O, float* __restrict__ L, float* __restrict__ D, int H,
-                   int N, float tau, int causal, unsigned int* err) {
+                   int Hkv, int N, float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem0& sm = *reinterpret_cast<Smem0*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
+  const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);  // shared key/value head
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
   const int col_end = causal ? min(N, row0 + BM) : N;  // keys j <= i under the causal mask
   const int T = (col_end + BN - 1) / BN;
@@ -99,8 +100,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int kt = phase_b ? t - T : t;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * TILE_BYTES);
-        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, kt * BN, bh);
-        if (phase_b) tma_load_3d(sm.kv[s][1], &mV, &sm.kv_full[s], 0, kt * BN, bh);
+        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, kt * BN, bkv);
+        if (phase_b) tma_load_3d(sm.kv[s][1], &mV, &sm.kv_full[s], 0, kt * BN, bkv);
         issued = t + 1;
       }
       drain_wait(&sm.bar_q, 0);
@@ -284,17 +285,18 @@ bool tc_prep_supported(const PrepArgs& a) { return a.bf16 && a.d == 64; }
 
 cudaError_t tc_prep(const PrepArgs& a) {
   const int BH = a.B * a.H;
+  const int BHkv = a.B * a.Hkv;
   CUtensorMap mq, mk, mv;
   cudaError_t e = tc::make_map_bf16_d64(&mq, a.Q, BH, a.N, kTcRows);
-  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mk, a.K, BH, a.N, kTcStream);
-  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mv, a.V, BH, a.N, kTcStream);
+  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mk, a.K, BHkv, a.N, kTcStream);
+  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mv, a.V, BHkv, a.N, kTcStream);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem0) + 1024;
   e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
   tc_prep_kernel<<<grid, NTHREADS, smem, a.stream>>>(mq, mk, mv, (const __nv_bfloat16*)a.dO, a.O,
-                                                     a.L, a.D, a.H, a.N, a.tau,
+                                                     a.L, a.D, a.H, a.Hkv, a.N, a.tau,
                                                      a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }

@@ -27,10 +27,10 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _SIGNATURES = {
-    "flashbob_prep": ([_P] * 7 + [_I] * 4 + [_F, _I, _I, _P], _I),
-    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 6 + [_P], _I),
-    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 6 + [_P], _I),
-    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 6 + [_P], _I),
+    "flashbob_prep": ([_P] * 7 + [_I] * 5 + [_F, _I, _I, _P], _I),
+    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 7 + [_P], _I),
+    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 7 + [_P], _I),
+    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 7 + [_P], _I),
     "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
@@ -89,8 +89,9 @@ def flashbob_status_string(status: int) -> str:
 def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream=None) -> None:
     """O, L, D of [B, H, N, d] inputs (see flashbob_prep in the header)."""
     B, H, N, d = Q.shape
+    Hkv = K.shape[1]
     st = load_library().flashbob_prep(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, N, d,
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, Hkv, N, d,
         float(tau), int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_prep")
@@ -100,10 +101,11 @@ def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, dd
                  causal: bool = False, stream=None) -> None:
     """d~Q, d~K, d~V, d~dO, alpha, E (see flashbob_bob in the header)."""
     B, H, N, d = Q.shape
+    Hkv = K.shape[1]
     st = load_library().flashbob_bob(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
         _ptr(UV), float(tau), _ptr(dQt), _ptr(dKt), _ptr(dVt), _ptr(ddOt), _ptr(alpha), _ptr(E),
-        B, H, N, d, int(causal), _dtype_code(Q), _stream_handle(stream))
+        B, H, Hkv, N, d, int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob")
 
@@ -112,9 +114,10 @@ def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, 
                        causal: bool = False, stream=None) -> None:
     """Pass 1 only: d~Q, d~dO, alpha, E (see flashbob_bob_pass1 in the header)."""
     B, H, N, d = Q.shape
+    Hkv = K.shape[1]
     st = load_library().flashbob_bob_pass1(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
-        _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, N, d,
+        _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, Hkv, N, d,
         int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass1")
@@ -124,9 +127,10 @@ def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt,
                        causal: bool = False, stream=None) -> None:
     """Pass 2 only: d~K, d~V from pass 1's alpha, E (see flashbob_bob_pass2)."""
     B, H, N, d = Q.shape
+    Hkv = K.shape[1]
     st = load_library().flashbob_bob_pass2(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(D), _ptr(alpha), _ptr(E), _ptr(UQ),
-        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, N, d, int(causal),
+        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, Hkv, N, d, int(causal),
         _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass2")
@@ -164,12 +168,16 @@ def prep(Q, K, V, dO, tau: float, causal: bool = False, stream=None):
     return O, L, D
 
 
-def alloc_bob_outputs(Q, fill: float | None = None) -> dict:
-    """fp32 output buffers of flashbob_bob (optionally filled, e.g. with NaN)."""
+def alloc_bob_outputs(Q, fill: float | None = None, K=None) -> dict:
+    """fp32 output buffers of flashbob_bob (optionally filled, e.g. with NaN);
+    d~K and d~V take K's head count (grouped-query attention) when K is given."""
     import torch
     B, H, N, d = Q.shape
+    Hkv = K.shape[1] if K is not None else H
     out = {k: torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device)
-           for k in ("dQt", "dKt", "dVt", "ddOt")}
+           for k in ("dQt", "ddOt")}
+    out.update({k: torch.empty((B, Hkv, N, d), dtype=torch.float32, device=Q.device)
+                for k in ("dKt", "dVt")})
     out.update({k: torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
                 for k in ("alpha", "E")})
     if fill is not None:
@@ -182,7 +190,7 @@ def bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, out: dict | None = None,
         causal: bool = False, stream=None):
     """Run flashbob_bob into ``out`` (allocated when None); returns the dict."""
     if out is None:
-        out = alloc_bob_outputs(Q)
+        out = alloc_bob_outputs(Q, K=K)
     flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, out["dQt"], out["dKt"], out["dVt"],
                  out["ddOt"], out["alpha"], out["E"], causal, stream)
     return out

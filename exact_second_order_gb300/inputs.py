@@ -12,6 +12,8 @@ Recipe (the pages benchmark an isolated attention layer on synthetic tensors):
 * ``dist="unit"``: all seven tensors ~ N(0, 1) (the tiny fp32 workload);
 * ``dist="scaled"``: Q, K, V ~ N(0, 1) / d**0.25 so that Q K^T has unit
   variance; dO, U_Q, U_K, U_V ~ N(0, 1);
+* grouped-query workloads draw K, V, U_K, U_V with ``Hkv`` heads (the
+  same draw order);
 * ``peaked_k_rows``: for every (b, h) pick floor(0.05 N) distinct key rows
   with the same generator (after the seven draws) and multiply them by 4,
   which makes some softmax rows peaked;
@@ -28,6 +30,7 @@ from dataclasses import dataclass
 import torch
 
 NAMES = ("Q", "K", "V", "dO", "UQ", "UK", "UV")
+KV_NAMES = ("K", "V", "UK", "UV")
 
 
 @dataclass(frozen=True)
@@ -45,6 +48,11 @@ class Workload:
     stress: bool = False
     seed: int = 0
     causal: bool = False
+    Hkv: int = 0  # key/value heads (grouped-query attention); 0 means H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv if self.Hkv else self.H
 
     @property
     def tau(self) -> float:
@@ -72,12 +80,16 @@ EXTREME_D128 = Workload("extreme_B1_H1_N131072_d128", 1, 1, 131072, 128, "bf16")
 # Causal shapes of the pages' isolated-layer timing table (B=4, H=12, bf16).
 CAUSAL_N4096 = Workload("causal_B4_H12_N4096_d64", 4, 12, 4096, 64, "bf16", causal=True)
 CAUSAL_N16384 = Workload("causal_B4_H12_N16384_d64", 4, 12, 16384, 64, "bf16", causal=True)
+# Grouped-query attention: 12 query heads share 4 key/value heads (and a
+# multi-query variant with one shared head).
+GQA_N8192 = Workload("gqa_B1_H12_Hkv4_N8192_d64", 1, 12, 8192, 64, "bf16", Hkv=4)
+MQA_N8192 = Workload("mqa_B1_H12_Hkv1_N8192_d64", 1, 12, 8192, 64, "bf16", Hkv=1)
 # A mid-size case for detailed profiles: inputs (~0.3 GB) larger than L2.
 PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
 
 WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PEAKED,
                                  MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128,
-                                 CAUSAL_N4096, CAUSAL_N16384, PROFILE)}
+                                 CAUSAL_N4096, CAUSAL_N16384, GQA_N8192, MQA_N8192, PROFILE)}
 
 
 def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
@@ -89,9 +101,11 @@ def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
+    kv_shape = (w.B, w.kv_heads, w.N, w.d)  # K, V, U_K, U_V (grouped-query attention)
     out = {}
     for name in NAMES:
-        out[name] = torch.randn(shape, generator=g, dtype=torch.float32)
+        out[name] = torch.randn(kv_shape if name in KV_NAMES else shape, generator=g,
+                                dtype=torch.float32)
     if w.dist == "scaled":
         s = w.d ** -0.25
         for name in ("Q", "K", "V"):
@@ -103,7 +117,7 @@ def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
     if w.peaked_k_rows:
         n_peak = int(math.floor(0.05 * w.N))
         for b in range(w.B):
-            for h in range(w.H):
+            for h in range(w.kv_heads):
                 idx = torch.randperm(w.N, generator=g)[:n_peak]
                 out["K"][b, h, idx, :] *= 4.0
     if w.dtype == "bf16":

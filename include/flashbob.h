@@ -21,7 +21,11 @@
  * (F = tau (U_Q K^T + Q U_K^T)) and E_i = sum_j P_ij d~P_ij.
  *
  * Layout: every N x d tensor is a contiguous row-major [B, H, N, d] array;
- * every length-N row vector is a contiguous [B, H, N] array.  Inputs are
+ * every length-N row vector is a contiguous [B, H, N] array.  Grouped-query
+ * attention ([FBN] 关键设计 3): the key-side tensors K, V, U_K, U_V, dKt, dVt
+ * are [B, Hkv, N, d] with Hkv dividing H; query head h uses key/value head
+ * h / (H / Hkv), and d~K, d~V of a shared head sum its query heads.  Hkv = H
+ * is ordinary multi-head attention, Hkv = 1 multi-query attention.  Inputs are
  * either all fp32 or all bf16 (Q, K, V, dO, U_Q, U_K, U_V; selected by
  * in_dtype); O, L, D and every output are fp32.
  *
@@ -63,26 +67,30 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
 /*
  * flashbob_prep: forward row state for the BoB ([FAB] sections 一/二,
  * [FBN] 关键设计 1 for D).
- *   in : Q, K, V, dO  [B,H,N,d] of in_dtype
+ *   in : Q, dO [B,H,N,d] and K, V [B,Hkv,N,d] of in_dtype
  *   out: O [B,H,N,d] fp32 (O = P V), L [B,H,N] fp32 (natural-log logsumexp of
  *        tau Q K^T per row), D [B,H,N] fp32 (D_i = dO_i . O_i)
  *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
  *   causal: 0 = full attention; 1 = query i sees keys j <= i only (the
  *        setting of [FBN] 实验关键数据); other values are rejected.
- *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535.  One launch: bf16 inputs
+ *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535; 1 <= Hkv, H % Hkv == 0.
+ *   One launch: bf16 inputs
  *   with d = 64 run a tcgen05 kernel, every other case fp32 CUDA cores.
  */
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
-                              float* O, float* L, float* D, int B, int H, int N, int d,
+                              float* O, float* L, float* D, int B, int H, int Hkv, int N,
+                              int d,
                               float tau, int causal, flashbob_dtype in_dtype, void* stream);
 
 /*
  * flashbob_bob: exact BoB of softmax attention with the two-pass schedule of
  * [FBN] 关键设计 2; the closed form and affine correction of [FBN] 关键设计 1.
- *   in : Q, K, V, dO, U_Q, U_K, U_V [B,H,N,d] of in_dtype; O [B,H,N,d] fp32;
+ *   in : Q, dO, U_Q [B,H,N,d] and K, V, U_K, U_V [B,Hkv,N,d] of in_dtype;
+ *        O [B,H,N,d] fp32;
  *        L, D [B,H,N] fp32 (as written by flashbob_prep with the same
  *        causal flag); tau and causal as in prep.
- *   out: dQt, dKt, dVt, ddOt [B,H,N,d] fp32 (d~Q, d~K, d~V, d~dO);
+ *   out: dQt, ddOt [B,H,N,d] and dKt, dVt [B,Hkv,N,d] fp32 (d~Q, d~dO, d~K,
+ *        d~V);
  *        alpha, E [B,H,N] fp32.  Every element is written exactly once.
  *   Pass 1 (row-resident) writes d~Q, d~dO, alpha, E; pass 2 (column-
  *   resident) reads alpha, E and writes d~K, d~V.  No N x N tensor is ever
@@ -94,7 +102,7 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
                              const void* dO, const float* L, const float* D, const void* UQ,
                              const void* UK, const void* UV, float tau, float* dQt, float* dKt,
                              float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
-                             int N, int d, int causal, flashbob_dtype in_dtype, void* stream);
+                             int Hkv, int N, int d, int causal, flashbob_dtype in_dtype, void* stream);
 
 /*
  * flashbob_bob_pass1 / flashbob_bob_pass2: the two launches of flashbob_bob,
@@ -110,14 +118,14 @@ flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, 
                                    const void* dO, const float* L, const float* D,
                                    const void* UQ, const void* UK, const void* UV, float tau,
                                    float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
-                                   int N, int d, int causal, flashbob_dtype in_dtype,
+                                   int Hkv, int N, int d, int causal, flashbob_dtype in_dtype,
                                    void* stream);
 
 flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, const void* dO,
                                    const float* L, const float* D, const float* alpha,
                                    const float* E, const void* UQ, const void* UK,
                                    const void* UV, float tau, float* dKt, float* dVt, int B,
-                                   int H, int N, int d, int causal, flashbob_dtype in_dtype,
+                                   int H, int Hkv, int N, int d, int causal, flashbob_dtype in_dtype,
                                    void* stream);
 
 /*

@@ -6,7 +6,7 @@ import numpy as np
 import torch
 
 from exact_second_order_gb300 import flashbob as fb
-from exact_second_order_gb300.inputs import NAMES, as_float64_numpy, make_inputs
+from exact_second_order_gb300.inputs import KV_NAMES, NAMES, as_float64_numpy, make_inputs
 from oracle import bob as orc
 
 # Gates: relative Frobenius error on every output.
@@ -35,7 +35,7 @@ def run_cuda(w, stream=None, fill_nan=True):
     dev = {k: v.cuda() for k, v in x.items()}
     O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal,
                       stream=stream)
-    out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan") if fill_nan else None)
+    out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan") if fill_nan else None, K=dev["K"])
     fb.bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"], dev["UK"], dev["UV"],
            w.tau, out=out, causal=w.causal, stream=stream)
     torch.cuda.synchronize()
@@ -52,19 +52,40 @@ def oracle_inputs(x):
 
 
 def full_oracle_errors(w, x, state, out, heads=None):
-    """Relative Frobenius errors of every output against the full oracle."""
+    """Relative Frobenius errors of every output against the full oracle, on
+    all (b, h) query heads or the listed ones; d~K and d~V are compared on
+    the key/value heads those query heads use (grouped-query attention: a
+    shared head's reference sums every query head of its group)."""
     args = oracle_inputs(x)
-    Q, K, V, dO = args[:4]
-    ref = orc.bob_batched(*args, w.tau, heads=heads, causal=w.causal)
-    O, L, D = (orc.prep_batched(Q, K, V, dO, w.tau, causal=w.causal) if heads is None
-               else (None, None, None))
+    Q, K, V, dO, UQ, UK, UV = args
+    G = w.H // w.kv_heads
+    qheads = heads if heads is not None else [(b, h) for b in range(w.B) for h in range(w.H)]
+    kvheads = sorted({(b, h // G) for b, h in qheads})
+    ref_q = {k: {} for k in ("dQt", "ddOt", "alpha", "E", "L", "D")}
+    ref_k = {"dKt": {}, "dVt": {}}
+    for b, g in kvheads:
+        hs = slice(g * G, (g + 1) * G)
+        r = orc.bob_gqa(Q[b, hs], K[b, g:g + 1], V[b, g:g + 1], dO[b, hs], UQ[b, hs],
+                        UK[b, g:g + 1], UV[b, g:g + 1], w.tau, w.causal)
+        for k in ref_q:
+            for i in range(G):
+                ref_q[k][(b, g * G + i)] = r[k][i]
+        for k in ref_k:
+            ref_k[k][(b, g)] = r[k][0]
     errs = {}
-    sel = (lambda a: a) if heads is None else (lambda a: np.stack([a[b, h] for b, h in heads]))
-    for k in MAT_KEYS + ROW_KEYS:
-        errs[k] = rel_fro(sel(to_np(out[k])), sel(ref[k]))
-    errs["L"] = rel_fro(sel(to_np(state["L"])), sel(ref["L"]))
-    errs["D"] = rel_fro(sel(to_np(state["D"])), sel(ref["D"]))
-    if O is not None:
+    for k in ("dQt", "ddOt", "alpha", "E"):
+        errs[k] = rel_fro(np.stack([to_np(out[k][b, h]) for b, h in qheads]),
+                          np.stack([ref_q[k][(b, h)] for b, h in qheads]))
+    for k in ("dKt", "dVt"):
+        errs[k] = rel_fro(np.stack([to_np(out[k][b, g]) for b, g in kvheads]),
+                          np.stack([ref_k[k][(b, g)] for b, g in kvheads]))
+    for k in ("L", "D"):
+        errs[k] = rel_fro(np.stack([to_np(state[k][b, h]) for b, h in qheads]),
+                          np.stack([ref_q[k][(b, h)] for b, h in qheads]))
+    if heads is None:
+        O = np.stack([np.stack([orc.prep(Q[b, h], K[b, h // G], V[b, h // G], dO[b, h], w.tau,
+                                         w.causal)[0] for h in range(w.H)])
+                      for b in range(w.B)])
         errs["O"] = rel_fro(to_np(state["O"]), O)
     return errs
 
@@ -79,7 +100,8 @@ def sampled_row_errors(w, x, out, state, n_rows=256, seed=1234, heads=None):
     ref = {k: [] for k in got}
     for b, h in heads:
         rows = np.sort(rng.choice(N, size=min(n_rows, N), replace=False))
-        args = [as_float64_numpy(x[k][b, h]) for k in NAMES]
+        g = h // (w.H // w.kv_heads)  # shared key/value head
+        args = [as_float64_numpy(x[k][b, g if k in KV_NAMES else h]) for k in NAMES]
         r = orc.bob_rows(*args, w.tau, rows, causal=w.causal)
         for k in got:
             src = out[k] if k in out else state[k]

@@ -63,8 +63,9 @@ def test_tile_sizes(lib):
         fb.FLASHBOB_ERR_INVALID_ARG
 
 
-def _bob_raw(lib, ptrs, tau=0.125, B=1, H=1, N=8, d=64, dtype=0, causal=0):
-    return lib.flashbob_bob(*ptrs[:10], tau, *ptrs[10:], B, H, N, d, causal, dtype, None)
+def _bob_raw(lib, ptrs, tau=0.125, B=1, H=1, N=8, d=64, dtype=0, causal=0, Hkv=None):
+    Hkv = H if Hkv is None else Hkv
+    return lib.flashbob_bob(*ptrs[:10], tau, *ptrs[10:], B, H, Hkv, N, d, causal, dtype, None)
 
 
 def _fake_ptrs(n=16, stride=1 << 20, base=1 << 32):
@@ -83,7 +84,7 @@ def test_bob_rejects_bad_arguments_on_the_host(lib):
     # sizes and tau
     for kw in ({"B": 0}, {"H": -1}, {"N": 0}, {"d": 0}, {"tau": 0.0}, {"tau": -1.0},
                {"tau": float("nan")}, {"tau": float("inf")}, {"dtype": 3}, {"causal": 2},
-               {"causal": -1}):
+               {"causal": -1}, {"Hkv": 0}, {"H": 4, "Hkv": 3}, {"H": 2, "Hkv": 4}):
         assert _bob_raw(lib, ok, **kw) == E.FLASHBOB_ERR_INVALID_ARG, kw
     assert _bob_raw(lib, ok, d=129) == E.FLASHBOB_ERR_UNSUPPORTED
     assert _bob_raw(lib, ok, H=70000) == E.FLASHBOB_ERR_UNSUPPORTED
@@ -104,8 +105,9 @@ def test_bob_rejects_bad_arguments_on_the_host(lib):
 def test_prep_rejects_bad_arguments_on_the_host(lib):
     ok = _fake_ptrs(7)
 
-    def call(p=ok, B=1, H=1, N=8, d=64, tau=0.125, dtype=0, causal=0):
-        return lib.flashbob_prep(*p, B, H, N, d, tau, causal, dtype, None)
+    def call(p=ok, B=1, H=1, N=8, d=64, tau=0.125, dtype=0, causal=0, Hkv=None):
+        Hkv = H if Hkv is None else Hkv
+        return lib.flashbob_prep(*p, B, H, Hkv, N, d, tau, causal, dtype, None)
     for i in range(7):
         p = list(ok)
         p[i] = None
@@ -117,6 +119,7 @@ def test_prep_rejects_bad_arguments_on_the_host(lib):
     assert call(tau=float("nan")) == fb.FLASHBOB_ERR_INVALID_ARG
     assert call(d=200) == fb.FLASHBOB_ERR_UNSUPPORTED
     assert call(causal=3) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert call(H=6, Hkv=4) == fb.FLASHBOB_ERR_INVALID_ARG
     p = list(ok)
     p[4] = p[3]
     assert call(p) == fb.FLASHBOB_ERR_INVALID_ARG
@@ -137,22 +140,22 @@ def test_pass_entry_points_reject_bad_arguments_on_the_host(lib):
     p1 = ok[:15]
     bad = list(p1)
     bad[3] = None  # O
-    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 1, 8, 64, 0, 0, None) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     bad = list(p1)
     bad[10] = bad[4]  # d~Q over dO
-    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 1, 8, 64, 0, 0, None) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     p2 = ok[:13]
     bad = list(p2)
     bad[6] = None  # alpha
-    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 1, 8, 64, 0, 0, None) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     bad = list(p2)
     bad[11] = bad[6]  # d~K over alpha
-    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 1, 8, 64, 0, 0, None) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     bad = list(p2)
     bad[12] += 4
-    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 1, 8, 64, 0, 0, None) == \
         fb.FLASHBOB_ERR_MISALIGNED

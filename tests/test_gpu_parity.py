@@ -82,7 +82,7 @@ def _memory_checked_run(w):
     x = wl.make_inputs(w)
     dev = {k: v.cuda() for k, v in x.items()}
     O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
-    out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan"))
+    out = fb.alloc_bob_outputs(dev["Q"], fill=float("nan"), K=dev["K"])
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats()
     before_alloc = torch.cuda.memory_allocated()
@@ -163,4 +163,33 @@ def test_causal_pages_shape_sampled_rows():
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
     full = full_oracle_errors(w, x, state, out, heads=[(2, 7)])
+    assert max(full.values()) <= TOL["bf16"], full
+
+
+# --------------------------------------------------------------------------
+# Grouped-query / multi-query attention (shared key/value heads)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (4, 1), (6, 3)])
+@pytest.mark.parametrize("N", [1, 65, 300])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96)])
+def test_gqa_small_shapes(H, Hkv, N, dtype, d):
+    _check_full(wl.small_workload(2, H, N, d, dtype, seed=N + H, Hkv=Hkv))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_causal_bf16(causal):
+    _check_full(wl.small_workload(1, 4, 333, 64, "bf16", seed=8, Hkv=2, causal=causal))
+
+
+@pytest.mark.parametrize("w", [wl.GQA_N8192, wl.MQA_N8192], ids=lambda w: w.name)
+def test_gqa_workloads_sampled_rows(w):
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    heads = [(0, 0), (0, 5), (0, 11)]
+    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=heads)
+    assert max(errs.values()) <= TOL["bf16"], errs
+    res = column_sum_residuals(out)
+    assert max(res.values()) <= TOL["bf16"], res
+    full = full_oracle_errors(w, x, state, out, heads=[(0, 0)])
     assert max(full.values()) <= TOL["bf16"], full
