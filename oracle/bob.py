@@ -4,9 +4,11 @@ TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py``.  The CUDA library never imports,
 links or calls it, and it shares no code with the CUDA path.
 
-Every function works on ONE (batch, head) slice: 2-D numpy arrays of shape
-``[N, d]`` (rows are sequence positions) in float64, plus the scale ``tau``.
-The batched helpers at the end loop over ``[B, H]``.
+Every function works on ONE (batch, head) slice: 2-D numpy arrays in
+float64 (rows are sequence positions), plus the scale ``tau``.  The query-side
+arrays Q, dO, U_Q are ``[N_q, d]`` and the key-side arrays K, V, U_K, U_V are
+``[N_k, d]``; N_q = N_k is ordinary self-attention, N_q != N_k rectangular
+attention.  The batched helpers at the end loop over ``[B, H]``.
 
 Sources (web pages on the method; sections named as on the pages):
 
@@ -43,10 +45,13 @@ import numpy as np
 # Forward, row state and first backward  ([FAB] sections 一 and 二)
 # --------------------------------------------------------------------------
 
-def causal_mask(N):
+def causal_mask(Nq, Nk=None):
     """True where key j is visible from query i (j <= i): the causal mask of
-    the pages' benchmarks ([FBN] 实验关键数据)."""
-    return np.tril(np.ones((N, N), dtype=bool))
+    the pages' benchmarks ([FBN] 实验关键数据).  For N_q != N_k the same
+    rule on absolute positions (the mask's diagonal starts at the top left),
+    so every query row sees at least key 0."""
+    Nk = Nq if Nk is None else Nk
+    return np.tril(np.ones((Nq, Nk), dtype=bool))
 
 
 def forward(Q, K, V, tau, causal=False):
@@ -58,7 +63,7 @@ def forward(Q, K, V, tau, causal=False):
     """
     S = tau * (Q @ K.T)
     if causal:
-        S = np.where(causal_mask(Q.shape[0]), S, -np.inf)
+        S = np.where(causal_mask(Q.shape[0], K.shape[0]), S, -np.inf)
     m = S.max(axis=1, keepdims=True)
     L = m[:, 0] + np.log(np.exp(S - m).sum(axis=1))
     P = np.exp(S - L[:, None])
@@ -227,7 +232,8 @@ def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     loop over (i, j, k), so a transposed operand or a dropped term in the
     matrix form shows up as a mismatch.
     """
-    N, d = Q.shape
+    Nq, d = Q.shape
+    Nk = K.shape[0]
 
     def dot(a, b):
         s = 0.0
@@ -238,35 +244,35 @@ def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     def visible(i, j):
         return j <= i or not causal
 
-    S = [[tau * dot(Q[i], K[j]) for j in range(N)] for i in range(N)]
-    P = [[0.0] * N for _ in range(N)]
-    L = [0.0] * N
-    for i in range(N):
-        m = max(S[i][j] for j in range(N) if visible(i, j))
+    S = [[tau * dot(Q[i], K[j]) for j in range(Nk)] for i in range(Nq)]
+    P = [[0.0] * Nk for _ in range(Nq)]
+    L = [0.0] * Nq
+    for i in range(Nq):
+        m = max(S[i][j] for j in range(Nk) if visible(i, j))
         z = 0.0
-        for j in range(N):
+        for j in range(Nk):
             if visible(i, j):
                 z += np.exp(S[i][j] - m)
         L[i] = m + np.log(z)
-        for j in range(N):
+        for j in range(Nk):
             P[i][j] = np.exp(S[i][j] - L[i]) if visible(i, j) else 0.0
-    O = [[sum(P[i][j] * V[j][k] for j in range(N)) for k in range(d)] for i in range(N)]
-    D = [dot(dO[i], O[i]) for i in range(N)]
-    dP = [[dot(dO[i], V[j]) for j in range(N)] for i in range(N)]
-    F = [[tau * (dot(UQ[i], K[j]) + dot(Q[i], UK[j])) for j in range(N)] for i in range(N)]
-    G = [[dot(dO[i], UV[j]) for j in range(N)] for i in range(N)]
-    alpha = [sum(P[i][j] * F[i][j] for j in range(N)) for i in range(N)]
-    dPt = [[F[i][j] * (dP[i][j] - D[i]) + G[i][j] - alpha[i] * dP[i][j] for j in range(N)]
-           for i in range(N)]
-    E = [sum(P[i][j] * dPt[i][j] for j in range(N)) for i in range(N)]
-    dS = [[P[i][j] * (dP[i][j] - D[i]) for j in range(N)] for i in range(N)]
-    dSt = [[P[i][j] * (dPt[i][j] - E[i]) for j in range(N)] for i in range(N)]
-    dQt = np.zeros((N, d))
-    dKt = np.zeros((N, d))
-    dVt = np.zeros((N, d))
-    ddOt = np.zeros((N, d))
-    for i in range(N):
-        for j in range(N):
+    O = [[sum(P[i][j] * V[j][k] for j in range(Nk)) for k in range(d)] for i in range(Nq)]
+    D = [dot(dO[i], O[i]) for i in range(Nq)]
+    dP = [[dot(dO[i], V[j]) for j in range(Nk)] for i in range(Nq)]
+    F = [[tau * (dot(UQ[i], K[j]) + dot(Q[i], UK[j])) for j in range(Nk)] for i in range(Nq)]
+    G = [[dot(dO[i], UV[j]) for j in range(Nk)] for i in range(Nq)]
+    alpha = [sum(P[i][j] * F[i][j] for j in range(Nk)) for i in range(Nq)]
+    dPt = [[F[i][j] * (dP[i][j] - D[i]) + G[i][j] - alpha[i] * dP[i][j] for j in range(Nk)]
+           for i in range(Nq)]
+    E = [sum(P[i][j] * dPt[i][j] for j in range(Nk)) for i in range(Nq)]
+    dS = [[P[i][j] * (dP[i][j] - D[i]) for j in range(Nk)] for i in range(Nq)]
+    dSt = [[P[i][j] * (dPt[i][j] - E[i]) for j in range(Nk)] for i in range(Nq)]
+    dQt = np.zeros((Nq, d))
+    dKt = np.zeros((Nk, d))
+    dVt = np.zeros((Nk, d))
+    ddOt = np.zeros((Nq, d))
+    for i in range(Nq):
+        for j in range(Nk):
             w = P[i][j] * (F[i][j] - alpha[i])
             for k in range(d):
                 dQt[i, k] += tau * (dSt[i][j] * K[j][k] + dS[i][j] * UK[j][k])
@@ -283,10 +289,10 @@ def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
 
 def prep_batched(Q, K, V, dO, tau, causal=False):
     """``prep`` for every (b, h) of [B, H, N, d] arrays."""
-    B, H, N, d = Q.shape
-    O = np.empty((B, H, N, d))
-    L = np.empty((B, H, N))
-    D = np.empty((B, H, N))
+    B, H, Nq, d = Q.shape
+    O = np.empty((B, H, Nq, d))
+    L = np.empty((B, H, Nq))
+    D = np.empty((B, H, Nq))
     for b in range(B):
         for h in range(H):
             O[b, h], L[b, h], D[b, h] = prep(Q[b, h], K[b, h], V[b, h], dO[b, h], tau, causal)
@@ -295,10 +301,12 @@ def prep_batched(Q, K, V, dO, tau, causal=False):
 
 def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None, causal=False):
     """``bob`` for every (b, h) (or the listed (b, h) pairs)."""
-    B, H, N, d = Q.shape
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    shapes = {"dQt": (B, H, Nq, d), "ddOt": (B, H, Nq, d), "dKt": (B, H, Nk, d),
+              "dVt": (B, H, Nk, d)}
     keys = ("dQt", "dKt", "dVt", "ddOt", "alpha", "E", "L", "D")
-    out = {k: np.full((B, H, N, d) if k in ("dQt", "dKt", "dVt", "ddOt") else (B, H, N),
-                      np.nan) for k in keys}
+    out = {k: np.full(shapes.get(k, (B, H, Nq)), np.nan) for k in keys}
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in pairs:
         r = bob(Q[b, h], K[b, h], V[b, h], dO[b, h], UQ[b, h], UK[b, h], UV[b, h], tau, causal)
@@ -312,7 +320,7 @@ def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None, causal=False):
 # --------------------------------------------------------------------------
 
 def phi_gqa(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
-    """Phi for [H, N, d] query-side arrays and [H_kv, N, d] key-side arrays:
+    """Phi for [H, N_q, d] query-side arrays and [H_kv, N_k, d] key-side arrays:
     query head h attends to key/value head h // (H / H_kv), and the first
     backward's dK, dV of a shared head sum the contributions of its query
     heads ([FBN] 关键设计 3), so Phi is the sum of the per-head objectives."""

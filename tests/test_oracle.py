@@ -431,3 +431,77 @@ def test_gqa_with_one_group_is_mha():
         m = orc.bob(Q[h], K[h], V[h], dO[h], UQ[h], UK[h], UV[h], 0.4)
         for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
             assert rel(r[key][h], m[key]) < 1e-14, key
+
+
+# --------------------------------------------------------------------------
+# Rectangular attention (N_q query rows, N_k key rows)
+# --------------------------------------------------------------------------
+
+def _rand_rect(Nq, Nk, d, seed):
+    rng = np.random.default_rng(seed)
+    q = [rng.standard_normal((Nq, d)) for _ in range(3)]  # Q, dO, U_Q
+    k = [rng.standard_normal((Nk, d)) for _ in range(4)]  # K, V, U_K, U_V
+    return q[0], k[0], k[1], q[1], q[2], k[2], k[3]
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(4, 9, False), (9, 4, False), (5, 8, True),
+                                          (8, 5, True)])
+def test_rectangular_bob_matches_fd_of_phi(Nq, Nk, causal):
+    Q, K, V, dO, UQ, UK, UV = _rand_rect(Nq, Nk, 3, 50 + Nq)
+    tau = 0.45
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, tau, causal)
+    assert r["dQt"].shape == (Nq, 3) and r["dKt"].shape == (Nk, 3)
+    args = [Q, K, V, dO]
+    for pos, key in enumerate(("dQt", "dKt", "dVt", "ddOt")):
+        def f(X, pos=pos):
+            a = list(args)
+            a[pos] = X
+            return orc.phi(*a, UQ, UK, UV, tau, causal)
+        assert rel(r[key], _fd_grad(f, args[pos])) < RTOL_FD, key
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rectangular_matches_bruteforce_rows_affine_and_torch(causal):
+    torch = pytest.importorskip("torch")
+    Nq, Nk, d = 11, 7, 4
+    args = _rand_rect(Nq, Nk, d, 51)
+    tau = 0.5
+    r = orc.bob(*args, tau, causal)
+    b = orc.bob_bruteforce(*args, tau, causal)
+    a = orc.bob_affine(*args, tau, causal)
+    rows = [0, 3, 6, 7, 10]
+    s = orc.bob_rows(*args, tau, rows, causal=causal)
+    for key in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+        assert rel(r[key], b[key]) < 1e-12, key
+    for key in ("dQt", "ddOt", "alpha", "E"):
+        assert rel(a[key], r[key]) < 1e-12, key
+        assert rel(s[key], r[key][rows]) < 1e-12, key
+    # torch fp64 autograd double-backward, mask on absolute positions (j <= i)
+    tq, tk, tv, tdo = (torch.tensor(x, requires_grad=True) for x in (args[0], args[1], args[2],
+                                                                      args[3]))
+    uq, uk, uv = (torch.tensor(x) for x in args[4:])
+    sc = tau * tq @ tk.T
+    if causal:
+        keep = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None]
+        sc = sc.masked_fill(~keep, float("-inf"))
+    out = torch.softmax(sc, dim=-1) @ tv
+    dq, dk, dv = torch.autograd.grad(out, (tq, tk, tv), tdo, create_graph=True)
+    ph = (dq * uq).sum() + (dk * uk).sum() + (dv * uv).sum()
+    g = torch.autograd.grad(ph, (tq, tk, tv, tdo))
+    for key, t in zip(("dQt", "dKt", "dVt", "ddOt"), g):
+        assert rel(r[key], t.numpy()) < 1e-12, key
+
+
+def test_rectangular_causal_unseen_keys_and_invariants():
+    """Keys j >= N_q are seen by no query under the causal mask: their d~K,
+    d~V are exactly zero; the shift invariances hold over the key axis."""
+    Nq, Nk, d = 5, 9, 3
+    Q, K, V, dO, UQ, UK, UV = _rand_rect(Nq, Nk, d, 52)
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, 0.7, causal=True)
+    assert np.abs(r["dKt"][Nq:]).max() == 0.0 and np.abs(r["dVt"][Nq:]).max() == 0.0
+    for causal in (False, True):
+        r = orc.bob(Q, K, V, dO, UQ, UK, UV, 0.7, causal=causal)
+        ph = orc.phi(Q, K, V, dO, UQ, UK, UV, 0.7, causal=causal)
+        assert abs((r["ddOt"] * dO).sum() - ph) < 1e-12 * (abs(ph) + 1)
+        for key in ("dKt", "dVt"):
+            assert np.abs(r[key].sum(axis=0)).max() < 1e-12 * np.abs(r[key]).max() * Nk
