@@ -27,9 +27,11 @@
 // TMEM: [0,64) d~K, [64,128) d~V accumulators; [128,384) one score buffer
 // S^T | F'^T | dP^T | G^T (64 columns each); [384,480) the bf16 A operands
 // dS^T, d~S^T, W^T of the output GEMMs.  Because the operands have their own
-// columns, the score buffer is free as soon as both warpgroups have read it
-// into registers, and the score GEMMs of the next tile run while the
-// warpgroups do the arithmetic of this one.
+// columns, the score buffer is released as soon as the warpgroups have read
+// it into registers, in two halves: S^T | F'^T first (read before any
+// arithmetic), then dP^T | G^T.  The score GEMMs of the next tile are issued
+// in the same two halves, so the S/F' half of tile t + 1 runs on the tensor
+// pipe while the warpgroups still read and process dP/G of tile t.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -54,7 +56,8 @@ struct Smem2 {
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
   uint64_t sc_full;   // score GEMMs of a tile have completed
-  uint64_t sc_free;   // both warpgroups have read the score buffer (8 warps)
+  uint64_t sf_free;   // both warpgroups have read S^T and F'^T (8 warps)
+  uint64_t pg_free;   // both warpgroups have read dP^T and G^T (8 warps)
   uint64_t op_ready;  // the operands of a tile are in TMEM (8 warps)
   uint64_t op_free;   // the output GEMMs of a tile have completed
   uint64_t out_full;
@@ -103,36 +106,39 @@ __device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t
   }
 }
 
-__device__ __forceinline__ void load_scores(uint32_t sc, int col, uint32_t (&s)[16],
-                                            uint32_t (&dp)[16], uint32_t (&f)[16],
-                                            uint32_t (&g)[16]) {
-  tmem_ld16(sc + kColS + col, s);
-  tmem_ld16(sc + kColdP + col, dp);
-  tmem_ld16(sc + kColF + col, f);
-  tmem_ld16(sc + kColG + col, g);
-}
-
-// The 32 query rows of one warpgroup: read both 16-row chunks of the scores
-// (then release the buffer), form the operands, and write them to the
-// operand area once the previous tile's output GEMMs are done with it.
+// The 32 query rows of one warpgroup: read S^T and F'^T of both 16-row
+// chunks and release them, then dP^T and G^T chunk by chunk (releasing them
+// after the second), form the operands, and write them to the operand area
+// once the previous tile's output GEMMs are done with it.
 template <bool MASKED>
 __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const float4* scal,
                                         int ibase, int gj, float c1, float tau, Smem2& sm,
                                         int t, volatile int* abort_flag, unsigned int* err) {
   uint32_t a_ds[8], a_dst[8], a_w[8], b_ds[8], b_dst[8], b_w[8];
+  const int col = 32 * wg;
+  uint32_t s0[16], f0[16], s1[16], f1[16];
+  tmem_ld16(sc + kColS + col, s0);
+  tmem_ld16(sc + kColF + col, f0);
+  tmem_ld16(sc + kColS + col + 16, s1);
+  tmem_ld16(sc + kColF + col + 16, f1);
+  tmem_wait_ld();
+  tc_fence_before();
+  warp_arrive(&sm.sf_free);  // this warp is done with S^T | F'^T
   {
-    uint32_t s[16], dp[16], f[16], g[16];
-    load_scores(sc, 32 * wg, s, dp, f, g);
+    uint32_t dp[16], g[16];
+    tmem_ld16(sc + kColdP + col, dp);
+    tmem_ld16(sc + kColG + col, g);
     tmem_wait_ld();
-    p2_chunk<MASKED>(s, dp, f, g, scal, ibase, gj, c1, tau, a_ds, a_dst, a_w);
+    p2_chunk<MASKED>(s0, dp, f0, g, scal, ibase, gj, c1, tau, a_ds, a_dst, a_w);
   }
   {
-    uint32_t s[16], dp[16], f[16], g[16];
-    load_scores(sc, 32 * wg + 16, s, dp, f, g);
+    uint32_t dp[16], g[16];
+    tmem_ld16(sc + kColdP + col + 16, dp);
+    tmem_ld16(sc + kColG + col + 16, g);
     tmem_wait_ld();
     tc_fence_before();
-    warp_arrive(&sm.sc_free);  // this warp is done with the score buffer
-    p2_chunk<MASKED>(s, dp, f, g, scal + 16, ibase + 16, gj, c1, tau, b_ds, b_dst, b_w);
+    warp_arrive(&sm.pg_free);  // this warp is done with dP^T | G^T
+    p2_chunk<MASKED>(s1, dp, f1, g, scal + 16, ibase + 16, gj, c1, tau, b_ds, b_dst, b_w);
   }
   if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
   tc_fence_after();
@@ -185,7 +191,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.st_empty[s], 1);
     }
     mbar_init(&sm.sc_full, 1);
-    mbar_init(&sm.sc_free, 8);
+    mbar_init(&sm.sf_free, 8);
+    mbar_init(&sm.pg_free, 8);
     mbar_init(&sm.op_ready, 8);
     mbar_init(&sm.op_free, 1);
     mbar_init(&sm.out_full, 1);
@@ -238,17 +245,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
     const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
     const uint32_t sc = tbase + kSc;
-    auto issue_scores = [&](int t) {
+    // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
+    auto issue_sf = [&](int t) {
       const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t o = 2 * kk;  // 16 bf16 along d = 32 bytes >> 4
-          const uint32_t acc = kk > 0;
-          mma_ss(sc + kColS, dK + o, dQ0 + so + o, idS128, acc);    // [S^T | F'^T] = K [Q; U_Q]^T
-          mma_ss(sc + kColF, dUK + o, dQ0 + so + o, idS64, 1);      // F'^T += U_K Q^T
-          mma_ss(sc + kColdP, dV + o, ddO0 + so + o, idS64, acc);   // dP^T = V dO^T
-          mma_ss(sc + kColG, dUV + o, ddO0 + so + o, idS64, acc);   // G^T  = U_V dO^T
+          mma_ss(sc + kColS, dK + o, dQ0 + so + o, idS128, kk > 0);  // [S^T | F'^T] = K [Q; U_Q]^T
+          mma_ss(sc + kColF, dUK + o, dQ0 + so + o, idS64, 1);       // F'^T += U_K Q^T
+        }
+      }
+      __syncwarp();
+    };
+    auto issue_pg = [&](int t) {
+      const uint64_t so = (uint64_t)((t % NST) * 3 * TILE_BYTES) >> 4;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t o = 2 * kk;
+          mma_ss(sc + kColdP, dV + o, ddO0 + so + o, idS64, kk > 0);  // dP^T = V dO^T
+          mma_ss(sc + kColG, dUV + o, ddO0 + so + o, idS64, kk > 0);  // G^T  = U_V dO^T
         }
         mma_commit(&sm.sc_full);
       }
@@ -273,14 +290,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     bool ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
     for (int t = 0; ok && t < T; ++t) {
-      if (t > 0) {  // both warpgroups hold the scores of tile t - 1 in registers
-        ok = mbar_wait_warp(&sm.sc_free, (t - 1) & 1, abort_flag, err);
+      if (t > 0) {  // both warpgroups hold S^T, F'^T of tile t - 1 in registers
+        ok = mbar_wait_warp(&sm.sf_free, (t - 1) & 1, abort_flag, err);
         if (!ok) break;
       }
       ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
       if (!ok) break;
       tc_fence_after();
-      issue_scores(t);
+      issue_sf(t);
+      if (t > 0) {  // ... and dP^T, G^T
+        ok = mbar_wait_warp(&sm.pg_free, (t - 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      issue_pg(t);
       if (t > 0) {
         ok = mbar_wait_warp(&sm.op_ready, (t - 1) & 1, abort_flag, err);
         if (!ok) break;
