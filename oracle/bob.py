@@ -183,6 +183,33 @@ def bob_affine(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
 
 
 # --------------------------------------------------------------------------
+# Forward-mode derivative of attention (the JVP by-product of pass 1)
+# --------------------------------------------------------------------------
+
+def attention_jvp(Q, K, V, UQ, UK, UV, tau, causal=False):
+    """Directional derivative of the attention forward along (U_Q, U_K, U_V),
+    by its definition: with S = tau Q K^T and its tangent
+    S' = tau (U_Q K^T + Q U_K^T), the softmax tangent is
+    P' = P o (S' - rowsum(P o S')), so that
+
+        L' = rowsum(P o S'),   O' = P' V + P U_V.
+
+    Returns (O, L, O', L').  S' is the matrix F of [FBN] 关键设计 1, and
+    L', O' are the alpha and d~dO that pass 1 produces (reading them as a
+    JVP is this module's reading; the pins check it against finite
+    differences and torch forward-mode AD).
+    """
+    S, P, O, L = forward(Q, K, V, tau, causal)
+    Sd = tau * (UQ @ K.T + Q @ UK.T)
+    if causal:
+        Sd = np.where(causal_mask(Q.shape[0], K.shape[0]), Sd, 0.0)
+    Ld = (P * Sd).sum(axis=1)
+    Pd = P * (Sd - Ld[:, None])
+    Od = Pd @ V + P @ UV
+    return O, L, Od, Ld
+
+
+# --------------------------------------------------------------------------
 # One row at a time: O(N d) per row, for long sequences
 # --------------------------------------------------------------------------
 

@@ -505,3 +505,54 @@ def test_rectangular_causal_unseen_keys_and_invariants():
         assert abs((r["ddOt"] * dO).sum() - ph) < 1e-12 * (abs(ph) + 1)
         for key in ("dKt", "dVt"):
             assert np.abs(r[key].sum(axis=0)).max() < 1e-12 * np.abs(r[key]).max() * Nk
+
+
+# --------------------------------------------------------------------------
+# Attention JVP (forward-mode derivative along U_Q, U_K, U_V)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(9, 9, False), (9, 9, True), (5, 11, True),
+                                          (11, 5, False)])
+def test_attention_jvp_matches_fd_of_the_forward(Nq, Nk, causal):
+    Q, K, V, _, UQ, UK, UV = _rand_rect(Nq, Nk, 4, 60 + Nq + Nk)
+    tau = 0.45
+    O, L, Od, Ld = orc.attention_jvp(Q, K, V, UQ, UK, UV, tau, causal)
+    h = 1e-5
+    _, _, Op, Lp = orc.forward(Q + h * UQ, K + h * UK, V + h * UV, tau, causal)
+    _, _, Om, Lm = orc.forward(Q - h * UQ, K - h * UK, V - h * UV, tau, causal)
+    assert rel(Od, (Op - Om) / (2 * h)) < 1e-8
+    assert rel(Ld, (Lp - Lm) / (2 * h)) < 1e-8
+    _, _, O0, L0 = orc.forward(Q, K, V, tau, causal)
+    assert rel(O, O0) < 1e-15 and rel(L, L0) < 1e-15
+
+
+def test_attention_jvp_matches_torch_forward_ad():
+    torch = pytest.importorskip("torch")
+    import torch.autograd.forward_ad as fwAD
+    Nq, Nk, d = 7, 10, 3
+    Q, K, V, _, UQ, UK, UV = _rand_rect(Nq, Nk, d, 61)
+    tau = 0.6
+    for causal in (False, True):
+        O, L, Od, Ld = orc.attention_jvp(Q, K, V, UQ, UK, UV, tau, causal)
+        with fwAD.dual_level():
+            q = fwAD.make_dual(torch.tensor(Q), torch.tensor(UQ))
+            k = fwAD.make_dual(torch.tensor(K), torch.tensor(UK))
+            v = fwAD.make_dual(torch.tensor(V), torch.tensor(UV))
+            sc = tau * q @ k.T
+            if causal:
+                keep = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None]
+                sc = sc.masked_fill(~keep, float("-inf"))
+            lse = torch.logsumexp(sc, dim=-1)
+            out = torch.softmax(sc, dim=-1) @ v
+            t_od = fwAD.unpack_dual(out).tangent.numpy()
+            t_ld = fwAD.unpack_dual(lse).tangent.numpy()
+        assert rel(Od, t_od) < 1e-12 and rel(Ld, t_ld) < 1e-12
+
+
+def test_attention_jvp_is_the_bob_by_product():
+    """alpha and d~dO of the BoB equal L' and O' for any dO."""
+    Q, K, V, dO, UQ, UK, UV = _rand_rect(8, 12, 4, 62)
+    _, _, Od, Ld = orc.attention_jvp(Q, K, V, UQ, UK, UV, 0.5, True)
+    for scale in (1.0, -3.0):
+        r = orc.bob(Q, K, V, scale * dO, UQ, UK, UV, 0.5, True)
+        assert rel(r["ddOt"], Od) < 1e-13 and rel(r["alpha"], Ld) < 1e-13
