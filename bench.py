@@ -26,7 +26,7 @@ if ROOT not in sys.path:
 METRIC = "BoB TFLOP/s & % of GB300 bf16 tensor peak vs N (d=64); ms/call"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "long_B1_H4_N65536_d64"
-PASS1_GEMMS, PASS2_GEMMS = 11, 8  # each 2 N^2 d flops per (batch, head)
+PASS1_GEMMS, PASS2_GEMMS = 11, 8  # each 2 d flops per visible (query, key) pair
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_long_context.txt")
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -168,9 +168,9 @@ def oracle_rows_sample(w, x, seconds: float, rows_per_chunk: int = 16, seed: int
 
 
 def row_flops(w) -> float:
-    """FLOPs credited per oracle row: the row-side GEMMs (pass 1 list); a
-    causal row sees half the keys on average."""
-    return (0.5 if w.causal else 1.0) * 2.0 * PASS1_GEMMS * w.N * w.d
+    """FLOPs credited per oracle row: the row-side GEMMs (pass 1 list) over
+    the keys an average query row sees."""
+    return 2.0 * PASS1_GEMMS * (w.pairs / w.N) * w.d
 
 
 def run_reference(args, w, rank, world):
@@ -193,7 +193,8 @@ def run_reference(args, w, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
-                                        "d": w.d, "Hkv": w.kv_heads, "causal": w.causal},
+                                        "Nk": w.kv_len, "d": w.d, "Hkv": w.kv_heads,
+                                        "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{t_rows} seeded rows of head (0,0) through oracle.bob_rows "
                                    f"(fp64 numpy), {row_flops(w):.3e} flops credited per row"},
@@ -270,8 +271,8 @@ def main():
     total_ms = reduce_max(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
     heads = w.B * w.H
-    # one N x N x d GEMM per (batch, head); half of it under the causal mask
-    unit_flops = (0.5 if w.causal else 1.0) * 2.0 * w.N * w.N * w.d * heads
+    # one Nq x Nk x d GEMM per (batch, head), over the visible pairs only
+    unit_flops = 2.0 * w.pairs * w.d * heads
     flops = (PASS1_GEMMS + PASS2_GEMMS) * unit_flops
     value = job_tflops(flops, args.steps, world, total_ms)
 
@@ -328,10 +329,11 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "N": w.N, "d": w.d,
-                   "causal": w.causal,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "N": w.N,
+                   "Nk": w.kv_len, "d": w.d, "causal": w.causal,
                    "tau": w.tau, "flops_per_step_per_gpu": flops,
-                   "flop_convention": "38*N^2*d*B*H (19 GEMMs of 2*N^2*d)",
+                   "flop_convention": "38*N^2*d*B*H (19 GEMMs of 2*N^2*d); rectangular "
+                                      "N*Nk for N^2, causal the pairs j <= i",
                    "l2": f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
                          f"{L2_BYTES / 2**20:.0f} MiB",
                    "pass1_ms": p1_ms, "pass2_ms": p2_ms,

@@ -29,8 +29,9 @@ bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-flashbob_status check_sizes(int B, int H, int Hkv, int N, int d, float tau) {
-  if (B <= 0 || H <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return FLASHBOB_ERR_INVALID_ARG;
+flashbob_status check_sizes(int B, int H, int Hkv, int Nq, int Nk, int d, float tau) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0)
+    return FLASHBOB_ERR_INVALID_ARG;
   if (H % Hkv != 0) return FLASHBOB_ERR_INVALID_ARG;
   if (!(isfinite(tau) && tau > 0.f)) return FLASHBOB_ERR_INVALID_ARG;
   if (d > 128 || B > 65535 || H > 65535) return FLASHBOB_ERR_UNSUPPORTED;
@@ -70,9 +71,10 @@ flashbob_status run_bob(BobArgs& a, int causal, flashbob_dtype in_dtype) {
   a.causal = causal == 1;
   a.bf16 = in_dtype == FLASHBOB_BF16;
   const bool p1 = a.passes & kPass1, p2 = a.passes & kPass2;
-  const size_t B = a.B > 0 ? a.B : 0, N = a.N > 0 ? a.N : 0, dd = a.d > 0 ? a.d : 0;
-  const size_t rows = B * (a.H > 0 ? a.H : 0) * N;      // query-side rows
-  const size_t krows = B * (a.Hkv > 0 ? a.Hkv : 0) * N; // key-side rows
+  const size_t B = a.B > 0 ? a.B : 0, dd = a.d > 0 ? a.d : 0;
+  const size_t Nq = a.Nq > 0 ? a.Nq : 0, Nk = a.Nk > 0 ? a.Nk : 0;
+  const size_t rows = B * (a.H > 0 ? a.H : 0) * Nq;      // query-side rows
+  const size_t krows = B * (a.Hkv > 0 ? a.Hkv : 0) * Nk; // key-side rows
   const size_t esz = a.bf16 ? 2 : 4;
   const size_t inb = rows * dd * esz, mat = rows * dd * 4, vec = rows * 4;
   const size_t kinb = krows * dd * esz, kmat = krows * dd * 4;
@@ -106,7 +108,7 @@ flashbob_status run_bob(BobArgs& a, int causal, flashbob_dtype in_dtype) {
   add(a.E, vec, p1);
   for (int i = 0; i < n; ++i)
     if (!bufs[i].p) return FLASHBOB_ERR_INVALID_ARG;
-  st = check_sizes(a.B, a.H, a.Hkv, a.N, a.d, a.tau);
+  st = check_sizes(a.B, a.H, a.Hkv, a.Nq, a.Nk, a.d, a.tau);
   if (st != FLASHBOB_OK) return st;
   for (int i = 0; i < n; ++i)
     if (!aligned16(bufs[i].p)) return FLASHBOB_ERR_MISALIGNED;
@@ -144,19 +146,19 @@ const char* flashbob_status_string(flashbob_status s) {
 }
 
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
-                              float* O, float* L, float* D, int B, int H, int Hkv, int N,
-                              int d, float tau, int causal, flashbob_dtype in_dtype,
+                              float* O, float* L, float* D, int B, int H, int Hkv, int Nq,
+                              int Nk, int d, float tau, int causal, flashbob_dtype in_dtype,
                               void* stream) {
   flashbob_status st = check_dtype(in_dtype);
   if (st != FLASHBOB_OK) return st;
   if (causal != 0 && causal != 1) return FLASHBOB_ERR_INVALID_ARG;
   if (!Q || !K || !V || !dO || !O || !L || !D) return FLASHBOB_ERR_INVALID_ARG;
-  st = check_sizes(B, H, Hkv, N, d, tau);
+  st = check_sizes(B, H, Hkv, Nq, Nk, d, tau);
   if (st != FLASHBOB_OK) return st;
   const void* ptrs[] = {Q, K, V, dO, O, L, D};
   for (const void* p : ptrs)
     if (!aligned16(p)) return FLASHBOB_ERR_MISALIGNED;
-  const size_t rows = (size_t)B * H * N, krows = (size_t)B * Hkv * N;
+  const size_t rows = (size_t)B * H * Nq, krows = (size_t)B * Hkv * Nk;
   const size_t esz = in_dtype == FLASHBOB_BF16 ? 2 : 4;
   const Range ins[] = {{(uintptr_t)Q, (uintptr_t)Q + rows * d * esz},
                        {(uintptr_t)K, (uintptr_t)K + krows * d * esz},
@@ -171,7 +173,7 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
     for (const Range& o2 : outs)
       if (&o != &o2 && overlaps(o, o2)) return FLASHBOB_ERR_INVALID_ARG;
   }
-  PrepArgs a{Q,   K, V, dO, O, L, D, B, H, Hkv, N, d, tau, causal == 1,
+  PrepArgs a{Q,  K,  V, dO,  O,  L, D, B, H, Hkv, Nq, Nk, d, tau, causal == 1,
              in_dtype == FLASHBOB_BF16, (cudaStream_t)stream, nullptr};
   if (error_word_ptr(&a.err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
   const cudaError_t e = tc_prep_supported(a) ? tc_prep(a) : simt_prep(a);
@@ -182,10 +184,11 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
                              const void* dO, const float* L, const float* D, const void* UQ,
                              const void* UK, const void* UV, float tau, float* dQt, float* dKt,
                              float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
-                             int Hkv, int N, int d, int causal, flashbob_dtype in_dtype,
+                             int Hkv, int Nq, int Nk, int d, int causal, flashbob_dtype in_dtype,
                              void* stream) {
-  BobArgs a{Q, K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, dKt, dVt, ddOt, alpha, E, B, H, Hkv, N,
-            d, false, false, (cudaStream_t)stream, nullptr, kPass1 | kPass2};
+  BobArgs a{Q,  K,  V,     O, dO, L,     D,     UQ,    UK, UV, tau, dQt, dKt, dVt,
+            ddOt, alpha, E, B, H,  Hkv, Nq, Nk, d, false, false, (cudaStream_t)stream,
+            nullptr, kPass1 | kPass2};
   return run_bob(a, causal, in_dtype);
 }
 
@@ -193,10 +196,11 @@ flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, 
                                    const void* dO, const float* L, const float* D,
                                    const void* UQ, const void* UK, const void* UV, float tau,
                                    float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
-                                   int Hkv, int N, int d, int causal, flashbob_dtype in_dtype,
-                                   void* stream) {
-  BobArgs a{Q, K, V, O, dO, L, D, UQ, UK, UV, tau, dQt, nullptr, nullptr, ddOt, alpha, E, B, H,
-            Hkv, N, d, false, false, (cudaStream_t)stream, nullptr, kPass1};
+                                   int Hkv, int Nq, int Nk, int d, int causal,
+                                   flashbob_dtype in_dtype, void* stream) {
+  BobArgs a{Q,    K,     V, O, dO, L,   D,  UQ, UK, UV,    tau,   dQt, nullptr, nullptr,
+            ddOt, alpha, E, B, H,  Hkv, Nq, Nk, d,  false, false, (cudaStream_t)stream,
+            nullptr, kPass1};
   return run_bob(a, causal, in_dtype);
 }
 
@@ -204,11 +208,11 @@ flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, 
                                    const float* L, const float* D, const float* alpha,
                                    const float* E, const void* UQ, const void* UK,
                                    const void* UV, float tau, float* dKt, float* dVt, int B,
-                                   int H, int Hkv, int N, int d, int causal,
+                                   int H, int Hkv, int Nq, int Nk, int d, int causal,
                                    flashbob_dtype in_dtype, void* stream) {
   // alpha and E are inputs of pass 2; the BobArgs fields keep their names.
   BobArgs a{Q,       K,   V,   nullptr, dO, L, D, UQ, UK, UV, tau, nullptr, dKt, dVt, nullptr,
-            (float*)alpha, (float*)E, B, H, Hkv, N, d, false, false, (cudaStream_t)stream,
+            (float*)alpha, (float*)E, B, H, Hkv, Nq, Nk, d, false, false, (cudaStream_t)stream,
             nullptr, kPass2};
   return run_bob(a, causal, in_dtype);
 }
@@ -220,7 +224,7 @@ flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1
   if (d <= 0 || d > 128) return FLASHBOB_ERR_UNSUPPORTED;
   BobArgs probe{};
   probe.d = d;
-  probe.N = 1;
+  probe.Nq = probe.Nk = 1;
   probe.bf16 = in_dtype == FLASHBOB_BF16;
   const bool tc = tc_supported(probe);
   const int br1 = tc ? kTcRows : kSimtTile, bc1 = tc ? kTcStream : kSimtTile;

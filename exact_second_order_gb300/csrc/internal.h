@@ -9,7 +9,8 @@ namespace flashbob {
 struct PrepArgs {
   const void *Q, *K, *V, *dO;
   float *O, *L, *D;
-  int B, H, Hkv, N, d;  // Hkv key/value heads, shared by H / Hkv query heads each
+  int B, H, Hkv;  // Hkv key/value heads, shared by H / Hkv query heads each
+  int Nq, Nk, d;  // query rows, key rows, head dim
   float tau;
   bool causal;
   bool bf16;
@@ -25,7 +26,8 @@ struct BobArgs {
   const void *UQ, *UK, *UV;
   float tau;
   float *dQt, *dKt, *dVt, *ddOt, *alpha, *E;
-  int B, H, Hkv, N, d;  // Hkv key/value heads, shared by H / Hkv query heads each
+  int B, H, Hkv;  // Hkv key/value heads, shared by H / Hkv query heads each
+  int Nq, Nk, d;  // query rows, key rows, head dim
   bool causal;
   bool bf16;
   cudaStream_t stream;

@@ -63,33 +63,33 @@ template <typename T, int DP>
 __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                   const T* __restrict__ V, const T* __restrict__ dO,
                                                   float* __restrict__ O, float* __restrict__ L,
-                                                  float* __restrict__ D, int H, int Hkv, int N,
-                                                  int d, float tau, int causal) {
+                                                  float* __restrict__ D, int H, int Hkv, int Nq,
+                                                  int Nk, int d, float tau, int causal) {
   extern __shared__ float sm[];
   float* Qs = sm;
   float* Ks = Qs + SB * (DP + 1);
   float* Vs = Ks + SB * (DP + 1);
   float* Ps = Vs + SB * (DP + 1);  // [SB][SB + 1]
   const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
-  const size_t base = bh * N * d;
+  const size_t base = bh * Nq * d;
   // key/value head shared by this query head (grouped-query attention)
-  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * N * d;
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * Nk * d;
   const int row0 = blockIdx.x * SB;
   const int t = threadIdx.x, r = t >> 3, q = t & 7;
   const float c = tau * kLog2e;  // scores in log2 units
 
-  load_tile<T, DP>(Qs, Q + base, row0, N, d);
+  load_tile<T, DP>(Qs, Q + base, row0, Nq, d);
   float m = -INFINITY, l = 0.f;
   float acc[DP / 8];
 #pragma unroll
   for (int j = 0; j < DP / 8; ++j) acc[j] = 0.f;
 
   const int gr = row0 + r;
-  const int col_end = causal ? min(N, row0 + SB) : N;  // keys j <= i under the causal mask
+  const int col_end = causal ? min(Nk, row0 + SB) : Nk;  // keys j <= i under the causal mask
   for (int col0 = 0; col0 < col_end; col0 += SB) {
     __syncthreads();
-    load_tile<T, DP>(Ks, K + kbase, col0, N, d);
-    load_tile<T, DP>(Vs, V + kbase, col0, N, d);
+    load_tile<T, DP>(Ks, K + kbase, col0, Nk, d);
+    load_tile<T, DP>(Vs, V + kbase, col0, Nk, d);
     __syncthreads();
     float s[4];
 #pragma unroll
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int j = col0 + q + 8 * u;
-      s[u] = (j < N && !(causal && j > gr)) ? s[u] * c : -INFINITY;
+      s[u] = (j < Nk && !(causal && j > gr)) ? s[u] * c : -INFINITY;
       mx = fmaxf(mx, s[u]);
     }
     mx = row8_max(mx);
@@ -136,15 +136,15 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
   for (int j = 0; j < DP / 8; ++j) {
     const int k = q + 8 * j;
     const float o = acc[j] * inv_l;
-    if (gr < N && k < d) {
+    if (gr < Nq && k < d) {
       O[base + (size_t)gr * d + k] = o;
       dsum = fmaf(ldf(dO + base + (size_t)gr * d + k), o, dsum);
     }
   }
   dsum = row8_sum(dsum);
-  if (gr < N && q == 0) {
-    L[bh * N + gr] = (m + log2f(l)) * kLn2;
-    D[bh * N + gr] = dsum;
+  if (gr < Nq && q == 0) {
+    L[bh * Nq + gr] = (m + log2f(l)) * kLn2;
+    D[bh * Nq + gr] = dsum;
   }
 }
 
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
     const float* __restrict__ O, const T* __restrict__ dO, const float* __restrict__ L,
     const float* __restrict__ D, const T* __restrict__ UQ, const T* __restrict__ UK,
     const T* __restrict__ UV, float tau, float* __restrict__ dQt, float* __restrict__ ddOt,
-    float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv, int N, int d,
+    float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv, int Nq, int Nk, int d,
     int causal) {
   extern __shared__ float sm[];
   constexpr int TP = SB * (DP + 1);
@@ -181,32 +181,32 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
   float* PFs = dSs + OP;
 
   const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
-  const size_t base = bh * N * d;
+  const size_t base = bh * Nq * d;
   // key/value head shared by this query head (grouped-query attention)
-  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * N * d;
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * Nk * d;
   const int row0 = blockIdx.x * SB;
   const int t = threadIdx.x, r = t >> 3, q = t & 7;
   const int gr = row0 + r;
   const float c = tau * kLog2e;
-  const float Lr2 = gr < N ? L[bh * N + gr] * kLog2e : 0.f;
-  const float Dr = gr < N ? D[bh * N + gr] : 0.f;
+  const float Lr2 = gr < Nq ? L[bh * Nq + gr] * kLog2e : 0.f;
+  const float Dr = gr < Nq ? D[bh * Nq + gr] : 0.f;
 
-  load_tile<T, DP>(Qs, Q + base, row0, N, d);
-  load_tile<T, DP>(dOs, dO + base, row0, N, d);
-  load_tile<T, DP>(UQs, UQ + base, row0, N, d);
+  load_tile<T, DP>(Qs, Q + base, row0, Nq, d);
+  load_tile<T, DP>(dOs, dO + base, row0, Nq, d);
+  load_tile<T, DP>(UQs, UQ + base, row0, Nq, d);
 
   float accB[DP / 8], accR[DP / 8], accW[DP / 8], accO[DP / 8];
 #pragma unroll
   for (int j = 0; j < DP / 8; ++j) accB[j] = accR[j] = accW[j] = accO[j] = 0.f;
   float a_part = 0.f, e_part = 0.f;
-  const int col_end = causal ? min(N, row0 + SB) : N;
+  const int col_end = causal ? min(Nk, row0 + SB) : Nk;
 
   for (int col0 = 0; col0 < col_end; col0 += SB) {
     __syncthreads();
-    load_tile<T, DP>(Ks, K + kbase, col0, N, d);
-    load_tile<T, DP>(Vs, V + kbase, col0, N, d);
-    load_tile<T, DP>(UKs, UK + kbase, col0, N, d);
-    load_tile<T, DP>(UVs, UV + kbase, col0, N, d);
+    load_tile<T, DP>(Ks, K + kbase, col0, Nk, d);
+    load_tile<T, DP>(Vs, V + kbase, col0, Nk, d);
+    load_tile<T, DP>(UKs, UK + kbase, col0, Nk, d);
+    load_tile<T, DP>(UVs, UV + kbase, col0, Nk, d);
     __syncthreads();
     float s[4], dp[4], f[4], g[4];
 #pragma unroll
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
     for (int u = 0; u < 4; ++u) {
       const int cc = q + 8 * u;
       const int j = col0 + cc;
-      const float p = (j < N && !(causal && j > gr)) ? exp2f(s[u] * c - Lr2) : 0.f;
+      const float p = (j < Nk && !(causal && j > gr)) ? exp2f(s[u] * c - Lr2) : 0.f;
       const float x = dp[u] - Dr;
       const float ft = f[u] * tau;
       const float dpt0 = fmaf(ft, x, g[u]);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
   const float al = row8_sum(a_part);
   const float e0 = row8_sum(e_part);
   const float Ei = e0 - al * Dr;
-  if (gr < N) {
+  if (gr < Nq) {
 #pragma unroll
     for (int j = 0; j < DP / 8; ++j) {
       const int k = q + 8 * j;
@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
       }
     }
     if (q == 0) {
-      alpha[bh * N + gr] = al;
-      E[bh * N + gr] = Ei;
+      alpha[bh * Nq + gr] = al;
+      E[bh * Nq + gr] = Ei;
     }
   }
 }
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
     const T* __restrict__ dO, const float* __restrict__ L, const float* __restrict__ D,
     const float* __restrict__ alpha, const float* __restrict__ E, const T* __restrict__ UQ,
     const T* __restrict__ UK, const T* __restrict__ UV, float tau, float* __restrict__ dKt,
-    float* __restrict__ dVt, int H, int Hkv, int N, int d, int causal) {
+    float* __restrict__ dVt, int H, int Hkv, int Nq, int Nk, int d, int causal) {
   extern __shared__ float sm[];
   constexpr int TP = SB * (DP + 1);
   constexpr int OP = SB * (SB + 1);
@@ -316,15 +316,15 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
   // One CTA per key block of a key/value head; the H / Hkv query heads that
   // share the head are summed on chip (grouped-query attention).
   const int G = H / Hkv;
-  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y) * N * d;
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y) * Nk * d;
   const int j0 = blockIdx.x * SB;
   const int t = threadIdx.x, jr = t >> 3, q = t & 7;
   const float c = tau * kLog2e;
 
-  load_tile<T, DP>(Ks, K + kbase, j0, N, d);
-  load_tile<T, DP>(Vs, V + kbase, j0, N, d);
-  load_tile<T, DP>(UKs, UK + kbase, j0, N, d);
-  load_tile<T, DP>(UVs, UV + kbase, j0, N, d);
+  load_tile<T, DP>(Ks, K + kbase, j0, Nk, d);
+  load_tile<T, DP>(Vs, V + kbase, j0, Nk, d);
+  load_tile<T, DP>(UKs, UK + kbase, j0, Nk, d);
+  load_tile<T, DP>(UVs, UV + kbase, j0, Nk, d);
 
   float accK[DP / 8], accV[DP / 8];
 #pragma unroll
@@ -333,20 +333,21 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
   const int gj = j0 + jr;
   for (int hh = 0; hh < G; ++hh) {
     const size_t bh = (size_t)blockIdx.z * H + (size_t)blockIdx.y * G + hh;
-    const size_t base = bh * N * d;
-    // Under the causal mask key j is seen by queries i >= j only.
-    for (int row0 = causal ? j0 : 0; row0 < N; row0 += SB) {
+    const size_t base = bh * Nq * d;
+    // Under the causal mask key j is seen by queries i >= j only (none when
+    // j >= Nq: those keys keep d~K = d~V = 0).
+    for (int row0 = causal ? j0 : 0; row0 < Nq; row0 += SB) {
       __syncthreads();
-      load_tile<T, DP>(Qs, Q + base, row0, N, d);
-      load_tile<T, DP>(dOs, dO + base, row0, N, d);
-      load_tile<T, DP>(UQs, UQ + base, row0, N, d);
+      load_tile<T, DP>(Qs, Q + base, row0, Nq, d);
+      load_tile<T, DP>(dOs, dO + base, row0, Nq, d);
+      load_tile<T, DP>(UQs, UQ + base, row0, Nq, d);
       if (t < SB) {
         const int gi = row0 + t;
-        const bool ok = gi < N;
-        Ls2[t] = ok ? L[bh * N + gi] * kLog2e : 0.f;
-        Ds[t] = ok ? D[bh * N + gi] : 0.f;
-        As[t] = ok ? alpha[bh * N + gi] : 0.f;
-        Es[t] = ok ? E[bh * N + gi] : 0.f;
+        const bool ok = gi < Nq;
+        Ls2[t] = ok ? L[bh * Nq + gi] * kLog2e : 0.f;
+        Ds[t] = ok ? D[bh * Nq + gi] : 0.f;
+        As[t] = ok ? alpha[bh * Nq + gi] : 0.f;
+        Es[t] = ok ? E[bh * Nq + gi] : 0.f;
       }
       __syncthreads();
       float s[4], dp[4], f[4], g[4];
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
       for (int u = 0; u < 4; ++u) {
         const int ii = q + 8 * u;
         const int i = row0 + ii;
-        const float p = (i < N && !(causal && i < gj)) ? exp2f(s[u] * c - Ls2[ii]) : 0.f;
+        const float p = (i < Nq && !(causal && i < gj)) ? exp2f(s[u] * c - Ls2[ii]) : 0.f;
         const float x = dp[u] - Ds[ii];
         const float ft = f[u] * tau;
         const float a = As[ii];
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
 
   }  // query heads of the group
 
-  if (gj < N) {
+  if (gj < Nk) {
 #pragma unroll
     for (int j = 0; j < DP / 8; ++j) {
       const int k = q + 8 * j;
@@ -418,10 +419,10 @@ cudaError_t run_prep(const PrepArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(prep_kernel<T, DP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + SB - 1) / SB, a.H, a.B);
+  dim3 grid((a.Nq + SB - 1) / SB, a.H, a.B);
   prep_kernel<T, DP><<<grid, NT, smem, a.stream>>>(
       (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.O, a.L, a.D, a.H, a.Hkv,
-      a.N, a.d, a.tau, a.causal ? 1 : 0);
+      a.Nq, a.Nk, a.d, a.tau, a.causal ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -434,21 +435,21 @@ cudaError_t run_bob(const BobArgs& a) {
   e = cudaFuncSetAttribute(pass2_kernel<T, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)s2);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + SB - 1) / SB, a.H, a.B);
+  dim3 grid((a.Nq + SB - 1) / SB, a.H, a.B);
   if (a.passes & kPass1) {
     pass1_kernel<T, DP><<<grid, NT, s1, a.stream>>>(
         (const T*)a.Q, (const T*)a.K, (const T*)a.V, a.O, (const T*)a.dO, a.L, a.D,
         (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dQt, a.ddOt, a.alpha, a.E, a.H,
-        a.Hkv, a.N, a.d, a.causal ? 1 : 0);
+        a.Hkv, a.Nq, a.Nk, a.d, a.causal ? 1 : 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (a.passes & kPass2) {
-    const dim3 grid2((a.N + SB - 1) / SB, a.Hkv, a.B);  // one CTA per key block of a shared head
+    const dim3 grid2((a.Nk + SB - 1) / SB, a.Hkv, a.B);  // one CTA per key block of a shared head
     pass2_kernel<T, DP><<<grid2, NT, s2, a.stream>>>(
         (const T*)a.Q, (const T*)a.K, (const T*)a.V, (const T*)a.dO, a.L, a.D, a.alpha, a.E,
-        (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dKt, a.dVt, a.H, a.Hkv, a.N,
-        a.d, a.causal ? 1 : 0);
+        (const T*)a.UQ, (const T*)a.UK, (const T*)a.UV, a.tau, a.dKt, a.dVt, a.H, a.Hkv, a.Nq,
+        a.Nk, a.d, a.causal ? 1 : 0);
     e = cudaGetLastError();
   }
   return e;

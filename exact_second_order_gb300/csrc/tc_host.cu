@@ -20,9 +20,9 @@ cudaError_t tc_bob(const BobArgs& a) {
     const void* rows[3] = {a.Q, a.dO, a.UQ};
     const void* cols[4] = {a.K, a.V, a.UK, a.UV};
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m128[i], rows[i], BH, a.N, kTcRows);
+      e = tc::make_map_bf16_d64(&m128[i], rows[i], BH, a.Nq, kTcRows);
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m32[i], cols[i], BHkv, a.N, kTcStream);
+      e = tc::make_map_bf16_d64(&m32[i], cols[i], BHkv, a.Nk, kTcStream);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass1(a, m128, m32);
     if (e != cudaSuccess) return e;
@@ -32,9 +32,9 @@ cudaError_t tc_bob(const BobArgs& a) {
     const void* res[4] = {a.K, a.UK, a.V, a.UV};
     const void* str[3] = {a.Q, a.UQ, a.dO};
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m128[i], res[i], BHkv, a.N, kTcRows);
+      e = tc::make_map_bf16_d64(&m128[i], res[i], BHkv, a.Nk, kTcRows);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m64[i], str[i], BH, a.N, kTcStream2);
+      e = tc::make_map_bf16_d64(&m64[i], str[i], BH, a.Nq, kTcStream2);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass2(a, m128, m64);
   }

@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap mUV, const float* __restrict__ O,
                     const float* __restrict__ L, const float* __restrict__ D,
                     float* __restrict__ dQt, float* __restrict__ ddOt,
-                    float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv, int N,
-                    float tau, int causal, unsigned int* err) {
+                    float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv, int Nq,
+                    int Nk, float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem1& sm = *reinterpret_cast<Smem1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);
   // Causal: the last row blocks see the most keys, so they start first.
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
-  const int col_end = causal ? min(N, row0 + BM) : N;  // keys j <= i under the causal mask
+  const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
   const int T = (col_end + BN - 1) / BN;
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -294,10 +294,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quad * 32 + lane;      // row inside the block = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int gr = row0 + r;
-    const size_t rowvec = static_cast<size_t>(bh) * N + gr;
+    const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
-    const float Lr2 = gr < N ? L[rowvec] * kLog2e : 0.f;
-    const float Dr = gr < N ? D[rowvec] : 0.f;
+    const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
+    const float Dr = gr < Nq ? D[rowvec] : 0.f;
     float a_acc = 0.f, e_acc = 0.f;
     bool ok = true;
     const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
@@ -310,10 +310,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const int col0 = t * BN;
-      // Columns past N, or (causal) past this row, get P = 0.  Only tiles
-      // that reach past N or past the block's first row take the masked path.
-      const bool masked = (col0 + BN > N) || (causal && col0 + BN - 1 > row0);
-      const int jmax = causal ? min(N - 1, gr) : N - 1;
+      // Columns past Nk, or (causal) past this row, get P = 0.  Only tiles
+      // that reach past Nk or past the block's first row take the masked path.
+      const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
+      const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (masked) {
         p1_tile<true>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
       } else {
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld16(acc_base + kAccW + col, vw);
       tmem_ld16(acc_base + kAccdO + col, vo);
       tmem_wait_ld();
-      if (ok && gr < N) {
+      if (ok && gr < Nq) {
         const size_t off = rowvec * DH + col;
         const float4* o4 = reinterpret_cast<const float4*>(O + off);
         float4* q4 = reinterpret_cast<float4*>(dQt + off);
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    if (ok && wg == 0 && gr < N) {
+    if (ok && wg == 0 && gr < Nq) {
       alpha[rowvec] = al;
       E[rowvec] = Ei;
     }
@@ -389,10 +389,11 @@ cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
+  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_pass1_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.N, a.tau, a.causal ? 1 : 0, a.err);
+      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
+      a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap mdO, const float* __restrict__ L,
                     const float* __restrict__ D, const float* __restrict__ alpha,
                     const float* __restrict__ E, float* __restrict__ dKt,
-                    float* __restrict__ dVt, int H, int Hkv, int N, float tau, int causal,
+                    float* __restrict__ dVt, int H, int Hkv, int Nq, int Nk, float tau,
+                    int causal,
                     unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem2& sm = *reinterpret_cast<Smem2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -176,11 +177,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int hq0 = blockIdx.z * H + blockIdx.y * G;  // first query head of the group
   const int j0 = blockIdx.x * BM;
   // Query tiles t0 .. of 64 rows stream past; under the causal mask key j is
-  // seen only by queries i >= j, so the tiles before the block are skipped.
+  // seen only by queries i >= j, so the tiles before the block are skipped
+  // (all of them when j0 >= Nq: then T = 0 and the block's d~K, d~V are 0).
   // f = (query head in group) * Tq + (tile - t0) numbers the streamed tiles;
   // ring slots and barrier phases count f.
   const int t0 = causal ? j0 / BQ : 0;
-  const int Tq = (N + BQ - 1) / BQ - t0;
+  const int Tq = max(0, (Nq + BQ - 1) / BQ - t0);
   const int T = G * Tq;
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -335,15 +337,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // fh; rows past N get L = +inf so that P = exp2(-inf) = 0.  (ft, fh)
     // step along with f instead of dividing f by Tq.
     int ft = 0;
-    const float* fL = L + static_cast<size_t>(hq0) * N;
+    const float* fL = L + static_cast<size_t>(hq0) * Nq;
     auto load_scalars = [&](int f) {
       const int i = (ft + t0) * BQ + 32 * wg + lane;
       float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
-      if (f < T && i < N) {
+      if (f < T && i < Nq) {
         const size_t o = static_cast<size_t>(fL - L) + i;
         v = make_float4(fL[i] * kLog2e, D[o], alpha[o], E[o]);
       }
-      if (++ft == Tq) { ft = 0; fL += N; }
+      if (++ft == Tq) { ft = 0; fL += Nq; }
       return v;
     };
     // The loader warp fetches the scalars one tile ahead into registers, so
@@ -386,10 +388,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld16(acc_base + kAccK + col, vk);
       tmem_ld16(acc_base + kAccV + col, vv);
       tmem_wait_ld();
-      if (ok && gj < N) {
-        const size_t off = (static_cast<size_t>(bkv) * N + gj) * DH + col;
+      if (ok && gj < Nk) {
+        const size_t off = (static_cast<size_t>(bkv) * Nk + gj) * DH + col;
         float4* k4 = reinterpret_cast<float4*>(dKt + off);
         float4* v4 = reinterpret_cast<float4*>(dVt + off);
+        // T = 0: no query sees this key block, the accumulators were never
+        // written, and the outputs are exact zeros.
+        if (T == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           k4[k] = make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]),
@@ -421,10 +429,11 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + BM - 1) / BM, a.Hkv, a.B);  // one CTA per key block of a shared head
+  dim3 grid((a.Nk + BM - 1) / BM, a.Hkv, a.B);  // one CTA per key block of a shared head
   tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L, a.D,
-      a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.N, a.tau, a.causal ? 1 : 0, a.err);
+      a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
+      a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 

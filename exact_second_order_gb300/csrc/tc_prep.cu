@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __nv_bfloat16* __restrict__ dO,
                    float* __restrict__ O, float* __restrict__ L, float* __restrict__ D, int H,
-                   int Hkv, int N, float tau, int causal, unsigned int* err) {
+                   int Hkv, int Nq, int Nk, float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem0& sm = *reinterpret_cast<Smem0*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int bh = blockIdx.z * H + blockIdx.y;
   const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);  // shared key/value head
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
-  const int col_end = causal ? min(N, row0 + BM) : N;  // keys j <= i under the causal mask
+  const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
   const int T = (col_end + BN - 1) / BN;
   const int T2 = 2 * T;  // phase A tiles 0..T-1, phase B tiles T..2T-1
   volatile int* abort_flag = &sm.abort_flag;
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int gr = row0 + r;
-    const size_t rowvec = static_cast<size_t>(bh) * N + gr;
+    const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const uint32_t sc = tbase + lane_off + 64 + 32 * wg;
     float m = -INFINITY, l = 0.f, L2 = 0.f;
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok) {
         tc_fence_after();
         const int col0 = (phase_b ? t - T : t) * BN;
-        const int jmax = causal ? min(N - 1, gr) : N - 1;  // visible keys j <= jmax
+        const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;  // visible keys j <= jmax
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t s[16];
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t vo[16];
       tmem_ld16(tbase + lane_off + col, vo);
       tmem_wait_ld();
-      if (ok && gr < N) {
+      if (ok && gr < Nq) {
         const size_t off = rowvec * DH + col;
         float4* o4 = reinterpret_cast<float4*>(O + off);
         const uint4* g4 = reinterpret_cast<const uint4*>(dO + off);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     sm.part_d[wg][r] = dpart;
     named_bar_sync(1, 256);
-    if (ok && wg == 0 && gr < N) {
+    if (ok && wg == 0 && gr < Nq) {
       L[rowvec] = L2 * kLn2;
       D[rowvec] = sm.part_d[0][r] + sm.part_d[1][r];
     }
@@ -287,16 +287,16 @@ cudaError_t tc_prep(const PrepArgs& a) {
   const int BH = a.B * a.H;
   const int BHkv = a.B * a.Hkv;
   CUtensorMap mq, mk, mv;
-  cudaError_t e = tc::make_map_bf16_d64(&mq, a.Q, BH, a.N, kTcRows);
-  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mk, a.K, BHkv, a.N, kTcStream);
-  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mv, a.V, BHkv, a.N, kTcStream);
+  cudaError_t e = tc::make_map_bf16_d64(&mq, a.Q, BH, a.Nq, kTcRows);
+  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mk, a.K, BHkv, a.Nk, kTcStream);
+  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mv, a.V, BHkv, a.Nk, kTcStream);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem0) + 1024;
   e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + BM - 1) / BM, a.H, a.B);
+  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_prep_kernel<<<grid, NTHREADS, smem, a.stream>>>(mq, mk, mv, (const __nv_bfloat16*)a.dO, a.O,
-                                                     a.L, a.D, a.H, a.Hkv, a.N, a.tau,
+                                                     a.L, a.D, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
                                                      a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }

@@ -27,10 +27,10 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _SIGNATURES = {
-    "flashbob_prep": ([_P] * 7 + [_I] * 5 + [_F, _I, _I, _P], _I),
-    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 7 + [_P], _I),
-    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 7 + [_P], _I),
-    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 7 + [_P], _I),
+    "flashbob_prep": ([_P] * 7 + [_I] * 6 + [_F, _I, _I, _P], _I),
+    "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 8 + [_P], _I),
+    "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 8 + [_P], _I),
+    "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 8 + [_P], _I),
     "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
@@ -87,11 +87,12 @@ def flashbob_status_string(status: int) -> str:
 
 
 def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream=None) -> None:
-    """O, L, D of [B, H, N, d] inputs (see flashbob_prep in the header)."""
-    B, H, N, d = Q.shape
-    Hkv = K.shape[1]
+    """O, L, D of [B, H, Nq, d] queries and [B, Hkv, Nk, d] keys/values
+    (see flashbob_prep in the header)."""
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
     st = load_library().flashbob_prep(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, Hkv, N, d,
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, Hkv, Nq, Nk, d,
         float(tau), int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_prep")
@@ -100,12 +101,12 @@ def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream
 def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, ddOt, alpha, E,
                  causal: bool = False, stream=None) -> None:
     """d~Q, d~K, d~V, d~dO, alpha, E (see flashbob_bob in the header)."""
-    B, H, N, d = Q.shape
-    Hkv = K.shape[1]
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
     st = load_library().flashbob_bob(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
         _ptr(UV), float(tau), _ptr(dQt), _ptr(dKt), _ptr(dVt), _ptr(ddOt), _ptr(alpha), _ptr(E),
-        B, H, Hkv, N, d, int(causal), _dtype_code(Q), _stream_handle(stream))
+        B, H, Hkv, Nq, Nk, d, int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob")
 
@@ -113,11 +114,11 @@ def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, dd
 def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, alpha, E,
                        causal: bool = False, stream=None) -> None:
     """Pass 1 only: d~Q, d~dO, alpha, E (see flashbob_bob_pass1 in the header)."""
-    B, H, N, d = Q.shape
-    Hkv = K.shape[1]
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
     st = load_library().flashbob_bob_pass1(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
-        _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, Hkv, N, d,
+        _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, Hkv, Nq, Nk, d,
         int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass1")
@@ -126,11 +127,11 @@ def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, 
 def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt, dVt,
                        causal: bool = False, stream=None) -> None:
     """Pass 2 only: d~K, d~V from pass 1's alpha, E (see flashbob_bob_pass2)."""
-    B, H, N, d = Q.shape
-    Hkv = K.shape[1]
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
     st = load_library().flashbob_bob_pass2(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(D), _ptr(alpha), _ptr(E), _ptr(UQ),
-        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, Hkv, N, d, int(causal),
+        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, Hkv, Nq, Nk, d, int(causal),
         _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass2")
@@ -160,25 +161,26 @@ def flashbob_last_device_error() -> int:
 def prep(Q, K, V, dO, tau: float, causal: bool = False, stream=None):
     """Allocate O, L, D on Q's device and run flashbob_prep."""
     import torch
-    B, H, N, d = Q.shape
-    O = torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device)
-    L = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
-    D = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    B, H, Nq, d = Q.shape
+    O = torch.empty((B, H, Nq, d), dtype=torch.float32, device=Q.device)
+    L = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
+    D = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
     flashbob_prep(Q, K, V, dO, O, L, D, tau, causal, stream)
     return O, L, D
 
 
 def alloc_bob_outputs(Q, fill: float | None = None, K=None) -> dict:
     """fp32 output buffers of flashbob_bob (optionally filled, e.g. with NaN);
-    d~K and d~V take K's head count (grouped-query attention) when K is given."""
+    d~K and d~V take K's head count and length (grouped-query, rectangular
+    attention) when K is given."""
     import torch
-    B, H, N, d = Q.shape
-    Hkv = K.shape[1] if K is not None else H
-    out = {k: torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device)
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = (K.shape[1], K.shape[2]) if K is not None else (H, Nq)
+    out = {k: torch.empty((B, H, Nq, d), dtype=torch.float32, device=Q.device)
            for k in ("dQt", "ddOt")}
-    out.update({k: torch.empty((B, Hkv, N, d), dtype=torch.float32, device=Q.device)
+    out.update({k: torch.empty((B, Hkv, Nk, d), dtype=torch.float32, device=Q.device)
                 for k in ("dKt", "dVt")})
-    out.update({k: torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    out.update({k: torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
                 for k in ("alpha", "E")})
     if fill is not None:
         for t in out.values():

@@ -8,13 +8,14 @@ Recipe (the pages benchmark an isolated attention layer on synthetic tensors):
 
 * one CPU ``torch.Generator`` seeded with ``seed``;
 * draws in the fixed order Q, K, V, dO, U_Q, U_K, U_V, each of shape
-  ``[B, H, N, d]`` (contiguous, row-major);
+  ``[B, H, N, d]`` (contiguous, row-major); rectangular workloads draw the
+  key-side tensors K, V, U_K, U_V with ``Nk`` rows (the same draw order);
 * ``dist="unit"``: all seven tensors ~ N(0, 1) (the tiny fp32 workload);
 * ``dist="scaled"``: Q, K, V ~ N(0, 1) / d**0.25 so that Q K^T has unit
   variance; dO, U_Q, U_K, U_V ~ N(0, 1);
 * grouped-query workloads draw K, V, U_K, U_V with ``Hkv`` heads (the
   same draw order);
-* ``peaked_k_rows``: for every (b, h) pick floor(0.05 N) distinct key rows
+* ``peaked_k_rows``: for every (b, h) pick floor(0.05 N_k) distinct key rows
   with the same generator (after the seven draws) and multiply them by 4,
   which makes some softmax rows peaked;
 * ``stress``: Q, K ~ N(0, 1) (unscaled), so the scaled scores tau Q K^T have
@@ -35,7 +36,8 @@ KV_NAMES = ("K", "V", "UK", "UV")
 
 @dataclass(frozen=True)
 class Workload:
-    """A named problem shape: batch B, heads H, sequence N, head dim d."""
+    """A named problem shape: batch B, heads H, query rows N, head dim d
+    (key rows Nk and key/value heads Hkv where they differ)."""
 
     name: str
     B: int
@@ -49,10 +51,26 @@ class Workload:
     seed: int = 0
     causal: bool = False
     Hkv: int = 0  # key/value heads (grouped-query attention); 0 means H
+    Nk: int = 0  # key rows (rectangular attention); 0 means N
 
     @property
     def kv_heads(self) -> int:
         return self.Hkv if self.Hkv else self.H
+
+    @property
+    def kv_len(self) -> int:
+        return self.Nk if self.Nk else self.N
+
+    @property
+    def pairs(self) -> int:
+        """(query, key) pairs the softmax sees per head: N Nk, or under the
+        causal mask (key j visible from query i when j <= i) the count of
+        pairs with j <= i."""
+        n, nk = self.N, self.kv_len
+        if not self.causal:
+            return n * nk
+        m = min(n, nk)
+        return m * (m + 1) // 2 + (n - m) * nk
 
     @property
     def tau(self) -> float:
@@ -60,9 +78,9 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Fixed GEMM list of both passes: 19 GEMMs of 2 N^2 d each (half of
-        that under the causal mask)."""
-        return (0.5 if self.causal else 1.0) * 38.0 * self.N * self.N * self.d * self.B * self.H
+        """Fixed GEMM list of both passes: 19 GEMMs of 2 d flops per visible
+        (query, key) pair, i.e. 38 N^2 d per head without a mask."""
+        return 38.0 * self.pairs * self.d * self.B * self.H
 
 
 # The five workloads of the isolated-layer benchmark (non-causal).
@@ -84,24 +102,29 @@ CAUSAL_N16384 = Workload("causal_B4_H12_N16384_d64", 4, 12, 16384, 64, "bf16", c
 # multi-query variant with one shared head).
 GQA_N8192 = Workload("gqa_B1_H12_Hkv4_N8192_d64", 1, 12, 8192, 64, "bf16", Hkv=4)
 MQA_N8192 = Workload("mqa_B1_H12_Hkv1_N8192_d64", 1, 12, 8192, 64, "bf16", Hkv=1)
+# Rectangular attention: fewer queries than keys and the reverse.
+RECT_Q4096_K16384 = Workload("rect_B1_H8_Nq4096_Nk16384_d64", 1, 8, 4096, 64, "bf16", Nk=16384)
+RECT_Q16384_K4096 = Workload("rect_B1_H8_Nq16384_Nk4096_d64", 1, 8, 16384, 64, "bf16", Nk=4096)
 # A mid-size case for detailed profiles: inputs (~0.3 GB) larger than L2.
 PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
 
 WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PEAKED,
                                  MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128,
-                                 CAUSAL_N4096, CAUSAL_N16384, GQA_N8192, MQA_N8192, PROFILE)}
+                                 CAUSAL_N4096, CAUSAL_N16384, GQA_N8192, MQA_N8192,
+                                 RECT_Q4096_K16384, RECT_Q16384_K4096, PROFILE)}
 
 
 def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
     """Draw the seven input tensors of ``w`` on the CPU.
 
     Returns fp32 tensors for ``dtype="f32"`` and bf16 tensors for
-    ``dtype="bf16"``, all contiguous ``[B, H, N, d]``.
+    ``dtype="bf16"``, all contiguous: ``[B, H, N, d]`` for Q, dO, U_Q and
+    ``[B, Hkv, Nk, d]`` for K, V, U_K, U_V.
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
-    kv_shape = (w.B, w.kv_heads, w.N, w.d)  # K, V, U_K, U_V (grouped-query attention)
+    kv_shape = (w.B, w.kv_heads, w.kv_len, w.d)  # K, V, U_K, U_V (grouped-query, rectangular)
     out = {}
     for name in NAMES:
         out[name] = torch.randn(kv_shape if name in KV_NAMES else shape, generator=g,
@@ -115,10 +138,10 @@ def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
     elif w.dist != "unit":
         raise ValueError(f"unknown dist {w.dist!r}")
     if w.peaked_k_rows:
-        n_peak = int(math.floor(0.05 * w.N))
+        n_peak = int(math.floor(0.05 * w.kv_len))
         for b in range(w.B):
             for h in range(w.kv_heads):
-                idx = torch.randperm(w.N, generator=g)[:n_peak]
+                idx = torch.randperm(w.kv_len, generator=g)[:n_peak]
                 out["K"][b, h, idx, :] *= 4.0
     if w.dtype == "bf16":
         out = {k: v.to(torch.bfloat16) for k, v in out.items()}
@@ -132,7 +155,8 @@ def small_workload(B: int, H: int, N: int, d: int, dtype: str, seed: int = 0,
     """An ad-hoc shape for parity and edge-case tests."""
     if dist is None:
         dist = "unit" if dtype == "f32" else "scaled"
-    return Workload(f"adhoc_B{B}_H{H}_N{N}_d{d}_{dtype}", B, H, N, d, dtype, dist=dist,
+    nk = f"_Nk{kw['Nk']}" if kw.get("Nk") else ""
+    return Workload(f"adhoc_B{B}_H{H}_N{N}{nk}_d{d}_{dtype}", B, H, N, d, dtype, dist=dist,
                     seed=seed, **kw)
 
 

@@ -11,7 +11,8 @@
  *         section 一 (forward and first-backward formulas), section 二 (P is
  *         recomputed from saved row statistics).
  *
- * Notation, per (batch b, head h): Q, K, V, dO, U_Q, U_K, U_V are N x d;
+ * Notation, per (batch b, head h): Q, dO, U_Q are N_q x d and K, V, U_K,
+ * U_V are N_k x d (N_q = N_k: self-attention; N_q != N_k: rectangular);
  * S = tau Q K^T, L_i = log sum_j exp(S_ij), P = exp(S - L), O = P V,
  * D_i = dO_i . O_i, dP = dO V^T, dS = P o (dP - D), dQ = tau dS K,
  * dK = tau dS^T Q, dV = P^T dO, and
@@ -20,12 +21,16 @@
  * respect to Q, K, V and dO, plus the row scalars alpha_i = sum_j P_ij F_ij
  * (F = tau (U_Q K^T + Q U_K^T)) and E_i = sum_j P_ij d~P_ij.
  *
- * Layout: every N x d tensor is a contiguous row-major [B, H, N, d] array;
- * every length-N row vector is a contiguous [B, H, N] array.  Grouped-query
- * attention ([FBN] 关键设计 3): the key-side tensors K, V, U_K, U_V, dKt, dVt
- * are [B, Hkv, N, d] with Hkv dividing H; query head h uses key/value head
+ * Layout: every matrix is a contiguous row-major array: the query-side
+ * tensors Q, dO, U_Q, O, dQt, ddOt are [B, H, N_q, d], the key-side tensors
+ * K, V, U_K, U_V, dKt, dVt are [B, Hkv, N_k, d]; every row vector (L, D,
+ * alpha, E) is a contiguous [B, H, N_q] array.  Grouped-query attention
+ * ([FBN] 关键设计 3): Hkv divides H; query head h uses key/value head
  * h / (H / Hkv), and d~K, d~V of a shared head sum its query heads.  Hkv = H
- * is ordinary multi-head attention, Hkv = 1 multi-query attention.  Inputs are
+ * is ordinary multi-head attention, Hkv = 1 multi-query attention.
+ * Causal mask: query i sees the keys j <= i (absolute positions, also for
+ * N_q != N_k, so every query sees key 0; keys j >= N_q then get d~K = d~V =
+ * 0).  Inputs are
  * either all fp32 or all bf16 (Q, K, V, dO, U_Q, U_K, U_V; selected by
  * in_dtype); O, L, D and every output are fp32.
  *
@@ -67,31 +72,31 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
 /*
  * flashbob_prep: forward row state for the BoB ([FAB] sections 一/二,
  * [FBN] 关键设计 1 for D).
- *   in : Q, dO [B,H,N,d] and K, V [B,Hkv,N,d] of in_dtype
- *   out: O [B,H,N,d] fp32 (O = P V), L [B,H,N] fp32 (natural-log logsumexp of
- *        tau Q K^T per row), D [B,H,N] fp32 (D_i = dO_i . O_i)
+ *   in : Q, dO [B,H,Nq,d] and K, V [B,Hkv,Nk,d] of in_dtype
+ *   out: O [B,H,Nq,d] fp32 (O = P V), L [B,H,Nq] fp32 (natural-log
+ *        logsumexp of tau Q K^T per row), D [B,H,Nq] fp32 (D_i = dO_i . O_i)
  *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
  *   causal: 0 = full attention; 1 = query i sees keys j <= i only (the
  *        setting of [FBN] 实验关键数据); other values are rejected.
- *   Limits: 1 <= d <= 128; 1 <= N; B, H <= 65535; 1 <= Hkv, H % Hkv == 0.
+ *   Limits: 1 <= d <= 128; 1 <= Nq, Nk; B, H <= 65535; 1 <= Hkv,
+ *        H % Hkv == 0.
  *   One launch: bf16 inputs
  *   with d = 64 run a tcgen05 kernel, every other case fp32 CUDA cores.
  */
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
-                              float* O, float* L, float* D, int B, int H, int Hkv, int N,
-                              int d,
-                              float tau, int causal, flashbob_dtype in_dtype, void* stream);
+                              float* O, float* L, float* D, int B, int H, int Hkv, int Nq,
+                              int Nk, int d, float tau, int causal, flashbob_dtype in_dtype,
+                              void* stream);
 
 /*
  * flashbob_bob: exact BoB of softmax attention with the two-pass schedule of
  * [FBN] 关键设计 2; the closed form and affine correction of [FBN] 关键设计 1.
- *   in : Q, dO, U_Q [B,H,N,d] and K, V, U_K, U_V [B,Hkv,N,d] of in_dtype;
- *        O [B,H,N,d] fp32;
- *        L, D [B,H,N] fp32 (as written by flashbob_prep with the same
- *        causal flag); tau and causal as in prep.
- *   out: dQt, ddOt [B,H,N,d] and dKt, dVt [B,Hkv,N,d] fp32 (d~Q, d~dO, d~K,
- *        d~V);
- *        alpha, E [B,H,N] fp32.  Every element is written exactly once.
+ *   in : Q, dO, U_Q [B,H,Nq,d] and K, V, U_K, U_V [B,Hkv,Nk,d] of in_dtype;
+ *        O [B,H,Nq,d] fp32; L, D [B,H,Nq] fp32 (as written by flashbob_prep
+ *        with the same causal flag); tau and causal as in prep.
+ *   out: dQt, ddOt [B,H,Nq,d] and dKt, dVt [B,Hkv,Nk,d] fp32 (d~Q, d~dO,
+ *        d~K, d~V); alpha, E [B,H,Nq] fp32.  Every element is written
+ *        exactly once.
  *   Pass 1 (row-resident) writes d~Q, d~dO, alpha, E; pass 2 (column-
  *   resident) reads alpha, E and writes d~K, d~V.  No N x N tensor is ever
  *   written to device memory and no atomics are used.
@@ -102,7 +107,8 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
                              const void* dO, const float* L, const float* D, const void* UQ,
                              const void* UK, const void* UV, float tau, float* dQt, float* dKt,
                              float* dVt, float* ddOt, float* alpha, float* E, int B, int H,
-                             int Hkv, int N, int d, int causal, flashbob_dtype in_dtype, void* stream);
+                             int Hkv, int Nq, int Nk, int d, int causal, flashbob_dtype in_dtype,
+                             void* stream);
 
 /*
  * flashbob_bob_pass1 / flashbob_bob_pass2: the two launches of flashbob_bob,
@@ -118,15 +124,15 @@ flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, 
                                    const void* dO, const float* L, const float* D,
                                    const void* UQ, const void* UK, const void* UV, float tau,
                                    float* dQt, float* ddOt, float* alpha, float* E, int B, int H,
-                                   int Hkv, int N, int d, int causal, flashbob_dtype in_dtype,
-                                   void* stream);
+                                   int Hkv, int Nq, int Nk, int d, int causal,
+                                   flashbob_dtype in_dtype, void* stream);
 
 flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, const void* dO,
                                    const float* L, const float* D, const float* alpha,
                                    const float* E, const void* UQ, const void* UK,
                                    const void* UV, float tau, float* dKt, float* dVt, int B,
-                                   int H, int Hkv, int N, int d, int causal, flashbob_dtype in_dtype,
-                                   void* stream);
+                                   int H, int Hkv, int Nq, int Nk, int d, int causal,
+                                   flashbob_dtype in_dtype, void* stream);
 
 /*
  * flashbob_bob_tile_sizes: the tiles flashbob_bob uses for (d, in_dtype):

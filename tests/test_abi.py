@@ -63,9 +63,11 @@ def test_tile_sizes(lib):
         fb.FLASHBOB_ERR_INVALID_ARG
 
 
-def _bob_raw(lib, ptrs, tau=0.125, B=1, H=1, N=8, d=64, dtype=0, causal=0, Hkv=None):
+def _bob_raw(lib, ptrs, tau=0.125, B=1, H=1, N=8, d=64, dtype=0, causal=0, Hkv=None, Nk=None):
     Hkv = H if Hkv is None else Hkv
-    return lib.flashbob_bob(*ptrs[:10], tau, *ptrs[10:], B, H, Hkv, N, d, causal, dtype, None)
+    Nk = N if Nk is None else Nk
+    return lib.flashbob_bob(*ptrs[:10], tau, *ptrs[10:], B, H, Hkv, N, Nk, d, causal, dtype,
+                            None)
 
 
 def _fake_ptrs(n=16, stride=1 << 20, base=1 << 32):
@@ -82,7 +84,8 @@ def test_bob_rejects_bad_arguments_on_the_host(lib):
         p[i] = None
         assert _bob_raw(lib, p) == E.FLASHBOB_ERR_INVALID_ARG
     # sizes and tau
-    for kw in ({"B": 0}, {"H": -1}, {"N": 0}, {"d": 0}, {"tau": 0.0}, {"tau": -1.0},
+    for kw in ({"B": 0}, {"H": -1}, {"N": 0}, {"Nk": 0}, {"Nk": -3}, {"d": 0}, {"tau": 0.0},
+               {"tau": -1.0},
                {"tau": float("nan")}, {"tau": float("inf")}, {"dtype": 3}, {"causal": 2},
                {"causal": -1}, {"Hkv": 0}, {"H": 4, "Hkv": 3}, {"H": 2, "Hkv": 4}):
         assert _bob_raw(lib, ok, **kw) == E.FLASHBOB_ERR_INVALID_ARG, kw
@@ -102,12 +105,28 @@ def test_bob_rejects_bad_arguments_on_the_host(lib):
     assert _bob_raw(lib, p) == E.FLASHBOB_ERR_INVALID_ARG
 
 
+def test_bob_sizes_key_side_buffers_by_nk_and_hkv(lib):
+    """The overlap check sizes K, V, U_K, U_V, d~K, d~V with Hkv heads of Nk
+    rows and the query-side buffers with H heads of Nq rows."""
+    ok = _fake_ptrs()
+    # d~K starts 2 KiB into K: inside K's 4 KiB at Nk = 16 (fp32, d = 64),
+    # outside it if K were sized with Nq = 1 rows.
+    p = list(ok)
+    p[11] = p[1] + 2048
+    assert _bob_raw(lib, p, N=1, Nk=16) == fb.FLASHBOB_ERR_INVALID_ARG
+    # d~Q starts 2 KiB into Q: inside Q's 4 KiB at Nq = 16.
+    p = list(ok)
+    p[10] = p[0] + 2048
+    assert _bob_raw(lib, p, N=16, Nk=1) == fb.FLASHBOB_ERR_INVALID_ARG
+
+
 def test_prep_rejects_bad_arguments_on_the_host(lib):
     ok = _fake_ptrs(7)
 
-    def call(p=ok, B=1, H=1, N=8, d=64, tau=0.125, dtype=0, causal=0, Hkv=None):
+    def call(p=ok, B=1, H=1, N=8, d=64, tau=0.125, dtype=0, causal=0, Hkv=None, Nk=None):
         Hkv = H if Hkv is None else Hkv
-        return lib.flashbob_prep(*p, B, H, Hkv, N, d, tau, causal, dtype, None)
+        Nk = N if Nk is None else Nk
+        return lib.flashbob_prep(*p, B, H, Hkv, N, Nk, d, tau, causal, dtype, None)
     for i in range(7):
         p = list(ok)
         p[i] = None
@@ -116,6 +135,7 @@ def test_prep_rejects_bad_arguments_on_the_host(lib):
         p[i] += 4
         assert call(p) == fb.FLASHBOB_ERR_MISALIGNED
     assert call(N=0) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert call(Nk=0) == fb.FLASHBOB_ERR_INVALID_ARG
     assert call(tau=float("nan")) == fb.FLASHBOB_ERR_INVALID_ARG
     assert call(d=200) == fb.FLASHBOB_ERR_UNSUPPORTED
     assert call(causal=3) == fb.FLASHBOB_ERR_INVALID_ARG
@@ -137,25 +157,26 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
 
 def test_pass_entry_points_reject_bad_arguments_on_the_host(lib):
     ok = _fake_ptrs()
+    sizes = (1, 1, 1, 8, 8, 64, 0, 0, None)  # B, H, Hkv, Nq, Nk, d, causal, dtype, stream
     p1 = ok[:15]
     bad = list(p1)
     bad[3] = None  # O
-    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], *sizes) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     bad = list(p1)
     bad[10] = bad[4]  # d~Q over dO
-    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], 1, 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass1(*bad[:10], 0.125, *bad[10:14], *sizes) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     p2 = ok[:13]
     bad = list(p2)
     bad[6] = None  # alpha
-    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], *sizes) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     bad = list(p2)
     bad[11] = bad[6]  # d~K over alpha
-    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], *sizes) == \
         fb.FLASHBOB_ERR_INVALID_ARG
     bad = list(p2)
     bad[12] += 4
-    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], 1, 1, 1, 8, 64, 0, 0, None) == \
+    assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], *sizes) == \
         fb.FLASHBOB_ERR_MISALIGNED

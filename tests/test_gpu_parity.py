@@ -193,3 +193,33 @@ def test_gqa_workloads_sampled_rows(w):
     assert max(res.values()) <= TOL["bf16"], res
     full = full_oracle_errors(w, x, state, out, heads=[(0, 0)])
     assert max(full.values()) <= TOL["bf16"], full
+
+
+# --------------------------------------------------------------------------
+# Rectangular attention (N_q query rows, N_k key rows)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,Nk", [(1, 300), (65, 7), (129, 300), (300, 129), (200, 1)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96)])
+def test_rectangular_small_shapes(N, Nk, dtype, d, causal):
+    # causal with Nk >= Nq + 128 leaves whole key blocks that no query sees
+    _check_full(wl.small_workload(1, 2, N, d, dtype, seed=N + Nk, Nk=Nk, causal=causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rectangular_gqa_bf16(causal):
+    _check_full(wl.small_workload(2, 4, 200, 64, "bf16", seed=12, Hkv=2, Nk=333, causal=causal))
+
+
+@pytest.mark.parametrize("w", [wl.RECT_Q4096_K16384, wl.RECT_Q16384_K4096], ids=lambda w: w.name)
+def test_rectangular_workloads_sampled_rows(w):
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    heads = [(0, 0), (0, 7)]
+    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=heads)
+    assert max(errs.values()) <= TOL["bf16"], errs
+    res = column_sum_residuals(out)
+    assert max(res.values()) <= TOL["bf16"], res
+    full = full_oracle_errors(w, x, state, out, heads=[(0, 3)])
+    assert max(full.values()) <= TOL["bf16"], full
