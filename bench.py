@@ -7,7 +7,8 @@ already resident in device memory.  FLOPs per step follow the fixed GEMM
 list of both passes: 38 N^2 d per (batch, head).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle on the host cores instead (rows of the same workload).
+oracle on the host cores instead (rows of the same workload).  ``--entry
+jvp`` times flashbob_attention_jvp instead (5 GEMMs, 10 N^2 d per head).
 """
 from __future__ import annotations
 
@@ -27,6 +28,8 @@ METRIC = "BoB TFLOP/s & % of GB300 bf16 tensor peak vs N (d=64); ms/call"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "long_B1_H4_N65536_d64"
 PASS1_GEMMS, PASS2_GEMMS = 11, 8  # each 2 d flops per visible (query, key) pair
+JVP_GEMMS = 5  # S, U_Q K^T, Q U_K^T, P U_V, (P o F) V
+JVP_METRIC = "attention JVP TFLOP/s (5 GEMMs of 2*N^2*d per head); ms/call"
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_long_context.txt")
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -46,6 +49,8 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--entry", choices=("bob", "jvp"), default="bob",
+                    help="bob: flashbob_bob (the benchmark); jvp: flashbob_attention_jvp")
     return ap.parse_args()
 
 
@@ -203,6 +208,60 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
+    """Time flashbob_attention_jvp on resident inputs (O, L from a
+    forward-only prep outside the timed region)."""
+    O, L, _ = fb.prep(dev["Q"], dev["K"], dev["V"], None, w.tau, causal=w.causal)
+    Od, Ld = torch.empty_like(O), torch.empty_like(L)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fb.flashbob_attention_jvp(dev["Q"], dev["K"], dev["V"], O, L, dev["UQ"], dev["UK"],
+                                  dev["UV"], w.tau, Od, Ld, causal=w.causal, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(None)
+    time.sleep(0.3)
+    barrier()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    ms = t0.elapsed_time(t1) / args.steps
+    total_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
+    flops = JVP_GEMMS * 2.0 * w.pairs * w.d * w.B * w.H
+    value = job_tflops(flops, args.steps, world, total_ms)
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": JVP_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "entry": "flashbob_attention_jvp", "B": w.B, "H": w.H,
+                   "Hkv": w.kv_heads, "N": w.N, "Nk": w.kv_len, "d": w.d, "causal": w.causal,
+                   "flops_per_step_per_gpu": flops},
+        "roofline": {"kernel": "jvp", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"bf16_tflops_sustained of {peak_src} peaks"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -227,6 +286,8 @@ def main():
 
     x = make_inputs(rank_workload(w, rank))
     dev = {k: v.cuda() for k, v in x.items()}
+    if args.entry == "jvp":
+        return run_jvp(args, w, dev, rank, world, local, barrier, fb, torch)
     O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
     out = fb.alloc_bob_outputs(dev["Q"], K=dev["K"])
     stream = torch.cuda.current_stream()

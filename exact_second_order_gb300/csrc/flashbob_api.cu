@@ -152,21 +152,24 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
   flashbob_status st = check_dtype(in_dtype);
   if (st != FLASHBOB_OK) return st;
   if (causal != 0 && causal != 1) return FLASHBOB_ERR_INVALID_ARG;
-  if (!Q || !K || !V || !dO || !O || !L || !D) return FLASHBOB_ERR_INVALID_ARG;
+  // dO and D are both given (the BoB's row state) or both null (forward only).
+  if (!Q || !K || !V || !O || !L || (!dO != !D)) return FLASHBOB_ERR_INVALID_ARG;
   st = check_sizes(B, H, Hkv, Nq, Nk, d, tau);
   if (st != FLASHBOB_OK) return st;
   const void* ptrs[] = {Q, K, V, dO, O, L, D};
   for (const void* p : ptrs)
-    if (!aligned16(p)) return FLASHBOB_ERR_MISALIGNED;
+    if (p && !aligned16(p)) return FLASHBOB_ERR_MISALIGNED;
   const size_t rows = (size_t)B * H * Nq, krows = (size_t)B * Hkv * Nk;
   const size_t esz = in_dtype == FLASHBOB_BF16 ? 2 : 4;
+  // A null dO / D gets an empty range.
+  const size_t dob = dO ? rows * d * esz : 0, db = D ? rows * 4 : 0;
   const Range ins[] = {{(uintptr_t)Q, (uintptr_t)Q + rows * d * esz},
                        {(uintptr_t)K, (uintptr_t)K + krows * d * esz},
                        {(uintptr_t)V, (uintptr_t)V + krows * d * esz},
-                       {(uintptr_t)dO, (uintptr_t)dO + rows * d * esz}};
+                       {(uintptr_t)dO, (uintptr_t)dO + dob}};
   const Range outs[] = {{(uintptr_t)O, (uintptr_t)O + rows * d * 4},
                         {(uintptr_t)L, (uintptr_t)L + rows * 4},
-                        {(uintptr_t)D, (uintptr_t)D + rows * 4}};
+                        {(uintptr_t)D, (uintptr_t)D + db}};
   for (const Range& o : outs) {
     for (const Range& i : ins)
       if (overlaps(o, i)) return FLASHBOB_ERR_INVALID_ARG;
@@ -236,6 +239,44 @@ flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1
   if (smem_bytes_pass1) *smem_bytes_pass1 = tc ? tc_pass1_smem() : simt_pass1_smem(d);
   if (smem_bytes_pass2) *smem_bytes_pass2 = tc ? tc_pass2_smem() : simt_pass2_smem(d);
   return FLASHBOB_OK;
+}
+
+flashbob_status flashbob_attention_jvp(const void* Q, const void* K, const void* V,
+                                       const float* O, const float* L, const void* UQ,
+                                       const void* UK, const void* UV, float tau, float* Od,
+                                       float* Ld, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                       int causal, flashbob_dtype in_dtype, void* stream) {
+  flashbob_status st = check_dtype(in_dtype);
+  if (st != FLASHBOB_OK) return st;
+  if (causal != 0 && causal != 1) return FLASHBOB_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, O, L, UQ, UK, UV, Od, Ld};
+  for (const void* p : ptrs)
+    if (!p) return FLASHBOB_ERR_INVALID_ARG;
+  st = check_sizes(B, H, Hkv, Nq, Nk, d, tau);
+  if (st != FLASHBOB_OK) return st;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return FLASHBOB_ERR_MISALIGNED;
+  const size_t rows = (size_t)B * H * Nq, krows = (size_t)B * Hkv * Nk;
+  const size_t esz = in_dtype == FLASHBOB_BF16 ? 2 : 4;
+  const Range ins[] = {{(uintptr_t)Q, (uintptr_t)Q + rows * d * esz},
+                       {(uintptr_t)K, (uintptr_t)K + krows * d * esz},
+                       {(uintptr_t)V, (uintptr_t)V + krows * d * esz},
+                       {(uintptr_t)O, (uintptr_t)O + rows * d * 4},
+                       {(uintptr_t)L, (uintptr_t)L + rows * 4},
+                       {(uintptr_t)UQ, (uintptr_t)UQ + rows * d * esz},
+                       {(uintptr_t)UK, (uintptr_t)UK + krows * d * esz},
+                       {(uintptr_t)UV, (uintptr_t)UV + krows * d * esz}};
+  const Range outs[] = {{(uintptr_t)Od, (uintptr_t)Od + rows * d * 4},
+                        {(uintptr_t)Ld, (uintptr_t)Ld + rows * 4}};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlaps(o, i)) return FLASHBOB_ERR_INVALID_ARG;
+  if (overlaps(outs[0], outs[1])) return FLASHBOB_ERR_INVALID_ARG;
+  JvpArgs a{Q,  K,  V,  O,  L,   UQ,  UK, UV, tau, Od, Ld, B, H, Hkv, Nq, Nk, d, causal == 1,
+            in_dtype == FLASHBOB_BF16, (cudaStream_t)stream, nullptr};
+  if (error_word_ptr(&a.err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  const cudaError_t e = tc_jvp_supported(a) ? tc_jvp(a) : simt_jvp(a);
+  return e == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
 }
 
 flashbob_status flashbob_last_device_error(void) {

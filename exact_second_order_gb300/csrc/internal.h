@@ -35,6 +35,21 @@ struct BobArgs {
   int passes;         // bit 0: pass 1, bit 1: pass 2
 };
 
+// Attention JVP (forward-mode derivative along U_Q, U_K, U_V).
+struct JvpArgs {
+  const void *Q, *K, *V;
+  const float *O, *L;
+  const void *UQ, *UK, *UV;
+  float tau;
+  float *Od, *Ld;
+  int B, H, Hkv;
+  int Nq, Nk, d;
+  bool causal;
+  bool bf16;
+  cudaStream_t stream;
+  unsigned int* err;
+};
+
 constexpr int kPass1 = 1;
 constexpr int kPass2 = 2;
 
@@ -42,6 +57,7 @@ constexpr int kPass2 = 2;
 constexpr int kSimtTile = 32;
 cudaError_t simt_prep(const PrepArgs& a);
 cudaError_t simt_bob(const BobArgs& a);
+cudaError_t simt_jvp(const JvpArgs& a);
 size_t simt_pass1_smem(int d);
 size_t simt_pass2_smem(int d);
 
@@ -53,6 +69,8 @@ bool tc_supported(const BobArgs& a);
 bool tc_prep_supported(const PrepArgs& a);
 cudaError_t tc_prep(const PrepArgs& a);
 cudaError_t tc_bob(const BobArgs& a);
+bool tc_jvp_supported(const JvpArgs& a);
+cudaError_t tc_jvp(const JvpArgs& a);
 size_t tc_pass1_smem();
 size_t tc_pass2_smem();
 

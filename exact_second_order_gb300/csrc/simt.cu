@@ -138,13 +138,13 @@ __global__ void __launch_bounds__(NT) prep_kernel(const T* __restrict__ Q, const
     const float o = acc[j] * inv_l;
     if (gr < Nq && k < d) {
       O[base + (size_t)gr * d + k] = o;
-      dsum = fmaf(ldf(dO + base + (size_t)gr * d + k), o, dsum);
+      if (dO) dsum = fmaf(ldf(dO + base + (size_t)gr * d + k), o, dsum);
     }
   }
   dsum = row8_sum(dsum);
   if (gr < Nq && q == 0) {
     L[bh * Nq + gr] = (m + log2f(l)) * kLn2;
-    D[bh * Nq + gr] = dsum;
+    if (D) D[bh * Nq + gr] = dsum;  // dO = D = null: forward only
   }
 }
 
@@ -282,6 +282,105 @@ __global__ void __launch_bounds__(NT) pass1_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Attention JVP along (U_Q, U_K, U_V): pass 1 without dO.  Per column tile
+// S = Q K^T and its tangent F = tau (U_Q K^T + Q U_K^T); P = exp(S - L);
+// row sums L' += P o F and the accumulator P U_V + (P o F) V; at the end
+// O' = P U_V + (P o F) V - L' O  (the d~dO and alpha of pass 1, whose
+// other terms all carry dO).
+// ---------------------------------------------------------------------------
+template <typename T, int DP>
+__global__ void __launch_bounds__(NT) jvp_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+    const float* __restrict__ O, const float* __restrict__ L, const T* __restrict__ UQ,
+    const T* __restrict__ UK, const T* __restrict__ UV, float tau, float* __restrict__ Od,
+    float* __restrict__ Ld, int H, int Hkv, int Nq, int Nk, int d, int causal) {
+  extern __shared__ float sm[];
+  constexpr int TP = SB * (DP + 1);
+  constexpr int OP = SB * (SB + 1);
+  float* Qs = sm;
+  float* UQs = Qs + TP;
+  float* Ks = UQs + TP;
+  float* Vs = Ks + TP;
+  float* UKs = Vs + TP;
+  float* UVs = UKs + TP;
+  float* Ps = UVs + TP;
+  float* PFs = Ps + OP;
+
+  const size_t bh = (size_t)blockIdx.z * H + blockIdx.y;
+  const size_t base = bh * Nq * d;
+  const size_t kbase = ((size_t)blockIdx.z * Hkv + blockIdx.y / (H / Hkv)) * Nk * d;
+  const int row0 = blockIdx.x * SB;
+  const int t = threadIdx.x, r = t >> 3, q = t & 7;
+  const int gr = row0 + r;
+  const float c = tau * kLog2e;
+  const float Lr2 = gr < Nq ? L[bh * Nq + gr] * kLog2e : 0.f;
+
+  load_tile<T, DP>(Qs, Q + base, row0, Nq, d);
+  load_tile<T, DP>(UQs, UQ + base, row0, Nq, d);
+
+  float accO[DP / 8];
+#pragma unroll
+  for (int j = 0; j < DP / 8; ++j) accO[j] = 0.f;
+  float a_part = 0.f;
+  const int col_end = causal ? min(Nk, row0 + SB) : Nk;
+
+  for (int col0 = 0; col0 < col_end; col0 += SB) {
+    __syncthreads();
+    load_tile<T, DP>(Ks, K + kbase, col0, Nk, d);
+    load_tile<T, DP>(Vs, V + kbase, col0, Nk, d);
+    load_tile<T, DP>(UKs, UK + kbase, col0, Nk, d);
+    load_tile<T, DP>(UVs, UV + kbase, col0, Nk, d);
+    __syncthreads();
+    float s[4], f[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s[u] = f[u] = 0.f;
+    for (int k = 0; k < d; ++k) {
+      const float qv = Qs[r * (DP + 1) + k];
+      const float uqv = UQs[r * (DP + 1) + k];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cr = (q + 8 * u) * (DP + 1) + k;
+        s[u] = fmaf(qv, Ks[cr], s[u]);
+        f[u] = fmaf(uqv, Ks[cr], fmaf(qv, UKs[cr], f[u]));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cc = q + 8 * u;
+      const int j = col0 + cc;
+      const float p = (j < Nk && !(causal && j > gr)) ? exp2f(s[u] * c - Lr2) : 0.f;
+      const float pf = p * (f[u] * tau);
+      a_part += pf;
+      Ps[r * (SB + 1) + cc] = p;
+      PFs[r * (SB + 1) + cc] = pf;
+    }
+    __syncwarp();
+    for (int cc = 0; cc < SB; ++cc) {
+      const float p = Ps[r * (SB + 1) + cc];
+      const float pf = PFs[r * (SB + 1) + cc];
+#pragma unroll
+      for (int j = 0; j < DP / 8; ++j) {
+        const int ck = cc * (DP + 1) + q + 8 * j;
+        accO[j] = fmaf(p, UVs[ck], fmaf(pf, Vs[ck], accO[j]));
+      }
+    }
+  }
+
+  const float al = row8_sum(a_part);
+  if (gr < Nq) {
+#pragma unroll
+    for (int j = 0; j < DP / 8; ++j) {
+      const int k = q + 8 * j;
+      if (k < d) {
+        const size_t o = base + (size_t)gr * d + k;
+        Od[o] = accO[j] - al * O[o];
+      }
+    }
+    if (q == 0) Ld[bh * Nq + gr] = al;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Pass 2 (column-resident).  Per query-row tile, transposed scores; with the
 // row scalars L, D, alpha, E of the streamed rows:
 //   dS = P o (dP - D), d~S = P o (F o (dP - D) + G - alpha dP - E),
@@ -409,6 +508,7 @@ __global__ void __launch_bounds__(NT) pass2_kernel(
 
 size_t prep_smem(int dp) { return (size_t)(3 * SB * (dp + 1) + SB * (SB + 1)) * sizeof(float); }
 size_t pass1_smem(int dp) { return (size_t)(7 * SB * (dp + 1) + 5 * SB * (SB + 1)) * sizeof(float); }
+size_t jvp_smem(int dp) { return (size_t)(6 * SB * (dp + 1) + 2 * SB * (SB + 1)) * sizeof(float); }
 size_t pass2_smem(int dp) {
   return (size_t)(7 * SB * (dp + 1) + 3 * SB * (SB + 1) + 4 * SB) * sizeof(float);
 }
@@ -455,7 +555,25 @@ cudaError_t run_bob(const BobArgs& a) {
   return e;
 }
 
+template <typename T, int DP>
+cudaError_t run_jvp(const JvpArgs& a) {
+  const size_t smem = jvp_smem(DP);
+  cudaError_t e = cudaFuncSetAttribute(jvp_kernel<T, DP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nq + SB - 1) / SB, a.H, a.B);
+  jvp_kernel<T, DP><<<grid, NT, smem, a.stream>>>(
+      (const T*)a.Q, (const T*)a.K, (const T*)a.V, a.O, a.L, (const T*)a.UQ, (const T*)a.UK,
+      (const T*)a.UV, a.tau, a.Od, a.Ld, a.H, a.Hkv, a.Nq, a.Nk, a.d, a.causal ? 1 : 0);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t simt_jvp(const JvpArgs& a) {
+  if (a.bf16) return a.d <= 64 ? run_jvp<__nv_bfloat16, 64>(a) : run_jvp<__nv_bfloat16, 128>(a);
+  return a.d <= 64 ? run_jvp<float, 64>(a) : run_jvp<float, 128>(a);
+}
 
 size_t simt_pass1_smem(int d) { return pass1_smem(d <= 64 ? 64 : 128); }
 size_t simt_pass2_smem(int d) { return pass2_smem(d <= 64 ? 64 : 128); }

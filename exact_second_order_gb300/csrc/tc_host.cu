@@ -9,6 +9,8 @@ cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps32);
 cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps64);
+cudaError_t tc_launch_jvp(const JvpArgs& a, const CUtensorMap* maps128,
+                          const CUtensorMap* maps32);
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && a.d == 64; }
 
@@ -39,6 +41,21 @@ cudaError_t tc_bob(const BobArgs& a) {
     e = tc_launch_pass2(a, m128, m64);
   }
   return e;
+}
+
+bool tc_jvp_supported(const JvpArgs& a) { return a.bf16 && a.d == 64; }
+
+cudaError_t tc_jvp(const JvpArgs& a) {
+  CUtensorMap m128[2], m32[4];
+  const void* rows[2] = {a.Q, a.UQ};
+  const void* cols[4] = {a.K, a.V, a.UK, a.UV};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+    e = tc::make_map_bf16_d64(&m128[i], rows[i], a.B * a.H, a.Nq, kTcRows);
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    e = tc::make_map_bf16_d64(&m32[i], cols[i], a.B * a.Hkv, a.Nk, kTcStream);
+  if (e != cudaSuccess) return e;
+  return tc_launch_jvp(a, m128, m32);
 }
 
 }  // namespace flashbob

@@ -25,6 +25,10 @@
 // warpgroup has read a score buffer it overwrites consumed columns with the
 // bf16 A operands (P, P o dP, P o d~P0, dS, P o F) of the output GEMMs,
 // which read A straight from TMEM.
+//
+// The same kernel, instantiated with JVP = true, serves the attention JVP
+// along (U_Q, U_K, U_V): alpha and d~dO do not depend on dO, so with dO = 0
+// (no dP, G scores; only P and P o F as operands) it returns L' and O'.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -117,13 +121,56 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
   tmem_st8(sc + slot_PF(C), oPF);
 }
 
+// The attention JVP's version of p1_chunk (no dO: dP = G = 0): P and
+// P o F only, and the row sum alpha = L'.  The slots of P and P o F lie in
+// S, F' or the dP/G columns, which the JVP's score GEMMs never write.
+template <bool MASKED, int C>
+__device__ __forceinline__ void p1_chunk_jvp(uint32_t sc, const uint32_t (&s)[16],
+                                             const uint32_t (&f)[16], int col0, int jmax,
+                                             float c1, float Lr2, float tau, float& a_acc) {
+  uint32_t oP[8], oPF[8];
+  const int jbase = col0 + 16 * C;
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float pv[2], pf[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = e + h;
+      float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
+      if (MASKED && jbase + j > jmax) p = 0.f;
+      pv[h] = p;
+      pf[h] = p * (u2f(f[j]) * tau);
+      a_acc += pf[h];
+    }
+    oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+    oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
+  }
+  tmem_st8(sc + slot_P(C), oP);
+  tmem_st8(sc + slot_PF(C), oPF);
+}
+
 // One 32-column tile, one row per thread: read all of S, F', dP, G (both
-// 16-column chunks) with a single wait, form the bf16 A operands of the
-// output GEMMs, and hand the tile to the MMA issuer once they are in TMEM.
-template <bool MASKED>
+// 16-column chunks; S and F' only for the JVP) with a single wait, form the
+// bf16 A operands of the output GEMMs, and hand the tile to the MMA issuer
+// once they are in TMEM.
+template <bool MASKED, bool JVP>
 __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready, int col0, int jmax,
                                         float c1, float Lr2, float Dr, float tau, float& a_acc,
                                         float& e_acc) {
+  if constexpr (JVP) {
+    uint32_t s0[16], f0[16], s1[16], f1[16];
+    tmem_ld16(sc + kColS, s0);
+    tmem_ld16(sc + kColF, f0);
+    tmem_ld16(sc + kColS + 16, s1);
+    tmem_ld16(sc + kColF + 16, f1);
+    tmem_wait_ld();
+    p1_chunk_jvp<MASKED, 0>(sc, s0, f0, col0, jmax, c1, Lr2, tau, a_acc);
+    p1_chunk_jvp<MASKED, 1>(sc, s1, f1, col0, jmax, c1, Lr2, tau, a_acc);
+    tmem_wait_st();
+    tc_fence_before();
+    warp_arrive(ready);
+    return;
+  }
   uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
   tmem_ld16(sc + kColS, s0);
   tmem_ld16(sc + kColdP, dp0);
@@ -141,6 +188,10 @@ __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready, int col0, 
   warp_arrive(ready);
 }
 
+// JVP = true: the attention JVP along (U_Q, U_K, U_V), i.e. this pass with
+// dO = 0: no dO block, no dP/G scores, only the d~dO0 accumulator; ddOt
+// receives O' and alpha receives L' (dQt, E, D and mdO are not used).
+template <bool JVP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                     const __grid_constant__ CUtensorMap mUQ, const __grid_constant__ CUtensorMap mK,
@@ -191,9 +242,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mUK);
       tma_prefetch_desc(&mUV);
-      mbar_expect_tx(&sm.bar_q, 3 * BLOCK_BYTES);
+      mbar_expect_tx(&sm.bar_q, (JVP ? 2 : 3) * BLOCK_BYTES);
       tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
-      tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
+      if (!JVP) tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
       tma_load_3d(sm.uq, &mUQ, &sm.bar_q, 0, row0, bh);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -228,6 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t dK0 = smem_desc_sw128(kv0, 16, 1024);                   // K (and K;U_K)
       const uint64_t dV0 = smem_desc_sw128(kv0 + 2 * TILE_BYTES, 16, 1024);  // V (and V;U_V)
       const uint64_t dUK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);
+      const uint64_t dUV0 = smem_desc_sw128(kv0 + 3 * TILE_BYTES, 16, 1024);
       // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
       const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
       // One elected lane issues each group of MMAs as one straight block.
@@ -241,7 +293,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t acc = kk > 0;
             mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);   // [S | F'] = Q [K; U_K]^T
             mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);    // F' += U_Q K^T
-            mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc); // [dP | G] = dO [V; U_V]^T
+            if (!JVP) mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
           }
           mma_commit(&sm.sc_full[t & 1]);
         }
@@ -256,6 +308,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int c = 0; c < 2; ++c) {
             const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
             const uint32_t acc = (t > 0 || c > 0);
+            if (JVP) {  // O'0 += P U_V + (P o F) V
+              mma_ts(tbase + kAccdO, sc + slot_P(c), dUV0 + so + o, idO64, acc);
+              mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);
+              continue;
+            }
             mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
             mma_ts(tbase + kAccR, sc + slot_PdP(c), dK0 + so + o, idO64, acc);   // R += (P o dP) K
             mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
@@ -297,7 +354,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
-    const float Dr = gr < Nq ? D[rowvec] : 0.f;
+    const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
     float a_acc = 0.f, e_acc = 0.f;
     bool ok = true;
     const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
@@ -315,9 +372,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (masked) {
-        p1_tile<true>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_tile<true, JVP>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
       } else {
-        p1_tile<false>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_tile<false, JVP>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
       }
     }
 
@@ -336,12 +393,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int h = 0; h < 2; ++h) {
       const int col = 32 * wg + 16 * h;
       uint32_t vb[16], vr[16], vw[16], vo[16];
-      tmem_ld16(acc_base + kAccB + col, vb);
-      tmem_ld16(acc_base + kAccR + col, vr);
-      tmem_ld16(acc_base + kAccW + col, vw);
+      if (!JVP) {
+        tmem_ld16(acc_base + kAccB + col, vb);
+        tmem_ld16(acc_base + kAccR + col, vr);
+        tmem_ld16(acc_base + kAccW + col, vw);
+      }
       tmem_ld16(acc_base + kAccdO + col, vo);
       tmem_wait_ld();
-      if (ok && gr < Nq) {
+      if (JVP && ok && gr < Nq) {  // O' = (P U_V + (P o F) V) - L' O
+        const size_t off = rowvec * DH + col;
+        const float4* o4 = reinterpret_cast<const float4*>(O + off);
+        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 ov = o4[k];
+          d4[k] = make_float4(u2f(vo[4 * k + 0]) - al * ov.x, u2f(vo[4 * k + 1]) - al * ov.y,
+                              u2f(vo[4 * k + 2]) - al * ov.z, u2f(vo[4 * k + 3]) - al * ov.w);
+        }
+      }
+      if (!JVP && ok && gr < Nq) {
         const size_t off = rowvec * DH + col;
         const float4* o4 = reinterpret_cast<const float4*>(O + off);
         float4* q4 = reinterpret_cast<float4*>(dQt + off);
@@ -365,7 +435,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (ok && wg == 0 && gr < Nq) {
       alpha[rowvec] = al;
-      E[rowvec] = Ei;
+      if (!JVP) E[rowvec] = Ei;
     }
   }
 
@@ -382,15 +452,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 size_t tc_pass1_smem() { return sizeof(Smem1) + 1024; }
 
+cudaError_t tc_launch_jvp(const JvpArgs& a, const CUtensorMap* maps128,
+                          const CUtensorMap* maps32) {
+  // maps128: Q, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
+  const size_t smem = tc_pass1_smem();
+  cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
+  tc_pass1_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[0], maps128[1], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
+      nullptr, nullptr, a.Od, a.Ld, nullptr, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0,
+      a.err);
+  return cudaGetLastError();
+}
+
 cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps32) {
   // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
   const size_t smem = tc_pass1_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+  tc_pass1_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
       a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
       a.causal ? 1 : 0, a.err);

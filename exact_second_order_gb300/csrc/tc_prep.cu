@@ -243,9 +243,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok && gr < Nq) {
         const size_t off = rowvec * DH + col;
         float4* o4 = reinterpret_cast<float4*>(O + off);
-        const uint4* g4 = reinterpret_cast<const uint4*>(dO + off);
+        // dO = D = null: the forward only, no D.
+        const uint4* g4 = dO ? reinterpret_cast<const uint4*>(dO + off) : nullptr;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < 2 && g4; ++k) {
           const uint4 raw = g4[k];  // 8 bf16 of dO
           const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     named_bar_sync(1, 256);
     if (ok && wg == 0 && gr < Nq) {
       L[rowvec] = L2 * kLn2;
-      D[rowvec] = sm.part_d[0][r] + sm.part_d[1][r];
+      if (D) D[rowvec] = sm.part_d[0][r] + sm.part_d[1][r];
     }
   }
 

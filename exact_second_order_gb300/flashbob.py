@@ -31,6 +31,7 @@ _SIGNATURES = {
     "flashbob_bob": ([_P] * 10 + [_F] + [_P] * 6 + [_I] * 8 + [_P], _I),
     "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 8 + [_P], _I),
     "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 8 + [_P], _I),
+    "flashbob_attention_jvp": ([_P] * 8 + [_F] + [_P] * 2 + [_I] * 8 + [_P], _I),
     "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
@@ -78,8 +79,8 @@ def _stream_handle(stream) -> int | None:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _ptr(t) -> int:
-    return t.data_ptr()
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
 
 
 def flashbob_status_string(status: int) -> str:
@@ -88,7 +89,7 @@ def flashbob_status_string(status: int) -> str:
 
 def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream=None) -> None:
     """O, L, D of [B, H, Nq, d] queries and [B, Hkv, Nk, d] keys/values
-    (see flashbob_prep in the header)."""
+    (see flashbob_prep in the header); dO = D = None computes O and L only."""
     B, H, Nq, d = Q.shape
     Hkv, Nk = K.shape[1], K.shape[2]
     st = load_library().flashbob_prep(
@@ -137,6 +138,19 @@ def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt,
         raise FlashbobError(st, "flashbob_bob_pass2")
 
 
+def flashbob_attention_jvp(Q, K, V, O, L, UQ, UK, UV, tau: float, Od, Ld,
+                           causal: bool = False, stream=None) -> None:
+    """O' and L' along the tangents (U_Q, U_K, U_V) (see flashbob_attention_jvp)."""
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    st = load_library().flashbob_attention_jvp(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), _ptr(UQ), _ptr(UK), _ptr(UV), float(tau),
+        _ptr(Od), _ptr(Ld), B, H, Hkv, Nq, Nk, d, int(causal), _dtype_code(Q),
+        _stream_handle(stream))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_attention_jvp")
+
+
 def flashbob_bob_tile_sizes(d: int, in_dtype: int) -> dict:
     """Tiles and dynamic shared memory of flashbob_bob for (d, in_dtype)."""
     v = [ctypes.c_int() for _ in range(4)]
@@ -159,14 +173,27 @@ def flashbob_last_device_error() -> int:
 # ---------------------------------------------------------------------------
 
 def prep(Q, K, V, dO, tau: float, causal: bool = False, stream=None):
-    """Allocate O, L, D on Q's device and run flashbob_prep."""
+    """Allocate O, L, D on Q's device and run flashbob_prep (dO = None: the
+    forward only, D is returned as None)."""
     import torch
     B, H, Nq, d = Q.shape
     O = torch.empty((B, H, Nq, d), dtype=torch.float32, device=Q.device)
     L = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
-    D = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
+    D = None if dO is None else torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
     flashbob_prep(Q, K, V, dO, O, L, D, tau, causal, stream)
     return O, L, D
+
+
+def attention_jvp(Q, K, V, UQ, UK, UV, tau: float, causal: bool = False, O=None, L=None,
+                  stream=None):
+    """O, L (from flashbob_prep when not given) and the tangents O', L'."""
+    import torch
+    if O is None or L is None:
+        O, L, _ = prep(Q, K, V, None, tau, causal, stream)
+    Od = torch.empty_like(O)
+    Ld = torch.empty_like(L)
+    flashbob_attention_jvp(Q, K, V, O, L, UQ, UK, UV, tau, Od, Ld, causal, stream)
+    return O, L, Od, Ld
 
 
 def alloc_bob_outputs(Q, fill: float | None = None, K=None) -> dict:

@@ -75,6 +75,8 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
  *   in : Q, dO [B,H,Nq,d] and K, V [B,Hkv,Nk,d] of in_dtype
  *   out: O [B,H,Nq,d] fp32 (O = P V), L [B,H,Nq] fp32 (natural-log
  *        logsumexp of tau Q K^T per row), D [B,H,Nq] fp32 (D_i = dO_i . O_i)
+ *   dO and D may both be NULL: the forward only (O and L, e.g. for
+ *        flashbob_attention_jvp); exactly one of them NULL is rejected.
  *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
  *   causal: 0 = full attention; 1 = query i sees keys j <= i only (the
  *        setting of [FBN] 实验关键数据); other values are rejected.
@@ -133,6 +135,27 @@ flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, 
                                    const void* UV, float tau, float* dKt, float* dVt, int B,
                                    int H, int Hkv, int Nq, int Nk, int d, int causal,
                                    flashbob_dtype in_dtype, void* stream);
+
+/*
+ * flashbob_attention_jvp: forward-mode derivative of softmax attention
+ * along the tangents (U_Q, U_K, U_V) of (Q, K, V):
+ *     S' = tau (U_Q K^T + Q U_K^T)   (the matrix F of [FBN] 关键设计 1),
+ *     L'_i = sum_j P_ij S'_ij,        O' = P o (S' - L') V + P U_V.
+ *   L' and O' are the alpha and d~dO that flashbob_bob's pass 1 produces
+ *   (neither depends on dO); this call is that pass without dO, so it runs
+ *   5 of pass 1's 11 GEMMs.  No counterpart call is named on the pages; it
+ *   is their pass 1 restricted to the terms without dO.
+ *   in : Q, U_Q [B,H,Nq,d] and K, V, U_K, U_V [B,Hkv,Nk,d] of in_dtype;
+ *        O [B,H,Nq,d], L [B,H,Nq] fp32 from flashbob_prep (dO = D = NULL
+ *        there is enough); tau and causal as in prep.
+ *   out: Od [B,H,Nq,d] fp32 (O'), Ld [B,H,Nq] fp32 (L').
+ *   Limits, ownership and errors: as flashbob_bob.
+ */
+flashbob_status flashbob_attention_jvp(const void* Q, const void* K, const void* V,
+                                       const float* O, const float* L, const void* UQ,
+                                       const void* UK, const void* UV, float tau, float* Od,
+                                       float* Ld, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                       int causal, flashbob_dtype in_dtype, void* stream);
 
 /*
  * flashbob_bob_tile_sizes: the tiles flashbob_bob uses for (d, in_dtype):

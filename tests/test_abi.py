@@ -180,3 +180,35 @@ def test_pass_entry_points_reject_bad_arguments_on_the_host(lib):
     bad[12] += 4
     assert lib.flashbob_bob_pass2(*bad[:11], 0.125, *bad[11:13], *sizes) == \
         fb.FLASHBOB_ERR_MISALIGNED
+
+
+def test_jvp_and_forward_only_prep_reject_bad_arguments_on_the_host(lib):
+    ok = _fake_ptrs(10)
+    sizes = (1, 2, 1, 8, 8, 64, 0, 0, None)  # B, H, Hkv, Nq, Nk, d, causal, dtype, stream
+
+    def jvp(p, tau=0.125, sz=sizes):
+        return lib.flashbob_attention_jvp(*p[:8], tau, *p[8:], *sz)
+    for i in range(10):
+        p = list(ok)
+        p[i] = None
+        assert jvp(p) == fb.FLASHBOB_ERR_INVALID_ARG
+        p = list(ok)
+        p[i] += 8
+        assert jvp(p) == fb.FLASHBOB_ERR_MISALIGNED
+    assert jvp(ok, tau=float("nan")) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert jvp(ok, sz=(1, 3, 2, 8, 8, 64, 0, 0, None)) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert jvp(ok, sz=(1, 2, 1, 8, 0, 64, 0, 0, None)) == fb.FLASHBOB_ERR_INVALID_ARG
+    assert jvp(ok, sz=(1, 2, 1, 8, 8, 64, 2, 0, None)) == fb.FLASHBOB_ERR_INVALID_ARG
+    p = list(ok)
+    p[8] = p[3] + 16  # O' over O
+    assert jvp(p) == fb.FLASHBOB_ERR_INVALID_ARG
+    p = list(ok)
+    p[9] = p[8]  # L' over O'
+    assert jvp(p) == fb.FLASHBOB_ERR_INVALID_ARG
+    # prep: dO and D are both given or both null
+    q = _fake_ptrs(7)
+    for i in (3, 6):
+        p = list(q)
+        p[i] = None
+        assert lib.flashbob_prep(*p, 1, 1, 1, 8, 8, 64, 0.125, 0, 0, None) == \
+            fb.FLASHBOB_ERR_INVALID_ARG
