@@ -229,15 +229,18 @@ flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1
   probe.d = d;
   probe.Nq = probe.Nk = 1;
   probe.bf16 = in_dtype == FLASHBOB_BF16;
-  const bool tc = tc_supported(probe);
+  const bool tc = tc_supported(probe), wide = tc && d == 128;
   const int br1 = tc ? kTcRows : kSimtTile, bc1 = tc ? kTcStream : kSimtTile;
-  const int bc2 = tc ? kTcRows : kSimtTile, br2 = tc ? kTcStream2 : kSimtTile;
+  const int bc2 = tc ? kTcRows : kSimtTile;
+  const int br2 = wide ? kTcStream : tc ? kTcStream2 : kSimtTile;
   if (Br1) *Br1 = br1;
   if (Bc1) *Bc1 = bc1;
   if (Br2) *Br2 = br2;
   if (Bc2) *Bc2 = bc2;
-  if (smem_bytes_pass1) *smem_bytes_pass1 = tc ? tc_pass1_smem() : simt_pass1_smem(d);
-  if (smem_bytes_pass2) *smem_bytes_pass2 = tc ? tc_pass2_smem() : simt_pass2_smem(d);
+  if (smem_bytes_pass1)
+    *smem_bytes_pass1 = wide ? tc_pass1_d128_smem() : tc ? tc_pass1_smem() : simt_pass1_smem(d);
+  if (smem_bytes_pass2)
+    *smem_bytes_pass2 = wide ? tc_pass2_d128_smem() : tc ? tc_pass2_smem() : simt_pass2_smem(d);
   return FLASHBOB_OK;
 }
 

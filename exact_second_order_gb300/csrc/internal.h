@@ -61,7 +61,7 @@ cudaError_t simt_jvp(const JvpArgs& a);
 size_t simt_pass1_smem(int d);
 size_t simt_pass2_smem(int d);
 
-// tcgen05 tensor-core kernels (bf16 inputs, d = 64).
+// tcgen05 tensor-core kernels (bf16 inputs, d = 64; the BoB also d = 128).
 constexpr int kTcRows = 128;    // rows of the resident block (MMA M) in both passes
 constexpr int kTcStream = 32;   // rows of a streamed key tile in pass 1 and prep
 constexpr int kTcStream2 = 64;  // rows of a streamed query tile in pass 2
@@ -73,6 +73,8 @@ bool tc_jvp_supported(const JvpArgs& a);
 cudaError_t tc_jvp(const JvpArgs& a);
 size_t tc_pass1_smem();
 size_t tc_pass2_smem();
+size_t tc_pass1_d128_smem();
+size_t tc_pass2_d128_smem();
 
 // Device error word (one per device): a kernel writes a nonzero code when a
 // bounded wait gives up.  Codes: 1 = mbarrier wait timed out.

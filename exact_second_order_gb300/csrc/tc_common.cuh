@@ -263,10 +263,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // --------------------------------------------------------------------------
 // Host: tensor maps
 // --------------------------------------------------------------------------
-// [BH][N][64] bf16 tensor, box {64, rows, 1}, 128-byte swizzle, zero fill
-// out of bounds.
-inline cudaError_t make_map_bf16_d64(CUtensorMap* map, const void* base, int BH, int N,
-                                     int rows) {
+// [BH][N][dh] bf16 tensor (dh = 64 or 128), box {64, rows, 1}: one
+// 64-column (128-byte) slice of `rows` rows, 128-byte swizzle, zero fill out
+// of bounds.  A 128-column row is loaded as two boxes at x = 0 and x = 64.
+inline cudaError_t make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int rows,
+                                 int dh) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (encode == nullptr) {
     cudaDriverEntryPointQueryResult q;
@@ -277,8 +278,8 @@ inline cudaError_t make_map_bf16_d64(CUtensorMap* map, const void* base, int BH,
       return e != cudaSuccess ? e : cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {64 * 2, (cuuint64_t)N * 64 * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)dh * 2, (cuuint64_t)N * dh * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
@@ -286,6 +287,11 @@ inline cudaError_t make_map_bf16_d64(CUtensorMap* map, const void* base, int BH,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+inline cudaError_t make_map_bf16_d64(CUtensorMap* map, const void* base, int BH, int N,
+                                     int rows) {
+  return make_map_bf16(map, base, BH, N, rows, 64);
 }
 
 }  // namespace tc

@@ -11,10 +11,49 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps64);
 cudaError_t tc_launch_jvp(const JvpArgs& a, const CUtensorMap* maps128,
                           const CUtensorMap* maps32);
+cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
+                                 const CUtensorMap* maps32);
+cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
+                                 const CUtensorMap* maps32);
 
-bool tc_supported(const BobArgs& a) { return a.bf16 && a.d == 64; }
+bool tc_supported(const BobArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
+
+namespace {
+
+// Head dim 128: both passes stream 32-row tiles against 128-row blocks.
+cudaError_t tc_bob_d128(const BobArgs& a) {
+  const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
+  cudaError_t e = cudaSuccess;
+  if (a.passes & kPass1) {
+    CUtensorMap m128[3], m32[4];
+    const void* rows[3] = {a.Q, a.dO, a.UQ};
+    const void* cols[4] = {a.K, a.V, a.UK, a.UV};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16(&m128[i], rows[i], BH, a.Nq, kTcRows, 128);
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16(&m32[i], cols[i], BHkv, a.Nk, kTcStream, 128);
+    if (e != cudaSuccess) return e;
+    e = tc_launch_pass1_d128(a, m128, m32);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.passes & kPass2) {
+    CUtensorMap m128[4], m32[3];
+    const void* res[4] = {a.K, a.UK, a.V, a.UV};
+    const void* str[3] = {a.Q, a.UQ, a.dO};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16(&m128[i], res[i], BHkv, a.Nk, kTcRows, 128);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+      e = tc::make_map_bf16(&m32[i], str[i], BH, a.Nq, kTcStream, 128);
+    if (e != cudaSuccess) return e;
+    e = tc_launch_pass2_d128(a, m128, m32);
+  }
+  return e;
+}
+
+}  // namespace
 
 cudaError_t tc_bob(const BobArgs& a) {
+  if (a.d == 128) return tc_bob_d128(a);
   const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
   cudaError_t e = cudaSuccess;
   if (a.passes & kPass1) {

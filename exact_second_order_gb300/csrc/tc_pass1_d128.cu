@@ -1,0 +1,430 @@
+// Pass 1 of the exact attention backward-over-backward on sm_103a tensor
+// cores for head dim 128 (bf16 inputs, fp32 accumulation in tensor memory).
+//
+// "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+// Attention" (paper notes), 关键设计 2: a block of 128 query rows stays on
+// chip while key/value tiles stream past and every output row is written
+// once.  At d = 128 the four alpha-free accumulators of 关键设计 1 (B, R,
+// Omega, d~dO0, 128 fp32 columns each) would fill all 512 TMEM columns, so
+// this kernel takes the other exact route the same section allows: it
+// streams the key tiles twice.
+//   phase A: scores S, F' = U_Q K^T + Q U_K^T, dP = dO V^T, G = dO U_V^T and
+//            the row sums alpha = sum_j P F and E0 = sum_j P d~P0 only;
+//            then E = E0 - alpha D.
+//   phase B: the same scores again; with alpha and E known per row,
+//            d~S = P o (d~P0 - alpha dP - E), dS = P o (dP - D) and
+//            W = P o (F - alpha) are final, and
+//              d~Q  = tau (d~S K + dS U_K),   d~dO = P U_V + W V
+//            accumulate directly (two 128-column accumulators).
+// The GEMM count per tile is 5 (phase A) + 9 (phase B) instead of 11; the
+// benchmark's FLOP convention still counts the 11 of the one-phase form.
+//
+// CTA = 128 query rows, 320 threads: warp 0 TMA (Q, dO, U_Q once; K, U_K,
+// V, U_V tiles of 32 key rows through a 3-stage ring, each tensor as two
+// 64-column halves in the 128-byte swizzle), warp 1 TMEM allocation and MMA
+// issue, warps 2-5 / 6-9 elementwise warpgroups on alternate tiles.
+// TMEM: [0,128) d~Q accumulator (without tau), [128,256) d~dO accumulator,
+// [256,384) and [384,512) score buffers S | F' | dP | G (32 columns each);
+// in phase B a warpgroup reads a buffer one 16-column chunk at a time and
+// overwrites the columns of that chunk with its bf16 A operands d~S, dS, P,
+// W of the output GEMMs.
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace flashbob {
+namespace {
+using namespace tc;
+
+constexpr int BM = kTcRows;    // 128 query rows per CTA
+constexpr int BN = kTcStream;  // 32 key rows per streamed tile
+constexpr int DH = 128;
+constexpr int NST = 3;
+constexpr int NTHREADS = 320;
+constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB: 128 rows x 64 columns
+constexpr uint32_t HALF_TILE = BN * 64 * 2;   // 4 KiB: 32 rows x 64 columns
+constexpr uint32_t STAGE_BYTES = 2 * 4 * HALF_TILE;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct SmemW1 {
+  alignas(1024) uint8_t q[2][HALF_BLOCK];    // Q, columns 0..63 and 64..127
+  alignas(1024) uint8_t dO[2][HALF_BLOCK];
+  alignas(1024) uint8_t uq[2][HALF_BLOCK];
+  alignas(1024) uint8_t kv[NST][2][4][HALF_TILE];  // [stage][half][K, U_K, V, U_V]
+  float part_a[2][BM];
+  float part_e[2][BM];
+  uint64_t bar_q;
+  uint64_t kv_full[NST];
+  uint64_t kv_empty[NST];
+  uint64_t sc_full[2];
+  uint64_t op_ready[2];
+  uint64_t out_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(SmemW1) + 1024 <= 232448, "shared memory");
+
+constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;
+constexpr uint32_t kAccQ = 0, kAccdO = 128;
+// Phase-B operand slots inside a score buffer: chunk c (key columns
+// 16c..16c+15) writes only the S and F' columns of its own chunk, which it
+// has already read.
+__device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return 16 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 16 * c + 8; }
+__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return kColF + 16 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_W(int c) { return kColF + 16 * c + 8; }
+
+// S, dP, F', G of one 16-column chunk of a score buffer, one row per thread.
+struct Chunk {
+  uint32_t s[16], dp[16], f[16], g[16];
+};
+
+__device__ __forceinline__ void load_chunk(uint32_t sc, int c, Chunk& x) {
+  tmem_ld16(sc + kColS + 16 * c, x.s);
+  tmem_ld16(sc + kColdP + 16 * c, x.dp);
+  tmem_ld16(sc + kColF + 16 * c, x.f);
+  tmem_ld16(sc + kColG + 16 * c, x.g);
+}
+
+// Phase A on one chunk: the row sums alpha += P F and E0 += P d~P0.
+template <bool MASKED>
+__device__ __forceinline__ void phase_a_sums(const Chunk& x, int jbase, int jmax, float c1,
+                                             float Lr2, float Dr, float tau, float& a_acc,
+                                             float& e_acc) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float p = ex2_approx(fmaf(u2f(x.s[j]), c1, -Lr2));
+    if (MASKED && jbase + j > jmax) p = 0.f;
+    const float ft = u2f(x.f[j]) * tau;
+    const float dpt0 = fmaf(ft, u2f(x.dp[j]) - Dr, u2f(x.g[j]));
+    a_acc = fmaf(p, ft, a_acc);
+    e_acc = fmaf(p, dpt0, e_acc);
+  }
+}
+
+// Phase B on one 16-column chunk: the four bf16 A operands, written to TMEM.
+template <bool MASKED, int C>
+__device__ __forceinline__ void phase_b_chunk(uint32_t sc, const Chunk& x, int col0, int jmax,
+                                              float c1, float Lr2, float Dr, float tau, float al,
+                                              float Ei) {
+  uint32_t odst[8], ods[8], op[8], ow[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float vdst[2], vds[2], vp[2], vw[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = e + h;
+      float p = ex2_approx(fmaf(u2f(x.s[j]), c1, -Lr2));
+      if (MASKED && col0 + 16 * C + j > jmax) p = 0.f;
+      const float dpv = u2f(x.dp[j]);
+      const float xx = dpv - Dr;
+      const float ft = u2f(x.f[j]) * tau;
+      const float dpt0 = fmaf(ft, xx, u2f(x.g[j]));
+      vdst[h] = p * (dpt0 - fmaf(al, dpv, Ei));
+      vds[h] = p * xx;
+      vp[h] = p;
+      vw[h] = p * (ft - al);
+    }
+    odst[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
+    ods[e >> 1] = pack_bf16x2(vds[0], vds[1]);
+    op[e >> 1] = pack_bf16x2(vp[0], vp[1]);
+    ow[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+  }
+  tmem_st8(sc + slot_dSt(C), odst);
+  tmem_st8(sc + slot_dS(C), ods);
+  tmem_st8(sc + slot_P(C), op);
+  tmem_st8(sc + slot_W(C), ow);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_pass1_d128_kernel(const __grid_constant__ CUtensorMap mQ,
+                         const __grid_constant__ CUtensorMap mdO,
+                         const __grid_constant__ CUtensorMap mUQ,
+                         const __grid_constant__ CUtensorMap mK,
+                         const __grid_constant__ CUtensorMap mV,
+                         const __grid_constant__ CUtensorMap mUK,
+                         const __grid_constant__ CUtensorMap mUV, const float* __restrict__ O,
+                         const float* __restrict__ L, const float* __restrict__ D,
+                         float* __restrict__ dQt, float* __restrict__ ddOt,
+                         float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv,
+                         int Nq, int Nk, float tau, int causal, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemW1& sm = *reinterpret_cast<SmemW1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * H + blockIdx.y;
+  const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);  // shared key/value head
+  const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
+  const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
+  const int T = (col_end + BN - 1) / BN;  // key tiles per phase
+  const int T2 = 2 * T;                   // phase A tiles 0..T-1, phase B tiles T..2T-1
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.bar_q, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.sc_full[b], 1);
+      mbar_init(&sm.op_ready[b], 4);
+    }
+    mbar_init(&sm.out_full, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      tma_prefetch_desc(&mUK);
+      tma_prefetch_desc(&mUV);
+      mbar_expect_tx(&sm.bar_q, 6 * HALF_BLOCK);
+      for (int h = 0; h < 2; ++h) {
+        tma_load_3d(sm.q[h], &mQ, &sm.bar_q, 64 * h, row0, bh);
+        tma_load_3d(sm.dO[h], &mdO, &sm.bar_q, 64 * h, row0, bh);
+        tma_load_3d(sm.uq[h], &mUQ, &sm.bar_q, 64 * h, row0, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < T2; ++t) {
+        const int s = t % NST;
+        const int kt = t < T ? t : t - T;
+        if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+        mbar_expect_tx(&sm.kv_full[s], STAGE_BYTES);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(sm.kv[s][h][0], &mK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+          tma_load_3d(sm.kv[s][h][1], &mUK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+          tma_load_3d(sm.kv[s][h][2], &mV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+          tma_load_3d(sm.kv[s][h][3], &mUV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+        }
+        issued = t + 1;
+      }
+      // No copy may still be in flight when the CTA exits.
+      drain_wait(&sm.bar_q, 0);
+      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
+        drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
+    constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
+    constexpr uint32_t idO128 = idesc_bf16(BM, DH, true);      // N = 128, B MN-major
+    uint64_t dq[2], ddo[2], duq[2], dK[2], dV[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      dq[h] = smem_desc_sw128(smem_u32(sm.q[h]), 16, 1024);
+      ddo[h] = smem_desc_sw128(smem_u32(sm.dO[h]), 16, 1024);
+      duq[h] = smem_desc_sw128(smem_u32(sm.uq[h]), 16, 1024);
+      dK[h] = smem_desc_sw128(smem_u32(sm.kv[0][h][0]), 16, 1024);  // K (and K; U_K)
+      dV[h] = smem_desc_sw128(smem_u32(sm.kv[0][h][2]), 16, 1024);  // V (and V; U_V)
+    }
+    // MN-major N = 128 operands: columns 64..127 (half 1) sit 4 tiles after
+    // columns 0..63 (half 0) of the same tensor.
+    constexpr uint32_t kHalfStride = 4 * HALF_TILE;
+    const uint64_t dKmn = smem_desc_sw128(smem_u32(sm.kv[0][0][0]), kHalfStride, 1024);
+    const uint64_t dUKmn = smem_desc_sw128(smem_u32(sm.kv[0][0][1]), kHalfStride, 1024);
+    const uint64_t dVmn = smem_desc_sw128(smem_u32(sm.kv[0][0][2]), kHalfStride, 1024);
+    const uint64_t dUVmn = smem_desc_sw128(smem_u32(sm.kv[0][0][3]), kHalfStride, 1024);
+    auto issue_scores = [&](int t) {
+      const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
+      const uint32_t sc = tbase + 256 + 128 * (t & 1);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const int h = kk >> 2;
+          const uint64_t o = 2 * (kk & 3);  // 16 bf16 inside the 128-byte row
+          const uint32_t acc = kk > 0;
+          mma_ss(sc + kColS, dq[h] + o, dK[h] + so + o, idS64, acc);    // [S | F'] = Q [K; U_K]^T
+          mma_ss(sc + kColF, duq[h] + o, dK[h] + so + o, idS32, 1);     // F' += U_Q K^T
+          mma_ss(sc + kColdP, ddo[h] + o, dV[h] + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
+        }
+        mma_commit(&sm.sc_full[t & 1]);
+      }
+      __syncwarp();
+    };
+    auto issue_outputs = [&](int t) {  // phase B only; phase A just frees the stage
+      const int s = t % NST;
+      const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
+      const uint32_t sc = tbase + 256 + 128 * (t & 1);
+      if (elect_one()) {
+        if (t >= T) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
+            const uint32_t acc = (t > T || c > 0);
+            mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
+            mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //     +  dS U_K
+            mma_ts(tbase + kAccdO, sc + slot_P(c), dUVmn + so + o, idO128, acc);  // d~dO += P U_V
+            mma_ts(tbase + kAccdO, sc + slot_W(c), dVmn + so + o, idO128, 1);     //      +  W V
+          }
+        }
+        mma_commit(&sm.kv_empty[s]);
+      }
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
+    tc_fence_after();
+    for (int t = 0; ok && t < 2 && t < T2; ++t) {
+      ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+      tc_fence_after();
+      if (ok) issue_scores(t);
+    }
+    for (int t = 0; ok && t < T2; ++t) {
+      ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+      if (!ok) break;
+      tc_fence_after();
+      issue_outputs(t);
+      if (t + 2 < T2) {
+        ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores(t + 2);
+      }
+    }
+    if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
+    __syncwarp();
+  } else {
+    // ---------------- elementwise warpgroups + epilogue ----------------
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // row inside the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int gr = row0 + r;
+    const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
+    const float c1 = tau * kLog2e;
+    const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
+    const float Dr = gr < Nq ? D[rowvec] : 0.f;
+    float a_acc = 0.f, e_acc = 0.f, al = 0.f, Ei = 0.f;
+    bool ok = true, have_ae = false;
+    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
+    // Both warpgroups have finished phase A: alpha and E of the row.  Each
+    // warpgroup passes here exactly once (named barrier 1).
+    auto combine = [&]() {
+      sm.part_a[wg][r] = a_acc;
+      sm.part_e[wg][r] = e_acc;
+      named_bar_sync(1, 256);
+      al = sm.part_a[0][r] + sm.part_a[1][r];
+      Ei = (sm.part_e[0][r] + sm.part_e[1][r]) - al * Dr;
+      have_ae = true;
+    };
+
+    for (int u = 0;; ++u) {
+      const int t = 2 * u + wg;
+      if (t >= T2) break;
+      const bool phase_b = t >= T;
+      if (phase_b && !have_ae) combine();
+      // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
+      // failed wait keep looping so both warpgroups reach the named barrier.
+      ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
+      if (!ok) continue;
+      tc_fence_after();
+      const int col0 = (phase_b ? t - T : t) * BN;
+      const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
+      const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
+      if (!phase_b) {
+        Chunk x0, x1;
+        load_chunk(sc, 0, x0);
+        load_chunk(sc, 1, x1);
+        tmem_wait_ld();
+        tc_fence_before();
+        warp_arrive(&sm.op_ready[wg]);  // the buffer is in registers
+        if (masked) {
+          phase_a_sums<true>(x0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+          phase_a_sums<true>(x1, col0 + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        } else {
+          phase_a_sums<false>(x0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+          phase_a_sums<false>(x1, col0 + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        }
+      } else {
+        {
+          Chunk x;
+          load_chunk(sc, 0, x);
+          tmem_wait_ld();
+          if (masked)
+            phase_b_chunk<true, 0>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al, Ei);
+          else
+            phase_b_chunk<false, 0>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al, Ei);
+        }
+        {
+          Chunk x;
+          load_chunk(sc, 1, x);
+          tmem_wait_ld();
+          if (masked)
+            phase_b_chunk<true, 1>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al, Ei);
+          else
+            phase_b_chunk<false, 1>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al, Ei);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&sm.op_ready[wg]);
+      }
+    }
+    if (!have_ae) combine();  // a warpgroup with no phase-B tile (T = 1)
+
+    // Epilogue: warpgroup wg writes output columns [64 wg, 64 wg + 64).
+    ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    tc_fence_after();
+    const uint32_t acc_base = tbase + lane_off;
+#pragma unroll 1
+    for (int h = 0; h < 4; ++h) {
+      const int col = 64 * wg + 16 * h;
+      uint32_t vq[16], vo[16];
+      tmem_ld16(acc_base + kAccQ + col, vq);
+      tmem_ld16(acc_base + kAccdO + col, vo);
+      tmem_wait_ld();
+      if (ok && gr < Nq) {
+        const size_t off = rowvec * DH + col;
+        float4* q4 = reinterpret_cast<float4*>(dQt + off);
+        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          q4[k] = make_float4(tau * u2f(vq[4 * k]), tau * u2f(vq[4 * k + 1]),
+                              tau * u2f(vq[4 * k + 2]), tau * u2f(vq[4 * k + 3]));
+          d4[k] = make_float4(u2f(vo[4 * k]), u2f(vo[4 * k + 1]), u2f(vo[4 * k + 2]),
+                              u2f(vo[4 * k + 3]));
+        }
+      }
+    }
+    if (ok && wg == 0 && gr < Nq) {
+      alpha[rowvec] = al;
+      E[rowvec] = Ei;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+size_t tc_pass1_d128_smem() { return sizeof(SmemW1) + 1024; }
+
+cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
+                                 const CUtensorMap* maps32) {
+  // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
+  // boxes; every box is 64 columns wide (one half of a 128-column row).
+  const size_t smem = tc_pass1_d128_smem();
+  cudaError_t e = cudaFuncSetAttribute(tc_pass1_d128_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
+  tc_pass1_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
+      a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace flashbob

@@ -1,0 +1,411 @@
+// Pass 2 of the exact attention backward-over-backward on sm_103a tensor
+// cores for head dim 128 (bf16 inputs, fp32 accumulation in tensor memory).
+//
+// "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+// Attention" (paper notes), 关键设计 2: a block of 128 key rows stays on chip
+// while query row tiles stream past with the row scalars (alpha, E) of pass
+// 1; d~K and d~V are summed on chip and written once, with no atomics.  With
+// the transposed scores of the resident key rows j against a streamed query
+// row i:
+//     dS = P o (dP - D),  d~S = P o (F o (dP - D) + G - alpha dP - E),
+//     W = P o (F - alpha),
+//     d~K_j = tau sum_i (d~S_ij Q_i + dS_ij U_Q,i),   d~V_j = sum_i W_ij dO_i.
+//
+// CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
+//   warp 0      TMA: the resident K, U_K, V, U_V block (each as two 64-column
+//               halves in the 128-byte swizzle), then Q, U_Q, dO tiles of 32
+//               query rows through a 3-stage ring;
+//   warp 1      TMEM allocation and MMA issue;
+//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: query rows 0-15 / 16-31
+//               of every tile (the K step of the output GEMMs they feed).
+// TMEM: [0,128) d~K, [128,256) d~V accumulators; [256,384) one score buffer
+// S^T | F'^T | dP^T | G^T (32 columns each); [384,432) the bf16 A operands
+// dS^T, d~S^T, W^T.  The score buffer is released in two halves, S^T | F'^T
+// first, so the S/F' GEMMs of the next tile run while the warpgroups still
+// read and process dP/G.  Grouped-query attention: the query tiles of all
+// H / Hkv heads sharing the key/value head stream past the same block
+// ([FBN] 关键设计 3).
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace flashbob {
+namespace {
+using namespace tc;
+
+constexpr int BM = kTcRows;  // 128 key rows per CTA
+constexpr int BQ = 32;       // query rows per streamed tile
+constexpr int DH = 128;
+constexpr int NST = 3;
+constexpr int NTHREADS = 320;
+constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB
+constexpr uint32_t HALF_TILE = BQ * 64 * 2;   // 4 KiB
+constexpr uint32_t STAGE_BYTES = 2 * 3 * HALF_TILE;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct SmemW2 {
+  alignas(1024) uint8_t kb[4][2][HALF_BLOCK];         // K, U_K, V, U_V (resident) x halves
+  alignas(1024) uint8_t st[NST][2][3][HALF_TILE];     // [stage][half][Q, U_Q, dO]
+  float4 scal[2][2][16];  // per warpgroup, double-buffered: (L log2 e, D, alpha, E)
+  uint64_t bar_kv;
+  uint64_t st_full[NST];
+  uint64_t st_empty[NST];
+  uint64_t sc_full;
+  uint64_t sf_free;   // both warpgroups have read S^T and F'^T (8 warps)
+  uint64_t pg_free;   // both warpgroups have read dP^T and G^T (8 warps)
+  uint64_t op_ready;  // the operands of a tile are in TMEM (8 warps)
+  uint64_t op_free;   // the output GEMMs of a tile have completed
+  uint64_t out_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(SmemW2) + 1024 <= 232448, "shared memory");
+
+constexpr uint32_t kAccK = 0, kAccV = 128;
+constexpr uint32_t kSc = 256;
+constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;  // inside the score buffer
+constexpr uint32_t kOp = 384;  // operand x, K step kk at kOp + 16 x + 8 kk
+constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
+
+__device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
+  return kOp + 16 * x + 8 * kk;
+}
+
+// The 16 query rows of one warpgroup: read S^T, F'^T (release), dP^T, G^T
+// (release), form dS, d~S, W as bf16 pairs and write them to the operand
+// area once the previous tile's output GEMMs are done with it.
+template <bool MASKED>
+__device__ __forceinline__ bool p2w_half(uint32_t sc, uint32_t opb, int wg, const float4* scal,
+                                         int ibase, int gj, float c1, float tau, SmemW2& sm,
+                                         int t, volatile int* abort_flag, unsigned int* err) {
+  const int col = 16 * wg;
+  uint32_t s[16], f[16], dp[16], g[16];
+  tmem_ld16(sc + kColS + col, s);
+  tmem_ld16(sc + kColF + col, f);
+  tmem_wait_ld();
+  tc_fence_before();
+  warp_arrive(&sm.sf_free);
+  tmem_ld16(sc + kColdP + col, dp);
+  tmem_ld16(sc + kColG + col, g);
+  tmem_wait_ld();
+  tc_fence_before();
+  warp_arrive(&sm.pg_free);
+  uint32_t ods[8], odst[8], ow[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float vds[2], vdst[2], vw[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = e + h;
+      const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row ibase + i
+      float p = ex2_approx(fmaf(u2f(s[i]), c1, -rs.x));
+      if (MASKED && ibase + i < gj) p = 0.f;
+      const float dpv = u2f(dp[i]);
+      const float x = dpv - rs.y;
+      const float ft = u2f(f[i]) * tau;
+      vds[h] = p * x;
+      vdst[h] = p * (fmaf(ft, x, u2f(g[i])) - fmaf(rs.z, dpv, rs.w));
+      vw[h] = p * (ft - rs.z);
+    }
+    ods[e >> 1] = pack_bf16x2(vds[0], vds[1]);
+    odst[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
+    ow[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+  }
+  if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
+  tc_fence_after();
+  tmem_st8(opb + op_col(kOpdS, wg), ods);
+  tmem_st8(opb + op_col(kOpdSt, wg), odst);
+  tmem_st8(opb + op_col(kOpW, wg), ow);
+  tmem_wait_st();
+  tc_fence_before();
+  warp_arrive(&sm.op_ready);
+  return true;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_pass2_d128_kernel(const __grid_constant__ CUtensorMap mK,
+                         const __grid_constant__ CUtensorMap mUK,
+                         const __grid_constant__ CUtensorMap mV,
+                         const __grid_constant__ CUtensorMap mUV,
+                         const __grid_constant__ CUtensorMap mQ,
+                         const __grid_constant__ CUtensorMap mUQ,
+                         const __grid_constant__ CUtensorMap mdO, const float* __restrict__ L,
+                         const float* __restrict__ D, const float* __restrict__ alpha,
+                         const float* __restrict__ E, float* __restrict__ dKt,
+                         float* __restrict__ dVt, int H, int Hkv, int Nq, int Nk, float tau,
+                         int causal, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemW2& sm = *reinterpret_cast<SmemW2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = H / Hkv;
+  const int bkv = blockIdx.z * Hkv + blockIdx.y;
+  const int hq0 = blockIdx.z * H + blockIdx.y * G;  // first query head of the group
+  const int j0 = blockIdx.x * BM;
+  // Query tiles t0 .. stream past (causal: key j is seen only by queries
+  // i >= j; none when j0 >= Nq, and then T = 0 and the outputs are 0).
+  // f = (query head in group) * Tq + (tile - t0) numbers the streamed tiles.
+  const int t0 = causal ? j0 / BQ : 0;
+  const int Tq = max(0, (Nq + BQ - 1) / BQ - t0);
+  const int T = G * Tq;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.bar_kv, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.st_full[s], 1);
+      mbar_init(&sm.st_empty[s], 1);
+    }
+    mbar_init(&sm.sc_full, 1);
+    mbar_init(&sm.sf_free, 8);
+    mbar_init(&sm.pg_free, 8);
+    mbar_init(&sm.op_ready, 8);
+    mbar_init(&sm.op_free, 1);
+    mbar_init(&sm.out_full, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mUQ);
+      tma_prefetch_desc(&mdO);
+      mbar_expect_tx(&sm.bar_kv, 8 * HALF_BLOCK);
+      for (int h = 0; h < 2; ++h) {
+        tma_load_3d(sm.kb[0][h], &mK, &sm.bar_kv, 64 * h, j0, bkv);
+        tma_load_3d(sm.kb[1][h], &mUK, &sm.bar_kv, 64 * h, j0, bkv);
+        tma_load_3d(sm.kb[2][h], &mV, &sm.bar_kv, 64 * h, j0, bkv);
+        tma_load_3d(sm.kb[3][h], &mUV, &sm.bar_kv, 64 * h, j0, bkv);
+      }
+      int issued = 0, ft = 0, fz = hq0;  // (tile in head, query head) of tile t
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NST;
+        if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+        const int row = (ft + t0) * BQ;
+        mbar_expect_tx(&sm.st_full[s], STAGE_BYTES);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(sm.st[s][h][0], &mQ, &sm.st_full[s], 64 * h, row, fz);
+          tma_load_3d(sm.st[s][h][1], &mUQ, &sm.st_full[s], 64 * h, row, fz);
+          tma_load_3d(sm.st[s][h][2], &mdO, &sm.st_full[s], 64 * h, row, fz);
+        }
+        if (++ft == Tq) { ft = 0; ++fz; }
+        issued = t + 1;
+      }
+      // No copy may still be in flight when the CTA exits.
+      drain_wait(&sm.bar_kv, 0);
+      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
+        drain_wait(&sm.st_full[t % NST], (t / NST) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BQ, false);  // N = 64, B K-major
+    constexpr uint32_t idS32 = idesc_bf16(BM, BQ, false);      // N = 32, B K-major
+    constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 128, B MN-major
+    uint64_t dK[2], dUK[2], dV[2], dUV[2], dQ[2], ddO[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      dK[h] = smem_desc_sw128(smem_u32(sm.kb[0][h]), 16, 1024);
+      dUK[h] = smem_desc_sw128(smem_u32(sm.kb[1][h]), 16, 1024);
+      dV[h] = smem_desc_sw128(smem_u32(sm.kb[2][h]), 16, 1024);
+      dUV[h] = smem_desc_sw128(smem_u32(sm.kb[3][h]), 16, 1024);
+      dQ[h] = smem_desc_sw128(smem_u32(sm.st[0][h][0]), 16, 1024);  // Q (and Q; U_Q)
+      ddO[h] = smem_desc_sw128(smem_u32(sm.st[0][h][2]), 16, 1024);
+    }
+    // MN-major N = 128 operands of the output GEMMs: columns 64..127 (half 1)
+    // sit 3 tiles after columns 0..63 (half 0) of the same tensor.
+    constexpr uint32_t kHalfStride = 3 * HALF_TILE;
+    const uint64_t dQmn = smem_desc_sw128(smem_u32(sm.st[0][0][0]), kHalfStride, 1024);
+    const uint64_t dUQmn = smem_desc_sw128(smem_u32(sm.st[0][0][1]), kHalfStride, 1024);
+    const uint64_t ddOmn = smem_desc_sw128(smem_u32(sm.st[0][0][2]), kHalfStride, 1024);
+    const uint32_t sc = tbase + kSc;
+    // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
+    auto issue_sf = [&](int t) {
+      const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const int h = kk >> 2;
+          const uint64_t o = 2 * (kk & 3);
+          mma_ss(sc + kColS, dK[h] + o, dQ[h] + so + o, idS64, kk > 0);  // [S^T | F'^T] = K [Q; U_Q]^T
+          mma_ss(sc + kColF, dUK[h] + o, dQ[h] + so + o, idS32, 1);      // F'^T += U_K Q^T
+        }
+      }
+      __syncwarp();
+    };
+    auto issue_pg = [&](int t) {
+      const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const int h = kk >> 2;
+          const uint64_t o = 2 * (kk & 3);
+          mma_ss(sc + kColdP, dV[h] + o, ddO[h] + so + o, idS32, kk > 0);  // dP^T = V dO^T
+          mma_ss(sc + kColG, dUV[h] + o, ddO[h] + so + o, idS32, kk > 0);  // G^T  = U_V dO^T
+        }
+        mma_commit(&sm.sc_full);
+      }
+      __syncwarp();
+    };
+    auto issue_outputs = [&](int t) {
+      const int s = t % NST;
+      const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint64_t o = (uint64_t)(16 * 128 * kk) >> 4;  // 16 query rows further down
+          const uint32_t acc = (t > 0 || kk > 0);
+          mma_ts(tbase + kAccK, tbase + op_col(kOpdSt, kk), dQmn + so + o, idO, acc);  // d~K += d~S^T Q
+          mma_ts(tbase + kAccK, tbase + op_col(kOpdS, kk), dUQmn + so + o, idO, 1);    //     +  dS^T U_Q
+          mma_ts(tbase + kAccV, tbase + op_col(kOpW, kk), ddOmn + so + o, idO, acc);   // d~V += W^T dO
+        }
+        mma_commit(&sm.op_free);
+        mma_commit(&sm.st_empty[s]);
+      }
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
+    for (int t = 0; ok && t < T; ++t) {
+      if (t > 0) {
+        ok = mbar_wait_warp(&sm.sf_free, (t - 1) & 1, abort_flag, err);
+        if (!ok) break;
+      }
+      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+      if (!ok) break;
+      tc_fence_after();
+      issue_sf(t);
+      if (t > 0) {
+        ok = mbar_wait_warp(&sm.pg_free, (t - 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      issue_pg(t);
+      if (t > 0) {
+        ok = mbar_wait_warp(&sm.op_ready, (t - 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_outputs(t - 1);
+      }
+    }
+    if (ok && T > 0) {
+      ok = mbar_wait_warp(&sm.op_ready, (T - 1) & 1, abort_flag, err);
+      tc_fence_after();
+      if (ok) issue_outputs(T - 1);
+    }
+    if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
+    __syncwarp();
+  } else {
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // key row inside the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int gj = j0 + r;
+    const float c1 = tau * kLog2e;
+    const uint32_t sc = tbase + lane_off + kSc;
+    const uint32_t opb = tbase + lane_off;
+    const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
+    bool ok = true;
+
+    // Row scalars of this warpgroup's 16 query rows of streamed tile f
+    // (tile ft of the head whose rows start at fL - L); rows past Nq get
+    // L = +inf so that P = exp2(-inf) = 0.  Lanes 16..31 load nothing.
+    int ft = 0;
+    const float* fL = L + static_cast<size_t>(hq0) * Nq;
+    auto load_scalars = [&](int f) {
+      const int i = (ft + t0) * BQ + 16 * wg + lane;
+      float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
+      if (lane < 16 && f < T && i < Nq) {
+        const size_t o = static_cast<size_t>(fL - L) + i;
+        v = make_float4(fL[i] * kLog2e, D[o], alpha[o], E[o]);
+      }
+      if (++ft == Tq) { ft = 0; fL += Nq; }
+      return v;
+    };
+    if (loader) {
+      const float4 v = load_scalars(0);
+      if (lane < 16) sm.scal[wg][0][lane] = v;
+    }
+    int tq = 0;  // tile of the current query head
+    for (int t = 0; t < T; ++t) {
+      const float4* scal = sm.scal[wg][t & 1];
+      named_bar_sync(2 + wg, 128);  // scal is written; last tile's readers are done
+      float4 next = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (loader) next = load_scalars(t + 1);
+      ok = ok && mbar_wait_warp(&sm.sc_full, t & 1, abort_flag, err);
+      if (ok) {
+        tc_fence_after();
+        const int ibase = (tq + t0) * BQ + 16 * wg;
+        if (causal && ibase < j0 + BM)
+          ok = p2w_half<true>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+        else
+          ok = p2w_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+      }
+      if (loader && lane < 16) sm.scal[wg][(t + 1) & 1][lane] = next;
+      if (++tq == Tq) tq = 0;
+    }
+
+    ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    tc_fence_after();
+    const uint32_t acc_base = tbase + lane_off;
+#pragma unroll 1
+    for (int h = 0; h < 4; ++h) {
+      const int col = 64 * wg + 16 * h;
+      uint32_t vk[16], vv[16];
+      tmem_ld16(acc_base + kAccK + col, vk);
+      tmem_ld16(acc_base + kAccV + col, vv);
+      tmem_wait_ld();
+      if (ok && gj < Nk) {
+        const size_t off = (static_cast<size_t>(bkv) * Nk + gj) * DH + col;
+        float4* k4 = reinterpret_cast<float4*>(dKt + off);
+        float4* v4 = reinterpret_cast<float4*>(dVt + off);
+        // T = 0: no query sees this key block, the accumulators were never
+        // written, and the outputs are exact zeros.
+        if (T == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          k4[k] = make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]),
+                              tau * u2f(vk[4 * k + 2]), tau * u2f(vk[4 * k + 3]));
+          v4[k] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
+                              u2f(vv[4 * k + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+size_t tc_pass2_d128_smem() { return sizeof(SmemW2) + 1024; }
+
+cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
+                                 const CUtensorMap* maps32) {
+  // maps128: K, U_K, V, U_V with 128-row boxes; maps32: Q, U_Q, dO with
+  // 32-row boxes; every box is 64 columns wide.
+  const size_t smem = tc_pass2_d128_smem();
+  cudaError_t e = cudaFuncSetAttribute(tc_pass2_d128_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nk + BM - 1) / BM, a.Hkv, a.B);  // one CTA per key block of a shared head
+  tc_pass2_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D,
+      a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace flashbob

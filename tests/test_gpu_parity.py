@@ -148,7 +148,7 @@ def test_bad_arguments_return_codes_and_launch_nothing():
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("N", [1, 5, 32, 127, 128, 129, 300, 700])
-@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (64, "f32"), (96, "bf16")])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (64, "f32"), (96, "bf16"), (128, "bf16")])
 def test_causal_small_shapes(N, d, dtype):
     _check_full(wl.small_workload(1, 2, N, d, dtype, seed=N + d, causal=True))
 
@@ -172,7 +172,7 @@ def test_causal_pages_shape_sampled_rows():
 
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (4, 1), (6, 3)])
 @pytest.mark.parametrize("N", [1, 65, 300])
-@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96), ("bf16", 128)])
 def test_gqa_small_shapes(H, Hkv, N, dtype, d):
     _check_full(wl.small_workload(2, H, N, d, dtype, seed=N + H, Hkv=Hkv))
 
@@ -201,7 +201,7 @@ def test_gqa_workloads_sampled_rows(w):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,Nk", [(1, 300), (65, 7), (129, 300), (300, 129), (200, 1)])
-@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96), ("bf16", 128)])
 def test_rectangular_small_shapes(N, Nk, dtype, d, causal):
     # causal with Nk >= Nq + 128 leaves whole key blocks that no query sees
     _check_full(wl.small_workload(1, 2, N, d, dtype, seed=N + Nk, Nk=Nk, causal=causal))
@@ -222,4 +222,35 @@ def test_rectangular_workloads_sampled_rows(w):
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
     full = full_oracle_errors(w, x, state, out, heads=[(0, 3)])
+    assert max(full.values()) <= TOL["bf16"], full
+
+
+# --------------------------------------------------------------------------
+# Head dim 128 on the tensor cores
+# --------------------------------------------------------------------------
+
+def test_d128_runs_the_tensor_core_tiles():
+    t = fb.flashbob_bob_tile_sizes(128, fb.FLASHBOB_BF16)
+    assert (t["Br1"], t["Bc1"], t["Br2"], t["Bc2"]) == (128, 32, 32, 128)
+
+
+@pytest.mark.parametrize("w", [wl.small_workload(1, 2, 700, 128, "bf16", seed=21,
+                                                 peaked_k_rows=True, stress=True),
+                               wl.small_workload(2, 6, 1000, 128, "bf16", seed=22, Hkv=2,
+                                                 causal=True),
+                               wl.small_workload(1, 3, 777, 128, "bf16", seed=23, Nk=1300)],
+                         ids=lambda w: w.name)
+def test_d128_stress_gqa_causal_rectangular(w):
+    _check_full(w)
+
+
+def test_d128_mid_length_sampled_rows():
+    w = wl.Workload("mid_B1_H4_N8192_d128", 1, 4, 8192, 128, "bf16", causal=True)
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=[(0, 0), (0, 3)])
+    assert max(errs.values()) <= TOL["bf16"], errs
+    res = column_sum_residuals(out)
+    assert max(res.values()) <= TOL["bf16"], res
+    full = full_oracle_errors(w, x, state, out, heads=[(0, 1)])
     assert max(full.values()) <= TOL["bf16"], full
