@@ -71,6 +71,10 @@ constexpr uint32_t kSc = 128;  // score buffer
 constexpr uint32_t kColS = 0, kColF = 64, kColdP = 128, kColG = 192;  // inside the score buffer
 constexpr uint32_t kOp = 384;  // operand area: operand x, K step kk at kOp + 32 x + 8 kk
 constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
+// Cluster split: a row of staged partial sums (d~K | d~V, fp32) in the ring
+// buffer, padded against bank conflicts.
+constexpr int kStageStride = 2 * DH + 4;
+static_assert(BM * kStageStride * 4 <= NST * 3 * TILE_BYTES, "staging fits in the ring");
 
 __device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
   return kOp + 32 * x + 8 * kk;
@@ -163,18 +167,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float* __restrict__ D, const float* __restrict__ alpha,
                     const float* __restrict__ E, float* __restrict__ dKt,
                     float* __restrict__ dVt, int H, int Hkv, int Nq, int Nk, float tau,
-                    int causal,
-                    unsigned int* err) {
+                    int causal, int S, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   Smem2& sm = *reinterpret_cast<Smem2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // One CTA per key block of a key/value head.  Grouped-query attention: the
   // G = H / Hkv query heads sharing the head stream past one after the other
-  // and their contributions are summed on chip ([FBN] 关键设计 3).
-  const int G = H / Hkv;
-  const int bkv = blockIdx.z * Hkv + blockIdx.y;
-  const int hq0 = blockIdx.z * H + blockIdx.y * G;  // first query head of the group
+  // and their contributions are summed on chip ([FBN] 关键设计 3).  When the
+  // key blocks alone cannot fill the GPU, a cluster of S CTAs (blockIdx.y =
+  // S * head + rank) shares a key block, each streams G / S of the heads, and
+  // the partial sums meet in distributed shared memory before the one write.
+  const int G = H / Hkv, Gs = G / S;
+  const int bkv = blockIdx.z * Hkv + blockIdx.y / S;
+  const int hq0 = blockIdx.z * H + (blockIdx.y / S) * G + (blockIdx.y % S) * Gs;  // first head
   const int j0 = blockIdx.x * BM;
   // Query tiles t0 .. of 64 rows stream past; under the causal mask key j is
   // seen only by queries i >= j, so the tiles before the block are skipped
@@ -183,7 +189,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ring slots and barrier phases count f.
   const int t0 = causal ? j0 / BQ : 0;
   const int Tq = max(0, (Nq + BQ - 1) / BQ - t0);
-  const int T = G * Tq;
+  const int T = Gs * Tq;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -381,8 +387,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
+    if (S > 1) {
+      // Stage this CTA's partial d~K | d~V rows (every MMA is done and the
+      // ring is idle) for the cluster-wide sum below.
+      float* row = reinterpret_cast<float*>(&sm.st[0][0][0]) + r * kStageStride;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 2; ++h) {
+        const int col = 32 * wg + 16 * h;
+        uint32_t vk[16], vv[16];
+        tmem_ld16(acc_base + kAccK + col, vk);
+        tmem_ld16(acc_base + kAccV + col, vv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          reinterpret_cast<float4*>(row + col)[k] =
+              make_float4(u2f(vk[4 * k]), u2f(vk[4 * k + 1]), u2f(vk[4 * k + 2]),
+                          u2f(vk[4 * k + 3]));
+          reinterpret_cast<float4*>(row + DH + col)[k] =
+              make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
+                          u2f(vv[4 * k + 3]));
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2 && S == 1; ++h) {
       const int col = 32 * wg + 16 * h;
       uint32_t vk[16], vv[16];
       tmem_ld16(acc_base + kAccK + col, vk);
@@ -409,6 +437,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  if (S > 1) {
+    // Cluster rank q sums key rows [128 q / S, 128 (q + 1) / S) of the block
+    // over the S CTAs' staged partials and writes them: one write per
+    // element, no atomics.  All threads pass both cluster barriers; the
+    // second keeps every CTA's staged rows alive until all reads are done.
+    cluster_sync();
+    if (warp >= 2) {
+      const uint32_t q = cluster_ctarank();
+      const int rb = (BM * (int)q) / S, re = (BM * ((int)q + 1)) / S;
+      const uint32_t stage = smem_u32(&sm.st[0][0][0]);
+      const int tid = threadIdx.x - 64;
+      for (int e = tid; e < (re - rb) * 32; e += 256) {
+        const int rr = rb + e / 32, c4 = e % 32;  // row, float4 column of d~K | d~V
+        const uint32_t off = static_cast<uint32_t>((rr * kStageStride + 4 * c4) * 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < S; ++p) {
+          const float4 v = ld_shared_cluster_f4(mapa_shared(stage + off, p));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        const int gjr = j0 + rr;
+        if (gjr < Nk && !*abort_flag) {
+          if (T == 0) acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          const bool isK = c4 < DH / 4;
+          const size_t o = (static_cast<size_t>(bkv) * Nk + gjr) * DH + 4 * (isK ? c4 : c4 - DH / 4);
+          if (isK)
+            *reinterpret_cast<float4*>(dKt + o) =
+                make_float4(tau * acc.x, tau * acc.y, tau * acc.z, tau * acc.w);
+          else
+            *reinterpret_cast<float4*>(dVt + o) = acc;
+        }
+      }
+    }
+    cluster_sync();
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -429,12 +495,42 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Nk + BM - 1) / BM, a.Hkv, a.B);  // one CTA per key block of a shared head
-  tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L, a.D,
-      a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
-      a.causal ? 1 : 0, a.err);
-  return cudaGetLastError();
+  // One CTA per key block of a shared head; when those cannot fill the SMs,
+  // split each group's query heads over a cluster of S CTAs (S divides
+  // H / Hkv, at most 8, the largest that still fits one wave).
+  const int blocks = ((a.Nk + BM - 1) / BM) * a.Hkv * a.B;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int G = a.H / a.Hkv;
+  int S = 1;
+  for (int s = 2; s <= 8; ++s)
+    if (G % s == 0 && blocks * s <= sms) S = s;
+  dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
+  if (S == 1) {
+    tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+        maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L,
+        a.D, a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, 1,
+        a.err);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_pass2_kernel, maps128[0], maps128[1], maps128[2],
+                            maps128[3], maps64[0], maps64[1], maps64[2], a.L, a.D, a.alpha, a.E,
+                            a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, S,
+                            a.err);
 }
 
 }  // namespace flashbob
