@@ -75,6 +75,9 @@ size_t tc_pass1_smem();
 size_t tc_pass2_smem();
 size_t tc_pass1_d128_smem();
 size_t tc_pass2_d128_smem();
+// Pass 2 cluster split: how many CTAs share a key block (S divides the
+// group size, S <= 8, blocks * S fits one wave of the device's SMs).
+cudaError_t tc_group_split(int blocks, int group, int* S);
 
 // Device error word (one per device): a kernel writes a nonzero code when a
 // bounded wait gives up.  Codes: 1 = mbarrier wait timed out.

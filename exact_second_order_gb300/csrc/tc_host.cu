@@ -18,6 +18,17 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
+cudaError_t tc_group_split(int blocks, int group, int* S) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  *S = 1;
+  for (int s = 2; s <= 8; ++s)
+    if (group % s == 0 && blocks * s <= sms) *S = s;
+  return cudaSuccess;
+}
+
 namespace {
 
 // Head dim 128: both passes stream 32-row tiles against 128-row blocks.

@@ -498,15 +498,9 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   // One CTA per key block of a shared head; when those cannot fill the SMs,
   // split each group's query heads over a cluster of S CTAs (S divides
   // H / Hkv, at most 8, the largest that still fits one wave).
-  const int blocks = ((a.Nk + BM - 1) / BM) * a.Hkv * a.B;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const int G = a.H / a.Hkv;
   int S = 1;
-  for (int s = 2; s <= 8; ++s)
-    if (G % s == 0 && blocks * s <= sms) S = s;
+  e = tc_group_split(((a.Nk + BM - 1) / BM) * a.Hkv * a.B, a.H / a.Hkv, &S);
+  if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {
     tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(

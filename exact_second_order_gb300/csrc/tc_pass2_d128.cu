@@ -65,6 +65,10 @@ constexpr uint32_t kSc = 256;
 constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;  // inside the score buffer
 constexpr uint32_t kOp = 384;  // operand x, K step kk at kOp + 16 x + 8 kk
 constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
+// Cluster split: staged partial rows d~K | d~V (64 float4 each) fill the
+// 128 KiB of the resident block exactly; float4 c of row r sits at
+// c ^ (r mod 8) against bank conflicts.
+static_assert(BM * 2 * DH * 4 <= 4 * 2 * HALF_BLOCK, "staging fits in the resident block");
 
 __device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
   return kOp + 16 * x + 8 * kk;
@@ -132,21 +136,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          const float* __restrict__ D, const float* __restrict__ alpha,
                          const float* __restrict__ E, float* __restrict__ dKt,
                          float* __restrict__ dVt, int H, int Hkv, int Nq, int Nk, float tau,
-                         int causal, unsigned int* err) {
+                         int causal, int S, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   SmemW2& sm = *reinterpret_cast<SmemW2*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = H / Hkv;
-  const int bkv = blockIdx.z * Hkv + blockIdx.y;
-  const int hq0 = blockIdx.z * H + blockIdx.y * G;  // first query head of the group
+  // A cluster of S CTAs (blockIdx.y = S * head + rank) may share a key
+  // block, each streaming G / S of the group's heads; the partial sums meet
+  // in distributed shared memory before the one write (see the end).
+  const int G = H / Hkv, Gs = G / S;
+  const int bkv = blockIdx.z * Hkv + blockIdx.y / S;
+  const int hq0 = blockIdx.z * H + (blockIdx.y / S) * G + (blockIdx.y % S) * Gs;  // first head
   const int j0 = blockIdx.x * BM;
   // Query tiles t0 .. stream past (causal: key j is seen only by queries
   // i >= j; none when j0 >= Nq, and then T = 0 and the outputs are 0).
   // f = (query head in group) * Tq + (tile - t0) numbers the streamed tiles.
   const int t0 = causal ? j0 / BQ : 0;
   const int Tq = max(0, (Nq + BQ - 1) / BQ - t0);
-  const int T = G * Tq;
+  const int T = Gs * Tq;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -352,8 +359,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
+    if (S > 1) {
+      // Stage this CTA's partial rows (every MMA is done; the resident
+      // block is no longer read) for the cluster-wide sum below.
+      float4* row = reinterpret_cast<float4*>(&sm.kb[0][0][0]) + r * (2 * DH / 4);
 #pragma unroll 1
-    for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < 4; ++h) {
+        const int col = 64 * wg + 16 * h;
+        uint32_t vk[16], vv[16];
+        tmem_ld16(acc_base + kAccK + col, vk);
+        tmem_ld16(acc_base + kAccV + col, vv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ck = col / 4 + k, cv = DH / 4 + col / 4 + k;
+          row[ck ^ (r & 7)] = make_float4(u2f(vk[4 * k]), u2f(vk[4 * k + 1]),
+                                          u2f(vk[4 * k + 2]), u2f(vk[4 * k + 3]));
+          row[cv ^ (r & 7)] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]),
+                                          u2f(vv[4 * k + 2]), u2f(vv[4 * k + 3]));
+        }
+      }
+    }
+#pragma unroll 1
+    for (int h = 0; h < 4 && S == 1; ++h) {
       const int col = 64 * wg + 16 * h;
       uint32_t vk[16], vv[16];
       tmem_ld16(acc_base + kAccK + col, vk);
@@ -380,6 +408,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  if (S > 1) {
+    // Cluster rank q sums key rows [128 q / S, 128 (q + 1) / S) over the S
+    // CTAs' staged partials and writes them once.  All threads pass both
+    // cluster barriers; the second keeps every staged row alive until all
+    // reads are done.
+    cluster_sync();
+    if (warp >= 2) {
+      const uint32_t q = cluster_ctarank();
+      const int rb = (BM * (int)q) / S, re = (BM * ((int)q + 1)) / S;
+      const uint32_t stage = smem_u32(&sm.kb[0][0][0]);
+      const int tid = threadIdx.x - 64;
+      constexpr int kRow4 = 2 * DH / 4;  // float4 per staged row
+      for (int e = tid; e < (re - rb) * kRow4; e += 256) {
+        const int rr = rb + e / kRow4, c4 = e % kRow4;
+        const uint32_t off = static_cast<uint32_t>((rr * kRow4 + (c4 ^ (rr & 7))) * 16);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < S; ++p) {
+          const float4 v = ld_shared_cluster_f4(mapa_shared(stage + off, p));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        const int gjr = j0 + rr;
+        if (gjr < Nk && !*abort_flag) {
+          if (T == 0) acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          const bool isK = c4 < DH / 4;
+          const size_t o =
+              (static_cast<size_t>(bkv) * Nk + gjr) * DH + 4 * (isK ? c4 : c4 - DH / 4);
+          if (isK)
+            *reinterpret_cast<float4*>(dKt + o) =
+                make_float4(tau * acc.x, tau * acc.y, tau * acc.z, tau * acc.w);
+          else
+            *reinterpret_cast<float4*>(dVt + o) = acc;
+        }
+      }
+    }
+    cluster_sync();
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -401,11 +469,35 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_d128_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Nk + BM - 1) / BM, a.Hkv, a.B);  // one CTA per key block of a shared head
-  tc_pass2_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D,
-      a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
-  return cudaGetLastError();
+  // One CTA per key block of a shared head, or a cluster of S of them (the
+  // group's query heads split S ways) when the blocks cannot fill the SMs.
+  int S = 1;
+  e = tc_group_split(((a.Nk + BM - 1) / BM) * a.Hkv * a.B, a.H / a.Hkv, &S);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
+  if (S == 1) {
+    tc_pass2_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+        maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L,
+        a.D, a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, 1,
+        a.err);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_pass2_d128_kernel, maps128[0], maps128[1], maps128[2],
+                            maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D, a.alpha,
+                            a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0,
+                            S, a.err);
 }
 
 }  // namespace flashbob

@@ -170,7 +170,9 @@ def test_causal_pages_shape_sampled_rows():
 # Grouped-query / multi-query attention (shared key/value heads)
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("H,Hkv", [(4, 2), (4, 1), (6, 3)])
+# Small grids split each group over a cluster of S CTAs (S = 2, 4, 2, 3, 8
+# for these head counts), so these shapes also cover the cluster-wide sum.
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (4, 1), (6, 3), (6, 2), (8, 1)])
 @pytest.mark.parametrize("N", [1, 65, 300])
 @pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96), ("bf16", 128)])
 def test_gqa_small_shapes(H, Hkv, N, dtype, d):
