@@ -15,8 +15,9 @@
 // from global memory) dotted with the fp32 O.
 //
 // 320 threads: warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps 2-5
-// and 6-9 elementwise warpgroups on alternate tiles.  TMEM: [0,64) O,
-// [64,96) and [96,128) score buffers.
+// and 6-9 elementwise warpgroups on alternate tiles.  TMEM: [0,DH) O,
+// [DH,DH+32) and [DH+32,DH+64) score buffers.  Head dim 64 or 128: a row of
+// 128 columns is two 64-column boxes in the 128-byte swizzle.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -26,17 +27,25 @@ using namespace tc;
 
 constexpr int BM = kTcRows;
 constexpr int BN = kTcStream;
-constexpr int DH = 64;
-constexpr int NST = 6;
 constexpr int NTHREADS = 320;
-constexpr uint32_t BLOCK_BYTES = BM * DH * 2;
-constexpr uint32_t TILE_BYTES = BN * DH * 2;
+constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 128 rows x 64 columns bf16
+constexpr uint32_t HALF_TILE = BN * 64 * 2;   // 32 rows x 64 columns bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+template <int DH>
+struct PrepCfg {
+  static constexpr int kHalves = DH / 64;
+  static constexpr int kStages = DH == 64 ? 6 : 4;
+  static constexpr uint32_t kTmemCols = DH == 64 ? 128 : 256;  // O + two 32-column buffers
+};
+
+template <int DH>
 struct Smem0 {
-  alignas(1024) uint8_t q[BLOCK_BYTES];
-  alignas(1024) uint8_t kv[NST][2][TILE_BYTES];  // K, V
+  static constexpr int NST = PrepCfg<DH>::kStages;
+  static constexpr int NH = PrepCfg<DH>::kHalves;
+  alignas(1024) uint8_t q[NH][HALF_BLOCK];
+  alignas(1024) uint8_t kv[NST][2][NH][HALF_TILE];  // [stage][K, V][half]
   float part_m[2][BM];
   float part_l[2][BM];
   float part_d[2][BM];
@@ -50,14 +59,17 @@ struct Smem0 {
   int abort_flag;
 };
 
+template <int DH>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __nv_bfloat16* __restrict__ dO,
                    float* __restrict__ O, float* __restrict__ L, float* __restrict__ D, int H,
                    int Hkv, int Nq, int Nk, float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
-  Smem0& sm = *reinterpret_cast<Smem0*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~static_cast<uintptr_t>(1023));
+  constexpr int NST = PrepCfg<DH>::kStages;
+  constexpr int NH = PrepCfg<DH>::kHalves;
+  Smem0<DH>& sm = *reinterpret_cast<Smem0<DH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * H + blockIdx.y;
   const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);  // shared key/value head
@@ -81,7 +93,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     sm.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&sm.tmem_base, 128);
+  if (warp == 1) tmem_alloc(&sm.tmem_base, PrepCfg<DH>::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -91,17 +103,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
-      mbar_expect_tx(&sm.bar_q, BLOCK_BYTES);
-      tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
+      mbar_expect_tx(&sm.bar_q, NH * HALF_BLOCK);
+      for (int h = 0; h < NH; ++h) tma_load_3d(sm.q[h], &mQ, &sm.bar_q, 64 * h, row0, bh);
       int issued = 0;
       for (int t = 0; t < T2; ++t) {
         const int s = t % NST;
         const bool phase_b = t >= T;
         const int kt = phase_b ? t - T : t;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
-        mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * TILE_BYTES);
-        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, kt * BN, bkv);
-        if (phase_b) tma_load_3d(sm.kv[s][1], &mV, &sm.kv_full[s], 0, kt * BN, bkv);
+        mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * NH * HALF_TILE);
+        for (int h = 0; h < NH; ++h) {
+          tma_load_3d(sm.kv[s][0][h], &mK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+          if (phase_b) tma_load_3d(sm.kv[s][1][h], &mV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+        }
         issued = t + 1;
       }
       drain_wait(&sm.bar_q, 0);
@@ -112,28 +126,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     {  // MMA issuer: whole warp, one elected lane issues
       constexpr uint32_t idS = idesc_bf16(BM, BN, false);
       constexpr uint32_t idO = idesc_bf16(BM, DH, true);
-      const uint32_t aq = smem_u32(sm.q);
       auto issue_scores = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + 64 + 32 * (t & 1);
-        const uint32_t bk = smem_u32(sm.kv[s][0]);
+        const uint32_t sc = tbase + DH + 32 * (t & 1);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t o = 32 * kk;
-          if (elect_one()) mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
-                 kk > 0);
+          const int h = kk >> 2;  // 64-column half of the head dim
+          const uint32_t o = 32 * (kk & 3);
+          const uint32_t aq = smem_u32(sm.q[h]), bk = smem_u32(sm.kv[s][0][h]);
+          if (elect_one())
+            mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
+                   kk > 0);
         }
         if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
         if (t < T && elect_one()) mma_commit(&sm.kv_empty[s]);  // phase A reads the stage only here
       };
       auto issue_pv = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + 64 + 32 * (t & 1);
-        const uint32_t bv = smem_u32(sm.kv[s][1]);
+        const uint32_t sc = tbase + DH + 32 * (t & 1);
+        // V as an N = DH MN-major operand: its second 64-column half (d = 128)
+        // sits HALF_TILE bytes after the first.
+        const uint32_t bv = smem_u32(sm.kv[s][1][0]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          if (elect_one()) mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, 16, 1024), idO,
-                 (t > T || c > 0));
+          if (elect_one())
+            mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HALF_TILE, 1024), idO,
+                   (t > T || c > 0));
         }
         if (elect_one()) mma_commit(&sm.kv_empty[s]);
       };
@@ -166,7 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int gr = row0 + r;
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
-    const uint32_t sc = tbase + lane_off + 64 + 32 * wg;
+    const uint32_t sc = tbase + lane_off + DH + 32 * wg;
     float m = -INFINITY, l = 0.f, L2 = 0.f;
     bool ok = true, have_L = false;
     // Both warpgroups have finished phase A: combine their (m, l) into L.
@@ -235,8 +253,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     float dpart = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = 32 * wg + 16 * h;
+    for (int h = 0; h < DH / 32; ++h) {  // warpgroup wg writes columns [DH/2 wg, DH/2 (wg+1))
+      const int col = (DH / 2) * wg + 16 * h;
       uint32_t vo[16];
       tmem_ld16(tbase + lane_off + col, vo);
       tmem_wait_ld();
@@ -276,30 +294,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, 128);
+    tmem_dealloc(tbase, PrepCfg<DH>::kTmemCols);
   }
+}
+
+template <int DH>
+cudaError_t launch_prep(const PrepArgs& a) {
+  const int BH = a.B * a.H;
+  const int BHkv = a.B * a.Hkv;
+  CUtensorMap mq, mk, mv;
+  cudaError_t e = tc::make_map_bf16(&mq, a.Q, BH, a.Nq, kTcRows, DH);
+  if (e == cudaSuccess) e = tc::make_map_bf16(&mk, a.K, BHkv, a.Nk, kTcStream, DH);
+  if (e == cudaSuccess) e = tc::make_map_bf16(&mv, a.V, BHkv, a.Nk, kTcStream, DH);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(Smem0<DH>) + 1024;
+  e = cudaFuncSetAttribute(tc_prep_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
+  tc_prep_kernel<DH><<<grid, NTHREADS, smem, a.stream>>>(
+      mq, mk, mv, (const __nv_bfloat16*)a.dO, a.O, a.L, a.D, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
+      a.causal ? 1 : 0, a.err);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-bool tc_prep_supported(const PrepArgs& a) { return a.bf16 && a.d == 64; }
+bool tc_prep_supported(const PrepArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
 cudaError_t tc_prep(const PrepArgs& a) {
-  const int BH = a.B * a.H;
-  const int BHkv = a.B * a.Hkv;
-  CUtensorMap mq, mk, mv;
-  cudaError_t e = tc::make_map_bf16_d64(&mq, a.Q, BH, a.Nq, kTcRows);
-  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mk, a.K, BHkv, a.Nk, kTcStream);
-  if (e == cudaSuccess) e = tc::make_map_bf16_d64(&mv, a.V, BHkv, a.Nk, kTcStream);
-  if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(Smem0) + 1024;
-  e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_prep_kernel<<<grid, NTHREADS, smem, a.stream>>>(mq, mk, mv, (const __nv_bfloat16*)a.dO, a.O,
-                                                     a.L, a.D, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
-                                                     a.causal ? 1 : 0, a.err);
-  return cudaGetLastError();
+  return a.d == 128 ? launch_prep<128>(a) : launch_prep<64>(a);
 }
 
 }  // namespace flashbob
