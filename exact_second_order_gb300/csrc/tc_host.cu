@@ -15,6 +15,8 @@ cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
                                  const CUtensorMap* maps32);
 cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
                                  const CUtensorMap* maps32);
+cudaError_t tc_launch_jvp_d128(const JvpArgs& a, const CUtensorMap* maps128,
+                               const CUtensorMap* maps32);
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
@@ -93,7 +95,7 @@ cudaError_t tc_bob(const BobArgs& a) {
   return e;
 }
 
-bool tc_jvp_supported(const JvpArgs& a) { return a.bf16 && a.d == 64; }
+bool tc_jvp_supported(const JvpArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
 cudaError_t tc_jvp(const JvpArgs& a) {
   CUtensorMap m128[2], m32[4];
@@ -101,11 +103,11 @@ cudaError_t tc_jvp(const JvpArgs& a) {
   const void* cols[4] = {a.K, a.V, a.UK, a.UV};
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < 2 && e == cudaSuccess; ++i)
-    e = tc::make_map_bf16_d64(&m128[i], rows[i], a.B * a.H, a.Nq, kTcRows);
+    e = tc::make_map_bf16(&m128[i], rows[i], a.B * a.H, a.Nq, kTcRows, a.d);
   for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-    e = tc::make_map_bf16_d64(&m32[i], cols[i], a.B * a.Hkv, a.Nk, kTcStream);
+    e = tc::make_map_bf16(&m32[i], cols[i], a.B * a.Hkv, a.Nk, kTcStream, a.d);
   if (e != cudaSuccess) return e;
-  return tc_launch_jvp(a, m128, m32);
+  return a.d == 128 ? tc_launch_jvp_d128(a, m128, m32) : tc_launch_jvp(a, m128, m32);
 }
 
 }  // namespace flashbob

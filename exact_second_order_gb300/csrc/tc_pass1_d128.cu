@@ -28,6 +28,11 @@
 // in phase B a warpgroup reads a buffer one 16-column chunk at a time and
 // overwrites the columns of that chunk with its bf16 A operands d~S, dS, P,
 // W of the output GEMMs.
+//
+// Instantiated with JVP = true the kernel computes the attention JVP along
+// (U_Q, U_K, U_V) instead (no dO): one pass over the key tiles with S and F'
+// only, operands P and P o F, O'0 = P U_V + (P o F) V in the d~dO
+// accumulator, and O' = O'0 - L' O, L' = alpha in the epilogue.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -101,6 +106,32 @@ __device__ __forceinline__ void phase_a_sums(const Chunk& x, int jbase, int jmax
   }
 }
 
+// The JVP's chunk: P and P o F (into the P and W slots) and the row sum
+// alpha = L' (no dO: dP = G = 0).
+template <bool MASKED, int C>
+__device__ __forceinline__ void jvp_chunk(uint32_t sc, const uint32_t (&s)[16],
+                                          const uint32_t (&f)[16], int col0, int jmax, float c1,
+                                          float Lr2, float tau, float& a_acc) {
+  uint32_t op[8], opf[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float vp[2], vpf[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = e + h;
+      float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
+      if (MASKED && col0 + 16 * C + j > jmax) p = 0.f;
+      vp[h] = p;
+      vpf[h] = p * (u2f(f[j]) * tau);
+      a_acc += vpf[h];
+    }
+    op[e >> 1] = pack_bf16x2(vp[0], vp[1]);
+    opf[e >> 1] = pack_bf16x2(vpf[0], vpf[1]);
+  }
+  tmem_st8(sc + slot_P(C), op);
+  tmem_st8(sc + slot_W(C), opf);
+}
+
 // Phase B on one 16-column chunk: the four bf16 A operands, written to TMEM.
 template <bool MASKED, int C>
 __device__ __forceinline__ void phase_b_chunk(uint32_t sc, const Chunk& x, int col0, int jmax,
@@ -135,6 +166,7 @@ __device__ __forceinline__ void phase_b_chunk(uint32_t sc, const Chunk& x, int c
   tmem_st8(sc + slot_W(C), ow);
 }
 
+template <bool JVP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_d128_kernel(const __grid_constant__ CUtensorMap mQ,
                          const __grid_constant__ CUtensorMap mdO,
@@ -156,7 +188,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
   const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
   const int T = (col_end + BN - 1) / BN;  // key tiles per phase
-  const int T2 = 2 * T;                   // phase A tiles 0..T-1, phase B tiles T..2T-1
+  // Phase A tiles 0..T-1, phase B tiles T..2T-1; the JVP has phase B only.
+  const int TB = JVP ? 0 : T;  // first phase-B tile
+  const int T2 = TB + T;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -186,16 +220,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mUK);
       tma_prefetch_desc(&mUV);
-      mbar_expect_tx(&sm.bar_q, 6 * HALF_BLOCK);
+      mbar_expect_tx(&sm.bar_q, (JVP ? 4 : 6) * HALF_BLOCK);
       for (int h = 0; h < 2; ++h) {
         tma_load_3d(sm.q[h], &mQ, &sm.bar_q, 64 * h, row0, bh);
-        tma_load_3d(sm.dO[h], &mdO, &sm.bar_q, 64 * h, row0, bh);
+        if (!JVP) tma_load_3d(sm.dO[h], &mdO, &sm.bar_q, 64 * h, row0, bh);
         tma_load_3d(sm.uq[h], &mUQ, &sm.bar_q, 64 * h, row0, bh);
       }
       int issued = 0;
       for (int t = 0; t < T2; ++t) {
         const int s = t % NST;
-        const int kt = t < T ? t : t - T;
+        const int kt = t < TB ? t : t - TB;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.kv_full[s], STAGE_BYTES);
         for (int h = 0; h < 2; ++h) {
@@ -243,7 +277,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t acc = kk > 0;
           mma_ss(sc + kColS, dq[h] + o, dK[h] + so + o, idS64, acc);    // [S | F'] = Q [K; U_K]^T
           mma_ss(sc + kColF, duq[h] + o, dK[h] + so + o, idS32, 1);     // F' += U_Q K^T
-          mma_ss(sc + kColdP, ddo[h] + o, dV[h] + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
+          if (!JVP) mma_ss(sc + kColdP, ddo[h] + o, dV[h] + so + o, idS64, acc);  // [dP | G]
         }
         mma_commit(&sm.sc_full[t & 1]);
       }
@@ -254,15 +288,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
       const uint32_t sc = tbase + 256 + 128 * (t & 1);
       if (elect_one()) {
-        if (t >= T) {
+        if (t >= TB) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
-            const uint32_t acc = (t > T || c > 0);
-            mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
-            mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //     +  dS U_K
+            const uint32_t acc = (t > TB || c > 0);
+            if (!JVP) {
+              mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
+              mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //  + dS U_K
+            }
             mma_ts(tbase + kAccdO, sc + slot_P(c), dUVmn + so + o, idO128, acc);  // d~dO += P U_V
-            mma_ts(tbase + kAccdO, sc + slot_W(c), dVmn + so + o, idO128, 1);     //      +  W V
+            mma_ts(tbase + kAccdO, sc + slot_W(c), dVmn + so + o, idO128, 1);     //  + W V (P o F V)
           }
         }
         mma_commit(&sm.kv_empty[s]);
@@ -300,7 +336,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
-    const float Dr = gr < Nq ? D[rowvec] : 0.f;
+    const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
     float a_acc = 0.f, e_acc = 0.f, al = 0.f, Ei = 0.f;
     bool ok = true, have_ae = false;
     const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
@@ -318,14 +354,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
       if (t >= T2) break;
-      const bool phase_b = t >= T;
-      if (phase_b && !have_ae) combine();
+      const bool phase_b = t >= TB;
+      if (!JVP && phase_b && !have_ae) combine();
       // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
       // failed wait keep looping so both warpgroups reach the named barrier.
       ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
       if (!ok) continue;
       tc_fence_after();
-      const int col0 = (phase_b ? t - T : t) * BN;
+      const int col0 = (phase_b ? t - TB : t) * BN;
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (!phase_b) {
@@ -342,6 +378,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           phase_a_sums<false>(x0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
           phase_a_sums<false>(x1, col0 + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
         }
+      } else if (JVP) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[16], fv[16];
+          tmem_ld16(sc + kColS + 16 * c, sv);
+          tmem_ld16(sc + kColF + 16 * c, fv);
+          tmem_wait_ld();
+          if (c == 0) {
+            if (masked) jvp_chunk<true, 0>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
+            else jvp_chunk<false, 0>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
+          } else {
+            if (masked) jvp_chunk<true, 1>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
+            else jvp_chunk<false, 1>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&sm.op_ready[wg]);
       } else {
         {
           Chunk x;
@@ -366,7 +420,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         warp_arrive(&sm.op_ready[wg]);
       }
     }
-    if (!have_ae) combine();  // a warpgroup with no phase-B tile (T = 1)
+    if (!have_ae) combine();  // a warpgroup with no phase-B tile (T = 1), or the JVP
 
     // Epilogue: warpgroup wg writes output columns [64 wg, 64 wg + 64).
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
@@ -377,10 +431,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int h = 0; h < 4; ++h) {
       const int col = 64 * wg + 16 * h;
       uint32_t vq[16], vo[16];
-      tmem_ld16(acc_base + kAccQ + col, vq);
+      if (!JVP) tmem_ld16(acc_base + kAccQ + col, vq);
       tmem_ld16(acc_base + kAccdO + col, vo);
       tmem_wait_ld();
-      if (ok && gr < Nq) {
+      if (JVP && ok && gr < Nq) {  // O' = O'0 - L' O
+        const size_t off = rowvec * DH + col;
+        const float4* o4 = reinterpret_cast<const float4*>(O + off);
+        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 ov = o4[k];
+          d4[k] = make_float4(u2f(vo[4 * k]) - al * ov.x, u2f(vo[4 * k + 1]) - al * ov.y,
+                              u2f(vo[4 * k + 2]) - al * ov.z, u2f(vo[4 * k + 3]) - al * ov.w);
+        }
+      }
+      if (!JVP && ok && gr < Nq) {
         const size_t off = rowvec * DH + col;
         float4* q4 = reinterpret_cast<float4*>(dQt + off);
         float4* d4 = reinterpret_cast<float4*>(ddOt + off);
@@ -395,7 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (ok && wg == 0 && gr < Nq) {
       alpha[rowvec] = al;
-      E[rowvec] = Ei;
+      if (!JVP) E[rowvec] = Ei;
     }
   }
 
@@ -417,13 +482,33 @@ cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
   // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
   // boxes; every box is 64 columns wide (one half of a 128-column row).
   const size_t smem = tc_pass1_d128_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass1_d128_kernel,
+  cudaError_t e = cudaFuncSetAttribute(tc_pass1_d128_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+  tc_pass1_d128_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
       a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace flashbob
+
+namespace flashbob {
+
+cudaError_t tc_launch_jvp_d128(const JvpArgs& a, const CUtensorMap* maps128,
+                               const CUtensorMap* maps32) {
+  // maps128: Q, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
+  // boxes (64-column halves).
+  const size_t smem = tc_pass1_d128_smem();
+  cudaError_t e = cudaFuncSetAttribute(tc_pass1_d128_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
+  tc_pass1_d128_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[0], maps128[1], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
+      nullptr, nullptr, a.Od, a.Ld, nullptr, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0,
+      a.err);
   return cudaGetLastError();
 }
 

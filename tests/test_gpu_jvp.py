@@ -48,7 +48,7 @@ def _full_errors(w, x, O, L, Od, Ld):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,Nk,H,Hkv", [(1, 1, 2, 2), (129, 129, 2, 2), (300, 77, 4, 2),
                                         (65, 300, 3, 1), (1000, 1000, 1, 1)])
-@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96), ("bf16", 128)])
 def test_jvp_small_shapes_full_oracle(N, Nk, H, Hkv, dtype, d, causal):
     w = wl.small_workload(1, H, N, d, dtype, seed=N + Nk + H, Hkv=Hkv, Nk=Nk, causal=causal)
     x, dev, O, L, Od, Ld = _run_jvp(w)
@@ -68,7 +68,9 @@ def test_forward_only_prep_matches_full_prep():
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
 
 
-@pytest.mark.parametrize("w", [wl.MID_LENGTH, wl.GQA_N8192, wl.RECT_Q4096_K16384],
+@pytest.mark.parametrize("w", [wl.MID_LENGTH, wl.GQA_N8192, wl.RECT_Q4096_K16384,
+                               wl.Workload("jvp_B1_H4_N8192_d128", 1, 4, 8192, 128, "bf16",
+                                           causal=True)],
                          ids=lambda w: w.name)
 def test_jvp_workloads_sampled_rows(w):
     """Rows of O' and L' against the row form of the oracle (its alpha and
