@@ -159,6 +159,8 @@ __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const
   return true;
 }
 
+// SPLIT: launched as clusters of S > 1 CTAs that share a key block.
+template <bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mUK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mUV,
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
-    if (S > 1) {
+    if (SPLIT) {
       // Stage this CTA's partial d~K | d~V rows (every MMA is done and the
       // ring is idle) for the cluster-wide sum below.
       float* row = reinterpret_cast<float*>(&sm.st[0][0][0]) + r * kStageStride;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
 #pragma unroll
-    for (int h = 0; h < 2 && S == 1; ++h) {
+    for (int h = 0; h < 2 && !SPLIT; ++h) {
       const int col = 32 * wg + 16 * h;
       uint32_t vk[16], vv[16];
       tmem_ld16(acc_base + kAccK + col, vk);
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
-  if (S > 1) {
+  if (SPLIT) {
     // Cluster rank q sums key rows [128 q / S, 128 (q + 1) / S) of the block
     // over the S CTAs' staged partials and writes them: one write per
     // element, no atomics.  All threads pass both cluster barriers; the
@@ -492,8 +494,8 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps64) {
   // maps128: K, U_K, V, U_V with 128-row boxes; maps64: Q, U_Q, dO with 64-row boxes.
   const size_t smem = tc_pass2_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // One CTA per key block of a shared head; when those cannot fill the SMs,
   // split each group's query heads over a cluster of S CTAs (S divides
@@ -503,12 +505,15 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {
-    tc_pass2_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+    tc_pass2_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
         maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L,
         a.D, a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, 1,
         a.err);
     return cudaGetLastError();
   }
+  e = cudaFuncSetAttribute(tc_pass2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHREADS);
@@ -521,7 +526,7 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_pass2_kernel, maps128[0], maps128[1], maps128[2],
+  return cudaLaunchKernelEx(&cfg, tc_pass2_kernel<true>, maps128[0], maps128[1], maps128[2],
                             maps128[3], maps64[0], maps64[1], maps64[2], a.L, a.D, a.alpha, a.E,
                             a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, S,
                             a.err);

@@ -125,6 +125,8 @@ __device__ __forceinline__ bool p2w_half(uint32_t sc, uint32_t opb, int wg, cons
   return true;
 }
 
+// SPLIT: launched as clusters of S > 1 CTAs that share a key block.
+template <bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_d128_kernel(const __grid_constant__ CUtensorMap mK,
                          const __grid_constant__ CUtensorMap mUK,
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
-    if (S > 1) {
+    if (SPLIT) {
       // Stage this CTA's partial rows (every MMA is done; the resident
       // block is no longer read) for the cluster-wide sum below.
       float4* row = reinterpret_cast<float4*>(&sm.kb[0][0][0]) + r * (2 * DH / 4);
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
 #pragma unroll 1
-    for (int h = 0; h < 4 && S == 1; ++h) {
+    for (int h = 0; h < 4 && !SPLIT; ++h) {
       const int col = 64 * wg + 16 * h;
       uint32_t vk[16], vv[16];
       tmem_ld16(acc_base + kAccK + col, vk);
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
-  if (S > 1) {
+  if (SPLIT) {
     // Cluster rank q sums key rows [128 q / S, 128 (q + 1) / S) over the S
     // CTAs' staged partials and writes them once.  All threads pass both
     // cluster barriers; the second keeps every staged row alive until all
@@ -466,7 +468,7 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
   // maps128: K, U_K, V, U_V with 128-row boxes; maps32: Q, U_Q, dO with
   // 32-row boxes; every box is 64 columns wide.
   const size_t smem = tc_pass2_d128_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass2_d128_kernel,
+  cudaError_t e = cudaFuncSetAttribute(tc_pass2_d128_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // One CTA per key block of a shared head, or a cluster of S of them (the
@@ -476,12 +478,15 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {
-    tc_pass2_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+    tc_pass2_d128_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
         maps128[0], maps128[1], maps128[2], maps128[3], maps32[0], maps32[1], maps32[2], a.L,
         a.D, a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, 1,
         a.err);
     return cudaGetLastError();
   }
+  e = cudaFuncSetAttribute(tc_pass2_d128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHREADS);
@@ -494,7 +499,7 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_pass2_d128_kernel, maps128[0], maps128[1], maps128[2],
+  return cudaLaunchKernelEx(&cfg, tc_pass2_d128_kernel<true>, maps128[0], maps128[1], maps128[2],
                             maps128[3], maps32[0], maps32[1], maps32[2], a.L, a.D, a.alpha,
                             a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0,
                             S, a.err);
