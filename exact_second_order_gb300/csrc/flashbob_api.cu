@@ -282,6 +282,13 @@ flashbob_status flashbob_attention_jvp(const void* Q, const void* K, const void*
   return e == cudaSuccess ? FLASHBOB_OK : FLASHBOB_ERR_CUDA;
 }
 
+flashbob_status flashbob_check_wait_timeout(void* stream) {
+  unsigned int* err = nullptr;
+  if (error_word_ptr(&err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  return launch_wait_timeout((cudaStream_t)stream, err) == cudaSuccess ? FLASHBOB_OK
+                                                                       : FLASHBOB_ERR_CUDA;
+}
+
 flashbob_status flashbob_last_device_error(void) {
   unsigned int* p = nullptr;
   if (error_word_ptr(&p) != cudaSuccess) return FLASHBOB_ERR_CUDA;

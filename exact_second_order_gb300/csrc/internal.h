@@ -82,5 +82,7 @@ cudaError_t tc_group_split(int blocks, int group, int* S);
 // Device error word (one per device): a kernel writes a nonzero code when a
 // bounded wait gives up.  Codes: 1 = mbarrier wait timed out.
 cudaError_t error_word_ptr(unsigned int** ptr);
+// One CTA whose bounded wait runs out (the timeout report, tested on a GPU).
+cudaError_t launch_wait_timeout(cudaStream_t stream, unsigned int* err);
 
 }  // namespace flashbob

@@ -35,6 +35,7 @@ _SIGNATURES = {
     "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
+    "flashbob_check_wait_timeout": ([_P], _I),
     "flashbob_status_string": ([_I], ctypes.c_char_p),
 }
 
@@ -161,6 +162,13 @@ def flashbob_bob_tile_sizes(d: int, in_dtype: int) -> dict:
         raise FlashbobError(st, "flashbob_bob_tile_sizes")
     return {"Br1": v[0].value, "Bc1": v[1].value, "Br2": v[2].value, "Bc2": v[3].value,
             "smem_bytes_pass1": s[0].value, "smem_bytes_pass2": s[1].value}
+
+
+def flashbob_check_wait_timeout(stream=None) -> None:
+    """Launch the diagnostic whose bounded wait runs out (see the header)."""
+    st = load_library().flashbob_check_wait_timeout(_stream_handle(stream))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_check_wait_timeout")
 
 
 def flashbob_last_device_error() -> int:

@@ -175,6 +175,16 @@ flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1
  */
 flashbob_status flashbob_last_device_error(void);
 
+/*
+ * flashbob_check_wait_timeout: a diagnostic of the bounded waits, with no
+ * counterpart on the pages.  Launches one CTA on `stream` whose mbarrier
+ * wait has nothing to wait for; after the wait limit (2 s) the kernel records
+ * a timeout in the device error word and returns, so that the next
+ * flashbob_last_device_error() reports FLASHBOB_ERR_TIMEOUT and the context
+ * stays usable.  Returns FLASHBOB_ERR_CUDA if the launch fails.
+ */
+flashbob_status flashbob_check_wait_timeout(void* stream);
+
 /* flashbob_status_string: a static, human-readable name of `s`. */
 const char* flashbob_status_string(flashbob_status s);
 

@@ -256,3 +256,19 @@ def test_d128_mid_length_sampled_rows():
     assert max(res.values()) <= TOL["bf16"], res
     full = full_oracle_errors(w, x, state, out, heads=[(0, 1)])
     assert max(full.values()) <= TOL["bf16"], full
+
+
+# --------------------------------------------------------------------------
+# Failure detection: a bounded wait that runs out is reported, not hung
+# --------------------------------------------------------------------------
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    import time
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    t0 = time.perf_counter()
+    fb.flashbob_check_wait_timeout()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_ERR_TIMEOUT  # synchronises
+    assert time.perf_counter() - t0 >= 1.5  # the 2 s limit, not an early exit
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK  # the report clears the word
+    # the context is still usable
+    _check_full(wl.small_workload(1, 2, 150, 64, "bf16", seed=31))
