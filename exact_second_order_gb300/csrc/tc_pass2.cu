@@ -51,7 +51,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Smem2 {
   alignas(1024) uint8_t kb[4][BLOCK_BYTES];      // K, U_K, V, U_V (resident)
   alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, U_Q, dO (Q|U_Q adjacent)
-  float4 scal[2][2][32];  // per warpgroup, double-buffered: (L log2 e, D, alpha, E)
+  float4 scal[2][2][32];  // per warpgroup, double-buffered: (L log2 e, D, alpha, alpha D + E)
   uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
@@ -94,15 +94,16 @@ __device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = e + h;
-      const float4 rs = scal[i];  // (L log2 e, D, alpha, E) of query row ibase + i
+      // (L log2 e, D, alpha, alpha D + E) of query row ibase + i.  With
+      // X = dP - D:  F o X + G - alpha dP - E = X (F - alpha) + G - (alpha D + E).
+      const float4 rs = scal[i];
       float p = ex2_approx(fmaf(u2f(s[i]), c1, -rs.x));
       if (MASKED && ibase + i < gj) p = 0.f;
-      const float dpv = u2f(dp[i]);
-      const float x = dpv - rs.y;
-      const float ft = u2f(f[i]) * tau;
+      const float x = u2f(dp[i]) - rs.y;
+      const float w0 = fmaf(u2f(f[i]), tau, -rs.z);  // F - alpha
       vds[h] = p * x;
-      vdst[h] = p * (fmaf(ft, x, u2f(g[i])) - fmaf(rs.z, dpv, rs.w));
-      vw[h] = p * (ft - rs.z);
+      vdst[h] = p * (fmaf(x, w0, u2f(g[i])) - rs.w);
+      vw[h] = p * w0;
     }
     ods[e >> 1] = pack_bf16x2(vds[0], vds[1]);
     odst[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
     bool ok = true;
 
-    // Row scalars (L log2 e, D, alpha, E) of this warpgroup's 32 query rows
+    // Row scalars (L log2 e, D, alpha, alpha D + E) of this warpgroup's 32 query rows
     // of streamed tile f, which is tile ft of the head whose rows start at
     // fh; rows past N get L = +inf so that P = exp2(-inf) = 0.  (ft, fh)
     // step along with f instead of dividing f by Tq.
@@ -352,7 +353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
       if (f < T && i < Nq) {
         const size_t o = static_cast<size_t>(fL - L) + i;
-        v = make_float4(fL[i] * kLog2e, D[o], alpha[o], E[o]);
+        const float dv = D[o], av = alpha[o];
+        v = make_float4(fL[i] * kLog2e, dv, av, fmaf(av, dv, E[o]));
       }
       if (++ft == Tq) { ft = 0; fL += Nq; }
       return v;
