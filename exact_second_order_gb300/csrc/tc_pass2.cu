@@ -342,10 +342,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
     bool ok = true;
 
-    // Row scalars (L log2 e, D, alpha, alpha D + E) of this warpgroup's 32 query rows
-    // of streamed tile f, which is tile ft of the head whose rows start at
-    // fh; rows past N get L = +inf so that P = exp2(-inf) = 0.  (ft, fh)
-    // step along with f instead of dividing f by Tq.
+    // Row scalars (L, D, alpha, E) of this warpgroup's 32 query rows of
+    // streamed tile f, which is tile ft of the head whose L row starts at
+    // fL; rows past Nq get L = +inf so that P = exp2(-inf) = 0.  (ft, fL)
+    // step along with f (calls come in order) instead of dividing f by Tq.
+    // The loads are only issued here: nothing uses the values until
+    // stage() at the end of the tile, so the warp does not wait for them.
     int ft = 0;
     const float* fL = L + static_cast<size_t>(hq0) * Nq;
     auto load_scalars = [&](int f) {
@@ -353,15 +355,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
       if (f < T && i < Nq) {
         const size_t o = static_cast<size_t>(fL - L) + i;
-        const float dv = D[o], av = alpha[o];
-        v = make_float4(fL[i] * kLog2e, dv, av, fmaf(av, dv, E[o]));
+        v = make_float4(fL[i], D[o], alpha[o], E[o]);
       }
       if (++ft == Tq) { ft = 0; fL += Nq; }
       return v;
     };
+    // What the element-wise code reads: (L log2 e, D, alpha, alpha D + E).
+    auto stage = [](float4 v) {
+      return make_float4(v.x * kLog2e, v.y, v.z, fmaf(v.z, v.y, v.w));
+    };
     // The loader warp fetches the scalars one tile ahead into registers, so
     // their global-memory latency hides behind the current tile.
-    if (loader) sm.scal[wg][0][lane] = load_scalars(0);
+    if (loader) sm.scal[wg][0][lane] = stage(load_scalars(0));
     int tq = 0;  // tile of the current query head, (t mod Tq)
     for (int t = 0; t < T; ++t) {
       const float4* scal = sm.scal[wg][t & 1];
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // Every thread passed this iteration's barrier, so nobody still reads
       // the other buffer.
-      if (loader) sm.scal[wg][(t + 1) & 1][lane] = next;
+      if (loader) sm.scal[wg][(t + 1) & 1][lane] = stage(next);
       if (++tq == Tq) tq = 0;
     }
 

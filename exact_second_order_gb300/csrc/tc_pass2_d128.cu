@@ -330,15 +330,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
       if (lane < 16 && f < T && i < Nq) {
         const size_t o = static_cast<size_t>(fL - L) + i;
-        const float dv = D[o], av = alpha[o];
-        v = make_float4(fL[i] * kLog2e, dv, av, fmaf(av, dv, E[o]));
+        v = make_float4(fL[i], D[o], alpha[o], E[o]);
       }
       if (++ft == Tq) { ft = 0; fL += Nq; }
       return v;
     };
+    // Only the loads are issued in load_scalars; the values are first used
+    // here, at the end of the tile: (L log2 e, D, alpha, alpha D + E).
+    auto stage = [](float4 v) {
+      return make_float4(v.x * kLog2e, v.y, v.z, fmaf(v.z, v.y, v.w));
+    };
     if (loader) {
       const float4 v = load_scalars(0);
-      if (lane < 16) sm.scal[wg][0][lane] = v;
+      if (lane < 16) sm.scal[wg][0][lane] = stage(v);
     }
     int tq = 0;  // tile of the current query head
     for (int t = 0; t < T; ++t) {
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         else
           ok = p2w_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
       }
-      if (loader && lane < 16) sm.scal[wg][(t + 1) & 1][lane] = next;
+      if (loader && lane < 16) sm.scal[wg][(t + 1) & 1][lane] = stage(next);
       if (++tq == Tq) tq = 0;
     }
 
