@@ -112,11 +112,12 @@ __device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t
 }
 
 // The 32 query rows of one warpgroup: read S^T and F'^T of both 16-row
-// chunks and release them; then per chunk read dP^T and G^T, form dS, d~S,
-// W and write them to the operand area (the first chunk once the previous
-// tile's output GEMMs are done with it), releasing dP^T | G^T after the
-// second chunk's read.  Writing chunk 0 before reading chunk 1 keeps one
-// chunk's operands live at a time.
+// chunks and release them; read dP^T, G^T of the first chunk and form its
+// dS, d~S, W; read dP^T, G^T of the second chunk and release the score
+// buffer; only then wait until the previous tile's output GEMMs are done
+// with the operand area, write the first chunk's operands, form and write
+// the second's.  The release does not wait for the output GEMMs, and only
+// one chunk's operands are live at a time.
 template <bool MASKED>
 __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const float4* scal,
                                         int ibase, int gj, float c1, float tau, Smem2& sm,
@@ -131,25 +132,27 @@ __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const
   tmem_wait_ld();
   tc_fence_before();
   warp_arrive(&sm.sf_free);  // this warp is done with S^T | F'^T
+  uint32_t a_ds[8], a_dst[8], a_w[8];
   {
-    uint32_t dp[16], g[16], o_ds[8], o_dst[8], o_w[8];
+    uint32_t dp[16], g[16];
     tmem_ld16(sc + kColdP + col, dp);
     tmem_ld16(sc + kColG + col, g);
     tmem_wait_ld();
-    p2_chunk<MASKED>(s0, dp, f0, g, scal, ibase, gj, c1, tau, o_ds, o_dst, o_w);
-    if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
-    tc_fence_after();
-    tmem_st8(opb + op_col(kOpdS, kk), o_ds);
-    tmem_st8(opb + op_col(kOpdSt, kk), o_dst);
-    tmem_st8(opb + op_col(kOpW, kk), o_w);
+    p2_chunk<MASKED>(s0, dp, f0, g, scal, ibase, gj, c1, tau, a_ds, a_dst, a_w);
   }
+  uint32_t dp[16], g[16];
+  tmem_ld16(sc + kColdP + col + 16, dp);
+  tmem_ld16(sc + kColG + col + 16, g);
+  tmem_wait_ld();
+  tc_fence_before();
+  warp_arrive(&sm.pg_free);  // this warp is done with dP^T | G^T
+  if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
+  tc_fence_after();
+  tmem_st8(opb + op_col(kOpdS, kk), a_ds);
+  tmem_st8(opb + op_col(kOpdSt, kk), a_dst);
+  tmem_st8(opb + op_col(kOpW, kk), a_w);
   {
-    uint32_t dp[16], g[16], o_ds[8], o_dst[8], o_w[8];
-    tmem_ld16(sc + kColdP + col + 16, dp);
-    tmem_ld16(sc + kColG + col + 16, g);
-    tmem_wait_ld();
-    tc_fence_before();
-    warp_arrive(&sm.pg_free);  // this warp is done with dP^T | G^T
+    uint32_t o_ds[8], o_dst[8], o_w[8];
     p2_chunk<MASKED>(s1, dp, f1, g, scal + 16, ibase + 16, gj, c1, tau, o_ds, o_dst, o_w);
     tmem_st8(opb + op_col(kOpdS, kk + 1), o_ds);
     tmem_st8(opb + op_col(kOpdSt, kk + 1), o_dst);
