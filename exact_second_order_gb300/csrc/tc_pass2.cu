@@ -305,12 +305,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     bool ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
     for (int t = 0; ok && t < T; ++t) {
+      // Tile t's data is normally in the ring long before the warpgroups
+      // release S^T | F'^T of tile t - 1: check it first, so that the S/F
+      // GEMMs issue as soon as the release arrives.
+      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+      if (!ok) break;
       if (t > 0) {  // both warpgroups hold S^T, F'^T of tile t - 1 in registers
         ok = mbar_wait_warp(&sm.sf_free, (t - 1) & 1, abort_flag, err);
         if (!ok) break;
       }
-      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
-      if (!ok) break;
       tc_fence_after();
       issue_sf(t);
       if (t > 0) {  // ... and dP^T, G^T

@@ -280,12 +280,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     bool ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
     for (int t = 0; ok && t < T; ++t) {
+      // Tile t's data is normally in the ring before the S/F release of tile
+      // t - 1 arrives: check it first, so the S/F GEMMs follow the release.
+      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
+      if (!ok) break;
       if (t > 0) {
         ok = mbar_wait_warp(&sm.sf_free, (t - 1) & 1, abort_flag, err);
         if (!ok) break;
       }
-      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
-      if (!ok) break;
       tc_fence_after();
       issue_sf(t);
       if (t > 0) {
