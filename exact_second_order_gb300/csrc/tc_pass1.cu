@@ -12,7 +12,7 @@
 // CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
 //   warp 0      TMA producer: Q, dO, U_Q blocks once, then K, U_K, V, U_V
 //               tiles of 32 key rows through a 6-stage mbarrier ring;
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer;
+//   warp 1      TMEM allocator; one elected lane runs the MMA schedule;
 //   warps 2-5   elementwise warpgroup 0 (tiles 0, 2, 4, ...),
 //   warps 6-9   elementwise warpgroup 1 (tiles 1, 3, 5, ...).
 // TMEM (512 columns x 128 lanes, fp32):
@@ -282,11 +282,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t dUV0 = smem_desc_sw128(kv0 + 3 * TILE_BYTES, 16, 1024);
       // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
       const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
-      // One elected lane issues each group of MMAs as one straight block.
+      // One elected lane runs the whole schedule below: every wait and every
+      // MMA, with no warp-wide broadcast between them (the MMA-warp time per
+      // tile is what bounds this pass).
       auto issue_scores = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        if (elect_one()) {
+        {
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
             const uint64_t o = 2 * kk;  // 32 bytes >> 4
@@ -297,13 +299,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           mma_commit(&sm.sc_full[t & 1]);
         }
-        __syncwarp();
       };
       auto issue_outputs = [&](int t) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        if (elect_one()) {
+        {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
@@ -321,28 +322,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           mma_commit(&sm.kv_empty[s]);
         }
-        __syncwarp();
       };
-      bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
-      tc_fence_after();
-      for (int t = 0; ok && t < 2 && t < T; ++t) {
-        ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+      if (elect_one()) {
+        bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
         tc_fence_after();
-        if (ok) issue_scores(t);
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
-        issue_outputs(t);
-        if (t + 2 < T) {
-          ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+        for (int t = 0; ok && t < 2 && t < T; ++t) {
+          ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+          tc_fence_after();
+          if (ok) issue_scores(t);
+        }
+        for (int t = 0; ok && t < T; ++t) {
+          ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          issue_scores(t + 2);
+          issue_outputs(t);
+          if (t + 2 < T) {
+            ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_scores(t + 2);
+          }
         }
+        mma_commit(&sm.out_full);  // every MMA issued above has finished
       }
-      if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
+      __syncwarp();
     }
   } else {
     // ---------------- elementwise warpgroups + epilogue ----------------

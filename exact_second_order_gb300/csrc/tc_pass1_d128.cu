@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto issue_scores = [&](int t) {
       const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
       const uint32_t sc = tbase + 256 + 128 * (t & 1);
-      if (elect_one()) {
+      {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int h = kk >> 2;
@@ -281,13 +281,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit(&sm.sc_full[t & 1]);
       }
-      __syncwarp();
     };
     auto issue_outputs = [&](int t) {  // phase B only; phase A just frees the stage
       const int s = t % NST;
       const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
       const uint32_t sc = tbase + 256 + 128 * (t & 1);
-      if (elect_one()) {
+      {
         if (t >= TB) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -303,28 +302,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit(&sm.kv_empty[s]);
       }
-      __syncwarp();
     };
-    bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
-    tc_fence_after();
-    for (int t = 0; ok && t < 2 && t < T2; ++t) {
-      ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+    // One elected lane runs the whole schedule: every wait and every MMA.
+    if (elect_one()) {
+      bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
       tc_fence_after();
-      if (ok) issue_scores(t);
-    }
-    for (int t = 0; ok && t < T2; ++t) {
-      ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
-      if (!ok) break;
-      tc_fence_after();
-      issue_outputs(t);
-      if (t + 2 < T2) {
-        ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+      for (int t = 0; ok && t < 2 && t < T2; ++t) {
+        ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+        tc_fence_after();
+        if (ok) issue_scores(t);
+      }
+      for (int t = 0; ok && t < T2; ++t) {
+        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_scores(t + 2);
+        issue_outputs(t);
+        if (t + 2 < T2) {
+          ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + 2);
+        }
       }
+      mma_commit(&sm.out_full);  // every MMA issued above has finished
     }
-    if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
     __syncwarp();
   } else {
     // ---------------- elementwise warpgroups + epilogue ----------------

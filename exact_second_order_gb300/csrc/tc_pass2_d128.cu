@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
     auto issue_sf = [&](int t) {
       const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
-      if (elect_one()) {
+      {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int h = kk >> 2;
@@ -245,11 +245,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColF, dUK[h] + o, dQ[h] + so + o, idS32, 1);      // F'^T += U_K Q^T
         }
       }
-      __syncwarp();
     };
     auto issue_pg = [&](int t) {
       const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
-      if (elect_one()) {
+      {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int h = kk >> 2;
@@ -259,12 +258,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit(&sm.sc_full);
       }
-      __syncwarp();
     };
     auto issue_outputs = [&](int t) {
       const int s = t % NST;
       const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
-      if (elect_one()) {
+      {
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint64_t o = (uint64_t)(16 * 128 * kk) >> 4;  // 16 query rows further down
@@ -276,39 +274,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_commit(&sm.op_free);
         mma_commit(&sm.st_empty[s]);
       }
-      __syncwarp();
     };
-    bool ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
-    for (int t = 0; ok && t < T; ++t) {
-      // Tile t's data is normally in the ring before the S/F release of tile
-      // t - 1 arrives: check it first, so the S/F GEMMs follow the release.
-      ok = mbar_wait_warp(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
-      if (!ok) break;
-      if (t > 0) {
-        ok = mbar_wait_warp(&sm.sf_free, (t - 1) & 1, abort_flag, err);
+    // One elected lane runs the whole schedule: every wait and every MMA.
+    if (elect_one()) {
+      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err);
+      for (int t = 0; ok && t < T; ++t) {
+        // Tile t's data is normally in the ring before the S/F release of
+        // tile t - 1 arrives: check it first, so the S/F GEMMs follow it.
+        ok = mbar_wait(&sm.st_full[t % NST], (t / NST) & 1, abort_flag, err);
         if (!ok) break;
-      }
-      tc_fence_after();
-      issue_sf(t);
-      if (t > 0) {
-        ok = mbar_wait_warp(&sm.pg_free, (t - 1) & 1, abort_flag, err);
-        if (!ok) break;
+        if (t > 0) {
+          ok = mbar_wait(&sm.sf_free, (t - 1) & 1, abort_flag, err);
+          if (!ok) break;
+        }
         tc_fence_after();
+        issue_sf(t);
+        if (t > 0) {
+          ok = mbar_wait(&sm.pg_free, (t - 1) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_pg(t);
+        if (t > 0) {
+          ok = mbar_wait(&sm.op_ready, (t - 1) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_outputs(t - 1);
+        }
       }
-      issue_pg(t);
-      if (t > 0) {
-        ok = mbar_wait_warp(&sm.op_ready, (t - 1) & 1, abort_flag, err);
-        if (!ok) break;
+      if (ok && T > 0) {
+        ok = mbar_wait(&sm.op_ready, (T - 1) & 1, abort_flag, err);
         tc_fence_after();
-        issue_outputs(t - 1);
+        if (ok) issue_outputs(T - 1);
       }
+      mma_commit(&sm.out_full);  // every MMA issued above has finished
     }
-    if (ok && T > 0) {
-      ok = mbar_wait_warp(&sm.op_ready, (T - 1) & 1, abort_flag, err);
-      tc_fence_after();
-      if (ok) issue_outputs(T - 1);
-    }
-    if (elect_one()) mma_commit(&sm.out_full);  // every MMA issued above has finished
     __syncwarp();
   } else {
     const int wg = (warp - 2) >> 2;
