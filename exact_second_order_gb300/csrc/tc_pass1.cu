@@ -8,23 +8,27 @@
 // alpha-free, and 关键设计 1's affine correction
 //     E = E0 - alpha D,  d~dO = d~dO0 - alpha O,  d~Q = tau (Omega - alpha R - E B)
 // runs once in the epilogue, so every output row is written exactly once.
+// R is carried as R' = dS K = R - D B (dS = P o (dP - D)), which turns the
+// correction into d~Q = tau (Omega - alpha R' - E0 B): the same value, one
+// bf16 operand fewer, and dS [U_K | K] yields Omega's dS U_K term and R' in
+// one MMA (20 MMAs per tile instead of 22; this pass is MMA-bound).
 //
 // CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
-//   warp 0      TMA producer: Q, dO, U_Q blocks once, then K, U_K, V, U_V
+//   warp 0      TMA producer: Q, dO, U_Q blocks once, then U_K, K, V, U_V
 //               tiles of 32 key rows through a 6-stage mbarrier ring;
 //   warp 1      TMEM allocator; one elected lane runs the MMA schedule;
 //   warps 2-5   elementwise warpgroup 0 (tiles 0, 2, 4, ...),
 //   warps 6-9   elementwise warpgroup 1 (tiles 1, 3, 5, ...).
 // TMEM (512 columns x 128 lanes, fp32):
-//   [0,64) B = P K   [64,128) d~dO0   [128,192) R = (P o dP) K   [192,256) Omega
+//   [0,64) B = P K   [64,128) d~dO0   [128,192) Omega   [192,256) R' = dS K
 //   [256,384) score buffer 0, [384,512) score buffer 1, each holding
-//   S = Q K^T | F' = Q U_K^T + U_Q K^T | dP = dO V^T | G = dO U_V^T (32 columns each).
-// GEMMs that share an operand run as one wider MMA: Q [K; U_K]^T gives S and
-// half of F' (N = 64), dO [V; U_V]^T gives dP and G (N = 64), and
-// P [K | U_V] gives both B and the P U_V part of d~dO0 (N = 128).  Once a
-// warpgroup has read a score buffer it overwrites consumed columns with the
-// bf16 A operands (P, P o dP, P o d~P0, dS, P o F) of the output GEMMs,
-// which read A straight from TMEM.
+//   F' = Q U_K^T + U_Q K^T | S = Q K^T | dP = dO V^T | G = dO U_V^T (32 columns each).
+// GEMMs that share an operand run as one wider MMA: Q [U_K; K]^T gives half
+// of F' and S (N = 64), dO [V; U_V]^T gives dP and G (N = 64), P [K | U_V]
+// gives B and the P U_V part of d~dO0 (N = 128), and dS [U_K | K] gives
+// Omega's dS U_K part and R' (N = 128).  Once a warpgroup has read a score
+// buffer it overwrites it with the bf16 A operands (P, P o d~P0, dS, P o F)
+// of the output GEMMs, which read A straight from TMEM.
 //
 // The same kernel, instantiated with JVP = true, serves the attention JVP
 // along (U_Q, U_K, U_V): alpha and d~dO do not depend on dO, so with dO = 0
@@ -49,7 +53,7 @@ struct Smem1 {
   alignas(1024) uint8_t q[BLOCK_BYTES];
   alignas(1024) uint8_t dO[BLOCK_BYTES];
   alignas(1024) uint8_t uq[BLOCK_BYTES];
-  alignas(1024) uint8_t kv[NST][4][TILE_BYTES];  // K, U_K, V, U_V (K|U_K and V|U_V adjacent)
+  alignas(1024) uint8_t kv[NST][4][TILE_BYTES];  // U_K, K, V, U_V (U_K|K and V|U_V adjacent)
   float part_a[2][BM];
   float part_e[2][BM];
   uint64_t bar_q;
@@ -62,19 +66,18 @@ struct Smem1 {
   int abort_flag;
 };
 
-// Score buffer layout (columns): S at 0, F' at 32, dP at 64, G at 96.
-constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;
+// Score buffer layout (columns): F' at 0, S at 32, dP at 64, G at 96.
+constexpr uint32_t kColF = 0, kColS = 32, kColdP = 64, kColG = 96;
 // TMEM columns of the bf16 operand slots inside a score buffer, for the two
-// K = 16 steps of the output GEMMs.  Chunk 0 (score columns 0..15) writes
-// only columns it has consumed (the first 16 of each 32-column score);
-// chunk 1 may also use columns 16..31 of S and F', which it loaded itself.
-__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return c ? 72 : 0; }
-__device__ __forceinline__ constexpr uint32_t slot_PdP(int c) { return c ? 96 : 8; }
-__device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return c ? 104 : 32; }
-__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return c ? 16 : 40; }
-__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return c ? 48 : 64; }
+// K = 16 steps (chunks) of the output GEMMs.  A warpgroup reads the whole
+// buffer (the JVP: S and F') before it writes any slot; the JVP's score
+// GEMMs never write the dP/G columns.
+__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 8 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return 16 + 8 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 32 + 8 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 48 + 8 * c; }
 // Output accumulators.
-constexpr uint32_t kAccB = 0, kAccdO = 64, kAccR = 128, kAccW = 192;
+constexpr uint32_t kAccB = 0, kAccdO = 64, kAccW = 128, kAccR = 192;  // R' = dS K
 
 // One 16-column chunk of a score buffer, one row per thread: read S, dP, F',
 // G from TMEM, form P = exp(S - L) and the five bf16 A operands of the
@@ -86,11 +89,11 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
                                          const uint32_t (&g)[16], int col0, int jmax, float c1,
                                          float Lr2, float Dr, float tau, float& a_acc,
                                          float& e_acc) {
-  uint32_t oP[8], oPdP[8], oPdPt[8], odS[8], oPF[8];
+  uint32_t oP[8], oPdPt[8], odS[8], oPF[8];
   const int jbase = col0 + 16 * C;
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    float pv[2], pdp[2], pdpt[2], ds[2], pf[2];
+    float pv[2], pdpt[2], ds[2], pf[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int j = e + h;
@@ -101,7 +104,6 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
       const float ft = u2f(f[j]) * tau;
       const float dpt0 = fmaf(ft, x, u2f(g[j]));
       pv[h] = p;
-      pdp[h] = p * dpv;
       pdpt[h] = p * dpt0;
       ds[h] = p * x;
       pf[h] = p * ft;
@@ -109,13 +111,11 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
       e_acc += pdpt[h];
     }
     oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-    oPdP[e >> 1] = pack_bf16x2(pdp[0], pdp[1]);
     oPdPt[e >> 1] = pack_bf16x2(pdpt[0], pdpt[1]);
     odS[e >> 1] = pack_bf16x2(ds[0], ds[1]);
     oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
   }
   tmem_st8(sc + slot_P(C), oP);
-  tmem_st8(sc + slot_PdP(C), oPdP);
   tmem_st8(sc + slot_PdPt(C), oPdPt);
   tmem_st8(sc + slot_dS(C), odS);
   tmem_st8(sc + slot_PF(C), oPF);
@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int s = t % NST;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.kv_full[s], 4 * TILE_BYTES);
-        tma_load_3d(sm.kv[s][0], &mK, &sm.kv_full[s], 0, t * BN, bkv);
-        tma_load_3d(sm.kv[s][1], &mUK, &sm.kv_full[s], 0, t * BN, bkv);
+        tma_load_3d(sm.kv[s][0], &mUK, &sm.kv_full[s], 0, t * BN, bkv);
+        tma_load_3d(sm.kv[s][1], &mK, &sm.kv_full[s], 0, t * BN, bkv);
         tma_load_3d(sm.kv[s][2], &mV, &sm.kv_full[s], 0, t * BN, bkv);
         tma_load_3d(sm.kv[s][3], &mUV, &sm.kv_full[s], 0, t * BN, bkv);
         issued = t + 1;
@@ -276,12 +276,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t ddo0 = smem_desc_sw128(smem_u32(sm.dO), 16, 1024);
       const uint64_t duq0 = smem_desc_sw128(smem_u32(sm.uq), 16, 1024);
       const uint32_t kv0 = smem_u32(sm.kv[0][0]);
-      const uint64_t dK0 = smem_desc_sw128(kv0, 16, 1024);                   // K (and K;U_K)
+      const uint64_t dUK0 = smem_desc_sw128(kv0, 16, 1024);                  // U_K (and U_K;K)
+      const uint64_t dK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);      // K
       const uint64_t dV0 = smem_desc_sw128(kv0 + 2 * TILE_BYTES, 16, 1024);  // V (and V;U_V)
-      const uint64_t dUK0 = smem_desc_sw128(kv0 + TILE_BYTES, 16, 1024);
       const uint64_t dUV0 = smem_desc_sw128(kv0 + 3 * TILE_BYTES, 16, 1024);
-      // MN-major [K | U_V]: the second 64-column chunk sits 3 tiles further.
-      const uint64_t dKUV0 = smem_desc_sw128(kv0, 3 * TILE_BYTES, 1024);
+      // MN-major [K | U_V] (second half 2 tiles on) and [U_K | K] (1 tile on).
+      const uint64_t dKUV0 = smem_desc_sw128(kv0 + TILE_BYTES, 2 * TILE_BYTES, 1024);
+      const uint64_t dUKK0 = smem_desc_sw128(kv0, TILE_BYTES, 1024);
       // One elected lane runs the whole schedule below: every wait and every
       // MMA, with no warp-wide broadcast between them (the MMA-warp time per
       // tile is what bounds this pass).
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int kk = 0; kk < DH / 16; ++kk) {
             const uint64_t o = 2 * kk;  // 32 bytes >> 4
             const uint32_t acc = kk > 0;
-            mma_ss(sc + kColS, dq0 + o, dK0 + so + o, idS64, acc);   // [S | F'] = Q [K; U_K]^T
+            mma_ss(sc + kColF, dq0 + o, dUK0 + so + o, idS64, acc);  // [F' | S] = Q [U_K; K]^T
             mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);    // F' += U_Q K^T
             if (!JVP) mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
           }
@@ -315,9 +316,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               continue;
             }
             mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
-            mma_ts(tbase + kAccR, sc + slot_PdP(c), dK0 + so + o, idO64, acc);   // R += (P o dP) K
-            mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, acc);  // Omega += (P o d~P0) K
-            mma_ts(tbase + kAccW, sc + slot_dS(c), dUK0 + so + o, idO64, 1);     //       +  dS U_K
+            mma_ts(tbase + kAccW, sc + slot_dS(c), dUKK0 + so + o, idO128, acc); // [Omega | R'] += dS [U_K | K]
+            mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, 1);    // Omega += (P o d~P0) K
             mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);     // d~dO0 += (P o F) V
           }
           mma_commit(&sm.kv_empty[s]);
@@ -387,7 +387,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     sm.part_e[wg][r] = e_acc;
     named_bar_sync(1, 256);
     const float al = sm.part_a[0][r] + sm.part_a[1][r];
-    const float Ei = (sm.part_e[0][r] + sm.part_e[1][r]) - al * Dr;
+    const float E0 = sm.part_e[0][r] + sm.part_e[1][r];
+    const float Ei = E0 - al * Dr;
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
@@ -423,10 +424,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int k = 0; k < 4; ++k) {
           const float4 ov = o4[k];
           float4 qv, dv;
-          qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - Ei * u2f(vb[4 * k + 0]));
-          qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - Ei * u2f(vb[4 * k + 1]));
-          qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - Ei * u2f(vb[4 * k + 2]));
-          qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - Ei * u2f(vb[4 * k + 3]));
+          qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - E0 * u2f(vb[4 * k + 0]));
+          qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - E0 * u2f(vb[4 * k + 1]));
+          qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - E0 * u2f(vb[4 * k + 2]));
+          qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - E0 * u2f(vb[4 * k + 3]));
           dv.x = u2f(vo[4 * k + 0]) - al * ov.x;
           dv.y = u2f(vo[4 * k + 1]) - al * ov.y;
           dv.z = u2f(vo[4 * k + 2]) - al * ov.z;

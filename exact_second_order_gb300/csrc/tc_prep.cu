@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
-    {  // MMA issuer: whole warp, one elected lane issues
+    {  // MMA issuer: one elected lane runs the whole schedule
       constexpr uint32_t idS = idesc_bf16(BM, BN, false);
       constexpr uint32_t idO = idesc_bf16(BM, DH, true);
       auto issue_scores = [&](int t) {
@@ -134,12 +134,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int h = kk >> 2;  // 64-column half of the head dim
           const uint32_t o = 32 * (kk & 3);
           const uint32_t aq = smem_u32(sm.q[h]), bk = smem_u32(sm.kv[s][0][h]);
-          if (elect_one())
-            mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
-                   kk > 0);
+          mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
+                 kk > 0);
         }
-        if (elect_one()) mma_commit(&sm.sc_full[t & 1]);
-        if (t < T && elect_one()) mma_commit(&sm.kv_empty[s]);  // phase A reads the stage only here
+        mma_commit(&sm.sc_full[t & 1]);
+        if (t < T) mma_commit(&sm.kv_empty[s]);  // phase A reads the stage only here
       };
       auto issue_pv = [&](int t) {
         const int s = t % NST;
@@ -148,33 +147,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // sits HALF_TILE bytes after the first.
         const uint32_t bv = smem_u32(sm.kv[s][1][0]);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (elect_one())
-            mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HALF_TILE, 1024), idO,
-                   (t > T || c > 0));
-        }
-        if (elect_one()) mma_commit(&sm.kv_empty[s]);
+        for (int c = 0; c < 2; ++c)
+          mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HALF_TILE, 1024), idO,
+                 (t > T || c > 0));
+        mma_commit(&sm.kv_empty[s]);
       };
-      bool ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
-      tc_fence_after();
-      for (int t = 0; ok && t < 2 && t < T2; ++t) {
-        ok = mbar_wait_warp(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+      if (elect_one()) {
+        bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
         tc_fence_after();
-        if (ok) issue_scores(t);
-      }
-      for (int t = 0; ok && t < T2; ++t) {
-        ok = mbar_wait_warp(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
-        if (t >= T) issue_pv(t);
-        if (t + 2 < T2) {
-          ok = mbar_wait_warp(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+        for (int t = 0; ok && t < 2 && t < T2; ++t) {
+          ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+          tc_fence_after();
+          if (ok) issue_scores(t);
+        }
+        for (int t = 0; ok && t < T2; ++t) {
+          ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          issue_scores(t + 2);
+          if (t >= T) issue_pv(t);
+          if (t + 2 < T2) {
+            ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_scores(t + 2);
+          }
         }
+        mma_commit(&sm.out_full);
       }
-      if (elect_one()) mma_commit(&sm.out_full);
+      __syncwarp();
     }
   } else {
     const int wg = (warp - 2) >> 2;
