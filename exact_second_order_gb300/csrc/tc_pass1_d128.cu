@@ -16,18 +16,23 @@
 //            W = P o (F - alpha) are final, and
 //              d~Q  = tau (d~S K + dS U_K),   d~dO = P U_V + W V
 //            accumulate directly (two 128-column accumulators).
-// The GEMM count per tile is 5 (phase A) + 9 (phase B) instead of 11; the
+// The GEMM count per key is 5 (phase A) + 9 (phase B) instead of 11; the
 // benchmark's FLOP convention still counts the 11 of the one-phase form.
 //
 // CTA = 128 query rows, 320 threads: warp 0 TMA (Q, dO, U_Q once; K, U_K,
-// V, U_V tiles of 32 key rows through a 3-stage ring, each tensor as two
+// V, U_V tiles of 32 key rows through a 4-slot ring, each tensor as two
 // 64-column halves in the 128-byte swizzle), warp 1 TMEM allocation and MMA
 // issue, warps 2-5 / 6-9 elementwise warpgroups on alternate tiles.
-// TMEM: [0,128) d~Q accumulator (without tau), [128,256) d~dO accumulator,
-// [256,384) and [384,512) score buffers S | F' | dP | G (32 columns each);
-// in phase B a warpgroup reads a buffer one 16-column chunk at a time and
-// overwrites the columns of that chunk with its bf16 A operands d~S, dS, P,
-// W of the output GEMMs.
+// Phase A has no accumulators, so it takes 64 keys per tile: two adjacent
+// ring slots hold, per 64-column half, K_a K_b U_K,a U_K,b V_a V_b U_V,a
+// U_V,b (a, b the two 32-key halves), and each K step is three MMAs with
+// N = 128, 64, 128: [S | F'] = Q [K; U_K]^T, F' += U_Q K^T, [dP | G] =
+// dO [V; U_V]^T, into a 256-column score buffer per warpgroup (all of TMEM).
+// Phase B: [0,128) d~Q accumulator (without tau), [128,256) d~dO
+// accumulator, [256,384) and [384,512) score buffers S | F' | dP | G (32
+// columns each) of 32-key tiles; a warpgroup reads a buffer one 16-column
+// chunk at a time and overwrites the columns of that chunk with its bf16 A
+// operands d~S, dS, P, W of the output GEMMs.
 //
 // Instantiated with JVP = true the kernel computes the attention JVP along
 // (U_Q, U_K, U_V) instead (no dO): one pass over the key tiles with S and F'
@@ -43,7 +48,7 @@ using namespace tc;
 constexpr int BM = kTcRows;    // 128 query rows per CTA
 constexpr int BN = kTcStream;  // 32 key rows per streamed tile
 constexpr int DH = 128;
-constexpr int NST = 3;
+constexpr int NST = 4;  // ring slots of BN keys; phase A pairs slots (0, 1) and (2, 3)
 constexpr int NTHREADS = 320;
 constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB: 128 rows x 64 columns
 constexpr uint32_t HALF_TILE = BN * 64 * 2;   // 4 KiB: 32 rows x 64 columns
@@ -54,9 +59,10 @@ struct SmemW1 {
   alignas(1024) uint8_t q[2][HALF_BLOCK];    // Q, columns 0..63 and 64..127
   alignas(1024) uint8_t dO[2][HALF_BLOCK];
   alignas(1024) uint8_t uq[2][HALF_BLOCK];
-  alignas(1024) uint8_t kv[NST][2][4][HALF_TILE];  // [stage][half][K, U_K, V, U_V]
-  float part_a[2][BM];
-  float part_e[2][BM];
+  // Phase B: [slot][half][K, U_K, V, U_V].  Phase A: slots 2p, 2p + 1 as one
+  // region [half][K_a, K_b, U_K,a, U_K,b, V_a, V_b, U_V,a, U_V,b].
+  alignas(1024) uint8_t kv[NST][2][4][HALF_TILE];
+  float2 part[BM];  // (alpha, E0) partial row sums passed between the warpgroups
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
@@ -78,6 +84,9 @@ __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 16 * c + 8
 __device__ __forceinline__ constexpr uint32_t slot_P(int c) { return kColF + 16 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_W(int c) { return kColF + 16 * c + 8; }
 
+// Phase-A score buffer (256 columns, 64 keys): S | F' | dP | G, 64 each.
+constexpr uint32_t kAColS = 0, kAColF = 64, kAColdP = 128, kAColG = 192;
+
 // S, dP, F', G of one 16-column chunk of a score buffer, one row per thread.
 struct Chunk {
   uint32_t s[16], dp[16], f[16], g[16];
@@ -88,6 +97,14 @@ __device__ __forceinline__ void load_chunk(uint32_t sc, int c, Chunk& x) {
   tmem_ld16(sc + kColdP + 16 * c, x.dp);
   tmem_ld16(sc + kColF + 16 * c, x.f);
   tmem_ld16(sc + kColG + 16 * c, x.g);
+}
+
+// Chunk c (keys 16c .. 16c + 15) of a phase-A buffer.
+__device__ __forceinline__ void load_chunk_a(uint32_t sc, int c, Chunk& x) {
+  tmem_ld16(sc + kAColS + 16 * c, x.s);
+  tmem_ld16(sc + kAColdP + 16 * c, x.dp);
+  tmem_ld16(sc + kAColF + 16 * c, x.f);
+  tmem_ld16(sc + kAColG + 16 * c, x.g);
 }
 
 // Phase A on one chunk: the row sums alpha += P F and E0 += P d~P0.
@@ -187,10 +204,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int bkv = blockIdx.z * Hkv + blockIdx.y / (H / Hkv);  // shared key/value head
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
   const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
-  const int T = (col_end + BN - 1) / BN;  // key tiles per phase
-  // Phase A tiles 0..T-1, phase B tiles T..2T-1; the JVP has phase B only.
-  const int TB = JVP ? 0 : T;  // first phase-B tile
-  const int T2 = TB + T;
+  const int T = (col_end + BN - 1) / BN;                                 // phase-B tiles
+  const int TA = JVP ? 0 : (col_end + 2 * BN - 1) / (2 * BN);          // phase-A tiles
+  // Ring uses in order: phase-A tile a takes uses 2a, 2a + 1 (the slot pair
+  // a mod 2), phase-B tile t takes use 2 TA + t (slot (2 TA + t) mod NST).
+  const int QN = 2 * TA + T;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -227,30 +245,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_3d(sm.uq[h], &mUQ, &sm.bar_q, 64 * h, row0, bh);
       }
       int issued = 0;
-      for (int t = 0; t < T2; ++t) {
-        const int s = t % NST;
-        const int kt = t < TB ? t : t - TB;
-        if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+      for (int q = 0; q < QN; ++q) {
+        const int s = q % NST;
+        if (q >= NST && !mbar_wait(&sm.kv_empty[s], ((q / NST) - 1) & 1, abort_flag, err)) break;
         mbar_expect_tx(&sm.kv_full[s], STAGE_BYTES);
-        for (int h = 0; h < 2; ++h) {
-          tma_load_3d(sm.kv[s][h][0], &mK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
-          tma_load_3d(sm.kv[s][h][1], &mUK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
-          tma_load_3d(sm.kv[s][h][2], &mV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
-          tma_load_3d(sm.kv[s][h][3], &mUV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+        if (q < 2 * TA) {
+          // Key rows 32 q .. of phase-A tile q / 2, half b = q & 1 of the
+          // pair: it lands in both slots' memory, so the partner slot's
+          // previous use must be released as well.
+          const int b = q & 1;
+          if (b == 0 && q + 1 >= NST &&
+              !mbar_wait(&sm.kv_empty[s + 1], (((q + 1) / NST) - 1) & 1, abort_flag, err))
+            break;
+          uint8_t* pair = sm.kv[s & ~1][0][0];
+          for (int h = 0; h < 2; ++h) {
+            uint8_t* hp = pair + h * 8 * HALF_TILE;
+            tma_load_3d(hp + (0 + b) * HALF_TILE, &mK, &sm.kv_full[s], 64 * h, q * BN, bkv);
+            tma_load_3d(hp + (2 + b) * HALF_TILE, &mUK, &sm.kv_full[s], 64 * h, q * BN, bkv);
+            tma_load_3d(hp + (4 + b) * HALF_TILE, &mV, &sm.kv_full[s], 64 * h, q * BN, bkv);
+            tma_load_3d(hp + (6 + b) * HALF_TILE, &mUV, &sm.kv_full[s], 64 * h, q * BN, bkv);
+          }
+        } else {
+          const int kt = q - 2 * TA;
+          for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sm.kv[s][h][0], &mK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+            tma_load_3d(sm.kv[s][h][1], &mUK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+            tma_load_3d(sm.kv[s][h][2], &mV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+            tma_load_3d(sm.kv[s][h][3], &mUV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+          }
         }
-        issued = t + 1;
+        issued = q + 1;
       }
       // No copy may still be in flight when the CTA exits.
       drain_wait(&sm.bar_q, 0);
-      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
-        drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
+      for (int q = issued > NST ? issued - NST : 0; q < issued; ++q)
+        drain_wait(&sm.kv_full[q % NST], (q / NST) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
     constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
     constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
+    constexpr uint32_t idS128 = idesc_bf16(BM, 4 * BN, false);  // N = 128, B K-major
     constexpr uint32_t idO128 = idesc_bf16(BM, DH, true);      // N = 128, B MN-major
-    uint64_t dq[2], ddo[2], duq[2], dK[2], dV[2];
+    uint64_t dq[2], ddo[2], duq[2], dK[2], dV[2], dA[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       dq[h] = smem_desc_sw128(smem_u32(sm.q[h]), 16, 1024);
@@ -258,6 +295,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       duq[h] = smem_desc_sw128(smem_u32(sm.uq[h]), 16, 1024);
       dK[h] = smem_desc_sw128(smem_u32(sm.kv[0][h][0]), 16, 1024);  // K (and K; U_K)
       dV[h] = smem_desc_sw128(smem_u32(sm.kv[0][h][2]), 16, 1024);  // V (and V; U_V)
+      // Phase A: half h of pair 0 (K_a, K_b, U_K,a, U_K,b, then V_a ...).
+      dA[h] = smem_desc_sw128(smem_u32(sm.kv[0][0][0]) + h * 8 * HALF_TILE, 16, 1024);
     }
     // MN-major N = 128 operands: columns 64..127 (half 1) sit 4 tiles after
     // columns 0..63 (half 0) of the same tensor.
@@ -266,8 +305,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dUKmn = smem_desc_sw128(smem_u32(sm.kv[0][0][1]), kHalfStride, 1024);
     const uint64_t dVmn = smem_desc_sw128(smem_u32(sm.kv[0][0][2]), kHalfStride, 1024);
     const uint64_t dUVmn = smem_desc_sw128(smem_u32(sm.kv[0][0][3]), kHalfStride, 1024);
+    // Phase-A tile a: pair a mod 2, warpgroup a mod 2's 256-column buffer.
+    // The slots are free again once these MMAs have read them.
+    auto issue_scores_a = [&](int a) {
+      const uint64_t po = (uint64_t)((a & 1) * 2 * STAGE_BYTES) >> 4;
+      constexpr uint64_t kVUV = (uint64_t)(4 * HALF_TILE) >> 4;  // V_a V_b U_V,a U_V,b
+      const uint32_t sc = tbase + 256 * (a & 1);
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        const int h = kk >> 2;
+        const uint64_t o = 2 * (kk & 3);
+        const uint32_t acc = kk > 0;
+        mma_ss(sc + kAColS, dq[h] + o, dA[h] + po + o, idS128, acc);  // [S | F'] = Q [K; U_K]^T
+        mma_ss(sc + kAColF, duq[h] + o, dA[h] + po + o, idS64, 1);    // F' += U_Q K^T
+        mma_ss(sc + kAColdP, ddo[h] + o, dA[h] + po + kVUV + o, idS128, acc);  // [dP | G]
+      }
+      mma_commit(&sm.sc_full[a & 1]);
+      mma_commit(&sm.kv_empty[(2 * a) % NST]);
+      mma_commit(&sm.kv_empty[(2 * a + 1) % NST]);
+    };
     auto issue_scores = [&](int t) {
-      const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
+      const uint64_t so = (uint64_t)(((2 * TA + t) % NST) * STAGE_BYTES) >> 4;
       const uint32_t sc = tbase + 256 + 128 * (t & 1);
       {
 #pragma unroll
@@ -282,43 +340,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_commit(&sm.sc_full[t & 1]);
       }
     };
-    auto issue_outputs = [&](int t) {  // phase B only; phase A just frees the stage
-      const int s = t % NST;
+    auto issue_outputs = [&](int t) {
+      const int s = (2 * TA + t) % NST;
       const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
       const uint32_t sc = tbase + 256 + 128 * (t & 1);
-      {
-        if (t >= TB) {
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
-            const uint32_t acc = (t > TB || c > 0);
-            if (!JVP) {
-              mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
-              mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //  + dS U_K
-            }
-            mma_ts(tbase + kAccdO, sc + slot_P(c), dUVmn + so + o, idO128, acc);  // d~dO += P U_V
-            mma_ts(tbase + kAccdO, sc + slot_W(c), dVmn + so + o, idO128, 1);     //  + W V (P o F V)
-          }
+      for (int c = 0; c < 2; ++c) {
+        const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
+        const uint32_t acc = (t > 0 || c > 0);
+        if (!JVP) {
+          mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
+          mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //  + dS U_K
         }
-        mma_commit(&sm.kv_empty[s]);
+        mma_ts(tbase + kAccdO, sc + slot_P(c), dUVmn + so + o, idO128, acc);  // d~dO += P U_V
+        mma_ts(tbase + kAccdO, sc + slot_W(c), dVmn + so + o, idO128, 1);     //  + W V (P o F V)
       }
+      mma_commit(&sm.kv_empty[s]);
     };
     // One elected lane runs the whole schedule: every wait and every MMA.
     if (elect_one()) {
       bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
       tc_fence_after();
-      for (int t = 0; ok && t < 2 && t < T2; ++t) {
-        ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+      // Phase A: tile a goes to warpgroup a mod 2 once that warpgroup holds
+      // tile a - 2 in registers.
+      for (int a = 0; ok && a < TA; ++a) {
+        if (a >= 2 && !(ok = mbar_wait(&sm.op_ready[a & 1], ((a >> 1) - 1) & 1, abort_flag, err)))
+          break;
+        ok = mbar_wait(&sm.kv_full[(2 * a) % NST], ((2 * a) / NST) & 1, abort_flag, err) &&
+             mbar_wait(&sm.kv_full[(2 * a + 1) % NST], ((2 * a + 1) / NST) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores_a(a);
+      }
+      // Phase B's score buffers [256, 512) were warpgroup 1's phase-A buffer
+      // and its accumulators [0, 256) warpgroup 0's: wait until each
+      // warpgroup holds its last phase-A tile in registers.  (This also keeps
+      // sc_full from running two phases ahead of a warpgroup.)
+      const int nA0 = (TA + 1) / 2, nA1 = TA / 2;  // phase-A tiles per warpgroup
+      if (ok && nA0 > 0) ok = mbar_wait(&sm.op_ready[0], (nA0 - 1) & 1, abort_flag, err);
+      if (ok && nA1 > 0) ok = mbar_wait(&sm.op_ready[1], (nA1 - 1) & 1, abort_flag, err);
+      tc_fence_after();
+      for (int t = 0; ok && t < 2 && t < T; ++t) {
+        const int q = 2 * TA + t;
+        ok = mbar_wait(&sm.kv_full[q % NST], (q / NST) & 1, abort_flag, err);
         tc_fence_after();
         if (ok) issue_scores(t);
       }
-      for (int t = 0; ok && t < T2; ++t) {
-        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+      for (int t = 0; ok && t < T; ++t) {
+        ok = mbar_wait(&sm.op_ready[t & 1], ((t & 1 ? nA1 : nA0) + (t >> 1)) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t);
-        if (t + 2 < T2) {
-          ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+        if (t + 2 < T) {
+          const int q = 2 * TA + t + 2;
+          ok = mbar_wait(&sm.kv_full[q % NST], (q / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           issue_scores(t + 2);
@@ -339,47 +414,68 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
     const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
     float a_acc = 0.f, e_acc = 0.f, al = 0.f, Ei = 0.f;
-    bool ok = true, have_ae = false;
-    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
-    // Both warpgroups have finished phase A: alpha and E of the row.  Each
-    // warpgroup passes here exactly once (named barrier 1).
+    bool ok = true;
+    const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
+    // Both warpgroups' partial row sums meet here (each warpgroup passes
+    // exactly once, named barrier 1): warpgroup 1 hands its sums over,
+    // warpgroup 0 forms alpha and E = E0 - alpha D and hands them back.
     auto combine = [&]() {
-      sm.part_a[wg][r] = a_acc;
-      sm.part_e[wg][r] = e_acc;
+      if (wg == 1) sm.part[r] = make_float2(a_acc, e_acc);
       named_bar_sync(1, 256);
-      al = sm.part_a[0][r] + sm.part_a[1][r];
-      Ei = (sm.part_e[0][r] + sm.part_e[1][r]) - al * Dr;
-      have_ae = true;
+      if (wg == 0) {
+        const float2 o = sm.part[r];
+        al = a_acc + o.x;
+        Ei = (e_acc + o.y) - al * Dr;
+        sm.part[r] = make_float2(al, Ei);
+      }
+      named_bar_sync(1, 256);
+      if (wg == 1) {
+        const float2 o = sm.part[r];
+        al = o.x;
+        Ei = o.y;
+      }
     };
 
-    for (int u = 0;; ++u) {
-      const int t = 2 * u + wg;
-      if (t >= T2) break;
-      const bool phase_b = t >= TB;
-      if (!JVP && phase_b && !have_ae) combine();
-      // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
-      // failed wait keep looping so both warpgroups reach the named barrier.
+    // u counts this warpgroup's tiles (phase A, then phase B): sc_full and
+    // op_ready phases.  Warp-uniform decisions (tcgen05.ld/st are
+    // warp-collective); after a failed wait keep looping so both warpgroups
+    // reach the named barriers.
+    int u = 0;
+    for (int a = wg; a < TA; a += 2, ++u) {
       ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
       if (!ok) continue;
       tc_fence_after();
-      const int col0 = (phase_b ? t - TB : t) * BN;
-      const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
-      const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
-      if (!phase_b) {
+      const uint32_t sca = tbase + lane_off + 256 * wg;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {  // keys 32 g .. 32 g + 31 of the tile
         Chunk x0, x1;
-        load_chunk(sc, 0, x0);
-        load_chunk(sc, 1, x1);
+        load_chunk_a(sca, 2 * g, x0);
+        load_chunk_a(sca, 2 * g + 1, x1);
         tmem_wait_ld();
-        tc_fence_before();
-        warp_arrive(&sm.op_ready[wg]);  // the buffer is in registers
-        if (masked) {
-          phase_a_sums<true>(x0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
-          phase_a_sums<true>(x1, col0 + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
-        } else {
-          phase_a_sums<false>(x0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
-          phase_a_sums<false>(x1, col0 + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        if (g == 1) {
+          tc_fence_before();
+          warp_arrive(&sm.op_ready[wg]);  // the buffer is in registers
         }
-      } else if (JVP) {
+        const int cg = 2 * BN * a + BN * g;
+        if ((cg + BN > Nk) || (causal && cg + BN - 1 > row0)) {
+          phase_a_sums<true>(x0, cg, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+          phase_a_sums<true>(x1, cg + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        } else {
+          phase_a_sums<false>(x0, cg, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+          phase_a_sums<false>(x1, cg + 16, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        }
+      }
+    }
+    if (!JVP) combine();
+
+    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
+    for (int t = wg; t < T; t += 2, ++u) {
+      ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
+      if (!ok) continue;
+      tc_fence_after();
+      const int col0 = t * BN;
+      const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
+      if (JVP) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sv[16], fv[16];
@@ -421,7 +517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         warp_arrive(&sm.op_ready[wg]);
       }
     }
-    if (!have_ae) combine();  // a warpgroup with no phase-B tile (T = 1), or the JVP
+    if (JVP) combine();
 
     // Epilogue: warpgroup wg writes output columns [64 wg, 64 wg + 64).
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
