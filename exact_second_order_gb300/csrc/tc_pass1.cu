@@ -27,8 +27,12 @@
 // of F' and S (N = 64), dO [V; U_V]^T gives dP and G (N = 64), P [K | U_V]
 // gives B and the P U_V part of d~dO0 (N = 128), and dS [U_K | K] gives
 // Omega's dS U_K part and R' (N = 128).  Once a warpgroup has read a score
-// buffer it overwrites it with the bf16 A operands (P, P o d~P0, dS, P o F)
-// of the output GEMMs, which read A straight from TMEM.
+// buffer it overwrites the dP | G half with the bf16 A operands (P, P o d~P0,
+// dS, P o F) of the output GEMMs, which read A straight from TMEM.  The F' | S
+// half is free as soon as the warpgroup holds the tile in registers, so the
+// F'/S GEMMs of the tile two ahead run while it still computes; only the
+// dP/G GEMMs wait for the output GEMMs (the tensor pipe runs MMAs in issue
+// order, so they overwrite the operands after those have been read).
 //
 // The same kernel, instantiated with JVP = true, serves the attention JVP
 // along (U_Q, U_K, U_V): alpha and d~dO do not depend on dO, so with dO = 0
@@ -60,6 +64,7 @@ struct Smem1 {
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
   uint64_t sc_full[2];
+  uint64_t sf_free[2];   // per buffer: the warpgroup holds the tile in registers
   uint64_t op_ready[2];  // per buffer: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
@@ -69,13 +74,13 @@ struct Smem1 {
 // Score buffer layout (columns): F' at 0, S at 32, dP at 64, G at 96.
 constexpr uint32_t kColF = 0, kColS = 32, kColdP = 64, kColG = 96;
 // TMEM columns of the bf16 operand slots inside a score buffer, for the two
-// K = 16 steps (chunks) of the output GEMMs.  A warpgroup reads the whole
-// buffer (the JVP: S and F') before it writes any slot; the JVP's score
-// GEMMs never write the dP/G columns.
-__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 8 * c; }
-__device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return 16 + 8 * c; }
-__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 32 + 8 * c; }
-__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 48 + 8 * c; }
+// K = 16 steps (chunks) of the output GEMMs: the dP | G half.  A warpgroup
+// reads the whole buffer (the JVP: S and F') before it writes any slot; the
+// JVP's score GEMMs never write the dP/G columns.
+__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 64 + 8 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return 80 + 8 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 96 + 8 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 112 + 8 * c; }
 // Output accumulators.
 constexpr uint32_t kAccB = 0, kAccdO = 64, kAccW = 128, kAccR = 192;  // R' = dS K
 
@@ -150,11 +155,12 @@ __device__ __forceinline__ void p1_chunk_jvp(uint32_t sc, const uint32_t (&s)[16
 }
 
 // One 32-column tile, one row per thread: read all of S, F', dP, G (both
-// 16-column chunks; S and F' only for the JVP) with a single wait, form the
-// bf16 A operands of the output GEMMs, and hand the tile to the MMA issuer
-// once they are in TMEM.
+// 16-column chunks; S and F' only for the JVP) with a single wait and free
+// the F' | S half, form the bf16 A operands of the output GEMMs in the dP | G
+// half, and hand the tile to the MMA issuer once they are in TMEM.
 template <bool MASKED, bool JVP>
-__device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready, int col0, int jmax,
+__device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* sf_free, uint64_t* ready,
+                                        int col0, int jmax,
                                         float c1, float Lr2, float Dr, float tau, float& a_acc,
                                         float& e_acc) {
   if constexpr (JVP) {
@@ -164,6 +170,8 @@ __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready, int col0, 
     tmem_ld16(sc + kColS + 16, s1);
     tmem_ld16(sc + kColF + 16, f1);
     tmem_wait_ld();
+    tc_fence_before();
+    warp_arrive(sf_free);  // F' | S may be overwritten
     p1_chunk_jvp<MASKED, 0>(sc, s0, f0, col0, jmax, c1, Lr2, tau, a_acc);
     p1_chunk_jvp<MASKED, 1>(sc, s1, f1, col0, jmax, c1, Lr2, tau, a_acc);
     tmem_wait_st();
@@ -181,6 +189,8 @@ __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* ready, int col0, 
   tmem_ld16(sc + kColF + 16, f1);
   tmem_ld16(sc + kColG + 16, g1);
   tmem_wait_ld();
+  tc_fence_before();
+  warp_arrive(sf_free);  // F' | S may be overwritten
   p1_chunk<MASKED, 0>(sc, s0, dp0, f0, g0, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
   p1_chunk<MASKED, 1>(sc, s1, dp1, f1, g1, col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
   tmem_wait_st();
@@ -224,6 +234,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b], 4);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(&sm.sf_free[b], 4);
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
@@ -286,20 +297,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // One elected lane runs the whole schedule below: every wait and every
       // MMA, with no warp-wide broadcast between them (the MMA-warp time per
       // tile is what bounds this pass).
-      auto issue_scores = [&](int t) {
+      // Score GEMMs of tile t in two halves: F' | S, then dP | G (+ commit).
+      auto issue_sf = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
         const uint32_t sc = tbase + 256 + 128 * (t & 1);
-        {
 #pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint64_t o = 2 * kk;  // 32 bytes >> 4
-            const uint32_t acc = kk > 0;
-            mma_ss(sc + kColF, dq0 + o, dUK0 + so + o, idS64, acc);  // [F' | S] = Q [U_K; K]^T
-            mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);    // F' += U_Q K^T
-            if (!JVP) mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
-          }
-          mma_commit(&sm.sc_full[t & 1]);
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t o = 2 * kk;  // 32 bytes >> 4
+          mma_ss(sc + kColF, dq0 + o, dUK0 + so + o, idS64, kk > 0);  // [F' | S] = Q [U_K; K]^T
+          mma_ss(sc + kColF, duq0 + o, dK0 + so + o, idS32, 1);       // F' += U_Q K^T
         }
+      };
+      // Issued after the output GEMMs of tile t - 2, so the commit also
+      // covers their reads of the operand slots that tile t's warpgroup is
+      // about to overwrite (the JVP has no dP/G GEMMs, only the commit).
+      auto issue_pg = [&](int t) {
+        const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
+        const uint32_t sc = tbase + 256 + 128 * (t & 1);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16 && !JVP; ++kk) {
+          const uint64_t o = 2 * kk;
+          mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, kk > 0);  // [dP | G] = dO [V; U_V]^T
+        }
+        mma_commit(&sm.sc_full[t & 1]);
       };
       auto issue_outputs = [&](int t) {
         const int s = t % NST;
@@ -329,19 +349,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int t = 0; ok && t < 2 && t < T; ++t) {
           ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
           tc_fence_after();
-          if (ok) issue_scores(t);
+          if (ok) {
+            issue_sf(t);
+            issue_pg(t);
+          }
         }
         for (int t = 0; ok && t < T; ++t) {
-          ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+          const uint32_t ph = (t >> 1) & 1;  // phase of this warpgroup's barriers
+          if (t + 2 < T) {  // the warpgroup holds tile t in registers: F' | S of t + 2
+            ok = mbar_wait(&sm.sf_free[t & 1], ph, abort_flag, err) &&
+                 mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_sf(t + 2);
+          }
+          ok = mbar_wait(&sm.op_ready[t & 1], ph, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           issue_outputs(t);
-          if (t + 2 < T) {
-            ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
-            if (!ok) break;
-            tc_fence_after();
-            issue_scores(t + 2);
-          }
+          if (t + 2 < T) issue_pg(t + 2);  // after the output GEMMs have read the operands
         }
         mma_commit(&sm.out_full);  // every MMA issued above has finished
       }
@@ -375,9 +401,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (masked) {
-        p1_tile<true, JVP>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_tile<true, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau,
+                           a_acc, e_acc);
       } else {
-        p1_tile<false, JVP>(sc, &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau, a_acc, e_acc);
+        p1_tile<false, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau,
+                            a_acc, e_acc);
       }
     }
 
