@@ -84,41 +84,39 @@ __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 112 + 8 * 
 // Output accumulators.
 constexpr uint32_t kAccB = 0, kAccdO = 64, kAccW = 128, kAccR = 192;  // R' = dS K
 
-// One 16-column chunk of a score buffer, one row per thread: read S, dP, F',
-// G from TMEM, form P = exp(S - L) and the five bf16 A operands of the
-// output GEMMs, add to the row sums alpha and E0, and write the operands back
-// over consumed columns.
+// One 16-column chunk of a score buffer, one row per thread: from S, dP, F',
+// G form P = exp(S - L) and the four bf16 A operands of the output GEMMs, add
+// to the row sums alpha and E0 (kept as two partial sums, even and odd
+// columns), and write the operands to the chunk's slots.  Two columns per
+// step in the paired fp32 instructions.
 template <bool MASKED, int C>
 __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
                                          const uint32_t (&dp)[16], const uint32_t (&f)[16],
                                          const uint32_t (&g)[16], int col0, int jmax, float c1,
-                                         float Lr2, float Dr, float tau, float& a_acc,
-                                         float& e_acc) {
+                                         float Lr2, float Dr, float tau, float2& a_acc,
+                                         float2& e_acc) {
   uint32_t oP[8], oPdPt[8], odS[8], oPF[8];
   const int jbase = col0 + 16 * C;
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
+  const float2 nD = make_float2(-Dr, -Dr), tau2 = make_float2(tau, tau);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    float pv[2], pdpt[2], ds[2], pf[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = e + h;
-      float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
-      if (MASKED && jbase + j > jmax) p = 0.f;
-      const float dpv = u2f(dp[j]);
-      const float x = dpv - Dr;
-      const float ft = u2f(f[j]) * tau;
-      const float dpt0 = fmaf(ft, x, u2f(g[j]));
-      pv[h] = p;
-      pdpt[h] = p * dpt0;
-      ds[h] = p * x;
-      pf[h] = p * ft;
-      a_acc += pf[h];
-      e_acc += pdpt[h];
+    const float2 t = ffma2(f2(s[e], s[e + 1]), c12, nL);
+    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (MASKED) {
+      if (jbase + e > jmax) p.x = 0.f;
+      if (jbase + e + 1 > jmax) p.y = 0.f;
     }
-    oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-    oPdPt[e >> 1] = pack_bf16x2(pdpt[0], pdpt[1]);
-    odS[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-    oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
+    const float2 x = fadd2(f2(dp[e], dp[e + 1]), nD);           // dP - D
+    const float2 ft = fmul2(f2(f[e], f[e + 1]), tau2);           // F = tau F'
+    const float2 dpt0 = ffma2(ft, x, f2(g[e], g[e + 1]));       // d~P0 = F o (dP - D) + G
+    const float2 pdpt = fmul2(p, dpt0), ds = fmul2(p, x), pf = fmul2(p, ft);
+    a_acc = fadd2(a_acc, pf);
+    e_acc = fadd2(e_acc, pdpt);
+    oP[e >> 1] = pack_bf16x2(p.x, p.y);
+    oPdPt[e >> 1] = pack_bf16x2(pdpt.x, pdpt.y);
+    odS[e >> 1] = pack_bf16x2(ds.x, ds.y);
+    oPF[e >> 1] = pack_bf16x2(pf.x, pf.y);
   }
   tmem_st8(sc + slot_P(C), oP);
   tmem_st8(sc + slot_PdPt(C), oPdPt);
@@ -128,27 +126,27 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
 
 // The attention JVP's version of p1_chunk (no dO: dP = G = 0): P and
 // P o F only, and the row sum alpha = L'.  The slots of P and P o F lie in
-// S, F' or the dP/G columns, which the JVP's score GEMMs never write.
+// the dP/G columns, which the JVP's score GEMMs never write.
 template <bool MASKED, int C>
 __device__ __forceinline__ void p1_chunk_jvp(uint32_t sc, const uint32_t (&s)[16],
                                              const uint32_t (&f)[16], int col0, int jmax,
-                                             float c1, float Lr2, float tau, float& a_acc) {
+                                             float c1, float Lr2, float tau, float2& a_acc) {
   uint32_t oP[8], oPF[8];
   const int jbase = col0 + 16 * C;
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
+  const float2 tau2 = make_float2(tau, tau);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    float pv[2], pf[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = e + h;
-      float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
-      if (MASKED && jbase + j > jmax) p = 0.f;
-      pv[h] = p;
-      pf[h] = p * (u2f(f[j]) * tau);
-      a_acc += pf[h];
+    const float2 t = ffma2(f2(s[e], s[e + 1]), c12, nL);
+    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (MASKED) {
+      if (jbase + e > jmax) p.x = 0.f;
+      if (jbase + e + 1 > jmax) p.y = 0.f;
     }
-    oP[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-    oPF[e >> 1] = pack_bf16x2(pf[0], pf[1]);
+    const float2 pf = fmul2(p, fmul2(f2(f[e], f[e + 1]), tau2));
+    a_acc = fadd2(a_acc, pf);
+    oP[e >> 1] = pack_bf16x2(p.x, p.y);
+    oPF[e >> 1] = pack_bf16x2(pf.x, pf.y);
   }
   tmem_st8(sc + slot_P(C), oP);
   tmem_st8(sc + slot_PF(C), oPF);
@@ -161,8 +159,8 @@ __device__ __forceinline__ void p1_chunk_jvp(uint32_t sc, const uint32_t (&s)[16
 template <bool MASKED, bool JVP>
 __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* sf_free, uint64_t* ready,
                                         int col0, int jmax,
-                                        float c1, float Lr2, float Dr, float tau, float& a_acc,
-                                        float& e_acc) {
+                                        float c1, float Lr2, float Dr, float tau, float2& a_acc,
+                                        float2& e_acc) {
   if constexpr (JVP) {
     uint32_t s0[16], f0[16], s1[16], f1[16];
     tmem_ld16(sc + kColS, s0);
@@ -384,7 +382,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
     const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
-    float a_acc = 0.f, e_acc = 0.f;
+    float2 a_acc = make_float2(0.f, 0.f), e_acc = make_float2(0.f, 0.f);
     bool ok = true;
     const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
 
@@ -411,8 +409,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // Epilogue: combine the two warpgroups' row sums, then the affine
     // correction; warpgroup wg writes output columns [32 wg, 32 wg + 32).
-    sm.part_a[wg][r] = a_acc;
-    sm.part_e[wg][r] = e_acc;
+    sm.part_a[wg][r] = a_acc.x + a_acc.y;
+    sm.part_e[wg][r] = e_acc.x + e_acc.y;
     named_bar_sync(1, 256);
     const float al = sm.part_a[0][r] + sm.part_a[1][r];
     const float E0 = sm.part_e[0][r] + sm.part_e[1][r];
