@@ -107,19 +107,29 @@ __device__ __forceinline__ void load_chunk_a(uint32_t sc, int c, Chunk& x) {
   tmem_ld16(sc + kAColG + 16 * c, x.g);
 }
 
+// The element-wise functions below take two columns per step in the paired
+// fp32 instructions; the row sums are kept as two partial sums (even and odd
+// columns).
+
 // Phase A on one chunk: the row sums alpha += P F and E0 += P d~P0.
 template <bool MASKED>
 __device__ __forceinline__ void phase_a_sums(const Chunk& x, int jbase, int jmax, float c1,
-                                             float Lr2, float Dr, float tau, float& a_acc,
-                                             float& e_acc) {
+                                             float Lr2, float Dr, float tau, float2& a_acc,
+                                             float2& e_acc) {
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
+  const float2 nD = make_float2(-Dr, -Dr), tau2 = make_float2(tau, tau);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float p = ex2_approx(fmaf(u2f(x.s[j]), c1, -Lr2));
-    if (MASKED && jbase + j > jmax) p = 0.f;
-    const float ft = u2f(x.f[j]) * tau;
-    const float dpt0 = fmaf(ft, u2f(x.dp[j]) - Dr, u2f(x.g[j]));
-    a_acc = fmaf(p, ft, a_acc);
-    e_acc = fmaf(p, dpt0, e_acc);
+  for (int e = 0; e < 16; e += 2) {
+    const float2 t = ffma2(f2(x.s[e], x.s[e + 1]), c12, nL);
+    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (MASKED) {
+      if (jbase + e > jmax) p.x = 0.f;
+      if (jbase + e + 1 > jmax) p.y = 0.f;
+    }
+    const float2 ft = fmul2(f2(x.f[e], x.f[e + 1]), tau2);
+    const float2 dpt0 = ffma2(ft, fadd2(f2(x.dp[e], x.dp[e + 1]), nD), f2(x.g[e], x.g[e + 1]));
+    a_acc = ffma2(p, ft, a_acc);
+    e_acc = ffma2(p, dpt0, e_acc);
   }
 }
 
@@ -128,22 +138,22 @@ __device__ __forceinline__ void phase_a_sums(const Chunk& x, int jbase, int jmax
 template <bool MASKED, int C>
 __device__ __forceinline__ void jvp_chunk(uint32_t sc, const uint32_t (&s)[16],
                                           const uint32_t (&f)[16], int col0, int jmax, float c1,
-                                          float Lr2, float tau, float& a_acc) {
+                                          float Lr2, float tau, float2& a_acc) {
   uint32_t op[8], opf[8];
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
+  const float2 tau2 = make_float2(tau, tau);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    float vp[2], vpf[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = e + h;
-      float p = ex2_approx(fmaf(u2f(s[j]), c1, -Lr2));
-      if (MASKED && col0 + 16 * C + j > jmax) p = 0.f;
-      vp[h] = p;
-      vpf[h] = p * (u2f(f[j]) * tau);
-      a_acc += vpf[h];
+    const float2 t = ffma2(f2(s[e], s[e + 1]), c12, nL);
+    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (MASKED) {
+      if (col0 + 16 * C + e > jmax) p.x = 0.f;
+      if (col0 + 16 * C + e + 1 > jmax) p.y = 0.f;
     }
-    op[e >> 1] = pack_bf16x2(vp[0], vp[1]);
-    opf[e >> 1] = pack_bf16x2(vpf[0], vpf[1]);
+    const float2 pf = fmul2(p, fmul2(f2(f[e], f[e + 1]), tau2));
+    a_acc = fadd2(a_acc, pf);
+    op[e >> 1] = pack_bf16x2(p.x, p.y);
+    opf[e >> 1] = pack_bf16x2(pf.x, pf.y);
   }
   tmem_st8(sc + slot_P(C), op);
   tmem_st8(sc + slot_W(C), opf);
@@ -155,27 +165,28 @@ __device__ __forceinline__ void phase_b_chunk(uint32_t sc, const Chunk& x, int c
                                               float c1, float Lr2, float Dr, float tau, float al,
                                               float Ei) {
   uint32_t odst[8], ods[8], op[8], ow[8];
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
+  const float2 nD = make_float2(-Dr, -Dr), tau2 = make_float2(tau, tau);
+  const float2 nal = make_float2(-al, -al), nEi = make_float2(-Ei, -Ei);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    float vdst[2], vds[2], vp[2], vw[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = e + h;
-      float p = ex2_approx(fmaf(u2f(x.s[j]), c1, -Lr2));
-      if (MASKED && col0 + 16 * C + j > jmax) p = 0.f;
-      const float dpv = u2f(x.dp[j]);
-      const float xx = dpv - Dr;
-      const float ft = u2f(x.f[j]) * tau;
-      const float dpt0 = fmaf(ft, xx, u2f(x.g[j]));
-      vdst[h] = p * (dpt0 - fmaf(al, dpv, Ei));
-      vds[h] = p * xx;
-      vp[h] = p;
-      vw[h] = p * (ft - al);
+    const float2 t = ffma2(f2(x.s[e], x.s[e + 1]), c12, nL);
+    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (MASKED) {
+      if (col0 + 16 * C + e > jmax) p.x = 0.f;
+      if (col0 + 16 * C + e + 1 > jmax) p.y = 0.f;
     }
-    odst[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
-    ods[e >> 1] = pack_bf16x2(vds[0], vds[1]);
-    op[e >> 1] = pack_bf16x2(vp[0], vp[1]);
-    ow[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+    const float2 dpv = f2(x.dp[e], x.dp[e + 1]);
+    const float2 xx = fadd2(dpv, nD);                                  // dP - D
+    const float2 ft = fmul2(f2(x.f[e], x.f[e + 1]), tau2);             // F = tau F'
+    const float2 dpt0 = ffma2(ft, xx, f2(x.g[e], x.g[e + 1]));        // d~P0
+    const float2 vdst = fmul2(p, fadd2(dpt0, ffma2(nal, dpv, nEi)));  // P (d~P0 - alpha dP - E)
+    const float2 vds = fmul2(p, xx);
+    const float2 vw = fmul2(p, fadd2(ft, nal));                        // P (F - alpha)
+    odst[e >> 1] = pack_bf16x2(vdst.x, vdst.y);
+    ods[e >> 1] = pack_bf16x2(vds.x, vds.y);
+    op[e >> 1] = pack_bf16x2(p.x, p.y);
+    ow[e >> 1] = pack_bf16x2(vw.x, vw.y);
   }
   tmem_st8(sc + slot_dSt(C), odst);
   tmem_st8(sc + slot_dS(C), ods);
@@ -413,19 +424,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
     const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
-    float a_acc = 0.f, e_acc = 0.f, al = 0.f, Ei = 0.f;
+    float2 a_acc = make_float2(0.f, 0.f), e_acc = make_float2(0.f, 0.f);
+    float al = 0.f, Ei = 0.f;
     bool ok = true;
     const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
     // Both warpgroups' partial row sums meet here (each warpgroup passes
     // exactly once, named barrier 1): warpgroup 1 hands its sums over,
     // warpgroup 0 forms alpha and E = E0 - alpha D and hands them back.
     auto combine = [&]() {
-      if (wg == 1) sm.part[r] = make_float2(a_acc, e_acc);
+      const float a_own = a_acc.x + a_acc.y, e_own = e_acc.x + e_acc.y;
+      if (wg == 1) sm.part[r] = make_float2(a_own, e_own);
       named_bar_sync(1, 256);
       if (wg == 0) {
         const float2 o = sm.part[r];
-        al = a_acc + o.x;
-        Ei = (e_acc + o.y) - al * Dr;
+        al = a_own + o.x;
+        Ei = (e_own + o.y) - al * Dr;
         sm.part[r] = make_float2(al, Ei);
       }
       named_bar_sync(1, 256);

@@ -45,7 +45,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct SmemW2 {
   alignas(1024) uint8_t kb[4][2][HALF_BLOCK];         // K, U_K, V, U_V (resident) x halves
   alignas(1024) uint8_t st[NST][2][3][HALF_TILE];     // [stage][half][Q, U_Q, dO]
-  float4 scal[2][2][16];  // per warpgroup, double-buffered: (L log2 e, D, alpha, alpha D + E)
+  float4 scal[2][2][16];  // per warpgroup, double-buffered row scalars (see stage())
   uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
@@ -94,26 +94,28 @@ __device__ __forceinline__ bool p2w_half(uint32_t sc, uint32_t opb, int wg, cons
   tc_fence_before();
   warp_arrive(&sm.pg_free);
   uint32_t ods[8], odst[8], ow[8];
+  const float2 c12 = make_float2(c1, c1), tau2 = make_float2(tau, tau);
+  // Two query rows per step in the paired fp32 instructions; scal holds, per
+  // pair of rows, (-L log2 e, -D) and (-alpha, -(alpha D + E)) of both.  With
+  // X = dP - D:  F o X + G - alpha dP - E = X (F - alpha) + G - (alpha D + E).
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    float vds[2], vdst[2], vw[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = e + h;
-      // (L log2 e, D, alpha, alpha D + E) of query row ibase + i.  With
-      // X = dP - D:  F o X + G - alpha dP - E = X (F - alpha) + G - (alpha D + E).
-      const float4 rs = scal[i];
-      float p = ex2_approx(fmaf(u2f(s[i]), c1, -rs.x));
-      if (MASKED && ibase + i < gj) p = 0.f;
-      const float x = u2f(dp[i]) - rs.y;
-      const float w0 = fmaf(u2f(f[i]), tau, -rs.z);  // F - alpha
-      vds[h] = p * x;
-      vdst[h] = p * (fmaf(x, w0, u2f(g[i])) - rs.w);
-      vw[h] = p * w0;
+    const float4 sa = scal[e], sb = scal[e + 1];
+    const float2 tt = ffma2(f2(s[e], s[e + 1]), c12, make_float2(sa.x, sa.y));
+    float2 p = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
+    if (MASKED) {
+      if (ibase + e < gj) p.x = 0.f;
+      if (ibase + e + 1 < gj) p.y = 0.f;
     }
-    ods[e >> 1] = pack_bf16x2(vds[0], vds[1]);
-    odst[e >> 1] = pack_bf16x2(vdst[0], vdst[1]);
-    ow[e >> 1] = pack_bf16x2(vw[0], vw[1]);
+    const float2 x = fadd2(f2(dp[e], dp[e + 1]), make_float2(sa.z, sa.w));       // dP - D
+    const float2 w0 = ffma2(f2(f[e], f[e + 1]), tau2, make_float2(sb.x, sb.y));  // F - alpha
+    const float2 vds = fmul2(p, x);
+    const float2 vdst =
+        fmul2(p, fadd2(ffma2(x, w0, f2(g[e], g[e + 1])), make_float2(sb.z, sb.w)));
+    const float2 vw = fmul2(p, w0);
+    ods[e >> 1] = pack_bf16x2(vds.x, vds.y);
+    odst[e >> 1] = pack_bf16x2(vdst.x, vdst.y);
+    ow[e >> 1] = pack_bf16x2(vw.x, vw.y);
   }
   if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
   tc_fence_after();
@@ -338,13 +340,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return v;
     };
     // Only the loads are issued in load_scalars; the values are first used
-    // here, at the end of the tile: (L log2 e, D, alpha, alpha D + E).
-    auto stage = [](float4 v) {
-      return make_float4(v.x * kLog2e, v.y, v.z, fmaf(v.z, v.y, v.w));
+    // here, at the end of the tile, negated and interleaved by pairs of rows
+    // (lane = row): (-L log2 e, -D) of rows 2m, 2m + 1 in float4 2m,
+    // (-alpha, -(alpha D + E)) in float4 2m + 1.
+    auto stage = [&](float4* dst, float4 v) {
+      float* pr = reinterpret_cast<float*>(dst + (lane & ~1)) + (lane & 1);
+      pr[0] = -(v.x * kLog2e);
+      pr[2] = -v.y;
+      pr[4] = -v.z;
+      pr[6] = -fmaf(v.z, v.y, v.w);
     };
     if (loader) {
       const float4 v = load_scalars(0);
-      if (lane < 16) sm.scal[wg][0][lane] = stage(v);
+      if (lane < 16) stage(sm.scal[wg][0], v);
     }
     int tq = 0;  // tile of the current query head
     for (int t = 0; t < T; ++t) {
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         else
           ok = p2w_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
       }
-      if (loader && lane < 16) sm.scal[wg][(t + 1) & 1][lane] = stage(next);
+      if (loader && lane < 16) stage(sm.scal[wg][(t + 1) & 1], next);
       if (++tq == Tq) tq = 0;
     }
 
