@@ -1,23 +1,26 @@
 // Row state of the attention backward-over-backward on sm_103a tensor cores:
 // O = P V, L = logsumexp(tau Q K^T) and D_i = dO_i . O_i for bf16 inputs,
-// head dim 64 ("FlashAttention 的反向传播设计" blog, sections 一 and 二; D as
-// in "FlashBoB" paper notes, 关键设计 1).
+// head dim 64 or 128 ("FlashAttention 的反向传播设计" blog, sections 一 and
+// 二; D as in "FlashBoB" paper notes, 关键设计 1).
 //
 // Two phases inside one CTA of 128 query rows, both streaming the same key
-// tiles of 32 rows:
-//   phase A: S = Q K^T on the tensor cores; the elementwise warpgroups keep
-//            a running row max m and sum l of exp2(S tau log2 e - m), which
-//            gives L at the end of the phase;
+// tiles (128 keys at d = 64, 64 at d = 128):
+//   phase A: S = Q K^T on the tensor cores (one N = 128 or 64 MMA per K
+//            step); the elementwise warpgroups keep a running row max m and
+//            sum l of exp2(S tau log2 e - m), which gives L at the end;
 //   phase B: S = Q K^T again, P = exp(S - L) (already normalised, so the
-//            accumulator never needs rescaling) goes to TMEM as bf16 and
-//            O += P V runs with A read from TMEM.
+//            accumulator never needs rescaling) goes to TMEM as bf16 over
+//            the consumed score columns and O += P V runs with A read from
+//            TMEM.
 // The epilogue writes O and the row scalars; D comes from dO (bf16, read
 // from global memory) dotted with the fp32 O.
 //
 // 320 threads: warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps 2-5
-// and 6-9 elementwise warpgroups on alternate tiles.  TMEM: [0,DH) O,
-// [DH,DH+32) and [DH+32,DH+64) score buffers.  Head dim 64 or 128: a row of
-// 128 columns is two 64-column boxes in the 128-byte swizzle.
+// and 6-9 elementwise warpgroups on alternate tiles.  TMEM: [0,DH) O, then
+// three score buffers of one tile each; the score GEMMs of tile t + 3 go
+// into tile t's buffer as soon as its warpgroup has finished with it, so a
+// warpgroup finds its next tile's scores ready.  A row of 128 columns is
+// two 64-column boxes in the 128-byte swizzle.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -26,18 +29,19 @@ namespace {
 using namespace tc;
 
 constexpr int BM = kTcRows;
-constexpr int BN = kTcStream;
 constexpr int NTHREADS = 320;
+constexpr int NBUF = 3;  // score buffers
 constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 128 rows x 64 columns bf16
-constexpr uint32_t HALF_TILE = BN * 64 * 2;   // 32 rows x 64 columns bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int DH>
 struct PrepCfg {
   static constexpr int kHalves = DH / 64;
-  static constexpr int kStages = DH == 64 ? 6 : 4;
-  static constexpr uint32_t kTmemCols = DH == 64 ? 128 : 256;  // O + two 32-column buffers
+  static constexpr int kBN = DH == 64 ? 128 : 64;          // keys per streamed tile
+  static constexpr int kStages = 5;
+  static constexpr uint32_t kHalfTile = kBN * 64 * 2;       // kBN rows x 64 columns bf16
+  static_assert(DH + NBUF * kBN <= 512, "TMEM columns");
 };
 
 template <int DH>
@@ -45,19 +49,70 @@ struct Smem0 {
   static constexpr int NST = PrepCfg<DH>::kStages;
   static constexpr int NH = PrepCfg<DH>::kHalves;
   alignas(1024) uint8_t q[NH][HALF_BLOCK];
-  alignas(1024) uint8_t kv[NST][2][NH][HALF_TILE];  // [stage][K, V][half]
+  alignas(1024) uint8_t kv[NST][2][NH][PrepCfg<DH>::kHalfTile];  // [stage][K, V][half]
   float part_m[2][BM];
   float part_l[2][BM];
   float part_d[2][BM];
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
-  uint64_t sc_full[2];
-  uint64_t op_ready[2];
+  uint64_t sc_full[NBUF];
+  uint64_t op_ready[NBUF];
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Phase A on 64 columns of a tile (one row per thread): fold them into the
+// running (m, l) of exp2(S c1 - m).  Invisible columns (past Nk or, causal,
+// past the row) do not count.
+template <bool MASKED>
+__device__ __forceinline__ void prep_rowsum(const uint32_t (&s)[4][16], int jbase, int jmax,
+                                            float c1, float& m, float& l) {
+  float mr = -INFINITY;  // max of the raw scores (c1 > 0, so max(S) c1 = max(S c1) exactly)
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (!MASKED || jbase + 16 * q + j <= jmax) mr = fmaxf(mr, u2f(s[q][j]));
+  const float mx = fmaxf(m, mr * c1);
+  if (mx == -INFINITY) return;  // nothing visible yet
+  const float2 c12 = make_float2(c1, c1), nmx = make_float2(-mx, -mx);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const float2 t = ffma2(f2(s[q][j], s[q][j + 1]), c12, nmx);
+      float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+      if (MASKED) {
+        if (jbase + 16 * q + j > jmax) e.x = 0.f;
+        if (jbase + 16 * q + j + 1 > jmax) e.y = 0.f;
+      }
+      acc = fadd2(acc, e);
+    }
+  l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mx)) + (acc.x + acc.y);
+  m = mx;
+}
+
+// Phase B on 64 columns: P = exp2(S c1 - L2) as bf16 pairs (32 registers).
+template <bool MASKED>
+__device__ __forceinline__ void prep_p(const uint32_t (&s)[4][16], int jbase, int jmax, float c1,
+                                       float L2, uint32_t (&pk)[4][8]) {
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-L2, -L2);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const float2 t = ffma2(f2(s[q][e], s[q][e + 1]), c12, nL);
+      float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+      if (MASKED) {
+        if (jbase + 16 * q + e > jmax) p.x = 0.f;
+        if (jbase + 16 * q + e + 1 > jmax) p.y = 0.f;
+      }
+      pk[q][e >> 1] = pack_bf16x2(p.x, p.y);
+    }
+}
 
 template <int DH>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -68,6 +123,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   constexpr int NST = PrepCfg<DH>::kStages;
   constexpr int NH = PrepCfg<DH>::kHalves;
+  constexpr int BN = PrepCfg<DH>::kBN;
+  constexpr uint32_t HT = PrepCfg<DH>::kHalfTile;
   Smem0<DH>& sm = *reinterpret_cast<Smem0<DH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -85,7 +142,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b], 4);  // one arrive per elementwise warp
     }
@@ -93,7 +150,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     sm.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&sm.tmem_base, PrepCfg<DH>::kTmemCols);
+  if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -111,7 +168,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool phase_b = t >= T;
         const int kt = phase_b ? t - T : t;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
-        mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * NH * HALF_TILE);
+        mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * NH * HT);
         for (int h = 0; h < NH; ++h) {
           tma_load_3d(sm.kv[s][0][h], &mK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
           if (phase_b) tma_load_3d(sm.kv[s][1][h], &mV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
@@ -128,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t idO = idesc_bf16(BM, DH, true);
       auto issue_scores = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + DH + 32 * (t & 1);
+        const uint32_t sc = tbase + DH + BN * (t % NBUF);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int h = kk >> 2;  // 64-column half of the head dim
@@ -137,39 +194,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
                  kk > 0);
         }
-        mma_commit(&sm.sc_full[t & 1]);
+        mma_commit(&sm.sc_full[t % NBUF]);
         if (t < T) mma_commit(&sm.kv_empty[s]);  // phase A reads the stage only here
       };
       auto issue_pv = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + DH + 32 * (t & 1);
+        const uint32_t sc = tbase + DH + BN * (t % NBUF);
         // V as an N = DH MN-major operand: its second 64-column half (d = 128)
-        // sits HALF_TILE bytes after the first.
+        // sits HT bytes after the first.
         const uint32_t bv = smem_u32(sm.kv[s][1][0]);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HALF_TILE, 1024), idO,
+        for (int c = 0; c < BN / 16; ++c)
+          mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HT, 1024), idO,
                  (t > T || c > 0));
         mma_commit(&sm.kv_empty[s]);
       };
       if (elect_one()) {
         bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
         tc_fence_after();
-        for (int t = 0; ok && t < 2 && t < T2; ++t) {
+        for (int t = 0; ok && t < NBUF && t < T2; ++t) {
           ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
           tc_fence_after();
           if (ok) issue_scores(t);
         }
         for (int t = 0; ok && t < T2; ++t) {
-          ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+          // Tile t's warpgroup is done with buffer t mod NBUF (phase B: P is in it).
+          ok = mbar_wait(&sm.op_ready[t % NBUF], (t / NBUF) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           if (t >= T) issue_pv(t);
-          if (t + 2 < T2) {
-            ok = mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
+          if (t + NBUF < T2) {
+            const int tn = t + NBUF;
+            ok = mbar_wait(&sm.kv_full[tn % NST], (tn / NST) & 1, abort_flag, err);
             if (!ok) break;
             tc_fence_after();
-            issue_scores(t + 2);
+            issue_scores(tn);
           }
         }
         mma_commit(&sm.out_full);
@@ -184,7 +243,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int gr = row0 + r;
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
-    const uint32_t sc = tbase + lane_off + DH + 32 * wg;
+    const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;  // visible keys j <= jmax
     float m = -INFINITY, l = 0.f, L2 = 0.f;
     bool ok = true, have_L = false;
     // Both warpgroups have finished phase A: combine their (m, l) into L.
@@ -195,9 +254,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       named_bar_sync(1, 256);
       const float m0 = sm.part_m[0][r], m1 = sm.part_m[1][r];
       const float mm = fmaxf(m0, m1);  // finite: tile 0 always has a valid column
-      const float ll =
-          sm.part_l[0][r] * ex2_approx(m0 - mm) + sm.part_l[1][r] * ex2_approx(m1 - mm);
-      L2 = mm + __log2f(ll);
+      const float l0 = m0 == -INFINITY ? 0.f : sm.part_l[0][r] * ex2_approx(m0 - mm);
+      const float l1 = m1 == -INFINITY ? 0.f : sm.part_l[1][r] * ex2_approx(m1 - mm);
+      L2 = mm + __log2f(l0 + l1);
       have_L = true;
     };
 
@@ -206,44 +265,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (t >= T2) break;
       const bool phase_b = t >= T;
       if (phase_b && !have_L) combine();
-      ok = ok && mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
-      if (ok) {
-        tc_fence_after();
-        const int col0 = (phase_b ? t - T : t) * BN;
-        const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;  // visible keys j <= jmax
+      ok = ok && mbar_wait_warp(&sm.sc_full[t % NBUF], (t / NBUF) & 1, abort_flag, err);
+      if (!ok) continue;
+      tc_fence_after();
+      const uint32_t sc = tbase + lane_off + DH + BN * (t % NBUF);
+      const int col0 = (phase_b ? t - T : t) * BN;
+      // Only tiles that reach past Nk or past the block's first row need the mask.
+      const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t s[16];
-          tmem_ld16(sc + 16 * c, s);
-          tmem_wait_ld();
-          if (!phase_b) {
-            float mx = m;
+      for (int g = 0; g < BN / 64; ++g) {  // 64 columns at a time
+        uint32_t s[4][16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (col0 + 16 * c + j <= jmax) mx = fmaxf(mx, u2f(s[j]) * c1);
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (col0 + 16 * c + j <= jmax) acc += ex2_approx(u2f(s[j]) * c1 - mx);
-            // A chunk may hold no visible column (mx stays m, acc = 0).
-            l = (mx == -INFINITY) ? l : (m == -INFINITY ? acc : l * ex2_approx(m - mx) + acc);
-            m = mx;
-          } else {
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              float p0 = ex2_approx(fmaf(u2f(s[e]), c1, -L2));
-              float p1 = ex2_approx(fmaf(u2f(s[e + 1]), c1, -L2));
-              if (col0 + 16 * c + e > jmax) p0 = 0.f;
-              if (col0 + 16 * c + e + 1 > jmax) p1 = 0.f;
-              pk[e >> 1] = pack_bf16x2(p0, p1);
-            }
-            tmem_st8(sc + 8 * c, pk);  // P chunk c over consumed score columns
+        for (int q = 0; q < 4; ++q) tmem_ld16(sc + 64 * g + 16 * q, s[q]);
+        tmem_wait_ld();
+        const int jb = col0 + 64 * g;
+        if (!phase_b) {
+          if (g == BN / 64 - 1) {  // the whole buffer is in registers
+            tc_fence_before();
+            warp_arrive(&sm.op_ready[t % NBUF]);
           }
+          if (masked) prep_rowsum<true>(s, jb, jmax, c1, m, l);
+          else prep_rowsum<false>(s, jb, jmax, c1, m, l);
+        } else {
+          uint32_t pk[4][8];
+          if (masked) prep_p<true>(s, jb, jmax, c1, L2, pk);
+          else prep_p<false>(s, jb, jmax, c1, L2, pk);
+          // P of columns 16c..16c+15 goes to columns 8c..8c+7, already read.
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_st8(sc + 32 * g + 8 * q, pk[q]);
         }
-        if (phase_b) tmem_wait_st();
+      }
+      if (phase_b) {
+        tmem_wait_st();
         tc_fence_before();
-        warp_arrive(&sm.op_ready[wg]);
+        warp_arrive(&sm.op_ready[t % NBUF]);
       }
     }
     if (!have_L) combine();  // a warpgroup with no phase-B tile (T = 1)
@@ -294,7 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, PrepCfg<DH>::kTmemCols);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -304,8 +359,8 @@ cudaError_t launch_prep(const PrepArgs& a) {
   const int BHkv = a.B * a.Hkv;
   CUtensorMap mq, mk, mv;
   cudaError_t e = tc::make_map_bf16(&mq, a.Q, BH, a.Nq, kTcRows, DH);
-  if (e == cudaSuccess) e = tc::make_map_bf16(&mk, a.K, BHkv, a.Nk, kTcStream, DH);
-  if (e == cudaSuccess) e = tc::make_map_bf16(&mv, a.V, BHkv, a.Nk, kTcStream, DH);
+  if (e == cudaSuccess) e = tc::make_map_bf16(&mk, a.K, BHkv, a.Nk, PrepCfg<DH>::kBN, DH);
+  if (e == cudaSuccess) e = tc::make_map_bf16(&mv, a.V, BHkv, a.Nk, PrepCfg<DH>::kBN, DH);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem0<DH>) + 1024;
   e = cudaFuncSetAttribute(tc_prep_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
