@@ -63,9 +63,9 @@ struct Smem1 {
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
-  uint64_t sc_full[2];
+  uint64_t sc_full[3];
   uint64_t sf_free[2];   // per buffer: the warpgroup holds the tile in registers
-  uint64_t op_ready[2];  // per buffer: one arrive per elementwise warp
+  uint64_t op_ready[3];  // per buffer: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -81,6 +81,16 @@ __device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 64 + 8 * c;
 __device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return 80 + 8 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 96 + 8 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 112 + 8 * c; }
+// Score buffers: the BoB has two (tile t in buffer t mod 2 at column
+// 256 + 128 (t mod 2)); the JVP, which needs only the d~dO0 accumulator,
+// has three (tile t in buffer t mod 3 at column 128 + 128 (t mod 3)), so the
+// score GEMMs of tile t + 3 can run before the warpgroup of tile t + 2 starts.
+template <bool JVP>
+__device__ __forceinline__ int p1_buf(int t) { return JVP ? t % 3 : t & 1; }
+template <bool JVP>
+__device__ __forceinline__ uint32_t p1_buf_col(int t) {
+  return JVP ? 128 + 128 * (t % 3) : 256 + 128 * (t & 1);
+}
 // Output accumulators.
 constexpr uint32_t kAccB = 0, kAccdO = 64, kAccW = 128, kAccR = 192;  // R' = dS K
 
@@ -168,8 +178,6 @@ __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* sf_free, uint64_t
     tmem_ld16(sc + kColS + 16, s1);
     tmem_ld16(sc + kColF + 16, f1);
     tmem_wait_ld();
-    tc_fence_before();
-    warp_arrive(sf_free);  // F' | S may be overwritten
     p1_chunk_jvp<MASKED, 0>(sc, s0, f0, col0, jmax, c1, Lr2, tau, a_acc);
     p1_chunk_jvp<MASKED, 1>(sc, s1, f1, col0, jmax, c1, Lr2, tau, a_acc);
     tmem_wait_st();
@@ -228,7 +236,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b], 4);
     }
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Score GEMMs of tile t in two halves: F' | S, then dP | G (+ commit).
       auto issue_sf = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        const uint32_t sc = tbase + p1_buf_col<JVP>(t);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t o = 2 * kk;  // 32 bytes >> 4
@@ -311,18 +319,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // about to overwrite (the JVP has no dP/G GEMMs, only the commit).
       auto issue_pg = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        const uint32_t sc = tbase + p1_buf_col<JVP>(t);
 #pragma unroll
         for (int kk = 0; kk < DH / 16 && !JVP; ++kk) {
           const uint64_t o = 2 * kk;
           mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, kk > 0);  // [dP | G] = dO [V; U_V]^T
         }
-        mma_commit(&sm.sc_full[t & 1]);
+        mma_commit(&sm.sc_full[p1_buf<JVP>(t)]);
       };
       auto issue_outputs = [&](int t) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + 256 + 128 * (t & 1);
+        const uint32_t sc = tbase + p1_buf_col<JVP>(t);
         {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -344,7 +352,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (elect_one()) {
         bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
         tc_fence_after();
-        for (int t = 0; ok && t < 2 && t < T; ++t) {
+        constexpr int NB = JVP ? 3 : 2;  // score buffers
+        for (int t = 0; ok && t < NB && t < T; ++t) {
           ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
           tc_fence_after();
           if (ok) {
@@ -352,7 +361,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             issue_pg(t);
           }
         }
-        for (int t = 0; ok && t < T; ++t) {
+        // The JVP: tile t + 3 reuses tile t's buffer once tile t's output
+        // GEMMs are issued; the commit after them lets its warpgroup write.
+        for (int t = 0; JVP && ok && t < T; ++t) {
+          ok = mbar_wait(&sm.op_ready[t % 3], (t / 3) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_outputs(t);
+          if (t + 3 < T) {
+            ok = mbar_wait(&sm.kv_full[(t + 3) % NST], ((t + 3) / NST) & 1, abort_flag, err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_sf(t + 3);
+            issue_pg(t + 3);
+          }
+        }
+        for (int t = 0; !JVP && ok && t < T; ++t) {
           const uint32_t ph = (t >> 1) & 1;  // phase of this warpgroup's barriers
           if (t + 2 < T) {  // the warpgroup holds tile t in registers: F' | S of t + 2
             ok = mbar_wait(&sm.sf_free[t & 1], ph, abort_flag, err) &&
@@ -384,13 +408,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
     float2 a_acc = make_float2(0.f, 0.f), e_acc = make_float2(0.f, 0.f);
     bool ok = true;
-    const uint32_t sc = tbase + lane_off + 256 + 128 * wg;
 
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
       if (t >= T) break;
+      const int b = JVP ? t % 3 : wg;  // t mod 2 = wg
+      const uint32_t sc = tbase + lane_off + (JVP ? p1_buf_col<true>(t) : 256 + 128 * wg);
       // tcgen05.ld/st are warp-collective: take the decision warp-uniformly.
-      ok = mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
+      ok = mbar_wait_warp(&sm.sc_full[b], (JVP ? t / 3 : u) & 1, abort_flag, err);
       if (!ok) break;
       tc_fence_after();
       const int col0 = t * BN;
@@ -399,10 +424,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (masked) {
-        p1_tile<true, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau,
+        p1_tile<true, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[b], col0, jmax, c1, Lr2, Dr, tau,
                            a_acc, e_acc);
       } else {
-        p1_tile<false, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau,
+        p1_tile<false, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[b], col0, jmax, c1, Lr2, Dr, tau,
                             a_acc, e_acc);
       }
     }
