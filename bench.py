@@ -326,6 +326,14 @@ def main():
     barrier()
     clocks = sampler.stop()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    # prep (O, L, D) is not part of the step: timed on its own, after it
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    pev[0].record(stream)
+    for _ in range(3):
+        fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal, stream=stream)
+    pev[1].record(stream)
+    torch.cuda.synchronize()
+    prep_ms = pev[0].elapsed_time(pev[1]) / 3
     total_ms = evs[0][0].elapsed_time(evs[-1][2])
     p1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     p2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
@@ -398,6 +406,7 @@ def main():
                    "l2": f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
                          f"{L2_BYTES / 2**20:.0f} MiB",
                    "pass1_ms": p1_ms, "pass2_ms": p2_ms,
+                   "prep_ms_outside_step": prep_ms,
                    "pct_of_peak": 100.0 * (value / world) / peak,
                    "paths": "tcgen05" if fb.flashbob_bob_tile_sizes(w.d, fb.FLASHBOB_BF16)[
                        "Br1"] == 128 else "simt"},
