@@ -89,13 +89,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
-// One lane of the warp waits; the result is shared with the whole warp so
-// that warp-collective tcgen05 instructions that follow stay convergent.
+// A whole warp waits: all 32 lanes poll the barrier (one shared-memory
+// broadcast, the same answer for every lane) and a vote keeps the result
+// warp-uniform, so the warp-collective tcgen05 instructions that follow stay
+// convergent.  Letting one lane wait and broadcasting its result instead
+// (a divergent branch, then a shuffle) cost a warp hundreds of cycles per
+// wait.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                volatile int* abort_flag, unsigned int* err) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  const bool ok = mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, err);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // All lanes' tcgen05 stores are complete and fenced; one arrive per warp.
