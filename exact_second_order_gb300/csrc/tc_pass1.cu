@@ -11,7 +11,7 @@
 // R is carried as R' = dS K = R - D B (dS = P o (dP - D)), which turns the
 // correction into d~Q = tau (Omega - alpha R' - E0 B): the same value, one
 // bf16 operand fewer, and dS [U_K | K] yields Omega's dS U_K term and R' in
-// one MMA (20 MMAs per tile instead of 22; this pass is MMA-bound).
+// one MMA (20 MMAs per tile instead of 22).
 //
 // CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
 //   warp 0      TMA producer: Q, dO, U_Q blocks once, then U_K, K, V, U_V
