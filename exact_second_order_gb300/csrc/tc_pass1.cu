@@ -37,6 +37,8 @@
 // The same kernel, instantiated with JVP = true, serves the attention JVP
 // along (U_Q, U_K, U_V): alpha and d~dO do not depend on dO, so with dO = 0
 // (no dP, G scores; only P and P o F as operands) it returns L' and O'.
+// With a single accumulator it keeps three score buffers at [128,512) (tile t
+// in buffer t mod 3), so no warpgroup waits for its next tile's scores.
 #include "internal.h"
 #include "tc_common.cuh"
 

@@ -16,8 +16,8 @@
 // CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
 //   warp 0      TMA producer: the resident K, U_K, V, U_V block, then Q, U_Q,
 //               dO tiles of 64 query rows through a 4-stage mbarrier ring;
-//   warp 1      TMEM allocator and MMA issuer (all lanes, one elected lane
-//               issues each group of MMAs);
+//   warp 1      TMEM allocator; one elected lane runs the whole MMA schedule
+//               (every barrier wait and every MMA);
 //   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: query rows 0-31 / 32-63
 //               of every tile (the 16-row K steps 0-1 / 2-3 of its output
 //               GEMMs).
