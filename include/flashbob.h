@@ -82,8 +82,8 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
  *        setting of [FBN] 实验关键数据); other values are rejected.
  *   Limits: 1 <= d <= 128; 1 <= Nq, Nk; B, H <= 65535; 1 <= Hkv,
  *        H % Hkv == 0.
- *   One launch: bf16 inputs
- *   with d = 64 run a tcgen05 kernel, every other case fp32 CUDA cores.
+ *   One launch: bf16 inputs with d = 64 or d = 128 run a tcgen05 kernel,
+ *   every other case fp32 CUDA cores.
  */
 flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const void* dO,
                               float* O, float* L, float* D, int B, int H, int Hkv, int Nq,
@@ -102,8 +102,9 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
  *   Pass 1 (row-resident) writes d~Q, d~dO, alpha, E; pass 2 (column-
  *   resident) reads alpha, E and writes d~K, d~V.  No N x N tensor is ever
  *   written to device memory and no atomics are used.
- *   Limits: as flashbob_prep.  bf16 inputs with d = 64 run the tcgen05
- *   tensor-core kernels; every other case runs the fp32 CUDA-core kernels.
+ *   Limits: as flashbob_prep.  bf16 inputs with d = 64 or d = 128 run the
+ *   tcgen05 tensor-core kernels; every other case runs the fp32 CUDA-core
+ *   kernels.
  */
 flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const float* O,
                              const void* dO, const float* L, const float* D, const void* UQ,
