@@ -51,7 +51,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Smem2 {
   alignas(1024) uint8_t kb[4][BLOCK_BYTES];      // K, U_K, V, U_V (resident)
   alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, U_Q, dO (Q|U_Q adjacent)
-  float4 scal[2][2][32];  // per warpgroup, double-buffered row scalars (see stage())
+  float4 scal[2][4][32];  // per warpgroup, a ring of four tiles' row scalars (see stage())
   uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
@@ -379,15 +379,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       pr[4] = -v.z;
       pr[6] = -fmaf(v.z, v.y, v.w);
     };
-    // The loader warp fetches the scalars one tile ahead into registers, so
-    // their global-memory latency hides behind the current tile.
-    if (loader) stage(sm.scal[wg][0], load_scalars(0));
+    // The loader warp stages the scalars of two tiles at a time, at the
+    // warpgroup barrier of every even tile t: those of tiles t + 2 and t + 3,
+    // fetched into registers two tiles earlier (so their global-memory
+    // latency hides behind two tiles), into ring slots that tiles t - 2 and
+    // t - 1 used (every warp has passed the barrier, so none still reads
+    // them).  Tiles t and t + 1 were staged at the barrier of tile t - 2.
+    float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+    if (loader) {
+      const float4 v0 = load_scalars(0), v1 = load_scalars(1);
+      stage(sm.scal[wg][0], v0);
+      stage(sm.scal[wg][1], v1);
+      n0 = load_scalars(2);
+      n1 = load_scalars(3);
+    }
     int tq = 0;  // tile of the current query head, (t mod Tq)
     for (int t = 0; t < T; ++t) {
-      const float4* scal = sm.scal[wg][t & 1];
-      named_bar_sync(2 + wg, 128);  // scal is written; last tile's readers are done
-      float4 next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (loader) next = load_scalars(t + 1);
+      const float4* scal = sm.scal[wg][t & 3];
+      if ((t & 1) == 0) {
+        named_bar_sync(2 + wg, 128);  // tiles t, t + 1 staged; tiles t - 2, t - 1 read
+        if (loader) {
+          stage(sm.scal[wg][(t + 2) & 3], n0);
+          stage(sm.scal[wg][(t + 3) & 3], n1);
+          n0 = load_scalars(t + 4);
+          n1 = load_scalars(t + 5);
+        }
+      }
       // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
       // failed wait keep looping so every thread passes the same named
       // barriers, but skip the work.
@@ -402,9 +419,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         else
           ok = p2_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
       }
-      // Every thread passed this iteration's barrier, so nobody still reads
-      // the other buffer.
-      if (loader) stage(sm.scal[wg][(t + 1) & 1], next);
       if (++tq == Tq) tq = 0;
     }
 
