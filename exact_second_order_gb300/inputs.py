@@ -107,6 +107,14 @@ MQA_N8192 = Workload("mqa_B1_H12_Hkv1_N8192_d64", 1, 12, 8192, 64, "bf16", Hkv=1
 # Rectangular attention: fewer queries than keys and the reverse.
 RECT_Q4096_K16384 = Workload("rect_B1_H8_Nq4096_Nk16384_d64", 1, 8, 4096, 64, "bf16", Nk=16384)
 RECT_Q16384_K4096 = Workload("rect_B1_H8_Nq16384_Nk4096_d64", 1, 8, 16384, 64, "bf16", Nk=4096)
+# Long query streams against a few key blocks: pass 2's loop as long as in the
+# long-context and extreme workloads (1024 / 4096 query tiles per key block),
+# with few enough keys that the oracle covers every key column.
+LONGLOOP_D64 = Workload("longloop_B1_H4_Nq65536_Nk256_d64", 1, 4, 65536, 64, "bf16", Nk=256)
+LONGLOOP_EXTREME_D64 = Workload("longloop_B1_H1_Nq262144_Nk512_d64", 1, 1, 262144, 64, "bf16",
+                                Nk=512)
+LONGLOOP_D128 = Workload("longloop_B1_H1_Nq131072_Nk256_d128", 1, 1, 131072, 128, "bf16",
+                         Nk=256)
 # A mid-size case for detailed profiles: inputs (~0.3 GB) larger than L2.
 PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
 
@@ -114,7 +122,8 @@ WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PE
                                  MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128,
                                  CAUSAL_N4096, CAUSAL_N16384, CAUSAL_N16384_D128, GQA_N8192,
                                  MQA_N8192,
-                                 RECT_Q4096_K16384, RECT_Q16384_K4096, PROFILE)}
+                                 RECT_Q4096_K16384, RECT_Q16384_K4096, LONGLOOP_D64,
+                                 LONGLOOP_EXTREME_D64, LONGLOOP_D128, PROFILE)}
 
 
 def make_inputs(w: Workload) -> dict[str, torch.Tensor]:

@@ -34,7 +34,12 @@ Parity pins (tests/test_oracle.py): central finite differences of Phi, exact
 symbolic differentiation (sympy) on tiny inputs, a loop-only brute force,
 the printed affine identities, sum_j P_ij = 1, shift invariances, Hessian
 symmetry, the N = 1 closed form, the U_Q = U_K = 0 reduction to a first
-backward, and JVP identities of the forward.  No function here is unpinned.
+backward, JVP identities of the forward and torch fp64 double-backward.  The
+row form (``bob_rows``), the all-row scalars (``row_scalars``), the column
+form (``bob_cols``, ``bob_cols_group``) and the batched loop
+(``bob_batched``) each have pins of their own (finite differences of Phi
+entry by entry, torch double-backward, the matrix form).  No function here
+is unpinned.
 """
 from __future__ import annotations
 
@@ -249,6 +254,93 @@ def bob_rows(Q, K, V, dO, UQ, UK, UV, tau, rows, causal=False):
 
 
 # --------------------------------------------------------------------------
+# One key column at a time: the column outputs d~K_j, d~V_j for long sequences
+# --------------------------------------------------------------------------
+
+def row_scalars(Q, K, V, dO, UQ, UK, UV, tau, causal=False, chunk=256):
+    """L, D, alpha and E of every query row, by the same definitions as
+    ``bob`` ([FAB] sections 一/二 for L and D, [FBN] 关键设计 1 for alpha and
+    E), evaluated for ``chunk`` rows at a time so that no N_q x N_k array is
+    held at once.  The rows are independent: each row's values are exactly
+    those ``bob`` computes for it."""
+    Nq = Q.shape[0]
+    L, D, alpha, E = (np.empty(Nq) for _ in range(4))
+    for r0 in range(0, Nq, chunk):
+        r = slice(r0, min(Nq, r0 + chunk))
+        S = tau * (Q[r] @ K.T)
+        if causal:
+            S = np.where(causal_mask(Nq, K.shape[0])[r], S, -np.inf)
+        m = S.max(axis=1, keepdims=True)
+        Lr = m[:, 0] + np.log(np.exp(S - m).sum(axis=1))
+        P = np.exp(S - Lr[:, None])
+        Dr = (dO[r] * (P @ V)).sum(axis=1)
+        F = tau * (UQ[r] @ K.T + Q[r] @ UK.T)
+        dP = dO[r] @ V.T
+        G = dO[r] @ UV.T
+        ar = (P * F).sum(axis=1)
+        dPt = F * (dP - Dr[:, None]) + G - ar[:, None] * dP
+        L[r], D[r], alpha[r], E[r] = Lr, Dr, ar, (P * dPt).sum(axis=1)
+    return {"L": L, "D": D, "alpha": alpha, "E": E}
+
+
+def bob_cols(Q, K, V, dO, UQ, UK, UV, tau, cols, causal=False, scalars=None, chunk=64):
+    """Column outputs d~K_j and d~V_j for the listed key columns j only.
+
+    Column j of the transposed scores needs K_j, V_j, U_K,j, U_V,j, every
+    query-side row and the row scalars L, D, alpha, E of every row ([FBN]
+    关键设计 2: those scalars are all that crosses from the row pass to the
+    column pass).  Given them, each column costs O(N_q d):
+
+        P_ij = exp(tau Q_i.K_j - L_i),  dP_ij = dO_i.V_j,
+        F_ij = tau (U_Q,i.K_j + Q_i.U_K,j),  G_ij = dO_i.U_V,j,
+        dS = P (dP - D),  d~P = F (dP - D) + G - alpha dP,  d~S = P (d~P - E),
+        d~K_j = tau sum_i (d~S_ij Q_i + dS_ij U_Q,i),
+        d~V_j = sum_i P_ij (F_ij - alpha_i) dO_i
+
+    (the formulas of ``bob`` read down one column), for ``chunk`` listed
+    columns at a time.  ``scalars`` is a dict with L, D, alpha, E from
+    ``row_scalars`` or ``bob``; when omitted they are computed here with
+    ``row_scalars`` (O(N_q N_k d)).
+    """
+    sc = scalars if scalars is not None else row_scalars(Q, K, V, dO, UQ, UK, UV, tau, causal)
+    L, D, alpha, E = (sc[k][:, None] for k in ("L", "D", "alpha", "E"))
+    cols = np.asarray(cols, dtype=np.int64)
+    d = Q.shape[1]
+    dKt = np.empty((cols.size, d))
+    dVt = np.empty((cols.size, d))
+    rows = np.arange(Q.shape[0])[:, None]
+    for c0 in range(0, cols.size, chunk):
+        c = cols[c0:c0 + chunk]
+        S = tau * (Q @ K[c].T)  # [N_q, columns]
+        if causal:
+            S = np.where(rows >= c[None, :], S, -np.inf)
+        P = np.exp(S - L)
+        dP = dO @ V[c].T
+        F = tau * (UQ @ K[c].T + Q @ UK[c].T)
+        G = dO @ UV[c].T
+        dS = P * (dP - D)
+        dPt = F * (dP - D) + G - alpha * dP
+        dSt = P * (dPt - E)
+        dKt[c0:c0 + c.size] = tau * (dSt.T @ Q + dS.T @ UQ)
+        dVt[c0:c0 + c.size] = (P * (F - alpha)).T @ dO
+    return {"dKt": dKt, "dVt": dVt}
+
+
+def bob_cols_group(Qg, K, V, dOg, UQg, UK, UV, tau, cols, causal=False, scalars=None):
+    """``bob_cols`` for a key/value head shared by the query heads of a group
+    (``Qg``, ``dOg``, ``UQg`` are [G, N_q, d]): d~K_j, d~V_j of the shared
+    head are the sums of the per-query-head columns ([FBN] 关键设计 3).
+    ``scalars``, if given, is a list of one dict per query head."""
+    out = {"dKt": 0.0, "dVt": 0.0}
+    for h in range(Qg.shape[0]):
+        r = bob_cols(Qg[h], K, V, dOg[h], UQg[h], UK, UV, tau, cols, causal,
+                     None if scalars is None else scalars[h])
+        out["dKt"] = out["dKt"] + r["dKt"]
+        out["dVt"] = out["dVt"] + r["dVt"]
+    return out
+
+
+# --------------------------------------------------------------------------
 # Brute force: scalar loops only (tiny N, d), an independent restatement
 # --------------------------------------------------------------------------
 
@@ -314,18 +406,6 @@ def bob_bruteforce(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
 # Batched helpers over [B, H, N, d]
 # --------------------------------------------------------------------------
 
-def prep_batched(Q, K, V, dO, tau, causal=False):
-    """``prep`` for every (b, h) of [B, H, N, d] arrays."""
-    B, H, Nq, d = Q.shape
-    O = np.empty((B, H, Nq, d))
-    L = np.empty((B, H, Nq))
-    D = np.empty((B, H, Nq))
-    for b in range(B):
-        for h in range(H):
-            O[b, h], L[b, h], D[b, h] = prep(Q[b, h], K[b, h], V[b, h], dO[b, h], tau, causal)
-    return O, L, D
-
-
 def bob_batched(Q, K, V, dO, UQ, UK, UV, tau, heads=None, causal=False):
     """``bob`` for every (b, h) (or the listed (b, h) pairs)."""
     B, H, Nq, d = Q.shape
@@ -376,15 +456,3 @@ def bob_gqa(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
         out["dKt"][g] += r["dKt"]
         out["dVt"][g] += r["dVt"]
     return out
-
-
-def prep_gqa(Q, K, V, dO, tau, causal=False):
-    """O, L, D per query head with the shared key/value heads."""
-    H, Hkv = Q.shape[0], K.shape[0]
-    G = H // Hkv
-    O = np.empty(Q.shape)
-    L = np.empty(Q.shape[:2])
-    D = np.empty(Q.shape[:2])
-    for h in range(H):
-        O[h], L[h], D[h] = prep(Q[h], K[h // G], V[h // G], dO[h], tau, causal)
-    return O, L, D

@@ -23,3 +23,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the achieved parity errors of the session (tests/helpers.py
+    RECORDED) to $FLASHBOB_PARITY_LOG as JSON lines, when that is set."""
+    path = os.environ.get("FLASHBOB_PARITY_LOG")
+    if not path:
+        return
+    try:
+        from tests.helpers import RECORDED
+    except Exception:
+        return
+    import json
+    with open(path, "w") as fh:
+        for check, key, err in RECORDED:
+            fh.write(json.dumps({"check": check, "output": key, "rel_err": err}) + "\n")

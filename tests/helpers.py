@@ -14,6 +14,17 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}
 MAT_KEYS = ("dQt", "dKt", "dVt", "ddOt")
 ROW_KEYS = ("alpha", "E")
 
+# Achieved errors of this session, (check, output, error) in the order the
+# tests ran; written as JSON lines to $FLASHBOB_PARITY_LOG at the end of the
+# session (tests/conftest.py) so that the margins under the gates are kept.
+RECORDED: list[tuple[str, str, float]] = []
+
+
+def record(check: str, errs: dict) -> dict:
+    for k, v in errs.items():
+        RECORDED.append((check, k, float(v)))
+    return errs
+
 
 def rel_fro(got, ref) -> float:
     """Relative Frobenius error; where the exact result is zero (the oracle's
@@ -106,6 +117,32 @@ def sampled_row_errors(w, x, out, state, n_rows=256, seed=1234, heads=None):
         for k in got:
             src = out[k] if k in out else state[k]
             got[k].append(to_np(src[b, h][rows]))
+            ref[k].append(r[k])
+    return {k: rel_fro(np.concatenate(got[k]), np.concatenate(ref[k])) for k in got}
+
+
+def sampled_col_errors(w, x, out, kv_heads, n_cols=128, seed=4321):
+    """d~K and d~V of ``n_cols`` seeded key columns of each listed key/value
+    head (b, g) against the column-form oracle, element by element.  The
+    oracle's own row scalars (L, D, alpha, E of every row of every query head
+    of the group; plain C, fp64) feed ``oracle.bob_cols_group``: nothing the
+    CUDA path computed is used."""
+    from oracle import crows
+    rng = np.random.default_rng(seed)
+    G = w.H // w.kv_heads
+    got = {"dKt": [], "dVt": []}
+    ref = {"dKt": [], "dVt": []}
+    for b, g in kv_heads:
+        cols = np.sort(rng.choice(w.kv_len, size=min(n_cols, w.kv_len), replace=False))
+        kv = [as_float64_numpy(x[k][b, g]) for k in ("K", "V", "UK", "UV")]
+        hs = range(g * G, (g + 1) * G)
+        qs = {k: np.stack([as_float64_numpy(x[k][b, h]) for h in hs]) for k in ("Q", "dO", "UQ")}
+        scal = [crows.row_scalars(qs["Q"][i], kv[0], kv[1], qs["dO"][i], qs["UQ"][i], kv[2],
+                                  kv[3], w.tau, w.causal) for i in range(G)]
+        r = orc.bob_cols_group(qs["Q"], kv[0], kv[1], qs["dO"], qs["UQ"], kv[2], kv[3], w.tau,
+                               cols, w.causal, scalars=scal)
+        for k in got:
+            got[k].append(to_np(out[k][b, g][cols]))
             ref[k].append(r[k])
     return {k: rel_fro(np.concatenate(got[k]), np.concatenate(ref[k])) for k in got}
 

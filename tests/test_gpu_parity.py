@@ -1,10 +1,16 @@
 """GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
 
 Small shapes: every output against the full oracle, element by element
-(relative Frobenius error).  Full workload sizes: 256 seeded rows per head
-against the per-row oracle, plus the exact column-sum invariants of d~K
-and d~V, NaN-poisoned outputs (every element written) and the memory check.
+(relative Frobenius error).  Full workload sizes: seeded rows of every head
+against the per-row oracle (alpha, E, d~Q, d~dO, L, D) and seeded key
+columns against the column-form oracle (d~K, d~V, with the oracle's own row
+scalars of every row), plus the exact column-sum invariants of d~K and d~V,
+NaN-poisoned outputs (every element written) and the memory check.  Long
+query streams against a few key blocks run pass 2's full-length loop under
+the full oracle.  Every achieved error is recorded (tests/helpers.py).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -12,7 +18,7 @@ import torch
 from exact_second_order_gb300 import flashbob as fb
 from exact_second_order_gb300 import inputs as wl
 from tests.helpers import (MAT_KEYS, ROW_KEYS, TOL, column_sum_residuals, full_oracle_errors,
-                           run_cuda, sampled_row_errors)
+                           record, run_cuda, sampled_col_errors, sampled_row_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +31,7 @@ def _assert_all_written(out):
 def _check_full(w, heads=None):
     x, dev, state, out = run_cuda(w)
     _assert_all_written(out)
-    errs = full_oracle_errors(w, x, state, out, heads=heads)
+    errs = record(f"{w.name} full", full_oracle_errors(w, x, state, out, heads=heads))
     tol = TOL[w.dtype]
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{w.name}: {bad} (all: {errs})"
@@ -68,12 +74,15 @@ def test_gpt2_layer_workload_full_oracle():
 def test_mid_length_workloads(w):
     x, dev, state, out = run_cuda(w)
     _assert_all_written(out)
-    errs = sampled_row_errors(w, x, out, state)
+    errs = record(f"{w.name} rows", sampled_row_errors(w, x, out, state))
     assert max(errs.values()) <= TOL["bf16"], errs
+    cols = record(f"{w.name} cols", sampled_col_errors(
+        w, x, out, [(0, g) for g in range(w.kv_heads)], n_cols=64))
+    assert max(cols.values()) <= TOL["bf16"], cols
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
-    # full oracle on one head covers d~K and d~V element by element
-    full = full_oracle_errors(w, x, state, out, heads=[(0, 0)])
+    # full oracle on one head covers every element of that head
+    full = record(f"{w.name} full head", full_oracle_errors(w, x, state, out, heads=[(0, 0)]))
     assert max(full.values()) <= TOL["bf16"], full
 
 
@@ -99,14 +108,39 @@ def _memory_checked_run(w):
 
 @pytest.mark.parametrize("w", [wl.LONG_CONTEXT, wl.EXTREME_D64, wl.EXTREME_D128],
                          ids=lambda w: w.name)
-def test_long_workloads_sampled_rows_and_memory(w):
+def test_long_workloads_sampled_rows_columns_and_memory(w):
     x, dev, state, out = _memory_checked_run(w)
     _assert_all_written(out)
     heads = [(0, h) for h in range(w.H)]
-    errs = sampled_row_errors(w, x, out, state, n_rows=256 if w.H == 1 else 64, heads=heads)
+    errs = record(f"{w.name} rows", sampled_row_errors(
+        w, x, out, state, n_rows=256 if w.H == 1 else 64, heads=heads))
     assert max(errs.values()) <= TOL["bf16"], errs
-    res = column_sum_residuals(out)
+    res = record(f"{w.name} column sums", column_sum_residuals(out))
     assert max(res.values()) <= TOL["bf16"], res
+    # d~K, d~V element by element on seeded key columns: the oracle needs
+    # every row's scalars (O(N^2 d) per head on the host), so the longest
+    # sequences take minutes and are opted into with FLASHBOB_FULL_COLUMNS=1.
+    if w is wl.LONG_CONTEXT or os.environ.get("FLASHBOB_FULL_COLUMNS") == "1":
+        kv = [(0, g) for g in range(w.kv_heads)] if w is not wl.LONG_CONTEXT else [(0, 0), (0, 3)]
+        cols = record(f"{w.name} cols", sampled_col_errors(w, x, out, kv, n_cols=128))
+        assert max(cols.values()) <= TOL["bf16"], cols
+
+
+# Pass 2 at its full-size loop length: a query stream as long as the long
+# workloads' (1024, 4096 and 4096 tiles per key block) against a few key
+# blocks, so that every d~K, d~V column and sampled rows go through the
+# oracle in seconds.
+@pytest.mark.parametrize("w", [wl.LONGLOOP_D64, wl.LONGLOOP_EXTREME_D64, wl.LONGLOOP_D128],
+                         ids=lambda w: w.name)
+def test_long_query_streams_every_column(w):
+    x, dev, state, out = run_cuda(w)
+    _assert_all_written(out)
+    cols = record(f"{w.name} all cols", sampled_col_errors(
+        w, x, out, [(0, g) for g in range(w.kv_heads)], n_cols=w.kv_len))
+    assert max(cols.values()) <= TOL["bf16"], cols
+    errs = record(f"{w.name} rows", sampled_row_errors(
+        w, x, out, state, n_rows=512, heads=[(0, h) for h in range(w.H)]))
+    assert max(errs.values()) <= TOL["bf16"], errs
 
 
 def test_stream_argument_is_honoured():
@@ -158,11 +192,14 @@ def test_causal_pages_shape_sampled_rows():
     x, dev, state, out = run_cuda(w)
     _assert_all_written(out)
     heads = [(0, 0), (1, 5), (3, 11)]
-    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=heads)
+    errs = record(f"{w.name} rows", sampled_row_errors(w, x, out, state, n_rows=128,
+                                                       heads=heads))
     assert max(errs.values()) <= TOL["bf16"], errs
+    cols = record(f"{w.name} cols", sampled_col_errors(w, x, out, heads, n_cols=128))
+    assert max(cols.values()) <= TOL["bf16"], cols
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
-    full = full_oracle_errors(w, x, state, out, heads=[(2, 7)])
+    full = record(f"{w.name} full head", full_oracle_errors(w, x, state, out, heads=[(2, 7)]))
     assert max(full.values()) <= TOL["bf16"], full
 
 
@@ -189,11 +226,15 @@ def test_gqa_workloads_sampled_rows(w):
     x, dev, state, out = run_cuda(w)
     _assert_all_written(out)
     heads = [(0, 0), (0, 5), (0, 11)]
-    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=heads)
+    errs = record(f"{w.name} rows", sampled_row_errors(w, x, out, state, n_rows=128,
+                                                       heads=heads))
     assert max(errs.values()) <= TOL["bf16"], errs
+    cols = record(f"{w.name} cols", sampled_col_errors(
+        w, x, out, [(0, g) for g in range(w.kv_heads)], n_cols=64))
+    assert max(cols.values()) <= TOL["bf16"], cols
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
-    full = full_oracle_errors(w, x, state, out, heads=[(0, 0)])
+    full = record(f"{w.name} full group", full_oracle_errors(w, x, state, out, heads=[(0, 0)]))
     assert max(full.values()) <= TOL["bf16"], full
 
 
@@ -219,11 +260,14 @@ def test_rectangular_workloads_sampled_rows(w):
     x, dev, state, out = run_cuda(w)
     _assert_all_written(out)
     heads = [(0, 0), (0, 7)]
-    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=heads)
+    errs = record(f"{w.name} rows", sampled_row_errors(w, x, out, state, n_rows=128,
+                                                       heads=heads))
     assert max(errs.values()) <= TOL["bf16"], errs
+    cols = record(f"{w.name} cols", sampled_col_errors(w, x, out, heads, n_cols=128))
+    assert max(cols.values()) <= TOL["bf16"], cols
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
-    full = full_oracle_errors(w, x, state, out, heads=[(0, 3)])
+    full = record(f"{w.name} full head", full_oracle_errors(w, x, state, out, heads=[(0, 3)]))
     assert max(full.values()) <= TOL["bf16"], full
 
 
@@ -250,11 +294,14 @@ def test_d128_mid_length_sampled_rows():
     w = wl.Workload("mid_B1_H4_N8192_d128", 1, 4, 8192, 128, "bf16", causal=True)
     x, dev, state, out = run_cuda(w)
     _assert_all_written(out)
-    errs = sampled_row_errors(w, x, out, state, n_rows=128, heads=[(0, 0), (0, 3)])
+    errs = record(f"{w.name} rows", sampled_row_errors(w, x, out, state, n_rows=128,
+                                                       heads=[(0, 0), (0, 3)]))
     assert max(errs.values()) <= TOL["bf16"], errs
+    cols = record(f"{w.name} cols", sampled_col_errors(w, x, out, [(0, 0), (0, 3)], n_cols=128))
+    assert max(cols.values()) <= TOL["bf16"], cols
     res = column_sum_residuals(out)
     assert max(res.values()) <= TOL["bf16"], res
-    full = full_oracle_errors(w, x, state, out, heads=[(0, 1)])
+    full = record(f"{w.name} full head", full_oracle_errors(w, x, state, out, heads=[(0, 1)]))
     assert max(full.values()) <= TOL["bf16"], full
 
 

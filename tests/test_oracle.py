@@ -556,3 +556,163 @@ def test_attention_jvp_is_the_bob_by_product():
     for scale in (1.0, -3.0):
         r = orc.bob(Q, K, V, scale * dO, UQ, UK, UV, 0.5, True)
         assert rel(r["ddOt"], Od) < 1e-13 and rel(r["alpha"], Ld) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# Column form (d~K_j, d~V_j of chosen key columns) and the all-row scalars
+# --------------------------------------------------------------------------
+
+def _fd_entry(fun, X, idx, h=1e-5):
+    Xp, Xm = X.copy(), X.copy()
+    Xp[idx] += h
+    Xm[idx] -= h
+    return (fun(Xp) - fun(Xm)) / (2 * h)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(9, 9, False), (9, 9, True), (6, 11, False),
+                                          (11, 6, True)])
+def test_bob_cols_matches_fd_of_phi(Nq, Nk, causal):
+    """Each d~K_jk, d~V_jk of the column form is the derivative of Phi with
+    respect to K_jk, V_jk (central differences, straight from the definition
+    of Phi)."""
+    rng = np.random.default_rng(50 + Nq + Nk)
+    Q, dO, UQ = (rng.standard_normal((Nq, 4)) for _ in range(3))
+    K, V, UK, UV = (rng.standard_normal((Nk, 4)) for _ in range(4))
+    tau = 0.6
+    cols = [0, Nk // 2, Nk - 1]
+    r = orc.bob_cols(Q, K, V, dO, UQ, UK, UV, tau, cols, causal)
+    for n, j in enumerate(cols):
+        for k in range(4):
+            fk = _fd_entry(lambda X: orc.phi(Q, X, V, dO, UQ, UK, UV, tau, causal), K, (j, k))
+            fv = _fd_entry(lambda X: orc.phi(Q, K, X, dO, UQ, UK, UV, tau, causal), V, (j, k))
+            assert abs(r["dKt"][n, k] - fk) <= 1e-7 * max(1.0, abs(fk)), (j, k)
+            assert abs(r["dVt"][n, k] - fv) <= 1e-7 * max(1.0, abs(fv)), (j, k)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bob_cols_matches_torch_double_backward(causal):
+    torch = pytest.importorskip("torch")
+    Nq, Nk, d = 13, 21, 5
+    rng = np.random.default_rng(60)
+    Q, dO, UQ = (rng.standard_normal((Nq, d)) for _ in range(3))
+    K, V, UK, UV = (rng.standard_normal((Nk, d)) for _ in range(4))
+    tau = 1 / np.sqrt(d)
+    cols = np.array([0, 3, 12, 20])
+    r = orc.bob_cols(Q, K, V, dO, UQ, UK, UV, tau, cols, causal)
+    tq, tk, tv, tdo = (torch.tensor(x, requires_grad=True) for x in (Q, K, V, dO))
+    uq, uk, uv = (torch.tensor(x) for x in (UQ, UK, UV))
+    s = tau * tq @ tk.T
+    if causal:
+        s = s.masked_fill(~torch.tensor(orc.causal_mask(Nq, Nk)), float("-inf"))
+    out = torch.softmax(s, dim=-1) @ tv
+    dq, dk, dv = torch.autograd.grad(out, (tq, tk, tv), tdo, create_graph=True)
+    ph = (dq * uq).sum() + (dk * uk).sum() + (dv * uv).sum()
+    gk, gv = torch.autograd.grad(ph, (tk, tv))
+    assert rel(r["dKt"], gk.numpy()[cols]) < 1e-12
+    assert rel(r["dVt"], gv.numpy()[cols]) < 1e-12
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(40, 40, False), (40, 40, True), (25, 70, True),
+                                          (70, 25, False)])
+def test_row_scalars_and_bob_cols_match_matrix_form(Nq, Nk, causal):
+    """Chunked all-row scalars and the column form against ``bob`` (whose
+    pins are finite differences, sympy and torch); the chunk size splits the
+    rows unevenly so that the ragged last chunk is covered."""
+    rng = np.random.default_rng(70 + Nq)
+    Q, dO, UQ = (rng.standard_normal((Nq, 8)) for _ in range(3))
+    K, V, UK, UV = (rng.standard_normal((Nk, 8)) for _ in range(4))
+    tau = 0.4
+    full = orc.bob(Q, K, V, dO, UQ, UK, UV, tau, causal)
+    sc = orc.row_scalars(Q, K, V, dO, UQ, UK, UV, tau, causal, chunk=7)
+    for key in ("L", "D", "alpha", "E"):
+        assert rel(sc[key], full[key]) < 1e-13, key
+    cols = np.arange(Nk)
+    r = orc.bob_cols(Q, K, V, dO, UQ, UK, UV, tau, cols, causal, scalars=sc)
+    assert rel(r["dKt"], full["dKt"]) < 1e-13
+    assert rel(r["dVt"], full["dVt"]) < 1e-13
+
+
+def test_row_scalars_alpha_is_the_jvp_of_L():
+    """alpha_i is the directional derivative of L_i along (U_Q, U_K) (finite
+    differences of the forward), independently of ``bob``."""
+    rng = np.random.default_rng(80)
+    Q, K, V, dO, UQ, UK, UV = (rng.standard_normal((30, 6)) for _ in range(7))
+    tau, h = 0.45, 1e-5
+    sc = orc.row_scalars(Q, K, V, dO, UQ, UK, UV, tau, chunk=8)
+    _, _, O, Lp = orc.forward(Q + h * UQ, K + h * UK, V, tau)
+    _, _, _, Lm = orc.forward(Q - h * UQ, K - h * UK, V, tau)
+    assert rel(sc["alpha"], (Lp - Lm) / (2 * h)) < 1e-8
+    from scipy.special import logsumexp
+    assert rel(sc["L"], logsumexp(tau * Q @ K.T, axis=1)) < 1e-14
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bob_cols_group_matches_fd_of_phi_gqa(causal):
+    Q, K, V, dO, UQ, UK, UV = _rand_gqa(4, 2, 6, 3, 90)
+    tau = 0.55
+    cols = [1, 4]
+    for g in range(2):
+        hs = slice(2 * g, 2 * g + 2)
+        r = orc.bob_cols_group(Q[hs], K[g], V[g], dO[hs], UQ[hs], UK[g], UV[g], tau, cols,
+                               causal)
+        for n, j in enumerate(cols):
+            for k in range(3):
+                fk = _fd_entry(lambda X: orc.phi_gqa(Q, X, V, dO, UQ, UK, UV, tau, causal), K,
+                               (g, j, k))
+                fv = _fd_entry(lambda X: orc.phi_gqa(Q, K, X, dO, UQ, UK, UV, tau, causal), V,
+                               (g, j, k))
+                assert abs(r["dKt"][n, k] - fk) <= 1e-7 * max(1.0, abs(fk))
+                assert abs(r["dVt"][n, k] - fv) <= 1e-7 * max(1.0, abs(fv))
+
+
+def test_bob_batched_matches_torch_double_backward_over_batch_and_heads():
+    """The [B, H] loop of ``bob_batched`` (every head, and a listed subset)
+    against torch fp64 double-backward of Phi summed over all (b, h)."""
+    torch = pytest.importorskip("torch")
+    B, H, N, d = 2, 3, 10, 4
+    rng = np.random.default_rng(95)
+    args = [rng.standard_normal((B, H, N, d)) for _ in range(7)]
+    tau = 0.5
+    r = orc.bob_batched(*args, tau)
+    tq, tk, tv, tdo = (torch.tensor(x, requires_grad=True) for x in args[:4])
+    uq, uk, uv = (torch.tensor(x) for x in args[4:])
+    out = torch.softmax(tau * tq @ tk.transpose(-1, -2), dim=-1) @ tv
+    dq, dk, dv = torch.autograd.grad(out, (tq, tk, tv), tdo, create_graph=True)
+    ph = (dq * uq).sum() + (dk * uk).sum() + (dv * uv).sum()
+    g = torch.autograd.grad(ph, (tq, tk, tv, tdo))
+    for key, t in zip(("dQt", "dKt", "dVt", "ddOt"), g):
+        assert rel(r[key], t.numpy()) < 1e-12, key
+    sub = orc.bob_batched(*args, tau, heads=[(1, 2), (0, 1)])
+    for key, t in zip(("dQt", "dKt", "dVt", "ddOt"), g):
+        for b, h in ((1, 2), (0, 1)):
+            assert rel(sub[key][b, h], t.numpy()[b, h]) < 1e-12, key
+        assert np.isnan(sub[key][0, 0]).all()  # heads not listed stay unwritten
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(1, 1, False), (33, 33, False), (65, 65, True),
+                                          (70, 25, True), (25, 70, True), (100, 3, False)])
+def test_c_row_scalars_match_numpy_and_matrix_form(Nq, Nk, causal):
+    """The plain-C row scalars (oracle/rowscal.c) against ``bob`` and the
+    numpy ``row_scalars``, on shapes whose row count is not a multiple of the
+    C code's 32-row groups; inputs are fp32-exact (bf16-rounded) values."""
+    torch = pytest.importorskip("torch")
+    from oracle import crows
+    rng = np.random.default_rng(100 + Nq + Nk)
+    q = [torch.tensor(rng.standard_normal((Nq, 7))).to(torch.bfloat16).double().numpy()
+         for _ in range(3)]
+    k = [torch.tensor(rng.standard_normal((Nk, 7))).to(torch.bfloat16).double().numpy()
+         for _ in range(4)]
+    Q, dO, UQ = q
+    K, V, UK, UV = k
+    tau = 0.42
+    c = crows.row_scalars(Q, K, V, dO, UQ, UK, UV, tau, causal)
+    full = orc.bob(Q, K, V, dO, UQ, UK, UV, tau, causal)
+    for key in ("L", "D", "alpha", "E"):
+        assert rel(c[key], full[key]) < 1e-13, key
+
+
+def test_c_row_scalars_rejects_inexact_inputs():
+    from oracle import crows
+    x = np.full((4, 3), 0.1)  # 0.1 is not an fp32 value
+    with pytest.raises(ValueError):
+        crows.row_scalars(x, x, x, x, x, x, x, 0.5)
