@@ -7,17 +7,22 @@ already resident in device memory.  FLOPs per step follow the fixed GEMM
 list of both passes: 38 N^2 d per (batch, head).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle on the host cores instead (rows of the same workload).  ``--entry
-jvp`` times flashbob_attention_jvp instead (5 GEMMs, 10 N^2 d per head).
+oracle on the host cores instead (rows and columns of the same workload).
+``--entry jvp`` times flashbob_attention_jvp instead (5 GEMMs, 10 N^2 d per
+head).  ``--sweep`` prints, after that line, one more line per workload of
+the throughput-vs-length table (the five benchmark configurations and the
+pages' causal timing shapes).
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -51,6 +56,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--entry", choices=("bob", "jvp"), default="bob",
                     help="bob: flashbob_bob (the benchmark); jvp: flashbob_attention_jvp")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time every workload of the throughput-vs-length table")
+    ap.add_argument("--sweep-oracle", action="store_true",
+                    help="with --sweep: time the full fp64 oracle on the small configurations")
     return ap.parse_args()
 
 
@@ -92,6 +101,38 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def tensor_peak():
+    """The denominator of every fraction: the burst dense-bf16 figure (a
+    cuBLAS GEMM timed alone, at the clocks a sub-second timed region also
+    runs at), with the sustained figure (a seconds-long loop under the power
+    cap, at lower clocks) kept beside it."""
+    peaks, src = measured_peaks()
+    burst = float(peaks.get("bf16_tflops"))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    clk = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    note = (f"bf16_tflops (burst) of {src} peaks; sustained {sustained:.1f} TFLOP/s was "
+            f"measured at a median {clk} MHz" if clk else f"bf16_tflops (burst) of {src} peaks")
+    return burst, sustained, note
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def read_traffic():
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
     summary (a line ``<kernel> dram_bytes_per_launch <int>``), else None."""
@@ -111,13 +152,13 @@ class ClockSampler:
 
     def __init__(self, uuid: str | None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="flashbob_clocks_", suffix=".csv")
+        os.close(fd)
         cmd = ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "200"]
         if uuid:
             cmd += ["-i", uuid]
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
@@ -125,6 +166,7 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
@@ -134,48 +176,87 @@ class ClockSampler:
         self.fh.close()
         sm, smax, reasons, power = [], [], set(), []
         with open(self.path) as fh:
-            for line in fh:
-                f = [x.strip() for x in line.split(",")]
-                if len(f) < 9:
-                    continue
-                try:
-                    sm.append(float(f[1]))
-                    smax.append(float(f[2]))
-                    power.append(float(f[3]))
-                except ValueError:
-                    continue
-                for name, val in zip(REASONS, f[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(name)
+            lines = fh.readlines()
+        os.unlink(self.path)
+        for line in lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def oracle_rows_sample(w, x, seconds: float, rows_per_chunk: int = 16, seed: int = 7):
-    """Time oracle.bob_rows on seeded rows of head (0, 0) for about
-    ``seconds``; returns (rows done, elapsed)."""
+def config_dict(w) -> dict:
+    """The workload keys every line carries (our arm and the reference arm)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "N": w.N,
+            "Nk": w.kv_len, "d": w.d, "causal": w.causal, "tau": w.tau,
+            "flop_convention": "38*N^2*d*B*H (19 GEMMs of 2*N^2*d); rectangular N*Nk for "
+                               "N^2, causal the pairs j <= i"}
+
+
+def oracle_sample(w, x, seconds: float, chunk: int = 16, seed: int = 7):
+    """Time the oracle on a bounded sample of the workload: seeded query rows
+    of head (0, 0) through ``bob_rows`` (the row outputs: L, D, alpha, E,
+    d~Q, d~dO) and as many seeded key columns through ``bob_cols`` (d~K,
+    d~V), alternating chunks for about ``seconds``.  ``bob_cols`` takes every
+    row's scalars as input; for the timing they are the sampled rows' values
+    repeated, which changes no operation.  Returns the counts and times."""
     import numpy as np
 
     from exact_second_order_gb300.inputs import NAMES, as_float64_numpy
     from oracle import bob as orc
     args = [as_float64_numpy(x[k][0, 0]) for k in NAMES]  # query head 0 uses key head 0
     rng = np.random.default_rng(seed)
-    done, t0 = 0, time.perf_counter()
-    while True:
-        rows = rng.choice(w.N, size=rows_per_chunk, replace=False)
-        orc.bob_rows(*args, w.tau, rows, causal=w.causal)
-        done += rows_per_chunk
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            return done, el
+    rows = cols = 0
+    t_rows = t_cols = 0.0
+    scal = None
+    while t_rows + t_cols < seconds:
+        t0 = time.perf_counter()
+        r = orc.bob_rows(*args, w.tau, rng.choice(w.N, size=chunk, replace=False),
+                         causal=w.causal)
+        t_rows += time.perf_counter() - t0
+        rows += chunk
+        if scal is None:
+            reps = -(-w.N // chunk)
+            scal = {k: np.tile(r[k], reps)[:w.N] for k in ("L", "D", "alpha", "E")}
+        t0 = time.perf_counter()
+        orc.bob_cols(*args, w.tau, rng.choice(w.kv_len, size=chunk, replace=False),
+                     causal=w.causal, scalars=scal)
+        t_cols += time.perf_counter() - t0
+        cols += chunk
+    return {"rows": rows, "cols": cols, "t_rows": t_rows, "t_cols": t_cols}
 
 
-def row_flops(w) -> float:
-    """FLOPs credited per oracle row: the row-side GEMMs (pass 1 list) over
-    the keys an average query row sees."""
-    return 2.0 * PASS1_GEMMS * (w.pairs / w.N) * w.d
+def oracle_baseline(w, smp: dict) -> dict:
+    """Throughput of the oracle sample on the BoB GEMM list: a row carries
+    pass 1's 11 GEMMs over the keys it sees, a column pass 2's 8 over the
+    queries that see it; plus the labelled extrapolation to one full call
+    (every row and every key column of every head)."""
+    per_row = 2.0 * PASS1_GEMMS * (w.pairs / w.N) * w.d
+    per_col = 2.0 * PASS2_GEMMS * (w.pairs / w.kv_len) * w.d
+    el = smp["t_rows"] + smp["t_cols"]
+    value = (smp["rows"] * per_row + smp["cols"] * per_col) / el / 1e12
+    s_row, s_col = smp["t_rows"] / smp["rows"], smp["t_cols"] / smp["cols"]
+    full = w.B * (w.H * w.N * s_row + w.kv_heads * (w.H // w.kv_heads) * w.kv_len * s_col)
+    return {"value": value, "unit": UNIT, "cores": os.cpu_count(), "cpu_model": cpu_model(),
+            "kind": "oracle", "seconds_per_row": s_row, "seconds_per_column": s_col,
+            "extrapolated_full_call_s": full,
+            "sample": f"{smp['rows']} seeded rows (oracle.bob_rows) and {smp['cols']} seeded "
+                      f"key columns (oracle.bob_cols) of head (0,0), fp64 numpy, {el:.1f} s; "
+                      f"credited {per_row:.3e} flops per row, {per_col:.3e} per column; "
+                      f"extrapolated_full_call_s = all B*H*N rows and B*H*Nk columns at the "
+                      f"sampled rates (an extrapolation, not a measurement)"}
 
 
 def run_reference(args, w, rank, world):
@@ -185,24 +266,21 @@ def run_reference(args, w, rank, world):
     x = make_inputs(w)
     per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_rows_sample(w, x, min(per_step, 2.0))
-    t_rows, t_el = 0, 0.0
+        oracle_sample(w, x, min(per_step, 2.0))
+    tot = {"rows": 0, "cols": 0, "t_rows": 0.0, "t_cols": 0.0}
     for _ in range(args.steps):
-        r, el = oracle_rows_sample(w, x, per_step)
-        t_rows += r
-        t_el += el
-    value = t_rows * row_flops(w) / t_el / 1e12
-    cores = os.cpu_count()
+        smp = oracle_sample(w, x, per_step)
+        for k in tot:
+            tot[k] += smp[k]
+    base = oracle_baseline(w, tot)
+    value = base["value"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_el / args.steps,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * (tot["t_rows"] + tot["t_cols"]) / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
-                                        "Nk": w.kv_len, "d": w.d, "Hkv": w.kv_heads,
-                                        "causal": w.causal},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{t_rows} seeded rows of head (0,0) through oracle.bob_rows "
-                                   f"(fp64 numpy), {row_flops(w):.3e} flops credited per row"},
+        "data": "synthetic", "config": config_dict(w),
+        "cpu_baseline": base,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -238,8 +316,7 @@ def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
     total_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
     flops = JVP_GEMMS * 2.0 * w.pairs * w.d * w.B * w.H
     value = job_tflops(flops, args.steps, world, total_ms)
-    peaks, peak_src = measured_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak, _, peak_note = tensor_peak()
     achieved = flops / (ms * 1e-3) / 1e12
     line = {
         "metric": JVP_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -251,7 +328,7 @@ def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
                    "flops_per_step_per_gpu": flops},
         "roofline": {"kernel": "jvp", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                     "peak_source": f"bf16_tflops_sustained of {peak_src} peaks"},
+                     "peak_source": peak_note},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "e2e": None,
@@ -260,6 +337,154 @@ def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# The throughput-vs-length table (--sweep): the benchmark configurations at
+# head dim 64 (N = 1K ... 256K) and 128, then the pages' causal timing shapes
+# (B = 4, H = 12, bf16; [FBN] 实验关键数据).
+SWEEP = ("gpt2_layer_B4_H12_N1024_d64", "mid_B1_H12_N8192_d64", "mid_peaked_B1_H12_N8192_d64",
+         "long_B1_H4_N65536_d64", "extreme_B1_H1_N262144_d64", "extreme_B1_H1_N131072_d128",
+         "causal_B4_H12_N4096_d64", "causal_B4_H12_N8192_d64", "causal_B4_H12_N16384_d64",
+         "causal_B4_H12_N16384_d128", "causal_B4_H12_N32768_d128",
+         "causal_B4_H12_N65536_d128")
+
+
+def gpu_uuid(torch, local):
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        return None
+
+
+class Resident:
+    """Inputs, row state and outputs of one workload in device memory, and the
+    timed step (pass 1 then pass 2 on the current stream)."""
+
+    def __init__(self, w, x, fb, torch):
+        self.w, self.fb = w, fb
+        self.dev = {k: v.cuda() for k, v in x.items()}
+        d = self.dev
+        self.O, self.L, self.D = fb.prep(d["Q"], d["K"], d["V"], d["dO"], w.tau, causal=w.causal)
+        self.out = fb.alloc_bob_outputs(d["Q"], K=d["K"])
+        self.stream = torch.cuda.current_stream()
+
+    def step(self, ev=None):
+        w, d, o, fb, st = self.w, self.dev, self.out, self.fb, self.stream
+        if ev is not None:
+            ev[0].record(st)
+        fb.flashbob_bob_pass1(d["Q"], d["K"], d["V"], self.O, d["dO"], self.L, self.D, d["UQ"],
+                              d["UK"], d["UV"], w.tau, o["dQt"], o["ddOt"], o["alpha"], o["E"],
+                              causal=w.causal, stream=st)
+        if ev is not None:
+            ev[1].record(st)
+        fb.flashbob_bob_pass2(d["Q"], d["K"], d["V"], d["dO"], self.L, self.D, o["alpha"],
+                              o["E"], d["UQ"], d["UK"], d["UV"], w.tau, o["dKt"], o["dVt"],
+                              causal=w.causal, stream=st)
+        if ev is not None:
+            ev[2].record(st)
+
+    def prep_ms(self, torch, reps=3):
+        d, st = self.dev, self.stream
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(st)
+        for _ in range(reps):
+            self.fb.prep(d["Q"], d["K"], d["V"], d["dO"], self.w.tau, causal=self.w.causal,
+                         stream=st)
+        ev[1].record(st)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / reps
+
+    def input_bytes(self):
+        return sum(t.numel() * t.element_size() for t in list(self.dev.values())
+                   + [self.O, self.L, self.D])
+
+
+def timed_steps(res, steps, warmup, torch, barrier, uuid):
+    """W warm-up steps, then K steps with CUDA events around each pass on the
+    launching stream and nvidia-smi clocks sampled during the timed region."""
+    fb = res.fb
+    for _ in range(max(3, warmup)):
+        res.step()
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    barrier()
+    for i in range(steps):
+        res.step(evs[i])
+    barrier()
+    clocks = sampler.stop()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    return {"total_ms": evs[0][0].elapsed_time(evs[-1][2]),
+            "p1_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+            "p2_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+            "clocks": clocks}
+
+
+def roofline(w, t, peak, peak_note, traffic=None):
+    """The dominant pass: its algorithmic FLOPs over its mean event time."""
+    unit_flops = 2.0 * w.pairs * w.d * w.B * w.H  # one Nq x Nk x d GEMM per (b, h)
+    dominant = "pass1" if t["p1_ms"] >= t["p2_ms"] else "pass2"
+    dom_ms = t["p1_ms"] if dominant == "pass1" else t["p2_ms"]
+    dom_flops = (PASS1_GEMMS if dominant == "pass1" else PASS2_GEMMS) * unit_flops
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    return {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+            "peak_source": peak_note}
+
+
+def run_sweep(args, fb, torch, barrier, uuid, peak, peak_note):
+    """One JSON line per workload of SWEEP: TFLOP/s, ms/call, the fraction of
+    the tensor peak, both passes' times and the clocks."""
+    from exact_second_order_gb300.inputs import WORKLOADS, make_inputs
+    for name in SWEEP:
+        w = WORKLOADS[name]
+        res = Resident(w, make_inputs(w), fb, torch)
+        # about half a second of timed work, at least 5 steps
+        res.step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        res.step()
+        torch.cuda.synchronize()
+        est = max(time.perf_counter() - t0, 1e-5)
+        steps = int(min(200, max(5, 0.5 / est)))
+        t = timed_steps(res, steps, 3, torch, barrier, uuid)
+        ms = t["total_ms"] / steps
+        value = w.flops / (ms * 1e-3) / 1e12
+        line = {"sweep": True, "metric": METRIC, "value": value, "unit": UNIT,
+                "ms_per_step": ms, "steps": steps, "warmup": 3, "dtype": "bf16",
+                "pct_of_peak": 100.0 * value / peak,
+                "config": dict(config_dict(w), pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
+                               prep_ms_outside_step=res.prep_ms(torch),
+                               flops_per_step=w.flops),
+                "roofline": roofline(w, t, peak, peak_note), "clocks": t["clocks"]}
+        if args.sweep_oracle and w.N * w.kv_len * w.B * w.H <= 12 * 8192 * 8192:
+            line["oracle_full"] = oracle_full_timing(w, make_inputs(w))
+        print(json.dumps(line), flush=True)
+        del res
+        torch.cuda.empty_cache()
+
+
+def oracle_full_timing(w, x):
+    """The full fp64 oracle (``bob`` on every head: N x N matrices) on the
+    host cores; at most two heads are run and the rest extrapolated."""
+    from exact_second_order_gb300.inputs import NAMES, as_float64_numpy
+    from oracle import bob as orc
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    run = heads[:2]
+    G = w.H // w.kv_heads
+    t0 = time.perf_counter()
+    for b, h in run:
+        a = [as_float64_numpy(x[k][b, h // G if k in ("K", "V", "UK", "UV") else h])
+             for k in NAMES]
+        orc.bob(*a, w.tau, causal=w.causal)
+    el = time.perf_counter() - t0
+    return {"heads_run": len(run), "heads": len(heads), "seconds_run": el,
+            "seconds_full_call": el * len(heads) / len(run),
+            "note": "full_call extrapolated from the heads run" if len(run) < len(heads)
+                    else "every head run", "cores": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def main():
@@ -285,65 +510,18 @@ def main():
         torch.cuda.synchronize()
 
     x = make_inputs(rank_workload(w, rank))
-    dev = {k: v.cuda() for k, v in x.items()}
     if args.entry == "jvp":
+        dev = {k: v.cuda() for k, v in x.items()}
         return run_jvp(args, w, dev, rank, world, local, barrier, fb, torch)
-    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal)
-    out = fb.alloc_bob_outputs(dev["Q"], K=dev["K"])
-    stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        fb.flashbob_bob_pass1(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"],
-                              dev["UK"], dev["UV"], w.tau, out["dQt"], out["ddOt"],
-                              out["alpha"], out["E"], causal=w.causal, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        fb.flashbob_bob_pass2(dev["Q"], dev["K"], dev["V"], dev["dO"], L, D, out["alpha"],
-                              out["E"], dev["UQ"], dev["UK"], dev["UV"], w.tau, out["dKt"],
-                              out["dVt"], causal=w.causal, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(local).uuid)
-        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-    except Exception:
-        uuid = None
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sampler = ClockSampler(uuid)
-    time.sleep(0.3)
-    barrier()
-    for i in range(args.steps):
-        step(evs[i])
-    barrier()
-    clocks = sampler.stop()
-    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-    # prep (O, L, D) is not part of the step: timed on its own, after it
-    pev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    pev[0].record(stream)
-    for _ in range(3):
-        fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=w.causal, stream=stream)
-    pev[1].record(stream)
-    torch.cuda.synchronize()
-    prep_ms = pev[0].elapsed_time(pev[1]) / 3
-    total_ms = evs[0][0].elapsed_time(evs[-1][2])
-    p1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    p2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    total_ms = reduce_max(total_ms, world, "cuda")
+    res = Resident(w, x, fb, torch)
+    uuid = gpu_uuid(torch, local)
+    t = timed_steps(res, args.steps, args.warmup, torch, barrier, uuid)
+    prep_ms = res.prep_ms(torch)
+    total_ms = reduce_max(t["total_ms"], world, "cuda")
     ms_per_step = total_ms / args.steps
-    heads = w.B * w.H
-    # one Nq x Nk x d GEMM per (batch, head), over the visible pairs only
-    unit_flops = 2.0 * w.pairs * w.d * heads
-    flops = (PASS1_GEMMS + PASS2_GEMMS) * unit_flops
+    flops = w.flops
     value = job_tflops(flops, args.steps, world, total_ms)
+    dev, out, O, L, D, stream = res.dev, res.out, res.O, res.L, res.D, res.stream
 
     # end to end: pinned host inputs -> device, the C-ABI call, outputs -> host
     e2e = None
@@ -353,9 +531,9 @@ def main():
                       "D": D.cpu().pin_memory()}
         host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in out.items()}
         dev_state = {"O": O, "L": L, "D": D}
-        h2d = sum(t.numel() * t.element_size() for t in list(host_in.values())
+        h2d = sum(t_.numel() * t_.element_size() for t_ in list(host_in.values())
                   + list(host_state.values()))
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        d2h = sum(t_.numel() * t_.element_size() for t_ in host_out.values())
         n_e2e = max(3, args.steps // 2)
 
         def e2e_step():
@@ -384,48 +562,35 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / n_e2e, "steps": n_e2e}
 
-    peaks, peak_src = measured_peaks()
-    dominant = "pass1" if p1_ms >= p2_ms else "pass2"
-    dom_ms = p1_ms if dominant == "pass1" else p2_ms
-    dom_flops = (PASS1_GEMMS if dominant == "pass1" else PASS2_GEMMS) * unit_flops
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    traffic = read_traffic().get(dominant)
-    in_bytes = sum(t.numel() * t.element_size() for t in dev.values()) + sum(
-        t.numel() * t.element_size() for t in (O, L, D))
-
+    peak, sustained, peak_note = tensor_peak()
+    rl = roofline(w, t, peak, peak_note)
+    rl["traffic"] = read_traffic().get(rl["kernel"])
+    rl["frac_of_sustained"] = rl["achieved"] / sustained
+    in_bytes = res.input_bytes()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "N": w.N,
-                   "Nk": w.kv_len, "d": w.d, "causal": w.causal,
-                   "tau": w.tau, "flops_per_step_per_gpu": flops,
-                   "flop_convention": "38*N^2*d*B*H (19 GEMMs of 2*N^2*d); rectangular "
-                                      "N*Nk for N^2, causal the pairs j <= i",
-                   "l2": f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
-                         f"{L2_BYTES / 2**20:.0f} MiB",
-                   "pass1_ms": p1_ms, "pass2_ms": p2_ms,
-                   "prep_ms_outside_step": prep_ms,
-                   "pct_of_peak": 100.0 * (value / world) / peak,
-                   "paths": "tcgen05" if fb.flashbob_bob_tile_sizes(w.d, fb.FLASHBOB_BF16)[
-                       "Br1"] == 128 else "simt"},
-        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"bf16_tflops_sustained of {peak_src} peaks"},
+        "config": dict(config_dict(w), flops_per_step_per_gpu=flops,
+                       l2=f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
+                          f"{L2_BYTES / 2**20:.0f} MiB",
+                       pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"], prep_ms_outside_step=prep_ms,
+                       pct_of_peak=100.0 * (value / world) / peak,
+                       paths="tcgen05" if fb.flashbob_bob_tile_sizes(w.d, fb.FLASHBOB_BF16)[
+                           "Br1"] == 128 else "simt"),
+        "roofline": rl,
         "gpu_launches": 2 * args.steps,
-        "clocks": clocks,
+        "clocks": t["clocks"],
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows, el = oracle_rows_sample(w, x, args.cpu_seconds)
-        line["cpu_baseline"] = {
-            "value": rows * row_flops(w) / el / 1e12, "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{rows} seeded rows of head (0,0) through oracle.bob_rows (fp64 numpy, "
-                      f"{el:.1f} s); {row_flops(w):.3e} flops credited per row"}
+        line["cpu_baseline"] = oracle_baseline(w, oracle_sample(w, x, args.cpu_seconds))
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if args.sweep and world == 1:
+        del res, dev, out, O, L, D
+        torch.cuda.empty_cache()
+        run_sweep(args, fb, torch, barrier, uuid, peak, peak_note)
     if world > 1:
         dist.destroy_process_group()
 

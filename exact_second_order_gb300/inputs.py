@@ -97,8 +97,13 @@ EXTREME_D128 = Workload("extreme_B1_H1_N131072_d128", 1, 1, 131072, 128, "bf16")
 
 # Causal shapes of the pages' isolated-layer timing table (B=4, H=12, bf16).
 CAUSAL_N4096 = Workload("causal_B4_H12_N4096_d64", 4, 12, 4096, 64, "bf16", causal=True)
+CAUSAL_N8192 = Workload("causal_B4_H12_N8192_d64", 4, 12, 8192, 64, "bf16", causal=True)
 CAUSAL_N16384 = Workload("causal_B4_H12_N16384_d64", 4, 12, 16384, 64, "bf16", causal=True)
 CAUSAL_N16384_D128 = Workload("causal_B4_H12_N16384_d128", 4, 12, 16384, 128, "bf16",
+                              causal=True)
+CAUSAL_N32768_D128 = Workload("causal_B4_H12_N32768_d128", 4, 12, 32768, 128, "bf16",
+                              causal=True)
+CAUSAL_N65536_D128 = Workload("causal_B4_H12_N65536_d128", 4, 12, 65536, 128, "bf16",
                               causal=True)
 # Grouped-query attention: 12 query heads share 4 key/value heads (and a
 # multi-query variant with one shared head).
@@ -120,7 +125,8 @@ PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
 
 WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PEAKED,
                                  MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128,
-                                 CAUSAL_N4096, CAUSAL_N16384, CAUSAL_N16384_D128, GQA_N8192,
+                                 CAUSAL_N4096, CAUSAL_N8192, CAUSAL_N16384, CAUSAL_N16384_D128,
+                                 CAUSAL_N32768_D128, CAUSAL_N65536_D128, GQA_N8192,
                                  MQA_N8192,
                                  RECT_Q4096_K16384, RECT_Q16384_K4096, LONGLOOP_D64,
                                  LONGLOOP_EXTREME_D64, LONGLOOP_D128, PROFILE)}
