@@ -271,6 +271,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor, no swizzle, K-major: 8-row x 16-byte core
+// matrices; lbo = byte distance between core matrices adjacent along K,
+// sbo = byte distance between adjacent 8-row groups.  Layout type 0.
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Generic-proxy writes to shared memory (st.shared) made visible to the
+// async proxy (tcgen05.mma operand reads) before a barrier that orders them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, dense.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B
 // format (1 = bf16), 15 A major (0 = K), 16 B major (0 = K, 1 = MN),
@@ -292,6 +306,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// v = h + m + l with h, m, l bf16 (round to nearest each): h = bf16(v),
+// m = bf16(v - h), l = bf16(v - h - m).  Both differences are exact in fp32
+// (each part is within a factor 2 of what it rounds), so v - (h + m + l) is
+// below |v| 2^-24.  Returned as the bf16 pairs (h, m) and (l, 0).
+__device__ __forceinline__ uint2 split3_bf16(float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(m);
+  const __nv_bfloat16 l = __float2bfloat16_rn(r2);
+  return make_uint2((uint32_t)__bfloat16_as_ushort(h) | ((uint32_t)__bfloat16_as_ushort(m) << 16),
+                    (uint32_t)__bfloat16_as_ushort(l));
+}
 
 // Two fp32 lanes per instruction (sm_100 family: fma / mul / add .rn.f32x2).
 // Each lane rounds exactly like the scalar instruction, so a pair of

@@ -14,8 +14,9 @@
 // (F = tau (U_Q K^T + Q U_K^T), G = dO U_V^T; the same chain rule as pass 1).
 //
 // CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
-//   warp 0      TMA producer: the resident K, U_K, V, U_V block, then Q, U_Q,
-//               dO tiles of 64 query rows through a 4-stage mbarrier ring;
+//   warp 0      producer: TMA of the resident K, U_K, V, U_V block, then of
+//               Q, U_Q, dO tiles of 64 query rows through a 4-stage mbarrier
+//               ring, plus each tile's row-scalar columns (below);
 //   warp 1      TMEM allocator; one elected lane runs the whole MMA schedule
 //               (every barrier wait and every MMA);
 //   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: query rows 0-31 / 32-63
@@ -24,10 +25,18 @@
 // Every tcgen05.mma costs the pipe tens of cycles whatever its width, so
 // the tile is 64 query rows wide: the score GEMMs are K [Q; U_Q]^T (N = 128,
 // S^T and half of F'^T), U_K Q^T, V dO^T and U_V dO^T (N = 64 each).
+// Row scalars ride in the score GEMMs.  Each query row's L, D, alpha and
+// alpha D + E enter the score buffer through one more K step: an all-ones
+// A operand (TMEM) against a 16-column B tile the producer writes per query
+// tile, which holds -L / tau, -alpha / tau, -D and -(alpha D + E) as sums of
+// three bf16 parts (exact to 2^-24 relative).  The score buffer then holds
+// S^T - L / tau, F'^T - alpha / tau, dP^T - D and G^T - (alpha D + E), and
+// the element-wise code needs no per-column scalars at all.
 // TMEM: [0,64) d~K, [64,128) d~V accumulators; [128,384) one score buffer
 // S^T | F'^T | dP^T | G^T (64 columns each); [384,480) the bf16 A operands
-// dS^T, d~S^T, W^T of the output GEMMs.  Because the operands have their own
-// columns, the score buffer is released as soon as the warpgroups have read
+// dS^T, d~S^T, W^T of the output GEMMs; [480,488) the all-ones A operand.
+// Because the operands have their own columns, the score buffer is released
+// as soon as the warpgroups have read
 // it into registers, in two halves: S^T | F'^T first (read before any
 // arithmetic), then dP^T | G^T.  The score GEMMs of the next tile are issued
 // in the same two halves, so the S/F' half of tile t + 1 runs on the tensor
@@ -48,10 +57,16 @@ constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
 constexpr uint32_t TILE_BYTES = BQ * DH * 2;   // 8 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
+constexpr uint32_t EX_BYTES = 2 * BQ * 16 * 2;  // 128 rows x 16 bf16: one extra K step
+
 struct Smem2 {
   alignas(1024) uint8_t kb[4][BLOCK_BYTES];      // K, U_K, V, U_V (resident)
   alignas(1024) uint8_t st[NST][3][TILE_BYTES];  // Q, U_Q, dO (Q|U_Q adjacent)
-  float4 scal[2][4][32];  // per warpgroup, a ring of four tiles' row scalars (see stage())
+  // Row-scalar K step of each stage: [0] for S^T | F'^T (rows 0-63: -L/tau
+  // of query rows 0-63, rows 64-127: -alpha/tau), [1] for dP^T | G^T (-D,
+  // -(alpha D + E)).  No swizzle, K-major: 8-row x 16-byte core matrices,
+  // row r at (r / 8) * 256 + (r % 8) * 16, k 8-15 128 bytes further.
+  alignas(1024) uint8_t ex[NST][2][EX_BYTES];
   uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
@@ -64,6 +79,7 @@ struct Smem2 {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Smem2) + 1024 <= 232448, "shared memory");
 
 // TMEM columns.
 constexpr uint32_t kAccK = 0, kAccV = 64;
@@ -71,6 +87,10 @@ constexpr uint32_t kSc = 128;  // score buffer
 constexpr uint32_t kColS = 0, kColF = 64, kColdP = 128, kColG = 192;  // inside the score buffer
 constexpr uint32_t kOp = 384;  // operand area: operand x, K step kk at kOp + 32 x + 8 kk
 constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
+constexpr uint32_t kOnes = 480;  // all-ones A operand (k = 0, 1, 2) of the row-scalar K step
+// Padded query rows (i >= N_q, zero-filled by TMA) get -L / tau = -kFar, so
+// their P = exp2(c1 (0 - kFar)) is exactly 0.
+constexpr float kFar = 1e30f;
 // Cluster split: a row of staged partial sums (d~K | d~V, fp32) in the ring
 // buffer, padded against bank conflicts.
 constexpr int kStageStride = 2 * DH + 4;
@@ -81,31 +101,31 @@ __device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
 }
 
 // 16 query rows (one K step of the output GEMMs) of the score buffer, one
-// key row per thread: dS, d~S and W packed as bf16 pairs (8 registers each).
-// Two query rows per step in the paired fp32 instructions; scal holds, per
-// pair of rows, (-L log2 e, -D) and (-alpha, -(alpha D + E)) of both.  With
-// X = dP - D:  F o X + G - alpha dP - E = X (F - alpha) + G - (alpha D + E).
+// key row per thread: dS, d~S and W packed as bf16 pairs (8 registers each),
+// two query rows per step in the paired fp32 instructions.  The buffer
+// already holds S' = S^T - L / tau, F'' = F'^T - alpha / tau, X = dP^T - D
+// and G' = G^T - (alpha D + E), so with F - alpha = tau F'':
+//     P = exp2(tau log2(e) S'),  dS = P X,  W = P (F - alpha),
+//     d~S = P (X (F - alpha) + G')   (= P (F X + G - alpha dP - E)).
 template <bool MASKED>
 __device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t (&dp)[16],
                                          const uint32_t (&f)[16], const uint32_t (&g)[16],
-                                         const float4* scal, int ibase, int gj, float c1,
-                                         float tau, uint32_t (&ods)[8], uint32_t (&odst)[8],
+                                         int ibase, int gj, float c1, float tau,
+                                         uint32_t (&ods)[8], uint32_t (&odst)[8],
                                          uint32_t (&ow)[8]) {
   const float2 c12 = make_float2(c1, c1), tau2 = make_float2(tau, tau);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    const float4 sa = scal[e], sb = scal[e + 1];
-    const float2 t = ffma2(f2(s[e], s[e + 1]), c12, make_float2(sa.x, sa.y));
+    const float2 t = fmul2(f2(s[e], s[e + 1]), c12);
     float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
     if (MASKED) {
       if (ibase + e < gj) p.x = 0.f;
       if (ibase + e + 1 < gj) p.y = 0.f;
     }
-    const float2 x = fadd2(f2(dp[e], dp[e + 1]), make_float2(sa.z, sa.w));       // dP - D
-    const float2 w0 = ffma2(f2(f[e], f[e + 1]), tau2, make_float2(sb.x, sb.y));  // F - alpha
+    const float2 x = f2(dp[e], dp[e + 1]);
+    const float2 w0 = fmul2(f2(f[e], f[e + 1]), tau2);  // F - alpha
     const float2 vds = fmul2(p, x);
-    const float2 vdst =
-        fmul2(p, fadd2(ffma2(x, w0, f2(g[e], g[e + 1])), make_float2(sb.z, sb.w)));
+    const float2 vdst = fmul2(p, ffma2(x, w0, f2(g[e], g[e + 1])));
     const float2 vw = fmul2(p, w0);
     ods[e >> 1] = pack_bf16x2(vds.x, vds.y);
     odst[e >> 1] = pack_bf16x2(vdst.x, vdst.y);
@@ -121,9 +141,9 @@ __device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t
 // the second's.  The release does not wait for the output GEMMs, and only
 // one chunk's operands are live at a time.
 template <bool MASKED>
-__device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const float4* scal,
-                                        int ibase, int gj, float c1, float tau, Smem2& sm,
-                                        int t, volatile int* abort_flag, unsigned int* err) {
+__device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, int ibase, int gj,
+                                        float c1, float tau, Smem2& sm, int t,
+                                        volatile int* abort_flag, unsigned int* err) {
   const int col = 32 * wg;
   const int kk = 2 * wg;
   uint32_t s0[16], f0[16], s1[16], f1[16];
@@ -140,7 +160,7 @@ __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const
     tmem_ld16(sc + kColdP + col, dp);
     tmem_ld16(sc + kColG + col, g);
     tmem_wait_ld();
-    p2_chunk<MASKED>(s0, dp, f0, g, scal, ibase, gj, c1, tau, a_ds, a_dst, a_w);
+    p2_chunk<MASKED>(s0, dp, f0, g, ibase, gj, c1, tau, a_ds, a_dst, a_w);
   }
   uint32_t dp[16], g[16];
   tmem_ld16(sc + kColdP + col + 16, dp);
@@ -155,7 +175,7 @@ __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, const
   tmem_st8(opb + op_col(kOpW, kk), a_w);
   {
     uint32_t o_ds[8], o_dst[8], o_w[8];
-    p2_chunk<MASKED>(s1, dp, f1, g, scal + 16, ibase + 16, gj, c1, tau, o_ds, o_dst, o_w);
+    p2_chunk<MASKED>(s1, dp, f1, g, ibase + 16, gj, c1, tau, o_ds, o_dst, o_w);
     tmem_st8(opb + op_col(kOpdS, kk + 1), o_ds);
     tmem_st8(opb + op_col(kOpdSt, kk + 1), o_dst);
     tmem_st8(opb + op_col(kOpW, kk + 1), o_w);
@@ -204,7 +224,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_kv, 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&sm.st_full[s], 1);
+      mbar_init(&sm.st_full[s], 2);  // the TMA transaction, and the row-scalar K step written
       mbar_init(&sm.st_empty[s], 1);
     }
     mbar_init(&sm.sc_full, 1);
@@ -221,8 +241,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  if (warp >= 2 && warp < 6) {
+    // The all-ones A operand of the row-scalar K step: k = 0, 1, 2 are 1
+    // (column c holds k = 2c in its low half, 2c + 1 in its high half).
+    const uint32_t one = 0x3F80u;  // bf16 1.0
+    const uint32_t v[8] = {one | (one << 16), one, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st8(tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kOnes, v);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == 0) {
+    // Producer.  Lane 0 issues the TMA copies; the whole warp writes the
+    // row-scalar K step of every tile: lane l takes query rows l and l + 32.
+    const float inv_tau = 1.f / tau;
+    auto load_rows = [&](int f, float4 (&v)[2]) {
+      // (L, D, alpha, E) of rows lane, lane + 32 of streamed tile f; a row
+      // past N_q (or a tile past the last) is marked by L = NaN.
+      v[0] = v[1] = make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
+      if (f >= T) return;
+      const int zq = hq0 + f / Tq, row0 = (f % Tq + t0) * BQ;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = row0 + lane + 32 * h;
+        if (i < Nq) {
+          const size_t o = static_cast<size_t>(zq) * Nq + i;
+          v[h] = make_float4(L[o], D[o], alpha[o], E[o]);
+        }
+      }
+    };
     if (lane == 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mUQ);
@@ -232,17 +281,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_load_3d(sm.kb[1], &mUK, &sm.bar_kv, 0, j0, bkv);
       tma_load_3d(sm.kb[2], &mV, &sm.bar_kv, 0, j0, bkv);
       tma_load_3d(sm.kb[3], &mUV, &sm.bar_kv, 0, j0, bkv);
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
-        const int s = t % NST;
-        if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+    }
+    float4 cur[2];
+    load_rows(0, cur);
+    int issued = 0;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % NST;
+      if (t >= NST && !mbar_wait_warp(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err))
+        break;
+      if (lane == 0) {
         const int row = (t % Tq + t0) * BQ, zq = hq0 + t / Tq;
         mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
         tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, row, zq);
         tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, row, zq);
         tma_load_3d(sm.st[s][2], &mdO, &sm.st_full[s], 0, row, zq);
-        issued = t + 1;
       }
+      // Four B rows per query row: k = 0, 1, 2 hold the three bf16 parts of
+      // the scalar, k = 3 .. 15 zero.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 v = cur[h];
+        const bool pad = v.x != v.x;
+        const float vals[4] = {pad ? -kFar : -v.x * inv_tau, -v.z * inv_tau, -v.y,
+                               -fmaf(v.z, v.y, v.w)};
+        const int r = lane + 32 * h;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = r + BQ * (q & 1);  // -L/tau, -alpha/tau ; -D, -(alpha D + E)
+          uint8_t* base = sm.ex[s][q >> 1] + (row >> 3) * 256 + (row & 7) * 16;
+          const uint2 hm_l0 = split3_bf16(vals[q]);
+          *reinterpret_cast<uint4*>(base) = make_uint4(hm_l0.x, hm_l0.y, 0u, 0u);
+          *reinterpret_cast<uint4*>(base + 128) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.st_full[s]);
+      issued = t + 1;
+      load_rows(t + 1, cur);  // lands while the ring is full
+    }
+    if (lane == 0) {
       // No copy may still be in flight when the CTA exits.
       drain_wait(&sm.bar_kv, 0);
       for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
@@ -261,6 +339,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dQ0 = smem_desc_sw128(st0, 16, 1024);                   // Q (and Q;U_Q)
     const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
     const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
+    const uint64_t dEx0 = smem_desc_noswz(smem_u32(sm.ex[0][0]), 128, 256);
+    constexpr uint64_t kExStage = (2 * EX_BYTES) >> 4, kExPG = EX_BYTES >> 4;
     const uint32_t sc = tbase + kSc;
     // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
     auto issue_sf = [&](int t) {
@@ -272,6 +352,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColS, dK + o, dQ0 + so + o, idS128, kk > 0);  // [S^T | F'^T] = K [Q; U_Q]^T
           mma_ss(sc + kColF, dUK + o, dQ0 + so + o, idS64, 1);       // F'^T += U_K Q^T
         }
+        // [S^T | F'^T] += 1 [-L / tau | -alpha / tau]^T (the row-scalar K step)
+        mma_ts(sc + kColS, tbase + kOnes, dEx0 + (t % NST) * kExStage, idS128, 1);
       }
     };
     auto issue_pg = [&](int t) {
@@ -283,6 +365,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColdP, dV + o, ddO0 + so + o, idS64, kk > 0);  // dP^T = V dO^T
           mma_ss(sc + kColG, dUV + o, ddO0 + so + o, idS64, kk > 0);  // G^T  = U_V dO^T
         }
+        // [dP^T | G^T] += 1 [-D | -(alpha D + E)]^T
+        mma_ts(sc + kColdP, tbase + kOnes, dEx0 + (t % NST) * kExStage + kExPG, idS128, 1);
         mma_commit(&sm.sc_full);
       }
     };
@@ -348,66 +432,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float c1 = tau * kLog2e;
     const uint32_t sc = tbase + lane_off + kSc;
     const uint32_t opb = tbase + lane_off;
-    const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
     bool ok = true;
-
-    // Row scalars (L, D, alpha, E) of this warpgroup's 32 query rows of
-    // streamed tile f, which is tile ft of the head whose L row starts at
-    // fL; rows past Nq get L = +inf so that P = exp2(-inf) = 0.  (ft, fL)
-    // step along with f (calls come in order) instead of dividing f by Tq.
-    // The loads are only issued here: nothing uses the values until
-    // stage() at the end of the tile, so the warp does not wait for them.
-    int ft = 0;
-    const float* fL = L + static_cast<size_t>(hq0) * Nq;
-    auto load_scalars = [&](int f) {
-      const int i = (ft + t0) * BQ + 32 * wg + lane;
-      float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
-      if (f < T && i < Nq) {
-        const size_t o = static_cast<size_t>(fL - L) + i;
-        v = make_float4(fL[i], D[o], alpha[o], E[o]);
-      }
-      if (++ft == Tq) { ft = 0; fL += Nq; }
-      return v;
-    };
-    // What the element-wise code reads, negated and interleaved by pairs of
-    // query rows (lane = row): (-L log2 e, -D) of rows 2m, 2m + 1 in float4
-    // 2m, (-alpha, -(alpha D + E)) in float4 2m + 1.
-    auto stage = [&](float4* dst, float4 v) {
-      float* pr = reinterpret_cast<float*>(dst + (lane & ~1)) + (lane & 1);
-      pr[0] = -(v.x * kLog2e);
-      pr[2] = -v.y;
-      pr[4] = -v.z;
-      pr[6] = -fmaf(v.z, v.y, v.w);
-    };
-    // The loader warp stages the scalars of two tiles at a time, at the
-    // warpgroup barrier of every even tile t: those of tiles t + 2 and t + 3,
-    // fetched into registers two tiles earlier (so their global-memory
-    // latency hides behind two tiles), into ring slots that tiles t - 2 and
-    // t - 1 used (every warp has passed the barrier, so none still reads
-    // them).  Tiles t and t + 1 were staged at the barrier of tile t - 2.
-    float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
-    if (loader) {
-      const float4 v0 = load_scalars(0), v1 = load_scalars(1);
-      stage(sm.scal[wg][0], v0);
-      stage(sm.scal[wg][1], v1);
-      n0 = load_scalars(2);
-      n1 = load_scalars(3);
-    }
     int tq = 0;  // tile of the current query head, (t mod Tq)
     for (int t = 0; t < T; ++t) {
-      const float4* scal = sm.scal[wg][t & 3];
-      if ((t & 1) == 0) {
-        named_bar_sync(2 + wg, 128);  // tiles t, t + 1 staged; tiles t - 2, t - 1 read
-        if (loader) {
-          stage(sm.scal[wg][(t + 2) & 3], n0);
-          stage(sm.scal[wg][(t + 3) & 3], n1);
-          n0 = load_scalars(t + 4);
-          n1 = load_scalars(t + 5);
-        }
-      }
       // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
-      // failed wait keep looping so every thread passes the same named
-      // barriers, but skip the work.
+      // failed wait the remaining tiles are skipped.
       ok = ok && mbar_wait_warp(&sm.sc_full, t & 1, abort_flag, err);
       if (ok) {
         tc_fence_after();
@@ -415,9 +444,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // tiles that overlap the key block take the masked path.
         const int ibase = (tq + t0) * BQ + 32 * wg;
         if (causal && ibase < j0 + BM)
-          ok = p2_half<true>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+          ok = p2_half<true>(sc, opb, wg, ibase, gj, c1, tau, sm, t, abort_flag, err);
         else
-          ok = p2_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+          ok = p2_half<false>(sc, opb, wg, ibase, gj, c1, tau, sm, t, abort_flag, err);
       }
       if (++tq == Tq) tq = 0;
     }

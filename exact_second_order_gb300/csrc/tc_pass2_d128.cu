@@ -12,15 +12,22 @@
 //     d~K_j = tau sum_i (d~S_ij Q_i + dS_ij U_Q,i),   d~V_j = sum_i W_ij dO_i.
 //
 // CTA = 128 key rows (MMA M = 128, one TMEM lane per key row), 320 threads:
-//   warp 0      TMA: the resident K, U_K, V, U_V block (each as two 64-column
-//               halves in the 128-byte swizzle), then Q, U_Q, dO tiles of 32
-//               query rows through a 3-stage ring;
+//   warp 0      producer: TMA of the resident K, U_K, V, U_V block (each as
+//               two 64-column halves in the 128-byte swizzle), then of Q,
+//               U_Q, dO tiles of 32 query rows through a 3-stage ring, plus
+//               each tile's row-scalar K step;
 //   warp 1      TMEM allocation and MMA issue;
 //   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: query rows 0-15 / 16-31
 //               of every tile (the K step of the output GEMMs they feed).
+// Row scalars ride in the score GEMMs as at head dim 64: one more K step,
+// an all-ones A operand in TMEM against a 16-column B tile that the producer
+// writes per query tile (-L / tau, -alpha / tau, -D, -(alpha D + E), each as
+// three bf16 parts), leaves S^T - L / tau, F'^T - alpha / tau, dP^T - D and
+// G^T - (alpha D + E) in the score buffer.
 // TMEM: [0,128) d~K, [128,256) d~V accumulators; [256,384) one score buffer
 // S^T | F'^T | dP^T | G^T (32 columns each); [384,432) the bf16 A operands
-// dS^T, d~S^T, W^T.  The score buffer is released in two halves, S^T | F'^T
+// dS^T, d~S^T, W^T; [432,440) the all-ones A operand.  The score buffer is
+// released in two halves, S^T | F'^T
 // first, so the S/F' GEMMs of the next tile run while the warpgroups still
 // read and process dP/G.  Grouped-query attention: the query tiles of all
 // H / Hkv heads sharing the key/value head stream past the same block
@@ -41,11 +48,15 @@ constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB
 constexpr uint32_t HALF_TILE = BQ * 64 * 2;   // 4 KiB
 constexpr uint32_t STAGE_BYTES = 2 * 3 * HALF_TILE;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t EX_BYTES = 2 * BQ * 16 * 2;  // 64 rows x 16 bf16: one extra K step
 
 struct SmemW2 {
   alignas(1024) uint8_t kb[4][2][HALF_BLOCK];         // K, U_K, V, U_V (resident) x halves
   alignas(1024) uint8_t st[NST][2][3][HALF_TILE];     // [stage][half][Q, U_Q, dO]
-  float4 scal[2][2][16];  // per warpgroup, double-buffered row scalars (see stage())
+  // Row-scalar K step of each stage: [0] for S^T | F'^T (rows 0-31: -L/tau,
+  // rows 32-63: -alpha/tau), [1] for dP^T | G^T (-D, -(alpha D + E)); no
+  // swizzle, K-major, row r at (r / 8) * 256 + (r % 8) * 16, k 8-15 at +128.
+  alignas(1024) uint8_t ex[NST][2][EX_BYTES];
   uint64_t bar_kv;
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
@@ -65,6 +76,8 @@ constexpr uint32_t kSc = 256;
 constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;  // inside the score buffer
 constexpr uint32_t kOp = 384;  // operand x, K step kk at kOp + 16 x + 8 kk
 constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
+constexpr uint32_t kOnes = 432;  // all-ones A operand (k = 0, 1, 2) of the row-scalar K step
+constexpr float kFar = 1e30f;    // -L / tau of a padded query row: its P is exactly 0
 // Cluster split: staged partial rows d~K | d~V (64 float4 each) fill the
 // 128 KiB of the resident block exactly; float4 c of row r sits at
 // c ^ (r mod 8) against bank conflicts.
@@ -76,11 +89,14 @@ __device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
 
 // The 16 query rows of one warpgroup: read S^T, F'^T (release), dP^T, G^T
 // (release), form dS, d~S, W as bf16 pairs and write them to the operand
-// area once the previous tile's output GEMMs are done with it.
+// area once the previous tile's output GEMMs are done with it.  The buffer
+// holds S' = S^T - L / tau, F'' = F'^T - alpha / tau, X = dP^T - D and
+// G' = G^T - (alpha D + E): P = exp2(tau log2(e) S'), dS = P X,
+// W = P (F - alpha) with F - alpha = tau F'', d~S = P (X (F - alpha) + G').
 template <bool MASKED>
-__device__ __forceinline__ bool p2w_half(uint32_t sc, uint32_t opb, int wg, const float4* scal,
-                                         int ibase, int gj, float c1, float tau, SmemW2& sm,
-                                         int t, volatile int* abort_flag, unsigned int* err) {
+__device__ __forceinline__ bool p2w_half(uint32_t sc, uint32_t opb, int wg, int ibase, int gj,
+                                         float c1, float tau, SmemW2& sm, int t,
+                                         volatile int* abort_flag, unsigned int* err) {
   const int col = 16 * wg;
   uint32_t s[16], f[16], dp[16], g[16];
   tmem_ld16(sc + kColS + col, s);
@@ -95,23 +111,18 @@ __device__ __forceinline__ bool p2w_half(uint32_t sc, uint32_t opb, int wg, cons
   warp_arrive(&sm.pg_free);
   uint32_t ods[8], odst[8], ow[8];
   const float2 c12 = make_float2(c1, c1), tau2 = make_float2(tau, tau);
-  // Two query rows per step in the paired fp32 instructions; scal holds, per
-  // pair of rows, (-L log2 e, -D) and (-alpha, -(alpha D + E)) of both.  With
-  // X = dP - D:  F o X + G - alpha dP - E = X (F - alpha) + G - (alpha D + E).
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    const float4 sa = scal[e], sb = scal[e + 1];
-    const float2 tt = ffma2(f2(s[e], s[e + 1]), c12, make_float2(sa.x, sa.y));
+    const float2 tt = fmul2(f2(s[e], s[e + 1]), c12);
     float2 p = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
     if (MASKED) {
       if (ibase + e < gj) p.x = 0.f;
       if (ibase + e + 1 < gj) p.y = 0.f;
     }
-    const float2 x = fadd2(f2(dp[e], dp[e + 1]), make_float2(sa.z, sa.w));       // dP - D
-    const float2 w0 = ffma2(f2(f[e], f[e + 1]), tau2, make_float2(sb.x, sb.y));  // F - alpha
+    const float2 x = f2(dp[e], dp[e + 1]);
+    const float2 w0 = fmul2(f2(f[e], f[e + 1]), tau2);  // F - alpha
     const float2 vds = fmul2(p, x);
-    const float2 vdst =
-        fmul2(p, fadd2(ffma2(x, w0, f2(g[e], g[e + 1])), make_float2(sb.z, sb.w)));
+    const float2 vdst = fmul2(p, ffma2(x, w0, f2(g[e], g[e + 1])));
     const float2 vw = fmul2(p, w0);
     ods[e >> 1] = pack_bf16x2(vds.x, vds.y);
     odst[e >> 1] = pack_bf16x2(vdst.x, vdst.y);
@@ -164,7 +175,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_kv, 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&sm.st_full[s], 1);
+      mbar_init(&sm.st_full[s], 2);  // the TMA transaction, and the row-scalar K step written
       mbar_init(&sm.st_empty[s], 1);
     }
     mbar_init(&sm.sc_full, 1);
@@ -181,8 +192,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  if (warp >= 2 && warp < 6) {
+    // The all-ones A operand: k = 0, 1, 2 are 1 (column c: k = 2c low, 2c + 1 high).
+    const uint32_t one = 0x3F80u;  // bf16 1.0
+    const uint32_t v[8] = {one | (one << 16), one, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st8(tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kOnes, v);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == 0) {
+    // Producer.  Lane 0 issues the TMA copies; lane l writes the row-scalar
+    // K step of query row l of every tile.
+    const float inv_tau = 1.f / tau;
+    auto load_row = [&](int f) {
+      // (L, D, alpha, E) of row `lane` of streamed tile f; a row past N_q
+      // (or a tile past the last) is marked by L = NaN.
+      float4 v = make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
+      if (f >= T) return v;
+      const int i = (f % Tq + t0) * BQ + lane;
+      if (i < Nq) {
+        const size_t o = static_cast<size_t>(hq0 + f / Tq) * Nq + i;
+        v = make_float4(L[o], D[o], alpha[o], E[o]);
+      }
+      return v;
+    };
     if (lane == 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mUQ);
@@ -194,20 +230,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_3d(sm.kb[2][h], &mV, &sm.bar_kv, 64 * h, j0, bkv);
         tma_load_3d(sm.kb[3][h], &mUV, &sm.bar_kv, 64 * h, j0, bkv);
       }
-      int issued = 0, ft = 0, fz = hq0;  // (tile in head, query head) of tile t
-      for (int t = 0; t < T; ++t) {
-        const int s = t % NST;
-        if (t >= NST && !mbar_wait(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
-        const int row = (ft + t0) * BQ;
+    }
+    float4 cur = load_row(0);
+    int issued = 0;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % NST;
+      if (t >= NST && !mbar_wait_warp(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err))
+        break;
+      if (lane == 0) {
+        const int row = (t % Tq + t0) * BQ, fz = hq0 + t / Tq;
         mbar_expect_tx(&sm.st_full[s], STAGE_BYTES);
         for (int h = 0; h < 2; ++h) {
           tma_load_3d(sm.st[s][h][0], &mQ, &sm.st_full[s], 64 * h, row, fz);
           tma_load_3d(sm.st[s][h][1], &mUQ, &sm.st_full[s], 64 * h, row, fz);
           tma_load_3d(sm.st[s][h][2], &mdO, &sm.st_full[s], 64 * h, row, fz);
         }
-        if (++ft == Tq) { ft = 0; ++fz; }
-        issued = t + 1;
       }
+      {
+        const bool pad = cur.x != cur.x;
+        const float vals[4] = {pad ? -kFar : -cur.x * inv_tau, -cur.z * inv_tau, -cur.y,
+                               -fmaf(cur.z, cur.y, cur.w)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = lane + BQ * (q & 1);  // -L/tau, -alpha/tau ; -D, -(alpha D + E)
+          uint8_t* base = sm.ex[s][q >> 1] + (row >> 3) * 256 + (row & 7) * 16;
+          const uint2 hm_l0 = split3_bf16(vals[q]);
+          *reinterpret_cast<uint4*>(base) = make_uint4(hm_l0.x, hm_l0.y, 0u, 0u);
+          *reinterpret_cast<uint4*>(base + 128) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.st_full[s]);
+      issued = t + 1;
+      cur = load_row(t + 1);  // lands while the ring is full
+    }
+    if (lane == 0) {
       // No copy may still be in flight when the CTA exits.
       drain_wait(&sm.bar_kv, 0);
       for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
@@ -234,6 +292,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dQmn = smem_desc_sw128(smem_u32(sm.st[0][0][0]), kHalfStride, 1024);
     const uint64_t dUQmn = smem_desc_sw128(smem_u32(sm.st[0][0][1]), kHalfStride, 1024);
     const uint64_t ddOmn = smem_desc_sw128(smem_u32(sm.st[0][0][2]), kHalfStride, 1024);
+    const uint64_t dEx0 = smem_desc_noswz(smem_u32(sm.ex[0][0]), 128, 256);
+    constexpr uint64_t kExStage = (2 * EX_BYTES) >> 4, kExPG = EX_BYTES >> 4;
     const uint32_t sc = tbase + kSc;
     // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
     auto issue_sf = [&](int t) {
@@ -246,6 +306,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColS, dK[h] + o, dQ[h] + so + o, idS64, kk > 0);  // [S^T | F'^T] = K [Q; U_Q]^T
           mma_ss(sc + kColF, dUK[h] + o, dQ[h] + so + o, idS32, 1);      // F'^T += U_K Q^T
         }
+        // [S^T | F'^T] += 1 [-L / tau | -alpha / tau]^T (the row-scalar K step)
+        mma_ts(sc + kColS, tbase + kOnes, dEx0 + (t % NST) * kExStage, idS64, 1);
       }
     };
     auto issue_pg = [&](int t) {
@@ -258,6 +320,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColdP, dV[h] + o, ddO[h] + so + o, idS32, kk > 0);  // dP^T = V dO^T
           mma_ss(sc + kColG, dUV[h] + o, ddO[h] + so + o, idS32, kk > 0);  // G^T  = U_V dO^T
         }
+        // [dP^T | G^T] += 1 [-D | -(alpha D + E)]^T
+        mma_ts(sc + kColdP, tbase + kOnes, dEx0 + (t % NST) * kExStage + kExPG, idS64, 1);
         mma_commit(&sm.sc_full);
       }
     };
@@ -321,55 +385,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float c1 = tau * kLog2e;
     const uint32_t sc = tbase + lane_off + kSc;
     const uint32_t opb = tbase + lane_off;
-    const bool loader = (warp & 3) == 0;  // one warp per warpgroup stages the row scalars
     bool ok = true;
-
-    // Row scalars of this warpgroup's 16 query rows of streamed tile f
-    // (tile ft of the head whose rows start at fL - L); rows past Nq get
-    // L = +inf so that P = exp2(-inf) = 0.  Lanes 16..31 load nothing.
-    int ft = 0;
-    const float* fL = L + static_cast<size_t>(hq0) * Nq;
-    auto load_scalars = [&](int f) {
-      const int i = (ft + t0) * BQ + 16 * wg + lane;
-      float4 v = make_float4(INFINITY, 0.f, 0.f, 0.f);
-      if (lane < 16 && f < T && i < Nq) {
-        const size_t o = static_cast<size_t>(fL - L) + i;
-        v = make_float4(fL[i], D[o], alpha[o], E[o]);
-      }
-      if (++ft == Tq) { ft = 0; fL += Nq; }
-      return v;
-    };
-    // Only the loads are issued in load_scalars; the values are first used
-    // here, at the end of the tile, negated and interleaved by pairs of rows
-    // (lane = row): (-L log2 e, -D) of rows 2m, 2m + 1 in float4 2m,
-    // (-alpha, -(alpha D + E)) in float4 2m + 1.
-    auto stage = [&](float4* dst, float4 v) {
-      float* pr = reinterpret_cast<float*>(dst + (lane & ~1)) + (lane & 1);
-      pr[0] = -(v.x * kLog2e);
-      pr[2] = -v.y;
-      pr[4] = -v.z;
-      pr[6] = -fmaf(v.z, v.y, v.w);
-    };
-    if (loader) {
-      const float4 v = load_scalars(0);
-      if (lane < 16) stage(sm.scal[wg][0], v);
-    }
     int tq = 0;  // tile of the current query head
     for (int t = 0; t < T; ++t) {
-      const float4* scal = sm.scal[wg][t & 1];
-      named_bar_sync(2 + wg, 128);  // scal is written; last tile's readers are done
-      float4 next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (loader) next = load_scalars(t + 1);
       ok = ok && mbar_wait_warp(&sm.sc_full, t & 1, abort_flag, err);
       if (ok) {
         tc_fence_after();
         const int ibase = (tq + t0) * BQ + 16 * wg;
         if (causal && ibase < j0 + BM)
-          ok = p2w_half<true>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+          ok = p2w_half<true>(sc, opb, wg, ibase, gj, c1, tau, sm, t, abort_flag, err);
         else
-          ok = p2w_half<false>(sc, opb, wg, scal, ibase, gj, c1, tau, sm, t, abort_flag, err);
+          ok = p2w_half<false>(sc, opb, wg, ibase, gj, c1, tau, sm, t, abort_flag, err);
       }
-      if (loader && lane < 16) stage(sm.scal[wg][(t + 1) & 1], next);
       if (++tq == Tq) tq = 0;
     }
 
