@@ -3,24 +3,24 @@
 // head dim 64 or 128 ("FlashAttention 的反向传播设计" blog, sections 一 and
 // 二; D as in "FlashBoB" paper notes, 关键设计 1).
 //
-// Two phases inside one CTA of 128 query rows, both streaming the same key
-// tiles (128 keys at d = 64, 64 at d = 128):
-//   phase A: S = Q K^T on the tensor cores (one N = 128 or 64 MMA per K
-//            step); the elementwise warpgroups keep a running row max m and
-//            sum l of exp2(S tau log2 e - m), which gives L at the end;
-//   phase B: S = Q K^T again, P = exp(S - L) (already normalised, so the
-//            accumulator never needs rescaling) goes to TMEM as bf16 over
-//            the consumed score columns and O += P V runs with A read from
-//            TMEM.
-// The epilogue writes O and the row scalars; D comes from dO (bf16, read
-// from global memory) dotted with the fp32 O.
+// One pass over the key tiles (128 keys at d = 64, 64 at d = 128) per CTA
+// of 128 query rows, with the softmax normalised at the end: S = Q K^T on
+// the tensor cores, P~ = exp2(S tau log2 e - m) with a running row maximum
+// m, l = sum P~, and O~ += P~ V with P~ read from TMEM as bf16.  m is raised
+// only when a tile's maximum exceeds it by more than kRescale (log2 units):
+// then l and O~ are multiplied by exp2(m_old - m_new) first; otherwise P~
+// stays below 2^kRescale and the stale m is kept.  At the end O = O~ / l
+// and L = (m + log2 l) ln 2.  One exponential per score element.
 //
 // 320 threads: warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps 2-5
-// and 6-9 elementwise warpgroups on alternate tiles.  TMEM: [0,DH) O, then
-// three score buffers of one tile each; the score GEMMs of tile t + 3 go
-// into tile t's buffer as soon as its warpgroup has finished with it, so a
-// warpgroup finds its next tile's scores ready.  A row of 128 columns is
-// two 64-column boxes in the 128-byte swizzle.
+// and 6-9 elementwise warpgroups on alternate tiles.  Each warpgroup keeps
+// its own (m, l) and its own O~ accumulator, so its rescales never touch the
+// other's; the two are merged in the epilogue.  TMEM: [0, DH) O~ of
+// warpgroup 0, [DH, 2 DH) of warpgroup 1, then three score buffers of one
+// tile each; the score GEMMs of tile t + 3 go into tile t's buffer right
+// after tile t's P V GEMMs, so a warpgroup finds its next tile's scores
+// ready.  A row of 128 columns is two 64-column boxes in the 128-byte
+// swizzle.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -34,14 +34,15 @@ constexpr int NBUF = 3;  // score buffers
 constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 128 rows x 64 columns bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.f;  // P~ <= 2^8 between rescales
 
 template <int DH>
 struct PrepCfg {
   static constexpr int kHalves = DH / 64;
   static constexpr int kBN = DH == 64 ? 128 : 64;          // keys per streamed tile
-  static constexpr int kStages = 5;
+  static constexpr int kStages = DH == 64 ? 4 : 5;
   static constexpr uint32_t kHalfTile = kBN * 64 * 2;       // kBN rows x 64 columns bf16
-  static_assert(DH + NBUF * kBN <= 512, "TMEM columns");
+  static_assert(2 * DH + NBUF * kBN <= 512, "TMEM columns");
 };
 
 template <int DH>
@@ -58,60 +59,45 @@ struct Smem0 {
   uint64_t kv_empty[NST];
   uint64_t sc_full[NBUF];
   uint64_t op_ready[NBUF];
+  uint64_t pv_done[2];  // per warpgroup: the P V GEMMs of its latest tile have completed
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// Phase A on 64 columns of a tile (one row per thread): fold them into the
-// running (m, l) of exp2(S c1 - m).  Invisible columns (past Nk or, causal,
-// past the row) do not count.
+// Largest visible raw score of 64 columns (c1 > 0, so max(S) c1 = max(S c1)).
 template <bool MASKED>
-__device__ __forceinline__ void prep_rowsum(const uint32_t (&s)[4][16], int jbase, int jmax,
-                                            float c1, float& m, float& l) {
-  float mr = -INFINITY;  // max of the raw scores (c1 > 0, so max(S) c1 = max(S c1) exactly)
+__device__ __forceinline__ float prep_max64(const uint32_t (&s)[4][16], int jbase, int jmax) {
+  float mr = -INFINITY;
 #pragma unroll
   for (int q = 0; q < 4; ++q)
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (!MASKED || jbase + 16 * q + j <= jmax) mr = fmaxf(mr, u2f(s[q][j]));
-  const float mx = fmaxf(m, mr * c1);
-  if (mx == -INFINITY) return;  // nothing visible yet
-  const float2 c12 = make_float2(c1, c1), nmx = make_float2(-mx, -mx);
+  return mr;
+}
+
+// P~ = exp2(S c1 - m) of 64 columns as bf16 pairs (32 registers), added to
+// the row sum l (fp32, before rounding).  Invisible columns get 0.
+template <bool MASKED>
+__device__ __forceinline__ void prep_p64(const uint32_t (&s)[4][16], int jbase, int jmax,
+                                         float c1, float m, float& l, uint32_t (&pk)[4][8]) {
+  const float2 c12 = make_float2(c1, c1), nm = make_float2(-m, -m);
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < 4; ++q)
 #pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-      const float2 t = ffma2(f2(s[q][j], s[q][j + 1]), c12, nmx);
-      float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-      if (MASKED) {
-        if (jbase + 16 * q + j > jmax) e.x = 0.f;
-        if (jbase + 16 * q + j + 1 > jmax) e.y = 0.f;
-      }
-      acc = fadd2(acc, e);
-    }
-  l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mx)) + (acc.x + acc.y);
-  m = mx;
-}
-
-// Phase B on 64 columns: P = exp2(S c1 - L2) as bf16 pairs (32 registers).
-template <bool MASKED>
-__device__ __forceinline__ void prep_p(const uint32_t (&s)[4][16], int jbase, int jmax, float c1,
-                                       float L2, uint32_t (&pk)[4][8]) {
-  const float2 c12 = make_float2(c1, c1), nL = make_float2(-L2, -L2);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
     for (int e = 0; e < 16; e += 2) {
-      const float2 t = ffma2(f2(s[q][e], s[q][e + 1]), c12, nL);
+      const float2 t = ffma2(f2(s[q][e], s[q][e + 1]), c12, nm);
       float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
       if (MASKED) {
         if (jbase + 16 * q + e > jmax) p.x = 0.f;
         if (jbase + 16 * q + e + 1 > jmax) p.y = 0.f;
       }
+      acc = fadd2(acc, p);
       pk[q][e >> 1] = pack_bf16x2(p.x, p.y);
     }
+  l += acc.x + acc.y;
 }
 
 template <int DH>
@@ -125,6 +111,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   constexpr int NH = PrepCfg<DH>::kHalves;
   constexpr int BN = PrepCfg<DH>::kBN;
   constexpr uint32_t HT = PrepCfg<DH>::kHalfTile;
+  constexpr uint32_t kScore = 2 * DH;  // first score buffer column
   Smem0<DH>& sm = *reinterpret_cast<Smem0<DH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,7 +120,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
   const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
   const int T = (col_end + BN - 1) / BN;
-  const int T2 = 2 * T;  // phase A tiles 0..T-1, phase B tiles T..2T-1
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -146,6 +132,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b], 4);  // one arrive per elementwise warp
     }
+    mbar_init(&sm.pv_done[0], 1);
+    mbar_init(&sm.pv_done[1], 1);
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
@@ -163,15 +151,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_expect_tx(&sm.bar_q, NH * HALF_BLOCK);
       for (int h = 0; h < NH; ++h) tma_load_3d(sm.q[h], &mQ, &sm.bar_q, 64 * h, row0, bh);
       int issued = 0;
-      for (int t = 0; t < T2; ++t) {
+      for (int t = 0; t < T; ++t) {
         const int s = t % NST;
-        const bool phase_b = t >= T;
-        const int kt = phase_b ? t - T : t;
         if (t >= NST && !mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
-        mbar_expect_tx(&sm.kv_full[s], (phase_b ? 2 : 1) * NH * HT);
+        mbar_expect_tx(&sm.kv_full[s], 2 * NH * HT);
         for (int h = 0; h < NH; ++h) {
-          tma_load_3d(sm.kv[s][0][h], &mK, &sm.kv_full[s], 64 * h, kt * BN, bkv);
-          if (phase_b) tma_load_3d(sm.kv[s][1][h], &mV, &sm.kv_full[s], 64 * h, kt * BN, bkv);
+          tma_load_3d(sm.kv[s][0][h], &mK, &sm.kv_full[s], 64 * h, t * BN, bkv);
+          tma_load_3d(sm.kv[s][1][h], &mV, &sm.kv_full[s], 64 * h, t * BN, bkv);
         }
         issued = t + 1;
       }
@@ -185,7 +171,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t idO = idesc_bf16(BM, DH, true);
       auto issue_scores = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + DH + BN * (t % NBUF);
+        const uint32_t sc = tbase + kScore + BN * (t % NBUF);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int h = kk >> 2;  // 64-column half of the head dim
@@ -195,40 +181,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  kk > 0);
         }
         mma_commit(&sm.sc_full[t % NBUF]);
-        if (t < T) mma_commit(&sm.kv_empty[s]);  // phase A reads the stage only here
       };
       auto issue_pv = [&](int t) {
         const int s = t % NST;
-        const uint32_t sc = tbase + DH + BN * (t % NBUF);
+        const uint32_t sc = tbase + kScore + BN * (t % NBUF);
         // V as an N = DH MN-major operand: its second 64-column half (d = 128)
-        // sits HT bytes after the first.
+        // sits HT bytes after the first.  Warpgroup t mod 2's accumulator;
+        // its first tile (t < 2) starts it.
         const uint32_t bv = smem_u32(sm.kv[s][1][0]);
+        const uint32_t acc_col = tbase + DH * (t & 1);
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c)
-          mma_ts(tbase, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HT, 1024), idO,
-                 (t > T || c > 0));
+          mma_ts(acc_col, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HT, 1024), idO,
+                 (t >= 2 || c > 0));
+        mma_commit(&sm.pv_done[t & 1]);
         mma_commit(&sm.kv_empty[s]);
       };
       if (elect_one()) {
         bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
         tc_fence_after();
-        for (int t = 0; ok && t < NBUF && t < T2; ++t) {
+        for (int t = 0; ok && t < NBUF && t < T; ++t) {
           ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
           tc_fence_after();
           if (ok) issue_scores(t);
         }
-        for (int t = 0; ok && t < T2; ++t) {
-          // Tile t's warpgroup is done with buffer t mod NBUF (phase B: P is in it).
+        for (int t = 0; ok && t < T; ++t) {
+          // Tile t's warpgroup has written P~ into buffer t mod NBUF.
           ok = mbar_wait(&sm.op_ready[t % NBUF], (t / NBUF) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          if (t >= T) issue_pv(t);
-          if (t + NBUF < T2) {
+          issue_pv(t);
+          if (t + NBUF < T) {
             const int tn = t + NBUF;
             ok = mbar_wait(&sm.kv_full[tn % NST], (tn / NST) & 1, abort_flag, err);
             if (!ok) break;
             tc_fence_after();
-            issue_scores(tn);
+            issue_scores(tn);  // after tile t's P V GEMMs have read the buffer
           }
         }
         mma_commit(&sm.out_full);
@@ -240,79 +228,118 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t acc_own = tbase + lane_off + DH * wg;  // this warpgroup's O~
     const int gr = row0 + r;
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;  // visible keys j <= jmax
-    float m = -INFINITY, l = 0.f, L2 = 0.f;
-    bool ok = true, have_L = false;
-    // Both warpgroups have finished phase A: combine their (m, l) into L.
-    // Each warpgroup passes here exactly once (named barrier 1).
-    auto combine = [&]() {
-      sm.part_m[wg][r] = m;
-      sm.part_l[wg][r] = l;
-      named_bar_sync(1, 256);
-      const float m0 = sm.part_m[0][r], m1 = sm.part_m[1][r];
-      const float mm = fmaxf(m0, m1);  // finite: tile 0 always has a valid column
-      const float l0 = m0 == -INFINITY ? 0.f : sm.part_l[0][r] * ex2_approx(m0 - mm);
-      const float l1 = m1 == -INFINITY ? 0.f : sm.part_l[1][r] * ex2_approx(m1 - mm);
-      L2 = mm + __log2f(l0 + l1);
-      have_L = true;
-    };
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
 
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
-      if (t >= T2) break;
-      const bool phase_b = t >= T;
-      if (phase_b && !have_L) combine();
+      if (t >= T) break;
       ok = ok && mbar_wait_warp(&sm.sc_full[t % NBUF], (t / NBUF) & 1, abort_flag, err);
-      if (!ok) continue;
+      if (!ok) break;
       tc_fence_after();
-      const uint32_t sc = tbase + lane_off + DH + BN * (t % NBUF);
-      const int col0 = (phase_b ? t - T : t) * BN;
+      const uint32_t sc = tbase + lane_off + kScore + BN * (t % NBUF);
+      const int col0 = t * BN;
       // Only tiles that reach past Nk or past the block's first row need the mask.
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
+      // The tile's visible maximum.  At d = 64 (two 64-column groups) the
+      // second group is read twice, so that only one group is held in
+      // registers at a time: P~ of columns 16c..16c+15 goes to columns
+      // 8c..8c+7, i.e. group 1's P~ lands on group 0's scores.
+      float mr = -INFINITY;
+      uint32_t s[4][16];
+      if (BN == 128) {
 #pragma unroll
-      for (int g = 0; g < BN / 64; ++g) {  // 64 columns at a time
-        uint32_t s[4][16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld16(sc + 64 * g + 16 * q, s[q]);
+        for (int q = 0; q < 4; ++q) tmem_ld16(sc + 64 + 16 * q, s[q]);
         tmem_wait_ld();
-        const int jb = col0 + 64 * g;
-        if (!phase_b) {
-          if (g == BN / 64 - 1) {  // the whole buffer is in registers
-            tc_fence_before();
-            warp_arrive(&sm.op_ready[t % NBUF]);
-          }
-          if (masked) prep_rowsum<true>(s, jb, jmax, c1, m, l);
-          else prep_rowsum<false>(s, jb, jmax, c1, m, l);
-        } else {
-          uint32_t pk[4][8];
-          if (masked) prep_p<true>(s, jb, jmax, c1, L2, pk);
-          else prep_p<false>(s, jb, jmax, c1, L2, pk);
-          // P of columns 16c..16c+15 goes to columns 8c..8c+7, already read.
+        mr = masked ? prep_max64<true>(s, col0 + 64, jmax) : prep_max64<false>(s, col0 + 64, jmax);
+      }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tmem_st8(sc + 32 * g + 8 * q, pk[q]);
+      for (int q = 0; q < 4; ++q) tmem_ld16(sc + 16 * q, s[q]);
+      tmem_wait_ld();
+      mr = fmaxf(mr, masked ? prep_max64<true>(s, col0, jmax) : prep_max64<false>(s, col0, jmax));
+      // Raise m only when the tile's maximum exceeds it by more than
+      // kRescale; then the running sum and this warpgroup's O~ (all its
+      // earlier tiles) are scaled down by exp2(m_old - m_new) first.
+      const float mt = mr * c1;
+      const bool raise = mt > m + kRescale;
+      const float factor = raise ? (m == -INFINITY ? 0.f : ex2_approx(m - mt)) : 1.f;
+      if (raise) {
+        l *= factor;
+        m = mt;
+      }
+      if (__any_sync(0xffffffffu, raise && factor < 1.f) && u > 0) {
+        // Rescale this warp's rows of O~ once its previous tile's P V GEMMs
+        // are done; a lane whose m did not move multiplies by 1.
+        ok = mbar_wait_warp(&sm.pv_done[wg], (u - 1) & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DH / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(acc_own + 16 * c, v);
+          tmem_wait_ld();
+          uint32_t w0[8], w1[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            w0[k] = __float_as_uint(u2f(v[k]) * factor);
+            w1[k] = __float_as_uint(u2f(v[8 + k]) * factor);
+          }
+          tmem_st8(acc_own + 16 * c, w0);
+          tmem_st8(acc_own + 16 * c + 8, w1);
         }
       }
-      if (phase_b) {
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(&sm.op_ready[t % NBUF]);
+      // P~ of columns 16c..16c+15 goes to columns 8c..8c+7 (already read).
+#pragma unroll
+      for (int g = 0; g < BN / 64; ++g) {
+        if (g > 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld16(sc + 64 * g + 16 * q, s[q]);
+          tmem_wait_ld();
+        }
+        uint32_t pk[4][8];
+        if (masked) prep_p64<true>(s, col0 + 64 * g, jmax, c1, m, l, pk);
+        else prep_p64<false>(s, col0 + 64 * g, jmax, c1, m, l, pk);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_st8(sc + 32 * g + 8 * q, pk[q]);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(&sm.op_ready[t % NBUF]);
     }
-    if (!have_L) combine();  // a warpgroup with no phase-B tile (T = 1)
 
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
+    // Merge the two warpgroups' (m, l, O~): m* = max, s_w = exp2(m_w - m*),
+    // O = (s_0 O~_0 + s_1 O~_1) / (s_0 l_0 + s_1 l_1).  A warpgroup with no
+    // visible column so far (m = -inf) contributes nothing.
+    sm.part_m[wg][r] = m;
+    sm.part_l[wg][r] = l;
+    named_bar_sync(1, 256);
+    const float m0 = sm.part_m[0][r], m1 = sm.part_m[1][r];
+    const float mm = fmaxf(m0, m1);  // finite: key 0 is visible to every row
+    const float s0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+    const float s1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+    const float lsum = s0 * sm.part_l[0][r] + s1 * sm.part_l[1][r];
+    const float inv = 1.f / lsum;
+    const bool one = T < 2;  // warpgroup 1 had no tile: its accumulator was never written
     float dpart = 0.f;
 #pragma unroll
     for (int h = 0; h < DH / 32; ++h) {  // warpgroup wg writes columns [DH/2 wg, DH/2 (wg+1))
       const int col = (DH / 2) * wg + 16 * h;
-      uint32_t vo[16];
-      tmem_ld16(tbase + lane_off + col, vo);
+      uint32_t v0[16], v1[16];
+      tmem_ld16(tbase + lane_off + col, v0);
+      tmem_ld16(tbase + lane_off + DH + col, v1);
       tmem_wait_ld();
+      float o[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        o[k] = (s0 * u2f(v0[k]) + (one ? 0.f : s1 * u2f(v1[k]))) * inv;
       if (ok && gr < Nq) {
         const size_t off = rowvec * DH + col;
         float4* o4 = reinterpret_cast<float4*>(O + off);
@@ -326,20 +353,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int q = 0; q < 4; ++q) {
             const float lo = __uint_as_float(w[q] << 16);
             const float hi = __uint_as_float(w[q] & 0xFFFF0000u);
-            dpart = fmaf(lo, u2f(vo[8 * k + 2 * q]), dpart);
-            dpart = fmaf(hi, u2f(vo[8 * k + 2 * q + 1]), dpart);
+            dpart = fmaf(lo, o[8 * k + 2 * q], dpart);
+            dpart = fmaf(hi, o[8 * k + 2 * q + 1], dpart);
           }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          o4[k] = make_float4(u2f(vo[4 * k]), u2f(vo[4 * k + 1]), u2f(vo[4 * k + 2]),
-                              u2f(vo[4 * k + 3]));
+          o4[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
       }
     }
     sm.part_d[wg][r] = dpart;
     named_bar_sync(1, 256);
     if (ok && wg == 0 && gr < Nq) {
-      L[rowvec] = L2 * kLn2;
+      L[rowvec] = (mm + __log2f(lsum)) * kLn2;
       if (D) D[rowvec] = sm.part_d[0][r] + sm.part_d[1][r];
     }
   }
