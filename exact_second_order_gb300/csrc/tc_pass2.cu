@@ -34,7 +34,11 @@
 // the element-wise code needs no per-column scalars at all.
 // TMEM: [0,64) d~K, [64,128) d~V accumulators; [128,384) one score buffer
 // S^T | F'^T | dP^T | G^T (64 columns each); [384,480) the bf16 A operands
-// dS^T, d~S^T, W^T of the output GEMMs; [480,488) the all-ones A operand.
+// dS^T, d~S^T, W^T of the output GEMMs; [480,512) U_K as the bf16 A operand
+// of F'^T += U_K Q^T (copied from shared memory once: with A in TMEM this
+// N = 64 GEMM runs at the tensor rate instead of waiting on shared-memory
+// operand reads).  The all-ones A operand of the row-scalar K step lives in
+// shared memory (at N = 128 that GEMM is tensor-bound either way).
 // Because the operands have their own columns, the score buffer is released
 // as soon as the warpgroups have read
 // it into registers, in two halves: S^T | F'^T first (read before any
@@ -67,7 +71,9 @@ struct Smem2 {
   // -(alpha D + E)).  No swizzle, K-major: 8-row x 16-byte core matrices,
   // row r at (r / 8) * 256 + (r % 8) * 16, k 8-15 128 bytes further.
   alignas(1024) uint8_t ex[NST][2][EX_BYTES];
+  alignas(1024) uint8_t ones[BM * 16 * 2];  // all-ones A: 128 rows x 16 bf16, same layout
   uint64_t bar_kv;
+  uint64_t a_ready;  // U_K is in TMEM (4 warps)
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
   uint64_t sc_full;   // score GEMMs of a tile have completed
@@ -87,7 +93,7 @@ constexpr uint32_t kSc = 128;  // score buffer
 constexpr uint32_t kColS = 0, kColF = 64, kColdP = 128, kColG = 192;  // inside the score buffer
 constexpr uint32_t kOp = 384;  // operand area: operand x, K step kk at kOp + 32 x + 8 kk
 constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
-constexpr uint32_t kOnes = 480;  // all-ones A operand (k = 0, 1, 2) of the row-scalar K step
+constexpr uint32_t kUKA = 480;  // U_K as an A operand, K step kk at kUKA + 8 kk
 // Padded query rows (i >= N_q, zero-filled by TMA) get -L / tau = -kFar, so
 // their P = exp2(c1 (0 - kFar)) is exactly 0.
 constexpr float kFar = 1e30f;
@@ -223,6 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_kv, 1);
+    mbar_init(&sm.a_ready, 4);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.st_full[s], 2);  // the TMA transaction, and the row-scalar K step written
       mbar_init(&sm.st_empty[s], 1);
@@ -241,22 +248,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
-  if (warp >= 2 && warp < 6) {
-    // The all-ones A operand of the row-scalar K step: k = 0, 1, 2 are 1
-    // (column c holds k = 2c in its low half, 2c + 1 in its high half).
-    const uint32_t one = 0x3F80u;  // bf16 1.0
-    const uint32_t v[8] = {one | (one << 16), one, 0u, 0u, 0u, 0u, 0u, 0u};
-    tmem_st8(tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kOnes, v);
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
   if (warp == 0) {
     // Producer.  Lane 0 issues the TMA copies; the whole warp writes the
-    // row-scalar K step of every tile: lane l takes query rows l and l + 32.
+    // row-scalar K step of every tile: lane l takes query rows l and l + 32
+    // (and, first, the all-ones A operand: k = 0, 1, 2 are 1).
     const float inv_tau = 1.f / tau;
+    for (int r = lane; r < BM; r += 32) {
+      uint8_t* base = sm.ones + (r >> 3) * 256 + (r & 7) * 16;
+      const uint32_t one = 0x3F80u;  // bf16 1.0
+      *reinterpret_cast<uint4*>(base) = make_uint4(one | (one << 16), one, 0u, 0u);
+      *reinterpret_cast<uint4*>(base + 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
     auto load_rows = [&](int f, float4 (&v)[2]) {
       // (L, D, alpha, E) of rows lane, lane + 32 of streamed tile f; a row
       // past N_q (or a tile past the last) is marked by L = NaN.
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           *reinterpret_cast<uint4*>(base + 128) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();  // also covers the ones operand before tile 0
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.st_full[s]);
       issued = t + 1;
@@ -332,7 +334,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t idS128 = idesc_bf16(BM, 2 * BQ, false);  // N = 128, B K-major
     constexpr uint32_t idO = idesc_bf16(BM, DH, true);          // N = 64, B MN-major
     const uint64_t dK = smem_desc_sw128(smem_u32(sm.kb[0]), 16, 1024);
-    const uint64_t dUK = smem_desc_sw128(smem_u32(sm.kb[1]), 16, 1024);
     const uint64_t dV = smem_desc_sw128(smem_u32(sm.kb[2]), 16, 1024);
     const uint64_t dUV = smem_desc_sw128(smem_u32(sm.kb[3]), 16, 1024);
     const uint32_t st0 = smem_u32(sm.st[0][0]);
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dUQ0 = smem_desc_sw128(st0 + TILE_BYTES, 16, 1024);
     const uint64_t ddO0 = smem_desc_sw128(st0 + 2 * TILE_BYTES, 16, 1024);
     const uint64_t dEx0 = smem_desc_noswz(smem_u32(sm.ex[0][0]), 128, 256);
+    const uint64_t dOnes = smem_desc_noswz(smem_u32(sm.ones), 128, 256);
     constexpr uint64_t kExStage = (2 * EX_BYTES) >> 4, kExPG = EX_BYTES >> 4;
     const uint32_t sc = tbase + kSc;
     // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
@@ -350,10 +352,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t o = 2 * kk;  // 16 bf16 along d = 32 bytes >> 4
           mma_ss(sc + kColS, dK + o, dQ0 + so + o, idS128, kk > 0);  // [S^T | F'^T] = K [Q; U_Q]^T
-          mma_ss(sc + kColF, dUK + o, dQ0 + so + o, idS64, 1);       // F'^T += U_K Q^T
+          mma_ts(sc + kColF, tbase + kUKA + 8 * kk, dQ0 + so + o, idS64, 1);  // F'^T += U_K Q^T
         }
         // [S^T | F'^T] += 1 [-L / tau | -alpha / tau]^T (the row-scalar K step)
-        mma_ts(sc + kColS, tbase + kOnes, dEx0 + (t % NST) * kExStage, idS128, 1);
+        mma_ss(sc + kColS, dOnes, dEx0 + (t % NST) * kExStage, idS128, 1);
       }
     };
     auto issue_pg = [&](int t) {
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColG, dUV + o, ddO0 + so + o, idS64, kk > 0);  // G^T  = U_V dO^T
         }
         // [dP^T | G^T] += 1 [-D | -(alpha D + E)]^T
-        mma_ts(sc + kColdP, tbase + kOnes, dEx0 + (t % NST) * kExStage + kExPG, idS128, 1);
+        mma_ss(sc + kColdP, dOnes, dEx0 + (t % NST) * kExStage + kExPG, idS128, 1);
         mma_commit(&sm.sc_full);
       }
     };
@@ -389,7 +391,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // One elected lane runs the whole schedule: every wait and every MMA,
     // with no warp-wide broadcast between them.
     if (elect_one()) {
-      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err);
+      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err) &&
+                mbar_wait(&sm.a_ready, 0, abort_flag, err);
       for (int t = 0; ok && t < T; ++t) {
         // Tile t's data is normally in the ring long before the warpgroups
         // release S^T | F'^T of tile t - 1: check it first, so that the S/F
@@ -433,6 +436,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t sc = tbase + lane_off + kSc;
     const uint32_t opb = tbase + lane_off;
     bool ok = true;
+    if (wg == 0) {
+      // Warpgroup 0 copies its key row of U_K from the 128-byte-swizzled TMA
+      // block (16-byte chunk c of row r at chunk c ^ (r mod 8)) into TMEM:
+      // K step kk is chunks 2 kk and 2 kk + 1.
+      ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
+      if (ok) {
+        const uint8_t* row = sm.kb[1] + r * 128;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint4 a = *reinterpret_cast<const uint4*>(row + (((2 * kk) ^ (r & 7)) << 4));
+          const uint4 b = *reinterpret_cast<const uint4*>(row + (((2 * kk + 1) ^ (r & 7)) << 4));
+          const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          tmem_st8(tbase + lane_off + kUKA + 8 * kk, v);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      warp_arrive(&sm.a_ready);
+    }
     int tq = 0;  // tile of the current query head, (t mod Tq)
     for (int t = 0; t < T; ++t) {
       // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a

@@ -26,7 +26,10 @@
 // G^T - (alpha D + E) in the score buffer.
 // TMEM: [0,128) d~K, [128,256) d~V accumulators; [256,384) one score buffer
 // S^T | F'^T | dP^T | G^T (32 columns each); [384,432) the bf16 A operands
-// dS^T, d~S^T, W^T; [432,440) the all-ones A operand.  The score buffer is
+// dS^T, d~S^T, W^T; [432,440) the all-ones A operand; [440,504) U_K as the
+// bf16 A operand of F'^T += U_K Q^T (copied from shared memory once; with A
+// in TMEM this N = 32 GEMM runs at the tensor rate instead of waiting on
+// shared-memory operand reads).  The score buffer is
 // released in two halves, S^T | F'^T
 // first, so the S/F' GEMMs of the next tile run while the warpgroups still
 // read and process dP/G.  Grouped-query attention: the query tiles of all
@@ -58,6 +61,7 @@ struct SmemW2 {
   // swizzle, K-major, row r at (r / 8) * 256 + (r % 8) * 16, k 8-15 at +128.
   alignas(1024) uint8_t ex[NST][2][EX_BYTES];
   uint64_t bar_kv;
+  uint64_t a_ready;  // U_K is in TMEM (4 warps)
   uint64_t st_full[NST];
   uint64_t st_empty[NST];
   uint64_t sc_full;
@@ -77,6 +81,7 @@ constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;  // inside th
 constexpr uint32_t kOp = 384;  // operand x, K step kk at kOp + 16 x + 8 kk
 constexpr uint32_t kOpdS = 0, kOpdSt = 1, kOpW = 2;
 constexpr uint32_t kOnes = 432;  // all-ones A operand (k = 0, 1, 2) of the row-scalar K step
+constexpr uint32_t kUKA = 440;   // U_K as an A operand, K step kk at kUKA + 8 kk
 constexpr float kFar = 1e30f;    // -L / tau of a padded query row: its P is exactly 0
 // Cluster split: staged partial rows d~K | d~V (64 float4 each) fill the
 // 128 KiB of the resident block exactly; float4 c of row r sits at
@@ -174,6 +179,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_kv, 1);
+    mbar_init(&sm.a_ready, 4);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.st_full[s], 2);  // the TMA transaction, and the row-scalar K step written
       mbar_init(&sm.st_empty[s], 1);
@@ -276,11 +282,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BQ, false);  // N = 64, B K-major
     constexpr uint32_t idS32 = idesc_bf16(BM, BQ, false);      // N = 32, B K-major
     constexpr uint32_t idO = idesc_bf16(BM, DH, true);         // N = 128, B MN-major
-    uint64_t dK[2], dUK[2], dV[2], dUV[2], dQ[2], ddO[2];
+    uint64_t dK[2], dV[2], dUV[2], dQ[2], ddO[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       dK[h] = smem_desc_sw128(smem_u32(sm.kb[0][h]), 16, 1024);
-      dUK[h] = smem_desc_sw128(smem_u32(sm.kb[1][h]), 16, 1024);
       dV[h] = smem_desc_sw128(smem_u32(sm.kb[2][h]), 16, 1024);
       dUV[h] = smem_desc_sw128(smem_u32(sm.kb[3][h]), 16, 1024);
       dQ[h] = smem_desc_sw128(smem_u32(sm.st[0][h][0]), 16, 1024);  // Q (and Q; U_Q)
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int h = kk >> 2;
           const uint64_t o = 2 * (kk & 3);
           mma_ss(sc + kColS, dK[h] + o, dQ[h] + so + o, idS64, kk > 0);  // [S^T | F'^T] = K [Q; U_Q]^T
-          mma_ss(sc + kColF, dUK[h] + o, dQ[h] + so + o, idS32, 1);      // F'^T += U_K Q^T
+          mma_ts(sc + kColF, tbase + kUKA + 8 * kk, dQ[h] + so + o, idS32, 1);  // F'^T += U_K Q^T
         }
         // [S^T | F'^T] += 1 [-L / tau | -alpha / tau]^T (the row-scalar K step)
         mma_ts(sc + kColS, tbase + kOnes, dEx0 + (t % NST) * kExStage, idS64, 1);
@@ -343,7 +348,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // One elected lane runs the whole schedule: every wait and every MMA.
     if (elect_one()) {
-      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err);
+      bool ok = mbar_wait(&sm.bar_kv, 0, abort_flag, err) &&
+                mbar_wait(&sm.a_ready, 0, abort_flag, err);
       for (int t = 0; ok && t < T; ++t) {
         // Tile t's data is normally in the ring before the S/F release of
         // tile t - 1 arrives: check it first, so the S/F GEMMs follow it.
@@ -386,6 +392,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t sc = tbase + lane_off + kSc;
     const uint32_t opb = tbase + lane_off;
     bool ok = true;
+    if (wg == 0) {
+      // Warpgroup 0 copies its key row of U_K from the two 128-byte-swizzled
+      // 64-column halves (16-byte chunk c of row r at chunk c ^ (r mod 8))
+      // into TMEM: K step kk is chunks 2 (kk mod 4), 2 (kk mod 4) + 1 of
+      // half kk / 4.
+      ok = mbar_wait_warp(&sm.bar_kv, 0, abort_flag, err);
+      if (ok) {
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint8_t* row = sm.kb[1][kk >> 2] + r * 128;
+          const int c = 2 * (kk & 3);
+          const uint4 a = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+          const uint4 b = *reinterpret_cast<const uint4*>(row + (((c + 1) ^ (r & 7)) << 4));
+          const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          tmem_st8(tbase + lane_off + kUKA + 8 * kk, v);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      warp_arrive(&sm.a_ready);
+    }
     int tq = 0;  // tile of the current query head
     for (int t = 0; t < T; ++t) {
       ok = ok && mbar_wait_warp(&sm.sc_full, t & 1, abort_flag, err);
