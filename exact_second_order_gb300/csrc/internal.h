@@ -75,9 +75,11 @@ size_t tc_pass1_smem();
 size_t tc_pass2_smem();
 size_t tc_pass1_d128_smem();
 size_t tc_pass2_d128_smem();
-// Pass 2 cluster split: how many CTAs share a key block (S divides the
-// group size, S <= 8, blocks * S fits one wave of the device's SMs).
-cudaError_t tc_group_split(int blocks, int group, int* S);
+// Pass 2 cluster split: how many CTAs (S = 1 .. 8) share a key block of
+// `tiles` streamed query tiles when the `blocks` key blocks cannot fill the
+// device: the largest S whose clusters of the split kernel all fit at once.
+cudaError_t tc_pass2_split(const void* split_kernel, size_t smem, int blocks, int tiles,
+                           int* S);
 
 // Device error word (one per device): a kernel writes a nonzero code when a
 // bounded wait gives up.  Codes: 1 = mbarrier wait timed out.

@@ -1,5 +1,7 @@
 // Host side of the tensor-core path: which calls it serves, the TMA tensor
 // maps of the seven bf16 inputs, and the two launches on the caller's stream.
+#include <mutex>
+
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -20,14 +22,76 @@ cudaError_t tc_launch_jvp_d128(const JvpArgs& a, const CUtensorMap* maps128,
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
-cudaError_t tc_group_split(int blocks, int group, int* S) {
-  int dev = 0, sms = 0;
+namespace {
+
+// How many clusters of S CTAs of `kernel` (1 CTA per SM at this shared-memory
+// size) the current device holds at once, for S = 1 .. 8; asked once per
+// (kernel, device) and kept.
+struct ClusterFit {
+  const void* kernel = nullptr;
+  int device = -1;
+  int fit[9] = {};
+};
+
+cudaError_t cluster_fit(const void* kernel, size_t smem, int S, int* out) {
+  static std::mutex mu;
+  static ClusterFit table[16];
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  ClusterFit* slot = nullptr;
+  for (ClusterFit& c : table) {
+    if (c.kernel == kernel && c.device == dev) { *out = c.fit[S]; return cudaSuccess; }
+    if (slot == nullptr && c.kernel == nullptr) slot = &c;
+  }
+  ClusterFit c;
+  c.kernel = kernel;
+  c.device = dev;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  c.fit[1] = sms;
+  for (int s = 2; s <= 8; ++s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, s, 1);
+    cfg.blockDim = dim3(320);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = s;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    c.fit[s] = n;
+  }
+  if (slot != nullptr) *slot = c;
+  *out = c.fit[S];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t tc_pass2_split(const void* split_kernel, size_t smem, int blocks, int tiles,
+                           int* S) {
+  // Split only grids that leave SMs idle: the largest S whose clusters still
+  // all fit at once.  Splitting a grid of a wave or more to even out its
+  // last wave was measured slower (the long-context pass 2 12.76 -> 13.43 ms
+  // at S = 2): cluster launches then wait for pairs of free SMs.
   *S = 1;
-  for (int s = 2; s <= 8; ++s)
-    if (group % s == 0 && blocks * s <= sms) *S = s;
+  int sms = 0;
+  cudaError_t e = cluster_fit(split_kernel, smem, 1, &sms);
+  if (e != cudaSuccess || blocks >= sms) return e;
+  for (int s = 2; s <= 8 && s <= tiles; ++s) {
+    int fit = 0;
+    e = cluster_fit(split_kernel, smem, s, &fit);
+    if (e != cudaSuccess) return e;
+    if (blocks <= fit) *S = s;
+  }
   return cudaSuccess;
 }
 

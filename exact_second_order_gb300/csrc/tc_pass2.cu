@@ -140,12 +140,11 @@ __device__ __forceinline__ void p2_chunk(const uint32_t (&s)[16], const uint32_t
 }
 
 // The 32 query rows of one warpgroup: read S^T and F'^T of both 16-row
-// chunks and release them; read dP^T, G^T of the first chunk and form its
-// dS, d~S, W; read dP^T, G^T of the second chunk and release the score
-// buffer; only then wait until the previous tile's output GEMMs are done
-// with the operand area, write the first chunk's operands, form and write
-// the second's.  The release does not wait for the output GEMMs, and only
-// one chunk's operands are live at a time.
+// chunks and release them, read dP^T and G^T of both chunks and release the
+// score buffer, so that the next tile's score GEMMs are queued on the tensor
+// pipe before any arithmetic of this one; only then form dS, d~S, W chunk by
+// chunk, writing them once the previous tile's output GEMMs are done with
+// the operand area.
 template <bool MASKED>
 __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, int ibase, int gj,
                                         float c1, float tau, Smem2& sm, int t,
@@ -160,28 +159,26 @@ __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, int i
   tmem_wait_ld();
   tc_fence_before();
   warp_arrive(&sm.sf_free);  // this warp is done with S^T | F'^T
-  uint32_t a_ds[8], a_dst[8], a_w[8];
-  {
-    uint32_t dp[16], g[16];
-    tmem_ld16(sc + kColdP + col, dp);
-    tmem_ld16(sc + kColG + col, g);
-    tmem_wait_ld();
-    p2_chunk<MASKED>(s0, dp, f0, g, ibase, gj, c1, tau, a_ds, a_dst, a_w);
-  }
-  uint32_t dp[16], g[16];
-  tmem_ld16(sc + kColdP + col + 16, dp);
-  tmem_ld16(sc + kColG + col + 16, g);
+  uint32_t dp0[16], g0[16], dp1[16], g1[16];
+  tmem_ld16(sc + kColdP + col, dp0);
+  tmem_ld16(sc + kColG + col, g0);
+  tmem_ld16(sc + kColdP + col + 16, dp1);
+  tmem_ld16(sc + kColG + col + 16, g1);
   tmem_wait_ld();
   tc_fence_before();
   warp_arrive(&sm.pg_free);  // this warp is done with dP^T | G^T
-  if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
-  tc_fence_after();
-  tmem_st8(opb + op_col(kOpdS, kk), a_ds);
-  tmem_st8(opb + op_col(kOpdSt, kk), a_dst);
-  tmem_st8(opb + op_col(kOpW, kk), a_w);
+  {
+    uint32_t a_ds[8], a_dst[8], a_w[8];
+    p2_chunk<MASKED>(s0, dp0, f0, g0, ibase, gj, c1, tau, a_ds, a_dst, a_w);
+    if (t > 0 && !mbar_wait_warp(&sm.op_free, (t - 1) & 1, abort_flag, err)) return false;
+    tc_fence_after();
+    tmem_st8(opb + op_col(kOpdS, kk), a_ds);
+    tmem_st8(opb + op_col(kOpdSt, kk), a_dst);
+    tmem_st8(opb + op_col(kOpW, kk), a_w);
+  }
   {
     uint32_t o_ds[8], o_dst[8], o_w[8];
-    p2_chunk<MASKED>(s1, dp, f1, g, ibase + 16, gj, c1, tau, o_ds, o_dst, o_w);
+    p2_chunk<MASKED>(s1, dp1, f1, g1, ibase + 16, gj, c1, tau, o_ds, o_dst, o_w);
     tmem_st8(opb + op_col(kOpdS, kk + 1), o_ds);
     tmem_st8(opb + op_col(kOpdSt, kk + 1), o_dst);
     tmem_st8(opb + op_col(kOpW, kk + 1), o_w);
@@ -209,22 +206,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // One CTA per key block of a key/value head.  Grouped-query attention: the
   // G = H / Hkv query heads sharing the head stream past one after the other
-  // and their contributions are summed on chip ([FBN] 关键设计 3).  When the
-  // key blocks alone cannot fill the GPU, a cluster of S CTAs (blockIdx.y =
-  // S * head + rank) shares a key block, each streams G / S of the heads, and
-  // the partial sums meet in distributed shared memory before the one write.
-  const int G = H / Hkv, Gs = G / S;
+  // and their contributions are summed on chip ([FBN] 关键设计 3).  A cluster
+  // of S CTAs (blockIdx.y = S * head + rank) shares a key block when the
+  // key blocks alone cannot fill the GPU: rank q streams the q-th of S equal
+  // runs of the group's query tiles, and the partial sums meet in
+  // distributed shared memory before the one write.
+  const int G = H / Hkv;
   const int bkv = blockIdx.z * Hkv + blockIdx.y / S;
-  const int hq0 = blockIdx.z * H + (blockIdx.y / S) * G + (blockIdx.y % S) * Gs;  // first head
+  const int rank = blockIdx.y % S;
+  const int hqb = blockIdx.z * H + (blockIdx.y / S) * G;  // first query head of the group
   const int j0 = blockIdx.x * BM;
   // Query tiles t0 .. of 64 rows stream past; under the causal mask key j is
   // seen only by queries i >= j, so the tiles before the block are skipped
-  // (all of them when j0 >= Nq: then T = 0 and the block's d~K, d~V are 0).
-  // f = (query head in group) * Tq + (tile - t0) numbers the streamed tiles;
-  // ring slots and barrier phases count f.
+  // (all of them when j0 >= Nq: then Tq = 0 and the block's d~K, d~V are 0).
+  // Group tile f = (query head in group) * Tq + (tile - t0); this CTA takes
+  // f = f0 .. f0 + T - 1, its own t = f - f0 counting ring slots and barrier
+  // phases.
   const int t0 = causal ? j0 / BQ : 0;
   const int Tq = max(0, (Nq + BQ - 1) / BQ - t0);
-  const int T = Gs * Tq;
+  const int Tall = G * Tq;
+  const int f0 = static_cast<int>(static_cast<long long>(Tall) * rank / S);
+  const int T = static_cast<int>(static_cast<long long>(Tall) * (rank + 1) / S) - f0;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // past N_q (or a tile past the last) is marked by L = NaN.
       v[0] = v[1] = make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
       if (f >= T) return;
-      const int zq = hq0 + f / Tq, row0 = (f % Tq + t0) * BQ;
+      const int zq = hqb + (f0 + f) / Tq, row0 = ((f0 + f) % Tq + t0) * BQ;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = row0 + lane + 32 * h;
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (t >= NST && !mbar_wait_warp(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err))
         break;
       if (lane == 0) {
-        const int row = (t % Tq + t0) * BQ, zq = hq0 + t / Tq;
+        const int row = ((f0 + t) % Tq + t0) * BQ, zq = hqb + (f0 + t) / Tq;
         mbar_expect_tx(&sm.st_full[s], 3 * TILE_BYTES);
         tma_load_3d(sm.st[s][0], &mQ, &sm.st_full[s], 0, row, zq);
         tma_load_3d(sm.st[s][1], &mUQ, &sm.st_full[s], 0, row, zq);
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       warp_arrive(&sm.a_ready);
     }
-    int tq = 0;  // tile of the current query head, (t mod Tq)
+    int tq = Tq > 0 ? f0 % Tq : 0;  // tile of the current query head, (f0 + t) mod Tq
     for (int t = 0; t < T; ++t) {
       // Warp-uniform decisions (tcgen05.ld/st are warp-collective); after a
       // failed wait the remaining tiles are skipped.
@@ -479,7 +481,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t acc_base = tbase + lane_off;
     if (SPLIT) {
       // Stage this CTA's partial d~K | d~V rows (every MMA is done and the
-      // ring is idle) for the cluster-wide sum below.
+      // ring is idle) for the cluster-wide sum below; a CTA with no tile
+      // (T = 0) never wrote its accumulators and stages zeros.
       float* row = reinterpret_cast<float*>(&sm.st[0][0][0]) + r * kStageStride;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -488,6 +491,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld16(acc_base + kAccK + col, vk);
         tmem_ld16(acc_base + kAccV + col, vv);
         tmem_wait_ld();
+        if (T == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           reinterpret_cast<float4*>(row + col)[k] =
@@ -551,7 +558,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const int gjr = j0 + rr;
         if (gjr < Nk && !*abort_flag) {
-          if (T == 0) acc = make_float4(0.f, 0.f, 0.f, 0.f);
           const bool isK = c4 < DH / 4;
           const size_t o = (static_cast<size_t>(bkv) * Nk + gjr) * DH + 4 * (isK ? c4 : c4 - DH / 4);
           if (isK)
@@ -585,11 +591,16 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // One CTA per key block of a shared head; when those cannot fill the SMs,
-  // split each group's query heads over a cluster of S CTAs (S divides
-  // H / Hkv, at most 8, the largest that still fits one wave).
+  // One CTA per key block of a shared head, or, when the key blocks cannot
+  // fill the SMs, a cluster of S of them that splits the block's query tiles
+  // S ways.
+  e = cudaFuncSetAttribute(tc_pass2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.H / a.Hkv) * ((a.Nq + BQ - 1) / BQ);
   int S = 1;
-  e = tc_group_split(((a.Nk + BM - 1) / BM) * a.Hkv * a.B, a.H / a.Hkv, &S);
+  e = tc_pass2_split(reinterpret_cast<const void*>(tc_pass2_kernel<true>), smem,
+                     ((a.Nk + BM - 1) / BM) * a.Hkv * a.B, tiles, &S);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {
@@ -599,9 +610,6 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
         a.err);
     return cudaGetLastError();
   }
-  e = cudaFuncSetAttribute(tc_pass2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHREADS);

@@ -163,18 +163,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                           ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A cluster of S CTAs (blockIdx.y = S * head + rank) may share a key
-  // block, each streaming G / S of the group's heads; the partial sums meet
-  // in distributed shared memory before the one write (see the end).
-  const int G = H / Hkv, Gs = G / S;
+  // block, rank q streaming the q-th of S equal runs of the group's query
+  // tiles; the partial sums meet in distributed shared memory before the one
+  // write (see the end).
+  const int G = H / Hkv;
   const int bkv = blockIdx.z * Hkv + blockIdx.y / S;
-  const int hq0 = blockIdx.z * H + (blockIdx.y / S) * G + (blockIdx.y % S) * Gs;  // first head
+  const int rank = blockIdx.y % S;
+  const int hqb = blockIdx.z * H + (blockIdx.y / S) * G;  // first query head of the group
   const int j0 = blockIdx.x * BM;
   // Query tiles t0 .. stream past (causal: key j is seen only by queries
-  // i >= j; none when j0 >= Nq, and then T = 0 and the outputs are 0).
-  // f = (query head in group) * Tq + (tile - t0) numbers the streamed tiles.
+  // i >= j; none when j0 >= Nq, and then Tq = 0 and the outputs are 0).
+  // Group tile f = (query head in group) * Tq + (tile - t0); this CTA takes
+  // f = f0 .. f0 + T - 1 (its own t = f - f0).
   const int t0 = causal ? j0 / BQ : 0;
   const int Tq = max(0, (Nq + BQ - 1) / BQ - t0);
-  const int T = Gs * Tq;
+  const int Tall = G * Tq;
+  const int f0 = static_cast<int>(static_cast<long long>(Tall) * rank / S);
+  const int T = static_cast<int>(static_cast<long long>(Tall) * (rank + 1) / S) - f0;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -218,9 +223,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // (or a tile past the last) is marked by L = NaN.
       float4 v = make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
       if (f >= T) return v;
-      const int i = (f % Tq + t0) * BQ + lane;
+      const int i = ((f0 + f) % Tq + t0) * BQ + lane;
       if (i < Nq) {
-        const size_t o = static_cast<size_t>(hq0 + f / Tq) * Nq + i;
+        const size_t o = static_cast<size_t>(hqb + (f0 + f) / Tq) * Nq + i;
         v = make_float4(L[o], D[o], alpha[o], E[o]);
       }
       return v;
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (t >= NST && !mbar_wait_warp(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err))
         break;
       if (lane == 0) {
-        const int row = (t % Tq + t0) * BQ, fz = hq0 + t / Tq;
+        const int row = ((f0 + t) % Tq + t0) * BQ, fz = hqb + (f0 + t) / Tq;
         mbar_expect_tx(&sm.st_full[s], STAGE_BYTES);
         for (int h = 0; h < 2; ++h) {
           tma_load_3d(sm.st[s][h][0], &mQ, &sm.st_full[s], 64 * h, row, fz);
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       warp_arrive(&sm.a_ready);
     }
-    int tq = 0;  // tile of the current query head
+    int tq = Tq > 0 ? f0 % Tq : 0;  // tile of the current query head, (f0 + t) mod Tq
     for (int t = 0; t < T; ++t) {
       ok = ok && mbar_wait_warp(&sm.sc_full, t & 1, abort_flag, err);
       if (ok) {
@@ -433,7 +438,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t acc_base = tbase + lane_off;
     if (SPLIT) {
       // Stage this CTA's partial rows (every MMA is done; the resident
-      // block is no longer read) for the cluster-wide sum below.
+      // block is no longer read) for the cluster-wide sum below; a CTA with
+      // no tile (T = 0) never wrote its accumulators and stages zeros.
       float4* row = reinterpret_cast<float4*>(&sm.kb[0][0][0]) + r * (2 * DH / 4);
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
@@ -442,6 +448,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld16(acc_base + kAccK + col, vk);
         tmem_ld16(acc_base + kAccV + col, vv);
         tmem_wait_ld();
+        if (T == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int ck = col / 4 + k, cv = DH / 4 + col / 4 + k;
@@ -505,7 +515,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const int gjr = j0 + rr;
         if (gjr < Nk && !*abort_flag) {
-          if (T == 0) acc = make_float4(0.f, 0.f, 0.f, 0.f);
           const bool isK = c4 < DH / 4;
           const size_t o =
               (static_cast<size_t>(bkv) * Nk + gjr) * DH + 4 * (isK ? c4 : c4 - DH / 4);
@@ -541,10 +550,16 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
   cudaError_t e = cudaFuncSetAttribute(tc_pass2_d128_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // One CTA per key block of a shared head, or a cluster of S of them (the
-  // group's query heads split S ways) when the blocks cannot fill the SMs.
+  // One CTA per key block of a shared head, or, when the key blocks cannot
+  // fill the SMs, a cluster of S of them that splits the block's query tiles
+  // S ways.
+  e = cudaFuncSetAttribute(tc_pass2_d128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.H / a.Hkv) * ((a.Nq + BQ - 1) / BQ);
   int S = 1;
-  e = tc_group_split(((a.Nk + BM - 1) / BM) * a.Hkv * a.B, a.H / a.Hkv, &S);
+  e = tc_pass2_split(reinterpret_cast<const void*>(tc_pass2_d128_kernel<true>), smem,
+                     ((a.Nk + BM - 1) / BM) * a.Hkv * a.B, tiles, &S);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {
@@ -554,9 +569,6 @@ cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
         a.err);
     return cudaGetLastError();
   }
-  e = cudaFuncSetAttribute(tc_pass2_d128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHREADS);
