@@ -487,6 +487,91 @@ def oracle_full_timing(w, x):
                     else "every head run", "cores": os.cpu_count(), "cpu_model": cpu_model()}
 
 
+def run_e2e(args, w, x, res, fb, torch, barrier, world):
+    """The benchmark step through the public C ABI (flashbob_bob) with the
+    data on the host: each step uploads its inputs and row state from pinned
+    host memory and downloads all six outputs.  Buffer set k % 2 serves step
+    k; uploads and downloads run on a copy stream, ordered against the
+    kernels by events, so they overlap the neighbouring steps' kernels."""
+    comp = res.stream
+    copy = torch.cuda.Stream()
+    host_in = {k: v.pin_memory() for k, v in x.items()}
+    host_state = {"O": res.O.cpu().pin_memory(), "L": res.L.cpu().pin_memory(),
+                  "D": res.D.cpu().pin_memory()}
+    host_out = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in res.out.items()}
+                for _ in range(2)]
+    sets = []
+    for b in range(2):
+        dev = res.dev if b == 0 else {k: torch.empty_like(v) for k, v in res.dev.items()}
+        state = ({"O": res.O, "L": res.L, "D": res.D} if b == 0 else
+                 {"O": torch.empty_like(res.O), "L": torch.empty_like(res.L),
+                  "D": torch.empty_like(res.D)})
+        out = res.out if b == 0 else {k: torch.empty_like(v) for k, v in res.out.items()}
+        sets.append((dev, state, out))
+    h2d = sum(t_.numel() * t_.element_size() for t_ in list(host_in.values())
+              + list(host_state.values()))
+    d2h = sum(t_.numel() * t_.element_size() for t_ in host_out[0].values())
+    uploaded = [torch.cuda.Event() for _ in range(2)]    # set b's inputs are on the device
+    computed = [torch.cuda.Event() for _ in range(2)]    # set b's outputs are written
+    downloaded = [torch.cuda.Event() for _ in range(2)]  # set b's outputs are on the host
+    for b in range(2):
+        downloaded[b].record(copy)
+
+    def upload(b):
+        dev, state, _ = sets[b]
+        with torch.cuda.stream(copy):
+            copy.wait_event(computed[b])  # the kernels that read this set last are done
+            for k in host_in:
+                dev[k].copy_(host_in[k], non_blocking=True)
+            for k in host_state:
+                state[k].copy_(host_state[k], non_blocking=True)
+            uploaded[b].record(copy)
+
+    def compute(b):
+        dev, state, out = sets[b]
+        comp.wait_event(uploaded[b])
+        comp.wait_event(downloaded[b])  # the previous use of these outputs is on the host
+        fb.flashbob_bob(dev["Q"], dev["K"], dev["V"], state["O"], dev["dO"], state["L"],
+                        state["D"], dev["UQ"], dev["UK"], dev["UV"], w.tau, out["dQt"],
+                        out["dKt"], out["dVt"], out["ddOt"], out["alpha"], out["E"],
+                        causal=w.causal, stream=comp)
+        computed[b].record(comp)
+
+    def download(b):
+        _, _, out = sets[b]
+        with torch.cuda.stream(copy):
+            copy.wait_event(computed[b])
+            for k in host_out[b]:
+                host_out[b][k].copy_(out[k], non_blocking=True)
+            downloaded[b].record(copy)
+
+    def run(n):
+        upload(0)
+        for k in range(n):
+            b = k & 1
+            compute(b)
+            if k + 1 < n:
+                upload(1 - b)
+            download(b)
+
+    run(2)
+    barrier()
+    n_e2e = max(3, args.steps // 2)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(comp)
+    copy.wait_event(t0)
+    run(n_e2e)
+    comp.wait_stream(copy)
+    t1.record(comp)
+    barrier()
+    e_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
+    return {"value": job_tflops(w.flops, n_e2e, world, e_ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": e_ms / n_e2e, "steps": n_e2e,
+            "overlap": "uploads and downloads on a copy stream, two buffer sets"}
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -517,56 +602,26 @@ def main():
     uuid = gpu_uuid(torch, local)
     t = timed_steps(res, args.steps, args.warmup, torch, barrier, uuid)
     prep_ms = res.prep_ms(torch)
+    in_bytes = res.input_bytes()
     total_ms = reduce_max(t["total_ms"], world, "cuda")
     ms_per_step = total_ms / args.steps
     flops = w.flops
     value = job_tflops(flops, args.steps, world, total_ms)
-    dev, out, O, L, D, stream = res.dev, res.out, res.O, res.L, res.D, res.stream
 
-    # end to end: pinned host inputs -> device, the C-ABI call, outputs -> host
+    # end to end: pinned host inputs -> device, the C-ABI call, outputs -> host,
+    # every step.  Two device copies of the inputs, row state and outputs
+    # alternate between steps, and the copies run on a second stream, so a
+    # step's uploads and the previous step's downloads overlap the kernels
+    # (events order every buffer's reuse).
     e2e = None
     if not args.no_e2e:
-        host_in = {k: v.pin_memory() for k, v in x.items()}
-        host_state = {"O": O.cpu().pin_memory(), "L": L.cpu().pin_memory(),
-                      "D": D.cpu().pin_memory()}
-        host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in out.items()}
-        dev_state = {"O": O, "L": L, "D": D}
-        h2d = sum(t_.numel() * t_.element_size() for t_ in list(host_in.values())
-                  + list(host_state.values()))
-        d2h = sum(t_.numel() * t_.element_size() for t_ in host_out.values())
-        n_e2e = max(3, args.steps // 2)
-
-        def e2e_step():
-            for k in host_in:
-                dev[k].copy_(host_in[k], non_blocking=True)
-            for k in host_state:
-                dev_state[k].copy_(host_state[k], non_blocking=True)
-            fb.flashbob_bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"],
-                            dev["UK"], dev["UV"], w.tau, out["dQt"], out["dKt"], out["dVt"],
-                            out["ddOt"], out["alpha"], out["E"], causal=w.causal,
-                            stream=stream)
-            for k in host_out:
-                host_out[k].copy_(out[k], non_blocking=True)
-
-        e2e_step()
-        barrier()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        t1.record(stream)
-        barrier()
-        e_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
-        e2e = {"value": job_tflops(flops, n_e2e, world, e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / n_e2e, "steps": n_e2e}
-
+        e2e = run_e2e(args, w, x, res, fb, torch, barrier, world)
+        del res
+        torch.cuda.empty_cache()
     peak, sustained, peak_note = tensor_peak()
     rl = roofline(w, t, peak, peak_note)
     rl["traffic"] = read_traffic().get(rl["kernel"])
     rl["frac_of_sustained"] = rl["achieved"] / sustained
-    in_bytes = res.input_bytes()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -588,7 +643,7 @@ def main():
     if rank == 0:
         print(json.dumps(line), flush=True)
     if args.sweep and world == 1:
-        del res, dev, out, O, L, D
+        res = None
         torch.cuda.empty_cache()
         run_sweep(args, fb, torch, barrier, uuid, peak, peak_note)
     if world > 1:
