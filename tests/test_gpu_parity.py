@@ -319,3 +319,41 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK  # the report clears the word
     # the context is still usable
     _check_full(wl.small_workload(1, 2, 150, 64, "bf16", seed=31))
+
+
+# --------------------------------------------------------------------------
+# Prep: the running row maximum is raised mid-sequence
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prep_when_later_keys_dominate(d, causal):
+    """Keys past position 640 are scaled up ×3 (scores of variance ~9 against
+    ~0.01 before), so most rows' softmax maximum jumps by far more than
+    2^8 after the first tiles and prep must rescale its running sums and
+    accumulators; O, L, D, and the BoB built on them, against the oracle."""
+    from exact_second_order_gb300.inputs import NAMES, as_float64_numpy
+    w = wl.small_workload(1, 2, 1500, d, "bf16", seed=40 + d, dist="unit", causal=causal)
+    x = wl.make_inputs(w)
+    scale = torch.full((w.N, 1), 0.1)
+    scale[640:] = 3.0
+    x["K"] = (x["K"].float() * scale).to(torch.bfloat16)
+    dev = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(dev["Q"], dev["K"], dev["V"], dev["dO"], w.tau, causal=causal)
+    out = fb.bob(dev["Q"], dev["K"], dev["V"], O, dev["dO"], L, D, dev["UQ"], dev["UK"],
+                 dev["UV"], w.tau, causal=causal)
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    from tests.helpers import rel_fro, to_np
+    from oracle import bob as orc
+    errs = {}
+    for h in range(w.H):
+        a = [as_float64_numpy(x[k][0, h]) for k in NAMES]
+        o, l, dd = orc.prep(*a[:4], w.tau, causal)
+        r = orc.bob(*a, w.tau, causal)
+        for k, got, ref in (("O", O, o), ("L", L, l), ("D", D, dd)):
+            errs[f"{k}{h}"] = rel_fro(to_np(got[0, h]), ref)
+        for k in ("dQt", "dKt", "dVt", "ddOt", "alpha", "E"):
+            errs[f"{k}{h}"] = rel_fro(to_np(out[k][0, h]), r[k])
+    record(f"prep rescale d{d} causal={causal}", errs)
+    assert max(errs.values()) <= TOL["bf16"], errs
