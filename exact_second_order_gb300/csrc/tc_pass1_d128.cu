@@ -37,7 +37,9 @@
 // Instantiated with JVP = true the kernel computes the attention JVP along
 // (U_Q, U_K, U_V) instead (no dO): one pass over the key tiles with S and F'
 // only, operands P and P o F, O'0 = P U_V + (P o F) V in the d~dO
-// accumulator, and O' = O'0 - L' O, L' = alpha in the epilogue.
+// accumulator, and O' = O'0 - L' O, L' = alpha in the epilogue.  Its d~Q
+// columns [0,128) are free, so Q and U_Q are copied there once as bf16 A
+// operands and its score GEMMs read only the key tile from shared memory.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -69,6 +71,7 @@ struct SmemW1 {
   uint64_t sc_full[2];
   uint64_t op_ready[2];
   uint64_t out_full;
+  uint64_t a_ready;  // the JVP: Q and U_Q are in TMEM (8 warps)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -76,6 +79,8 @@ static_assert(sizeof(SmemW1) + 1024 <= 232448, "shared memory");
 
 constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;
 constexpr uint32_t kAccQ = 0, kAccdO = 128;
+// The JVP (no d~Q accumulator): Q and U_Q as bf16 A operands, K step kk at +8 kk.
+constexpr uint32_t kJvpQA = 0, kJvpUQA = 64;
 // Phase-B operand slots inside a score buffer: chunk c (key columns
 // 16c..16c+15) writes only the S and F' columns of its own chunk, which it
 // has already read.
@@ -233,6 +238,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.op_ready[b], 4);
     }
     mbar_init(&sm.out_full, 1);
+    mbar_init(&sm.a_ready, 8);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -344,6 +350,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int h = kk >> 2;
           const uint64_t o = 2 * (kk & 3);  // 16 bf16 inside the 128-byte row
           const uint32_t acc = kk > 0;
+          if (JVP) {  // A from TMEM
+            mma_ts(sc + kColS, tbase + kJvpQA + 8 * kk, dK[h] + so + o, idS64, acc);
+            mma_ts(sc + kColF, tbase + kJvpUQA + 8 * kk, dK[h] + so + o, idS32, 1);
+            continue;
+          }
           mma_ss(sc + kColS, dq[h] + o, dK[h] + so + o, idS64, acc);    // [S | F'] = Q [K; U_K]^T
           mma_ss(sc + kColF, duq[h] + o, dK[h] + so + o, idS32, 1);     // F' += U_Q K^T
           if (!JVP) mma_ss(sc + kColdP, ddo[h] + o, dV[h] + so + o, idS64, acc);  // [dP | G]
@@ -370,7 +381,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // One elected lane runs the whole schedule: every wait and every MMA.
     if (elect_one()) {
-      bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
+      bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err) &&
+                (!JVP || mbar_wait(&sm.a_ready, 0, abort_flag, err));
       tc_fence_after();
       // Phase A: tile a goes to warpgroup a mod 2 once that warpgroup holds
       // tile a - 2 in registers.
@@ -448,6 +460,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Ei = o.y;
       }
     };
+
+    if (JVP) {
+      // Copy this thread's row of Q (warpgroup 0) or U_Q (warpgroup 1) from
+      // the two 128-byte-swizzled TMA halves (16-byte chunk c of row r at
+      // chunk c ^ (r mod 8)) into TMEM: K step kk is chunks 2 (kk mod 4) and
+      // 2 (kk mod 4) + 1 of half kk / 4.
+      ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
+      if (ok) {
+        const uint32_t col = wg == 0 ? kJvpQA : kJvpUQA;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint8_t* row = (wg == 0 ? sm.q[kk >> 2] : sm.uq[kk >> 2]) + r * 128;
+          const int c = 2 * (kk & 3);
+          const uint4 x = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+          const uint4 y = *reinterpret_cast<const uint4*>(row + (((c + 1) ^ (r & 7)) << 4));
+          const uint32_t v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+          tmem_st8(tbase + lane_off + col + 8 * kk, v);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      warp_arrive(&sm.a_ready);
+    }
 
     // u counts this warpgroup's tiles (phase A, then phase B): sc_full and
     // op_ready phases.  Warp-uniform decisions (tcgen05.ld/st are
