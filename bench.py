@@ -359,7 +359,10 @@ def gpu_uuid(torch, local):
 
 class Resident:
     """Inputs, row state and outputs of one workload in device memory, and the
-    timed step (pass 1 then pass 2 on the current stream)."""
+    timed step: one flashbob_bob call on the current stream (both passes;
+    with several head groups the library overlaps the groups' chains on its
+    own streams); step_passes runs the two passes as separate calls, each
+    bracketed by events, for the per-kernel times."""
 
     def __init__(self, w, x, fb, torch):
         self.w, self.fb = w, fb
@@ -370,6 +373,21 @@ class Resident:
         self.stream = torch.cuda.current_stream()
 
     def step(self, ev=None):
+        w, d, o, fb, st = self.w, self.dev, self.out, self.fb, self.stream
+        if ev is not None:
+            ev[0].record(st)
+        fb.flashbob_bob(d["Q"], d["K"], d["V"], self.O, d["dO"], self.L, self.D, d["UQ"],
+                        d["UK"], d["UV"], w.tau, o["dQt"], o["dKt"], o["dVt"], o["ddOt"],
+                        o["alpha"], o["E"], causal=w.causal, stream=st)
+        if ev is not None:
+            ev[1].record(st)
+
+    def launches_per_step(self):
+        w = self.w
+        return self.fb.flashbob_bob_launches(w.B, w.H, w.kv_heads, w.N, w.kv_len, w.d,
+                                             self.fb.FLASHBOB_BF16)
+
+    def step_passes(self, ev=None):
         w, d, o, fb, st = self.w, self.dev, self.out, self.fb, self.stream
         if ev is not None:
             ev[0].record(st)
@@ -401,14 +419,16 @@ class Resident:
 
 
 def timed_steps(res, steps, warmup, torch, barrier, uuid):
-    """W warm-up steps, then K steps with CUDA events around each pass on the
-    launching stream and nvidia-smi clocks sampled during the timed region."""
+    """W warm-up steps, then K steps (one flashbob_bob call each) with CUDA
+    events on the launching stream and nvidia-smi clocks sampled during the
+    timed region; then, outside it, K steps of the two passes as separate
+    calls, each pass between two events, for the per-kernel times."""
     fb = res.fb
     for _ in range(max(3, warmup)):
         res.step()
     torch.cuda.synchronize()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     sampler = ClockSampler(uuid)
     time.sleep(0.3)
     barrier()
@@ -417,9 +437,16 @@ def timed_steps(res, steps, warmup, torch, barrier, uuid):
     barrier()
     clocks = sampler.stop()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-    return {"total_ms": evs[0][0].elapsed_time(evs[-1][2]),
-            "p1_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-            "p2_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    res.step_passes()
+    for i in range(steps):
+        res.step_passes(pev[i])
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    return {"total_ms": evs[0][0].elapsed_time(evs[-1][1]),
+            "p1_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in pev),
+            "p2_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in pev),
+            "passes_ms": statistics.mean(e[0].elapsed_time(e[2]) for e in pev),
             "clocks": clocks}
 
 
@@ -457,6 +484,8 @@ def run_sweep(args, fb, torch, barrier, uuid, peak, peak_note):
                 "ms_per_step": ms, "steps": steps, "warmup": 3, "dtype": "bf16",
                 "pct_of_peak": 100.0 * value / peak,
                 "config": dict(config_dict(w), pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
+                               passes_as_separate_calls_ms=t["passes_ms"],
+                               head_group_streams=res.launches_per_step() // 2,
                                prep_ms_outside_step=res.prep_ms(torch),
                                flops_per_step=w.flops),
                 "roofline": roofline(w, t, peak, peak_note), "clocks": t["clocks"]}
@@ -601,6 +630,7 @@ def main():
     res = Resident(w, x, fb, torch)
     uuid = gpu_uuid(torch, local)
     t = timed_steps(res, args.steps, args.warmup, torch, barrier, uuid)
+    res_launches = res.launches_per_step()
     prep_ms = res.prep_ms(torch)
     in_bytes = res.input_bytes()
     total_ms = reduce_max(t["total_ms"], world, "cuda")
@@ -629,12 +659,14 @@ def main():
         "config": dict(config_dict(w), flops_per_step_per_gpu=flops,
                        l2=f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
                           f"{L2_BYTES / 2**20:.0f} MiB",
-                       pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"], prep_ms_outside_step=prep_ms,
+                       pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
+                       passes_as_separate_calls_ms=t["passes_ms"],
+                       head_group_streams=res_launches // 2, prep_ms_outside_step=prep_ms,
                        pct_of_peak=100.0 * (value / world) / peak,
                        paths="tcgen05" if fb.flashbob_bob_tile_sizes(w.d, fb.FLASHBOB_BF16)[
                            "Br1"] == 128 else "simt"),
         "roofline": rl,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": res_launches * args.steps,
         "clocks": t["clocks"],
         "e2e": e2e,
     }

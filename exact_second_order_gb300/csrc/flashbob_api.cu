@@ -220,6 +220,25 @@ flashbob_status flashbob_bob_pass2(const void* Q, const void* K, const void* V, 
   return run_bob(a, causal, in_dtype);
 }
 
+flashbob_status flashbob_bob_launches(int B, int H, int Hkv, int Nq, int Nk, int d,
+                                      flashbob_dtype in_dtype, int* launches) {
+  if (check_dtype(in_dtype) != FLASHBOB_OK || launches == nullptr)
+    return FLASHBOB_ERR_INVALID_ARG;
+  const flashbob_status st = check_sizes(B, H, Hkv, Nq, Nk, d, 1.0f);
+  if (st != FLASHBOB_OK) return st;
+  BobArgs a{};
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.bf16 = in_dtype == FLASHBOB_BF16;
+  a.passes = kPass1 | kPass2;
+  *launches = tc_supported(a) ? 2 * tc_bob_streams(a) : 2;
+  return FLASHBOB_OK;
+}
+
 flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1, int* Bc1,
                                         int* Br2, int* Bc2, size_t* smem_bytes_pass1,
                                         size_t* smem_bytes_pass2) {

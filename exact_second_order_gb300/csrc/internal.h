@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (flashbob_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,6 +34,7 @@ struct BobArgs {
   cudaStream_t stream;
   unsigned int* err;  // device error word of the current device
   int passes;         // bit 0: pass 1, bit 1: pass 2
+  bool whole_grid_only = false;  // pass 2: never split a key block across a cluster
 };
 
 // Attention JVP (forward-mode derivative along U_Q, U_K, U_V).
@@ -69,12 +71,25 @@ bool tc_supported(const BobArgs& a);
 bool tc_prep_supported(const PrepArgs& a);
 cudaError_t tc_prep(const PrepArgs& a);
 cudaError_t tc_bob(const BobArgs& a);
+// Streams tc_bob runs a call on: 1 (the caller's), or up to 4 internal
+// streams, one per slice of the key/value heads, when both passes are asked
+// for, there are several head groups and a pass has more than two waves of
+// CTAs (the groups' pass 1 -> pass 2 chains then overlap each other's tails).
+int tc_bob_streams(const BobArgs& a);
 bool tc_jvp_supported(const JvpArgs& a);
 cudaError_t tc_jvp(const JvpArgs& a);
 size_t tc_pass1_smem();
 size_t tc_pass2_smem();
 size_t tc_pass1_d128_smem();
 size_t tc_pass2_d128_smem();
+// Tensor map of a bf16 [BH, N, dh] tensor with 128-byte-swizzled boxes of
+// `rows` x 64 elements (tc::make_map_bf16), kept in a small per-process
+// cache keyed by every encoding argument: a map is a pure function of them,
+// so repeated calls on the same buffers skip the driver's encoder.
+cudaError_t tc_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int rows, int dh);
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes), once per
+// (kernel, device, bytes).
+cudaError_t tc_set_smem(const void* kernel, int bytes);
 // Pass 2 cluster split: how many CTAs (S = 1 .. 8) share a key block of
 // `tiles` streamed query tiles when the `blocks` key blocks cannot fill the
 // device: the largest S whose clusters of the split kernel all fit at once.

@@ -388,10 +388,5 @@ inline cudaError_t make_map_bf16(CUtensorMap* map, const void* base, int BH, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-inline cudaError_t make_map_bf16_d64(CUtensorMap* map, const void* base, int BH, int N,
-                                     int rows) {
-  return make_map_bf16(map, base, BH, N, rows, 64);
-}
-
 }  // namespace tc
 }  // namespace flashbob

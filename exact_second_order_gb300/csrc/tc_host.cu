@@ -76,6 +76,68 @@ cudaError_t cluster_fit(const void* kernel, size_t smem, int S, int* out) {
 
 }  // namespace
 
+namespace {
+
+struct MapEntry {
+  const void* base = nullptr;
+  int BH = 0, N = 0, rows = 0, dh = 0;
+  uint64_t used = 0;  // last use, for replacement
+  CUtensorMap map;
+};
+
+std::mutex g_map_mu;
+MapEntry g_maps[64];
+uint64_t g_map_clock = 0;
+
+struct SmemSet {
+  const void* kernel = nullptr;
+  int device = -1, bytes = 0;
+};
+
+std::mutex g_smem_mu;
+SmemSet g_smem[64];
+
+}  // namespace
+
+cudaError_t tc_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int rows, int dh) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry* victim = &g_maps[0];
+  for (MapEntry& m : g_maps) {
+    if (m.base == base && m.BH == BH && m.N == N && m.rows == rows && m.dh == dh &&
+        base != nullptr) {
+      m.used = ++g_map_clock;
+      *map = m.map;
+      return cudaSuccess;
+    }
+    if (m.used < victim->used) victim = &m;
+  }
+  const cudaError_t e = tc::make_map_bf16(map, base, BH, N, rows, dh);
+  if (e != cudaSuccess) return e;
+  victim->base = base;
+  victim->BH = BH;
+  victim->N = N;
+  victim->rows = rows;
+  victim->dh = dh;
+  victim->used = ++g_map_clock;
+  victim->map = *map;
+  return cudaSuccess;
+}
+
+cudaError_t tc_set_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  SmemSet* slot = nullptr;
+  for (SmemSet& s : g_smem) {
+    if (s.kernel == kernel && s.device == dev && s.bytes == bytes) return cudaSuccess;
+    if (slot == nullptr && s.kernel == nullptr) slot = &s;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && slot != nullptr) *slot = SmemSet{kernel, dev, bytes};
+  return e;
+}
+
 cudaError_t tc_pass2_split(const void* split_kernel, size_t smem, int blocks, int tiles,
                            int* S) {
   // Split only grids that leave SMs idle: the largest S whose clusters still
@@ -106,9 +168,9 @@ cudaError_t tc_bob_d128(const BobArgs& a) {
     const void* rows[3] = {a.Q, a.dO, a.UQ};
     const void* cols[4] = {a.K, a.V, a.UK, a.UV};
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16(&m128[i], rows[i], BH, a.Nq, kTcRows, 128);
+      e = tc_map_bf16(&m128[i], rows[i], BH, a.Nq, kTcRows, 128);
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16(&m32[i], cols[i], BHkv, a.Nk, kTcStream, 128);
+      e = tc_map_bf16(&m32[i], cols[i], BHkv, a.Nk, kTcStream, 128);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass1_d128(a, m128, m32);
     if (e != cudaSuccess) return e;
@@ -118,9 +180,9 @@ cudaError_t tc_bob_d128(const BobArgs& a) {
     const void* res[4] = {a.K, a.UK, a.V, a.UV};
     const void* str[3] = {a.Q, a.UQ, a.dO};
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16(&m128[i], res[i], BHkv, a.Nk, kTcRows, 128);
+      e = tc_map_bf16(&m128[i], res[i], BHkv, a.Nk, kTcRows, 128);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16(&m32[i], str[i], BH, a.Nq, kTcStream, 128);
+      e = tc_map_bf16(&m32[i], str[i], BH, a.Nq, kTcStream, 128);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass2_d128(a, m128, m32);
   }
@@ -129,8 +191,7 @@ cudaError_t tc_bob_d128(const BobArgs& a) {
 
 }  // namespace
 
-cudaError_t tc_bob(const BobArgs& a) {
-  if (a.d == 128) return tc_bob_d128(a);
+static cudaError_t tc_bob_d64(const BobArgs& a) {
   const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
   cudaError_t e = cudaSuccess;
   if (a.passes & kPass1) {
@@ -138,9 +199,9 @@ cudaError_t tc_bob(const BobArgs& a) {
     const void* rows[3] = {a.Q, a.dO, a.UQ};
     const void* cols[4] = {a.K, a.V, a.UK, a.UV};
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m128[i], rows[i], BH, a.Nq, kTcRows);
+      e = tc_map_bf16(&m128[i], rows[i], BH, a.Nq, kTcRows, 64);
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m32[i], cols[i], BHkv, a.Nk, kTcStream);
+      e = tc_map_bf16(&m32[i], cols[i], BHkv, a.Nk, kTcStream, 64);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass1(a, m128, m32);
     if (e != cudaSuccess) return e;
@@ -150,13 +211,151 @@ cudaError_t tc_bob(const BobArgs& a) {
     const void* res[4] = {a.K, a.UK, a.V, a.UV};
     const void* str[3] = {a.Q, a.UQ, a.dO};
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m128[i], res[i], BHkv, a.Nk, kTcRows);
+      e = tc_map_bf16(&m128[i], res[i], BHkv, a.Nk, kTcRows, 64);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = tc::make_map_bf16_d64(&m64[i], str[i], BH, a.Nq, kTcStream2);
+      e = tc_map_bf16(&m64[i], str[i], BH, a.Nq, kTcStream2, 64);
     if (e != cudaSuccess) return e;
     e = tc_launch_pass2(a, m128, m64);
   }
   return e;
+}
+
+namespace {
+
+// Head-group streams.  Pass 2 of a key/value head needs pass 1 of that
+// head's query rows only, so the two passes of disjoint head groups are
+// independent.  A call with several groups and more than a wave of CTAs per
+// pass runs the groups' pass 1 -> pass 2 chains on kSplitStreams internal
+// streams (forked from and joined back into the caller's stream): the SMs
+// that one group's last pass-1 wave leaves idle take other groups' CTAs
+// instead of waiting for the whole pass to drain.
+constexpr int kSplitStreams = 4;
+
+struct SplitStreams {
+  int device = -1;
+  cudaStream_t stream[kSplitStreams] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join[kSplitStreams] = {};
+};
+
+std::mutex g_split_mu;
+SplitStreams g_split[16];
+
+// The current device's streams and events, made on first use (g_split_mu
+// held); null when every slot is taken by another device.
+cudaError_t split_streams(SplitStreams** out) {
+  *out = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  SplitStreams* slot = nullptr;
+  for (SplitStreams& r : g_split) {
+    if (r.device == dev) {
+      *out = &r;
+      return cudaSuccess;
+    }
+    if (slot == nullptr && r.device < 0) slot = &r;
+  }
+  if (slot == nullptr) return cudaSuccess;
+  SplitStreams r;
+  e = cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming);
+  for (int k = 0; k < kSplitStreams && e == cudaSuccess; ++k) {
+    e = cudaStreamCreateWithFlags(&r.stream[k], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.join[k], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    if (r.fork) cudaEventDestroy(r.fork);
+    for (int k = 0; k < kSplitStreams; ++k) {
+      if (r.stream[k]) cudaStreamDestroy(r.stream[k]);
+      if (r.join[k]) cudaEventDestroy(r.join[k]);
+    }
+    return e;
+  }
+  r.device = dev;
+  *slot = r;
+  *out = slot;
+  return cudaSuccess;
+}
+
+// The sub-problem of key/value heads [g0, g1) of the flattened B * Hkv heads
+// (query heads [g0 G, g1 G) of the flattened B * H): contiguous slices of
+// every tensor, one batch of H' = (g1 - g0) G query heads.
+BobArgs head_slice(const BobArgs& a, int g0, int g1) {
+  const int G = a.H / a.Hkv;
+  const size_t d = static_cast<size_t>(a.d);
+  const size_t qr = static_cast<size_t>(g0) * G * a.Nq;  // first query row
+  const size_t kr = static_cast<size_t>(g0) * a.Nk;      // first key row
+  auto bf = [](const void* p, size_t elems) {
+    return static_cast<const void*>(static_cast<const char*>(p) + 2 * elems);
+  };
+  BobArgs s = a;
+  // The groups run side by side and fill the GPU together: no group's pass 2
+  // splits its key blocks across clusters (which would also change the
+  // order of its column sums).
+  s.whole_grid_only = true;
+  s.Q = bf(a.Q, qr * d);
+  s.dO = bf(a.dO, qr * d);
+  s.UQ = bf(a.UQ, qr * d);
+  s.K = bf(a.K, kr * d);
+  s.V = bf(a.V, kr * d);
+  s.UK = bf(a.UK, kr * d);
+  s.UV = bf(a.UV, kr * d);
+  s.O = a.O + qr * d;
+  s.L = a.L + qr;
+  s.D = a.D + qr;
+  s.dQt = a.dQt + qr * d;
+  s.ddOt = a.ddOt + qr * d;
+  s.alpha = a.alpha + qr;
+  s.E = a.E + qr;
+  s.dKt = a.dKt + kr * d;
+  s.dVt = a.dVt + kr * d;
+  s.B = 1;
+  s.Hkv = g1 - g0;
+  s.H = (g1 - g0) * G;
+  return s;
+}
+
+cudaError_t tc_bob_one(const BobArgs& a) { return a.d == 128 ? tc_bob_d128(a) : tc_bob_d64(a); }
+
+}  // namespace
+
+int tc_bob_streams(const BobArgs& a) {
+  const int groups = a.B * a.Hkv;
+  int dev = 0, sms = 0;
+  if (a.passes != (kPass1 | kPass2) || groups < 2 || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      static_cast<long long>(a.B) * a.H * ((a.Nq + kTcRows - 1) / kTcRows) <= 2LL * sms)
+    return 1;
+  return groups < kSplitStreams ? groups : kSplitStreams;
+}
+
+cudaError_t tc_bob(const BobArgs& a) {
+  const int groups = a.B * a.Hkv;
+  const int ns = tc_bob_streams(a);
+  if (ns == 1) return tc_bob_one(a);
+  std::lock_guard<std::mutex> lock(g_split_mu);
+  SplitStreams* ss = nullptr;
+  cudaError_t e = split_streams(&ss);
+  if (e != cudaSuccess) return e;
+  if (ss == nullptr) return tc_bob_one(a);
+  e = cudaEventRecord(ss->fork, a.stream);
+  if (e != cudaSuccess) return e;
+  for (int k = 0; k < ns && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(ss->stream[k], ss->fork, 0);
+  if (e != cudaSuccess) return e;
+  cudaError_t first = cudaSuccess;
+  for (int k = 0; k < ns; ++k) {
+    BobArgs s = head_slice(a, groups * k / ns, groups * (k + 1) / ns);
+    s.stream = ss->stream[k];
+    const cudaError_t ek = tc_bob_one(s);
+    if (first == cudaSuccess) first = ek;
+  }
+  // Join every stream back, whatever happened above.
+  for (int k = 0; k < ns; ++k) {
+    e = cudaEventRecord(ss->join[k], ss->stream[k]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(a.stream, ss->join[k], 0);
+    if (first == cudaSuccess) first = e;
+  }
+  return first;
 }
 
 bool tc_jvp_supported(const JvpArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
@@ -167,9 +366,9 @@ cudaError_t tc_jvp(const JvpArgs& a) {
   const void* cols[4] = {a.K, a.V, a.UK, a.UV};
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < 2 && e == cudaSuccess; ++i)
-    e = tc::make_map_bf16(&m128[i], rows[i], a.B * a.H, a.Nq, kTcRows, a.d);
+    e = tc_map_bf16(&m128[i], rows[i], a.B * a.H, a.Nq, kTcRows, a.d);
   for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-    e = tc::make_map_bf16(&m32[i], cols[i], a.B * a.Hkv, a.Nk, kTcStream, a.d);
+    e = tc_map_bf16(&m32[i], cols[i], a.B * a.Hkv, a.Nk, kTcStream, a.d);
   if (e != cudaSuccess) return e;
   return a.d == 128 ? tc_launch_jvp_d128(a, m128, m32) : tc_launch_jvp(a, m128, m32);
 }

@@ -513,8 +513,7 @@ cudaError_t tc_launch_jvp(const JvpArgs& a, const CUtensorMap* maps128,
                           const CUtensorMap* maps32) {
   // maps128: Q, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
   const size_t smem = tc_pass1_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_kernel<true>), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_pass1_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(
@@ -528,8 +527,7 @@ cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps32) {
   // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
   const size_t smem = tc_pass1_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass1_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_kernel<false>), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_pass1_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(

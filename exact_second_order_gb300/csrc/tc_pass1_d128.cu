@@ -627,8 +627,7 @@ cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
   // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
   // boxes; every box is 64 columns wide (one half of a 128-column row).
   const size_t smem = tc_pass1_d128_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass1_d128_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<false>), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_pass1_d128_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
@@ -646,8 +645,7 @@ cudaError_t tc_launch_jvp_d128(const JvpArgs& a, const CUtensorMap* maps128,
   // maps128: Q, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
   // boxes (64-column halves).
   const size_t smem = tc_pass1_d128_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass1_d128_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<true>), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_pass1_d128_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(

@@ -588,19 +588,18 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps64) {
   // maps128: K, U_K, V, U_V with 128-row boxes; maps64: Q, U_Q, dO with 64-row boxes.
   const size_t smem = tc_pass2_smem();
-  cudaError_t e = cudaFuncSetAttribute(tc_pass2_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass2_kernel<false>), (int)smem);
   if (e != cudaSuccess) return e;
   // One CTA per key block of a shared head, or, when the key blocks cannot
   // fill the SMs, a cluster of S of them that splits the block's query tiles
   // S ways.
-  e = cudaFuncSetAttribute(tc_pass2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  e = tc_set_smem(reinterpret_cast<const void*>(tc_pass2_kernel<true>), (int)smem);
   if (e != cudaSuccess) return e;
   const int tiles = (a.H / a.Hkv) * ((a.Nq + BQ - 1) / BQ);
   int S = 1;
-  e = tc_pass2_split(reinterpret_cast<const void*>(tc_pass2_kernel<true>), smem,
-                     ((a.Nk + BM - 1) / BM) * a.Hkv * a.B, tiles, &S);
+  if (!a.whole_grid_only)
+    e = tc_pass2_split(reinterpret_cast<const void*>(tc_pass2_kernel<true>), smem,
+                       ((a.Nk + BM - 1) / BM) * a.Hkv * a.B, tiles, &S);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {

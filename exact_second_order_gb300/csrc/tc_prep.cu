@@ -384,13 +384,12 @@ cudaError_t launch_prep(const PrepArgs& a) {
   const int BH = a.B * a.H;
   const int BHkv = a.B * a.Hkv;
   CUtensorMap mq, mk, mv;
-  cudaError_t e = tc::make_map_bf16(&mq, a.Q, BH, a.Nq, kTcRows, DH);
-  if (e == cudaSuccess) e = tc::make_map_bf16(&mk, a.K, BHkv, a.Nk, PrepCfg<DH>::kBN, DH);
-  if (e == cudaSuccess) e = tc::make_map_bf16(&mv, a.V, BHkv, a.Nk, PrepCfg<DH>::kBN, DH);
+  cudaError_t e = tc_map_bf16(&mq, a.Q, BH, a.Nq, kTcRows, DH);
+  if (e == cudaSuccess) e = tc_map_bf16(&mk, a.K, BHkv, a.Nk, PrepCfg<DH>::kBN, DH);
+  if (e == cudaSuccess) e = tc_map_bf16(&mv, a.V, BHkv, a.Nk, PrepCfg<DH>::kBN, DH);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem0<DH>) + 1024;
-  e = cudaFuncSetAttribute(tc_prep_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  e = tc_set_smem(reinterpret_cast<const void*>(tc_prep_kernel<DH>), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
   tc_prep_kernel<DH><<<grid, NTHREADS, smem, a.stream>>>(

@@ -32,6 +32,7 @@ _SIGNATURES = {
     "flashbob_bob_pass1": ([_P] * 10 + [_F] + [_P] * 4 + [_I] * 8 + [_P], _I),
     "flashbob_bob_pass2": ([_P] * 11 + [_F] + [_P] * 2 + [_I] * 8 + [_P], _I),
     "flashbob_attention_jvp": ([_P] * 8 + [_F] + [_P] * 2 + [_I] * 8 + [_P], _I),
+    "flashbob_bob_launches": ([_I] * 7 + [ctypes.POINTER(_I)], _I),
     "flashbob_bob_tile_sizes": ([_I, _I] + [ctypes.POINTER(_I)] * 4
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
@@ -150,6 +151,16 @@ def flashbob_attention_jvp(Q, K, V, O, L, UQ, UK, UV, tau: float, Od, Ld,
         _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_attention_jvp")
+
+
+def flashbob_bob_launches(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int,
+                          in_dtype: int) -> int:
+    """Kernel launches of one flashbob_bob call with these sizes."""
+    n = ctypes.c_int()
+    st = load_library().flashbob_bob_launches(B, H, Hkv, Nq, Nk, d, in_dtype, ctypes.byref(n))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_bob_launches")
+    return n.value
 
 
 def flashbob_bob_tile_sizes(d: int, in_dtype: int) -> dict:

@@ -105,6 +105,16 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
  *   Limits: as flashbob_prep.  bf16 inputs with d = 64 or d = 128 run the
  *   tcgen05 tensor-core kernels; every other case runs the fp32 CUDA-core
  *   kernels.
+ *   Streams: the work is ordered after everything already queued on
+ *   `stream` and before everything queued on it afterwards.  On the
+ *   tensor-core path, with B * Hkv >= 2 key/value heads and more than two
+ *   waves of pass-1 CTAs, the heads are cut into up to four contiguous
+ *   groups whose pass 1 -> pass 2 chains run on internal streams of the
+ *   library, forked from and joined back into `stream` by events (pass 2 of
+ *   a head reads only pass 1's alpha and E of that head's query rows); the
+ *   results are those of the one-stream order, bit for bit.  Those streams
+ *   are made once per device and kept; calls serialize their enqueueing on
+ *   them.  flashbob_bob_launches says how many kernels a call launches.
  */
 flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const float* O,
                              const void* dO, const float* L, const float* D, const void* UQ,
@@ -121,7 +131,8 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
  *     writes dQt, ddOt, alpha, E.
  *   pass 2 (column-resident): reads Q, K, V, dO, L, D, U_Q, U_K, U_V and the
  *     alpha, E written by pass 1, and writes dKt, dVt.
- * flashbob_bob(...) is exactly pass 1 followed by pass 2 on the same stream.
+ * flashbob_bob(...) computes exactly pass 1 followed by pass 2 on the same
+ * stream (it may run head groups on internal streams; see flashbob_bob).
  */
 flashbob_status flashbob_bob_pass1(const void* Q, const void* K, const void* V, const float* O,
                                    const void* dO, const float* L, const float* D,
@@ -157,6 +168,15 @@ flashbob_status flashbob_attention_jvp(const void* Q, const void* K, const void*
                                        const void* UK, const void* UV, float tau, float* Od,
                                        float* Ld, int B, int H, int Hkv, int Nq, int Nk, int d,
                                        int causal, flashbob_dtype in_dtype, void* stream);
+
+/*
+ * flashbob_bob_launches: how many kernel launches one flashbob_bob call with
+ * these sizes makes on the current device (2: pass 1 and pass 2; 2 per head
+ * group when the call runs head groups on internal streams).  Checks the
+ * sizes as flashbob_bob does; `launches` must not be NULL.
+ */
+flashbob_status flashbob_bob_launches(int B, int H, int Hkv, int Nq, int Nk, int d,
+                                      flashbob_dtype in_dtype, int* launches);
 
 /*
  * flashbob_bob_tile_sizes: the tiles flashbob_bob uses for (d, in_dtype):

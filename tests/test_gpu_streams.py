@@ -1,0 +1,68 @@
+"""The head-group streams of flashbob_bob (a call with several key/value
+heads and more than two waves of pass-1 CTAs runs each group's pass 1 ->
+pass 2 chain on an internal stream): the results equal those of the two
+passes called one after the other on one stream, bit for bit, and the call
+stays ordered within the caller's stream (a later kernel on that stream sees
+every output)."""
+import pytest
+import torch
+
+from exact_second_order_gb300 import flashbob as fb
+from exact_second_order_gb300 import inputs as wl
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    wl.small_workload(1, 4, 16384, 64, "bf16", seed=11),                 # 4 groups, 512 CTAs
+    wl.small_workload(2, 3, 8192, 64, "bf16", seed=12, causal=True),     # 6 groups, causal
+    wl.small_workload(1, 8, 16384, 64, "bf16", seed=13, Hkv=2),          # GQA: 2 groups of 4
+    wl.small_workload(1, 4, 16384, 128, "bf16", seed=14, Nk=12288),      # d = 128, rectangular
+    wl.small_workload(1, 6, 16384, 128, "bf16", seed=15, causal=True),   # d = 128, 6 groups
+]
+
+
+def _run(w, split):
+    x = wl.make_inputs(w)
+    d = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(d["Q"], d["K"], d["V"], d["dO"], w.tau, causal=w.causal)
+    out = fb.alloc_bob_outputs(d["Q"], fill=float("nan"), K=d["K"])
+    st = torch.cuda.current_stream()
+    if split:
+        fb.flashbob_bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"],
+                        w.tau, out["dQt"], out["dKt"], out["dVt"], out["ddOt"], out["alpha"],
+                        out["E"], causal=w.causal, stream=st)
+    else:
+        fb.flashbob_bob_pass1(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"],
+                              d["UV"], w.tau, out["dQt"], out["ddOt"], out["alpha"], out["E"],
+                              causal=w.causal, stream=st)
+        fb.flashbob_bob_pass2(d["Q"], d["K"], d["V"], d["dO"], L, D, out["alpha"], out["E"],
+                              d["UQ"], d["UK"], d["UV"], w.tau, out["dKt"], out["dVt"],
+                              causal=w.causal, stream=st)
+    # Read on the caller's stream right behind the call, before any device
+    # synchronisation: a kernel queued there must see every output.
+    sums = {k: torch.nan_to_num(v, nan=1e30).double().sum() for k, v in out.items()}
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    return out, {k: v.item() for k, v in sums.items()}
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_head_group_streams_match_one_stream_bit_for_bit(w):
+    launches = fb.flashbob_bob_launches(w.B, w.H, w.kv_heads, w.N, w.kv_len, w.d,
+                                        fb.FLASHBOB_BF16)
+    groups = w.B * w.kv_heads
+    assert launches == 2 * min(4, groups), launches
+    split, split_sums = _run(w, True)
+    ref, _ = _run(w, False)
+    for k in ref:
+        assert not torch.isnan(split[k]).any().item(), f"{k}: unwritten elements"
+        assert torch.equal(split[k], ref[k]), f"{k} differs from the one-stream passes"
+        # the stream-ordered reduction saw the finished outputs
+        assert split_sums[k] == pytest.approx(ref[k].double().sum().item(), rel=0, abs=0)
+
+
+def test_small_calls_stay_on_the_callers_stream():
+    # one wave of pass-1 CTAs, or one head group: no internal streams
+    assert fb.flashbob_bob_launches(1, 4, 4, 1024, 1024, 64, fb.FLASHBOB_BF16) == 2
+    assert fb.flashbob_bob_launches(1, 12, 1, 65536, 65536, 64, fb.FLASHBOB_BF16) == 2
+    assert fb.flashbob_bob_launches(1, 4, 4, 65536, 65536, 64, fb.FLASHBOB_F32) == 2
