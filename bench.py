@@ -60,7 +60,25 @@ def parse_args():
                     help="also time every workload of the throughput-vs-length table")
     ap.add_argument("--sweep-oracle", action="store_true",
                     help="with --sweep: time the full fp64 oracle on the small configurations")
+    ap.add_argument("--mma-costs", action="store_true",
+                    help="only measure SM cycles per tcgen05.mma (M 128, K 16) for N = 16..256, "
+                         "A from shared or tensor memory (flashbob_mma_cycles); one line each")
     return ap.parse_args()
+
+
+def run_mma_costs(fb, torch):
+    """One JSON line per MMA shape: the median of 5 runs of 4096 back-to-back
+    MMAs, and the tensor-pipe efficiency N/2 / cycles (an M = 128, K = 16 MMA
+    is N/2 cycles of math at the dense rate)."""
+    for a_in_tmem in (False, True):
+        for n in (16, 32, 48, 64, 96, 128, 192, 256):
+            c = statistics.median(fb.flashbob_mma_cycles(n, a_in_tmem) for _ in range(5))
+            print(json.dumps({"mma_costs": True, "m": 128, "n": n, "k": 16,
+                              "a": "tmem" if a_in_tmem else "smem", "b": "smem",
+                              "cycles_per_mma": round(c, 2),
+                              "math_cycles": n / 2, "efficiency": round(n / 2 / c, 3)}),
+                  flush=True)
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
 
 
 def dist_env():
@@ -387,6 +405,11 @@ class Resident:
         return self.fb.flashbob_bob_launches(w.B, w.H, w.kv_heads, w.N, w.kv_len, w.d,
                                              self.fb.FLASHBOB_BF16)
 
+    def streams_per_step(self):
+        w = self.w
+        per_stream = 3 if w.d == 128 else 2  # d = 128: pass 1 is two launches
+        return self.launches_per_step() // per_stream
+
     def step_passes(self, ev=None):
         w, d, o, fb, st = self.w, self.dev, self.out, self.fb, self.stream
         if ev is not None:
@@ -485,7 +508,7 @@ def run_sweep(args, fb, torch, barrier, uuid, peak, peak_note):
                 "pct_of_peak": 100.0 * value / peak,
                 "config": dict(config_dict(w), pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                                passes_as_separate_calls_ms=t["passes_ms"],
-                               head_group_streams=res.launches_per_step() // 2,
+                               head_group_streams=res.streams_per_step(),
                                prep_ms_outside_step=res.prep_ms(torch),
                                flops_per_step=w.flops),
                 "roofline": roofline(w, t, peak, peak_note), "clocks": t["clocks"]}
@@ -615,6 +638,8 @@ def main():
     from exact_second_order_gb300 import flashbob as fb
 
     torch.cuda.set_device(local)
+    if args.mma_costs:
+        return run_mma_costs(fb, torch)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
@@ -650,7 +675,8 @@ def main():
         torch.cuda.empty_cache()
     peak, sustained, peak_note = tensor_peak()
     rl = roofline(w, t, peak, peak_note)
-    rl["traffic"] = read_traffic().get(rl["kernel"])
+    # The committed counters are of the benchmark workload's bytes only.
+    rl["traffic"] = read_traffic().get(rl["kernel"]) if w.name == DEFAULT_WORKLOAD else None
     rl["frac_of_sustained"] = rl["achieved"] / sustained
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -661,7 +687,7 @@ def main():
                           f"{L2_BYTES / 2**20:.0f} MiB",
                        pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                        passes_as_separate_calls_ms=t["passes_ms"],
-                       head_group_streams=res_launches // 2, prep_ms_outside_step=prep_ms,
+                       head_group_streams=res.streams_per_step(), prep_ms_outside_step=prep_ms,
                        pct_of_peak=100.0 * (value / world) / peak,
                        paths="tcgen05" if fb.flashbob_bob_tile_sizes(w.d, fb.FLASHBOB_BF16)[
                            "Br1"] == 128 else "simt"),

@@ -235,7 +235,8 @@ flashbob_status flashbob_bob_launches(int B, int H, int Hkv, int Nq, int Nk, int
   a.d = d;
   a.bf16 = in_dtype == FLASHBOB_BF16;
   a.passes = kPass1 | kPass2;
-  *launches = tc_supported(a) ? 2 * tc_bob_streams(a) : 2;
+  // Per head group: pass 1 (d = 128: the JVP launch and the rows launch) and pass 2.
+  *launches = tc_supported(a) ? (d == 128 ? 3 : 2) * tc_bob_streams(a) : 2;
   return FLASHBOB_OK;
 }
 
@@ -306,6 +307,16 @@ flashbob_status flashbob_check_wait_timeout(void* stream) {
   if (error_word_ptr(&err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
   return launch_wait_timeout((cudaStream_t)stream, err) == cudaSuccess ? FLASHBOB_OK
                                                                        : FLASHBOB_ERR_CUDA;
+}
+
+flashbob_status flashbob_mma_cycles(int n, int a_in_tmem, void* stream, double* cycles_per_mma) {
+  if (cycles_per_mma == nullptr || n < 16 || n > 256 || n % 16 != 0)
+    return FLASHBOB_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  if (error_word_ptr(&err) != cudaSuccess) return FLASHBOB_ERR_CUDA;
+  return mma_cycles(n, a_in_tmem != 0, (cudaStream_t)stream, err, cycles_per_mma) == cudaSuccess
+             ? FLASHBOB_OK
+             : FLASHBOB_ERR_CUDA;
 }
 
 flashbob_status flashbob_last_device_error(void) {

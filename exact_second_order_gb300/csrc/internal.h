@@ -101,5 +101,10 @@ cudaError_t tc_pass2_split(const void* split_kernel, size_t smem, int blocks, in
 cudaError_t error_word_ptr(unsigned int** ptr);
 // One CTA whose bounded wait runs out (the timeout report, tested on a GPU).
 cudaError_t launch_wait_timeout(cudaStream_t stream, unsigned int* err);
+// Cycles per tcgen05.mma (M = 128, N = n, K = 16, bf16) issued back to back
+// by one thread of one CTA, A from shared memory or tensor memory; waits for
+// the result (0 cycles when the run's bounded wait gave up).
+cudaError_t mma_cycles(int n, bool a_in_tmem, cudaStream_t stream, unsigned int* err,
+                       double* cycles_per_mma);
 
 }  // namespace flashbob

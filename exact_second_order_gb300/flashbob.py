@@ -37,6 +37,7 @@ _SIGNATURES = {
                                 + [ctypes.POINTER(ctypes.c_size_t)] * 2, _I),
     "flashbob_last_device_error": ([], _I),
     "flashbob_check_wait_timeout": ([_P], _I),
+    "flashbob_mma_cycles": ([_I, _I, _P, ctypes.POINTER(ctypes.c_double)], _I),
     "flashbob_status_string": ([_I], ctypes.c_char_p),
 }
 
@@ -180,6 +181,16 @@ def flashbob_check_wait_timeout(stream=None) -> None:
     st = load_library().flashbob_check_wait_timeout(_stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_check_wait_timeout")
+
+
+def flashbob_mma_cycles(n: int, a_in_tmem: bool, stream=None) -> float:
+    """SM cycles per tcgen05.mma of M = 128, N = n, K = 16 (see the header)."""
+    c = ctypes.c_double()
+    st = load_library().flashbob_mma_cycles(n, int(a_in_tmem), _stream_handle(stream),
+                                             ctypes.byref(c))
+    if st != FLASHBOB_OK:
+        raise FlashbobError(st, "flashbob_mma_cycles")
+    return c.value
 
 
 def flashbob_last_device_error() -> int:

@@ -124,7 +124,7 @@ flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const 
                              void* stream);
 
 /*
- * flashbob_bob_pass1 / flashbob_bob_pass2: the two launches of flashbob_bob,
+ * flashbob_bob_pass1 / flashbob_bob_pass2: the two passes of flashbob_bob,
  * callable one at a time ([FBN] 关键设计 2).  Same arguments, layouts and
  * limits as flashbob_bob.
  *   pass 1 (row-resident): reads Q, K, V, O, dO, L, D, U_Q, U_K, U_V and
@@ -171,9 +171,11 @@ flashbob_status flashbob_attention_jvp(const void* Q, const void* K, const void*
 
 /*
  * flashbob_bob_launches: how many kernel launches one flashbob_bob call with
- * these sizes makes on the current device (2: pass 1 and pass 2; 2 per head
- * group when the call runs head groups on internal streams).  Checks the
- * sizes as flashbob_bob does; `launches` must not be NULL.
+ * these sizes makes on the current device: pass 1 and pass 2, where pass 1
+ * of the tensor-core path at d = 128 is two launches (the JVP with alpha,
+ * d~dO and E, then d~Q); that many per head group when the call runs head
+ * groups on internal streams.  Checks the sizes as flashbob_bob does;
+ * `launches` must not be NULL.
  */
 flashbob_status flashbob_bob_launches(int B, int H, int Hkv, int Nq, int Nk, int d,
                                       flashbob_dtype in_dtype, int* launches);
@@ -205,6 +207,21 @@ flashbob_status flashbob_last_device_error(void);
  * stays usable.  Returns FLASHBOB_ERR_CUDA if the launch fails.
  */
 flashbob_status flashbob_check_wait_timeout(void* stream);
+
+/*
+ * flashbob_mma_cycles: a diagnostic of the tensor-core issue rate, with no
+ * counterpart on the pages.  One CTA on `stream` issues 4096 tcgen05.mma of
+ * one shape back to back from one thread (M = 128, N = n, K = 16, bf16
+ * operands, fp32 accumulator in tensor memory; A from shared memory, or from
+ * tensor memory when a_in_tmem != 0; B from shared memory) and times them
+ * with the SM clock up to the completion of the last one.  Writes the SM
+ * cycles per MMA to *cycles_per_mma (0 if the run's bounded wait gave up)
+ * and synchronises `stream`.  The BoB kernels' schedules count their MMAs
+ * in these units.
+ *   n: 16 .. 256, a multiple of 16 (else FLASHBOB_ERR_INVALID_ARG, as for a
+ *      NULL cycles_per_mma); FLASHBOB_ERR_CUDA if a CUDA call fails.
+ */
+flashbob_status flashbob_mma_cycles(int n, int a_in_tmem, void* stream, double* cycles_per_mma);
 
 /* flashbob_status_string: a static, human-readable name of `s`. */
 const char* flashbob_status_string(flashbob_status s);

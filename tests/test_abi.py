@@ -212,3 +212,27 @@ def test_jvp_and_forward_only_prep_reject_bad_arguments_on_the_host(lib):
         p[i] = None
         assert lib.flashbob_prep(*p, 1, 1, 1, 8, 8, 64, 0.125, 0, 0, None) == \
             fb.FLASHBOB_ERR_INVALID_ARG
+
+
+def test_launch_count_query_checks_its_arguments(lib):
+    n = ctypes.c_int(-1)
+    # fp32 runs the two CUDA-core launches whatever the sizes
+    assert lib.flashbob_bob_launches(1, 4, 4, 65536, 65536, 64, fb.FLASHBOB_F32,
+                                     ctypes.byref(n)) == fb.FLASHBOB_OK
+    assert n.value == 2
+    for bad in ((0, 4, 4, 8, 8, 64), (1, 4, 3, 8, 8, 64), (1, 4, 4, 0, 8, 64),
+                (1, 4, 4, 8, 8, 129)):
+        assert lib.flashbob_bob_launches(*bad, fb.FLASHBOB_BF16, ctypes.byref(n)) != \
+            fb.FLASHBOB_OK, bad
+    assert lib.flashbob_bob_launches(1, 4, 4, 8, 8, 64, 7, ctypes.byref(n)) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+    assert lib.flashbob_bob_launches(1, 4, 4, 8, 8, 64, fb.FLASHBOB_BF16, None) == \
+        fb.FLASHBOB_ERR_INVALID_ARG
+
+
+def test_mma_cycles_rejects_bad_shapes_before_any_launch(lib):
+    c = ctypes.c_double()
+    for n in (0, 8, 24, 272, -16):
+        assert lib.flashbob_mma_cycles(n, 0, None, ctypes.byref(c)) == \
+            fb.FLASHBOB_ERR_INVALID_ARG, n
+    assert lib.flashbob_mma_cycles(64, 1, None, None) == fb.FLASHBOB_ERR_INVALID_ARG

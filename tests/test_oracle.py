@@ -716,3 +716,17 @@ def test_c_row_scalars_rejects_inexact_inputs():
     x = np.full((4, 3), 0.1)  # 0.1 is not an fp32 value
     with pytest.raises(ValueError):
         crows.row_scalars(x, x, x, x, x, x, x, 0.5)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal,scale", [(23, 23, False, 1.0), (23, 23, True, 1.0),
+                                                (9, 31, False, 2.0), (31, 9, True, 0.5)])
+def test_E_is_the_row_dot_of_dO_and_ddOt(Nq, Nk, causal, scale):
+    # E_i = sum_j P_ij d~P_ij with d~P = F o (dP - D) + G - alpha dP expands,
+    # through dP = dO V^T, G = dO U_V^T and D = dO . O, into the row dot
+    # dO_i . d~dO_i - alpha_i D_i (d~dO = P U_V + P o (F - alpha) V): E and
+    # d~dO come from different parts of the chain rule (the softmax node and
+    # the dO node), so this ties the two together.
+    Q, K, V, dO, UQ, UK, UV = [scale * m for m in _rand_rect(Nq, Nk, 5, 70 + Nq + Nk)]
+    r = orc.bob(Q, K, V, dO, UQ, UK, UV, 0.4, causal=causal)
+    E2 = (dO * r["ddOt"]).sum(axis=1) - r["alpha"] * r["D"]
+    assert np.allclose(E2, r["E"], rtol=1e-12, atol=1e-12 * np.abs(r["E"]).max())
