@@ -364,7 +364,8 @@ SWEEP = ("gpt2_layer_B4_H12_N1024_d64", "mid_B1_H12_N8192_d64", "mid_peaked_B1_H
          "long_B1_H4_N65536_d64", "extreme_B1_H1_N262144_d64", "extreme_B1_H1_N131072_d128",
          "causal_B4_H12_N4096_d64", "causal_B4_H12_N8192_d64", "causal_B4_H12_N16384_d64",
          "causal_B4_H12_N16384_d128", "causal_B4_H12_N32768_d128",
-         "causal_B4_H12_N65536_d128")
+         "causal_B4_H12_N65536_d128", "gqa_B1_H12_Hkv4_N8192_d64", "mqa_B1_H12_Hkv1_N8192_d64",
+         "rect_B1_H8_Nq4096_Nk16384_d64", "rect_B1_H8_Nq16384_Nk4096_d64")
 
 
 def gpu_uuid(torch, local):
@@ -656,6 +657,7 @@ def main():
     uuid = gpu_uuid(torch, local)
     t = timed_steps(res, args.steps, args.warmup, torch, barrier, uuid)
     res_launches = res.launches_per_step()
+    res_streams = res.streams_per_step()
     prep_ms = res.prep_ms(torch)
     in_bytes = res.input_bytes()
     total_ms = reduce_max(t["total_ms"], world, "cuda")
@@ -687,7 +689,7 @@ def main():
                           f"{L2_BYTES / 2**20:.0f} MiB",
                        pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                        passes_as_separate_calls_ms=t["passes_ms"],
-                       head_group_streams=res.streams_per_step(), prep_ms_outside_step=prep_ms,
+                       head_group_streams=res_streams, prep_ms_outside_step=prep_ms,
                        pct_of_peak=100.0 * (value / world) / peak,
                        paths="tcgen05" if fb.flashbob_bob_tile_sizes(w.d, fb.FLASHBOB_BF16)[
                            "Br1"] == 128 else "simt"),

@@ -122,6 +122,8 @@ LONGLOOP_D128 = Workload("longloop_B1_H1_Nq131072_Nk256_d128", 1, 1, 131072, 128
                          Nk=256)
 # A mid-size case for detailed profiles: inputs (~0.3 GB) larger than L2.
 PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
+# d = 128 kernels under ncu: one head (no head-group streams), inputs 176 MiB > L2.
+PROFILE_D128 = Workload("profile_B1_H1_N98304_d128", 1, 1, 98304, 128, "bf16")
 
 WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PEAKED,
                                  MID_LENGTH_STRESS, LONG_CONTEXT, EXTREME_D64, EXTREME_D128,
@@ -129,7 +131,7 @@ WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PE
                                  CAUSAL_N32768_D128, CAUSAL_N65536_D128, GQA_N8192,
                                  MQA_N8192,
                                  RECT_Q4096_K16384, RECT_Q16384_K4096, LONGLOOP_D64,
-                                 LONGLOOP_EXTREME_D64, LONGLOOP_D128, PROFILE)}
+                                 LONGLOOP_EXTREME_D64, LONGLOOP_D128, PROFILE, PROFILE_D128)}
 
 
 def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
