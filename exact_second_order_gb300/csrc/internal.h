@@ -63,7 +63,7 @@ cudaError_t simt_jvp(const JvpArgs& a);
 size_t simt_pass1_smem(int d);
 size_t simt_pass2_smem(int d);
 
-// tcgen05 tensor-core kernels (bf16 inputs, d = 64; the BoB also d = 128).
+// tcgen05 tensor-core kernels (bf16 inputs, d = 64 and d = 128).
 constexpr int kTcRows = 128;    // rows of the resident block (MMA M) in both passes
 constexpr int kTcStream = 32;   // rows of a streamed key tile in pass 1 (and of a d = 128 pass-2 query tile)
 constexpr int kTcStream2 = 64;  // rows of a streamed query tile in pass 2

@@ -55,6 +55,12 @@ constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
 constexpr uint32_t TILE_BYTES = BN * DH * 2;   // 4 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Epilogue staging: one 128 x 64 fp32 tile per output, rows padded to 68
+// floats (a warp's float4 accesses to 32 consecutive rows then take the
+// minimum four shared-memory wavefronts), in the ring, idle by then.
+constexpr int kStageLd = DH + 4;
+constexpr uint32_t kStageBytes = BM * kStageLd * 4;
+
 struct Smem1 {
   alignas(1024) uint8_t q[BLOCK_BYTES];
   alignas(1024) uint8_t dO[BLOCK_BYTES];
@@ -72,6 +78,7 @@ struct Smem1 {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(2 * kStageBytes <= sizeof(Smem1::kv), "epilogue staging fits in the ring");
 
 // Score buffer layout (columns): F' at 0, S at 32, dP at 64, G at 96.
 constexpr uint32_t kColF = 0, kColS = 32, kColdP = 64, kColG = 96;
@@ -446,6 +453,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
+    // Every MMA is done, so the ring is idle: the block's rows of O come in
+    // through shared memory with coalesced loads (256 threads, 16 float4 per
+    // row), each thread forms its row's outputs there, and the tiles leave
+    // with coalesced stores.  d~dO (O') overwrites O in place.
+    float* st_o = reinterpret_cast<float*>(&sm.kv[0][0][0]);  // O, then d~dO
+    float* st_q = st_o + BM * kStageLd;                         // d~Q
+    const int tid = threadIdx.x - 64;                           // 0 .. 255
+    const int rows = min(BM, Nq - row0);
+    const size_t blk = (static_cast<size_t>(bh) * Nq + row0) * DH;
+    for (int f = tid; f < rows * (DH / 4); f += 256) {
+      const int rr = f / (DH / 4), c4 = f % (DH / 4);
+      *reinterpret_cast<float4*>(st_o + rr * kStageLd + 4 * c4) =
+          reinterpret_cast<const float4*>(O + blk)[f];
+    }
+    named_bar_sync(1, 256);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = 32 * wg + 16 * h;
@@ -457,37 +479,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tmem_ld16(acc_base + kAccdO + col, vo);
       tmem_wait_ld();
-      if (JVP && ok && gr < Nq) {  // O' = (P U_V + (P o F) V) - L' O
-        const size_t off = rowvec * DH + col;
-        const float4* o4 = reinterpret_cast<const float4*>(O + off);
-        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
+      if (gr < Nq) {
+        float4* o4 = reinterpret_cast<float4*>(st_o + r * kStageLd + col);
+        float4* q4 = reinterpret_cast<float4*>(st_q + r * kStageLd + col);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 ov = o4[k];
-          d4[k] = make_float4(u2f(vo[4 * k + 0]) - al * ov.x, u2f(vo[4 * k + 1]) - al * ov.y,
+          const float4 ov = o4[k];  // d~dO = d~dO0 - alpha O  (O' = O'0 - L' O)
+          o4[k] = make_float4(u2f(vo[4 * k + 0]) - al * ov.x, u2f(vo[4 * k + 1]) - al * ov.y,
                               u2f(vo[4 * k + 2]) - al * ov.z, u2f(vo[4 * k + 3]) - al * ov.w);
+          if (!JVP) {  // d~Q = tau (Omega - alpha R' - E0 B)
+            float4 qv;
+            qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - E0 * u2f(vb[4 * k + 0]));
+            qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - E0 * u2f(vb[4 * k + 1]));
+            qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - E0 * u2f(vb[4 * k + 2]));
+            qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - E0 * u2f(vb[4 * k + 3]));
+            q4[k] = qv;
+          }
         }
       }
-      if (!JVP && ok && gr < Nq) {
-        const size_t off = rowvec * DH + col;
-        const float4* o4 = reinterpret_cast<const float4*>(O + off);
-        float4* q4 = reinterpret_cast<float4*>(dQt + off);
-        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 ov = o4[k];
-          float4 qv, dv;
-          qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - E0 * u2f(vb[4 * k + 0]));
-          qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - E0 * u2f(vb[4 * k + 1]));
-          qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - E0 * u2f(vb[4 * k + 2]));
-          qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - E0 * u2f(vb[4 * k + 3]));
-          dv.x = u2f(vo[4 * k + 0]) - al * ov.x;
-          dv.y = u2f(vo[4 * k + 1]) - al * ov.y;
-          dv.z = u2f(vo[4 * k + 2]) - al * ov.z;
-          dv.w = u2f(vo[4 * k + 3]) - al * ov.w;
-          q4[k] = qv;
-          d4[k] = dv;
-        }
+    }
+    named_bar_sync(1, 256);
+    if (ok) {
+      for (int f = tid; f < rows * (DH / 4); f += 256) {
+        const int rr = f / (DH / 4), c4 = f % (DH / 4);
+        reinterpret_cast<float4*>(ddOt + blk)[f] =
+            *reinterpret_cast<const float4*>(st_o + rr * kStageLd + 4 * c4);
+        if (!JVP)
+          reinterpret_cast<float4*>(dQt + blk)[f] =
+              *reinterpret_cast<const float4*>(st_q + rr * kStageLd + 4 * c4);
       }
     }
     if (ok && wg == 0 && gr < Nq) {

@@ -54,6 +54,10 @@ constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB: 128 rows x 64 columns
 constexpr uint32_t HALF_TILE = BN * 64 * 2;   // 4 KiB: 32 rows x 64 columns
 constexpr uint32_t STAGE_BYTES = 2 * 4 * HALF_TILE;
 constexpr float kLog2e = 1.4426950408889634f;
+// Epilogue staging: the block's 128 x 128 fp32 output tile, rows padded to
+// 132 floats (a warp's float4 accesses to 32 consecutive rows then take the
+// minimum four shared-memory wavefronts), in the ring, idle by then.
+constexpr int kStageLd = DH + 4;
 
 struct SmemW1 {
   alignas(1024) uint8_t q[2][HALF_BLOCK];    // Q, columns 0..63 and 64..127
@@ -72,6 +76,7 @@ struct SmemW1 {
   int abort_flag;
 };
 static_assert(sizeof(SmemW1) + 1024 <= 232448, "shared memory");
+static_assert(BM * kStageLd * 4 <= sizeof(SmemW1::kv), "epilogue staging fits in the ring");
 
 constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;
 constexpr uint32_t kAccQ = 0;                       // rows: d~Q
@@ -422,11 +427,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (wg == 1) al = sm.part[r].x;
     }
 
-    // Epilogue: warpgroup wg writes output columns [64 wg, 64 wg + 64).
+    // Epilogue: warpgroup wg forms output columns [64 wg, 64 wg + 64) of its
+    // row.  Every MMA is done, so the ring is idle: the block's rows of O
+    // (the JVP) come in through shared memory with coalesced loads, each
+    // thread forms its row's outputs there (O' over O), and the tile leaves
+    // with coalesced stores (256 threads, 32 float4 per row).
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
+    float* st = reinterpret_cast<float*>(&sm.kv[0][0][0][0]);
+    const int tid = threadIdx.x - 64;  // 0 .. 255
+    const int rows = min(BM, Nq - row0);
+    const size_t blk = (static_cast<size_t>(bh) * Nq + row0) * DH;
+    if (JVP) {
+      for (int f = tid; f < rows * (DH / 4); f += 256) {
+        const int rr = f / (DH / 4), c4 = f % (DH / 4);
+        *reinterpret_cast<float4*>(st + rr * kStageLd + 4 * c4) =
+            reinterpret_cast<const float4*>(O + blk)[f];
+      }
+      named_bar_sync(1, 256);
+    }
     float edot = 0.f;  // dO . d~dO over this warpgroup's columns
 #pragma unroll 1
     for (int h = 0; h < 4; ++h) {
@@ -434,10 +455,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t v[16];
       tmem_ld16(acc_base + (JVP ? kAccdO : kAccQ) + col, v);
       tmem_wait_ld();
-      if (JVP && ok && gr < Nq) {  // O' = O'0 - L' O
-        const size_t off = rowvec * DH + col;
-        const float4* o4 = reinterpret_cast<const float4*>(O + off);
-        float4* d4 = reinterpret_cast<float4*>(ddOt + off);
+      if (gr >= Nq) continue;
+      float4* s4 = reinterpret_cast<float4*>(st + r * kStageLd + col);
+      if (JVP) {  // O' = O'0 - L' O
         float dov[16];
         if (withE) {
           // dO columns col .. col + 15: 16-byte chunks 2h, 2h + 1 of half wg
@@ -453,22 +473,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 ov = o4[k];
+          const float4 ov = s4[k];
           const float4 dv = make_float4(u2f(v[4 * k]) - al * ov.x, u2f(v[4 * k + 1]) - al * ov.y,
                                         u2f(v[4 * k + 2]) - al * ov.z,
                                         u2f(v[4 * k + 3]) - al * ov.w);
-          d4[k] = dv;
+          s4[k] = dv;
           if (withE)
             edot += dov[4 * k] * dv.x + dov[4 * k + 1] * dv.y + dov[4 * k + 2] * dv.z +
                     dov[4 * k + 3] * dv.w;
         }
-      }
-      if (!JVP && ok && gr < Nq) {
-        float4* q4 = reinterpret_cast<float4*>(dQt + rowvec * DH + col);
+      } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          q4[k] = make_float4(tau * u2f(v[4 * k]), tau * u2f(v[4 * k + 1]),
+          s4[k] = make_float4(tau * u2f(v[4 * k]), tau * u2f(v[4 * k + 1]),
                               tau * u2f(v[4 * k + 2]), tau * u2f(v[4 * k + 3]));
+      }
+    }
+    named_bar_sync(1, 256);
+    if (ok) {
+      float* outp = JVP ? ddOt : dQt;
+      for (int f = tid; f < rows * (DH / 4); f += 256) {
+        const int rr = f / (DH / 4), c4 = f % (DH / 4);
+        reinterpret_cast<float4*>(outp + blk)[f] =
+            *reinterpret_cast<const float4*>(st + rr * kStageLd + 4 * c4);
       }
     }
     if (withE) {

@@ -101,6 +101,7 @@ constexpr float kFar = 1e30f;
 // buffer, padded against bank conflicts.
 constexpr int kStageStride = 2 * DH + 4;
 static_assert(BM * kStageStride * 4 <= NST * 3 * TILE_BYTES, "staging fits in the ring");
+static_assert(8 * 2 * 32 * 36 * 4 <= NST * 3 * TILE_BYTES, "per-warp staging fits in the ring");
 
 __device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
   return kOp + 32 * x + 8 * kk;
@@ -189,8 +190,61 @@ __device__ __forceinline__ bool p2_half(uint32_t sc, uint32_t opb, int wg, int i
   return true;
 }
 
+// Alone (no cluster split), each warp transposes its own 32 rows x 32
+// columns of d~K and d~V through a private slice of the idle ring (rows
+// padded to 36 floats) and writes them as whole 128-byte row segments, with
+// no barrier across warps.  Out of line: the CTA runs it once, and keeping
+// it out of the kernel body leaves the tile loop's code as it is.
+static __device__ __noinline__ void store_rows_alone(uint32_t acc_base, uint8_t* ring, int warp,
+                                                     int lane, int quad, int wg, int T,
+                                                     float tau, bool ok, int j0, int bkv,
+                                                     int Nk, float* __restrict__ dKt,
+                                                     float* __restrict__ dVt) {
+  constexpr int kLd = 36;
+  float* wk = reinterpret_cast<float*>(ring) + (warp - 2) * (2 * 32 * kLd);
+  float* wv = wk + 32 * kLd;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t vk[16], vv[16];
+    tmem_ld16(acc_base + kAccK + 32 * wg + 16 * h, vk);
+    tmem_ld16(acc_base + kAccV + 32 * wg + 16 * h, vv);
+    tmem_wait_ld();
+    if (T == 0) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      reinterpret_cast<float4*>(wk + lane * kLd + 16 * h)[k] =
+          make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]), tau * u2f(vk[4 * k + 2]),
+                      tau * u2f(vk[4 * k + 3]));
+      reinterpret_cast<float4*>(wv + lane * kLd + 16 * h)[k] =
+          make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
+                      u2f(vv[4 * k + 3]));
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int f = lane + 32 * k, rr = f >> 3, c4 = f & 7;  // 8 float4 per row
+    const int gjr = j0 + quad * 32 + rr;
+    if (ok && gjr < Nk) {
+      const size_t o = (static_cast<size_t>(bkv) * Nk + gjr) * DH + 32 * wg + 4 * c4;
+      *reinterpret_cast<float4*>(dKt + o) = *reinterpret_cast<const float4*>(wk + rr * kLd + 4 * c4);
+      *reinterpret_cast<float4*>(dVt + o) = *reinterpret_cast<const float4*>(wv + rr * kLd + 4 * c4);
+    }
+  }
+}
+
 // SPLIT: launched as clusters of S > 1 CTAs that share a key block.
-template <bool SPLIT>
+// STAGED (without SPLIT): the rows leave through shared memory
+// (store_rows_alone) instead of straight from each thread's registers.  The
+// staged epilogue is ~4 us shorter per CTA, but its instance ran the tile
+// loop 3% slower at 1,024 tiles per CTA (measured: the same source with the
+// other epilogue, swapped alone), so it serves CTAs of at most kStagedTiles
+// tiles, where the epilogue is a large share of the CTA.
+constexpr int kStagedTiles = 128;
+template <bool SPLIT, bool STAGED = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass2_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mUK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mUV,
@@ -479,10 +533,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
+    // A thread holds one key row, so writing global memory straight from
+    // registers would scatter each warp's float4 over 32 rows: the rows go
+    // through shared memory (every MMA is done and the ring is idle).  A CTA
+    // with no tile (T = 0) never wrote its accumulators and stages zeros.
     if (SPLIT) {
-      // Stage this CTA's partial d~K | d~V rows (every MMA is done and the
-      // ring is idle) for the cluster-wide sum below; a CTA with no tile
-      // (T = 0) never wrote its accumulators and stages zeros.
+      // Stage the CTA's partial d~K | d~V rows for the cluster-wide sum below.
       float* row = reinterpret_cast<float*>(&sm.st[0][0][0]) + r * kStageStride;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -505,30 +561,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                           u2f(vv[4 * k + 3]));
         }
       }
-    }
+    } else if (STAGED) {
+      store_rows_alone(acc_base, &sm.st[0][0][0], warp, lane, quad, wg, T, tau, ok, j0, bkv, Nk,
+                       dKt, dVt);
+    } else {
 #pragma unroll
-    for (int h = 0; h < 2 && !SPLIT; ++h) {
-      const int col = 32 * wg + 16 * h;
-      uint32_t vk[16], vv[16];
-      tmem_ld16(acc_base + kAccK + col, vk);
-      tmem_ld16(acc_base + kAccV + col, vv);
-      tmem_wait_ld();
-      if (ok && gj < Nk) {
-        const size_t off = (static_cast<size_t>(bkv) * Nk + gj) * DH + col;
-        float4* k4 = reinterpret_cast<float4*>(dKt + off);
-        float4* v4 = reinterpret_cast<float4*>(dVt + off);
-        // T = 0: no query sees this key block, the accumulators were never
-        // written, and the outputs are exact zeros.
-        if (T == 0) {
+      for (int h = 0; h < 2; ++h) {
+        const int col = 32 * wg + 16 * h;
+        uint32_t vk[16], vv[16];
+        tmem_ld16(acc_base + kAccK + col, vk);
+        tmem_ld16(acc_base + kAccV + col, vv);
+        tmem_wait_ld();
+        if (ok && gj < Nk) {
+          const size_t off = (static_cast<size_t>(bkv) * Nk + gj) * DH + col;
+          float4* k4 = reinterpret_cast<float4*>(dKt + off);
+          float4* v4 = reinterpret_cast<float4*>(dVt + off);
+          if (T == 0) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
-        }
+            for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+          }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          k4[k] = make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]),
-                              tau * u2f(vk[4 * k + 2]), tau * u2f(vk[4 * k + 3]));
-          v4[k] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
-                              u2f(vv[4 * k + 3]));
+          for (int k = 0; k < 4; ++k) {
+            k4[k] = make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]),
+                                tau * u2f(vk[4 * k + 2]), tau * u2f(vk[4 * k + 3]));
+            v4[k] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
+                                u2f(vv[4 * k + 3]));
+          }
         }
       }
     }
@@ -589,6 +647,8 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   // maps128: K, U_K, V, U_V with 128-row boxes; maps64: Q, U_Q, dO with 64-row boxes.
   const size_t smem = tc_pass2_smem();
   cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass2_kernel<false>), (int)smem);
+  if (e == cudaSuccess)
+    e = tc_set_smem(reinterpret_cast<const void*>(tc_pass2_kernel<false, true>), (int)smem);
   if (e != cudaSuccess) return e;
   // One CTA per key block of a shared head, or, when the key blocks cannot
   // fill the SMs, a cluster of S of them that splits the block's query tiles
@@ -603,7 +663,10 @@ cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nk + BM - 1) / BM, a.Hkv * S, a.B);
   if (S == 1) {
-    tc_pass2_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
+    // Tiles a CTA streams: every query tile of its group (fewer under the causal mask).
+    const bool staged = tiles <= kStagedTiles;
+    auto kernel = staged ? tc_pass2_kernel<false, true> : tc_pass2_kernel<false>;
+    kernel<<<grid, NTHREADS, smem, a.stream>>>(
         maps128[0], maps128[1], maps128[2], maps128[3], maps64[0], maps64[1], maps64[2], a.L,
         a.D, a.alpha, a.E, a.dKt, a.dVt, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, 1,
         a.err);

@@ -436,56 +436,51 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
-    if (SPLIT) {
-      // Stage this CTA's partial rows (every MMA is done; the resident
-      // block is no longer read) for the cluster-wide sum below; a CTA with
-      // no tile (T = 0) never wrote its accumulators and stages zeros.
-      float4* row = reinterpret_cast<float4*>(&sm.kb[0][0][0]) + r * (2 * DH / 4);
+    // Stage this CTA's d~K | d~V rows in the resident block (every MMA is
+    // done; it is no longer read), float4 c of row r at c ^ (r mod 8): a
+    // thread holds one key row, so writing global memory straight from
+    // registers would scatter each warp's float4 over 32 rows.  A CTA with no
+    // tile (T = 0) never wrote its accumulators and stages zeros.  With a
+    // cluster split the rows are summed over the cluster below; alone, the
+    // CTA writes them out here, coalesced.
+    constexpr int kRow4 = 2 * DH / 4;  // float4 per staged row
+    float4* stage = reinterpret_cast<float4*>(&sm.kb[0][0][0]);
+    float4* row = stage + r * kRow4;
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        const int col = 64 * wg + 16 * h;
-        uint32_t vk[16], vv[16];
-        tmem_ld16(acc_base + kAccK + col, vk);
-        tmem_ld16(acc_base + kAccV + col, vv);
-        tmem_wait_ld();
-        if (T == 0) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int ck = col / 4 + k, cv = DH / 4 + col / 4 + k;
-          row[ck ^ (r & 7)] = make_float4(u2f(vk[4 * k]), u2f(vk[4 * k + 1]),
-                                          u2f(vk[4 * k + 2]), u2f(vk[4 * k + 3]));
-          row[cv ^ (r & 7)] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]),
-                                          u2f(vv[4 * k + 2]), u2f(vv[4 * k + 3]));
-        }
-      }
-    }
-#pragma unroll 1
-    for (int h = 0; h < 4 && !SPLIT; ++h) {
+    for (int h = 0; h < 4; ++h) {
       const int col = 64 * wg + 16 * h;
       uint32_t vk[16], vv[16];
       tmem_ld16(acc_base + kAccK + col, vk);
       tmem_ld16(acc_base + kAccV + col, vv);
       tmem_wait_ld();
-      if (ok && gj < Nk) {
-        const size_t off = (static_cast<size_t>(bkv) * Nk + gj) * DH + col;
-        float4* k4 = reinterpret_cast<float4*>(dKt + off);
-        float4* v4 = reinterpret_cast<float4*>(dVt + off);
-        // T = 0: no query sees this key block, the accumulators were never
-        // written, and the outputs are exact zeros.
-        if (T == 0) {
+      if (T == 0) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
-        }
+        for (int k = 0; k < 16; ++k) vk[k] = vv[k] = 0u;
+      }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          k4[k] = make_float4(tau * u2f(vk[4 * k]), tau * u2f(vk[4 * k + 1]),
-                              tau * u2f(vk[4 * k + 2]), tau * u2f(vk[4 * k + 3]));
-          v4[k] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]), u2f(vv[4 * k + 2]),
-                              u2f(vv[4 * k + 3]));
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int ck = col / 4 + k, cv = DH / 4 + col / 4 + k;
+        row[ck ^ (r & 7)] = make_float4(u2f(vk[4 * k]), u2f(vk[4 * k + 1]),
+                                        u2f(vk[4 * k + 2]), u2f(vk[4 * k + 3]));
+        row[cv ^ (r & 7)] = make_float4(u2f(vv[4 * k]), u2f(vv[4 * k + 1]),
+                                        u2f(vv[4 * k + 2]), u2f(vv[4 * k + 3]));
+      }
+    }
+    if (!SPLIT) {
+      named_bar_sync(1, 256);
+      const int tid = threadIdx.x - 64;
+      for (int e = tid; e < BM * kRow4 && ok; e += 256) {
+        const int rr = e / kRow4, c4 = e % kRow4;
+        const int gjr = j0 + rr;
+        if (gjr >= Nk) break;  // rows ascend with e
+        const float4 v = stage[rr * kRow4 + (c4 ^ (rr & 7))];
+        const bool isK = c4 < DH / 4;
+        const size_t o =
+            (static_cast<size_t>(bkv) * Nk + gjr) * DH + 4 * (isK ? c4 : c4 - DH / 4);
+        if (isK)
+          *reinterpret_cast<float4*>(dKt + o) = make_float4(tau * v.x, tau * v.y, tau * v.z, tau * v.w);
+        else
+          *reinterpret_cast<float4*>(dVt + o) = v;
       }
     }
   }

@@ -45,6 +45,12 @@ struct PrepCfg {
   static_assert(2 * DH + NBUF * kBN <= 512, "TMEM columns");
 };
 
+// Epilogue staging: the block's 128 x DH fp32 O tile, rows padded by 4
+// floats (a warp's float4 accesses to 32 consecutive rows then take the
+// minimum four shared-memory wavefronts), in the ring, idle by then.
+template <int DH>
+constexpr int kStageLd0 = DH + 4;
+
 template <int DH>
 struct Smem0 {
   static constexpr int NST = PrepCfg<DH>::kStages;
@@ -53,7 +59,6 @@ struct Smem0 {
   alignas(1024) uint8_t kv[NST][2][NH][PrepCfg<DH>::kHalfTile];  // [stage][K, V][half]
   float part_m[2][BM];
   float part_l[2][BM];
-  float part_d[2][BM];
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
@@ -328,45 +333,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float lsum = s0 * sm.part_l[0][r] + s1 * sm.part_l[1][r];
     const float inv = 1.f / lsum;
     const bool one = T < 2;  // warpgroup 1 had no tile: its accumulator was never written
-    float dpart = 0.f;
+    // Every MMA is done, so the ring is idle: each thread forms its row of O
+    // in shared memory, then the tile leaves with coalesced stores and D is
+    // the row dot with dO read coalesced (DH / 4 consecutive lanes per row,
+    // summed by shuffles).
+    constexpr int LD = kStageLd0<DH>;
+    static_assert(BM * LD * 4 <= sizeof(Smem0<DH>::kv), "epilogue staging fits in the ring");
+    float* st = reinterpret_cast<float*>(&sm.kv[0][0][0][0]);
 #pragma unroll
-    for (int h = 0; h < DH / 32; ++h) {  // warpgroup wg writes columns [DH/2 wg, DH/2 (wg+1))
+    for (int h = 0; h < DH / 32; ++h) {  // warpgroup wg forms columns [DH/2 wg, DH/2 (wg+1))
       const int col = (DH / 2) * wg + 16 * h;
       uint32_t v0[16], v1[16];
       tmem_ld16(tbase + lane_off + col, v0);
       tmem_ld16(tbase + lane_off + DH + col, v1);
       tmem_wait_ld();
-      float o[16];
+      float4* s4 = reinterpret_cast<float4*>(st + r * LD + col);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        o[k] = (s0 * u2f(v0[k]) + (one ? 0.f : s1 * u2f(v1[k]))) * inv;
-      if (ok && gr < Nq) {
-        const size_t off = rowvec * DH + col;
-        float4* o4 = reinterpret_cast<float4*>(O + off);
-        // dO = D = null: the forward only, no D.
-        const uint4* g4 = dO ? reinterpret_cast<const uint4*>(dO + off) : nullptr;
+      for (int k = 0; k < 4; ++k) {
+        float o[4];
 #pragma unroll
-        for (int k = 0; k < 2 && g4; ++k) {
-          const uint4 raw = g4[k];  // 8 bf16 of dO
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float lo = __uint_as_float(w[q] << 16);
-            const float hi = __uint_as_float(w[q] & 0xFFFF0000u);
-            dpart = fmaf(lo, o[8 * k + 2 * q], dpart);
-            dpart = fmaf(hi, o[8 * k + 2 * q + 1], dpart);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          o4[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        for (int q = 0; q < 4; ++q)
+          o[q] = (s0 * u2f(v0[4 * k + q]) + (one ? 0.f : s1 * u2f(v1[4 * k + q]))) * inv;
+        s4[k] = make_float4(o[0], o[1], o[2], o[3]);
       }
     }
-    sm.part_d[wg][r] = dpart;
     named_bar_sync(1, 256);
-    if (ok && wg == 0 && gr < Nq) {
-      L[rowvec] = (mm + __log2f(lsum)) * kLn2;
-      if (D) D[rowvec] = sm.part_d[0][r] + sm.part_d[1][r];
+    if (ok && wg == 0 && gr < Nq) L[rowvec] = (mm + __log2f(lsum)) * kLn2;
+    const int tid = threadIdx.x - 64;  // 0 .. 255
+    const int rows = min(BM, Nq - row0);
+    const size_t blk = (static_cast<size_t>(bh) * Nq + row0) * DH;
+    constexpr int kRow4 = DH / 4;  // float4 per row: 16 or 32 lanes
+    // Every lane runs every iteration (the shuffles need the whole warp);
+    // rows past N_q only skip their memory accesses.
+    for (int f = tid; f < BM * kRow4; f += 256) {
+      const int rr = f / kRow4, c4 = f % kRow4;
+      const bool live = ok && rr < rows;
+      const float4 v = *reinterpret_cast<const float4*>(st + rr * LD + 4 * c4);
+      float dp = 0.f;
+      if (live) {
+        reinterpret_cast<float4*>(O + blk)[f] = v;
+        if (dO) {  // dO = D = null: the forward only, no D
+          const uint2 raw = reinterpret_cast<const uint2*>(
+              reinterpret_cast<const uint16_t*>(dO) + blk)[f];  // 4 bf16 of dO
+          dp = __uint_as_float(raw.x << 16) * v.x + __uint_as_float(raw.x & 0xFFFF0000u) * v.y +
+               __uint_as_float(raw.y << 16) * v.z + __uint_as_float(raw.y & 0xFFFF0000u) * v.w;
+        }
+      }
+#pragma unroll
+      for (int o = kRow4 / 2; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+      if (live && D && c4 == 0) D[static_cast<size_t>(bh) * Nq + row0 + rr] = dp;
     }
   }
 
