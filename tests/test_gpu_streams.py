@@ -66,3 +66,43 @@ def test_small_calls_stay_on_the_callers_stream():
     assert fb.flashbob_bob_launches(1, 4, 4, 1024, 1024, 64, fb.FLASHBOB_BF16) == 2
     assert fb.flashbob_bob_launches(1, 12, 1, 65536, 65536, 64, fb.FLASHBOB_BF16) == 2
     assert fb.flashbob_bob_launches(1, 4, 4, 65536, 65536, 64, fb.FLASHBOB_F32) == 2
+
+
+@pytest.mark.parametrize("w", [CASES[0], CASES[3]], ids=[CASES[0].name, CASES[3].name])
+def test_head_group_streams_under_cuda_graph_capture(w):
+    # The internal streams join a capture through the fork/join events, so a
+    # captured flashbob_bob replays the same launches: the replay's outputs
+    # equal a direct call's bit for bit, and a replay with changed inputs
+    # (same buffers) tracks them.
+    x = wl.make_inputs(w)
+    d = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(d["Q"], d["K"], d["V"], d["dO"], w.tau, causal=w.causal)
+    ref = fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+                 causal=w.causal)
+    out = fb.alloc_bob_outputs(d["Q"], fill=float("nan"), K=d["K"])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm the library's caches outside the capture
+        fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+               out=out, causal=w.causal, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for t in out.values():
+        t.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+               out=out, causal=w.causal, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    for k in ref:
+        assert torch.equal(out[k], ref[k]), f"{k}: graph replay differs from the direct call"
+    # new tangents in the same buffers: the replay follows them
+    d["UV"].mul_(2)
+    ref2 = fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+                  causal=w.causal)
+    g.replay()
+    torch.cuda.synchronize()
+    for k in ref2:
+        assert torch.equal(out[k], ref2[k]), f"{k}: replay after an input change differs"
