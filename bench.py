@@ -468,6 +468,7 @@ def timed_steps(res, steps, warmup, torch, barrier, uuid):
     torch.cuda.synchronize()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
     return {"total_ms": evs[0][0].elapsed_time(evs[-1][1]),
+            "median_ms": statistics.median(e[0].elapsed_time(e[1]) for e in evs),
             "p1_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in pev),
             "p2_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in pev),
             "passes_ms": statistics.mean(e[0].elapsed_time(e[2]) for e in pev),
@@ -507,7 +508,8 @@ def run_sweep(args, fb, torch, barrier, uuid, peak, peak_note):
         line = {"sweep": True, "metric": METRIC, "value": value, "unit": UNIT,
                 "ms_per_step": ms, "steps": steps, "warmup": 3, "dtype": "bf16",
                 "pct_of_peak": 100.0 * value / peak,
-                "config": dict(config_dict(w), pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
+                "config": dict(config_dict(w), ms_per_call_median=t["median_ms"],
+                               pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                                passes_as_separate_calls_ms=t["passes_ms"],
                                head_group_streams=res.streams_per_step(),
                                prep_ms_outside_step=res.prep_ms(torch),
@@ -687,6 +689,7 @@ def main():
         "config": dict(config_dict(w), flops_per_step_per_gpu=flops,
                        l2=f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
                           f"{L2_BYTES / 2**20:.0f} MiB",
+                       ms_per_call_median=t["median_ms"],
                        pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                        passes_as_separate_calls_ms=t["passes_ms"],
                        head_group_streams=res_streams, prep_ms_outside_step=prep_ms,
