@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 
     // Epilogue: combine the two warpgroups' row sums, then the affine
-    // correction; warpgroup wg writes output columns [32 wg, 32 wg + 32).
+    // correction; warpgroup wg forms output columns [32 wg, 32 wg + 32).
     sm.part_a[wg][r] = a_acc.x + a_acc.y;
     sm.part_e[wg][r] = e_acc.x + e_acc.y;
     named_bar_sync(1, 256);
