@@ -611,7 +611,9 @@ def run_e2e(args, w, x, res, fb, torch, barrier, world):
 
     run(2)
     barrier()
-    n_e2e = max(3, args.steps // 2)
+    # The same K steps as the device-resident leg: the first upload and the
+    # last download (the only copies not overlapped) spread over as many steps.
+    n_e2e = max(3, args.steps)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(comp)
