@@ -106,3 +106,44 @@ def test_head_group_streams_under_cuda_graph_capture(w):
     torch.cuda.synchronize()
     for k in ref2:
         assert torch.equal(out[k], ref2[k]), f"{k}: replay after an input change differs"
+
+
+def test_concurrent_calls_from_two_host_threads():
+    # ctypes releases the interpreter lock, so two host threads enqueue
+    # flashbob_bob calls at once, each on its own stream; the library
+    # serialises the use of its internal streams and events, and every result
+    # equals the one-thread result bit for bit.
+    import threading
+    w = CASES[0]
+    x = wl.make_inputs(w)
+    d = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(d["Q"], d["K"], d["V"], d["dO"], w.tau, causal=w.causal)
+    ref = fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+                 causal=w.causal)
+    torch.cuda.synchronize()
+    outs = [[fb.alloc_bob_outputs(d["Q"], fill=float("nan"), K=d["K"]) for _ in range(3)]
+            for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            for out in outs[i]:
+                fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"],
+                       w.tau, out=out, causal=w.causal, stream=streams[i])
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    for per_thread in outs:
+        for out in per_thread:
+            for k in ref:
+                assert torch.equal(out[k], ref[k]), k
