@@ -253,6 +253,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
+    // The resident block's copy starts now, while warp 1 allocates TMEM.
+    mbar_expect_tx(&sm.bar_q, (JVP ? 2 : 3) * BLOCK_BYTES);
+    tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
+    if (!JVP) tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
+    tma_load_3d(sm.uq, &mUQ, &sm.bar_q, 0, row0, bh);
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
   tc_fence_before();
@@ -268,10 +273,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mUK);
       tma_prefetch_desc(&mUV);
-      mbar_expect_tx(&sm.bar_q, (JVP ? 2 : 3) * BLOCK_BYTES);
-      tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
-      if (!JVP) tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
-      tma_load_3d(sm.uq, &mUQ, &sm.bar_q, 0, row0, bh);
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % NST;
