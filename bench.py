@@ -360,7 +360,9 @@ def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
 # The throughput-vs-length table (--sweep): the benchmark configurations at
 # head dim 64 (N = 1K ... 256K) and 128, then the pages' causal timing shapes
 # (B = 4, H = 12, bf16; [FBN] 实验关键数据).
-SWEEP = ("gpt2_layer_B4_H12_N1024_d64", "mid_B1_H12_N8192_d64", "mid_peaked_B1_H12_N8192_d64",
+SWEEP = ("gpt2_layer_B4_H12_N1024_d64", "curve_B4_H12_N2048_d64", "curve_B2_H12_N4096_d64",
+         "mid_B1_H12_N8192_d64", "curve_B1_H8_N16384_d64", "curve_B1_H4_N32768_d64",
+         "mid_peaked_B1_H12_N8192_d64",
          "long_B1_H4_N65536_d64", "extreme_B1_H1_N262144_d64", "extreme_B1_H1_N131072_d128",
          "causal_B4_H12_N4096_d64", "causal_B4_H12_N8192_d64", "causal_B4_H12_N16384_d64",
          "causal_B4_H12_N16384_d128", "causal_B4_H12_N32768_d128",

@@ -120,6 +120,11 @@ LONGLOOP_EXTREME_D64 = Workload("longloop_B1_H1_Nq262144_Nk512_d64", 1, 1, 26214
                                 Nk=512)
 LONGLOOP_D128 = Workload("longloop_B1_H1_Nq131072_Nk256_d128", 1, 1, 131072, 128, "bf16",
                          Nk=256)
+# The rest of the throughput-vs-length curve (d = 64, non-causal): N = 2048 .. 32768.
+CURVE_N2048 = Workload("curve_B4_H12_N2048_d64", 4, 12, 2048, 64, "bf16")
+CURVE_N4096 = Workload("curve_B2_H12_N4096_d64", 2, 12, 4096, 64, "bf16")
+CURVE_N16384 = Workload("curve_B1_H8_N16384_d64", 1, 8, 16384, 64, "bf16")
+CURVE_N32768 = Workload("curve_B1_H4_N32768_d64", 1, 4, 32768, 64, "bf16")
 # A mid-size case for detailed profiles: inputs (~0.3 GB) larger than L2.
 PROFILE = Workload("profile_B1_H8_N32768_d64", 1, 8, 32768, 64, "bf16")
 # d = 128 kernels under ncu: one head (no head-group streams), inputs 176 MiB > L2.
@@ -131,7 +136,8 @@ WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PE
                                  CAUSAL_N32768_D128, CAUSAL_N65536_D128, GQA_N8192,
                                  MQA_N8192,
                                  RECT_Q4096_K16384, RECT_Q16384_K4096, LONGLOOP_D64,
-                                 LONGLOOP_EXTREME_D64, LONGLOOP_D128, PROFILE, PROFILE_D128)}
+                                 LONGLOOP_EXTREME_D64, LONGLOOP_D128, PROFILE, PROFILE_D128,
+                                 CURVE_N2048, CURVE_N4096, CURVE_N16384, CURVE_N32768)}
 
 
 def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
