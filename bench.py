@@ -548,10 +548,12 @@ def run_e2e(args, w, x, res, fb, torch, barrier, world):
     """The benchmark step through the public C ABI (flashbob_bob) with the
     data on the host: each step uploads its inputs and row state from pinned
     host memory and downloads all six outputs.  Buffer set k % 2 serves step
-    k; uploads and downloads run on a copy stream, ordered against the
-    kernels by events, so they overlap the neighbouring steps' kernels."""
+    k; uploads and downloads run on two copy streams (one per direction),
+    ordered against the kernels by events, so they overlap the neighbouring
+    steps' kernels and each other."""
     comp = res.stream
-    copy = torch.cuda.Stream()
+    copy = torch.cuda.Stream()       # host -> device
+    copy_out = torch.cuda.Stream()   # device -> host, so the two directions overlap
     host_in = {k: v.pin_memory() for k, v in x.items()}
     host_state = {"O": res.O.cpu().pin_memory(), "L": res.L.cpu().pin_memory(),
                   "D": res.D.cpu().pin_memory()}
@@ -572,7 +574,7 @@ def run_e2e(args, w, x, res, fb, torch, barrier, world):
     computed = [torch.cuda.Event() for _ in range(2)]    # set b's outputs are written
     downloaded = [torch.cuda.Event() for _ in range(2)]  # set b's outputs are on the host
     for b in range(2):
-        downloaded[b].record(copy)
+        downloaded[b].record(copy_out)
 
     def upload(b):
         dev, state, _ = sets[b]
@@ -596,11 +598,11 @@ def run_e2e(args, w, x, res, fb, torch, barrier, world):
 
     def download(b):
         _, _, out = sets[b]
-        with torch.cuda.stream(copy):
-            copy.wait_event(computed[b])
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(computed[b])
             for k in host_out[b]:
                 host_out[b][k].copy_(out[k], non_blocking=True)
-            downloaded[b].record(copy)
+            downloaded[b].record(copy_out)
 
     def run(n):
         upload(0)
@@ -620,15 +622,17 @@ def run_e2e(args, w, x, res, fb, torch, barrier, world):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(comp)
     copy.wait_event(t0)
+    copy_out.wait_event(t0)
     run(n_e2e)
     comp.wait_stream(copy)
+    comp.wait_stream(copy_out)
     t1.record(comp)
     barrier()
     e_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
     return {"value": job_tflops(w.flops, n_e2e, world, e_ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": e_ms / n_e2e, "steps": n_e2e,
-            "overlap": "uploads and downloads on a copy stream, two buffer sets"}
+            "overlap": "uploads and downloads on two copy streams, two buffer sets"}
 
 
 def main():
