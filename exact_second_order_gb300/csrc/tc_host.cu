@@ -224,8 +224,8 @@ namespace {
 
 // Head-group streams.  Pass 2 of a key/value head needs pass 1 of that
 // head's query rows only, so the two passes of disjoint head groups are
-// independent.  A call with several groups and more than a wave of CTAs per
-// pass runs the groups' pass 1 -> pass 2 chains on kSplitStreams internal
+// independent.  A call with several groups and more than two waves of pass-1
+// CTAs runs the groups' pass 1 -> pass 2 chains on up to kSplitStreams internal
 // streams (forked from and joined back into the caller's stream): the SMs
 // that one group's last pass-1 wave leaves idle take other groups' CTAs
 // instead of waiting for the whole pass to drain.
