@@ -1,6 +1,7 @@
 // C ABI of libflashbob: argument checks, dispatch and the device error word.
 // The declarations and their contracts are in include/flashbob.h.
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -34,7 +35,9 @@ flashbob_status check_sizes(int B, int H, int Hkv, int Nq, int Nk, int d, float 
     return FLASHBOB_ERR_INVALID_ARG;
   if (H % Hkv != 0) return FLASHBOB_ERR_INVALID_ARG;
   if (!(isfinite(tau) && tau > 0.f)) return FLASHBOB_ERR_INVALID_ARG;
-  if (d > 128 || B > 65535 || H > 65535) return FLASHBOB_ERR_UNSUPPORTED;
+  if (d > 128 || B > kMaxGridY || H > kMaxGridY) return FLASHBOB_ERR_UNSUPPORTED;
+  // Kernels index a (batch, head) pair with a 32-bit integer.
+  if (static_cast<long long>(B) * H > INT_MAX) return FLASHBOB_ERR_UNSUPPORTED;
   return FLASHBOB_OK;
 }
 

@@ -52,6 +52,10 @@ struct JvpArgs {
   unsigned int* err;
 };
 
+// Largest grid y and z extents: the kernels launch heads along y and
+// batches along z.
+constexpr int kMaxGridY = 65535;
+
 constexpr int kPass1 = 1;
 constexpr int kPass2 = 2;
 
@@ -73,8 +77,9 @@ cudaError_t tc_prep(const PrepArgs& a);
 cudaError_t tc_bob(const BobArgs& a);
 // Streams tc_bob runs a call on: 1 (the caller's), or up to 4 internal
 // streams, one per slice of the key/value heads, when both passes are asked
-// for, there are several head groups and a pass has more than two waves of
-// CTAs (the groups' pass 1 -> pass 2 chains then overlap each other's tails).
+// for, there are several head groups, a pass has more than two waves of
+// CTAs (the groups' pass 1 -> pass 2 chains then overlap each other's tails)
+// and every slice's query heads fit the grid's y extent.
 int tc_bob_streams(const BobArgs& a);
 bool tc_jvp_supported(const JvpArgs& a);
 cudaError_t tc_jvp(const JvpArgs& a);

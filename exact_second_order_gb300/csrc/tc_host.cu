@@ -320,17 +320,21 @@ cudaError_t tc_bob_one(const BobArgs& a) { return a.d == 128 ? tc_bob_d128(a) : 
 }  // namespace
 
 int tc_bob_streams(const BobArgs& a) {
-  const int groups = a.B * a.Hkv;
+  const long long groups = static_cast<long long>(a.B) * a.Hkv;
   int dev = 0, sms = 0;
   if (a.passes != (kPass1 | kPass2) || groups < 2 || cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       static_cast<long long>(a.B) * a.H * ((a.Nq + kTcRows - 1) / kTcRows) <= 2LL * sms)
     return 1;
-  return groups < kSplitStreams ? groups : kSplitStreams;
+  const int ns = groups < kSplitStreams ? static_cast<int>(groups) : kSplitStreams;
+  // A slice launches its (at most ceil(groups / ns)) * G query heads along
+  // the grid's y extent: a call whose slices would not fit stays whole.
+  if ((groups + ns - 1) / ns * (a.H / a.Hkv) > kMaxGridY) return 1;
+  return ns;
 }
 
 cudaError_t tc_bob(const BobArgs& a) {
-  const int groups = a.B * a.Hkv;
+  const long long groups = static_cast<long long>(a.B) * a.Hkv;
   const int ns = tc_bob_streams(a);
   if (ns == 1) return tc_bob_one(a);
   std::lock_guard<std::mutex> lock(g_split_mu);
@@ -344,7 +348,8 @@ cudaError_t tc_bob(const BobArgs& a) {
   if (e != cudaSuccess) return e;
   cudaError_t first = cudaSuccess;
   for (int k = 0; k < ns; ++k) {
-    BobArgs s = head_slice(a, groups * k / ns, groups * (k + 1) / ns);
+    BobArgs s = head_slice(a, static_cast<int>(groups * k / ns),
+                           static_cast<int>(groups * (k + 1) / ns));
     s.stream = ss->stream[k];
     const cudaError_t ek = tc_bob_one(s);
     if (first == cudaSuccess) first = ek;

@@ -6,7 +6,9 @@ CPU oracle take their inputs from here without sharing any computation.
 
 Recipe (the pages benchmark an isolated attention layer on synthetic tensors):
 
-* one CPU ``torch.Generator`` seeded with ``seed``;
+* one CPU ``torch.Generator`` seeded with ``seed`` (a CUDA one, same recipe,
+  for the edge-case shapes with hundreds of thousands of heads, whose CPU
+  draw would take minutes);
 * draws in the fixed order Q, K, V, dO, U_Q, U_K, U_V, each of shape
   ``[B, H, N, d]`` (contiguous, row-major); rectangular workloads draw the
   key-side tensors K, V, U_K, U_V with ``Nk`` rows (the same draw order);
@@ -140,21 +142,26 @@ WORKLOADS = {w.name: w for w in (TINY_F32, GPT2_LAYER, MID_LENGTH, MID_LENGTH_PE
                                  CURVE_N2048, CURVE_N4096, CURVE_N16384, CURVE_N32768)}
 
 
-def make_inputs(w: Workload) -> dict[str, torch.Tensor]:
-    """Draw the seven input tensors of ``w`` on the CPU.
+def make_inputs(w: Workload, device: str = "cpu") -> dict[str, torch.Tensor]:
+    """Draw the seven input tensors of ``w`` (on the CPU by default).
 
     Returns fp32 tensors for ``dtype="f32"`` and bf16 tensors for
     ``dtype="bf16"``, all contiguous: ``[B, H, N, d]`` for Q, dO, U_Q and
-    ``[B, Hkv, Nk, d]`` for K, V, U_K, U_V.
+    ``[B, Hkv, Nk, d]`` for K, V, U_K, U_V.  ``device="cuda"`` draws the same
+    recipe with a CUDA generator (other values than the CPU draw, same
+    distribution), for shapes whose CPU draw would take minutes; the oracle
+    then reads the drawn values back.
     """
-    g = torch.Generator(device="cpu")
+    if device != "cpu" and w.peaked_k_rows:
+        raise ValueError("peaked key rows are drawn on the CPU only")
+    g = torch.Generator(device=device)
     g.manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
     kv_shape = (w.B, w.kv_heads, w.kv_len, w.d)  # K, V, U_K, U_V (grouped-query, rectangular)
     out = {}
     for name in NAMES:
         out[name] = torch.randn(kv_shape if name in KV_NAMES else shape, generator=g,
-                                dtype=torch.float32)
+                                dtype=torch.float32, device=device)
     if w.dist == "scaled":
         s = w.d ** -0.25
         for name in ("Q", "K", "V"):

@@ -80,8 +80,8 @@ typedef enum { FLASHBOB_F32 = 0, FLASHBOB_BF16 = 1 } flashbob_dtype;
  *   tau: score scale, finite and > 0 (1/sqrt(d) in the pages).
  *   causal: 0 = full attention; 1 = query i sees keys j <= i only (the
  *        setting of [FBN] 实验关键数据); other values are rejected.
- *   Limits: 1 <= d <= 128; 1 <= Nq, Nk; B, H <= 65535; 1 <= Hkv,
- *        H % Hkv == 0.
+ *   Limits: 1 <= d <= 128; 1 <= Nq, Nk; B, H <= 65535 and B * H < 2^31
+ *        (FLASHBOB_ERR_UNSUPPORTED beyond); 1 <= Hkv, H % Hkv == 0.
  *   One launch: bf16 inputs with d = 64 or d = 128 run a tcgen05 kernel,
  *   every other case fp32 CUDA cores.
  */
@@ -109,7 +109,8 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
  *   `stream` and before everything queued on it afterwards.  On the
  *   tensor-core path, with B * Hkv >= 2 key/value heads and more than two
  *   waves of pass-1 CTAs, the heads are cut into up to four contiguous
- *   groups whose pass 1 -> pass 2 chains run on internal streams of the
+ *   groups (when each group has at most 65535 query heads, the grid's
+ *   extent) whose pass 1 -> pass 2 chains run on internal streams of the
  *   library, forked from and joined back into `stream` by events (pass 2 of
  *   a head reads only pass 1's alpha and E of that head's query rows); the
  *   results are those of the one-stream order, bit for bit.  Those streams

@@ -91,6 +91,8 @@ def test_bob_rejects_bad_arguments_on_the_host(lib):
         assert _bob_raw(lib, ok, **kw) == E.FLASHBOB_ERR_INVALID_ARG, kw
     assert _bob_raw(lib, ok, d=129) == E.FLASHBOB_ERR_UNSUPPORTED
     assert _bob_raw(lib, ok, H=70000) == E.FLASHBOB_ERR_UNSUPPORTED
+    # B * H must fit the kernels' 32-bit (batch, head) index
+    assert _bob_raw(lib, ok, B=32769, H=65535) == E.FLASHBOB_ERR_UNSUPPORTED
     # misaligned pointer
     for i in range(16):
         p = list(ok)
@@ -138,6 +140,7 @@ def test_prep_rejects_bad_arguments_on_the_host(lib):
     assert call(Nk=0) == fb.FLASHBOB_ERR_INVALID_ARG
     assert call(tau=float("nan")) == fb.FLASHBOB_ERR_INVALID_ARG
     assert call(d=200) == fb.FLASHBOB_ERR_UNSUPPORTED
+    assert call(B=32769, H=65535) == fb.FLASHBOB_ERR_UNSUPPORTED
     assert call(causal=3) == fb.FLASHBOB_ERR_INVALID_ARG
     assert call(H=6, Hkv=4) == fb.FLASHBOB_ERR_INVALID_ARG
     p = list(ok)

@@ -271,6 +271,57 @@ def test_rectangular_workloads_sampled_rows(w):
     assert max(full.values()) <= TOL["bf16"], full
 
 
+# Maximum head counts: B * H = 5 * 65535 query heads, more than four times
+# the grid's y extent, so the heads cannot be cut into four head-group slices
+# of at most 65535 and the call runs whole on the caller's stream (d = 64,
+# and grouped-query d = 128).  Inputs are drawn on the device (the CPU draw
+# of 3e8 values takes minutes); key/value groups sampled across the whole
+# range of heads go through the full oracle.
+MAX_HEADS = [wl.small_workload(5, 65535, 3, 64, "bf16", seed=31),
+             wl.small_workload(5, 65535, 3, 128, "bf16", seed=32, Hkv=13107)]
+
+
+def _group_subproblem(w, x, state, out, groups):
+    """Key/value groups (b, g) of a large call as a workload of their own:
+    batch i = group i, with its H / Hkv query heads and one key/value head."""
+    G = w.H // w.kv_heads
+    sub = wl.small_workload(len(groups), G, w.N, w.d, w.dtype, seed=w.seed, Hkv=1,
+                            causal=w.causal)
+
+    def q(t):
+        return torch.stack([t[b, g * G:(g + 1) * G] for b, g in groups])
+
+    def kv(t):
+        return torch.stack([t[b, g:g + 1] for b, g in groups])
+
+    xs = {k: (kv(v) if k in wl.KV_NAMES else q(v)) for k, v in x.items()}
+    st = {k: q(v) for k, v in state.items()}
+    os_ = {k: (kv(v) if k in ("dKt", "dVt") else q(v)) for k, v in out.items()}
+    return sub, xs, st, os_
+
+
+@pytest.mark.parametrize("w", MAX_HEADS, ids=lambda w: w.name)
+def test_maximum_head_counts(w):
+    assert fb.flashbob_bob_launches(w.B, w.H, w.kv_heads, w.N, w.kv_len, w.d,
+                                    fb.FLASHBOB_BF16) == (3 if w.d == 128 else 2)
+    x = wl.make_inputs(w, device="cuda")
+    O, L, D = fb.prep(x["Q"], x["K"], x["V"], x["dO"], w.tau, causal=w.causal)
+    out = fb.alloc_bob_outputs(x["Q"], fill=float("nan"), K=x["K"])
+    fb.bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
+           out=out, causal=w.causal)
+    torch.cuda.synchronize()
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    _assert_all_written(out)
+    n = w.kv_heads
+    groups = [(0, 0), (0, n - 1), (1, n // 3), (2, n // 2), (3, 2 * n // 3), (4, n - 2),
+              (4, n - 1)]
+    sub, xs, st, os_ = _group_subproblem(w, x, {"O": O, "L": L, "D": D}, out, groups)
+    errs = record(f"{w.name} sampled groups", full_oracle_errors(sub, xs, st, os_))
+    assert max(errs.values()) <= TOL["bf16"], errs
+    del x, O, L, D, out
+    torch.cuda.empty_cache()
+
+
 # --------------------------------------------------------------------------
 # Head dim 128 on the tensor cores
 # --------------------------------------------------------------------------
