@@ -78,8 +78,9 @@ cudaError_t tc_bob(const BobArgs& a);
 // Streams tc_bob runs a call on: 1 (the caller's), or up to 4 internal
 // streams, one per slice of the key/value heads, when both passes are asked
 // for, there are several head groups, a pass has more than two waves of
-// CTAs (the groups' pass 1 -> pass 2 chains then overlap each other's tails)
-// and every slice's query heads fit the grid's y extent.
+// CTAs (the groups' pass 1 -> pass 2 chains then overlap each other's tails),
+// every slice's query heads fit the grid's y extent and the caller's stream
+// is not being captured into a CUDA graph.
 int tc_bob_streams(const BobArgs& a);
 bool tc_jvp_supported(const JvpArgs& a);
 cudaError_t tc_jvp(const JvpArgs& a);

@@ -330,7 +330,16 @@ int tc_bob_streams(const BobArgs& a) {
   // A slice launches its (at most ceil(groups / ns)) * G query heads along
   // the grid's y extent: a call whose slices would not fit stays whole.
   if ((groups + ns - 1) / ns * (a.H / a.Hkv) > kMaxGridY) return 1;
-  return ns;
+  // A call captured into a CUDA graph stays on the capturing stream: the
+  // internal streams are shared by every call on the device, and once a
+  // capture has drawn them in it keeps them until it ends, so another
+  // thread's direct call would launch into that capture instead of running.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(a.stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  return cs == cudaStreamCaptureStatusNone ? ns : 1;
 }
 
 cudaError_t tc_bob(const BobArgs& a) {

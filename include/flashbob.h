@@ -115,7 +115,10 @@ flashbob_status flashbob_prep(const void* Q, const void* K, const void* V, const
  *   a head reads only pass 1's alpha and E of that head's query rows); the
  *   results are those of the one-stream order, bit for bit.  Those streams
  *   are made once per device and kept; calls serialize their enqueueing on
- *   them.  flashbob_bob_launches says how many kernels a call launches.
+ *   them.  A call made while `stream` is being captured into a CUDA graph
+ *   stays on `stream` (two kernels, three at d = 128), so that no capture
+ *   draws in the shared streams and absorbs other threads' calls.
+ *   flashbob_bob_launches says how many kernels an uncaptured call launches.
  */
 flashbob_status flashbob_bob(const void* Q, const void* K, const void* V, const float* O,
                              const void* dO, const float* L, const float* D, const void* UQ,
@@ -175,8 +178,9 @@ flashbob_status flashbob_attention_jvp(const void* Q, const void* K, const void*
  * these sizes makes on the current device: pass 1 and pass 2, where pass 1
  * of the tensor-core path at d = 128 is two launches (the JVP with alpha,
  * d~dO and E, then d~Q); that many per head group when the call runs head
- * groups on internal streams.  Checks the sizes as flashbob_bob does;
- * `launches` must not be NULL.
+ * groups on internal streams (a call outside any CUDA graph capture; a
+ * captured call stays on its stream).  Checks the sizes as flashbob_bob
+ * does; `launches` must not be NULL.
  */
 flashbob_status flashbob_bob_launches(int B, int H, int Hkv, int Nq, int Nk, int d,
                                       flashbob_dtype in_dtype, int* launches);

@@ -70,10 +70,11 @@ def test_small_calls_stay_on_the_callers_stream():
 
 @pytest.mark.parametrize("w", [CASES[0], CASES[3]], ids=[CASES[0].name, CASES[3].name])
 def test_head_group_streams_under_cuda_graph_capture(w):
-    # The internal streams join a capture through the fork/join events, so a
-    # captured flashbob_bob replays the same launches: the replay's outputs
-    # equal a direct call's bit for bit, and a replay with changed inputs
-    # (same buffers) tracks them.
+    # A captured flashbob_bob stays on the capturing stream (the shared
+    # internal streams are never drawn into a capture): the replay's outputs
+    # equal a direct call's (which runs the head groups on the internal
+    # streams) bit for bit, and a replay with changed inputs (same buffers)
+    # tracks them.
     x = wl.make_inputs(w)
     d = {k: v.cuda() for k, v in x.items()}
     O, L, D = fb.prep(d["Q"], d["K"], d["V"], d["dO"], w.tau, causal=w.causal)
@@ -106,6 +107,64 @@ def test_head_group_streams_under_cuda_graph_capture(w):
     torch.cuda.synchronize()
     for k in ref2:
         assert torch.equal(out[k], ref2[k]), f"{k}: replay after an input change differs"
+
+
+def test_direct_call_while_another_thread_captures():
+    # One thread opens a capture (thread-local mode) and records a call; before
+    # it closes the capture, the main thread makes a direct call of a size that
+    # runs head groups on the internal streams.  The direct call runs and is
+    # exact (no capture holds the internal streams), and the graph recorded
+    # meanwhile replays exactly.
+    import threading
+    w = CASES[0]
+    x = wl.make_inputs(w)
+    d = {k: v.cuda() for k, v in x.items()}
+    O, L, D = fb.prep(d["Q"], d["K"], d["V"], d["dO"], w.tau, causal=w.causal)
+    ref = fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+                 causal=w.causal)
+    out_g = fb.alloc_bob_outputs(d["Q"], fill=float("nan"), K=d["K"])
+    out_d = fb.alloc_bob_outputs(d["Q"], fill=float("nan"), K=d["K"])
+    s_main = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    recorded, direct_done = threading.Event(), threading.Event()
+    errors = []
+    g = torch.cuda.CUDAGraph()
+
+    def capturer():
+        try:
+            torch.cuda.set_device(0)
+            cap = torch.cuda.Stream()
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"],
+                       w.tau, out=out_g, causal=w.causal, stream=cap)
+                recorded.set()
+                if not direct_done.wait(timeout=120):
+                    raise TimeoutError("the direct call did not finish")
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+        finally:
+            recorded.set()
+
+    t = threading.Thread(target=capturer)
+    t.start()
+    assert recorded.wait(timeout=120)
+    try:
+        if not errors:
+            fb.bob(d["Q"], d["K"], d["V"], O, d["dO"], L, D, d["UQ"], d["UK"], d["UV"], w.tau,
+                   out=out_d, causal=w.causal, stream=s_main)
+            s_main.synchronize()
+    finally:
+        direct_done.set()
+        t.join(timeout=120)
+    assert not t.is_alive()
+    assert not errors, errors
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+    for k in ref:
+        assert torch.equal(out_d[k], ref[k]), f"{k}: the direct call differs"
+    g.replay()
+    torch.cuda.synchronize()
+    for k in ref:
+        assert torch.equal(out_g[k], ref[k]), f"{k}: the replay differs"
 
 
 def test_concurrent_calls_from_two_host_threads():
