@@ -86,6 +86,50 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _check(where: str, Q, K, spec) -> None:
+    """The C ABI sees only pointers and sizes, so the binding checks what the
+    header fixes for each tensor before handing its pointer on: a CUDA tensor
+    on Q's device, contiguous (row-major), with the shape and dtype of its
+    role.  ``spec`` lists (name, tensor, role, dtype) with role "q"
+    ([B, H, N_q, d]), "k" ([B, H_kv, N_k, d]) or "row" ([B, H, N_q]) and
+    dtype "in" (the inputs' common dtype, Q's) or "f32"; None tensors are
+    skipped (the ABI decides which may be NULL)."""
+    import torch
+    for name, t in (("Q", Q), ("K", K)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError(f"{where}: {name} must be a 4-d tensor [B, heads, rows, d]")
+    B, H, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    shapes = {"q": (B, H, Nq, d), "k": (B, Hkv, Nk, d), "row": (B, H, Nq)}
+    for name, t, role, dt in spec:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != Q.device:
+            raise ValueError(f"{where}: {name} must be a CUDA tensor on {Q.device}")
+        if tuple(t.shape) != shapes[role]:
+            raise ValueError(f"{where}: {name} has shape {tuple(t.shape)}, "
+                             f"expected {shapes[role]}")
+        want = Q.dtype if dt == "in" else torch.float32
+        if t.dtype != want:
+            raise TypeError(f"{where}: {name} is {t.dtype}, expected {want}")
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} must be contiguous")
+
+
+def _input_specs(Q, K, V, dO, UQ, UK, UV):
+    """Check list of the seven inputs of the BoB calls (one common dtype)."""
+    return [("Q", Q, "q", "in"), ("K", K, "k", "in"), ("V", V, "k", "in"),
+            ("dO", dO, "q", "in"), ("UQ", UQ, "q", "in"), ("UK", UK, "k", "in"),
+            ("UV", UV, "k", "in")]
+
+
+def _device(t):
+    """The CUDA device context of tensor ``t``: the library works on the
+    current device, so every call runs with its tensors' device current."""
+    import torch
+    return torch.cuda.device(t.device)
+
+
 def flashbob_status_string(status: int) -> str:
     return load_library().flashbob_status_string(status).decode()
 
@@ -93,11 +137,16 @@ def flashbob_status_string(status: int) -> str:
 def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream=None) -> None:
     """O, L, D of [B, H, Nq, d] queries and [B, Hkv, Nk, d] keys/values
     (see flashbob_prep in the header); dO = D = None computes O and L only."""
+    _check("flashbob_prep", Q, K, [("Q", Q, "q", "in"), ("K", K, "k", "in"),
+                                    ("V", V, "k", "in"), ("dO", dO, "q", "in"),
+                                    ("O", O, "q", "f32"), ("L", L, "row", "f32"),
+                                    ("D", D, "row", "f32")])
     B, H, Nq, d = Q.shape
     Hkv, Nk = K.shape[1], K.shape[2]
-    st = load_library().flashbob_prep(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, Hkv, Nq, Nk, d,
-        float(tau), int(causal), _dtype_code(Q), _stream_handle(stream))
+    with _device(Q):
+        st = load_library().flashbob_prep(
+            _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(O), _ptr(L), _ptr(D), B, H, Hkv, Nq, Nk,
+            d, float(tau), int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_prep")
 
@@ -105,12 +154,18 @@ def flashbob_prep(Q, K, V, dO, O, L, D, tau: float, causal: bool = False, stream
 def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, ddOt, alpha, E,
                  causal: bool = False, stream=None) -> None:
     """d~Q, d~K, d~V, d~dO, alpha, E (see flashbob_bob in the header)."""
+    _check("flashbob_bob", Q, K, _input_specs(Q, K, V, dO, UQ, UK, UV) + [
+        ("O", O, "q", "f32"), ("L", L, "row", "f32"), ("D", D, "row", "f32"),
+        ("dQt", dQt, "q", "f32"), ("dKt", dKt, "k", "f32"), ("dVt", dVt, "k", "f32"),
+        ("ddOt", ddOt, "q", "f32"), ("alpha", alpha, "row", "f32"), ("E", E, "row", "f32")])
     B, H, Nq, d = Q.shape
     Hkv, Nk = K.shape[1], K.shape[2]
-    st = load_library().flashbob_bob(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
-        _ptr(UV), float(tau), _ptr(dQt), _ptr(dKt), _ptr(dVt), _ptr(ddOt), _ptr(alpha), _ptr(E),
-        B, H, Hkv, Nq, Nk, d, int(causal), _dtype_code(Q), _stream_handle(stream))
+    with _device(Q):
+        st = load_library().flashbob_bob(
+            _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ),
+            _ptr(UK), _ptr(UV), float(tau), _ptr(dQt), _ptr(dKt), _ptr(dVt), _ptr(ddOt),
+            _ptr(alpha), _ptr(E), B, H, Hkv, Nq, Nk, d, int(causal), _dtype_code(Q),
+            _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob")
 
@@ -118,12 +173,17 @@ def flashbob_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, dKt, dVt, dd
 def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, alpha, E,
                        causal: bool = False, stream=None) -> None:
     """Pass 1 only: d~Q, d~dO, alpha, E (see flashbob_bob_pass1 in the header)."""
+    _check("flashbob_bob_pass1", Q, K, _input_specs(Q, K, V, dO, UQ, UK, UV) + [
+        ("O", O, "q", "f32"), ("L", L, "row", "f32"), ("D", D, "row", "f32"),
+        ("dQt", dQt, "q", "f32"), ("ddOt", ddOt, "q", "f32"), ("alpha", alpha, "row", "f32"),
+        ("E", E, "row", "f32")])
     B, H, Nq, d = Q.shape
     Hkv, Nk = K.shape[1], K.shape[2]
-    st = load_library().flashbob_bob_pass1(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ), _ptr(UK),
-        _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H, Hkv, Nq, Nk, d,
-        int(causal), _dtype_code(Q), _stream_handle(stream))
+    with _device(Q):
+        st = load_library().flashbob_bob_pass1(
+            _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D), _ptr(UQ),
+            _ptr(UK), _ptr(UV), float(tau), _ptr(dQt), _ptr(ddOt), _ptr(alpha), _ptr(E), B, H,
+            Hkv, Nq, Nk, d, int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass1")
 
@@ -131,12 +191,16 @@ def flashbob_bob_pass1(Q, K, V, O, dO, L, D, UQ, UK, UV, tau: float, dQt, ddOt, 
 def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt, dVt,
                        causal: bool = False, stream=None) -> None:
     """Pass 2 only: d~K, d~V from pass 1's alpha, E (see flashbob_bob_pass2)."""
+    _check("flashbob_bob_pass2", Q, K, _input_specs(Q, K, V, dO, UQ, UK, UV) + [
+        ("L", L, "row", "f32"), ("D", D, "row", "f32"), ("alpha", alpha, "row", "f32"),
+        ("E", E, "row", "f32"), ("dKt", dKt, "k", "f32"), ("dVt", dVt, "k", "f32")])
     B, H, Nq, d = Q.shape
     Hkv, Nk = K.shape[1], K.shape[2]
-    st = load_library().flashbob_bob_pass2(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(D), _ptr(alpha), _ptr(E), _ptr(UQ),
-        _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, Hkv, Nq, Nk, d, int(causal),
-        _dtype_code(Q), _stream_handle(stream))
+    with _device(Q):
+        st = load_library().flashbob_bob_pass2(
+            _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(D), _ptr(alpha), _ptr(E),
+            _ptr(UQ), _ptr(UK), _ptr(UV), float(tau), _ptr(dKt), _ptr(dVt), B, H, Hkv, Nq, Nk,
+            d, int(causal), _dtype_code(Q), _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_bob_pass2")
 
@@ -144,12 +208,17 @@ def flashbob_bob_pass2(Q, K, V, dO, L, D, alpha, E, UQ, UK, UV, tau: float, dKt,
 def flashbob_attention_jvp(Q, K, V, O, L, UQ, UK, UV, tau: float, Od, Ld,
                            causal: bool = False, stream=None) -> None:
     """O' and L' along the tangents (U_Q, U_K, U_V) (see flashbob_attention_jvp)."""
+    _check("flashbob_attention_jvp", Q, K, [
+        ("Q", Q, "q", "in"), ("K", K, "k", "in"), ("V", V, "k", "in"), ("UQ", UQ, "q", "in"),
+        ("UK", UK, "k", "in"), ("UV", UV, "k", "in"), ("O", O, "q", "f32"),
+        ("L", L, "row", "f32"), ("Od", Od, "q", "f32"), ("Ld", Ld, "row", "f32")])
     B, H, Nq, d = Q.shape
     Hkv, Nk = K.shape[1], K.shape[2]
-    st = load_library().flashbob_attention_jvp(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), _ptr(UQ), _ptr(UK), _ptr(UV), float(tau),
-        _ptr(Od), _ptr(Ld), B, H, Hkv, Nq, Nk, d, int(causal), _dtype_code(Q),
-        _stream_handle(stream))
+    with _device(Q):
+        st = load_library().flashbob_attention_jvp(
+            _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), _ptr(UQ), _ptr(UK), _ptr(UV),
+            float(tau), _ptr(Od), _ptr(Ld), B, H, Hkv, Nq, Nk, d, int(causal), _dtype_code(Q),
+            _stream_handle(stream))
     if st != FLASHBOB_OK:
         raise FlashbobError(st, "flashbob_attention_jvp")
 

@@ -158,6 +158,25 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
         fb._lib = saved
 
 
+def test_binding_rejects_host_tensors_and_bad_ranks():
+    # The C ABI takes device pointers only; the binding refuses host tensors
+    # (and tensors that are not [B, heads, rows, d]) before any call.
+    import torch
+    x = {k: torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16) for k in
+         ("Q", "K", "V", "dO", "UQ", "UK", "UV")}
+    O = torch.zeros(1, 2, 8, 64)
+    L = torch.zeros(1, 2, 8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fb.flashbob_prep(x["Q"], x["K"], x["V"], x["dO"], O, L, L.clone(), 0.125)
+    out = {k: torch.zeros(1, 2, 8, 64) for k in ("dQt", "dKt", "dVt", "ddOt")}
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fb.flashbob_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, L, x["UQ"], x["UK"], x["UV"],
+                        0.125, out["dQt"], out["dKt"], out["dVt"], out["ddOt"], L, L)
+    with pytest.raises(ValueError, match="4-d"):
+        fb.flashbob_attention_jvp(x["Q"][0], x["K"], x["V"], O, L, x["UQ"], x["UK"], x["UV"],
+                                  0.125, O, L)
+
+
 def test_pass_entry_points_reject_bad_arguments_on_the_host(lib):
     ok = _fake_ptrs()
     sizes = (1, 1, 1, 8, 8, 64, 0, 0, None)  # B, H, Hkv, Nq, Nk, d, causal, dtype, stream

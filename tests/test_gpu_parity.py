@@ -177,6 +177,38 @@ def test_bad_arguments_return_codes_and_launch_nothing():
     np.testing.assert_equal(fb.flashbob_status_string(0), "FLASHBOB_OK")
 
 
+def test_binding_checks_every_tensor_before_the_call():
+    # Shape, dtype, layout and device of every tensor are checked in the
+    # binding (the C ABI sees only pointers and sizes); a rejected call
+    # launches nothing.
+    w = wl.small_workload(1, 2, 64, 64, "bf16", seed=8)
+    x, dev, state, out = run_cuda(w)
+    before = {k: v.clone() for k, v in out.items()}
+    args = dict(dev, O=state["O"], L=state["L"], D=state["D"])
+
+    def call(**over):
+        a = dict(args, **over)
+        fb.bob(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["L"], a["D"], a["UQ"], a["UK"],
+               a["UV"], w.tau, out=out)
+
+    with pytest.raises(ValueError, match="shape"):
+        call(K=dev["K"][..., :32].contiguous())                 # wrong head dim
+    with pytest.raises(ValueError, match="shape"):
+        call(L=state["L"][:, :1].contiguous())                  # wrong head count
+    with pytest.raises(TypeError, match="float32"):
+        call(K=dev["K"].float())                                # inputs of mixed dtypes
+    with pytest.raises(TypeError, match="float32"):
+        call(O=state["O"].bfloat16())                           # row state not fp32
+    with pytest.raises(ValueError, match="contiguous"):
+        call(V=dev["V"].transpose(2, 3).contiguous().transpose(2, 3))   # column-major V
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        call(UQ=dev["UQ"].cpu())
+    torch.cuda.synchronize()
+    for k in out:
+        assert torch.equal(out[k], before[k]), k
+    assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
+
+
 # --------------------------------------------------------------------------
 # Causal mask (the setting of the pages' timing tables)
 # --------------------------------------------------------------------------
