@@ -315,23 +315,34 @@ def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
         fb.flashbob_attention_jvp(dev["Q"], dev["K"], dev["V"], O, L, dev["UQ"], dev["UK"],
                                   dev["UV"], w.tau, Od, Ld, causal=w.causal, stream=stream)
 
+    resident = sum(t.numel() * t.element_size() for t in (dev["Q"], dev["K"], dev["V"],
+                                                          dev["UQ"], dev["UK"], dev["UV"], O, L))
+    flush, l2_note = l2_flusher(torch, resident)
     for _ in range(max(3, args.warmup)):
+        if flush is not None:
+            flush.zero_()
         step()
     torch.cuda.synchronize()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(None)
     time.sleep(0.3)
     barrier()
-    t0.record(stream)
-    for _ in range(args.steps):
+    for e in evs:
+        if flush is not None:
+            flush.zero_()
+        e[0].record(stream)
         step()
-    t1.record(stream)
+        e[1].record(stream)
     barrier()
     clocks = sampler.stop()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-    ms = t0.elapsed_time(t1) / args.steps
-    total_ms = reduce_max(t0.elapsed_time(t1), world, "cuda")
+    if flush is not None:
+        local_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    else:
+        local_ms = evs[0][0].elapsed_time(evs[-1][1])
+    ms = local_ms / args.steps
+    total_ms = reduce_max(local_ms, world, "cuda")
     flops = JVP_GEMMS * 2.0 * w.pairs * w.d * w.B * w.H
     value = job_tflops(flops, args.steps, world, total_ms)
     peak, _, peak_note = tensor_peak()
@@ -343,7 +354,7 @@ def run_jvp(args, w, dev, rank, world, local, barrier, fb, torch):
         "data": "synthetic",
         "config": {"workload": w.name, "entry": "flashbob_attention_jvp", "B": w.B, "H": w.H,
                    "Hkv": w.kv_heads, "N": w.N, "Nk": w.kv_len, "d": w.d, "causal": w.causal,
-                   "flops_per_step_per_gpu": flops},
+                   "flops_per_step_per_gpu": flops, "l2": l2_note},
         "roofline": {"kernel": "jvp", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                      "peak_source": peak_note},
@@ -444,13 +455,36 @@ class Resident:
                    + [self.O, self.L, self.D])
 
 
-def timed_steps(res, steps, warmup, torch, barrier, uuid):
+def l2_flusher(torch, resident_bytes):
+    """What keeps a step from finding the previous step's data in the L2:
+    inputs (with the row state) of more than twice the L2 evict it by
+    themselves; smaller ones get a write of twice the L2 before every timed
+    step, outside that step's events.  Returns (buffer or None, note)."""
+    mib = resident_bytes / 2**20
+    if resident_bytes > 2 * L2_BYTES:
+        return None, f"no flush: inputs {mib:.0f} MiB > 2 x L2 ({L2_BYTES / 2**20:.0f} MiB)"
+    buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    return buf, (f"L2 flushed before every step ({2 * L2_BYTES / 2**20:.0f} MiB written; "
+                 f"inputs {mib:.0f} MiB <= 2 x L2); ms_per_step sums the steps' own event "
+                 f"intervals")
+
+
+def timed_steps(res, steps, warmup, torch, barrier, uuid, flush=None):
     """W warm-up steps, then K steps (one flashbob_bob call each) with CUDA
     events on the launching stream and nvidia-smi clocks sampled during the
     timed region; then, outside it, K steps of the two passes as separate
-    calls, each pass between two events, for the per-kernel times."""
+    calls, each pass between two events, for the per-kernel times.  With a
+    ``flush`` buffer every step (and every pair of separate passes) follows a
+    write of it, outside its events, and the total is the sum of the steps'
+    own intervals."""
     fb = res.fb
+
+    def flush_l2():
+        if flush is not None:
+            flush.zero_()
+
     for _ in range(max(3, warmup)):
+        flush_l2()
         res.step()
     torch.cuda.synchronize()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
@@ -459,6 +493,7 @@ def timed_steps(res, steps, warmup, torch, barrier, uuid):
     time.sleep(0.3)
     barrier()
     for i in range(steps):
+        flush_l2()
         res.step(evs[i])
     barrier()
     clocks = sampler.stop()
@@ -466,10 +501,15 @@ def timed_steps(res, steps, warmup, torch, barrier, uuid):
     pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     res.step_passes()
     for i in range(steps):
+        flush_l2()
         res.step_passes(pev[i])
     torch.cuda.synchronize()
     assert fb.flashbob_last_device_error() == fb.FLASHBOB_OK
-    return {"total_ms": evs[0][0].elapsed_time(evs[-1][1]),
+    if flush is not None:
+        total_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    else:
+        total_ms = evs[0][0].elapsed_time(evs[-1][1])
+    return {"total_ms": total_ms,
             "median_ms": statistics.median(e[0].elapsed_time(e[1]) for e in evs),
             "p1_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in pev),
             "p2_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in pev),
@@ -496,6 +536,7 @@ def run_sweep(args, fb, torch, barrier, uuid, peak, peak_note):
     for name in SWEEP:
         w = WORKLOADS[name]
         res = Resident(w, make_inputs(w), fb, torch)
+        flush, l2_note = l2_flusher(torch, res.input_bytes())
         # about half a second of timed work, at least 5 steps
         res.step()
         torch.cuda.synchronize()
@@ -504,13 +545,14 @@ def run_sweep(args, fb, torch, barrier, uuid, peak, peak_note):
         torch.cuda.synchronize()
         est = max(time.perf_counter() - t0, 1e-5)
         steps = int(min(200, max(5, 0.5 / est)))
-        t = timed_steps(res, steps, 3, torch, barrier, uuid)
+        t = timed_steps(res, steps, 3, torch, barrier, uuid, flush)
+        del flush
         ms = t["total_ms"] / steps
         value = w.flops / (ms * 1e-3) / 1e12
         line = {"sweep": True, "metric": METRIC, "value": value, "unit": UNIT,
                 "ms_per_step": ms, "steps": steps, "warmup": 3, "dtype": "bf16",
                 "pct_of_peak": 100.0 * value / peak,
-                "config": dict(config_dict(w), ms_per_call_median=t["median_ms"],
+                "config": dict(config_dict(w), l2=l2_note, ms_per_call_median=t["median_ms"],
                                pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                                passes_as_separate_calls_ms=t["passes_ms"],
                                head_group_streams=res.streams_per_step(),
@@ -665,11 +707,12 @@ def main():
         return run_jvp(args, w, dev, rank, world, local, barrier, fb, torch)
     res = Resident(w, x, fb, torch)
     uuid = gpu_uuid(torch, local)
-    t = timed_steps(res, args.steps, args.warmup, torch, barrier, uuid)
+    flush, l2_note = l2_flusher(torch, res.input_bytes())
+    t = timed_steps(res, args.steps, args.warmup, torch, barrier, uuid, flush)
+    del flush
     res_launches = res.launches_per_step()
     res_streams = res.streams_per_step()
     prep_ms = res.prep_ms(torch)
-    in_bytes = res.input_bytes()
     total_ms = reduce_max(t["total_ms"], world, "cuda")
     ms_per_step = total_ms / args.steps
     flops = w.flops
@@ -695,8 +738,7 @@ def main():
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(config_dict(w), flops_per_step_per_gpu=flops,
-                       l2=f"no flush: inputs {in_bytes / 2**20:.0f} MiB > L2 "
-                          f"{L2_BYTES / 2**20:.0f} MiB",
+                       l2=l2_note,
                        ms_per_call_median=t["median_ms"],
                        pass1_ms=t["p1_ms"], pass2_ms=t["p2_ms"],
                        passes_as_separate_calls_ms=t["passes_ms"],
