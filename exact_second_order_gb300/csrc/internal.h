@@ -71,6 +71,7 @@ size_t simt_pass2_smem(int d);
 constexpr int kTcRows = 128;    // rows of the resident block (MMA M) in both passes
 constexpr int kTcStream = 32;   // rows of a streamed key tile in pass 1 (and of a d = 128 pass-2 query tile)
 constexpr int kTcStream2 = 64;  // rows of a streamed query tile in pass 2
+constexpr int kTcJvpStream = 64;  // rows of a streamed key tile in the d = 64 JVP
 bool tc_supported(const BobArgs& a);
 bool tc_prep_supported(const PrepArgs& a);
 cudaError_t tc_prep(const PrepArgs& a);

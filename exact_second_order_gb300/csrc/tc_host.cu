@@ -12,7 +12,7 @@ cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
 cudaError_t tc_launch_pass2(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps64);
 cudaError_t tc_launch_jvp(const JvpArgs& a, const CUtensorMap* maps128,
-                          const CUtensorMap* maps32);
+                          const CUtensorMap* maps64);
 cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
                                  const CUtensorMap* maps32);
 cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
@@ -375,16 +375,19 @@ cudaError_t tc_bob(const BobArgs& a) {
 bool tc_jvp_supported(const JvpArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
 cudaError_t tc_jvp(const JvpArgs& a) {
-  CUtensorMap m128[2], m32[4];
+  // Key tiles of 32 rows at d = 128, 64 rows at d = 64 (the d = 64 JVP
+  // kernel streams 64 keys per tile).
+  const int key_rows = a.d == 128 ? kTcStream : kTcJvpStream;
+  CUtensorMap m128[2], mk[4];
   const void* rows[2] = {a.Q, a.UQ};
   const void* cols[4] = {a.K, a.V, a.UK, a.UV};
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < 2 && e == cudaSuccess; ++i)
     e = tc_map_bf16(&m128[i], rows[i], a.B * a.H, a.Nq, kTcRows, a.d);
   for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-    e = tc_map_bf16(&m32[i], cols[i], a.B * a.Hkv, a.Nk, kTcStream, a.d);
+    e = tc_map_bf16(&mk[i], cols[i], a.B * a.Hkv, a.Nk, key_rows, a.d);
   if (e != cudaSuccess) return e;
-  return a.d == 128 ? tc_launch_jvp_d128(a, m128, m32) : tc_launch_jvp(a, m128, m32);
+  return a.d == 128 ? tc_launch_jvp_d128(a, m128, mk) : tc_launch_jvp(a, m128, mk);
 }
 
 }  // namespace flashbob

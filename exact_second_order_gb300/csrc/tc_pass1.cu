@@ -33,12 +33,6 @@
 // F'/S GEMMs of the tile two ahead run while it still computes; only the
 // dP/G GEMMs wait for the output GEMMs (the tensor pipe runs MMAs in issue
 // order, so they overwrite the operands after those have been read).
-//
-// The same kernel, instantiated with JVP = true, serves the attention JVP
-// along (U_Q, U_K, U_V): alpha and d~dO do not depend on dO, so with dO = 0
-// (no dP, G scores; only P and P o F as operands) it returns L' and O'.
-// With a single accumulator it keeps three score buffers at [128,512) (tile t
-// in buffer t mod 3), so no warpgroup waits for its next tile's scores.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -71,9 +65,9 @@ struct Smem1 {
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
-  uint64_t sc_full[3];
+  uint64_t sc_full[2];
   uint64_t sf_free[2];   // per buffer: the warpgroup holds the tile in registers
-  uint64_t op_ready[3];  // per buffer: one arrive per elementwise warp
+  uint64_t op_ready[2];  // per buffer: one arrive per elementwise warp
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -84,22 +78,14 @@ static_assert(2 * kStageBytes <= sizeof(Smem1::kv), "epilogue staging fits in th
 constexpr uint32_t kColF = 0, kColS = 32, kColdP = 64, kColG = 96;
 // TMEM columns of the bf16 operand slots inside a score buffer, for the two
 // K = 16 steps (chunks) of the output GEMMs: the dP | G half.  A warpgroup
-// reads the whole buffer (the JVP: S and F') before it writes any slot; the
-// JVP's score GEMMs never write the dP/G columns.
+// reads the whole buffer before it writes any slot.
 __device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 64 + 8 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_PdPt(int c) { return 80 + 8 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 96 + 8 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 112 + 8 * c; }
-// Score buffers: the BoB has two (tile t in buffer t mod 2 at column
-// 256 + 128 (t mod 2)); the JVP, which needs only the d~dO0 accumulator,
-// has three (tile t in buffer t mod 3 at column 128 + 128 (t mod 3)), so the
-// score GEMMs of tile t + 3 can run before the warpgroup of tile t + 2 starts.
-template <bool JVP>
-__device__ __forceinline__ int p1_buf(int t) { return JVP ? t % 3 : t & 1; }
-template <bool JVP>
-__device__ __forceinline__ uint32_t p1_buf_col(int t) {
-  return JVP ? 128 + 128 * (t % 3) : 256 + 128 * (t & 1);
-}
+// Score buffers: tile t in buffer t mod 2, at column 256 + 128 (t mod 2).
+__device__ __forceinline__ int p1_buf(int t) { return t & 1; }
+__device__ __forceinline__ uint32_t p1_buf_col(int t) { return 256 + 128 * (t & 1); }
 // Output accumulators.
 constexpr uint32_t kAccB = 0, kAccdO = 64, kAccW = 128, kAccR = 192;  // R' = dS K
 
@@ -143,57 +129,15 @@ __device__ __forceinline__ void p1_chunk(uint32_t sc, const uint32_t (&s)[16],
   tmem_st8(sc + slot_PF(C), oPF);
 }
 
-// The attention JVP's version of p1_chunk (no dO: dP = G = 0): P and
-// P o F only, and the row sum alpha = L'.  The slots of P and P o F lie in
-// the dP/G columns, which the JVP's score GEMMs never write.
-template <bool MASKED, int C>
-__device__ __forceinline__ void p1_chunk_jvp(uint32_t sc, const uint32_t (&s)[16],
-                                             const uint32_t (&f)[16], int col0, int jmax,
-                                             float c1, float Lr2, float tau, float2& a_acc) {
-  uint32_t oP[8], oPF[8];
-  const int jbase = col0 + 16 * C;
-  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
-  const float2 tau2 = make_float2(tau, tau);
-#pragma unroll
-  for (int e = 0; e < 16; e += 2) {
-    const float2 t = ffma2(f2(s[e], s[e + 1]), c12, nL);
-    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-    if (MASKED) {
-      if (jbase + e > jmax) p.x = 0.f;
-      if (jbase + e + 1 > jmax) p.y = 0.f;
-    }
-    const float2 pf = fmul2(p, fmul2(f2(f[e], f[e + 1]), tau2));
-    a_acc = fadd2(a_acc, pf);
-    oP[e >> 1] = pack_bf16x2(p.x, p.y);
-    oPF[e >> 1] = pack_bf16x2(pf.x, pf.y);
-  }
-  tmem_st8(sc + slot_P(C), oP);
-  tmem_st8(sc + slot_PF(C), oPF);
-}
-
 // One 32-column tile, one row per thread: read all of S, F', dP, G (both
-// 16-column chunks; S and F' only for the JVP) with a single wait and free
-// the F' | S half, form the bf16 A operands of the output GEMMs in the dP | G
-// half, and hand the tile to the MMA issuer once they are in TMEM.
-template <bool MASKED, bool JVP>
+// 16-column chunks) with a single wait and free the F' | S half, form the
+// bf16 A operands of the output GEMMs in the dP | G half, and hand the tile
+// to the MMA issuer once they are in TMEM.
+template <bool MASKED>
 __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* sf_free, uint64_t* ready,
                                         int col0, int jmax,
                                         float c1, float Lr2, float Dr, float tau, float2& a_acc,
                                         float2& e_acc) {
-  if constexpr (JVP) {
-    uint32_t s0[16], f0[16], s1[16], f1[16];
-    tmem_ld16(sc + kColS, s0);
-    tmem_ld16(sc + kColF, f0);
-    tmem_ld16(sc + kColS + 16, s1);
-    tmem_ld16(sc + kColF + 16, f1);
-    tmem_wait_ld();
-    p1_chunk_jvp<MASKED, 0>(sc, s0, f0, col0, jmax, c1, Lr2, tau, a_acc);
-    p1_chunk_jvp<MASKED, 1>(sc, s1, f1, col0, jmax, c1, Lr2, tau, a_acc);
-    tmem_wait_st();
-    tc_fence_before();
-    warp_arrive(ready);
-    return;
-  }
   uint32_t s0[16], dp0[16], f0[16], g0[16], s1[16], dp1[16], f1[16], g1[16];
   tmem_ld16(sc + kColS, s0);
   tmem_ld16(sc + kColdP, dp0);
@@ -213,10 +157,6 @@ __device__ __forceinline__ void p1_tile(uint32_t sc, uint64_t* sf_free, uint64_t
   warp_arrive(ready);
 }
 
-// JVP = true: the attention JVP along (U_Q, U_K, U_V), i.e. this pass with
-// dO = 0: no dO block, no dP/G scores, only the d~dO0 accumulator; ddOt
-// receives O' and alpha receives L' (dQt, E, D and mdO are not used).
-template <bool JVP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                     const __grid_constant__ CUtensorMap mUQ, const __grid_constant__ CUtensorMap mK,
@@ -245,18 +185,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 3; ++b) {
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.sc_full[b], 1);
       mbar_init(&sm.op_ready[b], 4);
+      mbar_init(&sm.sf_free[b], 4);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&sm.sf_free[b], 4);
     mbar_init(&sm.out_full, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
     // The resident block's copy starts now, while warp 1 allocates TMEM.
-    mbar_expect_tx(&sm.bar_q, (JVP ? 2 : 3) * BLOCK_BYTES);
+    mbar_expect_tx(&sm.bar_q, 3 * BLOCK_BYTES);
     tma_load_3d(sm.q, &mQ, &sm.bar_q, 0, row0, bh);
-    if (!JVP) tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
+    tma_load_3d(sm.dO, &mdO, &sm.bar_q, 0, row0, bh);
     tma_load_3d(sm.uq, &mUQ, &sm.bar_q, 0, row0, bh);
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
@@ -316,7 +256,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Score GEMMs of tile t in two halves: F' | S, then dP | G (+ commit).
       auto issue_sf = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + p1_buf_col<JVP>(t);
+        const uint32_t sc = tbase + p1_buf_col(t);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t o = 2 * kk;  // 32 bytes >> 4
@@ -326,31 +266,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       };
       // Issued after the output GEMMs of tile t - 2, so the commit also
       // covers their reads of the operand slots that tile t's warpgroup is
-      // about to overwrite (the JVP has no dP/G GEMMs, only the commit).
+      // about to overwrite.
       auto issue_pg = [&](int t) {
         const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + p1_buf_col<JVP>(t);
+        const uint32_t sc = tbase + p1_buf_col(t);
 #pragma unroll
-        for (int kk = 0; kk < DH / 16 && !JVP; ++kk) {
+        for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t o = 2 * kk;
           mma_ss(sc + kColdP, ddo0 + o, dV0 + so + o, idS64, kk > 0);  // [dP | G] = dO [V; U_V]^T
         }
-        mma_commit(&sm.sc_full[p1_buf<JVP>(t)]);
+        mma_commit(&sm.sc_full[p1_buf(t)]);
       };
       auto issue_outputs = [&](int t) {
         const int s = t % NST;
         const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
-        const uint32_t sc = tbase + p1_buf_col<JVP>(t);
+        const uint32_t sc = tbase + p1_buf_col(t);
         {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
             const uint32_t acc = (t > 0 || c > 0);
-            if (JVP) {  // O'0 += P U_V + (P o F) V
-              mma_ts(tbase + kAccdO, sc + slot_P(c), dUV0 + so + o, idO64, acc);
-              mma_ts(tbase + kAccdO, sc + slot_PF(c), dV0 + so + o, idO64, 1);
-              continue;
-            }
             mma_ts(tbase + kAccB, sc + slot_P(c), dKUV0 + so + o, idO128, acc);  // [B | d~dO0] += P [K | U_V]
             mma_ts(tbase + kAccW, sc + slot_dS(c), dUKK0 + so + o, idO128, acc); // [Omega | R'] += dS [U_K | K]
             mma_ts(tbase + kAccW, sc + slot_PdPt(c), dK0 + so + o, idO64, 1);    // Omega += (P o d~P0) K
@@ -362,8 +297,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (elect_one()) {
         bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
         tc_fence_after();
-        constexpr int NB = JVP ? 3 : 2;  // score buffers
-        for (int t = 0; ok && t < NB && t < T; ++t) {
+        for (int t = 0; ok && t < 2 && t < T; ++t) {  // both score buffers
           ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
           tc_fence_after();
           if (ok) {
@@ -371,22 +305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             issue_pg(t);
           }
         }
-        // The JVP: tile t + 3 reuses tile t's buffer once tile t's output
-        // GEMMs are issued; the commit after them lets its warpgroup write.
-        for (int t = 0; JVP && ok && t < T; ++t) {
-          ok = mbar_wait(&sm.op_ready[t % 3], (t / 3) & 1, abort_flag, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_outputs(t);
-          if (t + 3 < T) {
-            ok = mbar_wait(&sm.kv_full[(t + 3) % NST], ((t + 3) / NST) & 1, abort_flag, err);
-            if (!ok) break;
-            tc_fence_after();
-            issue_sf(t + 3);
-            issue_pg(t + 3);
-          }
-        }
-        for (int t = 0; !JVP && ok && t < T; ++t) {
+        for (int t = 0; ok && t < T; ++t) {
           const uint32_t ph = (t >> 1) & 1;  // phase of this warpgroup's barriers
           if (t + 2 < T) {  // the warpgroup holds tile t in registers: F' | S of t + 2
             ok = mbar_wait(&sm.sf_free[t & 1], ph, abort_flag, err) &&
@@ -415,17 +334,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
-    const float Dr = (!JVP && gr < Nq) ? D[rowvec] : 0.f;
+    const float Dr = gr < Nq ? D[rowvec] : 0.f;
     float2 a_acc = make_float2(0.f, 0.f), e_acc = make_float2(0.f, 0.f);
     bool ok = true;
 
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
       if (t >= T) break;
-      const int b = JVP ? t % 3 : wg;  // t mod 2 = wg
-      const uint32_t sc = tbase + lane_off + (JVP ? p1_buf_col<true>(t) : 256 + 128 * wg);
+      const uint32_t sc = tbase + lane_off + 256 + 128 * wg;  // buffer t mod 2 = wg
       // tcgen05.ld/st are warp-collective: take the decision warp-uniformly.
-      ok = mbar_wait_warp(&sm.sc_full[b], (JVP ? t / 3 : u) & 1, abort_flag, err);
+      ok = mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
       if (!ok) break;
       tc_fence_after();
       const int col0 = t * BN;
@@ -434,10 +352,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (masked) {
-        p1_tile<true, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[b], col0, jmax, c1, Lr2, Dr, tau,
+        p1_tile<true>(sc, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau,
                            a_acc, e_acc);
       } else {
-        p1_tile<false, JVP>(sc, &sm.sf_free[wg], &sm.op_ready[b], col0, jmax, c1, Lr2, Dr, tau,
+        p1_tile<false>(sc, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, Dr, tau,
                             a_acc, e_acc);
       }
     }
@@ -457,7 +375,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // Every MMA is done, so the ring is idle: the block's rows of O come in
     // through shared memory with coalesced loads (256 threads, 16 float4 per
     // row), each thread forms its row's outputs there, and the tiles leave
-    // with coalesced stores.  d~dO (O') overwrites O in place.
+    // with coalesced stores.  d~dO overwrites O in place.
     float* st_o = reinterpret_cast<float*>(&sm.kv[0][0][0]);  // O, then d~dO
     float* st_q = st_o + BM * kStageLd;                         // d~Q
     const int tid = threadIdx.x - 64;                           // 0 .. 255
@@ -473,11 +391,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int h = 0; h < 2; ++h) {
       const int col = 32 * wg + 16 * h;
       uint32_t vb[16], vr[16], vw[16], vo[16];
-      if (!JVP) {
-        tmem_ld16(acc_base + kAccB + col, vb);
-        tmem_ld16(acc_base + kAccR + col, vr);
-        tmem_ld16(acc_base + kAccW + col, vw);
-      }
+      tmem_ld16(acc_base + kAccB + col, vb);
+      tmem_ld16(acc_base + kAccR + col, vr);
+      tmem_ld16(acc_base + kAccW + col, vw);
       tmem_ld16(acc_base + kAccdO + col, vo);
       tmem_wait_ld();
       if (gr < Nq) {
@@ -485,17 +401,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float4* q4 = reinterpret_cast<float4*>(st_q + r * kStageLd + col);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 ov = o4[k];  // d~dO = d~dO0 - alpha O  (O' = O'0 - L' O)
+          const float4 ov = o4[k];  // d~dO = d~dO0 - alpha O
           o4[k] = make_float4(u2f(vo[4 * k + 0]) - al * ov.x, u2f(vo[4 * k + 1]) - al * ov.y,
                               u2f(vo[4 * k + 2]) - al * ov.z, u2f(vo[4 * k + 3]) - al * ov.w);
-          if (!JVP) {  // d~Q = tau (Omega - alpha R' - E0 B)
-            float4 qv;
-            qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - E0 * u2f(vb[4 * k + 0]));
-            qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - E0 * u2f(vb[4 * k + 1]));
-            qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - E0 * u2f(vb[4 * k + 2]));
-            qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - E0 * u2f(vb[4 * k + 3]));
-            q4[k] = qv;
-          }
+          float4 qv;  // d~Q = tau (Omega - alpha R' - E0 B)
+          qv.x = tau * (u2f(vw[4 * k + 0]) - al * u2f(vr[4 * k + 0]) - E0 * u2f(vb[4 * k + 0]));
+          qv.y = tau * (u2f(vw[4 * k + 1]) - al * u2f(vr[4 * k + 1]) - E0 * u2f(vb[4 * k + 1]));
+          qv.z = tau * (u2f(vw[4 * k + 2]) - al * u2f(vr[4 * k + 2]) - E0 * u2f(vb[4 * k + 2]));
+          qv.w = tau * (u2f(vw[4 * k + 3]) - al * u2f(vr[4 * k + 3]) - E0 * u2f(vb[4 * k + 3]));
+          q4[k] = qv;
         }
       }
     }
@@ -505,14 +419,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int rr = f / (DH / 4), c4 = f % (DH / 4);
         reinterpret_cast<float4*>(ddOt + blk)[f] =
             *reinterpret_cast<const float4*>(st_o + rr * kStageLd + 4 * c4);
-        if (!JVP)
-          reinterpret_cast<float4*>(dQt + blk)[f] =
-              *reinterpret_cast<const float4*>(st_q + rr * kStageLd + 4 * c4);
+        reinterpret_cast<float4*>(dQt + blk)[f] =
+            *reinterpret_cast<const float4*>(st_q + rr * kStageLd + 4 * c4);
       }
     }
     if (ok && wg == 0 && gr < Nq) {
       alpha[rowvec] = al;
-      if (!JVP) E[rowvec] = Ei;
+      E[rowvec] = Ei;
     }
   }
 
@@ -529,28 +442,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 size_t tc_pass1_smem() { return sizeof(Smem1) + 1024; }
 
-cudaError_t tc_launch_jvp(const JvpArgs& a, const CUtensorMap* maps128,
-                          const CUtensorMap* maps32) {
-  // maps128: Q, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
-  const size_t smem = tc_pass1_smem();
-  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_kernel<true>), (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[0], maps128[1], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      nullptr, nullptr, a.Od, a.Ld, nullptr, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0,
-      a.err);
-  return cudaGetLastError();
-}
-
 cudaError_t tc_launch_pass1(const BobArgs& a, const CUtensorMap* maps128,
                             const CUtensorMap* maps32) {
   // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row boxes.
   const size_t smem = tc_pass1_smem();
-  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_kernel<false>), (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_kernel), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
+  tc_pass1_kernel<<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
       a.D, a.dQt, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau,
       a.causal ? 1 : 0, a.err);
