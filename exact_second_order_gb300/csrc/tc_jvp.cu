@@ -15,7 +15,7 @@
 //               tiles of 64 key rows through a 5-stage mbarrier ring;
 //   warp 1      TMEM allocator; one elected lane runs the MMA schedule;
 //   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: tiles 0, 2, 4, ... /
-//               1, 3, 5, ... (tile t in score buffer t mod 2).
+//               1, 3, 5, ... (tile t in score buffer t mod 3).
 // With no dP or G scores the JVP needs two scores per element, so its tiles
 // are 64 keys wide: the score GEMMs are Q [U_K; K]^T (N = 128, half of F'
 // and S) and U_Q K^T (N = 64), against N = 64 and N = 32 for 32-key tiles,
@@ -23,16 +23,14 @@
 // width.
 // TMEM (512 columns x 128 lanes):
 //   [0,64)      O'0 = (P o F) V + P U_V accumulator;
-//   [64,128)    bf16 A operands of buffer 0: P at 64 + 8c, P o F at 96 + 8c
-//               (K step c = keys 16c .. 16c + 15 of the tile);
-//   [128,192)   the same for buffer 1;
-//   [256,384)   score buffer 0: F' = Q U_K^T + U_Q K^T (64) | S = Q K^T (64);
-//   [384,512)   score buffer 1.
-// A warpgroup reads its buffer's F' | S into registers and releases it
-// before any arithmetic, so the score GEMMs of tile t + 2 run while it
-// forms tile t's operands; the output GEMMs of tile t are issued before
-// that commit, so its completion also tells the warpgroup of tile t + 2 that
-// the operand columns it is about to overwrite have been read.
+//   [128 + 128 b, 256 + 128 b)   score buffer b = 0, 1, 2: F' = Q U_K^T +
+//               U_Q K^T (64 columns) | S = Q K^T (64 columns).
+// A warpgroup reads the whole buffer into registers, then writes the bf16 A
+// operands of the output GEMMs over F': P at column 8c, P o F at 32 + 8c
+// (K step c = keys 16c .. 16c + 15 of the tile).  The score GEMMs of tile
+// t + 3 follow tile t's output GEMMs on the in-order tensor pipe, so they
+// overwrite the buffer only after its operands were read, and each
+// warpgroup finds its next tile (t + 2) scored before it gets there.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -61,9 +59,8 @@ struct SmemJ {
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
-  uint64_t sc_full[2];   // per buffer: the scores are in (and the buffer's operands were read)
-  uint64_t sf_free[2];   // per buffer: the warpgroup holds F' | S in registers (4 warps)
-  uint64_t op_ready[2];  // per buffer: the operands are in TMEM (4 warps)
+  uint64_t sc_full[3];   // per buffer: the scores are in
+  uint64_t op_ready[3];  // per buffer: the operands are in TMEM (4 warps)
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -71,16 +68,17 @@ struct SmemJ {
 static_assert(sizeof(SmemJ) + 1024 <= 232448, "shared memory");
 
 constexpr uint32_t kAccO = 0;
-__device__ __forceinline__ constexpr uint32_t op_base(int b) { return 64 + 64 * b; }
+constexpr int NB = 3;  // score buffers
+__device__ __forceinline__ constexpr uint32_t sc_base(int b) { return 128 + 128 * b; }
+constexpr uint32_t kColF = 0, kColS = 64;  // inside a score buffer
+// Operand slots inside a score buffer, over F' (read before they are written).
 __device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 8 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 32 + 8 * c; }
-__device__ __forceinline__ constexpr uint32_t sc_base(int b) { return 256 + 128 * b; }
-constexpr uint32_t kColF = 0, kColS = 64;  // inside a score buffer
 
 // 16 keys of a tile, one query row per thread: P = exp(S - L), P o F with
 // F = tau F', the row sum L' += P o F, and the two bf16 operands.
 template <bool MASKED>
-__device__ __forceinline__ void jvp_chunk(uint32_t ob, int c, const uint32_t (&s)[16],
+__device__ __forceinline__ void jvp_chunk(uint32_t buf, int c, const uint32_t (&s)[16],
                                           const uint32_t (&f)[16], int jbase, int jmax,
                                           float2 c12, float2 nL, float2 tau2, float2& a_acc) {
   uint32_t oP[8], oPF[8];
@@ -97,16 +95,15 @@ __device__ __forceinline__ void jvp_chunk(uint32_t ob, int c, const uint32_t (&s
     oP[e >> 1] = pack_bf16x2(p.x, p.y);
     oPF[e >> 1] = pack_bf16x2(pf.x, pf.y);
   }
-  tmem_st8(ob + slot_P(c), oP);
-  tmem_st8(ob + slot_PF(c), oPF);
+  tmem_st8(buf + slot_P(c), oP);
+  tmem_st8(buf + slot_PF(c), oPF);
 }
 
-// One 64-key tile: read all of F' and S, release the score buffer, then form
-// and store the operands chunk by chunk and hand them to the MMA issuer.
+// One 64-key tile: read all of F' and S, then form the operands chunk by
+// chunk, store them over F' and hand them to the MMA issuer.
 template <bool MASKED>
-__device__ __forceinline__ void jvp_tile(uint32_t sc, uint32_t ob, uint64_t* sf_free,
-                                         uint64_t* ready, int col0, int jmax, float c1,
-                                         float Lr2, float tau, float2& a_acc) {
+__device__ __forceinline__ void jvp_tile(uint32_t sc, uint64_t* ready, int col0, int jmax,
+                                         float c1, float Lr2, float tau, float2& a_acc) {
   uint32_t f0[16], f1[16], f2_[16], f3[16], s0[16], s1[16], s2[16], s3[16];
   tmem_ld16(sc + kColF, f0);
   tmem_ld16(sc + kColF + 16, f1);
@@ -117,14 +114,12 @@ __device__ __forceinline__ void jvp_tile(uint32_t sc, uint32_t ob, uint64_t* sf_
   tmem_ld16(sc + kColS + 32, s2);
   tmem_ld16(sc + kColS + 48, s3);
   tmem_wait_ld();
-  tc_fence_before();
-  warp_arrive(sf_free);  // F' | S may be overwritten by the scores of tile t + 2
   const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
   const float2 tau2 = make_float2(tau, tau);
-  jvp_chunk<MASKED>(ob, 0, s0, f0, col0, jmax, c12, nL, tau2, a_acc);
-  jvp_chunk<MASKED>(ob, 1, s1, f1, col0 + 16, jmax, c12, nL, tau2, a_acc);
-  jvp_chunk<MASKED>(ob, 2, s2, f2_, col0 + 32, jmax, c12, nL, tau2, a_acc);
-  jvp_chunk<MASKED>(ob, 3, s3, f3, col0 + 48, jmax, c12, nL, tau2, a_acc);
+  jvp_chunk<MASKED>(sc, 0, s0, f0, col0, jmax, c12, nL, tau2, a_acc);
+  jvp_chunk<MASKED>(sc, 1, s1, f1, col0 + 16, jmax, c12, nL, tau2, a_acc);
+  jvp_chunk<MASKED>(sc, 2, s2, f2_, col0 + 32, jmax, c12, nL, tau2, a_acc);
+  jvp_chunk<MASKED>(sc, 3, s3, f3, col0 + 48, jmax, c12, nL, tau2, a_acc);
   tmem_wait_st();
   tc_fence_before();
   warp_arrive(ready);
@@ -157,9 +152,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(&sm.sc_full[b], 1);
-      mbar_init(&sm.sf_free[b], 4);
       mbar_init(&sm.op_ready[b], 4);
     }
     mbar_init(&sm.out_full, 1);
@@ -217,7 +211,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dUV0 = smem_desc_sw128(kv0 + 3 * TILE_BYTES, 16, 1024); // U_V
     auto issue_scores = [&](int t) {
       const uint64_t so = (uint64_t)((t % NST) * 4 * TILE_BYTES) >> 4;
-      const uint32_t sc = tbase + sc_base(t & 1);
+      const uint32_t sc = tbase + sc_base(t % NB);
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk) {
         const uint64_t o = 2 * kk;  // 32 bytes >> 4
@@ -228,7 +222,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto issue_outputs = [&](int t) {
       const int s = t % NST;
       const uint64_t so = (uint64_t)(s * 4 * TILE_BYTES) >> 4;
-      const uint32_t ob = tbase + op_base(t & 1);
+      const uint32_t ob = tbase + sc_base(t % NB);
 #pragma unroll
       for (int c = 0; c < BN / 16; ++c) {
         const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
@@ -242,7 +236,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (elect_one()) {
       bool ok = mbar_wait(&sm.bar_q, 0, abort_flag, err);
       tc_fence_after();
-      for (int t = 0; ok && t < 2 && t < T; ++t) {
+      for (int t = 0; ok && t < NB && t < T; ++t) {
         ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
         tc_fence_after();
         if (ok) {
@@ -251,21 +245,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       for (int t = 0; ok && t < T; ++t) {
-        const uint32_t ph = (t >> 1) & 1;  // phase of this buffer's barriers
-        if (t + 2 < T) {  // the warpgroup holds tile t in registers: scores of t + 2
-          ok = mbar_wait(&sm.sf_free[t & 1], ph, abort_flag, err) &&
-               mbar_wait(&sm.kv_full[(t + 2) % NST], ((t + 2) / NST) & 1, abort_flag, err);
-          if (!ok) break;
-          tc_fence_after();
-          issue_scores(t + 2);
-        }
-        ok = mbar_wait(&sm.op_ready[t & 1], ph, abort_flag, err);
+        ok = mbar_wait(&sm.op_ready[t % NB], (t / NB) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t);
-        // After tile t's output GEMMs: the warpgroup of tile t + 2 may then
-        // also overwrite the buffer's operand columns.
-        if (t + 2 < T) mma_commit(&sm.sc_full[t & 1]);
+        if (t + NB < T) {  // tile t + 3 reuses tile t's buffer, after its output GEMMs
+          ok = mbar_wait(&sm.kv_full[(t + NB) % NST], ((t + NB) / NST) & 1, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + NB);
+          mma_commit(&sm.sc_full[t % NB]);
+        }
       }
       mma_commit(&sm.out_full);  // every MMA issued above has finished
     }
@@ -280,16 +270,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
-    const uint32_t sc = tbase + lane_off + sc_base(wg);
-    const uint32_t ob = tbase + lane_off + op_base(wg);
     float2 a_acc = make_float2(0.f, 0.f);
     bool ok = true;
 
     for (int u = 0;; ++u) {
       const int t = 2 * u + wg;
       if (t >= T) break;
+      const int b = t % NB;
+      const uint32_t sc = tbase + lane_off + sc_base(b);
       // tcgen05.ld/st are warp-collective: take the decision warp-uniformly.
-      ok = mbar_wait_warp(&sm.sc_full[wg], u & 1, abort_flag, err);
+      ok = mbar_wait_warp(&sm.sc_full[b], (t / NB) & 1, abort_flag, err);
       if (!ok) break;
       tc_fence_after();
       const int col0 = t * BN;
@@ -298,11 +288,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
       const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
       if (masked)
-        jvp_tile<true>(sc, ob, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, tau,
-                       a_acc);
+        jvp_tile<true>(sc, &sm.op_ready[b], col0, jmax, c1, Lr2, tau, a_acc);
       else
-        jvp_tile<false>(sc, ob, &sm.sf_free[wg], &sm.op_ready[wg], col0, jmax, c1, Lr2, tau,
-                        a_acc);
+        jvp_tile<false>(sc, &sm.op_ready[b], col0, jmax, c1, Lr2, tau, a_acc);
     }
 
     // Epilogue: L' = the two warpgroups' row sums; warpgroup wg forms output
