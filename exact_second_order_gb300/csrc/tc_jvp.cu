@@ -25,9 +25,9 @@
 //   [0,64)      O'0 = (P o F) V + P U_V accumulator;
 //   [128 + 128 b, 256 + 128 b)   score buffer b = 0, 1, 2: F' = Q U_K^T +
 //               U_Q K^T (64 columns) | S = Q K^T (64 columns).
-// A warpgroup reads the whole buffer into registers, then writes the bf16 A
-// operands of the output GEMMs over F': P at column 8c, P o F at 32 + 8c
-// (K step c = keys 16c .. 16c + 15 of the tile).  The score GEMMs of tile
+// A warpgroup reads the buffer into registers and writes the bf16 A
+// operands of the output GEMMs over F': K step c (keys 16c .. 16c + 15 of the
+// tile) has P at column 16c and P o F at 16c + 8, over those keys' F'.  The score GEMMs of tile
 // t + 3 follow tile t's output GEMMs on the in-order tensor pipe, so they
 // overwrite the buffer only after its operands were read, and each
 // warpgroup finds its next tile (t + 2) scored before it gets there.
@@ -71,9 +71,10 @@ constexpr uint32_t kAccO = 0;
 constexpr int NB = 3;  // score buffers
 __device__ __forceinline__ constexpr uint32_t sc_base(int b) { return 128 + 128 * b; }
 constexpr uint32_t kColF = 0, kColS = 64;  // inside a score buffer
-// Operand slots inside a score buffer, over F' (read before they are written).
-__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 8 * c; }
-__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 32 + 8 * c; }
+// Operand slots inside a score buffer: K step c over the F' columns of the
+// same 16 keys (16c .. 16c + 15), which its warpgroup has read by then.
+__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return 16 * c; }
+__device__ __forceinline__ constexpr uint32_t slot_PF(int c) { return 16 * c + 8; }
 
 // 16 keys of a tile, one query row per thread: P = exp(S - L), P o F with
 // F = tau F', the row sum L' += P o F, and the two bf16 operands.
@@ -99,25 +100,28 @@ __device__ __forceinline__ void jvp_chunk(uint32_t buf, int c, const uint32_t (&
   tmem_st8(buf + slot_PF(c), oPF);
 }
 
-// One 64-key tile: read all of F' and S, then form the operands chunk by
-// chunk, store them over F' and hand them to the MMA issuer.
+// One 64-key tile: read the first 32 keys' F' and S, start reading the
+// other 32 and form the first half's operands meanwhile (each stored over
+// the F' columns of its own keys, already read), then the second half; hand
+// the operands to the MMA issuer.
 template <bool MASKED>
 __device__ __forceinline__ void jvp_tile(uint32_t sc, uint64_t* ready, int col0, int jmax,
                                          float c1, float Lr2, float tau, float2& a_acc) {
   uint32_t f0[16], f1[16], f2_[16], f3[16], s0[16], s1[16], s2[16], s3[16];
   tmem_ld16(sc + kColF, f0);
-  tmem_ld16(sc + kColF + 16, f1);
-  tmem_ld16(sc + kColF + 32, f2_);
-  tmem_ld16(sc + kColF + 48, f3);
   tmem_ld16(sc + kColS, s0);
+  tmem_ld16(sc + kColF + 16, f1);
   tmem_ld16(sc + kColS + 16, s1);
-  tmem_ld16(sc + kColS + 32, s2);
-  tmem_ld16(sc + kColS + 48, s3);
   tmem_wait_ld();
+  tmem_ld16(sc + kColF + 32, f2_);
+  tmem_ld16(sc + kColS + 32, s2);
+  tmem_ld16(sc + kColF + 48, f3);
+  tmem_ld16(sc + kColS + 48, s3);
   const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
   const float2 tau2 = make_float2(tau, tau);
   jvp_chunk<MASKED>(sc, 0, s0, f0, col0, jmax, c12, nL, tau2, a_acc);
   jvp_chunk<MASKED>(sc, 1, s1, f1, col0 + 16, jmax, c12, nL, tau2, a_acc);
+  tmem_wait_ld();
   jvp_chunk<MASKED>(sc, 2, s2, f2_, col0 + 32, jmax, c12, nL, tau2, a_acc);
   jvp_chunk<MASKED>(sc, 3, s3, f3, col0 + 48, jmax, c12, nL, tau2, a_acc);
   tmem_wait_st();
