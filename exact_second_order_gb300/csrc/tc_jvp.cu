@@ -100,29 +100,30 @@ __device__ __forceinline__ void jvp_chunk(uint32_t buf, int c, const uint32_t (&
   tmem_st8(buf + slot_PF(c), oPF);
 }
 
-// One 64-key tile: read the first 32 keys' F' and S, start reading the
-// other 32 and form the first half's operands meanwhile (each stored over
-// the F' columns of its own keys, already read), then the second half; hand
-// the operands to the MMA issuer.
+// One 64-key tile, 16 keys at a time: while a chunk's operands are formed
+// (and stored over the F' columns of its own keys, already read), the next
+// chunk's F' and S are being read; then hand the operands to the MMA issuer.
 template <bool MASKED>
 __device__ __forceinline__ void jvp_tile(uint32_t sc, uint64_t* ready, int col0, int jmax,
                                          float c1, float Lr2, float tau, float2& a_acc) {
   uint32_t f0[16], f1[16], f2_[16], f3[16], s0[16], s1[16], s2[16], s3[16];
+  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
+  const float2 tau2 = make_float2(tau, tau);
   tmem_ld16(sc + kColF, f0);
   tmem_ld16(sc + kColS, s0);
+  tmem_wait_ld();
   tmem_ld16(sc + kColF + 16, f1);
   tmem_ld16(sc + kColS + 16, s1);
+  jvp_chunk<MASKED>(sc, 0, s0, f0, col0, jmax, c12, nL, tau2, a_acc);
   tmem_wait_ld();
   tmem_ld16(sc + kColF + 32, f2_);
   tmem_ld16(sc + kColS + 32, s2);
-  tmem_ld16(sc + kColF + 48, f3);
-  tmem_ld16(sc + kColS + 48, s3);
-  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
-  const float2 tau2 = make_float2(tau, tau);
-  jvp_chunk<MASKED>(sc, 0, s0, f0, col0, jmax, c12, nL, tau2, a_acc);
   jvp_chunk<MASKED>(sc, 1, s1, f1, col0 + 16, jmax, c12, nL, tau2, a_acc);
   tmem_wait_ld();
+  tmem_ld16(sc + kColF + 48, f3);
+  tmem_ld16(sc + kColS + 48, s3);
   jvp_chunk<MASKED>(sc, 2, s2, f2_, col0 + 32, jmax, c12, nL, tau2, a_acc);
+  tmem_wait_ld();
   jvp_chunk<MASKED>(sc, 3, s3, f3, col0 + 48, jmax, c12, nL, tau2, a_acc);
   tmem_wait_st();
   tc_fence_before();
