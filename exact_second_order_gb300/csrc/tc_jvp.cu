@@ -10,12 +10,12 @@
 // This is the row pass of "FlashBoB" (paper notes, 关键设计 1/2) with dO = 0:
 // its alpha is L' and its d~dO is O'.
 //
-// CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
+// CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 448 threads:
 //   warp 0      TMA producer: the Q and U_Q blocks once, then U_K, K, V, U_V
 //               tiles of 64 key rows through a 5-stage mbarrier ring;
 //   warp 1      TMEM allocator; one elected lane runs the MMA schedule;
-//   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: tiles 0, 2, 4, ... /
-//               1, 3, 5, ... (tile t in score buffer t mod 3).
+//   warps 2-5 / 6-9 / 10-13   elementwise warpgroups 0 / 1 / 2: warpgroup
+//               w takes the tiles t = w mod 3, in score buffer w.
 // With no dP or G scores the JVP needs two scores per element, so its tiles
 // are 64 keys wide: the score GEMMs are Q [U_K; K]^T (N = 128, half of F'
 // and S) and U_Q K^T (N = 64), against N = 64 and N = 32 for 32-key tiles,
@@ -30,7 +30,7 @@
 // tile) has P at column 16c and P o F at 16c + 8, over those keys' F'.  The score GEMMs of tile
 // t + 3 follow tile t's output GEMMs on the in-order tensor pipe, so they
 // overwrite the buffer only after its operands were read, and each
-// warpgroup finds its next tile (t + 2) scored before it gets there.
+// warpgroup has three tiles' worth of MMA time for each of its tiles.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -42,7 +42,8 @@ constexpr int BM = kTcRows;   // 128 query rows per CTA
 constexpr int BN = kTcJvpStream;  // 64 key rows per streamed tile
 constexpr int DH = 64;        // head dim
 constexpr int NST = 5;        // stages of the U_K/K/V/U_V ring
-constexpr int NTHREADS = 320;
+constexpr int NWG = 3;  // elementwise warpgroups, one per score buffer
+constexpr int NTHREADS = 64 + 128 * NWG;
 constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
 constexpr uint32_t TILE_BYTES = BN * DH * 2;   // 8 KiB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,7 +56,7 @@ struct SmemJ {
   alignas(1024) uint8_t q[BLOCK_BYTES];
   alignas(1024) uint8_t uq[BLOCK_BYTES];
   alignas(1024) uint8_t kv[NST][4][TILE_BYTES];  // U_K, K, V, U_V (U_K | K adjacent)
-  float part_a[2][BM];                           // L' partial sums of the two warpgroups
+  float part_a[NWG][BM];                         // L' partial sums of the warpgroups
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   } else {
     // ---------------- elementwise warpgroups + epilogue ----------------
-    const int wg = (warp - 2) >> 2;      // 0 or 1
+    const int wg = (warp - 2) >> 2;      // 0 .. NWG - 1
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;      // row inside the block = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool ok = true;
 
     for (int u = 0;; ++u) {
-      const int t = 2 * u + wg;
+      const int t = NWG * u + wg;  // in buffer t mod 3 = wg
       if (t >= T) break;
       const int b = t % NB;
       const uint32_t sc = tbase + lane_off + sc_base(b);
@@ -298,11 +299,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         jvp_tile<false>(sc, &sm.op_ready[b], col0, jmax, c1, Lr2, tau, a_acc);
     }
 
-    // Epilogue: L' = the two warpgroups' row sums; warpgroup wg forms output
-    // columns [32 wg, 32 wg + 32) of O' = O'0 - L' O.
+    // Epilogue: L' = the warpgroups' row sums; warpgroup wg forms the 16-column
+    // chunks h = wg, wg + 3 of O' = O'0 - L' O.
     sm.part_a[wg][r] = a_acc.x + a_acc.y;
-    named_bar_sync(1, 256);
-    const float lp = sm.part_a[0][r] + sm.part_a[1][r];
+    named_bar_sync(1, 128 * NWG);
+    float lp = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWG; ++w) lp += sm.part_a[w][r];
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
@@ -311,18 +314,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // through shared memory with coalesced loads, each thread forms its
     // row's O' there in place, and the tile leaves with coalesced stores.
     float* st_o = reinterpret_cast<float*>(&sm.kv[0][0][0]);
-    const int tid = threadIdx.x - 64;  // 0 .. 255
+    const int tid = threadIdx.x - 64;  // 0 .. 128 NWG - 1
     const int rows = min(BM, Nq - row0);
     const size_t blk = (static_cast<size_t>(bh) * Nq + row0) * DH;
-    for (int f = tid; f < rows * (DH / 4); f += 256) {
+    for (int f = tid; f < rows * (DH / 4); f += 128 * NWG) {
       const int rr = f / (DH / 4), c4 = f % (DH / 4);
       *reinterpret_cast<float4*>(st_o + rr * kStageLd + 4 * c4) =
           reinterpret_cast<const float4*>(O + blk)[f];
     }
-    named_bar_sync(1, 256);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = 32 * wg + 16 * h;
+    named_bar_sync(1, 128 * NWG);
+    for (int h = wg; h < DH / 16; h += NWG) {
+      const int col = 16 * h;
       uint32_t vo[16];
       tmem_ld16(acc_base + kAccO + col, vo);
       tmem_wait_ld();
@@ -336,9 +338,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    named_bar_sync(1, 256);
+    named_bar_sync(1, 128 * NWG);
     if (ok) {
-      for (int f = tid; f < rows * (DH / 4); f += 256) {
+      for (int f = tid; f < rows * (DH / 4); f += 128 * NWG) {
         const int rr = f / (DH / 4), c4 = f % (DH / 4);
         reinterpret_cast<float4*>(Od + blk)[f] =
             *reinterpret_cast<const float4*>(st_o + rr * kStageLd + 4 * c4);
