@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libflashbob.so")
 SOURCES = ["flashbob_api.cu", "simt.cu", "tc_host.cu", "tc_pass1.cu", "tc_pass2.cu", "tc_prep.cu",
-           "tc_pass1_d128.cu", "tc_pass2_d128.cu", "tc_jvp.cu", "selftest.cu"]
+           "tc_pass1_d128.cu", "tc_pass2_d128.cu", "tc_jvp.cu", "tc_jvp_d128.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(os.path.dirname(HERE), "include")]

@@ -18,7 +18,9 @@ cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
 cudaError_t tc_launch_pass2_d128(const BobArgs& a, const CUtensorMap* maps128,
                                  const CUtensorMap* maps32);
 cudaError_t tc_launch_jvp_d128(const JvpArgs& a, const CUtensorMap* maps128,
-                               const CUtensorMap* maps32);
+                               const CUtensorMap* maps64);
+cudaError_t tc_launch_pass1_d128_jvp(const BobArgs& a, const CUtensorMap* maps128,
+                                     const CUtensorMap* maps64);
 
 bool tc_supported(const BobArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
@@ -159,20 +161,26 @@ cudaError_t tc_pass2_split(const void* split_kernel, size_t smem, int blocks, in
 
 namespace {
 
-// Head dim 128: both passes stream 32-row tiles against 128-row blocks.
+// Head dim 128: pass 1 is the JVP launch (64-row key tiles) and the rows
+// launch (32-row key tiles), pass 2 streams 32-row query tiles; every block
+// holds 128 rows.
 cudaError_t tc_bob_d128(const BobArgs& a) {
   const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
   cudaError_t e = cudaSuccess;
   if (a.passes & kPass1) {
-    CUtensorMap m128[3], m32[4];
+    CUtensorMap m128[3], m32[4], m64[4];
     const void* rows[3] = {a.Q, a.dO, a.UQ};
     const void* cols[4] = {a.K, a.V, a.UK, a.UV};
     for (int i = 0; i < 3 && e == cudaSuccess; ++i)
       e = tc_map_bf16(&m128[i], rows[i], BH, a.Nq, kTcRows, 128);
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
       e = tc_map_bf16(&m32[i], cols[i], BHkv, a.Nk, kTcStream, 128);
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = tc_map_bf16(&m64[i], cols[i], BHkv, a.Nk, kTcJvpStream, 128);
     if (e != cudaSuccess) return e;
-    e = tc_launch_pass1_d128(a, m128, m32);
+    const CUtensorMap mqu[2] = {m128[0], m128[2]};  // Q, U_Q
+    e = tc_launch_pass1_d128_jvp(a, mqu, m64);      // alpha, d~dO and E
+    if (e == cudaSuccess) e = tc_launch_pass1_d128(a, m128, m32);  // d~Q
     if (e != cudaSuccess) return e;
   }
   if (a.passes & kPass2) {
@@ -375,9 +383,7 @@ cudaError_t tc_bob(const BobArgs& a) {
 bool tc_jvp_supported(const JvpArgs& a) { return a.bf16 && (a.d == 64 || a.d == 128); }
 
 cudaError_t tc_jvp(const JvpArgs& a) {
-  // Key tiles of 32 rows at d = 128, 64 rows at d = 64 (the d = 64 JVP
-  // kernel streams 64 keys per tile).
-  const int key_rows = a.d == 128 ? kTcStream : kTcJvpStream;
+  const int key_rows = kTcJvpStream;  // both JVP kernels stream 64-row key tiles
   CUtensorMap m128[2], mk[4];
   const void* rows[2] = {a.Q, a.UQ};
   const void* cols[4] = {a.K, a.V, a.UK, a.UV};

@@ -522,42 +522,17 @@ size_t tc_pass1_d128_smem() { return sizeof(SmemW1) + 1024; }
 
 cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
                                  const CUtensorMap* maps32) {
-  // maps128: Q, dO, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
-  // boxes; every box is 64 columns wide (one half of a 128-column row).
-  // Launch 1, the JVP: alpha, d~dO and E; launch 2, the rows pass: d~Q.
+  // The rows launch of the d = 128 pass 1 (the JVP launch before it has
+  // written alpha and E): d~Q.  maps128: Q, dO, U_Q with 128-row boxes;
+  // maps32: K, V, U_K, U_V with 32-row boxes; every box is 64 columns wide
+  // (one half of a 128-column row).
   const size_t smem = tc_pass1_d128_smem();
-  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<true>), (int)smem);
-  if (e == cudaSuccess)
-    e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<false>), (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<false>), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_d128_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      a.D, nullptr, a.ddOt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   tc_pass1_d128_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
       maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
       a.D, a.dQt, nullptr, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
-  return cudaGetLastError();
-}
-
-}  // namespace flashbob
-
-namespace flashbob {
-
-cudaError_t tc_launch_jvp_d128(const JvpArgs& a, const CUtensorMap* maps128,
-                               const CUtensorMap* maps32) {
-  // maps128: Q, U_Q with 128-row boxes; maps32: K, V, U_K, U_V with 32-row
-  // boxes (64-column halves).
-  const size_t smem = tc_pass1_d128_smem();
-  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<true>), (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_d128_kernel<true><<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[0], maps128[1], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      nullptr, nullptr, a.Od, a.Ld, nullptr, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0,
-      a.err);
   return cudaGetLastError();
 }
 
