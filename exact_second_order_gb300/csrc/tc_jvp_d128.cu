@@ -13,9 +13,11 @@
 //
 // CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 320 threads:
 //   warp 0      TMA producer: the Q and U_Q blocks once (two 64-column halves
-//               each), then U_K, K, V, U_V tiles of 64 key rows through a
-//               3-stage ring whose third stage is the Q | U_Q block, free once
-//               the elementwise warps have copied Q and U_Q into TMEM;
+//               each), then tiles of 64 key rows through two 3-stage rings,
+//               one of U_K | K (read by the score GEMMs, free once they have
+//               completed) and one of V | U_V (read by the output GEMMs), whose
+//               third stages are the Q | U_Q block, free once the elementwise
+//               warps have copied Q and U_Q into TMEM;
 //   warp 1      TMEM allocator; one elected lane runs the MMA schedule;
 //   warps 2-5 / 6-9   elementwise warpgroups 0 / 1: tiles t = w mod 2, in
 //               score buffer w.
@@ -42,12 +44,12 @@ using namespace tc;
 constexpr int BM = kTcRows;       // 128 query rows per CTA
 constexpr int BN = kTcJvpStream;  // 64 key rows per streamed tile
 constexpr int DH = 128;
-constexpr int NST = 3;  // ring stages; stage 2 is the Q | U_Q block
+constexpr int NST = 3;  // stages of each ring; stage 2 lies in the Q | U_Q block
 constexpr int NWG = 2;  // elementwise warpgroups = score buffers
 constexpr int NTHREADS = 64 + 128 * NWG;
 constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB: 128 rows x 64 columns
 constexpr uint32_t HALF_TILE = BN * 64 * 2;   // 8 KiB: 64 rows x 64 columns
-constexpr uint32_t STAGE_BYTES = 2 * 4 * HALF_TILE;  // [half][U_K, K, V, U_V]
+constexpr uint32_t STAGE_BYTES = 2 * 2 * HALF_TILE;  // [half][U_K, K] or [half][V, U_V]
 constexpr float kLog2e = 1.4426950408889634f;
 // Epilogue staging in the idle ring: O (then O') as fp32 rows padded to 132
 // floats, and, for E, dO as bf16 rows padded to 136 elements.
@@ -55,24 +57,26 @@ constexpr int kStageLd = DH + 4;
 constexpr int kDoLd = DH + 8;
 
 struct SmemJ2 {
-  alignas(1024) uint8_t kv[2][STAGE_BYTES];        // ring stages 0 and 1
-  alignas(1024) uint8_t qu[2][2][HALF_BLOCK];      // [Q, U_Q][half]; then ring stage 2
+  alignas(1024) uint8_t kv[2][2][STAGE_BYTES];     // [U_K | K ring, V | U_V ring][stage 0, 1]
+  alignas(1024) uint8_t qu[2][2][HALF_BLOCK];      // [Q, U_Q][half]; then stage 2 of each ring
   float part_a[NWG][BM];  // L' partial sums of the warpgroups
   float part_e[NWG][BM];  // dO . O' partial sums
   uint64_t bar_q;
   uint64_t a_ready;  // Q and U_Q are in TMEM (8 warps)
-  uint64_t kv_full[NST];
-  uint64_t kv_empty[NST];
+  uint64_t k_full[NST];   // U_K | K ring
+  uint64_t k_empty[NST];
+  uint64_t v_full[NST];   // V | U_V ring
+  uint64_t v_empty[NST];
   uint64_t sc_full[NWG];
   uint64_t op_ready[NWG];  // 4 warps
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(SmemJ2::qu) == STAGE_BYTES, "the Q | U_Q block is one ring stage");
+static_assert(sizeof(SmemJ2::qu) == 2 * STAGE_BYTES, "the Q | U_Q block holds stage 2 of both rings");
 static_assert(sizeof(SmemJ2) + 1024 <= 232448, "shared memory");
 static_assert(BM * kStageLd * 4 + BM * kDoLd * 2 <= sizeof(SmemJ2::kv),
-              "epilogue staging fits in ring stages 0 and 1");
+              "epilogue staging fits in stages 0 and 1 of the rings");
 
 constexpr uint32_t kAccO = 0;
 constexpr uint32_t kQA = 128, kUQA = 192;
@@ -164,8 +168,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&sm.bar_q, 1);
     mbar_init(&sm.a_ready, 8);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int b = 0; b < NWG; ++b) {
       mbar_init(&sm.sc_full[b], 1);
@@ -194,56 +200,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mUK);
       tma_prefetch_desc(&mUV);
-      const CUtensorMap* maps[4] = {&mUK, &mK, &mV, &mUV};
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
+      // Stage s of ring r (0: U_K | K, 1: V | U_V): half h of its first / second
+      // tensor at (2 h + 0 / 1) HALF_TILE.
+      auto stage = [&](int r, int s) -> uint8_t* {
+        return s < 2 ? sm.kv[r][s] : sm.qu[r][0];
+      };
+      // The U_K | K tile of key tile t, then the V | U_V tile of tile t - 1:
+      // the score GEMMs of tile t free their stage before the output GEMMs
+      // of tile t - 1 free theirs.
+      auto load = [&](int r, int t) -> bool {
         const int s = t % NST;
+        uint64_t* full = r == 0 ? &sm.k_full[s] : &sm.v_full[s];
+        uint64_t* empty = r == 0 ? &sm.k_empty[s] : &sm.v_empty[s];
         if (t >= NST) {
-          if (!mbar_wait(&sm.kv_empty[s], ((t / NST) - 1) & 1, abort_flag, err)) break;
+          if (!mbar_wait(empty, ((t / NST) - 1) & 1, abort_flag, err)) return false;
         } else if (s == 2 && !mbar_wait(&sm.a_ready, 0, abort_flag, err)) {
-          break;  // stage 2 is the Q | U_Q block: wait until it has been copied out
+          return false;  // stage 2 is in the Q | U_Q block: wait until it was copied out
         }
-        uint8_t* base = s < 2 ? sm.kv[s] : &sm.qu[0][0][0];
-        mbar_expect_tx(&sm.kv_full[s], STAGE_BYTES);
-        for (int h = 0; h < 2; ++h)
-          for (int i = 0; i < 4; ++i)
-            tma_load_3d(base + (4 * h + i) * HALF_TILE, maps[i], &sm.kv_full[s], 64 * h,
-                        t * BN, bkv);
-        issued = t + 1;
+        const CUtensorMap* m0 = r == 0 ? &mUK : &mV;
+        const CUtensorMap* m1 = r == 0 ? &mK : &mUV;
+        uint8_t* base = stage(r, s);
+        mbar_expect_tx(full, STAGE_BYTES);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(base + (2 * h) * HALF_TILE, m0, full, 64 * h, t * BN, bkv);
+          tma_load_3d(base + (2 * h + 1) * HALF_TILE, m1, full, 64 * h, t * BN, bkv);
+        }
+        return true;
+      };
+      int issued_k = 0, issued_v = 0;
+      for (int t = 0; t <= T; ++t) {
+        if (t < T) {
+          if (!load(0, t)) break;
+          issued_k = t + 1;
+        }
+        if (t >= 1) {
+          if (!load(1, t - 1)) break;
+          issued_v = t;
+        }
       }
       // No copy may still be in flight when the CTA exits.
       drain_wait(&sm.bar_q, 0);
-      for (int t = issued > NST ? issued - NST : 0; t < issued; ++t)
-        drain_wait(&sm.kv_full[t % NST], (t / NST) & 1);
+      for (int t = issued_k > NST ? issued_k - NST : 0; t < issued_k; ++t)
+        drain_wait(&sm.k_full[t % NST], (t / NST) & 1);
+      for (int t = issued_v > NST ? issued_v - NST : 0; t < issued_v; ++t)
+        drain_wait(&sm.v_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
     constexpr uint32_t idS128 = idesc_bf16(BM, 2 * BN, false);  // N = 128, B K-major
     constexpr uint32_t idS64 = idesc_bf16(BM, BN, false);       // N = 64, B K-major
     constexpr uint32_t idO128 = idesc_bf16(BM, DH, true);       // N = 128, B MN-major
-    const uint32_t stage_addr[NST] = {smem_u32(sm.kv[0]), smem_u32(sm.kv[1]),
-                                      smem_u32(&sm.qu[0][0][0])};
-    // Inside a stage, tensor i of half h sits at (4 h + i) HALF_TILE; a K
-    // step of the score GEMMs adds 32 bytes inside the swizzled row (and
-    // moves to half 1 after 4 steps), one of the output GEMMs 16 key rows
-    // (2 KiB); descriptor start addresses are in 16-byte units.
+    auto stage_addr = [&](int r, int s) -> uint32_t {
+      return smem_u32(s < 2 ? sm.kv[r][s] : sm.qu[r][0]);
+    };
+    // Inside a stage, half h of the first / second tensor sits at
+    // (2 h + 0 / 1) HALF_TILE; a K step of the score GEMMs adds 32 bytes
+    // inside the swizzled row (and moves to half 1 after 4 steps), one of the
+    // output GEMMs 16 key rows (2 KiB); descriptor start addresses are in
+    // 16-byte units.
     auto issue_scores = [&](int t) {
-      const uint64_t d0 = smem_desc_sw128(stage_addr[t % NST], 16, 1024);  // U_K, half 0
+      const uint64_t d0 = smem_desc_sw128(stage_addr(0, t % NST), 16, 1024);  // U_K, half 0
       const uint32_t sc = tbase + sc_base(t & 1);
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk) {
-        const uint64_t dUK = d0 + ((kk >> 2) * 4 * HALF_TILE >> 4) + 2 * (kk & 3);
+        const uint64_t dUK = d0 + ((kk >> 2) * 2 * HALF_TILE >> 4) + 2 * (kk & 3);
         const uint64_t dK = dUK + (HALF_TILE >> 4);
         mma_ts(sc + kColF, tbase + kQA + 8 * kk, dUK, idS128, kk > 0);  // [F' | S] = Q [U_K; K]^T
         mma_ts(sc + kColF, tbase + kUQA + 8 * kk, dK, idS64, 1);        // F' += U_Q K^T
       }
+      mma_commit(&sm.k_empty[t % NST]);
     };
     auto issue_outputs = [&](int t) {
       const int s = t % NST;
-      // MN-major N = 128 operands: columns 64..127 (half 1) sit one half
-      // (4 tiles) after columns 0..63 of the same tensor.
-      const uint64_t dVmn = smem_desc_sw128(stage_addr[s] + 2 * HALF_TILE, 4 * HALF_TILE, 1024);
-      const uint64_t dUVmn = smem_desc_sw128(stage_addr[s] + 3 * HALF_TILE, 4 * HALF_TILE, 1024);
+      // MN-major N = 128 operands: columns 64..127 (half 1) sit two tiles
+      // after columns 0..63 of the same tensor.
+      const uint32_t vb = stage_addr(1, s);
+      const uint64_t dVmn = smem_desc_sw128(vb, 2 * HALF_TILE, 1024);
+      const uint64_t dUVmn = smem_desc_sw128(vb + HALF_TILE, 2 * HALF_TILE, 1024);
       const uint32_t sc = tbase + sc_base(t & 1);
 #pragma unroll
       for (int c = 0; c < BN / 16; ++c) {
@@ -252,14 +285,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_ts(tbase + kAccO, sc + slot_P(c), dUVmn + o, idO128, acc);  // O'0 += P U_V
         mma_ts(tbase + kAccO, sc + slot_PF(c), dVmn + o, idO128, 1);    //     + (P o F) V
       }
-      mma_commit(&sm.kv_empty[s]);
+      mma_commit(&sm.v_empty[s]);
     };
     // One elected lane runs the whole schedule: every wait and every MMA.
     if (elect_one()) {
       bool ok = mbar_wait(&sm.a_ready, 0, abort_flag, err);
       tc_fence_after();
       for (int t = 0; ok && t < NWG && t < T; ++t) {
-        ok = mbar_wait(&sm.kv_full[t % NST], (t / NST) & 1, abort_flag, err);
+        ok = mbar_wait(&sm.k_full[t % NST], (t / NST) & 1, abort_flag, err);
         tc_fence_after();
         if (ok) {
           issue_scores(t);
@@ -267,12 +300,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       for (int t = 0; ok && t < T; ++t) {
-        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err);
+        ok = mbar_wait(&sm.op_ready[t & 1], (t >> 1) & 1, abort_flag, err) &&
+             mbar_wait(&sm.v_full[t % NST], (t / NST) & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         issue_outputs(t);
         if (t + NWG < T) {  // tile t + 2 reuses tile t's buffer, after its output GEMMs
-          ok = mbar_wait(&sm.kv_full[(t + NWG) % NST], ((t + NWG) / NST) & 1, abort_flag, err);
+          ok = mbar_wait(&sm.k_full[(t + NWG) % NST], ((t + NWG) / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           issue_scores(t + NWG);
@@ -350,7 +384,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
     const uint32_t acc_base = tbase + lane_off;
-    float* st_o = reinterpret_cast<float*>(sm.kv[0]);
+    float* st_o = reinterpret_cast<float*>(&sm.kv[0][0][0]);
     __nv_bfloat16* st_do = reinterpret_cast<__nv_bfloat16*>(st_o + BM * kStageLd);
     const int tid = threadIdx.x - 64;  // 0 .. 128 NWG - 1
     const int rows = min(BM, Nq - row0);
