@@ -1,43 +1,34 @@
 // Pass 1 of the exact attention backward-over-backward on sm_103a tensor
-// cores for head dim 128 (bf16 inputs, fp32 accumulation in tensor memory).
+// cores for head dim 128 (bf16 inputs, fp32 accumulation in tensor memory):
+// its second launch, the rows pass.
 //
 // "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
 // Attention" (paper notes), 关键设计 2: a block of 128 query rows stays on
 // chip while key/value tiles stream past and every output row is written
 // once.  At d = 128 the four alpha-free accumulators of 关键设计 1 (B, R,
 // Omega, d~dO0, 128 fp32 columns each) would fill all 512 TMEM columns, so
-// the pass takes another exact route in two launches of this kernel:
-//   1. the attention JVP along (U_Q, U_K, U_V) (instance JVP = true): scores
-//      S and F' only, alpha = L' = sum_j P F and O' = P U_V + (P o F) V -
-//      alpha O, which is exactly d~dO (关键设计 1: d~dO0 - alpha O).  With dO
-//      and D given it also writes the second row scalar in closed form,
-//          E_i = sum_j P_ij d~P_ij = dO_i . d~dO_i - alpha_i D_i,
-//      which follows from d~P = F o (dP - D) + G - alpha dP with dP = dO V^T,
-//      G = dO U_V^T and D = dO . O (the row-dot form of E, as D is the
-//      row-dot form of sum_j P dP);
-//   2. the rows pass (instance JVP = false): with alpha and E known per row,
-//      d~S = P o (d~P0 - alpha dP - E) and dS = P o (dP - D) are final and
-//      d~Q = tau (d~S K + dS U_K) accumulates directly in one 128-column
-//      accumulator.
+// the pass takes another exact route in two launches:
+//   1. the attention JVP along (U_Q, U_K, U_V) with E (tc_jvp_d128.cu):
+//      alpha = L', d~dO = O' and E = dO . d~dO - alpha D;
+//   2. this kernel: with alpha and E known per row, d~S = P o (d~P0 -
+//      alpha dP - E) and dS = P o (dP - D) are final and d~Q = tau (d~S K +
+//      dS U_K) accumulates directly in one 128-column accumulator.
 // GEMMs per key: 5 (JVP) + 7 (rows: S, F' twice, dP, G, and two output
 // GEMMs) = 12 instead of the one-phase form's 11; the benchmark's FLOP
 // convention still counts 11.
 //
-// CTA = 128 query rows, 320 threads: warp 0 TMA (Q, U_Q and, where used, dO
-// once; K, U_K, V, U_V tiles of 32 key rows through a 4-slot ring, each
-// tensor as two 64-column halves in the 128-byte swizzle), warp 1 TMEM
-// allocation and MMA issue, warps 2-5 / 6-9 elementwise warpgroups on
-// alternate tiles.  Q and U_Q are copied once from shared memory into TMEM
-// as bf16 A operands (K step kk at +8 kk), so the S | F' score GEMMs read
-// only the key tile from shared memory.
-// TMEM, JVP: [0,64) Q, [64,128) U_Q, [128,256) the O'0 accumulator,
-//            [256,384) and [384,512) score buffers S | F' (32 columns each).
-// TMEM, rows: [0,128) the d~Q accumulator (without tau), [128,192) Q,
-//            [192,256) U_Q, [256,384) and [384,512) score buffers
-//            S | F' | dP | G (32 columns each).
-// A warpgroup reads a buffer one 16-column chunk at a time and overwrites
-// the columns of that chunk with its bf16 A operands of the output GEMMs
-// (JVP: P, P o F; rows: d~S, dS).
+// CTA = 128 query rows, 320 threads: warp 0 TMA (Q, dO, U_Q once; K, U_K,
+// V, U_V tiles of 32 key rows through a 4-slot ring, each tensor as two
+// 64-column halves in the 128-byte swizzle), warp 1 TMEM allocation and MMA
+// issue, warps 2-5 / 6-9 elementwise warpgroups on alternate tiles.  Q and
+// U_Q are copied once from shared memory into TMEM as bf16 A operands (K
+// step kk at +8 kk), so the S | F' score GEMMs read only the key tile from
+// shared memory.
+// TMEM: [0,128) the d~Q accumulator (without tau), [128,192) Q, [192,256)
+// U_Q, [256,384) and [384,512) score buffers S | F' | dP | G (32 columns
+// each).  A warpgroup reads a buffer one 16-column chunk at a time and
+// overwrites the S and F' columns of that chunk with its bf16 A operands of
+// the output GEMMs (d~S, dS).
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -64,7 +55,6 @@ struct SmemW1 {
   alignas(1024) uint8_t dO[2][HALF_BLOCK];
   alignas(1024) uint8_t uq[2][HALF_BLOCK];
   alignas(1024) uint8_t kv[NST][2][4][HALF_TILE];  // [slot][half][K, U_K, V, U_V]
-  float2 part[BM];  // partial row sums passed between the warpgroups
   uint64_t bar_q;
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
@@ -79,17 +69,13 @@ static_assert(sizeof(SmemW1) + 1024 <= 232448, "shared memory");
 static_assert(BM * kStageLd * 4 <= sizeof(SmemW1::kv), "epilogue staging fits in the ring");
 
 constexpr uint32_t kColS = 0, kColF = 32, kColdP = 64, kColG = 96;
-constexpr uint32_t kAccQ = 0;                       // rows: d~Q
-constexpr uint32_t kRowsQA = 128, kRowsUQA = 192;  // rows: Q, U_Q as A operands
-constexpr uint32_t kJvpQA = 0, kJvpUQA = 64;       // JVP: Q, U_Q as A operands
-constexpr uint32_t kAccdO = 128;                    // JVP: O'0
+constexpr uint32_t kAccQ = 0;           // d~Q
+constexpr uint32_t kQA = 128, kUQA = 192;  // Q, U_Q as A operands
 // Operand slots inside a score buffer: chunk c (key columns 16c..16c+15)
 // writes only the S and F' columns of its own chunk, which it has already
 // read.
 __device__ __forceinline__ constexpr uint32_t slot_dSt(int c) { return 16 * c; }
 __device__ __forceinline__ constexpr uint32_t slot_dS(int c) { return 16 * c + 8; }
-__device__ __forceinline__ constexpr uint32_t slot_P(int c) { return kColF + 16 * c; }
-__device__ __forceinline__ constexpr uint32_t slot_W(int c) { return kColF + 16 * c + 8; }
 
 // S, dP, F', G of one 16-column chunk of a score buffer, one row per thread.
 struct Chunk {
@@ -106,32 +92,6 @@ __device__ __forceinline__ void load_chunk(uint32_t sc, int c, Chunk& x) {
 // The element-wise functions below take two columns per step in the paired
 // fp32 instructions; the row sums are kept as two partial sums (even and odd
 // columns).
-
-// The JVP's chunk: P and P o F (into the P and W slots) and the row sum
-// alpha = L' (no dO: dP = G = 0).
-template <bool MASKED, int C>
-__device__ __forceinline__ void jvp_chunk(uint32_t sc, const uint32_t (&s)[16],
-                                          const uint32_t (&f)[16], int col0, int jmax, float c1,
-                                          float Lr2, float tau, float2& a_acc) {
-  uint32_t op[8], opf[8];
-  const float2 c12 = make_float2(c1, c1), nL = make_float2(-Lr2, -Lr2);
-  const float2 tau2 = make_float2(tau, tau);
-#pragma unroll
-  for (int e = 0; e < 16; e += 2) {
-    const float2 t = ffma2(f2(s[e], s[e + 1]), c12, nL);
-    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-    if (MASKED) {
-      if (col0 + 16 * C + e > jmax) p.x = 0.f;
-      if (col0 + 16 * C + e + 1 > jmax) p.y = 0.f;
-    }
-    const float2 pf = fmul2(p, fmul2(f2(f[e], f[e + 1]), tau2));
-    a_acc = fadd2(a_acc, pf);
-    op[e >> 1] = pack_bf16x2(p.x, p.y);
-    opf[e >> 1] = pack_bf16x2(pf.x, pf.y);
-  }
-  tmem_st8(sc + slot_P(C), op);
-  tmem_st8(sc + slot_W(C), opf);
-}
 
 // The rows pass on one 16-column chunk: d~S and dS as bf16 A operands,
 // written to TMEM.
@@ -164,10 +124,7 @@ __device__ __forceinline__ void rows_chunk(uint32_t sc, const Chunk& x, int col0
   tmem_st8(sc + slot_dS(C), ods);
 }
 
-// JVP = true: alpha (into `alpha`), O' = d~dO (into `ddOt`) and, when E is
-// not null, E = dO . d~dO - alpha D (reads dO and D).  JVP = false: the rows
-// pass, reading alpha and E, writing d~Q.
-template <bool JVP>
+// The rows pass: reads alpha and E, writes d~Q.
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pass1_d128_kernel(const __grid_constant__ CUtensorMap mQ,
                          const __grid_constant__ CUtensorMap mdO,
@@ -175,10 +132,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          const __grid_constant__ CUtensorMap mK,
                          const __grid_constant__ CUtensorMap mV,
                          const __grid_constant__ CUtensorMap mUK,
-                         const __grid_constant__ CUtensorMap mUV, const float* __restrict__ O,
+                         const __grid_constant__ CUtensorMap mUV,
                          const float* __restrict__ L, const float* __restrict__ D,
-                         float* __restrict__ dQt, float* __restrict__ ddOt,
-                         float* __restrict__ alpha, float* __restrict__ E, int H, int Hkv,
+                         float* __restrict__ dQt, const float* __restrict__ alpha,
+                         const float* __restrict__ E, int H, int Hkv,
                          int Nq, int Nk, float tau, int causal, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   SmemW1& sm = *reinterpret_cast<SmemW1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -189,8 +146,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int row0 = (causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * BM;
   const int col_end = causal ? min(Nk, row0 + BM) : Nk;  // keys j <= i under the causal mask
   const int T = (col_end + BN - 1) / BN;                  // key tiles
-  const bool withE = JVP && E != nullptr;  // the JVP launch of the BoB: E as well
-  const bool withdO = !JVP || withE;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -221,10 +176,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mUK);
       tma_prefetch_desc(&mUV);
-      mbar_expect_tx(&sm.bar_q, (withdO ? 6 : 4) * HALF_BLOCK);
+      mbar_expect_tx(&sm.bar_q, 6 * HALF_BLOCK);
       for (int h = 0; h < 2; ++h) {
         tma_load_3d(sm.q[h], &mQ, &sm.bar_q, 64 * h, row0, bh);
-        if (withdO) tma_load_3d(sm.dO[h], &mdO, &sm.bar_q, 64 * h, row0, bh);
+        tma_load_3d(sm.dO[h], &mdO, &sm.bar_q, 64 * h, row0, bh);
         tma_load_3d(sm.uq[h], &mUQ, &sm.bar_q, 64 * h, row0, bh);
       }
       int issued = 0;
@@ -250,7 +205,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t idS32 = idesc_bf16(BM, BN, false);      // N = 32, B K-major
     constexpr uint32_t idS64 = idesc_bf16(BM, 2 * BN, false);  // N = 64, B K-major
     constexpr uint32_t idO128 = idesc_bf16(BM, DH, true);      // N = 128, B MN-major
-    constexpr uint32_t kQA = JVP ? kJvpQA : kRowsQA, kUQA = JVP ? kJvpUQA : kRowsUQA;
     uint64_t ddo[2], dK[2], dV[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -275,7 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t acc = kk > 0;
         mma_ts(sc + kColS, tbase + kQA + 8 * kk, dK[h] + so + o, idS64, acc);  // [S | F'] = Q [K; U_K]^T
         mma_ts(sc + kColF, tbase + kUQA + 8 * kk, dK[h] + so + o, idS32, 1);   // F' += U_Q K^T
-        if (!JVP) mma_ss(sc + kColdP, ddo[h] + o, dV[h] + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
+        mma_ss(sc + kColdP, ddo[h] + o, dV[h] + so + o, idS64, acc);  // [dP | G] = dO [V; U_V]^T
       }
       mma_commit(&sm.sc_full[t & 1]);
     };
@@ -287,13 +241,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int c = 0; c < 2; ++c) {
         const uint64_t o = (uint64_t)(16 * 128 * c) >> 4;  // 16 key rows further down
         const uint32_t acc = (t > 0 || c > 0);
-        if (JVP) {
-          mma_ts(tbase + kAccdO, sc + slot_P(c), dUVmn + so + o, idO128, acc);  // O'0 += P U_V
-          mma_ts(tbase + kAccdO, sc + slot_W(c), dVmn + so + o, idO128, 1);     //  + (P o F) V
-        } else {
-          mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
-          mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //  + dS U_K
-        }
+        mma_ts(tbase + kAccQ, sc + slot_dSt(c), dKmn + so + o, idO128, acc);  // d~Q += d~S K
+        mma_ts(tbase + kAccQ, sc + slot_dS(c), dUKmn + so + o, idO128, 1);    //  + dS U_K
       }
       mma_commit(&sm.kv_empty[s]);
     };
@@ -334,11 +283,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t rowvec = static_cast<size_t>(bh) * Nq + gr;
     const float c1 = tau * kLog2e;
     const float Lr2 = gr < Nq ? L[rowvec] * kLog2e : 0.f;
-    const float Dr = (withdO && gr < Nq) ? D[rowvec] : 0.f;
-    // The rows pass takes alpha and E from the JVP launch.
-    const float al_in = (!JVP && gr < Nq) ? alpha[rowvec] : 0.f;
-    const float E_in = (!JVP && gr < Nq) ? E[rowvec] : 0.f;
-    float2 a_acc = make_float2(0.f, 0.f);
+    const float Dr = gr < Nq ? D[rowvec] : 0.f;
+    // alpha and E come from the JVP launch.
+    const float al_in = gr < Nq ? alpha[rowvec] : 0.f;
+    const float E_in = gr < Nq ? E[rowvec] : 0.f;
     bool ok = true;
     const int jmax = causal ? min(Nk - 1, gr) : Nk - 1;
 
@@ -348,7 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // 2 (kk mod 4) + 1 of half kk / 4.
     ok = mbar_wait_warp(&sm.bar_q, 0, abort_flag, err);
     if (ok) {
-      const uint32_t col = wg == 0 ? (JVP ? kJvpQA : kRowsQA) : (JVP ? kJvpUQA : kRowsUQA);
+      const uint32_t col = wg == 0 ? kQA : kUQA;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint8_t* row = (wg == 0 ? sm.q[kk >> 2] : sm.uq[kk >> 2]) + r * 128;
@@ -374,64 +322,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       const int col0 = t * BN;
       const bool masked = (col0 + BN > Nk) || (causal && col0 + BN - 1 > row0);
-      if (JVP) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[16], fv[16];
-          tmem_ld16(sc + kColS + 16 * c, sv);
-          tmem_ld16(sc + kColF + 16 * c, fv);
-          tmem_wait_ld();
-          if (c == 0) {
-            if (masked) jvp_chunk<true, 0>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
-            else jvp_chunk<false, 0>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
-          } else {
-            if (masked) jvp_chunk<true, 1>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
-            else jvp_chunk<false, 1>(sc, sv, fv, col0, jmax, c1, Lr2, tau, a_acc);
-          }
-        }
-      } else {
-        {
-          Chunk x;
-          load_chunk(sc, 0, x);
-          tmem_wait_ld();
-          if (masked)
-            rows_chunk<true, 0>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
-          else
-            rows_chunk<false, 0>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
-        }
-        {
-          Chunk x;
-          load_chunk(sc, 1, x);
-          tmem_wait_ld();
-          if (masked)
-            rows_chunk<true, 1>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
-          else
-            rows_chunk<false, 1>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
-        }
+      {
+        Chunk x;
+        load_chunk(sc, 0, x);
+        tmem_wait_ld();
+        if (masked)
+          rows_chunk<true, 0>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
+        else
+          rows_chunk<false, 0>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
+      }
+      {
+        Chunk x;
+        load_chunk(sc, 1, x);
+        tmem_wait_ld();
+        if (masked)
+          rows_chunk<true, 1>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
+        else
+          rows_chunk<false, 1>(sc, x, col0, jmax, c1, Lr2, Dr, tau, al_in, E_in);
       }
       tmem_wait_st();
       tc_fence_before();
       warp_arrive(&sm.op_ready[wg]);
     }
 
-    // The JVP's row sum alpha = L' over both warpgroups' tiles (named
-    // barrier 1, each warpgroup passes twice).
-    float al = al_in;
-    if (JVP) {
-      const float a_own = a_acc.x + a_acc.y;
-      if (wg == 1) sm.part[r].x = a_own;
-      named_bar_sync(1, 256);
-      al = a_own + (wg == 0 ? sm.part[r].x : 0.f);
-      if (wg == 0) sm.part[r].x = al;
-      named_bar_sync(1, 256);
-      if (wg == 1) al = sm.part[r].x;
-    }
-
     // Epilogue: warpgroup wg forms output columns [64 wg, 64 wg + 64) of its
-    // row.  Every MMA is done, so the ring is idle: the block's rows of O
-    // (the JVP) come in through shared memory with coalesced loads, each
-    // thread forms its row's outputs there (O' over O), and the tile leaves
-    // with coalesced stores (256 threads, 32 float4 per row).
+    // row, d~Q = tau (d~S K + dS U_K).  Every MMA is done, so the ring is
+    // idle: each thread stages its row there and the tile leaves with
+    // coalesced stores (256 threads, 32 float4 per row).
     ok = mbar_wait_warp(&sm.out_full, 0, abort_flag, err) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     tc_fence_after();
@@ -440,71 +357,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tid = threadIdx.x - 64;  // 0 .. 255
     const int rows = min(BM, Nq - row0);
     const size_t blk = (static_cast<size_t>(bh) * Nq + row0) * DH;
-    if (JVP) {
-      for (int f = tid; f < rows * (DH / 4); f += 256) {
-        const int rr = f / (DH / 4), c4 = f % (DH / 4);
-        *reinterpret_cast<float4*>(st + rr * kStageLd + 4 * c4) =
-            reinterpret_cast<const float4*>(O + blk)[f];
-      }
-      named_bar_sync(1, 256);
-    }
-    float edot = 0.f;  // dO . d~dO over this warpgroup's columns
 #pragma unroll 1
     for (int h = 0; h < 4; ++h) {
       const int col = 64 * wg + 16 * h;
       uint32_t v[16];
-      tmem_ld16(acc_base + (JVP ? kAccdO : kAccQ) + col, v);
+      tmem_ld16(acc_base + kAccQ + col, v);
       tmem_wait_ld();
       if (gr >= Nq) continue;
       float4* s4 = reinterpret_cast<float4*>(st + r * kStageLd + col);
-      if (JVP) {  // O' = O'0 - L' O
-        float dov[16];
-        if (withE) {
-          // dO columns col .. col + 15: 16-byte chunks 2h, 2h + 1 of half wg
-          const uint8_t* drow = sm.dO[wg] + r * 128;
-          const uint4 x = *reinterpret_cast<const uint4*>(drow + (((2 * h) ^ (r & 7)) << 4));
-          const uint4 y = *reinterpret_cast<const uint4*>(drow + (((2 * h + 1) ^ (r & 7)) << 4));
-          const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            dov[2 * k] = __uint_as_float(w[k] << 16);
-            dov[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 ov = s4[k];
-          const float4 dv = make_float4(u2f(v[4 * k]) - al * ov.x, u2f(v[4 * k + 1]) - al * ov.y,
-                                        u2f(v[4 * k + 2]) - al * ov.z,
-                                        u2f(v[4 * k + 3]) - al * ov.w);
-          s4[k] = dv;
-          if (withE)
-            edot += dov[4 * k] * dv.x + dov[4 * k + 1] * dv.y + dov[4 * k + 2] * dv.z +
-                    dov[4 * k + 3] * dv.w;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          s4[k] = make_float4(tau * u2f(v[4 * k]), tau * u2f(v[4 * k + 1]),
-                              tau * u2f(v[4 * k + 2]), tau * u2f(v[4 * k + 3]));
-      }
+      for (int k = 0; k < 4; ++k)
+        s4[k] = make_float4(tau * u2f(v[4 * k]), tau * u2f(v[4 * k + 1]),
+                            tau * u2f(v[4 * k + 2]), tau * u2f(v[4 * k + 3]));
     }
     named_bar_sync(1, 256);
     if (ok) {
-      float* outp = JVP ? ddOt : dQt;
       for (int f = tid; f < rows * (DH / 4); f += 256) {
         const int rr = f / (DH / 4), c4 = f % (DH / 4);
-        reinterpret_cast<float4*>(outp + blk)[f] =
+        reinterpret_cast<float4*>(dQt + blk)[f] =
             *reinterpret_cast<const float4*>(st + rr * kStageLd + 4 * c4);
       }
     }
-    if (withE) {
-      // E = dO . d~dO - alpha D: warpgroup 1 hands its half of the dot over.
-      if (wg == 1) sm.part[r].y = edot;
-      named_bar_sync(1, 256);
-      if (ok && wg == 0 && gr < Nq) E[rowvec] = (edot + sm.part[r].y) - al * Dr;
-    }
-    if (JVP && ok && wg == 0 && gr < Nq) alpha[rowvec] = al;
   }
 
   tc_fence_before();
@@ -527,12 +400,12 @@ cudaError_t tc_launch_pass1_d128(const BobArgs& a, const CUtensorMap* maps128,
   // maps32: K, V, U_K, U_V with 32-row boxes; every box is 64 columns wide
   // (one half of a 128-column row).
   const size_t smem = tc_pass1_d128_smem();
-  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel<false>), (int)smem);
+  cudaError_t e = tc_set_smem(reinterpret_cast<const void*>(tc_pass1_d128_kernel), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Nq + BM - 1) / BM, a.H, a.B);
-  tc_pass1_d128_kernel<false><<<grid, NTHREADS, smem, a.stream>>>(
-      maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.O, a.L,
-      a.D, a.dQt, nullptr, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
+  tc_pass1_d128_kernel<<<grid, NTHREADS, smem, a.stream>>>(
+      maps128[0], maps128[1], maps128[2], maps32[0], maps32[1], maps32[2], maps32[3], a.L, a.D,
+      a.dQt, a.alpha, a.E, a.H, a.Hkv, a.Nq, a.Nk, a.tau, a.causal ? 1 : 0, a.err);
   return cudaGetLastError();
 }
 
