@@ -45,7 +45,7 @@ using namespace tc;
 constexpr int BM = kTcRows;  // 128 key rows per CTA
 constexpr int BQ = 32;       // query rows per streamed tile
 constexpr int DH = 128;
-constexpr int NST = 3;
+constexpr int NST = 4;  // ring stages; stage 3 lies in the U_K block (free once U_K is in TMEM)
 constexpr int NTHREADS = 320;
 constexpr uint32_t HALF_BLOCK = BM * 64 * 2;  // 16 KiB
 constexpr uint32_t HALF_TILE = BQ * 64 * 2;   // 4 KiB
@@ -55,11 +55,11 @@ constexpr uint32_t EX_BYTES = 2 * BQ * 16 * 2;  // 64 rows x 16 bf16: one extra 
 
 struct SmemW2 {
   alignas(1024) uint8_t kb[4][2][HALF_BLOCK];         // K, U_K, V, U_V (resident) x halves
-  alignas(1024) uint8_t st[NST][2][3][HALF_TILE];     // [stage][half][Q, U_Q, dO]
+  alignas(1024) uint8_t st[NST - 1][2][3][HALF_TILE];  // [stage][half][Q, U_Q, dO]
   // Row-scalar K step of each stage: [0] for S^T | F'^T (rows 0-31: -L/tau,
   // rows 32-63: -alpha/tau), [1] for dP^T | G^T (-D, -(alpha D + E)); no
   // swizzle, K-major, row r at (r / 8) * 256 + (r % 8) * 16, k 8-15 at +128.
-  alignas(1024) uint8_t ex[NST][2][EX_BYTES];
+  alignas(1024) uint8_t ex[NST - 1][2][EX_BYTES];
   uint64_t bar_kv;
   uint64_t a_ready;  // U_K is in TMEM (4 warps)
   uint64_t st_full[NST];
@@ -74,6 +74,9 @@ struct SmemW2 {
   int abort_flag;
 };
 static_assert(sizeof(SmemW2) + 1024 <= 232448, "shared memory");
+// Stage 3: the tiles at offset 0 and the row-scalar K steps at STAGE_BYTES
+// of the U_K block.
+static_assert(STAGE_BYTES + 2 * EX_BYTES <= 2 * HALF_BLOCK, "stage 3 fits in the U_K block");
 
 constexpr uint32_t kAccK = 0, kAccV = 128;
 constexpr uint32_t kSc = 256;
@@ -90,6 +93,16 @@ static_assert(BM * 2 * DH * 4 <= 4 * 2 * HALF_BLOCK, "staging fits in the reside
 
 __device__ __forceinline__ constexpr uint32_t op_col(uint32_t x, int kk) {
   return kOp + 16 * x + 8 * kk;
+}
+
+// Ring stage s: tile i (Q, U_Q, dO) of half h, and its row-scalar K step q.
+__device__ __forceinline__ uint8_t* stage_tile(SmemW2& sm, int s, int h, int i) {
+  return s < NST - 1 ? sm.st[s][h][i]
+                      : reinterpret_cast<uint8_t*>(&sm.kb[1]) + (3 * h + i) * HALF_TILE;
+}
+__device__ __forceinline__ uint8_t* stage_ex(SmemW2& sm, int s, int q) {
+  return s < NST - 1 ? sm.ex[s][q]
+                      : reinterpret_cast<uint8_t*>(&sm.kb[1]) + STAGE_BYTES + q * EX_BYTES;
 }
 
 // The 16 query rows of one warpgroup: read S^T, F'^T (release), dP^T, G^T
@@ -248,13 +261,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int s = t % NST;
       if (t >= NST && !mbar_wait_warp(&sm.st_empty[s], ((t / NST) - 1) & 1, abort_flag, err))
         break;
+      // Stage 3 is the U_K block: wait until warpgroup 0 has copied U_K out.
+      if (t == NST - 1 && !mbar_wait_warp(&sm.a_ready, 0, abort_flag, err)) break;
       if (lane == 0) {
         const int row = ((f0 + t) % Tq + t0) * BQ, fz = hqb + (f0 + t) / Tq;
         mbar_expect_tx(&sm.st_full[s], STAGE_BYTES);
         for (int h = 0; h < 2; ++h) {
-          tma_load_3d(sm.st[s][h][0], &mQ, &sm.st_full[s], 64 * h, row, fz);
-          tma_load_3d(sm.st[s][h][1], &mUQ, &sm.st_full[s], 64 * h, row, fz);
-          tma_load_3d(sm.st[s][h][2], &mdO, &sm.st_full[s], 64 * h, row, fz);
+          tma_load_3d(stage_tile(sm, s, h, 0), &mQ, &sm.st_full[s], 64 * h, row, fz);
+          tma_load_3d(stage_tile(sm, s, h, 1), &mUQ, &sm.st_full[s], 64 * h, row, fz);
+          tma_load_3d(stage_tile(sm, s, h, 2), &mdO, &sm.st_full[s], 64 * h, row, fz);
         }
       }
       {
@@ -264,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int row = lane + BQ * (q & 1);  // -L/tau, -alpha/tau ; -D, -(alpha D + E)
-          uint8_t* base = sm.ex[s][q >> 1] + (row >> 3) * 256 + (row & 7) * 16;
+          uint8_t* base = stage_ex(sm, s, q >> 1) + (row >> 3) * 256 + (row & 7) * 16;
           const uint2 hm_l0 = split3_bf16(vals[q]);
           *reinterpret_cast<uint4*>(base) = make_uint4(hm_l0.x, hm_l0.y, 0u, 0u);
           *reinterpret_cast<uint4*>(base + 128) = make_uint4(0u, 0u, 0u, 0u);
@@ -303,11 +318,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dUQmn = smem_desc_sw128(smem_u32(sm.st[0][0][1]), kHalfStride, 1024);
     const uint64_t ddOmn = smem_desc_sw128(smem_u32(sm.st[0][0][2]), kHalfStride, 1024);
     const uint64_t dEx0 = smem_desc_noswz(smem_u32(sm.ex[0][0]), 128, 256);
-    constexpr uint64_t kExStage = (2 * EX_BYTES) >> 4, kExPG = EX_BYTES >> 4;
+    constexpr uint64_t kExPG = EX_BYTES >> 4;
+    // Start-address offsets (16-byte units) of stage s from stage 0: the
+    // stages in the ring are STAGE_BYTES apart, stage 3 lies in the U_K block
+    // (before the ring, so its offset is negative; the sums stay in range).
+    const int64_t so3 = (static_cast<int64_t>(smem_u32(stage_tile(sm, NST - 1, 0, 0))) -
+                         static_cast<int64_t>(smem_u32(sm.st[0][0][0]))) >> 4;
+    const int64_t eo3 = (static_cast<int64_t>(smem_u32(stage_ex(sm, NST - 1, 0))) -
+                         static_cast<int64_t>(smem_u32(sm.ex[0][0]))) >> 4;
+    auto stage_off = [&](int s) -> uint64_t {
+      return static_cast<uint64_t>(s < NST - 1 ? static_cast<int64_t>(s * STAGE_BYTES >> 4) : so3);
+    };
+    auto ex_off = [&](int s) -> uint64_t {
+      return static_cast<uint64_t>(s < NST - 1 ? static_cast<int64_t>(s * 2 * EX_BYTES >> 4) : eo3);
+    };
     const uint32_t sc = tbase + kSc;
     // Score GEMMs in two halves: S^T | F'^T, then dP^T | G^T (+ commit).
     auto issue_sf = [&](int t) {
-      const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
+      const uint64_t so = stage_off(t % NST);
       {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
@@ -317,11 +345,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ts(sc + kColF, tbase + kUKA + 8 * kk, dQ[h] + so + o, idS32, 1);  // F'^T += U_K Q^T
         }
         // [S^T | F'^T] += 1 [-L / tau | -alpha / tau]^T (the row-scalar K step)
-        mma_ts(sc + kColS, tbase + kOnes, dEx0 + (t % NST) * kExStage, idS64, 1);
+        mma_ts(sc + kColS, tbase + kOnes, dEx0 + ex_off(t % NST), idS64, 1);
       }
     };
     auto issue_pg = [&](int t) {
-      const uint64_t so = (uint64_t)((t % NST) * STAGE_BYTES) >> 4;
+      const uint64_t so = stage_off(t % NST);
       {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
@@ -331,13 +359,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_ss(sc + kColG, dUV[h] + o, ddO[h] + so + o, idS32, kk > 0);  // G^T  = U_V dO^T
         }
         // [dP^T | G^T] += 1 [-D | -(alpha D + E)]^T
-        mma_ts(sc + kColdP, tbase + kOnes, dEx0 + (t % NST) * kExStage + kExPG, idS64, 1);
+        mma_ts(sc + kColdP, tbase + kOnes, dEx0 + ex_off(t % NST) + kExPG, idS64, 1);
         mma_commit(&sm.sc_full);
       }
     };
     auto issue_outputs = [&](int t) {
       const int s = t % NST;
-      const uint64_t so = (uint64_t)(s * STAGE_BYTES) >> 4;
+      const uint64_t so = stage_off(s);
       {
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
