@@ -188,8 +188,10 @@ flashbob_status flashbob_bob_launches(int B, int H, int Hkv, int Nq, int Nk, int
 /*
  * flashbob_bob_tile_sizes: the tiles flashbob_bob uses for (d, in_dtype):
  * pass-1 row block Br1 and column tile Bc1, pass-2 column block Bc2 and row
- * tile Br2, and each pass's dynamic shared memory per CTA in bytes.  Any
- * output pointer may be NULL.  FLASHBOB_ERR_UNSUPPORTED for d outside 1..128.
+ * tile Br2, and each pass's dynamic shared memory per CTA in bytes (at
+ * d = 128 on the tensor cores, of pass 1's second launch, the rows pass; its
+ * first launch, the JVP, streams 64-row key tiles).  Any output pointer may
+ * be NULL.  FLASHBOB_ERR_UNSUPPORTED for d outside 1..128.
  */
 flashbob_status flashbob_bob_tile_sizes(int d, flashbob_dtype in_dtype, int* Br1, int* Bc1,
                                         int* Br2, int* Bc2, size_t* smem_bytes_pass1,
