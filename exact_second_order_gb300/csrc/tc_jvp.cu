@@ -31,11 +31,12 @@
 //   [128 + 128 b, 256 + 128 b)   score buffer b = 0, 1, 2: F' = Q U_K^T +
 //               U_Q K^T (64 columns) | S = Q K^T (64 columns).
 // A warpgroup reads the buffer into registers and writes the bf16 A
-// operands of the output GEMMs over F': K step c (keys 16c .. 16c + 15 of the
-// tile) has P at column 16c and P o F at 16c + 8, over those keys' F'.  The score GEMMs of tile
-// t + 3 follow tile t's output GEMMs on the in-order tensor pipe, so they
-// overwrite the buffer only after its operands were read, and each
-// warpgroup has three tiles' worth of MMA time for each of its tiles.
+// operands of the output GEMMs over F': K step c (keys 16c .. 16c + 15 of
+// the tile) has P at column 16c and P o F at 16c + 8, over those keys' F'.
+// The score GEMMs of tile t + 3 follow tile t's output GEMMs on the in-order
+// tensor pipe, so they overwrite the buffer only after its operands were
+// read, and each warpgroup has three tiles' worth of MMA time for each of
+// its tiles.
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -47,6 +48,7 @@ constexpr int BM = kTcRows;   // 128 query rows per CTA
 constexpr int BN = kTcJvpStream;  // 64 key rows per streamed tile
 constexpr int DH = 64;        // head dim
 constexpr int NST = 5;        // stages of the U_K/K/V/U_V ring
+constexpr int NB = 3;   // score buffers
 constexpr int NWG = 3;  // elementwise warpgroups, one per score buffer
 constexpr int NTHREADS = 64 + 128 * NWG;
 constexpr uint32_t BLOCK_BYTES = BM * DH * 2;  // 16 KiB
@@ -66,8 +68,8 @@ struct SmemJ {
   uint64_t a_ready;  // Q and U_Q are in TMEM (8 warps)
   uint64_t kv_full[NST];
   uint64_t kv_empty[NST];
-  uint64_t sc_full[3];   // per buffer: the scores are in
-  uint64_t op_ready[3];  // per buffer: the operands are in TMEM (4 warps)
+  uint64_t sc_full[NB];   // per buffer: the scores are in
+  uint64_t op_ready[NB];  // per buffer: the operands are in TMEM (4 warps)
   uint64_t out_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -76,7 +78,6 @@ static_assert(sizeof(SmemJ) + 1024 <= 232448, "shared memory");
 
 constexpr uint32_t kAccO = 0;
 constexpr uint32_t kQA = 64, kUQA = 96;  // K step kk at + 8 kk
-constexpr int NB = 3;  // score buffers
 __device__ __forceinline__ constexpr uint32_t sc_base(int b) { return 128 + 128 * b; }
 constexpr uint32_t kColF = 0, kColS = 64;  // inside a score buffer
 // Operand slots inside a score buffer: K step c over the F' columns of the
