@@ -27,7 +27,7 @@
 // S^T and half of F'^T), U_K Q^T, V dO^T and U_V dO^T (N = 64 each).
 // Row scalars ride in the score GEMMs.  Each query row's L, D, alpha and
 // alpha D + E enter the score buffer through one more K step: an all-ones
-// A operand (TMEM) against a 16-column B tile the producer writes per query
+// A operand (shared memory) against a 16-column B tile the producer writes per query
 // tile, which holds -L / tau, -alpha / tau, -D and -(alpha D + E) as sums of
 // three bf16 parts (exact to 2^-24 relative).  The score buffer then holds
 // S^T - L / tau, F'^T - alpha / tau, dP^T - D and G^T - (alpha D + E), and
