@@ -27,11 +27,12 @@
 // S^T and half of F'^T), U_K Q^T, V dO^T and U_V dO^T (N = 64 each).
 // Row scalars ride in the score GEMMs.  Each query row's L, D, alpha and
 // alpha D + E enter the score buffer through one more K step: an all-ones
-// A operand (shared memory) against a 16-column B tile the producer writes per query
-// tile, which holds -L / tau, -alpha / tau, -D and -(alpha D + E) as sums of
-// three bf16 parts (exact to 2^-24 relative).  The score buffer then holds
-// S^T - L / tau, F'^T - alpha / tau, dP^T - D and G^T - (alpha D + E), and
-// the element-wise code needs no per-column scalars at all.
+// A operand (shared memory) against a 16-column B tile the producer writes
+// per query tile, which holds -L / tau, -alpha / tau, -D and -(alpha D + E)
+// as sums of three bf16 parts (exact to 2^-24 relative).  The score buffer
+// then holds S^T - L / tau, F'^T - alpha / tau, dP^T - D and
+// G^T - (alpha D + E), and the element-wise code needs no per-column
+// scalars at all.
 // TMEM: [0,64) d~K, [64,128) d~V accumulators; [128,384) one score buffer
 // S^T | F'^T | dP^T | G^T (64 columns each); [384,480) the bf16 A operands
 // dS^T, d~S^T, W^T of the output GEMMs; [480,512) U_K as the bf16 A operand
