@@ -47,7 +47,10 @@ def _full_errors(w, x, O, L, Od, Ld):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,Nk,H,Hkv", [(1, 1, 2, 2), (129, 129, 2, 2), (300, 77, 4, 2),
-                                        (65, 300, 3, 1), (1000, 1000, 1, 1)])
+                                        (65, 300, 3, 1), (1000, 1000, 1, 1),
+                                        # one whole 64-key tile; seven whole tiles, so
+                                        # every ring of the key stream wraps
+                                        (64, 64, 2, 2), (200, 448, 2, 1)])
 @pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 64), ("bf16", 96), ("bf16", 128)])
 def test_jvp_small_shapes_full_oracle(N, Nk, H, Hkv, dtype, d, causal):
     w = wl.small_workload(1, H, N, d, dtype, seed=N + Nk + H, Hkv=Hkv, Nk=Nk, causal=causal)
