@@ -174,15 +174,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     {  // MMA issuer: one elected lane runs the whole schedule
       constexpr uint32_t idS = idesc_bf16(BM, BN, false);
       constexpr uint32_t idO = idesc_bf16(BM, DH, true);
+      // Base descriptors of Q, stage 0's K and stage 0's V: a stage, a half
+      // or a K step only adds its byte offset / 16 to the address field (no
+      // shared-memory address reaches 2^18, so the field cannot carry).
+      const uint64_t dQ = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(smem_u32(sm.kv[0][0][0]), 16, 1024);
+      const uint64_t dV0 = smem_desc_sw128(smem_u32(sm.kv[0][1][0]), HT, 1024);
+      constexpr uint64_t kStage = sizeof(sm.kv[0]) >> 4;
       auto issue_scores = [&](int t) {
-        const int s = t % NST;
+        const uint64_t so = (t % NST) * kStage;
         const uint32_t sc = tbase + kScore + BN * (t % NBUF);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
-          const int h = kk >> 2;  // 64-column half of the head dim
+          const uint32_t h = kk >> 2;  // 64-column half of the head dim
           const uint32_t o = 32 * (kk & 3);
-          const uint32_t aq = smem_u32(sm.q[h]), bk = smem_u32(sm.kv[s][0][h]);
-          mma_ss(sc, smem_desc_sw128(aq + o, 16, 1024), smem_desc_sw128(bk + o, 16, 1024), idS,
+          mma_ss(sc, dQ + ((h * HALF_BLOCK + o) >> 4), dK0 + so + ((h * HT + o) >> 4), idS,
                  kk > 0);
         }
         mma_commit(&sm.sc_full[t % NBUF]);
@@ -193,12 +199,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // V as an N = DH MN-major operand: its second 64-column half (d = 128)
         // sits HT bytes after the first.  Warpgroup t mod 2's accumulator;
         // its first tile (t < 2) starts it.
-        const uint32_t bv = smem_u32(sm.kv[s][1][0]);
+        const uint64_t dv = dV0 + s * kStage;
         const uint32_t acc_col = tbase + DH * (t & 1);
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c)
-          mma_ts(acc_col, sc + 8 * c, smem_desc_sw128(bv + 16 * 128 * c, HT, 1024), idO,
-                 (t >= 2 || c > 0));
+          mma_ts(acc_col, sc + 8 * c, dv + ((16 * 128 * c) >> 4), idO, (t >= 2 || c > 0));
         mma_commit(&sm.pv_done[t & 1]);
         mma_commit(&sm.kv_empty[s]);
       };
