@@ -40,7 +40,7 @@ template <int DH>
 struct PrepCfg {
   static constexpr int kHalves = DH / 64;
   static constexpr int kBN = DH == 64 ? 128 : 64;          // keys per streamed tile
-  static constexpr int kStages = DH == 64 ? 4 : 5;
+  static constexpr int kStages = DH == 64 ? 6 : 5;       // 208 / 192 KiB with Q
   static constexpr uint32_t kHalfTile = kBN * 64 * 2;       // kBN rows x 64 columns bf16
   static_assert(2 * DH + NBUF * kBN <= 512, "TMEM columns");
 };
