@@ -47,7 +47,7 @@ using namespace tc;
 constexpr int BM = kTcRows;   // 128 query rows per CTA
 constexpr int BN = kTcJvpStream;  // 64 key rows per streamed tile
 constexpr int DH = 64;        // head dim
-constexpr int NST = 5;        // stages of the U_K/K/V/U_V ring
+constexpr int NST = 6;        // stages of the U_K/K/V/U_V ring
 constexpr int NB = 3;   // score buffers
 constexpr int NWG = 3;  // elementwise warpgroups, one per score buffer
 constexpr int NTHREADS = 64 + 128 * NWG;
