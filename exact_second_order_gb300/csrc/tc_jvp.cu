@@ -12,7 +12,7 @@
 //
 // CTA = 128 query rows (MMA M = 128, one TMEM lane per row), 448 threads:
 //   warp 0      TMA producer: the Q and U_Q blocks once, then U_K, K, V, U_V
-//               tiles of 64 key rows through a 5-stage mbarrier ring;
+//               tiles of 64 key rows through a 6-stage mbarrier ring;
 //   warp 1      TMEM allocator; one elected lane runs the MMA schedule;
 //   warps 2-5 / 6-9 / 10-13   elementwise warpgroups 0 / 1 / 2: warpgroup
 //               w takes the tiles t = w mod 3, in score buffer w.
